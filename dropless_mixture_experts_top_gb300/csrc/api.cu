@@ -1,0 +1,412 @@
+// api.cu -- the C ABI (include/moe.h): argument validation, workspace
+// carving, and the launch sequence of each call.  Everything after validation
+// is enqueued on the caller's stream; nothing is allocated or synchronised
+// here except in moe_get_device_status.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "internal.h"
+
+namespace moe {
+
+void *tensor_map_encoder() {
+  static void *fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void *p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = p;
+  });
+  return fn;
+}
+
+namespace {
+
+constexpr size_t kHeader = 256;  // status word (offset 0) + route ticket (offset 4)
+
+inline size_t align256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
+
+struct Layout {
+  // route scratch
+  size_t r_lrank, r_hist, r_base, r_total;
+  // saved
+  size_t s_xperm, s_G, s_U, s_A, s_Y, s_total;
+  // forward scratch
+  size_t f_total;
+  // backward scratch
+  size_t b_dyw, b_dG, b_dU, b_dX, b_total;
+};
+
+bool shape_ok(const moe_config *c) {
+  if (!c) return false;
+  if (c->T < 0 || c->H < 64 || c->I < 64 || c->H % 64 || c->I % 64) return false;
+  if (c->E < 1 || c->E > kMaxExperts || c->k < 1 || c->k > kMaxTopK || c->k > c->E) return false;
+  if (static_cast<int64_t>(c->T) * c->k >= (int64_t{1} << 31)) return false;
+  if (c->precision != MOE_PREC_BF16 && c->precision != MOE_PREC_FP8_BWD) return false;
+  return true;
+}
+
+Layout layout_of(const moe_config *c) {
+  Layout L{};
+  const size_t T = c->T, H = c->H, I = c->I, E = c->E, k = c->k, M = T * k;
+  const size_t nblk = static_cast<size_t>(route_num_blocks(c->T));
+  size_t o = kHeader;
+  L.r_lrank = o;
+  o += align256(M * 4);
+  L.r_hist = o;
+  o += align256(nblk * E * 4);
+  L.r_base = o;
+  o += align256(nblk * E * 4);
+  L.r_total = o;
+  o = 0;
+  L.s_xperm = o;
+  o += align256(M * H * 2);
+  L.s_G = o;
+  o += align256(M * I * 2);
+  L.s_U = o;
+  o += align256(M * I * 2);
+  L.s_A = o;
+  o += align256(M * I * 2);
+  L.s_Y = o;
+  o += align256(M * H * 2);
+  L.s_total = o > 0 ? o : 256;
+  L.f_total = kHeader;
+  o = kHeader;
+  L.b_dyw = o;
+  o += align256(M * H * 2);
+  L.b_dG = o;
+  o += align256(M * I * 2);
+  L.b_dU = o;
+  o += align256(M * I * 2);
+  L.b_dX = o;
+  o += align256(M * H * 2);
+  L.b_total = o;
+  return L;
+}
+
+inline bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct DevInfo {
+  int sms = 0;
+  bool ok = false;
+};
+
+moe_status device_info(DevInfo *out) {
+  static DevInfo cache[64];
+  static std::once_flag flags[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  std::call_once(flags[dev], [dev] {
+    int maj = 0, min = 0, sms = 0;
+    cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev].sms = sms;
+    cache[dev].ok = (maj == 10 && min == 3);
+  });
+  if (!cache[dev].ok) return MOE_ERR_UNSUPPORTED;
+  *out = cache[dev];
+  return MOE_OK;
+}
+
+// ---- optional per-kernel timing
+std::atomic<void *const *> g_events{nullptr};
+std::atomic<int> g_cap{0};
+std::atomic<int> g_count{0};
+const char *g_labels[4096];
+
+template <class F>
+moe_status timed(const char *label, cudaStream_t s, F &&launch) {
+  void *const *ev = g_events.load();
+  int slot = -1;
+  if (ev) {
+    slot = g_count.fetch_add(1);
+    if (slot >= g_cap.load() || slot >= 4096) slot = -1;
+  }
+  if (slot >= 0) {
+    g_labels[slot] = label;
+    cudaEventRecord(static_cast<cudaEvent_t>(ev[2 * slot]), s);
+  }
+  cudaError_t e = launch();
+  if (slot >= 0) cudaEventRecord(static_cast<cudaEvent_t>(ev[2 * slot + 1]), s);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+#define MOE_TRY(x)                      \
+  do {                                  \
+    moe_status _st = (x);               \
+    if (_st != MOE_OK) return _st;      \
+  } while (0)
+
+// Token-sized arrays may be null when there are no tokens.
+moe_status check_routing(const moe_routing *r, int T) {
+  if (!r || !r->counts || !r->offsets) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!r->topk_idx || !r->topk_w || !r->row_of_slot || !r->slot_of_row || !r->w_row))
+    return MOE_ERR_INVALID_ARG;
+  if (!al16(r->topk_idx) || !al16(r->topk_w) || !al16(r->counts) || !al16(r->offsets) ||
+      !al16(r->row_of_slot) || !al16(r->slot_of_row) || !al16(r->w_row))
+    return MOE_ERR_ALIGNMENT;
+  return MOE_OK;
+}
+
+GemmArgs gemm_base(const moe_config *c, const moe_routing *r, int sms, int32_t *status) {
+  GemmArgs g{};
+  g.M_rows = c->T * c->k;
+  g.H = c->H;
+  g.I = c->I;
+  g.E = c->E;
+  g.offsets = r->offsets;
+  g.status = status;
+  g.num_sms = sms;
+  return g;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+moe_status moe_query_workspace(const moe_config *cfg, size_t *route_scratch, size_t *saved,
+                               size_t *fwd_scratch, size_t *bwd_scratch) {
+  if (!shape_ok(cfg)) return MOE_ERR_INVALID_ARG;
+  const Layout L = layout_of(cfg);
+  if (route_scratch) *route_scratch = L.r_total;
+  if (saved) *saved = L.s_total;
+  if (fwd_scratch) *fwd_scratch = L.f_total;
+  if (bwd_scratch) *bwd_scratch = L.b_total;
+  return MOE_OK;
+}
+
+moe_status moe_saved_offsets(const moe_config *cfg, moe_saved_layout *out) {
+  if (!shape_ok(cfg) || !out) return MOE_ERR_INVALID_ARG;
+  const Layout L = layout_of(cfg);
+  out->x_perm = L.s_xperm;
+  out->G = L.s_G;
+  out->U = L.s_U;
+  out->A = L.s_A;
+  out->Y = L.s_Y;
+  return MOE_OK;
+}
+
+moe_status moe_route(const moe_config *cfg, const float *logits, const moe_routing *r,
+                     void *scratch, size_t scratch_bytes, void *stream) {
+  if (!shape_ok(cfg)) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_routing(r, cfg->T));
+  if (!scratch || (cfg->T > 0 && !logits)) return MOE_ERR_INVALID_ARG;
+  if (!al16(scratch) || !al16(logits)) return MOE_ERR_ALIGNMENT;
+  const Layout L = layout_of(cfg);
+  if (scratch_bytes < L.r_total) return MOE_ERR_WORKSPACE;
+  DevInfo di;
+  MOE_TRY(device_info(&di));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t *sc = static_cast<uint8_t *>(scratch);
+  if (cudaMemsetAsync(sc, 0, kHeader, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cfg->T == 0) {  // no tokens: empty groups
+    if (cudaMemsetAsync(r->counts, 0, sizeof(int32_t) * cfg->E, s) != cudaSuccess ||
+        cudaMemsetAsync(r->offsets, 0, sizeof(int32_t) * (cfg->E + 1), s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  RouteArgs a{};
+  a.logits = logits;
+  a.T = cfg->T;
+  a.E = cfg->E;
+  a.k = cfg->k;
+  a.topk_idx = r->topk_idx;
+  a.topk_w = r->topk_w;
+  a.counts = r->counts;
+  a.offsets = r->offsets;
+  a.row_of_slot = r->row_of_slot;
+  a.slot_of_row = r->slot_of_row;
+  a.w_row = r->w_row;
+  a.lrank = reinterpret_cast<int32_t *>(sc + L.r_lrank);
+  a.hist = reinterpret_cast<int32_t *>(sc + L.r_hist);
+  a.block_base = reinterpret_cast<int32_t *>(sc + L.r_base);
+  a.ticket = reinterpret_cast<uint32_t *>(sc + 4);
+  a.status = reinterpret_cast<int32_t *>(sc);
+  MOE_TRY(timed("route_topk", s, [&] { return launch_route_topk(a, s); }));
+  MOE_TRY(timed("route_index", s, [&] { return launch_route_index(a, s); }));
+  return MOE_OK;
+}
+
+moe_status moe_forward(const moe_config *cfg, const void *x, const moe_routing *r,
+                       const void *W_gate, const void *W_up, const void *W_down, void *out,
+                       void *saved, size_t saved_bytes, void *scratch, size_t scratch_bytes,
+                       void *stream) {
+  if (!shape_ok(cfg)) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_routing(r, cfg->T));
+  if (!W_gate || !W_up || !W_down || !saved || !scratch || (cfg->T > 0 && (!x || !out)))
+    return MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(W_gate) || !al16(W_up) || !al16(W_down) || !al16(out) || !al16(saved) ||
+      !al16(scratch))
+    return MOE_ERR_ALIGNMENT;
+  const Layout L = layout_of(cfg);
+  if (saved_bytes < L.s_total || scratch_bytes < L.f_total) return MOE_ERR_WORKSPACE;
+  DevInfo di;
+  MOE_TRY(device_info(&di));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t *sc = static_cast<uint8_t *>(scratch);
+  uint8_t *sv = static_cast<uint8_t *>(saved);
+  if (cudaMemsetAsync(sc, 0, kHeader, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cfg->T == 0) return MOE_OK;
+  const int T = cfg->T, H = cfg->H, k = cfg->k;
+  int32_t *status = reinterpret_cast<int32_t *>(sc);
+  uint16_t *x_perm = reinterpret_cast<uint16_t *>(sv + L.s_xperm);
+  uint16_t *G = reinterpret_cast<uint16_t *>(sv + L.s_G);
+  uint16_t *U = reinterpret_cast<uint16_t *>(sv + L.s_U);
+  uint16_t *A = reinterpret_cast<uint16_t *>(sv + L.s_A);
+  uint16_t *Y = reinterpret_cast<uint16_t *>(sv + L.s_Y);
+
+  MOE_TRY(timed("permute_rows", s, [&] {
+    return launch_permute_rows(static_cast<const uint16_t *>(x), r->row_of_slot, x_perm, T, H, k,
+                               s);
+  }));
+  GemmArgs g = gemm_base(cfg, r, di.sms, status);
+  g.x_perm = x_perm;
+  g.W_gate = static_cast<const uint16_t *>(W_gate);
+  g.W_up = static_cast<const uint16_t *>(W_up);
+  g.W_down = static_cast<const uint16_t *>(W_down);
+  g.o0 = A;
+  g.o1 = G;
+  g.o2 = U;
+  MOE_TRY(timed(gemm_mode_name(kFwdGateUp), s, [&] { return launch_grouped_gemm(kFwdGateUp, g, s); }));
+  g.act = A;
+  g.o0 = Y;
+  g.o1 = g.o2 = nullptr;
+  MOE_TRY(timed(gemm_mode_name(kFwdDown), s, [&] { return launch_grouped_gemm(kFwdDown, g, s); }));
+  MOE_TRY(timed("combine", s, [&] {
+    return launch_gather_sum(Y, r->row_of_slot, r->topk_w, static_cast<uint16_t *>(out), T, H, k,
+                             s);
+  }));
+  return MOE_OK;
+}
+
+moe_status moe_backward(const moe_config *cfg, const void *dy, const void *x,
+                        const moe_routing *r, const void *W_gate, const void *W_up,
+                        const void *W_down, const void *saved, size_t saved_bytes, void *dx,
+                        void *dW_gate, void *dW_up, void *dW_down, float *d_logits,
+                        float *d_topk_w, void *scratch, size_t scratch_bytes, void *stream) {
+  if (!shape_ok(cfg)) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_routing(r, cfg->T));
+  if (!W_gate || !W_up || !W_down || !saved || !dW_gate || !dW_up || !dW_down || !scratch ||
+      (cfg->T > 0 && (!dy || !x || !dx || !d_logits)))
+    return MOE_ERR_INVALID_ARG;
+  if (!al16(dy) || !al16(x) || !al16(W_gate) || !al16(W_up) || !al16(W_down) || !al16(saved) ||
+      !al16(dx) || !al16(dW_gate) || !al16(dW_up) || !al16(dW_down) || !al16(d_logits) ||
+      !al16(scratch) || (d_topk_w && !al16(d_topk_w)))
+    return MOE_ERR_ALIGNMENT;
+  const Layout L = layout_of(cfg);
+  if (saved_bytes < L.s_total || scratch_bytes < L.b_total) return MOE_ERR_WORKSPACE;
+  if (cfg->precision != MOE_PREC_BF16) return MOE_ERR_UNSUPPORTED;
+  DevInfo di;
+  MOE_TRY(device_info(&di));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t *sc = static_cast<uint8_t *>(scratch);
+  const uint8_t *sv = static_cast<const uint8_t *>(saved);
+  if (cudaMemsetAsync(sc, 0, kHeader, s) != cudaSuccess) return MOE_ERR_CUDA;
+  const int T = cfg->T, H = cfg->H, I = cfg->I, E = cfg->E, k = cfg->k;
+  if (T == 0) {  // every expert is empty: weight gradients are zero
+    const size_t wbytes = static_cast<size_t>(E) * H * I * 2;
+    if (cudaMemsetAsync(dW_gate, 0, wbytes, s) != cudaSuccess ||
+        cudaMemsetAsync(dW_up, 0, wbytes, s) != cudaSuccess ||
+        cudaMemsetAsync(dW_down, 0, wbytes, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  int32_t *status = reinterpret_cast<int32_t *>(sc);
+  const uint16_t *x_perm = reinterpret_cast<const uint16_t *>(sv + L.s_xperm);
+  const uint16_t *G = reinterpret_cast<const uint16_t *>(sv + L.s_G);
+  const uint16_t *U = reinterpret_cast<const uint16_t *>(sv + L.s_U);
+  const uint16_t *A = reinterpret_cast<const uint16_t *>(sv + L.s_A);
+  const uint16_t *Y = reinterpret_cast<const uint16_t *>(sv + L.s_Y);
+  uint16_t *dyw = reinterpret_cast<uint16_t *>(sc + L.b_dyw);
+  uint16_t *dG = reinterpret_cast<uint16_t *>(sc + L.b_dG);
+  uint16_t *dU = reinterpret_cast<uint16_t *>(sc + L.b_dU);
+  uint16_t *dX = reinterpret_cast<uint16_t *>(sc + L.b_dX);
+
+  MOE_TRY(timed("router_bwd", s, [&] {
+    return launch_router_bwd(static_cast<const uint16_t *>(dy), Y, r->row_of_slot, r->topk_idx,
+                             r->topk_w, dyw, d_logits, d_topk_w, T, H, E, k, s);
+  }));
+  GemmArgs g = gemm_base(cfg, r, di.sms, status);
+  g.x_perm = x_perm;
+  g.W_gate = static_cast<const uint16_t *>(W_gate);
+  g.W_up = static_cast<const uint16_t *>(W_up);
+  g.W_down = static_cast<const uint16_t *>(W_down);
+  g.act = A;
+  g.G = G;
+  g.U = U;
+  g.dyw = dyw;
+  g.dG = dG;
+  g.dU = dU;
+  g.o0 = dG;
+  g.o1 = dU;
+  MOE_TRY(timed(gemm_mode_name(kBwdDA), s, [&] { return launch_grouped_gemm(kBwdDA, g, s); }));
+  g.o0 = dX;
+  g.o1 = nullptr;
+  MOE_TRY(timed(gemm_mode_name(kBwdDX), s, [&] { return launch_grouped_gemm(kBwdDX, g, s); }));
+  MOE_TRY(timed("unpermute_sum", s, [&] {
+    return launch_gather_sum(dX, r->row_of_slot, nullptr, static_cast<uint16_t *>(dx), T, H, k, s);
+  }));
+  g.o0 = static_cast<uint16_t *>(dW_down);
+  MOE_TRY(timed(gemm_mode_name(kBwdDWDown), s, [&] { return launch_grouped_gemm(kBwdDWDown, g, s); }));
+  g.o0 = static_cast<uint16_t *>(dW_gate);
+  g.o1 = static_cast<uint16_t *>(dW_up);
+  MOE_TRY(timed(gemm_mode_name(kBwdDWGateUp), s,
+                [&] { return launch_grouped_gemm(kBwdDWGateUp, g, s); }));
+  (void)I;
+  return MOE_OK;
+}
+
+moe_status moe_get_device_status(const void *scratch, void *stream, int32_t *host_code) {
+  if (!scratch || !host_code) return MOE_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, scratch, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  *host_code = v;
+  return v == 0 ? MOE_OK : MOE_ERR_DEVICE;
+}
+
+const char *moe_status_string(moe_status st) {
+  switch (st) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument (null pointer, shape or precision)";
+    case MOE_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case MOE_ERR_WORKSPACE: return "workspace smaller than moe_query_workspace requires";
+    case MOE_ERR_UNSUPPORTED: return "unsupported device or precision";
+    case MOE_ERR_CUDA: return "CUDA call failed";
+    case MOE_ERR_DEVICE: return "device reported an anomaly (see status flags)";
+  }
+  return "unknown status";
+}
+
+moe_status moe_timing_attach(void *const *events, int32_t capacity) {
+  if (events && capacity <= 0) return MOE_ERR_INVALID_ARG;
+  g_events.store(nullptr);
+  g_count.store(0);
+  g_cap.store(events ? capacity : 0);
+  g_events.store(events);
+  return MOE_OK;
+}
+
+int32_t moe_timing_count(void) {
+  const int n = g_count.load(), c = g_cap.load();
+  return n < c ? n : c;
+}
+
+const char *moe_timing_label(int32_t i) {
+  if (i < 0 || i >= moe_timing_count() || i >= 4096) return nullptr;
+  return g_labels[i];
+}
+
+}  // extern "C"

@@ -1,0 +1,239 @@
+// gather.cu -- the memory-bound row movements of the layer.
+//
+// On one GPU the expert-parallel exchange of the pages (dispatch: tokens are
+// permuted and sent to their experts; combine: results come back and are
+// accumulated in token order -- NVIDIA MoE article, "Optimizacion 2") becomes
+// a device-memory permute and a gather-sum.  All kernels use one warp per
+// token and 16-byte vectors; every token row is read once, every permuted row
+// written once.  Sums run over the token's k choices in a fixed order (j =
+// 0..k-1) in fp32, so results are deterministic (no atomics).
+//
+//   permute_rows : x_perm[row(t,j)] = x[t]                      (dispatch)
+//   gather_sum   : out[t] = sum_j w_tj * Y[row(t,j)]           (combine)
+//                  dx[t]  = sum_j dX_perm[row(t,j)]            (un-permute)
+//   router_bwd   : dyw[row(t,j)] = w_tj * dy[t]                (dy dispatch)
+//                  g_tj = <dy[t], Y[row(t,j)]>                 (d w_tj)
+//                  d_logits[t, S_tj] = w_tj (g_tj - sum_i w_ti g_ti), 0 elsewhere
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kWarps = 8;       // warps (tokens) per block
+constexpr int kVecPerLane = 8;  // 16-byte vectors per lane per chunk: 2048 bf16 per warp
+
+__device__ __forceinline__ void accum8(float (&acc)[8], const uint4 &q, float w) {
+  acc[0] = fmaf(w, bf16_lo(q.x), acc[0]);
+  acc[1] = fmaf(w, bf16_hi(q.x), acc[1]);
+  acc[2] = fmaf(w, bf16_lo(q.y), acc[2]);
+  acc[3] = fmaf(w, bf16_hi(q.y), acc[3]);
+  acc[4] = fmaf(w, bf16_lo(q.z), acc[4]);
+  acc[5] = fmaf(w, bf16_hi(q.z), acc[5]);
+  acc[6] = fmaf(w, bf16_lo(q.w), acc[6]);
+  acc[7] = fmaf(w, bf16_hi(q.w), acc[7]);
+}
+
+__device__ __forceinline__ float dot8(const uint4 &a, const uint4 &b) {
+  float s = bf16_lo(a.x) * bf16_lo(b.x);
+  s = fmaf(bf16_hi(a.x), bf16_hi(b.x), s);
+  s = fmaf(bf16_lo(a.y), bf16_lo(b.y), s);
+  s = fmaf(bf16_hi(a.y), bf16_hi(b.y), s);
+  s = fmaf(bf16_lo(a.z), bf16_lo(b.z), s);
+  s = fmaf(bf16_hi(a.z), bf16_hi(b.z), s);
+  s = fmaf(bf16_lo(a.w), bf16_lo(b.w), s);
+  s = fmaf(bf16_hi(a.w), bf16_hi(b.w), s);
+  return s;
+}
+
+__device__ __forceinline__ uint4 scale8(const uint4 &q, float w) {
+  uint4 r;
+  r.x = pack_bf16x2(w * bf16_lo(q.x), w * bf16_hi(q.x));
+  r.y = pack_bf16x2(w * bf16_lo(q.y), w * bf16_hi(q.y));
+  r.z = pack_bf16x2(w * bf16_lo(q.z), w * bf16_hi(q.z));
+  r.w = pack_bf16x2(w * bf16_lo(q.w), w * bf16_hi(q.w));
+  return r;
+}
+
+__global__ void __launch_bounds__(kWarps * 32) permute_rows_kernel(const uint4 *__restrict__ x,
+                                                                  const int32_t *__restrict__ ros,
+                                                                  uint4 *__restrict__ xp, int T,
+                                                                  int nv, int k) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const int myrow = lane < k ? __ldg(ros + static_cast<size_t>(t) * k + lane) : 0;
+  for (int v0 = 0; v0 < nv; v0 += 32 * kVecPerLane) {
+    uint4 buf[kVecPerLane];
+#pragma unroll
+    for (int u = 0; u < kVecPerLane; ++u) {
+      const int v = v0 + u * 32 + lane;
+      if (v < nv) buf[u] = __ldcs(x + static_cast<size_t>(t) * nv + v);
+    }
+    for (int j = 0; j < k; ++j) {
+      const int row = __shfl_sync(0xffffffffu, myrow, j);
+      uint4 *dst = xp + static_cast<size_t>(row) * nv;
+#pragma unroll
+      for (int u = 0; u < kVecPerLane; ++u) {
+        const int v = v0 + u * 32 + lane;
+        if (v < nv) dst[v] = buf[u];
+      }
+    }
+  }
+}
+
+template <bool kWeighted>
+__global__ void __launch_bounds__(kWarps * 32) gather_sum_kernel(const uint4 *__restrict__ rows,
+                                                                const int32_t *__restrict__ ros,
+                                                                const float *__restrict__ w,
+                                                                uint4 *__restrict__ out, int T,
+                                                                int nv, int k) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const int myrow = lane < k ? __ldg(ros + static_cast<size_t>(t) * k + lane) : 0;
+  const float myw = (kWeighted && lane < k) ? __ldg(w + static_cast<size_t>(t) * k + lane) : 1.f;
+  for (int v0 = 0; v0 < nv; v0 += 32 * kVecPerLane) {
+    float acc[kVecPerLane][8];
+#pragma unroll
+    for (int u = 0; u < kVecPerLane; ++u)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) acc[u][c] = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int row = __shfl_sync(0xffffffffu, myrow, j);
+      const float wj = __shfl_sync(0xffffffffu, myw, j);
+      const uint4 *src = rows + static_cast<size_t>(row) * nv;
+      uint4 q[kVecPerLane];
+#pragma unroll
+      for (int u = 0; u < kVecPerLane; ++u) {
+        const int v = v0 + u * 32 + lane;
+        if (v < nv) q[u] = __ldcs(src + v);
+      }
+#pragma unroll
+      for (int u = 0; u < kVecPerLane; ++u) {
+        const int v = v0 + u * 32 + lane;
+        if (v < nv) accum8(acc[u], q[u], wj);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kVecPerLane; ++u) {
+      const int v = v0 + u * 32 + lane;
+      if (v < nv) {
+        uint4 r;
+        r.x = pack_bf16x2(acc[u][0], acc[u][1]);
+        r.y = pack_bf16x2(acc[u][2], acc[u][3]);
+        r.z = pack_bf16x2(acc[u][4], acc[u][5]);
+        r.w = pack_bf16x2(acc[u][6], acc[u][7]);
+        out[static_cast<size_t>(t) * nv + v] = r;
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kWarps * 32) router_bwd_kernel(
+    const uint4 *__restrict__ dy, const uint4 *__restrict__ Y, const int32_t *__restrict__ ros,
+    const int32_t *__restrict__ topk_idx, const float *__restrict__ topk_w, uint4 *__restrict__ dyw,
+    float *__restrict__ d_logits, float *__restrict__ d_topk_w, int T, int nv, int E, int k) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const size_t sb = static_cast<size_t>(t) * k;
+  const int myrow = lane < k ? __ldg(ros + sb + lane) : 0;
+  const float myw = lane < k ? __ldg(topk_w + sb + lane) : 0.f;
+  const int mye = lane < k ? __ldg(topk_idx + sb + lane) : -1;
+  float dot[kMaxTopK];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) dot[j] = 0.f;
+  for (int v0 = 0; v0 < nv; v0 += 32 * kVecPerLane) {
+    uint4 d[kVecPerLane];
+#pragma unroll
+    for (int u = 0; u < kVecPerLane; ++u) {
+      const int v = v0 + u * 32 + lane;
+      if (v < nv) d[u] = __ldcs(dy + static_cast<size_t>(t) * nv + v);
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j < k) {
+        const int row = __shfl_sync(0xffffffffu, myrow, j);
+        const float wj = __shfl_sync(0xffffffffu, myw, j);
+        const uint4 *src = Y + static_cast<size_t>(row) * nv;
+        uint4 *dst = dyw + static_cast<size_t>(row) * nv;
+        uint4 q[kVecPerLane];
+#pragma unroll
+        for (int u = 0; u < kVecPerLane; ++u) {
+          const int v = v0 + u * 32 + lane;
+          if (v < nv) q[u] = __ldcs(src + v);
+        }
+#pragma unroll
+        for (int u = 0; u < kVecPerLane; ++u) {
+          const int v = v0 + u * 32 + lane;
+          if (v < nv) {
+            dot[j] += dot8(d[u], q[u]);
+            dst[v] = scale8(d[u], wj);
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j)
+    if (j < k) dot[j] = warp_sum(dot[j]);
+  float myg = 0.f;
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j)
+    if (j == lane) myg = dot[j];
+  if (d_topk_w && lane < k) d_topk_w[sb + lane] = myg;
+  // w_j (g_j - sum_i w_i g_i) written as w_j sum_i w_i (g_j - g_i) (the weights
+  // sum to one): no cancellation when one weight is close to 1.
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < kMaxTopK; ++i)
+    if (i < k) acc = fmaf(__shfl_sync(0xffffffffu, myw, i), myg - dot[i], acc);
+  const float mydl = myw * acc;
+  for (int e0 = 0; e0 < E; e0 += 32) {
+    const int e = e0 + lane;
+    float val = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int ej = __shfl_sync(0xffffffffu, mye, j);
+      const float dj = __shfl_sync(0xffffffffu, mydl, j);
+      if (ej == e) val = dj;
+    }
+    if (e < E) d_logits[static_cast<size_t>(t) * E + e] = val;
+  }
+}
+
+inline int blocks_for(int T) { return (T + kWarps - 1) / kWarps; }
+
+}  // namespace
+
+cudaError_t launch_permute_rows(const uint16_t *x, const int32_t *row_of_slot, uint16_t *x_perm,
+                                int T, int H, int k, cudaStream_t s) {
+  permute_rows_kernel<<<blocks_for(T), kWarps * 32, 0, s>>>(
+      reinterpret_cast<const uint4 *>(x), row_of_slot, reinterpret_cast<uint4 *>(x_perm), T, H / 8,
+      k);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_sum(const uint16_t *rows, const int32_t *row_of_slot, const float *w,
+                              uint16_t *out, int T, int H, int k, cudaStream_t s) {
+  if (w)
+    gather_sum_kernel<true><<<blocks_for(T), kWarps * 32, 0, s>>>(
+        reinterpret_cast<const uint4 *>(rows), row_of_slot, w, reinterpret_cast<uint4 *>(out), T,
+        H / 8, k);
+  else
+    gather_sum_kernel<false><<<blocks_for(T), kWarps * 32, 0, s>>>(
+        reinterpret_cast<const uint4 *>(rows), row_of_slot, nullptr,
+        reinterpret_cast<uint4 *>(out), T, H / 8, k);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_bwd(const uint16_t *dy, const uint16_t *Y, const int32_t *row_of_slot,
+                              const int32_t *topk_idx, const float *topk_w, uint16_t *dyw,
+                              float *d_logits, float *d_topk_w, int T, int H, int E, int k,
+                              cudaStream_t s) {
+  router_bwd_kernel<<<blocks_for(T), kWarps * 32, 0, s>>>(
+      reinterpret_cast<const uint4 *>(dy), reinterpret_cast<const uint4 *>(Y), row_of_slot,
+      topk_idx, topk_w, reinterpret_cast<uint4 *>(dyw), d_logits, d_topk_w, T, H / 8, E, k);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

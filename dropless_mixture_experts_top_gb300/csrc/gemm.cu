@@ -1,0 +1,630 @@
+// gemm.cu -- persistent grouped GEMMs over ragged expert segments on the
+// 5th-generation tensor core (tcgen05, sm_103a).
+//
+// A grouped GEMM handles every expert's matrix product in one launch, each at
+// its real token count, computing only the valid regions; counts stay on the
+// device so nothing is copied to the host (NVIDIA MoE article,
+// "Optimizacion 1, el GEMM agrupado").  Two shapes of raggedness occur:
+//   ragged M  (forward GEMMs, dA, dX): rows = the expert's permuted rows;
+//             output tiles of 128 rows start at each expert's first row, rows
+//             past the expert's end are computed but never stored.
+//   ragged K  (weight gradients): the reduction runs over the expert's rows;
+//             the last 64-row K block is cut at the expert's end by zeroing
+//             the rows past it in shared memory before the MMA; an expert with
+//             no rows gets an all-zero gradient.
+//
+// Kernel structure (one CTA per SM, persistent, static round-robin tiles):
+//   warp 0      TMA producer: 128B-swizzled boxes into a 4-stage ring
+//   warp 1      MMA issuer: tcgen05.mma kind::f16 (bf16 in, fp32 accumulate
+//               in TMEM), 128x256 tiles, K = 16 per instruction; owns TMEM
+//   warps 2..5  epilogue: tcgen05.ld from TMEM (two 256-column accumulators,
+//               double buffered), fused SwiGLU / dSwiGLU, bf16 stores
+// Every wait is bounded; on a timeout the kernel flags the status word,
+// drains its own copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;   // tile rows (TMEM lanes)
+constexpr int BN = 256;   // tile columns (TMEM columns per accumulator)
+constexpr int BK = 64;    // K per stage: one 128-byte swizzle row of bf16
+constexpr int STAGES = 4;
+constexpr int kABytes = BM * BK * 2;          // 16 KB
+constexpr int kBBytes = BN * BK * 2;          // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kBox = 64 * 64 * 2;             // one 64x64 bf16 box (MN-major pieces)
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 2 * BN;
+constexpr int kSmemBytes = STAGES * kStageBytes + 1024 /*align*/ + 256 /*barriers*/ +
+                           2 * (kMaxExperts + 1) * 4;
+
+struct Params {
+  int M_rows, H, I, E;
+  const int32_t *offsets;
+  const uint16_t *G, *U;  // dSwiGLU epilogue inputs
+  uint16_t *o0, *o1, *o2;
+  int32_t *status;
+  int kdim;     // ragged M: the fixed reduction length
+  int n_tiles;  // ragged M and K: column tiles per row tile
+  int m_tiles;  // ragged K: row tiles per expert
+};
+
+template <int MODE>
+struct Traits {
+  static constexpr bool kRaggedK = (MODE == kBwdDWDown || MODE == kBwdDWGateUp);
+  static constexpr int kAMN = kRaggedK ? 1 : 0;  // A operand MN-major in smem
+  static constexpr int kBMN = (MODE == kFwdGateUp || MODE == kFwdDown || kRaggedK) ? 1 : 0;
+  // column tile split in two halves from two sources (gate | up)
+  static constexpr bool kPair = (MODE == kFwdGateUp || MODE == kBwdDWGateUp);
+  static constexpr uint32_t kIdesc = idesc_bf16(BM, BN, kAMN, kBMN);
+};
+
+struct Tile {
+  int e;        // expert
+  int m0;       // first output row (ragged M: permuted row; ragged K: dW row)
+  int row_end;  // ragged M: end of the expert's rows
+  int n0;       // first output column
+  int nkb;      // K blocks
+  int krow0;    // ragged K: expert's first row
+  int kcount;   // ragged K: expert's rows
+};
+
+template <int MODE>
+__device__ __forceinline__ Tile decode_tile(int tile, const Params &p, const int *s_tp,
+                                            const int *s_off) {
+  using Tr = Traits<MODE>;
+  Tile t;
+  if constexpr (!Tr::kRaggedK) {
+    const int mt_lin = tile / p.n_tiles, nt = tile % p.n_tiles;
+    int lo = 0, hi = p.E - 1;  // largest e with s_tp[e] <= mt_lin
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_tp[mid] <= mt_lin)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    t.e = lo;
+    t.m0 = s_off[lo] + (mt_lin - s_tp[lo]) * BM;
+    t.row_end = s_off[lo + 1];
+    t.n0 = nt * (Tr::kPair ? BN / 2 : BN);
+    t.nkb = p.kdim / BK;
+    t.krow0 = 0;
+    t.kcount = 0;
+  } else {
+    const int per = p.m_tiles * p.n_tiles;
+    t.e = tile / per;
+    const int rem = tile % per;
+    t.m0 = (rem / p.n_tiles) * BM;
+    t.n0 = (rem % p.n_tiles) * (Tr::kPair ? BN / 2 : BN);
+    t.krow0 = s_off[t.e];
+    t.kcount = s_off[t.e + 1] - s_off[t.e];
+    t.nkb = (t.kcount + BK - 1) / BK;
+    t.row_end = 0;
+  }
+  return t;
+}
+
+// Warp-uniform bounded wait: lane 0 polls, the result is broadcast, then the
+// other lanes observe the completed phase themselves (acquire).
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+  const int lane = threadIdx.x & 31;
+  int ok = 1;
+  if (lane == 0) ok = mbar_wait(bar, parity, abort) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok && lane != 0) {
+    for (int i = 0; i < (1 << 20) && !mbar_try_wait(bar, parity); ++i) {
+    }
+  }
+  return ok != 0;
+}
+
+template <int MODE>
+__device__ __forceinline__ void produce_stage(const Tile &t, int kb, uint8_t *sa, uint8_t *sb,
+                                              uint64_t *bar, const Params &p,
+                                              const CUtensorMap *a0, const CUtensorMap *a1,
+                                              const CUtensorMap *b0, const CUtensorMap *b1) {
+  if constexpr (MODE == kFwdGateUp) {
+    tma_load_2d(sa, a0, bar, kb * BK, t.m0);
+    const int wrow = t.e * p.H + kb * BK;
+    tma_load_2d(sb + 0 * kBox, b0, bar, t.n0, wrow);
+    tma_load_2d(sb + 1 * kBox, b0, bar, t.n0 + 64, wrow);
+    tma_load_2d(sb + 2 * kBox, b1, bar, t.n0, wrow);
+    tma_load_2d(sb + 3 * kBox, b1, bar, t.n0 + 64, wrow);
+  } else if constexpr (MODE == kFwdDown) {
+    tma_load_2d(sa, a0, bar, kb * BK, t.m0);
+    const int wrow = t.e * p.I + kb * BK;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tma_load_2d(sb + c * kBox, b0, bar, t.n0 + 64 * c, wrow);
+  } else if constexpr (MODE == kBwdDA) {
+    tma_load_2d(sa, a0, bar, kb * BK, t.m0);
+    tma_load_2d(sb, b0, bar, kb * BK, t.e * p.I + t.n0);
+  } else if constexpr (MODE == kBwdDX) {
+    const int kbi = p.I / BK;
+    if (kb < kbi) {
+      tma_load_2d(sa, a0, bar, kb * BK, t.m0);
+      tma_load_2d(sb, b0, bar, kb * BK, t.e * p.H + t.n0);
+    } else {
+      tma_load_2d(sa, a1, bar, (kb - kbi) * BK, t.m0);
+      tma_load_2d(sb, b1, bar, (kb - kbi) * BK, t.e * p.H + t.n0);
+    }
+  } else if constexpr (MODE == kBwdDWDown) {
+    const int r = t.krow0 + kb * BK;
+    tma_load_2d(sa + 0 * kBox, a0, bar, t.m0, r);
+    tma_load_2d(sa + 1 * kBox, a0, bar, t.m0 + 64, r);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tma_load_2d(sb + c * kBox, b0, bar, t.n0 + 64 * c, r);
+  } else {  // kBwdDWGateUp
+    const int r = t.krow0 + kb * BK;
+    tma_load_2d(sa + 0 * kBox, a0, bar, t.m0, r);
+    tma_load_2d(sa + 1 * kBox, a0, bar, t.m0 + 64, r);
+    tma_load_2d(sb + 0 * kBox, b0, bar, t.n0, r);
+    tma_load_2d(sb + 1 * kBox, b0, bar, t.n0 + 64, r);
+    tma_load_2d(sb + 2 * kBox, b1, bar, t.n0, r);
+    tma_load_2d(sb + 3 * kBox, b1, bar, t.n0 + 64, r);
+  }
+}
+
+__device__ __forceinline__ void store32_bf16(uint16_t *dst, const float (&v)[32]) {
+  uint4 *d = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 w;
+    w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+    w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+    w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+    w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+    d[q] = w;
+  }
+}
+
+__device__ __forceinline__ void load32_bf16(const uint16_t *src, float (&v)[32]) {
+  const uint4 *s = reinterpret_cast<const uint4 *>(src);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 w = __ldg(s + q);
+    v[8 * q + 0] = bf16_lo(w.x);
+    v[8 * q + 1] = bf16_hi(w.x);
+    v[8 * q + 2] = bf16_lo(w.y);
+    v[8 * q + 3] = bf16_hi(w.y);
+    v[8 * q + 4] = bf16_lo(w.z);
+    v[8 * q + 5] = bf16_hi(w.z);
+    v[8 * q + 6] = bf16_lo(w.w);
+    v[8 * q + 7] = bf16_hi(w.w);
+  }
+}
+
+__device__ __forceinline__ float sigmoidf_(float z) { return 1.f / (1.f + __expf(-z)); }
+
+// Epilogue of one tile for one warp (32 rows).  tb: TMEM address of this
+// warp's lanes at the accumulator's first column.
+template <int MODE>
+__device__ __forceinline__ void epilogue_tile(const Tile &t, uint32_t tb, int rit,
+                                              const Params &p) {
+  uint32_t r0[32], r1[32];
+  float v0[32], v1[32], v2[32];
+  if constexpr (MODE == kFwdGateUp) {
+    const int row = t.m0 + rit;
+    const bool rv = row < t.row_end;
+    for (int c = 0; c < 4; ++c) {
+      const int col = t.n0 + 32 * c;
+      if (col >= p.I) break;
+      tmem_ld32(tb + 32 * c, r0);
+      tmem_ld32(tb + 128 + 32 * c, r1);
+      tmem_ld_wait();
+      if (rv) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float g = __uint_as_float(r0[i]), u = __uint_as_float(r1[i]);
+          v0[i] = g * sigmoidf_(g) * u;  // SwiGLU
+          v1[i] = g;
+          v2[i] = u;
+        }
+        const size_t off = static_cast<size_t>(row) * p.I + col;
+        store32_bf16(p.o0 + off, v0);
+        store32_bf16(p.o1 + off, v1);
+        store32_bf16(p.o2 + off, v2);
+      }
+    }
+  } else if constexpr (MODE == kFwdDown || MODE == kBwdDX) {
+    const int row = t.m0 + rit;
+    const bool rv = row < t.row_end;
+    for (int c = 0; c < 8; ++c) {
+      const int col = t.n0 + 32 * c;
+      if (col >= p.H) break;
+      tmem_ld32(tb + 32 * c, r0);
+      tmem_ld_wait();
+      if (rv) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v0[i] = __uint_as_float(r0[i]);
+        store32_bf16(p.o0 + static_cast<size_t>(row) * p.H + col, v0);
+      }
+    }
+  } else if constexpr (MODE == kBwdDA) {
+    const int row = t.m0 + rit;
+    const bool rv = row < t.row_end;
+    for (int c = 0; c < 8; ++c) {
+      const int col = t.n0 + 32 * c;
+      if (col >= p.I) break;
+      tmem_ld32(tb + 32 * c, r0);
+      tmem_ld_wait();
+      if (rv) {
+        const size_t off = static_cast<size_t>(row) * p.I + col;
+        load32_bf16(p.G + off, v1);
+        load32_bf16(p.U + off, v2);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float da = __uint_as_float(r0[i]), g = v1[i], u = v2[i];
+          const float s = sigmoidf_(g);
+          v0[i] = da * u * s * (1.f + g * (1.f - s));  // dG
+          v1[i] = da * g * s;                          // dU = dA * silu(G)
+        }
+        store32_bf16(p.o0 + off, v0);
+        store32_bf16(p.o1 + off, v1);
+      }
+    }
+  } else if constexpr (MODE == kBwdDWDown) {
+    const int i_row = t.m0 + rit;
+    const bool rv = i_row < p.I;
+    for (int c = 0; c < 8; ++c) {
+      const int col = t.n0 + 32 * c;
+      if (col >= p.H) break;
+      if (t.nkb > 0) {
+        tmem_ld32(tb + 32 * c, r0);
+        tmem_ld_wait();
+      }
+      if (rv) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v0[i] = t.nkb > 0 ? __uint_as_float(r0[i]) : 0.f;
+        store32_bf16(p.o0 + (static_cast<size_t>(t.e) * p.I + i_row) * p.H + col, v0);
+      }
+    }
+  } else {  // kBwdDWGateUp
+    const int h_row = t.m0 + rit;
+    const bool rv = h_row < p.H;
+    for (int c = 0; c < 4; ++c) {
+      const int col = t.n0 + 32 * c;
+      if (col >= p.I) break;
+      if (t.nkb > 0) {
+        tmem_ld32(tb + 32 * c, r0);
+        tmem_ld32(tb + 128 + 32 * c, r1);
+        tmem_ld_wait();
+      }
+      if (rv) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          v0[i] = t.nkb > 0 ? __uint_as_float(r0[i]) : 0.f;
+          v1[i] = t.nkb > 0 ? __uint_as_float(r1[i]) : 0.f;
+        }
+        const size_t off = (static_cast<size_t>(t.e) * p.H + h_row) * p.I + col;
+        store32_bf16(p.o0 + off, v0);
+        store32_bf16(p.o1 + off, v1);
+      }
+    }
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
+                        const __grid_constant__ CUtensorMap tmA1,
+                        const __grid_constant__ CUtensorMap tmB0,
+                        const __grid_constant__ CUtensorMap tmB1, const Params p) {
+  using Tr = Traits<MODE>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *stages = smem;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * kStageBytes);
+  uint64_t *full = bars;                 // [STAGES] TMA -> MMA
+  uint64_t *empty = bars + STAGES;       // [STAGES] MMA -> TMA
+  uint64_t *tfull = bars + 2 * STAGES;   // [2] MMA -> epilogue
+  uint64_t *tempty = tfull + 2;          // [2] epilogue -> MMA
+  uint64_t *drain = tempty + 2;          // abort path: MMA completion
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  int *s_tp = reinterpret_cast<int *>(smem + STAGES * kStageBytes + 256);  // [E+1] tile prefix
+  int *s_off = s_tp + (kMaxExperts + 1);                                    // [E+1] row offsets
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = p.E;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA0);
+    tma_prefetch_desc(&tmA1);
+    tma_prefetch_desc(&tmB0);
+    tma_prefetch_desc(&tmB1);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  for (int e = threadIdx.x; e <= E; e += kThreads) s_off[e] = __ldg(p.offsets + e);
+  __syncthreads();
+  if (warp == 2) {  // tile prefix over experts: ceil(rows / BM)
+    int carry = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      const int c = e < E ? (s_off[e + 1] - s_off[e] + BM - 1) / BM : 0;
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (e < E) s_tp[e] = carry + incl - c;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) s_tp[E] = carry;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int total = Tr::kRaggedK ? E * p.m_tiles * p.n_tiles : s_tp[E] * p.n_tiles;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t armed = 0;  // bit s: stage s armed at least once; parity of last arm in `arm_par`
+    uint32_t arm_par = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off);
+      for (int kb = 0; kb < t.nkb; ++kb) {
+        if (!warp_wait(&empty[stage], phase ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[stage], kStageBytes);
+          uint8_t *sa = stages + stage * kStageBytes;
+          produce_stage<MODE>(t, kb, sa, sa + kABytes, &full[stage], p, &tmA0, &tmA1, &tmB0, &tmB1);
+        }
+        armed |= 1u << stage;
+        arm_par = (arm_par & ~(1u << stage)) | (phase << stage);
+        __syncwarp();
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    if (*abort_flag && lane == 0) {  // let our own copies land before the CTA exits
+      for (int s = 0; s < STAGES; ++s) {
+        if (!((armed >> s) & 1u)) continue;
+        for (int i = 0; i < (1 << 22) && !mbar_try_wait(&full[s], (arm_par >> s) & 1u); ++i) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    int stage = 0;
+    uint32_t phase = 0;
+    int it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+      const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off);
+      const int buf = it & 1;
+      const uint32_t use = (it >> 1) & 1;
+      if (!warp_wait(&tempty[buf], use ^ 1, abort_flag)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + buf * BN;
+      if (t.nkb == 0) {
+        if (lane == 0) mbar_arrive(&tfull[buf]);
+        __syncwarp();
+        continue;
+      }
+      for (int kb = 0; kb < t.nkb; ++kb) {
+        if (!warp_wait(&full[stage], phase, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint8_t *sa = stages + stage * kStageBytes;
+        uint8_t *sb = sa + kABytes;
+        if constexpr (Tr::kRaggedK) {
+          const int valid = t.kcount - kb * BK;
+          if (valid < BK) {  // cut the K block at the expert's last row
+            const int nrows = BK - valid;
+            const int n16 = nrows * 8;  // 16-byte pieces per box
+            for (int q = lane; q < 6 * n16; q += 32) {
+              const int box = q / n16, rem = q % n16;
+              const int r = valid + rem / 8, c16 = rem % 8;
+              uint8_t *base = box < 2 ? sa + box * kBox : sb + (box - 2) * kBox;
+              *reinterpret_cast<uint4 *>(base + r * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+          }
+        }
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t a_base = smem_addr(sa), b_base = smem_addr(sb);
+#pragma unroll
+          for (int k16 = 0; k16 < BK / 16; ++k16) {
+            const uint64_t adesc = Tr::kAMN ? smem_desc_sw128(a_base + k16 * 2048, kBox, 1024)
+                                            : smem_desc_sw128(a_base + k16 * 32, 16, 1024);
+            const uint64_t bdesc = Tr::kBMN ? smem_desc_sw128(b_base + k16 * 2048, kBox, 1024)
+                                            : smem_desc_sw128(b_base + k16 * 32, 16, 1024);
+            tc_mma_f16(d_tmem, adesc, bdesc, Tr::kIdesc, (kb | k16) != 0 ? 1u : 0u);
+          }
+          tc_commit(&empty[stage]);
+        }
+        __syncwarp();
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) tc_commit(&tfull[buf]);
+      __syncwarp();
+    }
+    if (*abort_flag && lane == 0) {  // wait for our own MMAs before TMEM is freed
+      tc_commit(drain);
+      for (int i = 0; i < (1 << 22) && !mbar_try_wait(drain, 0); ++i) {
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int rit = q * 32 + lane;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+      const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off);
+      const int buf = it & 1;
+      const uint32_t use = (it >> 1) & 1;
+      if (!warp_wait(&tfull[buf], use, abort_flag)) break;
+      tc_fence_after();
+      epilogue_tile<MODE>(t, tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16), rit, p);
+      tc_fence_before();
+      mbar_arrive(&tempty[buf]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) flag_status(p.status, kDevWaitTimeout);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// 2-D bf16 tensor map over a row-major [rows, inner] matrix, box {64, box_rows},
+// 128-byte swizzle, zero fill out of bounds.
+bool make_map(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  auto fn = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder());
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MODE>
+cudaError_t launch_mode(const GemmArgs &a, cudaStream_t s) {
+  CUtensorMap mA0, mA1, mB0, mB1;
+  Params p{};
+  p.M_rows = a.M_rows;
+  p.H = a.H;
+  p.I = a.I;
+  p.E = a.E;
+  p.offsets = a.offsets;
+  p.o0 = a.o0;
+  p.o1 = a.o1;
+  p.o2 = a.o2;
+  p.status = a.status;
+  const uint64_t M = static_cast<uint64_t>(a.M_rows), H = a.H, I = a.I, E = a.E;
+  bool ok = true;
+  switch (MODE) {
+    case kFwdGateUp:
+      ok = make_map(&mA0, a.x_perm, H, M, 128) && make_map(&mB0, a.W_gate, I, E * H, 64) &&
+           make_map(&mB1, a.W_up, I, E * H, 64);
+      mA1 = mA0;
+      p.kdim = a.H;
+      p.n_tiles = (a.I + 127) / 128;
+      break;
+    case kFwdDown:
+      ok = make_map(&mA0, a.act, I, M, 128) && make_map(&mB0, a.W_down, H, E * I, 64);
+      mA1 = mA0;
+      mB1 = mB0;
+      p.kdim = a.I;
+      p.n_tiles = (a.H + 255) / 256;
+      break;
+    case kBwdDA:
+      ok = make_map(&mA0, a.dyw, H, M, 128) && make_map(&mB0, a.W_down, H, E * I, 256);
+      mA1 = mA0;
+      mB1 = mB0;
+      p.G = a.G;
+      p.U = a.U;
+      p.kdim = a.H;
+      p.n_tiles = (a.I + 255) / 256;
+      break;
+    case kBwdDX:
+      ok = make_map(&mA0, a.dG, I, M, 128) && make_map(&mA1, a.dU, I, M, 128) &&
+           make_map(&mB0, a.W_gate, I, E * H, 256) && make_map(&mB1, a.W_up, I, E * H, 256);
+      p.kdim = 2 * a.I;
+      p.n_tiles = (a.H + 255) / 256;
+      break;
+    case kBwdDWDown:
+      ok = make_map(&mA0, a.act, I, M, 64) && make_map(&mB0, a.dyw, H, M, 64);
+      mA1 = mA0;
+      mB1 = mB0;
+      p.m_tiles = (a.I + 127) / 128;
+      p.n_tiles = (a.H + 255) / 256;
+      break;
+    default:  // kBwdDWGateUp
+      ok = make_map(&mA0, a.x_perm, H, M, 64) && make_map(&mB0, a.dG, I, M, 64) &&
+           make_map(&mB1, a.dU, I, M, 64);
+      mA1 = mA0;
+      p.m_tiles = (a.H + 127) / 128;
+      p.n_tiles = (a.I + 127) / 128;
+      break;
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  grouped_gemm_kernel<MODE><<<a.num_sms, kThreads, kSmemBytes, s>>>(mA0, mA1, mB0, mB1, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm(GemmMode mode, const GemmArgs &a, cudaStream_t s) {
+  switch (mode) {
+    case kFwdGateUp: return launch_mode<kFwdGateUp>(a, s);
+    case kFwdDown: return launch_mode<kFwdDown>(a, s);
+    case kBwdDA: return launch_mode<kBwdDA>(a, s);
+    case kBwdDX: return launch_mode<kBwdDX>(a, s);
+    case kBwdDWDown: return launch_mode<kBwdDWDown>(a, s);
+    case kBwdDWGateUp: return launch_mode<kBwdDWGateUp>(a, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+const char *gemm_mode_name(GemmMode mode) {
+  switch (mode) {
+    case kFwdGateUp: return "gemm_gateup_swiglu";
+    case kFwdDown: return "gemm_down";
+    case kBwdDA: return "gemm_dA_dswiglu";
+    case kBwdDX: return "gemm_dX";
+    case kBwdDWDown: return "gemm_dW_down";
+    case kBwdDWGateUp: return "gemm_dW_gateup";
+  }
+  return "?";
+}
+
+}  // namespace moe

@@ -1,0 +1,86 @@
+// internal.h -- host-side declarations shared by the library's translation
+// units (kernel launchers called by the C-ABI in api.cu).  Not installed.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 16;
+
+// Status flags written by kernels into the scratch status word.
+constexpr int32_t kDevNonfiniteLogit = 0x1;
+constexpr int32_t kDevWaitTimeout = 0x2;
+
+// ---- routing (route.cu)
+constexpr int kRouteTokensPerBlock = 128;  // tokens per route block (one histogram row)
+constexpr int kRouteThreads = 512;
+
+struct RouteArgs {
+  const float *logits;  // [T,E]
+  int T, E, k;
+  int32_t *topk_idx;    // [T,k]
+  float *topk_w;        // [T,k]
+  int32_t *counts;      // [E]
+  int32_t *offsets;     // [E+1]
+  int32_t *row_of_slot; // [T*k]
+  int32_t *slot_of_row; // [T*k]
+  float *w_row;         // [T*k]
+  int32_t *lrank;       // [T*k] scratch: rank of a slot among its block's slots of the same expert
+  int32_t *hist;        // [nblk,E] scratch: per-block expert histogram
+  int32_t *block_base;  // [nblk,E] scratch: first row of each (block, expert) run
+  uint32_t *ticket;     // scratch: blocks finished (zeroed before launch)
+  int32_t *status;      // scratch status word
+};
+int route_num_blocks(int T);
+cudaError_t launch_route_topk(const RouteArgs &a, cudaStream_t s);
+cudaError_t launch_route_index(const RouteArgs &a, cudaStream_t s);
+
+// ---- row movement (gather.cu)
+// x_perm[row_of_slot[t,j]] = x[t]
+cudaError_t launch_permute_rows(const uint16_t *x, const int32_t *row_of_slot, uint16_t *x_perm,
+                                int T, int H, int k, cudaStream_t s);
+// out[t] = sum_j w[t,j] * rows[row_of_slot[t,j]]   (w == nullptr: plain sum)
+cudaError_t launch_gather_sum(const uint16_t *rows, const int32_t *row_of_slot, const float *w,
+                              uint16_t *out, int T, int H, int k, cudaStream_t s);
+// dyw[row] = w * dy[t]; g[t,j] = <dy[t], Y[row]>; d_logits; d_topk_w (nullable)
+cudaError_t launch_router_bwd(const uint16_t *dy, const uint16_t *Y, const int32_t *row_of_slot,
+                              const int32_t *topk_idx, const float *topk_w, uint16_t *dyw,
+                              float *d_logits, float *d_topk_w, int T, int H, int E, int k,
+                              cudaStream_t s);
+
+// ---- grouped GEMMs (gemm.cu)
+enum GemmMode : int {
+  kFwdGateUp = 0,   // [x_perm] . [W_gate | W_up]  -> SwiGLU epilogue: A, G, U      (ragged M)
+  kFwdDown = 1,     // A . W_down                 -> Y                              (ragged M)
+  kBwdDA = 2,       // dyw . W_down^T             -> dSwiGLU epilogue: dG, dU       (ragged M)
+  kBwdDX = 3,       // [dG | dU] . [W_gate | W_up]^T -> dX_perm                     (ragged M)
+  kBwdDWDown = 4,   // A^T . dyw                  -> dW_down                        (ragged K)
+  kBwdDWGateUp = 5  // x_perm^T . [dG | dU]       -> dW_gate, dW_up                 (ragged K)
+};
+
+struct GemmArgs {
+  int M_rows;  // permuted rows M = T*k
+  int H, I, E;
+  const int32_t *offsets;  // [E+1] expert row offsets (device)
+  // operands (device, bf16)
+  const uint16_t *x_perm, *W_gate, *W_up, *W_down;
+  const uint16_t *act;  // A [M,I]
+  const uint16_t *G, *U;
+  const uint16_t *dyw;
+  const uint16_t *dG, *dU;
+  // outputs (device, bf16)
+  uint16_t *o0, *o1, *o2;
+  int32_t *status;
+  int num_sms;
+};
+cudaError_t launch_grouped_gemm(GemmMode mode, const GemmArgs &a, cudaStream_t s);
+const char *gemm_mode_name(GemmMode mode);
+
+// driver entry point for tensor-map encoding (api.cu)
+void *tensor_map_encoder();
+
+}  // namespace moe

@@ -1,0 +1,161 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) dropless mixture-of-experts expert
+ * layer: training forward and backward on one GPU.
+ *
+ * The layer (dropless MoE; "NVIDIA lleva el MoE de DeepSeek-V3 de 103 a 1.068
+ * TFLOPS", sections on dropless vs capacity MoE, grouped GEMM and expert-
+ * parallel dispatch/combine; the Mega MoE kernel description in "Prime
+ * Intellect dopisal backward pass do kernela Mega MoE"):
+ *   route:    p = softmax(logits_t) over E experts; S_t = the k largest logits
+ *             (ties: lower expert index first); w_tj = p_{S_tj} / sum_S p.
+ *   dispatch: counts[e] = tokens that chose e; offsets = exclusive prefix;
+ *             row(t,j) = offsets[e] + #{t' < t that chose e}  (stable, no
+ *             capacity, no dropped token, no padding).
+ *   experts:  for every permuted row r of expert e, with x_r = x[token(r)]:
+ *             G = x_r W_gate[e], U = x_r W_up[e], A = silu(G) * U,
+ *             Y = A W_down[e]                      (SwiGLU MLP, no biases)
+ *   combine:  out_t = sum_j w_tj * Y[row(t,j)]      (token order restored)
+ *   backward: the same chain transposed -- dyw = w * dy (permuted), dA =
+ *             dyw W_down^T, dSwiGLU, dX = dG W_gate^T + dU W_up^T, un-permute
+ *             sum into dx, dW_* = grouped X^T-style products over each
+ *             expert's rows, and d_logits[t, S_tj] = w_tj (g_tj - sum_i w_ti
+ *             g_ti) with g_tj = <dy_t, Y[row(t,j)]>, zero for other experts.
+ *
+ * Conventions (all calls):
+ *   - Memory: the caller owns and allocates every buffer; the library never
+ *     allocates, frees or synchronises (only moe_get_device_status waits).
+ *     Pointers named "device" are CUDA device pointers; `stream` is a
+ *     cudaStream_t passed as void*; every kernel is enqueued on it, so the
+ *     calls can be captured into a CUDA graph.
+ *   - Counts and offsets stay on the device: no call copies routing results
+ *     to the host.
+ *   - Layouts are row-major, dense, as given per argument.  bf16 tensors are
+ *     IEEE bfloat16 bit patterns.
+ *   - Every device pointer must be 16-byte aligned.
+ *   - Shapes: T >= 0, H % 64 == 0 and I % 64 == 0 (both >= 64), 1 <= E <= 256,
+ *     1 <= k <= min(E, 16), T * k < 2^31.
+ *   - Errors found on the host (null pointer, bad shape, misalignment, a
+ *     too-small workspace) return a negative moe_status with nothing launched.
+ *     Anomalies found on the device (non-finite logits, a pipeline wait that
+ *     ran out of time) set flags in a status word at the start of the call's
+ *     scratch buffer; kernels never trap.  Read it with moe_get_device_status.
+ *   - The library holds no per-call state; calls on different streams with
+ *     disjoint buffers may run concurrently.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1, /* null pointer, bad shape or precision */
+  MOE_ERR_ALIGNMENT = -2,   /* a pointer is not 16-byte aligned */
+  MOE_ERR_WORKSPACE = -3,   /* a scratch/saved buffer is smaller than moe_query_workspace says */
+  MOE_ERR_UNSUPPORTED = -4, /* no sm_103a device, or a precision this build does not provide */
+  MOE_ERR_CUDA = -5,        /* a CUDA runtime/driver call failed */
+  MOE_ERR_DEVICE = -6       /* moe_get_device_status: the device reported an anomaly */
+} moe_status;
+
+typedef enum {
+  MOE_PREC_BF16 = 0,    /* bf16 operands, fp32 accumulation, everywhere */
+  MOE_PREC_FP8_BWD = 1  /* bf16 forward; backward grouped GEMMs in MXFP8 (E4M3 values,
+                           one UE8M0 scale per 32 elements along each GEMM's K) */
+} moe_precision;
+
+/* Device status flags (moe_get_device_status *host_code). */
+#define MOE_DEV_NONFINITE_LOGIT 0x1 /* a logit was NaN or +-Inf; routing outputs unspecified */
+#define MOE_DEV_WAIT_TIMEOUT 0x2    /* a pipeline wait exceeded its bound; outputs unspecified */
+
+typedef struct {
+  int32_t T;         /* tokens */
+  int32_t H;         /* hidden size */
+  int32_t I;         /* expert intermediate size */
+  int32_t E;         /* experts */
+  int32_t k;         /* experts per token */
+  int32_t precision; /* moe_precision */
+} moe_config;
+
+/* Routing results, written by moe_route, read by moe_forward/moe_backward.
+ * All device pointers, caller-owned, M = T*k. */
+typedef struct {
+  int32_t *topk_idx;    /* [T,k]  chosen experts, ordered by (logit desc, index asc) */
+  float *topk_w;        /* [T,k]  renormalised router weights */
+  int32_t *counts;      /* [E]    rows per expert */
+  int32_t *offsets;     /* [E+1]  exclusive prefix of counts; offsets[E] = M */
+  int32_t *row_of_slot; /* [T*k]  permuted row of slot t*k+j */
+  int32_t *slot_of_row; /* [M]    inverse: slot t*k+j held by permuted row r */
+  float *w_row;         /* [M]    router weight of permuted row r */
+} moe_routing;
+
+/* Byte sizes of the caller-provided buffers for a configuration:
+ *   route_scratch: moe_route's scratch;
+ *   saved:        activations moe_forward keeps for moe_backward (layout below);
+ *   fwd_scratch:  moe_forward's scratch;  bwd_scratch: moe_backward's scratch.
+ * Returns MOE_ERR_INVALID_ARG for an unsupported shape.  Host only. */
+moe_status moe_query_workspace(const moe_config *cfg, size_t *route_scratch, size_t *saved,
+                               size_t *fwd_scratch, size_t *bwd_scratch);
+
+/* Offsets (bytes) of the saved activations inside `saved`, for inspection:
+ * x_perm [M,H], G [M,I], U [M,I], A [M,I], Y [M,H], all bf16 (Y unweighted). */
+typedef struct {
+  size_t x_perm, G, U, A, Y;
+} moe_saved_layout;
+moe_status moe_saved_offsets(const moe_config *cfg, moe_saved_layout *layout);
+
+/* Router and dispatch indices.  logits: device fp32 [T,E].  Writes every field
+ * of *routing.  Per-expert counts, the scan and the permutation are computed
+ * on the device in one pass over the tokens (per-block expert histograms; the
+ * last block to finish scans them).  Non-finite logits set
+ * MOE_DEV_NONFINITE_LOGIT; the indices written are still in range. */
+moe_status moe_route(const moe_config *cfg, const float *logits, const moe_routing *routing,
+                     void *scratch, size_t scratch_bytes, void *stream);
+
+/* Forward.  x: device bf16 [T,H]; W_gate, W_up: device bf16 [E,H,I];
+ * W_down: device bf16 [E,I,H]; out: device bf16 [T,H].
+ * saved: device, at least moe_query_workspace's `saved` bytes; moe_backward
+ * reads it, so keep it unchanged between the two calls. */
+moe_status moe_forward(const moe_config *cfg, const void *x, const moe_routing *routing,
+                       const void *W_gate, const void *W_up, const void *W_down, void *out,
+                       void *saved, size_t saved_bytes, void *scratch, size_t scratch_bytes,
+                       void *stream);
+
+/* Backward.  dy: device bf16 [T,H] (gradient of out); x: the forward's input
+ * (must be unchanged); routing and saved as left by moe_route/moe_forward.
+ * Outputs (device): dx bf16 [T,H]; dW_gate, dW_up bf16 [E,H,I]; dW_down bf16
+ * [E,I,H] (overwritten, not accumulated; experts with no token get zeros);
+ * d_logits fp32 [T,E]; d_topk_w fp32 [T,k] = g_tj (may be NULL). */
+moe_status moe_backward(const moe_config *cfg, const void *dy, const void *x,
+                        const moe_routing *routing, const void *W_gate, const void *W_up,
+                        const void *W_down, const void *saved, size_t saved_bytes, void *dx,
+                        void *dW_gate, void *dW_up, void *dW_down, float *d_logits,
+                        float *d_topk_w, void *scratch, size_t scratch_bytes, void *stream);
+
+/* Waits for `stream`, then reads the status word at the start of `scratch` (a
+ * scratch buffer previously passed to moe_route, moe_forward or moe_backward).
+ * *host_code receives the MOE_DEV_* flags; returns MOE_OK when they are zero,
+ * MOE_ERR_DEVICE otherwise.  The only call that synchronises. */
+moe_status moe_get_device_status(const void *scratch, void *stream, int32_t *host_code);
+
+/* Static description of a status code. */
+const char *moe_status_string(moe_status status);
+
+/* Optional per-kernel timing for profiling.  When `events` is non-NULL, every
+ * later library call records events[2i] and events[2i+1] (cudaEvent_t as
+ * void*) on its stream around the i-th kernel it launches, counting from the
+ * attach, up to `capacity` kernels; moe_timing_count returns how many were
+ * recorded.  Process-wide, not thread-safe; pass NULL to detach. */
+moe_status moe_timing_attach(void *const *events, int32_t capacity);
+int32_t moe_timing_count(void);
+/* Name of the i-th timed kernel (static string; NULL when out of range). */
+const char *moe_timing_label(int32_t i);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

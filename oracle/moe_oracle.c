@@ -333,6 +333,27 @@ EXPORT int oracle_forward(const oracle_shape *sh, const uint16_t *x, const int32
   return bad ? -1 : 0;
 }
 
+/* Expert intermediates of listed (token, expert) pairs, for localising a
+ * mismatch: g, u, a [n, I] and y [n, H] of expert e on token t. */
+EXPORT int oracle_expert_rows(const oracle_shape *sh, const uint16_t *x, const uint16_t *Wg,
+                              const uint16_t *Wu, const uint16_t *Wd, int64_t n,
+                              const int64_t *tokens, const int32_t *experts, double *g, double *u,
+                              double *a, double *y) {
+  ctx_t c;
+  ctx_init(&c, sh, x, Wg, Wu, Wd, NULL, NULL, NULL, NULL);
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+  for (int64_t q = 0; q < n; ++q) {
+    if (tokens[q] < 0 || tokens[q] >= sh->T || experts[q] < 0 || experts[q] >= sh->E) {
+      bad = 1;
+      continue;
+    }
+    expert_fwd(&c, tokens[q], experts[q], g + q * sh->I, u + q * sh->I, a + q * sh->I,
+               y + q * sh->H);
+  }
+  return bad ? -1 : 0;
+}
+
 /* Backward for a list of tokens.
  *   gdot_j   = <dy_t, y(t, S_j)>                       (gradient wrt w_j)
  *   da       = w_j * dy_t . W_down[e]^T

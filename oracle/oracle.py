@@ -52,6 +52,7 @@ def lib():
             L.oracle_backward_tokens.argtypes = [P, P, P, P, P, P, P, P, P, i32, P, P, P, i64, P, P, P, P]
             L.oracle_dw_full.argtypes = [P, P, P, P, P, P, P, P, i32, P, P, P, P, P, P]
             L.oracle_dw_elements.argtypes = [P, P, P, P, P, P, P, P, i32, P, P, P, i64, P, P, P, P, P]
+            L.oracle_expert_rows.argtypes = [P, P, P, P, P, i64, P, P, P, P, P, P]
             L.oracle_e4m3_encode.argtypes = [ctypes.c_double]
             L.oracle_e4m3_encode.restype = ctypes.c_uint8
             L.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
@@ -61,6 +62,7 @@ def lib():
             L.oracle_mx_quantize_rows_bf16.argtypes = [i64, i64, P, P, P, P]
             L.oracle_mx_quantize_cols_bf16.argtypes = [i64, i64, i64, P, P, P]
             for f in ("oracle_route", "oracle_dispatch", "oracle_forward", "oracle_backward_tokens",
+                      "oracle_expert_rows",
                       "oracle_dw_full", "oracle_dw_elements", "oracle_mx_quantize_rows_bf16",
                       "oracle_mx_quantize_cols_bf16"):
                 getattr(L, f).restype = ctypes.c_int
@@ -120,6 +122,22 @@ def forward(shape, x, topk_idx, topk_w, W_gate, W_up, W_down, tokens=None, want_
                                 _p(_c(W_up, np.uint16)), _p(_c(W_down, np.uint16)), n, _p(tokens),
                                 _p(out), _p(y)), "forward")
     return (out, y) if want_y else out
+
+
+def expert_rows(shape, x, W_gate, W_up, W_down, tokens, experts):
+    """g, u, a [n,I] and y [n,H] (fp64) of expert experts[q] applied to token tokens[q]."""
+    tokens = _c(tokens, np.int64)
+    experts = _c(experts, np.int32)
+    n = len(tokens)
+    g = np.empty((n, shape.I))
+    u = np.empty((n, shape.I))
+    a = np.empty((n, shape.I))
+    y = np.empty((n, shape.H))
+    sh = _shape(shape)
+    _check(lib().oracle_expert_rows(ctypes.byref(sh), _p(_c(x, np.uint16)), _p(_c(W_gate, np.uint16)),
+                                    _p(_c(W_up, np.uint16)), _p(_c(W_down, np.uint16)), n, _p(tokens),
+                                    _p(experts), _p(g), _p(u), _p(a), _p(y)), "expert_rows")
+    return g, u, a, y
 
 
 def quant_weights(W_gate, W_up, W_down):

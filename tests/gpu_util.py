@@ -1,0 +1,100 @@
+"""Helpers for the GPU parity tests: run the layer through the C ABI on seeded
+inputs and compare with the fp64 oracle.
+
+Tolerances (floating point): relative L2 <= 5e-3 and max |diff| <= 2e-2 *
+max |ref| for bf16 outputs and gradients; router weights within 1e-6; integer
+routing and permutation bit-exact.
+"""
+import numpy as np
+import torch
+
+from dropless_mixture_experts_top_gb300 import moe, synth
+from dropless_mixture_experts_top_gb300.synth import bf16_bits_to_f32
+from oracle import oracle as O
+
+REL_L2 = 5e-3
+MAX_REL = 2e-2
+W_ATOL = 1e-6
+
+
+def to_dev(inp, dev="cuda"):
+    t = {n: torch.from_numpy(np.ascontiguousarray(inp[n]).view(np.int16)).to(dev)
+         for n in ("x", "W_gate", "W_up", "W_down", "dy") if n in inp}
+    t["logits"] = torch.from_numpy(inp["logits"]).to(dev)
+    return t
+
+
+def bf(t):
+    return bf16_bits_to_f32(t.cpu().numpy().view(np.uint16)).astype(np.float64)
+
+
+def close(name, got, ref, rel_l2=REL_L2, max_rel=MAX_REL):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{name}: non-finite values"
+    nref = np.linalg.norm(ref)
+    err = np.linalg.norm(got - ref)
+    rel = err / nref if nref > 0 else err
+    mx = np.abs(got - ref).max() if got.size else 0.0
+    amax = np.abs(ref).max() if ref.size else 0.0
+    assert rel <= rel_l2, f"{name}: rel L2 {rel:.3e} > {rel_l2}"
+    assert mx <= max_rel * amax + 1e-30, f"{name}: max|diff| {mx:.3e} > {max_rel} * {amax:.3e}"
+    return rel
+
+
+def run_layer(shape, inp, precision="bf16", layer=None, stream=None):
+    t = to_dev(inp)
+    layer = layer or moe.MoELayer(shape, precision=precision)
+    layer.route(t["logits"], stream)
+    out = layer.forward(t["x"], t["W_gate"], t["W_up"], t["W_down"], stream=stream)
+    grads = layer.backward(t["dy"], t["x"], t["W_gate"], t["W_up"], t["W_down"], stream=stream)
+    torch.cuda.synchronize()
+    return layer, out, grads
+
+
+def check_routing(shape, inp, layer):
+    idx, w = O.route(inp["logits"], shape.k)
+    counts, offsets, ros, sor = O.dispatch(idx, shape.E)
+    r = {n: v.cpu().numpy() for n, v in layer.routing.items()}
+    np.testing.assert_array_equal(r["topk_idx"], idx)
+    np.testing.assert_array_equal(r["counts"], counts)
+    np.testing.assert_array_equal(r["offsets"], offsets)
+    np.testing.assert_array_equal(r["row_of_slot"], ros)
+    np.testing.assert_array_equal(r["slot_of_row"], sor)
+    assert np.abs(r["topk_w"].astype(np.float64) - w).max() <= W_ATOL
+    np.testing.assert_array_equal(r["w_row"], r["topk_w"].ravel()[sor])
+    return idx, w, counts, offsets, ros, sor
+
+
+def check_full(shape, inp, layer, out, grads, precision="bf16", check_saved=True):
+    """Every output element against the oracle (small shapes)."""
+    idx, w, counts, offsets, ros, sor = check_routing(shape, inp, layer)
+    quant = precision == "fp8_bwd"
+    if check_saved:
+        xp = layer.saved_tensor("x_perm").cpu().numpy().view(np.uint16)
+        np.testing.assert_array_equal(xp, inp["x"][sor // shape.k])
+        toks = sor // shape.k
+        experts = idx.ravel()[sor]
+        g, u, a, y = O.expert_rows(shape, inp["x"], inp["W_gate"], inp["W_up"], inp["W_down"], toks, experts)
+        close("G", bf(layer.saved_tensor("G")), g)
+        close("U", bf(layer.saved_tensor("U")), u)
+        close("A", bf(layer.saved_tensor("A")), a)
+        close("Y", bf(layer.saved_tensor("Y")), y)
+    ref = O.forward(shape, inp["x"], idx, w, inp["W_gate"], inp["W_up"], inp["W_down"])
+    close("out", bf(out), ref)
+    dx, dl, gd = O.backward_tokens(shape, inp["x"], inp["logits"], idx, w, inp["W_gate"], inp["W_up"],
+                                   inp["W_down"], inp["dy"], quant=quant)
+    dWg, dWu, dWd = O.dw_full(shape, inp["x"], idx, w, inp["W_gate"], inp["W_up"], inp["W_down"],
+                              inp["dy"], quant=quant)
+    tol = dict(rel_l2=5e-2 if quant else REL_L2)
+    close("d_logits", grads["d_logits"].cpu().numpy(), dl)
+    close("d_topk_w", grads["d_topk_w"].cpu().numpy(), gd)
+    close("dx", bf(grads["dx"]), dx, **tol)
+    close("dW_gate", bf(grads["dW_gate"]), dWg, **tol)
+    close("dW_up", bf(grads["dW_up"]), dWu, **tol)
+    close("dW_down", bf(grads["dW_down"]), dWd, **tol)
+    for e in np.flatnonzero(counts == 0):
+        for n in ("dW_gate", "dW_up", "dW_down"):
+            assert np.all(grads[n][e].cpu().numpy() == 0), (n, e)
+    return idx, w

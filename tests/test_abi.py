@@ -1,0 +1,100 @@
+"""The C-ABI library builds, loads and exports every declared entry point; host-side
+validation rejects bad arguments before anything is launched (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from dropless_mixture_experts_top_gb300 import _build, moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return moe.lib()
+
+
+def declared_functions():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", h)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            names += re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", txt)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(moe.EXPORTED) <= set(names)
+
+
+def cfg(T=512, H=128, I=64, E=8, k=2, prec=0):
+    return moe.Config(T, H, I, E, k, prec)
+
+
+def test_query_workspace_sizes(L):
+    rs, sv, fs, bs = moe.query_workspace(cfg())
+    M = 512 * 2
+    assert sv >= M * (128 * 2 * 2 + 64 * 3 * 2)   # x_perm, Y, G, U, A
+    assert bs >= 256 + M * (128 * 2 * 2 + 64 * 2 * 2)  # dyw, dX, dG, dU
+    assert rs >= 256 + M * 4
+    offs = moe.saved_offsets(cfg())
+    assert offs["x_perm"] == 0 and all(v % 256 == 0 for v in offs.values())
+    assert offs["Y"] + M * 128 * 2 <= sv
+
+
+@pytest.mark.parametrize("bad", [dict(H=100), dict(I=32), dict(E=0), dict(E=257), dict(k=0), dict(k=17),
+                                 dict(E=4, k=5), dict(T=-1), dict(prec=7)])
+def test_bad_shapes_rejected(L, bad):
+    c = cfg(**bad)
+    sz = ctypes.c_size_t()
+    assert L.moe_query_workspace(ctypes.byref(c), ctypes.byref(sz), None, None, None) == -1
+
+
+def test_route_validation_before_launch(L):
+    c = cfg()
+    rs = moe.query_workspace(c)[0]
+    good = [0x1000 * (i + 1) for i in range(7)]
+    r = moe.Routing(*good)
+    P = ctypes.c_void_p
+    # null routing member
+    r0 = moe.Routing(*([0] + good[1:]))
+    assert L.moe_route(ctypes.byref(c), P(0x10000), ctypes.byref(r0), P(0x20000), rs, None) == -1
+    # misaligned logits
+    assert L.moe_route(ctypes.byref(c), P(0x10004), ctypes.byref(r), P(0x20000), rs, None) == -2
+    # scratch too small
+    assert L.moe_route(ctypes.byref(c), P(0x10000), ctypes.byref(r), P(0x20000), rs - 1, None) == -3
+
+
+def test_forward_backward_validation_before_launch(L):
+    c = cfg()
+    rs, sv, fs, bs = moe.query_workspace(c)
+    r = moe.Routing(*[0x1000 * (i + 1) for i in range(7)])
+    P = ctypes.c_void_p
+    a = [P(0x100000 * (i + 1)) for i in range(12)]
+    rc = L.moe_forward(ctypes.byref(c), a[0], ctypes.byref(r), a[1], a[2], a[3], a[4], a[5], sv - 16,
+                       a[6], fs, None)
+    assert rc == -3
+    rc = L.moe_forward(ctypes.byref(c), P(0x100008), ctypes.byref(r), a[1], a[2], a[3], a[4], a[5], sv,
+                       a[6], fs, None)
+    assert rc == -2
+    rc = L.moe_backward(ctypes.byref(c), a[0], a[1], ctypes.byref(r), a[2], a[3], a[4], a[5], sv, a[6],
+                        a[7], a[8], a[9], None, None, a[10], bs, None)
+    assert rc == -1  # d_logits is required
+    rc = L.moe_backward(ctypes.byref(c), a[0], a[1], ctypes.byref(r), a[2], a[3], a[4], a[5], sv, a[6],
+                        a[7], a[8], a[9], a[11], None, a[10], bs - 256, None)
+    assert rc == -3
+
+
+def test_status_strings(L):
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert len(moe.status_string(code)) >= 2
+    assert moe.status_string(-99) == "unknown status"
+    assert L.moe_timing_count() == 0

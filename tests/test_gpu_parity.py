@@ -1,0 +1,145 @@
+"""GPU path against the fp64 oracle, every output element, on small seeded shapes
+that span several tiles and ragged tails, plus the method's degenerate cases."""
+import numpy as np
+import pytest
+import torch
+
+from dropless_mixture_experts_top_gb300 import moe, synth
+from dropless_mixture_experts_top_gb300.synth import MoEShape
+from tests import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [
+    ("tiny", MoEShape(T=512, H=128, I=64, E=8, k=2)),
+    ("ragged_tiles", MoEShape(T=700, H=256, I=192, E=6, k=2)),   # several M/N/K tiles, ragged tails
+    ("wide", MoEShape(T=300, H=576, I=320, E=16, k=4)),          # N/K not multiples of the tile
+    ("k1", MoEShape(T=200, H=128, I=128, E=4, k=1)),
+    ("k_eq_E", MoEShape(T=130, H=128, I=64, E=3, k=3)),
+    ("single_expert", MoEShape(T=333, H=192, I=128, E=1, k=1)),
+]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _build():
+    from dropless_mixture_experts_top_gb300 import _build as B
+    B.build()
+
+
+@pytest.mark.parametrize("name,shape", SHAPES, ids=[s[0] for s in SHAPES])
+def test_layer_matches_oracle(name, shape):
+    inp = synth.make_inputs_shape(shape, 31)
+    layer, out, grads = G.run_layer(shape, inp)
+    assert layer.status() == {"route": 0, "forward": 0, "backward": 0}
+    G.check_full(shape, inp, layer, out, grads)
+
+
+def test_workload_tiny_config():
+    w = synth.WORKLOADS["tiny_t512_h128_i64_e8_k2"]
+    inp = synth.make_inputs(w)
+    layer, out, grads = G.run_layer(w.shape, inp)
+    G.check_full(w.shape, inp, layer, out, grads)
+
+
+def test_empty_experts_and_hot_expert():
+    shape = MoEShape(T=640, H=128, I=128, E=8, k=2)
+    inp = synth.make_inputs_shape(shape, 41)
+    inp["logits"][:, 2] -= 30.0   # never chosen
+    inp["logits"][:, 5] -= 30.0   # never chosen
+    inp["logits"][:, 6] += 12.0   # chosen by every token, weight close to 1
+    layer, out, grads = G.run_layer(shape, inp)
+    idx, _ = G.check_full(shape, inp, layer, out, grads)
+    counts = layer.routing["counts"].cpu().numpy()
+    assert counts[2] == 0 and counts[5] == 0 and counts[6] == shape.T
+
+
+def test_all_tokens_one_expert_tail():
+    # T not a multiple of 128, every token on expert 0 (k=1): one long ragged segment
+    shape = MoEShape(T=1000, H=128, I=64, E=4, k=1)
+    inp = synth.make_inputs_shape(shape, 43)
+    inp["logits"][:, 0] += 100.0
+    layer, out, grads = G.run_layer(shape, inp)
+    G.check_full(shape, inp, layer, out, grads)
+
+
+def test_zero_tokens():
+    shape = MoEShape(T=0, H=128, I=64, E=4, k=2)
+    layer = moe.MoELayer(shape)
+    dev = "cuda"
+    logits = torch.empty((0, 4), dtype=torch.float32, device=dev)
+    x = torch.empty((0, 128), dtype=torch.int16, device=dev)
+    W = [torch.ones((4, 128, 64), dtype=torch.int16, device=dev)] * 2 + \
+        [torch.ones((4, 64, 128), dtype=torch.int16, device=dev)]
+    layer.route(logits)
+    out = layer.forward(x, *W)
+    grads = {"dx": x.clone(), "dW_gate": torch.full((4, 128, 64), 7, dtype=torch.int16, device=dev),
+             "dW_up": torch.full((4, 128, 64), 7, dtype=torch.int16, device=dev),
+             "dW_down": torch.full((4, 64, 128), 7, dtype=torch.int16, device=dev),
+             "d_logits": logits.clone(), "d_topk_w": torch.empty((0, 2), dtype=torch.float32, device=dev)}
+    layer.backward(x, x, *W, grads=grads)
+    torch.cuda.synchronize()
+    assert out.numel() == 0
+    assert layer.routing["offsets"].cpu().tolist() == [0] * 5
+    for n in ("dW_gate", "dW_up", "dW_down"):
+        assert int(grads[n].abs().sum()) == 0
+
+
+def test_nonfinite_logits_flagged_not_trapped():
+    shape = MoEShape(T=256, H=128, I=64, E=8, k=2)
+    inp = synth.make_inputs_shape(shape, 47)
+    inp["logits"][3, 1] = np.nan
+    inp["logits"][7, 4] = np.inf
+    t = G.to_dev(inp)
+    layer = moe.MoELayer(shape)
+    layer.route(t["logits"])
+    code = moe.get_device_status(layer.route_scratch)
+    assert code & moe.DEV_NONFINITE_LOGIT
+    idx = layer.routing["topk_idx"].cpu().numpy()
+    assert idx.min() >= 0 and idx.max() < shape.E
+    assert np.all(np.sort(idx, 1)[:, 0] != np.sort(idx, 1)[:, 1])  # distinct experts per token
+    # the permutation is still a bijection
+    sor = layer.routing["slot_of_row"].cpu().numpy()
+    assert np.array_equal(np.sort(sor), np.arange(shape.T * shape.k))
+    # a clean call afterwards reports no anomaly (the status word is reset per call)
+    inp["logits"] = np.nan_to_num(inp["logits"], nan=0.0, posinf=0.0)
+    layer.route(G.to_dev(inp)["logits"])
+    assert moe.get_device_status(layer.route_scratch) == 0
+
+
+def test_deterministic_bitwise():
+    shape = MoEShape(T=700, H=256, I=192, E=6, k=2)
+    inp = synth.make_inputs_shape(shape, 53)
+    _, out1, g1 = G.run_layer(shape, inp)
+    _, out2, g2 = G.run_layer(shape, inp)
+    assert torch.equal(out1, out2)
+    for n in g1:
+        assert torch.equal(g1[n], g2[n]), n
+
+
+def test_cuda_graph_capture_and_replay_with_new_routing():
+    shape = MoEShape(T=512, H=128, I=128, E=8, k=2)
+    inp = synth.make_inputs_shape(shape, 59)
+    t = G.to_dev(inp)
+    layer = moe.MoELayer(shape)
+    s = torch.cuda.Stream()
+    out = torch.empty((shape.T, shape.H), dtype=torch.int16, device="cuda")
+    grads = None
+    with torch.cuda.stream(s):  # warm-up outside capture (first-call attribute setup)
+        layer.route(t["logits"], s)
+        layer.forward(t["x"], t["W_gate"], t["W_up"], t["W_down"], out=out, stream=s)
+        grads = layer.backward(t["dy"], t["x"], t["W_gate"], t["W_up"], t["W_down"], stream=s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        layer.route(t["logits"], s)
+        layer.forward(t["x"], t["W_gate"], t["W_up"], t["W_down"], out=out, stream=s)
+        layer.backward(t["dy"], t["x"], t["W_gate"], t["W_up"], t["W_down"], grads=grads, stream=s)
+    # new routing (different loads, including an empty expert) replayed through the same graph
+    inp2 = dict(inp)
+    lg = np.random.default_rng(5).standard_normal(inp["logits"].shape).astype(np.float32)
+    lg[:, 3] -= 50.0
+    inp2["logits"] = lg
+    t["logits"].copy_(torch.from_numpy(lg).cuda())
+    g.replay()
+    torch.cuda.synchronize()
+    G.check_full(shape, inp2, layer, out, grads)
