@@ -1,0 +1,421 @@
+"""Benchmark: one training step of the dropless MoE expert layer (route + forward +
+backward over one 16,384-token batch) on a GB300, through the C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-cpu-baseline]
+
+Prints one JSON line (rank 0).  `value` is whole-job tokens/s with inputs
+resident in HBM; `e2e` is the same step with host buffers (pinned host ->
+device copies of x, logits, dy and device -> host copies of out, dx, d_logits
+inside the timed region).  Each timed step is bracketed by CUDA events on the
+library's stream; an L2 flush (256 MiB write) runs between steps, outside the
+events.  `roofline` covers the kernel with the largest share of step time, timed
+live with per-kernel events.  `cpu_baseline` is the fp64 oracle timed on this
+host's cores on a bounded sub-batch.
+
+--impl reference times that oracle alone (the only reference this method has:
+the pages publish no runnable code), on bounded sub-batches of the same workload.
+
+N > 1 (torchrun): every rank runs an independent replica of the workload on its
+own GPU (the layer has no cross-GPU exchange on one GPU's worth of experts);
+`value` sums tokens over ranks and divides by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from dropless_mixture_experts_top_gb300 import synth  # noqa: E402
+
+METRIC = "MoE layer fwd+bwd ms, TFLOPS & tokens/s on 1 GB300; % of dense tensor peak"
+DEFAULT_WORKLOAD = "qwen3_30b_a3b_layer_t16384"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_work(shape):
+    """Algorithmic work per launch: (bound, amount, unit) -- flops for the grouped
+    GEMMs, bytes each memory-bound kernel must move at minimum."""
+    T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
+    M = T * k
+    MHI = float(M) * H * I
+    return {
+        "route_topk": ("hbm", T * E * 4 + T * k * 12.0, "B"),
+        "route_index": ("hbm", T * k * 12.0 + M * 12.0, "B"),
+        "permute_rows": ("hbm", T * H * 2 + M * H * 2.0 + M * 4, "B"),
+        "gemm_gateup_swiglu": ("tensor", 4 * MHI, "flop"),
+        "gemm_down": ("tensor", 2 * MHI, "flop"),
+        "combine": ("hbm", M * H * 2 + T * H * 2.0 + M * 8, "B"),
+        "router_bwd": ("hbm", T * H * 2 + 2 * M * H * 2.0 + T * E * 4 + M * 12, "B"),
+        "gemm_dA_dswiglu": ("tensor", 2 * MHI, "flop"),
+        "gemm_dX": ("tensor", 4 * MHI, "flop"),
+        "unpermute_sum": ("hbm", M * H * 2 + T * H * 2.0 + M * 4, "B"),
+        "gemm_dW_down": ("tensor", 2 * MHI, "flop"),
+        "gemm_dW_gateup": ("tensor", 4 * MHI, "flop"),
+    }
+
+
+def source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dropless_mixture_experts_top_gb300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, n), "rb") as f:
+            h.update(n.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel, workload):
+    """dram bytes per launch from a committed ncu summary, if taken on the current source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    ent = rec.get(workload, {}).get(kernel)
+    if not ent or ent.get("source_hash") != source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                p = [c.strip() for c in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    smax.append(float(p[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, p[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle leg
+
+def oracle_sub_batch_step(O, w, inp, S):
+    """The oracle's whole step (route, forward, backward incl. weight gradients) on the
+    first S tokens of the workload.  Returns seconds."""
+    shape = w.shape
+    sub = synth.MoEShape(T=S, H=shape.H, I=shape.I, E=shape.E, k=shape.k)
+    t0 = time.perf_counter()
+    idx, wts = O.route(inp["logits"][:S], shape.k)
+    O.dispatch(idx, shape.E)
+    O.forward(sub, inp["x"][:S], idx, wts, inp["W_gate"], inp["W_up"], inp["W_down"])
+    quant = w.precision == "fp8_bwd"
+    qW = O.quant_weights(inp["W_gate"], inp["W_up"], inp["W_down"]) if quant else None
+    O.backward_tokens(sub, inp["x"][:S], inp["logits"][:S], idx, wts, inp["W_gate"], inp["W_up"],
+                      inp["W_down"], inp["dy"][:S], quant=quant, qW=qW)
+    O.dw_full(sub, inp["x"][:S], idx, wts, inp["W_gate"], inp["W_up"], inp["W_down"], inp["dy"][:S],
+              quant=quant, qW=qW)
+    return time.perf_counter() - t0
+
+
+def size_oracle_sample(O, w, inp, target_s):
+    """Tokens per sub-batch so that one oracle step takes about target_s seconds
+    (two probes fit a fixed cost plus a per-token cost)."""
+    p1, p2 = 16, 64
+    t1 = oracle_sub_batch_step(O, w, inp, p1)
+    t2 = oracle_sub_batch_step(O, w, inp, p2)
+    per_tok = max((t2 - t1) / (p2 - p1), 1e-6)
+    fixed = max(t1 - per_tok * p1, 0.0)
+    S = int((target_s - fixed) / per_tok)
+    return max(p2, min(w.shape.T, S)), per_tok
+
+
+def cpu_cores():
+    n = os.environ.get("OMP_NUM_THREADS")
+    return int(n) if n else (len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count())
+
+
+def cpu_baseline(w, inp, target_s=15.0):
+    from oracle import oracle as O
+    S, _ = size_oracle_sample(O, w, inp, target_s)
+    dt = oracle_sub_batch_step(O, w, inp, S)
+    return {"value": S / dt, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"first {S} of {w.shape.T} tokens through the oracle's full step (route, forward, "
+                      f"backward with weight gradients), {dt:.1f} s"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from oracle import oracle as O
+    O.build()
+    w = synth.WORKLOADS[args.workload]
+    inp = synth.make_inputs(w)
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    S, _ = size_oracle_sample(O, w, inp, budget)
+    for _ in range(args.warmup):
+        oracle_sub_batch_step(O, w, inp, S)
+    times = [oracle_sub_batch_step(O, w, inp, S) for _ in range(args.steps)]
+    sec = statistics.mean(times)
+    value = S / sec
+    shape = w.shape
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "T": shape.T, "H": shape.H, "I": shape.I, "E": shape.E, "k": shape.k,
+                   "precision": w.precision, "sample_tokens_per_step": S},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"first {S} of {shape.T} tokens per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def ensure_built(rank):
+    from dropless_mixture_experts_top_gb300 import _build
+    if rank == 0:
+        _build.build()
+    else:
+        for _ in range(600):
+            if _build.up_to_date():
+                break
+            time.sleep(1)
+
+
+def run_ours(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    ensure_built(rank)
+    from dropless_mixture_experts_top_gb300 import moe
+
+    w = synth.WORKLOADS[args.workload]
+    shape = w.shape
+    inp = synth.make_inputs(w)
+    dev = torch.device("cuda", local)
+    d = {n: torch.from_numpy(inp[n].view(np.int16)).to(dev) for n in ("x", "W_gate", "W_up", "W_down", "dy")}
+    d["logits"] = torch.from_numpy(inp["logits"]).to(dev)
+    layer = moe.MoELayer(shape, precision=w.precision, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    grads = None
+
+    def step():
+        nonlocal grads
+        layer.route(d["logits"], stream)
+        layer.forward(d["x"], d["W_gate"], d["W_up"], d["W_down"], out=out, stream=stream)
+        ev_mid.record(stream)
+        grads = layer.backward(d["dy"], d["x"], d["W_gate"], d["W_up"], d["W_down"], grads=grads, stream=stream)
+
+    out = torch.empty((shape.T, shape.H), dtype=torch.int16, device=dev)
+    ev_mid = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.zero_()
+            step()
+    torch.cuda.synchronize()
+    st = layer.status(stream)
+    if any(st.values()):
+        raise RuntimeError(f"device status after warm-up: {st}")
+
+    # timed region: per-step events, per-kernel events through the library's timing hook
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    cap = 64 * K
+    kev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * cap)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        moe.timing_attach(kev)
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                flush.zero_()
+                starts[i].record(stream)
+                ev_mid = mids[i]
+                step()
+                ends[i].record(stream)
+        torch.cuda.synchronize()
+        nk = moe.timing_count()
+        labels = [moe.timing_label(i) for i in range(nk)]
+        moe.timing_attach(None)
+    if dist:
+        dist.barrier()
+    fwd = [starts[i].elapsed_time(mids[i]) for i in range(K)]
+    bwd = [mids[i].elapsed_time(ends[i]) for i in range(K)]
+    tot = [starts[i].elapsed_time(ends[i]) for i in range(K)]
+    ms = statistics.mean(tot)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    kern = {}
+    for i, lab in enumerate(labels):
+        kern.setdefault(lab, []).append(kev[2 * i].elapsed_time(kev[2 * i + 1]))
+
+    # end to end through the public API with host buffers
+    pin = {n: torch.from_numpy(inp[n].view(np.int16)).pin_memory() for n in ("x", "dy")}
+    pin["logits"] = torch.from_numpy(inp["logits"]).pin_memory()
+    host_out = torch.empty((shape.T, shape.H), dtype=torch.int16).pin_memory()
+    host_dx = torch.empty((shape.T, shape.H), dtype=torch.int16).pin_memory()
+    host_dl = torch.empty((shape.T, shape.E), dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = sum(t.numel() * t.element_size() for t in (host_out, host_dx, host_dl))
+    e_starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    e_ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            flush.zero_()
+            e_starts[i].record(stream)
+            for n in ("x", "dy", "logits"):
+                d[n].copy_(pin[n], non_blocking=True)
+            step()
+            host_out.copy_(out, non_blocking=True)
+            host_dx.copy_(grads["dx"], non_blocking=True)
+            host_dl.copy_(grads["d_logits"], non_blocking=True)
+            e_ends[i].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(e_starts[i].elapsed_time(e_ends[i]) for i in range(K))
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    st = layer.status(stream)
+    if any(st.values()):
+        raise RuntimeError(f"device status after timed steps: {st}")
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = load_peaks()
+    work = kernel_work(shape)
+    fwd_fl, bwd_fl = shape.gemm_flops()
+    kernels = {}
+    for lab, ts in kern.items():
+        bound, amount, unit = work.get(lab, ("?", 0.0, "?"))
+        avg = statistics.mean(ts)
+        if bound == "tensor":
+            ach, pk, u = amount / (avg * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+        else:
+            ach, pk, u = amount / (avg * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
+        kernels[lab] = {"launches": len(ts), "avg_ms": avg, "share": sum(ts) / sum(sum(v) for v in kern.values()),
+                        "bound": bound, "achieved": ach, "unit": u, "frac": ach / pk}
+    top = max(kernels, key=lambda n: kernels[n]["share"])
+    kt = kernels[top]
+    roofline = {"kernel": top, "bound": kt["bound"], "achieved": kt["achieved"],
+                "peak": peaks["bf16_tflops"] if kt["bound"] == "tensor" else peaks["hbm_gbs"],
+                "unit": kt["unit"], "frac": kt["frac"],
+                "traffic": committed_traffic(top, w.name),
+                "peak_source": f"{peak_src} ({'bf16 burst' if kt['bound'] == 'tensor' else 'HBM copy'})"}
+    world_tokens = shape.T * world
+    fwd_ms, bwd_ms = statistics.mean(fwd), statistics.mean(bwd)
+    line = {
+        "metric": METRIC, "value": world_tokens / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded normals; Qwen3-shaped layer)",
+        "config": {"workload": w.name, "T": shape.T, "H": shape.H, "I": shape.I, "E": shape.E, "k": shape.k,
+                   "precision": w.precision, "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "256 MiB flush between steps; inputs (weights 1.1+ GiB) exceed L2",
+                   "step": "route + forward + backward (all weight and data gradients)"},
+        "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "fwd_bwd_ms": ms, "ckpt_2f_plus_b_ms": 2 * fwd_ms + bwd_ms,
+        "tflops": (fwd_fl + bwd_fl) / (ms * 1e-3) / 1e12,
+        "frac_of_bf16_peak": (fwd_fl + bwd_fl) / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+        "roofline": roofline, "kernels": kernels,
+        "e2e": {"value": world_tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": nk, "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(w, inp)
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=15)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(synth.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -596,14 +596,22 @@ EXPORT int oracle_dw_elements(const oracle_shape *sh, const uint16_t *x, const i
     int64_t n = expert_rows(sh, topk_idx, e, tok, ch);
     double *L = malloc(sizeof(double) * (size_t)(n + 1));
     double *R = malloc(sizeof(double) * (size_t)(n + 1));
-    double *buf = malloc(sizeof(double) * (size_t)(4 * I + H));
-    double *g = buf, *u = g + I, *a = u + I, *dyw = a + I;
+    double *dyw = malloc(sizeof(double) * (size_t)H);
+    /* only column ci of g and u is needed: the same sums over h, in the same
+     * order, as expert_fwd computes for every column */
+    const int ci = (wh == 2) ? r0 : c0;
+    const uint16_t *wg = Wg + (int64_t)e * H * I, *wu = Wu + (int64_t)e * H * I;
     for (int64_t r = 0; r < n; ++r) {
       int64_t t = tok[r];
       double w = topk_w[t * k + ch[r]];
-      expert_fwd(&c, t, e, g, u, a, NULL);
+      double gi = 0.0, ui = 0.0;
+      for (int h = 0; h < H; ++h) {
+        double xv = bf(x[t * H + h]);
+        gi += xv * bf(wg[(int64_t)h * I + ci]);
+        ui += xv * bf(wu[(int64_t)h * I + ci]);
+      }
       if (wh == 2) { /* dW_down[e, i=r0, h=c0] = sum a_i * (w dy)_h */
-        L[r] = a[r0];
+        L[r] = silu(gi) * ui;
         R[r] = w * bf(dy[t * H + c0]);
       } else { /* dW_gate/up[e, h=r0, i=c0] = sum x_h * dg_i (du_i) */
         for (int h = 0; h < H; ++h) dyw[h] = w * bf(dy[t * H + h]);
@@ -616,9 +624,9 @@ EXPORT int oracle_dw_elements(const oracle_shape *sh, const uint16_t *x, const i
           const uint16_t *wd = Wd + ((int64_t)e * I + c0) * H;
           for (int h = 0; h < H; ++h) da += dyw[h] * bf(wd[h]);
         }
-        double gi = g[c0], sg = sigmoid(gi);
+        double sg = sigmoid(gi);
         L[r] = bf(x[t * H + r0]);
-        R[r] = (wh == 0) ? da * u[c0] * sg * (1.0 + gi * (1.0 - sg)) : da * silu(gi);
+        R[r] = (wh == 0) ? da * ui * sg * (1.0 + gi * (1.0 - sg)) : da * silu(gi);
       }
     }
     if (quant) {
@@ -632,7 +640,7 @@ EXPORT int oracle_dw_elements(const oracle_shape *sh, const uint16_t *x, const i
     free(ch);
     free(L);
     free(R);
-    free(buf);
+    free(dyw);
   }
   return bad ? -1 : 0;
 }

@@ -1,0 +1,89 @@
+"""Full-size workloads (T=16384, the 30B- and 235B-shaped layers) through the C ABI,
+in the launch configuration the benchmark times.
+
+Routing and the permutation are compared in full (bit-exact).  Floating-point
+outputs are compared on samples the oracle computes one by one: whole output
+rows of sampled tokens (out, dx, d_logits, d_topk_w) and sampled weight-gradient
+elements, including the largest and smallest experts; experts that received no
+token must have exactly zero weight gradients."""
+import numpy as np
+import pytest
+import torch
+
+from dropless_mixture_experts_top_gb300 import moe, synth
+from oracle import oracle as O
+from tests import gpu_util as G
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+BF16_WORKLOADS = ["qwen3_30b_a3b_layer_t16384", "qwen3_30b_a3b_layer_t16384_zipf",
+                  "qwen3_235b_a22b_layer_t16384"]
+
+
+def sample_tokens(T, counts, idx, rng, n=40):
+    toks = {0, T - 1}
+    toks |= set(int(t) for t in rng.integers(0, T, n))
+    nz = np.flatnonzero(counts)
+    for e in (nz[np.argmax(counts[nz])], nz[np.argmin(counts[nz])]):
+        on = np.flatnonzero((idx == e).any(1))
+        toks |= set(int(t) for t in on[:: max(1, len(on) // 3)][:3])
+    return np.array(sorted(toks), dtype=np.int64)
+
+
+def sample_dw(shape, counts, rng, n=24):
+    nz = np.flatnonzero(counts)
+    experts = [int(nz[np.argmax(counts[nz])]), int(nz[np.argmin(counts[nz])]), int(nz[0]), int(nz[-1])]
+    which, ee, rr, cc = [], [], [], []
+    for wh in range(3):
+        R, C = (shape.I, shape.H) if wh == 2 else (shape.H, shape.I)
+        for q in range(n):
+            e = experts[q % len(experts)] if q < 8 else int(rng.choice(nz))
+            r = [0, R - 1][q % 2] if q < 4 else int(rng.integers(R))
+            c = [C - 1, 0][q % 2] if q < 4 else int(rng.integers(C))
+            which.append(wh), ee.append(e), rr.append(r), cc.append(c)
+    return [np.array(a, np.int32) for a in (which, ee, rr, cc)]
+
+
+def run_workload(name):
+    w = synth.WORKLOADS[name]
+    shape = w.shape
+    inp = synth.make_inputs(w)
+    layer, out, grads = G.run_layer(shape, inp, precision=w.precision)
+    assert layer.status() == {"route": 0, "forward": 0, "backward": 0}
+    return w, shape, inp, layer, out, grads
+
+
+@pytest.mark.parametrize("name", BF16_WORKLOADS)
+def test_fullsize_sampled_parity(name):
+    w, shape, inp, layer, out, grads = run_workload(name)
+    idx, wts, counts, offsets, ros, sor = G.check_routing(shape, inp, layer)
+    assert counts.sum() == shape.T * shape.k
+    if w.routing == "zipf":
+        assert (counts == 0).sum() >= 1 and counts.max() > 8 * counts[counts > 0].min()
+    rng = np.random.default_rng(7)
+    toks = sample_tokens(shape.T, counts, idx, rng)
+    ref_out = O.forward(shape, inp["x"], idx, wts, inp["W_gate"], inp["W_up"], inp["W_down"], tokens=toks)
+    G.close("out[sampled tokens]", G.bf(out[torch.from_numpy(toks).cuda()]), ref_out)
+    dx, dl, gd = O.backward_tokens(shape, inp["x"], inp["logits"], idx, wts, inp["W_gate"], inp["W_up"],
+                                   inp["W_down"], inp["dy"], tokens=toks)
+    tk = torch.from_numpy(toks).cuda()
+    G.close("dx[sampled tokens]", G.bf(grads["dx"][tk]), dx)
+    G.close("d_logits[sampled tokens]", grads["d_logits"][tk].cpu().numpy(), dl)
+    G.close("d_topk_w[sampled tokens]", grads["d_topk_w"][tk].cpu().numpy(), gd)
+    which, ee, rr, cc = sample_dw(shape, counts, rng)
+    ref = O.dw_elements(shape, inp["x"], idx, wts, inp["W_gate"], inp["W_up"], inp["W_down"], inp["dy"],
+                        which, ee, rr, cc)
+    names = ["dW_gate", "dW_up", "dW_down"]
+    for wh in range(3):
+        m = which == wh
+        t = grads[names[wh]]
+        got = G.bf(t[torch.from_numpy(ee[m]).long().cuda(), torch.from_numpy(rr[m]).long().cuda(),
+                     torch.from_numpy(cc[m]).long().cuda()])
+        G.close(f"{names[wh]}[sampled]", got, ref[m])
+    for e in np.flatnonzero(counts == 0):
+        for n in names:
+            assert int(grads[n][int(e)].abs().sum()) == 0, (n, e)
+    # every output is finite at full size
+    for n in ("dx",) + tuple(names):
+        assert torch.isfinite(grads[n].view(torch.bfloat16).float()).all(), n
+    assert torch.isfinite(out.view(torch.bfloat16).float()).all()
