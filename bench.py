@@ -203,7 +203,7 @@ def run_reference(args):
         return 0
     from oracle import oracle as O
     O.build()
-    w = synth.WORKLOADS[args.workload]
+    w = workload_of(args)
     inp = synth.make_inputs(w)
     budget = 150.0 / max(1, args.steps + args.warmup)
     S, _ = size_oracle_sample(O, w, inp, budget)
@@ -229,6 +229,16 @@ def run_reference(args):
 
 # ----------------------------------------------------------------------------- GPU arm
 
+def workload_of(args):
+    """The named workload; --tokens shrinks T (small profiling cases only, never the bench line)."""
+    import dataclasses
+    w = synth.WORKLOADS[args.workload]
+    if args.tokens:
+        shape = dataclasses.replace(w.shape, T=args.tokens)
+        w = dataclasses.replace(w, name=f"{w.name}_T{args.tokens}", shape=shape)
+    return w
+
+
 def ensure_built(rank):
     from dropless_mixture_experts_top_gb300 import _build
     if rank == 0:
@@ -253,7 +263,7 @@ def run_ours(args):
     ensure_built(rank)
     from dropless_mixture_experts_top_gb300 import moe
 
-    w = synth.WORKLOADS[args.workload]
+    w = workload_of(args)
     shape = w.shape
     inp = synth.make_inputs(w)
     dev = torch.device("cuda", local)
@@ -409,6 +419,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0, help="override T (small profiling cases)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -132,10 +132,17 @@ moe_status timed(const char *label, cudaStream_t s, F &&launch) {
   }
   if (slot >= 0) {
     g_labels[slot] = label;
-    cudaEventRecord(static_cast<cudaEvent_t>(ev[2 * slot]), s);
+    if (cudaEventRecord(static_cast<cudaEvent_t>(ev[2 * slot]), s) != cudaSuccess) {
+      cudaGetLastError();  // the failed record, not a launch error
+      return MOE_ERR_CUDA;
+    }
   }
   cudaError_t e = launch();
-  if (slot >= 0) cudaEventRecord(static_cast<cudaEvent_t>(ev[2 * slot + 1]), s);
+  if (slot >= 0 && e == cudaSuccess &&
+      cudaEventRecord(static_cast<cudaEvent_t>(ev[2 * slot + 1]), s) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -157,12 +157,17 @@ def get_device_status(scratch, stream=None) -> int:
 
 
 def timing_attach(events):
-    """events: list of torch.cuda.Event (enable_timing=True), two per kernel."""
+    """events: list of torch.cuda.Event (enable_timing=True), two per kernel.
+    torch creates the CUDA event object lazily, so each one is recorded once here
+    to make its handle valid."""
     global _timing_keep
     if events is None:
         _check(lib().moe_timing_attach(None, 0), "moe_timing_attach")
         _timing_keep = None
         return
+    for e in events:
+        e.record()
+    torch.cuda.synchronize()
     arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
     _timing_keep = arr
     _check(lib().moe_timing_attach(arr, len(events) // 2), "moe_timing_attach")

@@ -5,6 +5,9 @@ Tolerances (floating point): relative L2 <= 5e-3 and max |diff| <= 2e-2 *
 max |ref| for bf16 outputs and gradients; router weights within 1e-6; integer
 routing and permutation bit-exact.
 """
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -38,6 +41,12 @@ def close(name, got, ref, rel_l2=REL_L2, max_rel=MAX_REL):
     rel = err / nref if nref > 0 else err
     mx = np.abs(got - ref).max() if got.size else 0.0
     amax = np.abs(ref).max() if ref.size else 0.0
+    log = os.environ.get("MOE_PARITY_LOG")
+    if log:
+        with open(log, "a") as f:
+            f.write(json.dumps({"test": os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0],
+                                "tensor": name, "n": int(got.size), "rel_l2": float(rel),
+                                "max_abs_over_max_ref": float(mx / amax) if amax else 0.0}) + "\n")
     assert rel <= rel_l2, f"{name}: rel L2 {rel:.3e} > {rel_l2}"
     assert mx <= max_rel * amax + 1e-30, f"{name}: max|diff| {mx:.3e} > {max_rel} * {amax:.3e}"
     return rel

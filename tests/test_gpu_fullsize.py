@@ -20,7 +20,7 @@ BF16_WORKLOADS = ["qwen3_30b_a3b_layer_t16384", "qwen3_30b_a3b_layer_t16384_zipf
                   "qwen3_235b_a22b_layer_t16384"]
 
 
-def sample_tokens(T, counts, idx, rng, n=40):
+def sample_tokens(T, counts, idx, rng, n=64):
     toks = {0, T - 1}
     toks |= set(int(t) for t in rng.integers(0, T, n))
     nz = np.flatnonzero(counts)
@@ -30,7 +30,7 @@ def sample_tokens(T, counts, idx, rng, n=40):
     return np.array(sorted(toks), dtype=np.int64)
 
 
-def sample_dw(shape, counts, rng, n=24):
+def sample_dw(shape, counts, rng, n=128):
     nz = np.flatnonzero(counts)
     experts = [int(nz[np.argmax(counts[nz])]), int(nz[np.argmin(counts[nz])]), int(nz[0]), int(nz[-1])]
     which, ee, rr, cc = [], [], [], []
