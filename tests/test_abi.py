@@ -58,39 +58,49 @@ def test_bad_shapes_rejected(L, bad):
     assert L.moe_query_workspace(ctypes.byref(c), ctypes.byref(sz), None, None, None) == -1
 
 
-def test_route_validation_before_launch(L):
-    c = cfg()
-    rs = moe.query_workspace(c)[0]
-    good = [0x1000 * (i + 1) for i in range(7)]
-    r = moe.Routing(*good)
-    P = ctypes.c_void_p
-    # null routing member
-    r0 = moe.Routing(*([0] + good[1:]))
-    assert L.moe_route(ctypes.byref(c), P(0x10000), ctypes.byref(r0), P(0x20000), rs, None) == -1
-    # misaligned logits
-    assert L.moe_route(ctypes.byref(c), P(0x10004), ctypes.byref(r), P(0x20000), rs, None) == -2
-    # scratch too small
-    assert L.moe_route(ctypes.byref(c), P(0x10000), ctypes.byref(r), P(0x20000), rs - 1, None) == -3
+# The validation checks below pass made-up device addresses on purpose.  They run
+# in a child process that sees no GPU (CUDA_VISIBLE_DEVICES=""), so even a
+# validation bug could never hand those addresses to a kernel.
+_VALIDATION_SCRIPT = r"""
+import ctypes, sys
+sys.path.insert(0, sys.argv[1])
+from dropless_mixture_experts_top_gb300 import moe
+L = moe.lib()
+P = ctypes.c_void_p
+res = {}
+c = moe.Config(512, 128, 64, 8, 2, 0)
+rs, sv, fs, bs = moe.query_workspace(c)
+good = [0x1000 * (i + 1) for i in range(7)]
+r = moe.Routing(*good)
+r0 = moe.Routing(*([0] + good[1:]))
+res["route_null_member"] = L.moe_route(ctypes.byref(c), P(0x10000), ctypes.byref(r0), P(0x20000), rs, None)
+res["route_misaligned"] = L.moe_route(ctypes.byref(c), P(0x10004), ctypes.byref(r), P(0x20000), rs, None)
+res["route_small_scratch"] = L.moe_route(ctypes.byref(c), P(0x10000), ctypes.byref(r), P(0x20000), rs - 1, None)
+a = [P(0x100000 * (i + 1)) for i in range(12)]
+res["fwd_small_saved"] = L.moe_forward(ctypes.byref(c), a[0], ctypes.byref(r), a[1], a[2], a[3], a[4], a[5],
+                                       sv - 16, a[6], fs, None)
+res["fwd_misaligned"] = L.moe_forward(ctypes.byref(c), P(0x100008), ctypes.byref(r), a[1], a[2], a[3], a[4],
+                                      a[5], sv, a[6], fs, None)
+res["bwd_null_dlogits"] = L.moe_backward(ctypes.byref(c), a[0], a[1], ctypes.byref(r), a[2], a[3], a[4], a[5],
+                                         sv, a[6], a[7], a[8], a[9], None, None, a[10], bs, None)
+res["bwd_small_scratch"] = L.moe_backward(ctypes.byref(c), a[0], a[1], ctypes.byref(r), a[2], a[3], a[4], a[5],
+                                          sv, a[6], a[7], a[8], a[9], a[11], None, a[10], bs - 256, None)
+print(repr(res))
+"""
+
+EXPECTED = {"route_null_member": -1, "route_misaligned": -2, "route_small_scratch": -3,
+            "fwd_small_saved": -3, "fwd_misaligned": -2, "bwd_null_dlogits": -1, "bwd_small_scratch": -3}
 
 
-def test_forward_backward_validation_before_launch(L):
-    c = cfg()
-    rs, sv, fs, bs = moe.query_workspace(c)
-    r = moe.Routing(*[0x1000 * (i + 1) for i in range(7)])
-    P = ctypes.c_void_p
-    a = [P(0x100000 * (i + 1)) for i in range(12)]
-    rc = L.moe_forward(ctypes.byref(c), a[0], ctypes.byref(r), a[1], a[2], a[3], a[4], a[5], sv - 16,
-                       a[6], fs, None)
-    assert rc == -3
-    rc = L.moe_forward(ctypes.byref(c), P(0x100008), ctypes.byref(r), a[1], a[2], a[3], a[4], a[5], sv,
-                       a[6], fs, None)
-    assert rc == -2
-    rc = L.moe_backward(ctypes.byref(c), a[0], a[1], ctypes.byref(r), a[2], a[3], a[4], a[5], sv, a[6],
-                        a[7], a[8], a[9], None, None, a[10], bs, None)
-    assert rc == -1  # d_logits is required
-    rc = L.moe_backward(ctypes.byref(c), a[0], a[1], ctypes.byref(r), a[2], a[3], a[4], a[5], sv, a[6],
-                        a[7], a[8], a[9], a[11], None, a[10], bs - 256, None)
-    assert rc == -3
+def test_validation_rejects_before_launch(L):
+    import ast
+    import subprocess
+    import sys
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    out = subprocess.run([sys.executable, "-c", _VALIDATION_SCRIPT, ROOT], env=env, capture_output=True,
+                         text=True, timeout=120)
+    assert out.returncode == 0, out.stderr
+    assert ast.literal_eval(out.stdout.strip().splitlines()[-1]) == EXPECTED
 
 
 def test_status_strings(L):
