@@ -136,6 +136,29 @@ moe_status moe_backward(const moe_config *cfg, const void *dy, const void *x,
                         void *dW_gate, void *dW_up, void *dW_down, float *d_logits,
                         float *d_topk_w, void *scratch, size_t scratch_bytes, void *stream);
 
+/* Routing without a caller-provided scratch buffer.  The paper has no
+ * counterpart: it exists for callers that cannot allocate device memory --
+ * code running while a CUDA graph is captured (cudaMalloc is not allowed
+ * there), code inside a framework whose allocator already owns the device
+ * memory, or a serving loop that must not allocate on its hot path.
+ * Same arguments, results and errors as moe_route, except that the scratch is a
+ * fixed 2.5 MiB + 4 KiB array inside this library's device memory (every GPU
+ * that loads the library keeps it until the process exits).  It fits every
+ * configuration with T <= 32768, and any other whose moe_query_workspace
+ * route_scratch is at most that size; for the rest it returns MOE_ERR_WORKSPACE
+ * and launches nothing.  Allocates nothing (no cudaMalloc/cudaFree, no
+ * allocating library call).
+ * device_status: optional device int32 that receives the call's MOE_DEV_* flags
+ * (copied on `stream` after the routing kernels); NULL to skip.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the one array and it keeps the last call's
+ * contents: calls that overlap on the GPU (for example on two streams) race,
+ * so serialise them. */
+moe_status moe_route_static_scratch(const moe_config *cfg, const float *logits,
+                                    const moe_routing *routing, int32_t *device_status,
+                                    void *stream);
+
 /* Waits for `stream`, then reads the status word at the start of `scratch` (a
  * scratch buffer previously passed to moe_route, moe_forward or moe_backward).
  * *host_code receives the MOE_DEV_* flags; returns MOE_OK when they are zero,
