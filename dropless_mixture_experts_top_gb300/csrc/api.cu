@@ -37,11 +37,11 @@ struct Layout {
   // route scratch
   size_t r_lrank, r_hist, r_base, r_total;
   // saved
-  size_t s_xperm, s_G, s_U, s_A, s_Y, s_total;
+  size_t s_xperm, s_G, s_U, s_A, s_Y, s_Aw, s_total;
   // forward scratch
   size_t f_total;
   // backward scratch
-  size_t b_dyw, b_dG, b_dU, b_dX, b_total;
+  size_t b_dyp, b_dG, b_dU, b_dX, b_total;
 };
 
 bool shape_ok(const moe_config *c) {
@@ -76,10 +76,12 @@ Layout layout_of(const moe_config *c) {
   o += align256(M * I * 2);
   L.s_Y = o;
   o += align256(M * H * 2);
+  L.s_Aw = o;
+  o += align256(M * I * 2);
   L.s_total = o > 0 ? o : 256;
   L.f_total = kHeader;
   o = kHeader;
-  L.b_dyw = o;
+  L.b_dyp = o;
   o += align256(M * H * 2);
   L.b_dG = o;
   o += align256(M * I * 2);
@@ -201,6 +203,7 @@ moe_status moe_saved_offsets(const moe_config *cfg, moe_saved_layout *out) {
   out->U = L.s_U;
   out->A = L.s_A;
   out->Y = L.s_Y;
+  out->A_w = L.s_Aw;
   return MOE_OK;
 }
 
@@ -272,6 +275,7 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const moe_routing *
   uint16_t *U = reinterpret_cast<uint16_t *>(sv + L.s_U);
   uint16_t *A = reinterpret_cast<uint16_t *>(sv + L.s_A);
   uint16_t *Y = reinterpret_cast<uint16_t *>(sv + L.s_Y);
+  uint16_t *A_w = reinterpret_cast<uint16_t *>(sv + L.s_Aw);
 
   MOE_TRY(timed("permute_rows", s, [&] {
     return launch_permute_rows(static_cast<const uint16_t *>(x), r->row_of_slot, x_perm, T, H, k,
@@ -282,13 +286,15 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const moe_routing *
   g.W_gate = static_cast<const uint16_t *>(W_gate);
   g.W_up = static_cast<const uint16_t *>(W_up);
   g.W_down = static_cast<const uint16_t *>(W_down);
+  g.w_row = r->w_row;
   g.o0 = A;
   g.o1 = G;
   g.o2 = U;
+  g.o3 = A_w;
   MOE_TRY(timed(gemm_mode_name(kFwdGateUp), s, [&] { return launch_grouped_gemm(kFwdGateUp, g, s); }));
   g.act = A;
   g.o0 = Y;
-  g.o1 = g.o2 = nullptr;
+  g.o1 = g.o2 = g.o3 = nullptr;
   MOE_TRY(timed(gemm_mode_name(kFwdDown), s, [&] { return launch_grouped_gemm(kFwdDown, g, s); }));
   MOE_TRY(timed("combine", s, [&] {
     return launch_gather_sum(Y, r->row_of_slot, r->topk_w, static_cast<uint16_t *>(out), T, H, k,
@@ -335,14 +341,15 @@ moe_status moe_backward(const moe_config *cfg, const void *dy, const void *x,
   const uint16_t *U = reinterpret_cast<const uint16_t *>(sv + L.s_U);
   const uint16_t *A = reinterpret_cast<const uint16_t *>(sv + L.s_A);
   const uint16_t *Y = reinterpret_cast<const uint16_t *>(sv + L.s_Y);
-  uint16_t *dyw = reinterpret_cast<uint16_t *>(sc + L.b_dyw);
+  const uint16_t *A_w = reinterpret_cast<const uint16_t *>(sv + L.s_Aw);
+  uint16_t *dy_perm = reinterpret_cast<uint16_t *>(sc + L.b_dyp);
   uint16_t *dG = reinterpret_cast<uint16_t *>(sc + L.b_dG);
   uint16_t *dU = reinterpret_cast<uint16_t *>(sc + L.b_dU);
   uint16_t *dX = reinterpret_cast<uint16_t *>(sc + L.b_dX);
 
   MOE_TRY(timed("router_bwd", s, [&] {
     return launch_router_bwd(static_cast<const uint16_t *>(dy), Y, r->row_of_slot, r->topk_idx,
-                             r->topk_w, dyw, d_logits, d_topk_w, T, H, E, k, s);
+                             r->topk_w, dy_perm, d_logits, d_topk_w, T, H, E, k, s);
   }));
   GemmArgs g = gemm_base(cfg, r, di.sms, status);
   g.x_perm = x_perm;
@@ -352,7 +359,9 @@ moe_status moe_backward(const moe_config *cfg, const void *dy, const void *x,
   g.act = A;
   g.G = G;
   g.U = U;
-  g.dyw = dyw;
+  g.dy_perm = dy_perm;
+  g.act_w = A_w;
+  g.w_row = r->w_row;
   g.dG = dG;
   g.dU = dU;
   g.o0 = dG;

@@ -11,7 +11,8 @@
 //   permute_rows : x_perm[row(t,j)] = x[t]                      (dispatch)
 //   gather_sum   : out[t] = sum_j w_tj * Y[row(t,j)]           (combine)
 //                  dx[t]  = sum_j dX_perm[row(t,j)]            (un-permute)
-//   router_bwd   : dyw[row(t,j)] = w_tj * dy[t]                (dy dispatch)
+//   router_bwd   : dy_perm[row(t,j)] = dy[t]                   (dy dispatch; the
+//                  router weight is applied later in fp32, so dy is never rounded)
 //                  g_tj = <dy[t], Y[row(t,j)]>                 (d w_tj)
 //                  d_logits[t, S_tj] = w_tj (g_tj - sum_i w_ti g_ti), 0 elsewhere
 #include "common.cuh"
@@ -43,15 +44,6 @@ __device__ __forceinline__ float dot8(const uint4 &a, const uint4 &b) {
   s = fmaf(bf16_lo(a.w), bf16_lo(b.w), s);
   s = fmaf(bf16_hi(a.w), bf16_hi(b.w), s);
   return s;
-}
-
-__device__ __forceinline__ uint4 scale8(const uint4 &q, float w) {
-  uint4 r;
-  r.x = pack_bf16x2(w * bf16_lo(q.x), w * bf16_hi(q.x));
-  r.y = pack_bf16x2(w * bf16_lo(q.y), w * bf16_hi(q.y));
-  r.z = pack_bf16x2(w * bf16_lo(q.z), w * bf16_hi(q.z));
-  r.w = pack_bf16x2(w * bf16_lo(q.w), w * bf16_hi(q.w));
-  return r;
 }
 
 __global__ void __launch_bounds__(kWarps * 32) permute_rows_kernel(const uint4 *__restrict__ x,
@@ -131,7 +123,7 @@ __global__ void __launch_bounds__(kWarps * 32) gather_sum_kernel(const uint4 *__
 
 __global__ void __launch_bounds__(kWarps * 32) router_bwd_kernel(
     const uint4 *__restrict__ dy, const uint4 *__restrict__ Y, const int32_t *__restrict__ ros,
-    const int32_t *__restrict__ topk_idx, const float *__restrict__ topk_w, uint4 *__restrict__ dyw,
+    const int32_t *__restrict__ topk_idx, const float *__restrict__ topk_w, uint4 *__restrict__ dyp,
     float *__restrict__ d_logits, float *__restrict__ d_topk_w, int T, int nv, int E, int k) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
@@ -154,9 +146,8 @@ __global__ void __launch_bounds__(kWarps * 32) router_bwd_kernel(
     for (int j = 0; j < kMaxTopK; ++j) {
       if (j < k) {
         const int row = __shfl_sync(0xffffffffu, myrow, j);
-        const float wj = __shfl_sync(0xffffffffu, myw, j);
         const uint4 *src = Y + static_cast<size_t>(row) * nv;
-        uint4 *dst = dyw + static_cast<size_t>(row) * nv;
+        uint4 *dst = dyp + static_cast<size_t>(row) * nv;
         uint4 q[kVecPerLane];
 #pragma unroll
         for (int u = 0; u < kVecPerLane; ++u) {
@@ -168,7 +159,7 @@ __global__ void __launch_bounds__(kWarps * 32) router_bwd_kernel(
           const int v = v0 + u * 32 + lane;
           if (v < nv) {
             dot[j] += dot8(d[u], q[u]);
-            dst[v] = scale8(d[u], wj);
+            dst[v] = d[u];
           }
         }
       }
@@ -227,12 +218,12 @@ cudaError_t launch_gather_sum(const uint16_t *rows, const int32_t *row_of_slot, 
 }
 
 cudaError_t launch_router_bwd(const uint16_t *dy, const uint16_t *Y, const int32_t *row_of_slot,
-                              const int32_t *topk_idx, const float *topk_w, uint16_t *dyw,
+                              const int32_t *topk_idx, const float *topk_w, uint16_t *dy_perm,
                               float *d_logits, float *d_topk_w, int T, int H, int E, int k,
                               cudaStream_t s) {
   router_bwd_kernel<<<blocks_for(T), kWarps * 32, 0, s>>>(
       reinterpret_cast<const uint4 *>(dy), reinterpret_cast<const uint4 *>(Y), row_of_slot,
-      topk_idx, topk_w, reinterpret_cast<uint4 *>(dyw), d_logits, d_topk_w, T, H / 8, E, k);
+      topk_idx, topk_w, reinterpret_cast<uint4 *>(dy_perm), d_logits, d_topk_w, T, H / 8, E, k);
   return cudaGetLastError();
 }
 

@@ -45,7 +45,8 @@ struct Params {
   int M_rows, H, I, E;
   const int32_t *offsets;
   const uint16_t *G, *U;  // dSwiGLU epilogue inputs
-  uint16_t *o0, *o1, *o2;
+  const float *w_row;     // router weight of each permuted row
+  uint16_t *o0, *o1, *o2, *o3;
   int32_t *status;
   int kdim;     // ragged M: the fixed reduction length
   int n_tiles;  // ragged M and K: column tiles per row tile
@@ -209,6 +210,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, uint32_t tb, int ri
   if constexpr (MODE == kFwdGateUp) {
     const int row = t.m0 + rit;
     const bool rv = row < t.row_end;
+    const float w = rv ? __ldg(p.w_row + row) : 0.f;
     for (int c = 0; c < 4; ++c) {
       const int col = t.n0 + 32 * c;
       if (col >= p.I) break;
@@ -227,6 +229,9 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, uint32_t tb, int ri
         store32_bf16(p.o0 + off, v0);
         store32_bf16(p.o1 + off, v1);
         store32_bf16(p.o2 + off, v2);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v0[i] *= w;  // A_w = w * A, the dW_down operand
+        store32_bf16(p.o3 + off, v0);
       }
     }
   } else if constexpr (MODE == kFwdDown || MODE == kBwdDX) {
@@ -246,6 +251,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, uint32_t tb, int ri
   } else if constexpr (MODE == kBwdDA) {
     const int row = t.m0 + rit;
     const bool rv = row < t.row_end;
+    const float w = rv ? __ldg(p.w_row + row) : 0.f;  // dA = w * (dy . W_down^T)
     for (int c = 0; c < 8; ++c) {
       const int col = t.n0 + 32 * c;
       if (col >= p.I) break;
@@ -257,7 +263,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, uint32_t tb, int ri
         load32_bf16(p.U + off, v2);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float da = __uint_as_float(r0[i]), g = v1[i], u = v2[i];
+          const float da = w * __uint_as_float(r0[i]), g = v1[i], u = v2[i];
           const float s = sigmoidf_(g);
           v0[i] = da * u * s * (1.f + g * (1.f - s));  // dG
           v1[i] = da * g * s;                          // dU = dA * silu(G)
@@ -539,6 +545,8 @@ cudaError_t launch_mode(const GemmArgs &a, cudaStream_t s) {
   p.o0 = a.o0;
   p.o1 = a.o1;
   p.o2 = a.o2;
+  p.o3 = a.o3;
+  p.w_row = a.w_row;
   p.status = a.status;
   const uint64_t M = static_cast<uint64_t>(a.M_rows), H = a.H, I = a.I, E = a.E;
   bool ok = true;
@@ -558,7 +566,7 @@ cudaError_t launch_mode(const GemmArgs &a, cudaStream_t s) {
       p.n_tiles = (a.H + 255) / 256;
       break;
     case kBwdDA:
-      ok = make_map(&mA0, a.dyw, H, M, 128) && make_map(&mB0, a.W_down, H, E * I, 256);
+      ok = make_map(&mA0, a.dy_perm, H, M, 128) && make_map(&mB0, a.W_down, H, E * I, 256);
       mA1 = mA0;
       mB1 = mB0;
       p.G = a.G;
@@ -573,7 +581,7 @@ cudaError_t launch_mode(const GemmArgs &a, cudaStream_t s) {
       p.n_tiles = (a.H + 255) / 256;
       break;
     case kBwdDWDown:
-      ok = make_map(&mA0, a.act, I, M, 64) && make_map(&mB0, a.dyw, H, M, 64);
+      ok = make_map(&mA0, a.act_w, I, M, 64) && make_map(&mB0, a.dy_perm, H, M, 64);
       mA1 = mA0;
       mB1 = mB0;
       p.m_tiles = (a.I + 127) / 128;

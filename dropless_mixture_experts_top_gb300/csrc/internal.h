@@ -46,19 +46,19 @@ cudaError_t launch_permute_rows(const uint16_t *x, const int32_t *row_of_slot, u
 // out[t] = sum_j w[t,j] * rows[row_of_slot[t,j]]   (w == nullptr: plain sum)
 cudaError_t launch_gather_sum(const uint16_t *rows, const int32_t *row_of_slot, const float *w,
                               uint16_t *out, int T, int H, int k, cudaStream_t s);
-// dyw[row] = w * dy[t]; g[t,j] = <dy[t], Y[row]>; d_logits; d_topk_w (nullable)
+// dy_perm[row(t,j)] = dy[t]; g[t,j] = <dy[t], Y[row]>; d_logits; d_topk_w (nullable)
 cudaError_t launch_router_bwd(const uint16_t *dy, const uint16_t *Y, const int32_t *row_of_slot,
-                              const int32_t *topk_idx, const float *topk_w, uint16_t *dyw,
+                              const int32_t *topk_idx, const float *topk_w, uint16_t *dy_perm,
                               float *d_logits, float *d_topk_w, int T, int H, int E, int k,
                               cudaStream_t s);
 
 // ---- grouped GEMMs (gemm.cu)
 enum GemmMode : int {
-  kFwdGateUp = 0,   // [x_perm] . [W_gate | W_up]  -> SwiGLU epilogue: A, G, U      (ragged M)
+  kFwdGateUp = 0,   // [x_perm] . [W_gate | W_up]  -> SwiGLU epilogue: A, G, U, A_w  (ragged M)
   kFwdDown = 1,     // A . W_down                 -> Y                              (ragged M)
-  kBwdDA = 2,       // dyw . W_down^T             -> dSwiGLU epilogue: dG, dU       (ragged M)
+  kBwdDA = 2,       // dy_perm . W_down^T, times w -> dSwiGLU epilogue: dG, dU      (ragged M)
   kBwdDX = 3,       // [dG | dU] . [W_gate | W_up]^T -> dX_perm                     (ragged M)
-  kBwdDWDown = 4,   // A^T . dyw                  -> dW_down                        (ragged K)
+  kBwdDWDown = 4,   // A_w^T . dy_perm            -> dW_down                        (ragged K)
   kBwdDWGateUp = 5  // x_perm^T . [dG | dU]       -> dW_gate, dW_up                 (ragged K)
 };
 
@@ -68,12 +68,14 @@ struct GemmArgs {
   const int32_t *offsets;  // [E+1] expert row offsets (device)
   // operands (device, bf16)
   const uint16_t *x_perm, *W_gate, *W_up, *W_down;
-  const uint16_t *act;  // A [M,I]
+  const uint16_t *act;    // A [M,I]
+  const uint16_t *act_w;  // A_w = w * A [M,I]
   const uint16_t *G, *U;
-  const uint16_t *dyw;
+  const uint16_t *dy_perm;  // dy rows in permuted order [M,H]
   const uint16_t *dG, *dU;
+  const float *w_row;       // [M] router weight per permuted row
   // outputs (device, bf16)
-  uint16_t *o0, *o1, *o2;
+  uint16_t *o0, *o1, *o2, *o3;
   int32_t *status;
   int num_sms;
 };

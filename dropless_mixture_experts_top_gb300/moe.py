@@ -42,7 +42,7 @@ class Routing(ctypes.Structure):
 
 
 class SavedLayout(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_size_t) for n in ("x_perm", "G", "U", "A", "Y")]
+    _fields_ = [(n, ctypes.c_size_t) for n in ("x_perm", "G", "U", "A", "Y", "A_w")]
 
 
 class MoEError(RuntimeError):

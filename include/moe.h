@@ -102,9 +102,10 @@ moe_status moe_query_workspace(const moe_config *cfg, size_t *route_scratch, siz
                                size_t *fwd_scratch, size_t *bwd_scratch);
 
 /* Offsets (bytes) of the saved activations inside `saved`, for inspection:
- * x_perm [M,H], G [M,I], U [M,I], A [M,I], Y [M,H], all bf16 (Y unweighted). */
+ * x_perm [M,H], G [M,I], U [M,I], A [M,I], Y [M,H] (unweighted), A_w [M,I]
+ * (A times the row's router weight: the weight-gradient operand), all bf16. */
 typedef struct {
-  size_t x_perm, G, U, A, Y;
+  size_t x_perm, G, U, A, Y, A_w;
 } moe_saved_layout;
 moe_status moe_saved_offsets(const moe_config *cfg, moe_saved_layout *layout);
 

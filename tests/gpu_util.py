@@ -90,6 +90,7 @@ def check_full(shape, inp, layer, out, grads, precision="bf16", check_saved=True
         close("U", bf(layer.saved_tensor("U")), u)
         close("A", bf(layer.saved_tensor("A")), a)
         close("Y", bf(layer.saved_tensor("Y")), y)
+        close("A_w", bf(layer.saved_tensor("A_w")), a * w.ravel()[sor][:, None])
     ref = O.forward(shape, inp["x"], idx, w, inp["W_gate"], inp["W_up"], inp["W_down"])
     close("out", bf(out), ref)
     dx, dl, gd = O.backward_tokens(shape, inp["x"], inp["logits"], idx, w, inp["W_gate"], inp["W_up"],
