@@ -182,22 +182,6 @@ __device__ __forceinline__ void store32_bf16(uint16_t *dst, const float (&v)[32]
   }
 }
 
-__device__ __forceinline__ void load32_bf16(const uint16_t *src, float (&v)[32]) {
-  const uint4 *s = reinterpret_cast<const uint4 *>(src);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint4 w = __ldg(s + q);
-    v[8 * q + 0] = bf16_lo(w.x);
-    v[8 * q + 1] = bf16_hi(w.x);
-    v[8 * q + 2] = bf16_lo(w.y);
-    v[8 * q + 3] = bf16_hi(w.y);
-    v[8 * q + 4] = bf16_lo(w.z);
-    v[8 * q + 5] = bf16_hi(w.z);
-    v[8 * q + 6] = bf16_lo(w.w);
-    v[8 * q + 7] = bf16_hi(w.w);
-  }
-}
-
 __device__ __forceinline__ float sigmoidf_(float z) { return 1.f / (1.f + __expf(-z)); }
 
 // Epilogue of one tile for one warp (32 rows).  tb: TMEM address of this
@@ -252,15 +236,42 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, uint32_t tb, int ri
     const int row = t.m0 + rit;
     const bool rv = row < t.row_end;
     const float w = rv ? __ldg(p.w_row + row) : 0.f;  // dA = w * (dy . W_down^T)
+    // G and U of the next 32-column chunk are loaded while this chunk is computed
+    uint4 gq[4], uq[4], gn[4], un[4];
+    const size_t rowoff = static_cast<size_t>(rv ? row : 0) * p.I;
+    if (rv && t.n0 < p.I) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        gq[q] = __ldg(reinterpret_cast<const uint4 *>(p.G + rowoff + t.n0) + q);
+        uq[q] = __ldg(reinterpret_cast<const uint4 *>(p.U + rowoff + t.n0) + q);
+      }
+    }
     for (int c = 0; c < 8; ++c) {
       const int col = t.n0 + 32 * c;
       if (col >= p.I) break;
+      const bool next = c + 1 < 8 && col + 32 < p.I;
+      if (rv && next) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          gn[q] = __ldg(reinterpret_cast<const uint4 *>(p.G + rowoff + col + 32) + q);
+          un[q] = __ldg(reinterpret_cast<const uint4 *>(p.U + rowoff + col + 32) + q);
+        }
+      }
       tmem_ld32(tb + 32 * c, r0);
       tmem_ld_wait();
       if (rv) {
-        const size_t off = static_cast<size_t>(row) * p.I + col;
-        load32_bf16(p.G + off, v1);
-        load32_bf16(p.U + off, v2);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t gw[4] = {gq[q].x, gq[q].y, gq[q].z, gq[q].w};
+          const uint32_t uw[4] = {uq[q].x, uq[q].y, uq[q].z, uq[q].w};
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            v1[8 * q + 2 * h] = bf16_lo(gw[h]);
+            v1[8 * q + 2 * h + 1] = bf16_hi(gw[h]);
+            v2[8 * q + 2 * h] = bf16_lo(uw[h]);
+            v2[8 * q + 2 * h + 1] = bf16_hi(uw[h]);
+          }
+        }
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const float da = w * __uint_as_float(r0[i]), g = v1[i], u = v2[i];
@@ -268,8 +279,13 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, uint32_t tb, int ri
           v0[i] = da * u * s * (1.f + g * (1.f - s));  // dG
           v1[i] = da * g * s;                          // dU = dA * silu(G)
         }
-        store32_bf16(p.o0 + off, v0);
-        store32_bf16(p.o1 + off, v1);
+        store32_bf16(p.o0 + rowoff + col, v0);
+        store32_bf16(p.o1 + rowoff + col, v1);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        gq[q] = gn[q];
+        uq[q] = un[q];
       }
     }
   } else if constexpr (MODE == kBwdDWDown) {

@@ -30,8 +30,65 @@ namespace {
 constexpr int TB = kRouteTokensPerBlock;
 constexpr int NW = kRouteThreads / 32;
 
+// Top-k of one token's logits held 8 per lane (lane l holds experts l + 32 i):
+// k rounds of a warp arg-max, larger logit first, lower expert index on ties.
+// Two tokens are processed together so that their shuffle chains overlap.
+template <int NT>
+__device__ __forceinline__ void warp_topk(const float (&v)[NT][8], int npl, int E, int k, int lane,
+                                          int (&sel_i)[NT][kMaxTopK], float (&sel_v)[NT][kMaxTopK]) {
+  uint32_t taken[NT];
+#pragma unroll
+  for (int q = 0; q < NT; ++q) taken[q] = 0;
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    if (j < k) {
+      float bv[NT];
+      int bi[NT];
+#pragma unroll
+      for (int q = 0; q < NT; ++q) {
+        bv[q] = -INFINITY;
+        bi[q] = INT_MAX;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int e = lane + 32 * i;
+          if (i < npl && e < E && !((taken[q] >> i) & 1u) &&
+              (v[q][i] > bv[q] || (v[q][i] == bv[q] && e < bi[q]))) {
+            bv[q] = v[q][i];
+            bi[q] = e;
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+        for (int q = 0; q < NT; ++q) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv[q], o);
+          const int oi = __shfl_xor_sync(0xffffffffu, bi[q], o);
+          if (ov > bv[q] || (ov == bv[q] && oi < bi[q])) {
+            bv[q] = ov;
+            bi[q] = oi;
+          }
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < NT; ++q) {
+        if ((bi[q] & 31) == lane) taken[q] |= 1u << (bi[q] >> 5);
+        sel_i[q][j] = bi[q];
+        sel_v[q][j] = bv[q];
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < NT; ++q) {
+        sel_i[q][j] = 0;
+        sel_v[q][j] = -INFINITY;
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(RouteArgs a, int nblk) {
-  __shared__ int32_t s_sel[TB][kMaxTopK];
+  __shared__ uint32_t s_mask[TB][kMaxExperts / 32];  // chosen experts of each token, as bits
+  __shared__ uint8_t s_pos[TB][kMaxExperts];         // position j of expert e in the token's list
   __shared__ int32_t s_part[kRouteThreads];
   __shared__ int32_t s_start[kRouteThreads];
   __shared__ int32_t s_cnt[kMaxExperts];
@@ -45,68 +102,54 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(RouteArgs a, 
   const int npl = (E + 31) >> 5;  // logits per lane (<= 8)
   bool bad = false;
 
-  for (int tl = warp; tl < ntok; tl += NW) {
-    const int t = t0 + tl;
-    const float *lt = a.logits + static_cast<size_t>(t) * E;
-    float v[8];
+  for (int tl0 = 2 * warp; tl0 < ntok; tl0 += 2 * NW) {
+    constexpr int NT = 2;
+    float v[NT][8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane + 32 * i;
-      float x = -INFINITY;
-      if (i < npl && e < E) {
-        x = __ldg(lt + e);
-        if (!isfinite(x)) {
-          bad = true;
-          if (isnan(x)) x = -INFINITY;  // keep the selection well defined
-        }
-      }
-      v[i] = x;
-    }
-    uint32_t taken = 0;
-    int sel_i[kMaxTopK];
-    float sel_v[kMaxTopK];
+    for (int q = 0; q < NT; ++q) {
+      const int tl = min(tl0 + q, ntok - 1);  // an odd tail repeats the last token
+      const float *lt = a.logits + static_cast<size_t>(t0 + tl) * E;
 #pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
-      sel_i[j] = 0;
-      sel_v[j] = -INFINITY;
-      if (j < k) {
-        float bv = -INFINITY;
-        int bi = INT_MAX;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int e = lane + 32 * i;
-          if (i < npl && e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
-            bv = v[i];
-            bi = e;
+      for (int i = 0; i < 8; ++i) {
+        const int e = lane + 32 * i;
+        float x = -INFINITY;
+        if (i < npl && e < E) {
+          x = __ldg(lt + e);
+          if (!isfinite(x)) {
+            bad = true;
+            if (isnan(x)) x = -INFINITY;  // keep the selection well defined
           }
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-          if (ov > bv || (ov == bv && oi < bi)) {
-            bv = ov;
-            bi = oi;
-          }
-        }
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        sel_i[j] = bi;
-        sel_v[j] = bv;
+        v[q][i] = x;
       }
     }
-    // renormalised weights: exp(l_j - l_max) / sum over the kept set
-    const float m = sel_v[0];
-    float ssum = 0.f;
+    int sel_i[NT][kMaxTopK];
+    float sel_v[NT][kMaxTopK];
+    warp_topk<NT>(v, npl, E, k, lane, sel_i, sel_v);
 #pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j)
-      if (j < k) ssum += expf(sel_v[j] - m);
+    for (int q = 0; q < NT; ++q) {
+      const int tl = tl0 + q;
+      if (tl >= ntok) break;
+      const size_t sb = static_cast<size_t>(t0 + tl) * k;
+      // renormalised weights: exp(l_j - l_max) / sum over the kept set
+      const float m = sel_v[q][0];
+      float ssum = 0.f;
 #pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
-      if (j < k && lane == j) {
-        a.topk_idx[static_cast<size_t>(t) * k + j] = sel_i[j];
-        a.topk_w[static_cast<size_t>(t) * k + j] = expf(sel_v[j] - m) / ssum;
-        s_sel[tl][j] = sel_i[j];
+      for (int j = 0; j < kMaxTopK; ++j)
+        if (j < k) ssum += expf(sel_v[q][j] - m);
+      uint32_t word = 0;
+#pragma unroll
+      for (int j = 0; j < kMaxTopK; ++j) {
+        if (j < k) {
+          if (lane == j) {
+            a.topk_idx[sb + j] = sel_i[q][j];
+            a.topk_w[sb + j] = expf(sel_v[q][j] - m) / ssum;
+            s_pos[tl][sel_i[q][j]] = static_cast<uint8_t>(j);
+          }
+          if ((sel_i[q][j] >> 5) == lane) word |= 1u << (sel_i[q][j] & 31);
+        }
       }
+      if (lane < npl) s_mask[tl][lane] = word;
     }
   }
   if (bad) flag_status(a.status, kDevNonfiniteLogit);
@@ -114,15 +157,12 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(RouteArgs a, 
 
   // per-(block, expert) histogram and ranks, in token order
   if (threadIdx.x < E) {
-    const int e = threadIdx.x;
+    const int e = threadIdx.x, w = e >> 5, b = e & 31;
     int cnt = 0;
+#pragma unroll 8
     for (int tl = 0; tl < ntok; ++tl) {
-      for (int j = 0; j < k; ++j) {
-        if (s_sel[tl][j] == e) {
-          a.lrank[static_cast<size_t>(t0 + tl) * k + j] = cnt++;
-          break;
-        }
-      }
+      if ((s_mask[tl][w] >> b) & 1u)
+        a.lrank[static_cast<size_t>(t0 + tl) * k + s_pos[tl][e]] = cnt++;
     }
     a.hist[static_cast<size_t>(blockIdx.x) * E + e] = cnt;
   }
@@ -141,6 +181,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(RouteArgs a, 
   const int b0 = p * chunk, b1 = min(nblk, b0 + chunk);
   if (p < P) {
     int s = 0;
+#pragma unroll 8
     for (int b = b0; b < b1; ++b) s += __ldcg(a.hist + static_cast<size_t>(b) * E + e);
     s_part[p * E + e] = s;
   }
@@ -175,6 +216,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(RouteArgs a, 
   if (threadIdx.x <= E) a.offsets[threadIdx.x] = s_off[threadIdx.x];
   if (p < P) {
     int run = s_off[e] + s_start[p * E + e];
+#pragma unroll 8
     for (int b = b0; b < b1; ++b) {
       a.block_base[static_cast<size_t>(b) * E + e] = run;
       run += __ldcg(a.hist + static_cast<size_t>(b) * E + e);
