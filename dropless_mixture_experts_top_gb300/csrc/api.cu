@@ -41,7 +41,7 @@ struct Layout {
   // forward scratch
   size_t f_total;
   // backward scratch
-  size_t b_dyp, b_dG, b_dU, b_dX, b_total;
+  size_t b_dyp, b_dG, b_dU, b_dX, b_maps, b_total;
 };
 
 bool shape_ok(const moe_config *c) {
@@ -89,6 +89,8 @@ Layout layout_of(const moe_config *c) {
   o += align256(M * I * 2);
   L.b_dX = o;
   o += align256(M * H * 2);
+  L.b_maps = o;
+  o += align256(E * kExpertMapBytes);
   L.b_total = o;
   return L;
 }
@@ -360,6 +362,7 @@ moe_status moe_backward(const moe_config *cfg, const void *dy, const void *x,
   g.G = G;
   g.U = U;
   g.dy_perm = dy_perm;
+  g.map_scratch = sc + L.b_maps;
   g.act_w = A_w;
   g.w_row = r->w_row;
   g.dG = dG;

@@ -1,24 +1,31 @@
 // gemm.cu -- persistent grouped GEMMs over ragged expert segments on the
-// 5th-generation tensor core (tcgen05, sm_103a).
+// 5th-generation tensor core (tcgen05, sm_103a), one CTA pair per tile.
 //
 // A grouped GEMM handles every expert's matrix product in one launch, each at
 // its real token count, computing only the valid regions; counts stay on the
 // device so nothing is copied to the host (NVIDIA MoE article,
 // "Optimizacion 1, el GEMM agrupado").  Two shapes of raggedness occur:
 //   ragged M  (forward GEMMs, dA, dX): rows = the expert's permuted rows;
-//             output tiles of 128 rows start at each expert's first row, rows
+//             output tiles of 256 rows start at each expert's first row, rows
 //             past the expert's end are computed but never stored.
 //   ragged K  (weight gradients): the reduction runs over the expert's rows;
-//             the last 64-row K block is cut at the expert's end by zeroing
-//             the rows past it in shared memory before the MMA; an expert with
-//             no rows gets an all-zero gradient.
+//             each expert gets its own tensor maps whose row extent ends at the
+//             expert's last row, so the last 64-row K block is zero-filled past
+//             it by the TMA unit itself; an expert with no rows gets an
+//             all-zero gradient.
 //
-// Kernel structure (one CTA per SM, persistent, static round-robin tiles):
-//   warp 0      TMA producer: 128B-swizzled boxes into a 4-stage ring
-//   warp 1      MMA issuer: tcgen05.mma kind::f16 (bf16 in, fp32 accumulate
-//               in TMEM), 128x256 tiles, K = 16 per instruction; owns TMEM
-//   warps 2..5  epilogue: tcgen05.ld from TMEM (two 256-column accumulators,
-//               double buffered), fused SwiGLU / dSwiGLU, bf16 stores
+// Kernel structure: clusters of two CTAs (a CTA pair on two SMs), persistent,
+// static round-robin over 256x256 output tiles.  Each CTA holds 128 rows of A
+// and 128 columns of B in a 6-stage shared-memory ring, so each SM reads half
+// the B operand it would need alone; the pair's MMAs (cta_group::2, M=256,
+// N=256, K=16, bf16 in, fp32 accumulate) are issued by the first CTA and write
+// each CTA's 128 accumulator rows into its own TMEM.
+//   warp 0      TMA producer (both CTAs): 128B-swizzled boxes into its ring;
+//               both CTAs' copies complete on CTA 0's barrier
+//   warp 1      CTA 0: MMA issuer (CTA 1's warp 1 only shares the TMEM allocation)
+//   warps 2..5  epilogue (both CTAs): tcgen05.ld of its 128 rows from two
+//               double-buffered 256-column accumulators, fused SwiGLU /
+//               dSwiGLU, bf16 stores
 // Every wait is bounded; on a timeout the kernel flags the status word,
 // drains its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -28,17 +35,18 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128;   // tile rows (TMEM lanes)
-constexpr int BN = 256;   // tile columns (TMEM columns per accumulator)
+constexpr int BM = 128;   // rows per CTA (TMEM lanes); a tile is 2*BM rows
+constexpr int BN = 256;   // tile columns (TMEM columns per accumulator); BN/2 per CTA
 constexpr int BK = 64;    // K per stage: one 128-byte swizzle row of bf16
-constexpr int STAGES = 4;
-constexpr int kABytes = BM * BK * 2;          // 16 KB
-constexpr int kBBytes = BN * BK * 2;          // 32 KB
+constexpr int STAGES = 6;
+constexpr int kABytes = BM * BK * 2;          // 16 KB: this CTA's rows of A
+constexpr int kBBytes = (BN / 2) * BK * 2;    // 16 KB: this CTA's columns of B
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kBox = 64 * 64 * 2;             // one 64x64 bf16 box (MN-major pieces)
+constexpr int kMapsPerExpert = 3;             // ragged K: A, B0, B1
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 2 * BN;
-constexpr int kSmemBytes = STAGES * kStageBytes + 1024 /*align*/ + 256 /*barriers*/ +
+constexpr int kSmemBytes = STAGES * kStageBytes + 1024 /*align*/ + 512 /*barriers*/ +
                            2 * (kMaxExperts + 1) * 4;
 
 struct Params {
@@ -48,8 +56,9 @@ struct Params {
   const float *w_row;     // router weight of each permuted row
   uint16_t *o0, *o1, *o2, *o3;
   int32_t *status;
+  const CUtensorMap *expert_maps;  // ragged K: [E][kMapsPerExpert] maps ending at each expert's end
   int kdim;     // ragged M: the fixed reduction length
-  int n_tiles;  // ragged M and K: column tiles per row tile
+  int n_tiles;  // column tiles per row tile
   int m_tiles;  // ragged K: row tiles per expert
 };
 
@@ -58,14 +67,16 @@ struct Traits {
   static constexpr bool kRaggedK = (MODE == kBwdDWDown || MODE == kBwdDWGateUp);
   static constexpr int kAMN = kRaggedK ? 1 : 0;  // A operand MN-major in smem
   static constexpr int kBMN = (MODE == kFwdGateUp || MODE == kFwdDown || kRaggedK) ? 1 : 0;
-  // column tile split in two halves from two sources (gate | up)
+  // column tile = [first source | second source], 128 columns each (gate | up):
+  // CTA 0 holds the first source's columns, CTA 1 the second's
   static constexpr bool kPair = (MODE == kFwdGateUp || MODE == kBwdDWGateUp);
-  static constexpr uint32_t kIdesc = idesc_bf16(BM, BN, kAMN, kBMN);
+
+  static constexpr uint32_t kIdesc = idesc_bf16(2 * BM, BN, kAMN, kBMN);
 };
 
 struct Tile {
   int e;        // expert
-  int m0;       // first output row (ragged M: permuted row; ragged K: dW row)
+  int m0;       // first output row of the pair (ragged M: permuted row; ragged K: dW row)
   int row_end;  // ragged M: end of the expert's rows
   int n0;       // first output column
   int nkb;      // K blocks
@@ -89,7 +100,7 @@ __device__ __forceinline__ Tile decode_tile(int tile, const Params &p, const int
         hi = mid - 1;
     }
     t.e = lo;
-    t.m0 = s_off[lo] + (mt_lin - s_tp[lo]) * BM;
+    t.m0 = s_off[lo] + (mt_lin - s_tp[lo]) * (2 * BM);
     t.row_end = s_off[lo + 1];
     t.n0 = nt * (Tr::kPair ? BN / 2 : BN);
     t.nkb = p.kdim / BK;
@@ -99,7 +110,7 @@ __device__ __forceinline__ Tile decode_tile(int tile, const Params &p, const int
     const int per = p.m_tiles * p.n_tiles;
     t.e = tile / per;
     const int rem = tile % per;
-    t.m0 = (rem / p.n_tiles) * BM;
+    t.m0 = (rem / p.n_tiles) * (2 * BM);
     t.n0 = (rem % p.n_tiles) * (Tr::kPair ? BN / 2 : BN);
     t.krow0 = s_off[t.e];
     t.kcount = s_off[t.e + 1] - s_off[t.e];
@@ -123,49 +134,60 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
   return ok != 0;
 }
 
-template <int MODE>
-__device__ __forceinline__ void produce_stage(const Tile &t, int kb, uint8_t *sa, uint8_t *sb,
-                                              uint64_t *bar, const Params &p,
+// One box into this CTA's stage, completing on CTA 0's barrier for the stage.
+struct StageLoad {
+  uint32_t bar_cl;  // CTA 0's full barrier for the stage (shared::cluster address)
+  __device__ __forceinline__ void operator()(void *dst, const CUtensorMap *m, int c0, int c1) const {
+    tma_load_2d_pair(dst, m, bar_cl, c0, c1);
+  }
+};
+
+// This CTA's share of one stage: 128 rows of A, 128 columns of B.
+template <int MODE, class Load>
+__device__ __forceinline__ void produce_stage(const Tile &t, int kb, int rank, uint8_t *sa,
+                                              uint8_t *sb, const Load &ld, const Params &p,
                                               const CUtensorMap *a0, const CUtensorMap *a1,
                                               const CUtensorMap *b0, const CUtensorMap *b1) {
+  const int arow = t.m0 + BM * rank;        // ragged M: this CTA's rows of A
+  const int bcol = t.n0 + (BN / 2) * rank;  // this CTA's columns of B (unpaired modes)
   if constexpr (MODE == kFwdGateUp) {
-    tma_load_2d(sa, a0, bar, kb * BK, t.m0);
+    ld(sa, a0, kb * BK, arow);
+    const CUtensorMap *w = rank == 0 ? b0 : b1;  // gate columns | up columns
     const int wrow = t.e * p.H + kb * BK;
-    tma_load_2d(sb + 0 * kBox, b0, bar, t.n0, wrow);
-    tma_load_2d(sb + 1 * kBox, b0, bar, t.n0 + 64, wrow);
-    tma_load_2d(sb + 2 * kBox, b1, bar, t.n0, wrow);
-    tma_load_2d(sb + 3 * kBox, b1, bar, t.n0 + 64, wrow);
+    ld(sb, w, t.n0, wrow);
+    ld(sb + kBox, w, t.n0 + 64, wrow);
   } else if constexpr (MODE == kFwdDown) {
-    tma_load_2d(sa, a0, bar, kb * BK, t.m0);
+    ld(sa, a0, kb * BK, arow);
     const int wrow = t.e * p.I + kb * BK;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) tma_load_2d(sb + c * kBox, b0, bar, t.n0 + 64 * c, wrow);
+    ld(sb, b0, bcol, wrow);
+    ld(sb + kBox, b0, bcol + 64, wrow);
   } else if constexpr (MODE == kBwdDA) {
-    tma_load_2d(sa, a0, bar, kb * BK, t.m0);
-    tma_load_2d(sb, b0, bar, kb * BK, t.e * p.I + t.n0);
+    ld(sa, a0, kb * BK, arow);
+    ld(sb, b0, kb * BK, t.e * p.I + bcol);
   } else if constexpr (MODE == kBwdDX) {
     const int kbi = p.I / BK;
     if (kb < kbi) {
-      tma_load_2d(sa, a0, bar, kb * BK, t.m0);
-      tma_load_2d(sb, b0, bar, kb * BK, t.e * p.H + t.n0);
+      ld(sa, a0, kb * BK, arow);
+      ld(sb, b0, kb * BK, t.e * p.H + bcol);
     } else {
-      tma_load_2d(sa, a1, bar, (kb - kbi) * BK, t.m0);
-      tma_load_2d(sb, b1, bar, (kb - kbi) * BK, t.e * p.H + t.n0);
+      ld(sa, a1, (kb - kbi) * BK, arow);
+      ld(sb, b1, (kb - kbi) * BK, t.e * p.H + bcol);
     }
   } else if constexpr (MODE == kBwdDWDown) {
+    const CUtensorMap *em = p.expert_maps + t.e * kMapsPerExpert;  // rows end at the expert's end
     const int r = t.krow0 + kb * BK;
-    tma_load_2d(sa + 0 * kBox, a0, bar, t.m0, r);
-    tma_load_2d(sa + 1 * kBox, a0, bar, t.m0 + 64, r);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) tma_load_2d(sb + c * kBox, b0, bar, t.n0 + 64 * c, r);
+    ld(sa, em + 0, t.m0 + BM * rank, r);
+    ld(sa + kBox, em + 0, t.m0 + BM * rank + 64, r);
+    ld(sb, em + 1, bcol, r);
+    ld(sb + kBox, em + 1, bcol + 64, r);
   } else {  // kBwdDWGateUp
+    const CUtensorMap *em = p.expert_maps + t.e * kMapsPerExpert;
     const int r = t.krow0 + kb * BK;
-    tma_load_2d(sa + 0 * kBox, a0, bar, t.m0, r);
-    tma_load_2d(sa + 1 * kBox, a0, bar, t.m0 + 64, r);
-    tma_load_2d(sb + 0 * kBox, b0, bar, t.n0, r);
-    tma_load_2d(sb + 1 * kBox, b0, bar, t.n0 + 64, r);
-    tma_load_2d(sb + 2 * kBox, b1, bar, t.n0, r);
-    tma_load_2d(sb + 3 * kBox, b1, bar, t.n0 + 64, r);
+    ld(sa, em + 0, t.m0 + BM * rank, r);
+    ld(sa + kBox, em + 0, t.m0 + BM * rank + 64, r);
+    const CUtensorMap *g = em + (rank == 0 ? 1 : 2);  // dG columns | dU columns
+    ld(sb, g, t.n0, r);
+    ld(sb + kBox, g, t.n0 + 64, r);
   }
 }
 
@@ -341,18 +363,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t *stages = smem;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * kStageBytes);
-  uint64_t *full = bars;                 // [STAGES] TMA -> MMA
-  uint64_t *empty = bars + STAGES;       // [STAGES] MMA -> TMA
-  uint64_t *tfull = bars + 2 * STAGES;   // [2] MMA -> epilogue
-  uint64_t *tempty = tfull + 2;          // [2] epilogue -> MMA
+  uint64_t *full = bars;                 // [STAGES] CTA 0 only: both CTAs' copies landed
+  uint64_t *empty = bars + STAGES;       // [STAGES] pair MMA done with the stage (both CTAs)
+  uint64_t *tfull = bars + 2 * STAGES;   // [2] accumulator ready (both CTAs)
+  uint64_t *tempty = tfull + 2;          // [2] CTA 0 only: both CTAs' epilogues done
   uint64_t *drain = tempty + 2;          // abort path: MMA completion
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  int *s_tp = reinterpret_cast<int *>(smem + STAGES * kStageBytes + 256);  // [E+1] tile prefix
+  int *s_tp = reinterpret_cast<int *>(smem + STAGES * kStageBytes + 512);  // [E+1] tile prefix
   int *s_off = s_tp + (kMaxExperts + 1);                                    // [E+1] row offsets
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
+  const int rank = static_cast<int>(cluster_ctarank());  // 0: issues the pair's MMAs
+  const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -361,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 128);
+      mbar_init(&tempty[b], 8);  // one arrival per epilogue warp of both CTAs
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -373,14 +397,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmB0);
     tma_prefetch_desc(&tmB1);
   }
-  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == 1) tmem_alloc_pair(tmem_slot, kTmemCols);
   for (int e = threadIdx.x; e <= E; e += kThreads) s_off[e] = __ldg(p.offsets + e);
   __syncthreads();
-  if (warp == 2) {  // tile prefix over experts: ceil(rows / BM)
+  if (warp == 2) {  // tile prefix over experts: ceil(rows / 256)
     int carry = 0;
     for (int base = 0; base < E; base += 32) {
       const int e = base + lane;
-      const int c = e < E ? (s_off[e + 1] - s_off[e] + BM - 1) / BM : 0;
+      const int c = e < E ? (s_off[e + 1] - s_off[e] + 2 * BM - 1) / (2 * BM) : 0;
       int incl = c;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -394,29 +418,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // both CTAs' barriers initialised before any remote arrival
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   const int total = Tr::kRaggedK ? E * p.m_tiles * p.n_tiles : s_tp[E] * p.n_tiles;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    const uint32_t full_cl0 = peer_smem_addr(&full[0], 0);  // CTA 0's full[] (direct mode)
     int stage = 0;
     uint32_t phase = 0;
-    uint32_t armed = 0;  // bit s: stage s armed at least once; parity of last arm in `arm_par`
-    uint32_t arm_par = 0;
+    uint32_t armed = 0, arm_par = 0;  // per stage: armed at least once, parity of last arm
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+    for (int tile = cluster; tile < total && ok; tile += nclusters) {
       const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off);
+      if constexpr (Tr::kRaggedK) {  // this expert's maps were written by the preceding launch
+        if (lane < kMapsPerExpert && t.nkb > 0) tmap_acquire(p.expert_maps + t.e * kMapsPerExpert + lane);
+        __syncwarp();
+      }
       for (int kb = 0; kb < t.nkb; ++kb) {
         if (!warp_wait(&empty[stage], phase ^ 1, abort_flag)) {
           ok = false;
           break;
         }
         if (lane == 0) {
-          mbar_arrive_expect_tx(&full[stage], kStageBytes);
           uint8_t *sa = stages + stage * kStageBytes;
-          produce_stage<MODE>(t, kb, sa, sa + kABytes, &full[stage], p, &tmA0, &tmA1, &tmB0, &tmB1);
+          if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);  // both CTAs' bytes
+          const StageLoad ld{full_cl0 + 8u * stage};
+          produce_stage<MODE>(t, kb, rank, sa, sa + kABytes, ld, p, &tmA0, &tmA1, &tmB0, &tmB1);
         }
         armed |= 1u << stage;
         arm_par = (arm_par & ~(1u << stage)) | (phase << stage);
@@ -427,28 +457,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (*abort_flag && lane == 0) {  // let our own copies land before the CTA exits
+    if (*abort_flag && lane == 0 && rank == 0) {  // let the pair's copies land before exit
       for (int s = 0; s < STAGES; ++s) {
         if (!((armed >> s) & 1u)) continue;
         for (int i = 0; i < (1 << 22) && !mbar_try_wait(&full[s], (arm_par >> s) & 1u); ++i) {
         }
       }
     }
+  } else if (warp == 1 && rank == 1) {
+    // CTA 1's warp 1 holds the pair's TMEM allocation with CTA 0's warp 1
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ MMA issuer (CTA 0)
     int stage = 0;
     uint32_t phase = 0;
     int it = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+    for (int tile = cluster; tile < total && ok; tile += nclusters, ++it) {
       const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off);
       const int buf = it & 1;
       const uint32_t use = (it >> 1) & 1;
       if (!warp_wait(&tempty[buf], use ^ 1, abort_flag)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + buf * BN;
-      if (t.nkb == 0) {
-        if (lane == 0) mbar_arrive(&tfull[buf]);
+      if (t.nkb == 0) {  // empty expert: both epilogues write zeros
+        if (lane == 0) {
+          mbar_arrive(&tfull[buf]);
+          mbar_arrive_cluster(peer_smem_addr(&tfull[buf], 1));
+        }
         __syncwarp();
         continue;
       }
@@ -460,21 +495,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         uint8_t *sa = stages + stage * kStageBytes;
         uint8_t *sb = sa + kABytes;
-        if constexpr (Tr::kRaggedK) {
-          const int valid = t.kcount - kb * BK;
-          if (valid < BK) {  // cut the K block at the expert's last row
-            const int nrows = BK - valid;
-            const int n16 = nrows * 8;  // 16-byte pieces per box
-            for (int q = lane; q < 6 * n16; q += 32) {
-              const int box = q / n16, rem = q % n16;
-              const int r = valid + rem / 8, c16 = rem % 8;
-              uint8_t *base = box < 2 ? sa + box * kBox : sb + (box - 2) * kBox;
-              *reinterpret_cast<uint4 *>(base + r * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async_smem();
-          }
-        }
-        __syncwarp();
         if (lane == 0) {
           const uint32_t a_base = smem_addr(sa), b_base = smem_addr(sb);
 #pragma unroll
@@ -483,9 +503,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             : smem_desc_sw128(a_base + k16 * 32, 16, 1024);
             const uint64_t bdesc = Tr::kBMN ? smem_desc_sw128(b_base + k16 * 2048, kBox, 1024)
                                             : smem_desc_sw128(b_base + k16 * 32, 16, 1024);
-            tc_mma_f16(d_tmem, adesc, bdesc, Tr::kIdesc, (kb | k16) != 0 ? 1u : 0u);
+            tc_mma_f16_pair(d_tmem, adesc, bdesc, Tr::kIdesc, (kb | k16) != 0 ? 1u : 0u);
           }
-          tc_commit(&empty[stage]);
+          tc_commit_pair(&empty[stage]);
         }
         __syncwarp();
         if (++stage == STAGES) {
@@ -494,20 +514,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      if (lane == 0) tc_commit(&tfull[buf]);
+      if (lane == 0) tc_commit_pair(&tfull[buf]);
       __syncwarp();
     }
-    if (*abort_flag && lane == 0) {  // wait for our own MMAs before TMEM is freed
-      tc_commit(drain);
+    if (*abort_flag && lane == 0) {  // wait for the pair's MMAs before TMEM is freed
+      tc_commit_pair(drain);
       for (int i = 0; i < (1 << 22) && !mbar_try_wait(drain, 0); ++i) {
       }
     }
   } else {
-    // ------------------------------------------------------------ epilogue
+    // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int rit = q * 32 + lane;
+    const int rit = BM * rank + q * 32 + lane;  // row within the pair's 256-row tile
+    const uint32_t tempty0 = peer_smem_addr(&tempty[0], 0);
+    const uint32_t tempty1 = peer_smem_addr(&tempty[1], 0);
     int it = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+    for (int tile = cluster; tile < total; tile += nclusters, ++it) {
       const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off);
       const int buf = it & 1;
       const uint32_t use = (it >> 1) & 1;
@@ -515,17 +537,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       epilogue_tile<MODE>(t, tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16), rit, p);
       tc_fence_before();
-      mbar_arrive(&tempty[buf]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(buf ? tempty1 : tempty0);
     }
   }
 
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x == 0 && *abort_flag) flag_status(p.status, kDevWaitTimeout);
+  cluster_sync();  // the pair is done with each other's barriers and TMEM
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc_pair(tmem_base, kTmemCols);
   }
+}
+
+// Ragged K: per-expert copies of the operand tensor maps whose row extent ends
+// at the expert's last row (offsets[e+1]); TMA then zero-fills the rows past it.
+struct MapTemplates {
+  CUtensorMap m[kMapsPerExpert];
+};
+
+__global__ void __launch_bounds__(256) expert_maps_kernel(const __grid_constant__ MapTemplates tm,
+                                                          const int32_t *__restrict__ offsets, int E,
+                                                          CUtensorMap *out) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= E) return;
+  const int end = __ldg(offsets + e + 1);
+  const uint32_t rows = end > 0 ? static_cast<uint32_t>(end) : 1u;  // an unused map still needs rows >= 1
+  for (int j = 0; j < kMapsPerExpert; ++j) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(&tm.m[j]);
+    CUtensorMap *dst = out + e * kMapsPerExpert + j;
+    uint4 *d = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) d[q] = src[q];
+    tmap_set_global_dim(dst, 1, rows);
+  }
+  tmap_release();
 }
 
 // ---------------------------------------------------------------- host side
@@ -582,7 +630,7 @@ cudaError_t launch_mode(const GemmArgs &a, cudaStream_t s) {
       p.n_tiles = (a.H + 255) / 256;
       break;
     case kBwdDA:
-      ok = make_map(&mA0, a.dy_perm, H, M, 128) && make_map(&mB0, a.W_down, H, E * I, 256);
+      ok = make_map(&mA0, a.dy_perm, H, M, 128) && make_map(&mB0, a.W_down, H, E * I, 128);
       mA1 = mA0;
       mB1 = mB0;
       p.G = a.G;
@@ -592,7 +640,7 @@ cudaError_t launch_mode(const GemmArgs &a, cudaStream_t s) {
       break;
     case kBwdDX:
       ok = make_map(&mA0, a.dG, I, M, 128) && make_map(&mA1, a.dU, I, M, 128) &&
-           make_map(&mB0, a.W_gate, I, E * H, 256) && make_map(&mB1, a.W_up, I, E * H, 256);
+           make_map(&mB0, a.W_gate, I, E * H, 128) && make_map(&mB1, a.W_up, I, E * H, 128);
       p.kdim = 2 * a.I;
       p.n_tiles = (a.H + 255) / 256;
       break;
@@ -600,28 +648,60 @@ cudaError_t launch_mode(const GemmArgs &a, cudaStream_t s) {
       ok = make_map(&mA0, a.act_w, I, M, 64) && make_map(&mB0, a.dy_perm, H, M, 64);
       mA1 = mA0;
       mB1 = mB0;
-      p.m_tiles = (a.I + 127) / 128;
+      p.m_tiles = (a.I + 2 * BM - 1) / (2 * BM);
       p.n_tiles = (a.H + 255) / 256;
       break;
     default:  // kBwdDWGateUp
       ok = make_map(&mA0, a.x_perm, H, M, 64) && make_map(&mB0, a.dG, I, M, 64) &&
            make_map(&mB1, a.dU, I, M, 64);
       mA1 = mA0;
-      p.m_tiles = (a.H + 127) / 128;
+      p.m_tiles = (a.H + 2 * BM - 1) / (2 * BM);
       p.n_tiles = (a.I + 127) / 128;
       break;
   }
   if (!ok) return cudaErrorInvalidValue;
-  static bool attr_set[64] = {};
+  if constexpr (Traits<MODE>::kRaggedK) {
+    if (!a.map_scratch) return cudaErrorInvalidValue;
+    MapTemplates tm;
+    tm.m[0] = mA0;
+    tm.m[1] = mB0;
+    tm.m[2] = mB1;
+    CUtensorMap *maps = static_cast<CUtensorMap *>(a.map_scratch);
+    expert_maps_kernel<<<(a.E + 255) / 256, 256, 0, s>>>(tm, a.offsets, a.E, maps);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    p.expert_maps = maps;
+  }
+  // once per device: the shared-memory opt-in, and how many CTA pairs fit at once
+  static int pair_grid[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (!pair_grid[dev]) {
     cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    cfg.gridDim = dim3(a.num_sms & ~1);
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_kernel<MODE>, &cfg);
+    if (e != cudaSuccess) return e;
+    if (clusters < 1) return cudaErrorInvalidConfiguration;
+    pair_grid[dev] = 2 * (clusters < a.num_sms / 2 ? clusters : a.num_sms / 2);
   }
-  grouped_gemm_kernel<MODE><<<a.num_sms, kThreads, kSmemBytes, s>>>(mA0, mA1, mB0, mB1, p);
+  cfg.gridDim = dim3(pair_grid[dev]);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE>, mA0, mA1, mB0, mB1, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

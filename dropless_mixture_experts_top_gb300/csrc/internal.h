@@ -77,8 +77,10 @@ struct GemmArgs {
   // outputs (device, bf16)
   uint16_t *o0, *o1, *o2, *o3;
   int32_t *status;
+  void *map_scratch;  // ragged K: device scratch for E * 3 tensor maps (128 B each, 128-B aligned)
   int num_sms;
 };
+constexpr size_t kExpertMapBytes = 3 * 128;  // per expert
 cudaError_t launch_grouped_gemm(GemmMode mode, const GemmArgs &a, cudaStream_t s);
 const char *gemm_mode_name(GemmMode mode);
 
