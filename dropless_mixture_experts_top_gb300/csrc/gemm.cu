@@ -433,8 +433,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int tile = cluster; tile < total && ok; tile += nclusters) {
       const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off);
-      if constexpr (Tr::kRaggedK) {  // this expert's maps were written by the preceding launch
-        if (lane < kMapsPerExpert && t.nkb > 0) tmap_acquire(p.expert_maps + t.e * kMapsPerExpert + lane);
+      if constexpr (Tr::kRaggedK) {  // this expert's maps were written by the preceding launch;
+        // the thread that issues the copies acquires every map it will use
+        if (lane == 0 && t.nkb > 0)
+          for (int j = 0; j < kMapsPerExpert; ++j) tmap_acquire(p.expert_maps + t.e * kMapsPerExpert + j);
         __syncwarp();
       }
       for (int kb = 0; kb < t.nkb; ++kb) {
