@@ -29,6 +29,9 @@
  *   - fp8_bwd: each backward GEMM operand is quantised to MXFP8 (E4M3 values,
  *     one power-of-two UE8M0 scale per 32 consecutive elements along the GEMM's
  *     reduction dimension); blocks along tokens start at each expert's first row.
+ *     The router weight is not folded into a quantised operand: dA's operands
+ *     are dy (along H) and W_down, with w applied to the product in full
+ *     precision; dW_down's operands are w*a and dy (along tokens).
  *
  * Arithmetic: fp64 throughout; bf16 inputs are widened exactly.  The oracle
  * never rounds intermediates.  Loops run in a fixed order; OpenMP only splits
@@ -398,13 +401,18 @@ EXPORT int oracle_backward_tokens(const oracle_shape *sh, const uint16_t *x, con
       double s = 0.0;
       for (int h = 0; h < H; ++h) s += bf(dyt[h]) * y[h];
       gd[j] = s;
-      for (int h = 0; h < H; ++h) dyw[h] = w * bf(dyt[h]);
-      if (quant) mx_vec(dyw, H, 1);
+      if (quant) { /* dA = w * (Q(dy) . Q(W_down)^T) */
+        for (int h = 0; h < H; ++h) dyw[h] = bf(dyt[h]);
+        mx_vec(dyw, H, 1);
+      } else {
+        for (int h = 0; h < H; ++h) dyw[h] = w * bf(dyt[h]);
+      }
       for (int i = 0; i < I; ++i) {
         double acc = 0.0;
         if (quant) {
           const float *wd = qWd + ((int64_t)e * I + i) * H;
           for (int h = 0; h < H; ++h) acc += dyw[h] * (double)wd[h];
+          acc *= w;
         } else {
           const uint16_t *wd = Wd + ((int64_t)e * I + i) * H;
           for (int h = 0; h < H; ++h) acc += dyw[h] * bf(wd[h]);
@@ -469,10 +477,11 @@ static int64_t expert_rows(const oracle_shape *sh, const int32_t *topk_idx, int 
   return n;
 }
 
-/* Per-row backward intermediates of expert e over its rows: a [n,I], dyw [n,H],
- * dg [n,I], du [n,I].  In quant mode dA's operands are quantised along H
- * (matching oracle_backward_tokens); the dW operands are quantised afterwards
- * along tokens by the caller. */
+/* Per-row backward intermediates of expert e over its rows: the two dW_down
+ * operands (exact: a [n,I] and w dy [n,H]; quant: w a and dy), dg [n,I], du [n,I].
+ * In quant mode dA's operands are quantised along H (matching
+ * oracle_backward_tokens); the dW operands are quantised afterwards along tokens
+ * by the caller. */
 static void expert_rows_bwd(const ctx_t *c, int e, int64_t n, const int64_t *tok,
                             const int32_t *choice, const double *topk_w, int quant, double *A,
                             double *DYW, double *DG, double *DU) {
@@ -483,7 +492,9 @@ static void expert_rows_bwd(const ctx_t *c, int e, int64_t n, const int64_t *tok
     int64_t t = tok[r];
     double w = topk_w[t * k + choice[r]];
     expert_fwd(c, t, e, g, u, a, NULL);
-    for (int h = 0; h < H; ++h) q[h] = w * bf(c->dy[t * H + h]);
+    /* exact: dW_down operands a and w dy.  quant: w a and dy, and dA = w (Q(dy) . Q(W_down)^T) */
+    const double ws = quant ? 1.0 : w;
+    for (int h = 0; h < H; ++h) q[h] = ws * bf(c->dy[t * H + h]);
     for (int h = 0; h < H; ++h) DYW[r * H + h] = q[h];
     if (quant) mx_vec(q, H, 1);
     for (int i = 0; i < I; ++i) {
@@ -491,6 +502,7 @@ static void expert_rows_bwd(const ctx_t *c, int e, int64_t n, const int64_t *tok
       if (quant) {
         const float *wd = c->qWd + ((int64_t)e * I + i) * H;
         for (int h = 0; h < H; ++h) acc += q[h] * (double)wd[h];
+        acc *= w;
       } else {
         const uint16_t *wd = c->Wd + ((int64_t)e * I + i) * H;
         for (int h = 0; h < H; ++h) acc += q[h] * bf(wd[h]);
@@ -499,7 +511,7 @@ static void expert_rows_bwd(const ctx_t *c, int e, int64_t n, const int64_t *tok
     }
     for (int i = 0; i < I; ++i) {
       double sg = sigmoid(g[i]);
-      A[r * I + i] = a[i];
+      A[r * I + i] = quant ? w * a[i] : a[i];
       DG[r * I + i] = da[i] * u[i] * sg * (1.0 + g[i] * (1.0 - sg));
       DU[r * I + i] = da[i] * silu(g[i]);
     }
@@ -611,16 +623,23 @@ EXPORT int oracle_dw_elements(const oracle_shape *sh, const uint16_t *x, const i
         ui += xv * bf(wu[(int64_t)h * I + ci]);
       }
       if (wh == 2) { /* dW_down[e, i=r0, h=c0] = sum a_i * (w dy)_h */
-        L[r] = silu(gi) * ui;
-        R[r] = w * bf(dy[t * H + c0]);
+        if (quant) { /* operands w*a and dy */
+          L[r] = w * silu(gi) * ui;
+          R[r] = bf(dy[t * H + c0]);
+        } else {
+          L[r] = silu(gi) * ui;
+          R[r] = w * bf(dy[t * H + c0]);
+        }
       } else { /* dW_gate/up[e, h=r0, i=c0] = sum x_h * dg_i (du_i) */
-        for (int h = 0; h < H; ++h) dyw[h] = w * bf(dy[t * H + h]);
-        if (quant) mx_vec(dyw, H, 1);
         double da = 0.0;
         if (quant) {
+          for (int h = 0; h < H; ++h) dyw[h] = bf(dy[t * H + h]);
+          mx_vec(dyw, H, 1);
           const float *wd = qWd + ((int64_t)e * I + c0) * H;
           for (int h = 0; h < H; ++h) da += dyw[h] * (double)wd[h];
+          da *= w;
         } else {
+          for (int h = 0; h < H; ++h) dyw[h] = w * bf(dy[t * H + h]);
           const uint16_t *wd = Wd + ((int64_t)e * I + c0) * H;
           for (int h = 0; h < H; ++h) da += dyw[h] * bf(wd[h]);
         }

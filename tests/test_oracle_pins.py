@@ -284,7 +284,7 @@ def test_expert_relabelling_equivariance():
 
 
 def test_sampled_entry_points_agree_with_full():
-    shape = MoEShape(T=50, H=32, I=16, E=4, k=2)
+    shape = MoEShape(T=50, H=64, I=32, E=4, k=2)
     inp = small_inputs(shape)
     idx, w = O.route(inp["logits"], shape.k)
     args = (shape, inp["x"], idx, w, inp["W_gate"], inp["W_up"], inp["W_down"], inp["dy"])
@@ -298,6 +298,10 @@ def test_sampled_entry_points_agree_with_full():
     vals = O.dw_elements(*args, which, e, r, c)
     ref = np.array([full[wh][ee, rr, cc] for wh, ee, rr, cc in zip(which, e, r, c)])
     np.testing.assert_allclose(vals, ref, rtol=1e-13, atol=1e-15)
+    qvals = O.dw_elements(*args, which, e, r, c, quant=True)  # fp8_bwd: the same two code paths agree
+    qfull = O.dw_full(*args, quant=True)
+    np.testing.assert_allclose(qvals, np.array([qfull[wh][ee, rr, cc] for wh, ee, rr, cc in zip(which, e, r, c)]),
+                               rtol=1e-13, atol=1e-15)
     toks = np.array([49, 0, 7])
     out_all = O.forward(shape, inp["x"], idx, w, inp["W_gate"], inp["W_up"], inp["W_down"])
     np.testing.assert_array_equal(
