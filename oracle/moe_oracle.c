@@ -32,6 +32,11 @@
  *     The router weight is not folded into a quantised operand: dA's operands
  *     are dy (along H) and W_down, with w applied to the product in full
  *     precision; dW_down's operands are w*a and dy (along tokens).
+ *     Every code is decided on the bf16 tensors the backward holds: the forward
+ *     runs in BF16, so the activations it saves (g, u) are bf16 when dSwiGLU
+ *     reads them, and dg, du and w*a are rounded to bf16 (nearest-even) before
+ *     they are quantised.  Where floating point decides an integer code, both
+ *     this oracle and the GPU take the decision on the same bf16 values.
  *
  * Arithmetic: fp64 throughout; bf16 inputs are widened exactly.  The oracle
  * never rounds intermediates.  Loops run in a fixed order; OpenMP only splits
@@ -54,6 +59,22 @@ static double bf(uint16_t h) {
   float f;
   memcpy(&f, &u, 4);
   return (double)f;
+}
+
+/* Nearest bf16 (8 significant bits, fp32's exponent range), ties to even;
+ * magnitudes that round past the largest finite bf16 become infinite. */
+EXPORT double oracle_round_bf16(double v) {
+  if (v == 0.0 || isnan(v) || isinf(v)) return v;
+  double a = fabs(v), r;
+  if (a < 0x1p-126) {
+    r = nearbyint(a / 0x1p-133) * 0x1p-133; /* subnormal spacing 2^-133 */
+  } else {
+    int ex;
+    double f = frexp(a, &ex);                 /* a = f 2^ex, f in [0.5, 1) */
+    r = ldexp(nearbyint(ldexp(f, 8)), ex - 8); /* 8 significant bits */
+    if (r > 0x1.FEp127) r = INFINITY;
+  }
+  return v < 0 ? -r : r;
 }
 
 static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
@@ -420,11 +441,18 @@ EXPORT int oracle_backward_tokens(const oracle_shape *sh, const uint16_t *x, con
         da[i] = acc;
       }
       for (int i = 0; i < I; ++i) {
-        double sg = sigmoid(g[i]);
-        dg[i] = da[i] * u[i] * sg * (1.0 + g[i] * (1.0 - sg));
-        du[i] = da[i] * silu(g[i]);
+        /* fp8_bwd: dSwiGLU reads the saved bf16 activations */
+        const double gi = quant ? oracle_round_bf16(g[i]) : g[i];
+        const double ui = quant ? oracle_round_bf16(u[i]) : u[i];
+        double sg = sigmoid(gi);
+        dg[i] = da[i] * ui * sg * (1.0 + gi * (1.0 - sg));
+        du[i] = da[i] * silu(gi);
       }
       if (quant) {
+        for (int i = 0; i < I; ++i) {
+          dg[i] = oracle_round_bf16(dg[i]);
+          du[i] = oracle_round_bf16(du[i]);
+        }
         mx_vec(dg, I, 1);
         mx_vec(du, I, 1);
       }
@@ -510,10 +538,18 @@ static void expert_rows_bwd(const ctx_t *c, int e, int64_t n, const int64_t *tok
       da[i] = acc;
     }
     for (int i = 0; i < I; ++i) {
-      double sg = sigmoid(g[i]);
-      A[r * I + i] = quant ? w * a[i] : a[i];
-      DG[r * I + i] = da[i] * u[i] * sg * (1.0 + g[i] * (1.0 - sg));
-      DU[r * I + i] = da[i] * silu(g[i]);
+      if (quant) { /* bf16 tensors: saved g, u in; w*a, dg, du out */
+        const double gi = oracle_round_bf16(g[i]), ui = oracle_round_bf16(u[i]);
+        const double sg = sigmoid(gi);
+        A[r * I + i] = oracle_round_bf16(w * a[i]);
+        DG[r * I + i] = oracle_round_bf16(da[i] * ui * sg * (1.0 + gi * (1.0 - sg)));
+        DU[r * I + i] = oracle_round_bf16(da[i] * silu(gi));
+      } else {
+        const double sg = sigmoid(g[i]);
+        A[r * I + i] = a[i];
+        DG[r * I + i] = da[i] * u[i] * sg * (1.0 + g[i] * (1.0 - sg));
+        DU[r * I + i] = da[i] * silu(g[i]);
+      }
     }
   }
   free(g);
@@ -623,8 +659,8 @@ EXPORT int oracle_dw_elements(const oracle_shape *sh, const uint16_t *x, const i
         ui += xv * bf(wu[(int64_t)h * I + ci]);
       }
       if (wh == 2) { /* dW_down[e, i=r0, h=c0] = sum a_i * (w dy)_h */
-        if (quant) { /* operands w*a and dy */
-          L[r] = w * silu(gi) * ui;
+        if (quant) { /* operands w*a (a bf16 tensor) and dy */
+          L[r] = oracle_round_bf16(w * silu(gi) * ui);
           R[r] = bf(dy[t * H + c0]);
         } else {
           L[r] = silu(gi) * ui;
@@ -643,9 +679,14 @@ EXPORT int oracle_dw_elements(const oracle_shape *sh, const uint16_t *x, const i
           const uint16_t *wd = Wd + ((int64_t)e * I + c0) * H;
           for (int h = 0; h < H; ++h) da += dyw[h] * bf(wd[h]);
         }
+        if (quant) { /* saved bf16 activations in, a bf16 gradient out */
+          gi = oracle_round_bf16(gi);
+          ui = oracle_round_bf16(ui);
+        }
         double sg = sigmoid(gi);
         L[r] = bf(x[t * H + r0]);
         R[r] = (wh == 0) ? da * ui * sg * (1.0 + gi * (1.0 - sg)) : da * silu(gi);
+        if (quant) R[r] = oracle_round_bf16(R[r]);
       }
     }
     if (quant) {

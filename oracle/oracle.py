@@ -59,6 +59,8 @@ def lib():
             L.oracle_e4m3_decode.restype = ctypes.c_double
             L.oracle_mx_scale_exp.argtypes = [ctypes.c_double]
             L.oracle_mx_scale_exp.restype = ctypes.c_int
+            L.oracle_round_bf16.argtypes = [ctypes.c_double]
+            L.oracle_round_bf16.restype = ctypes.c_double
             L.oracle_mx_quantize_rows_bf16.argtypes = [i64, i64, P, P, P, P]
             L.oracle_mx_quantize_cols_bf16.argtypes = [i64, i64, i64, P, P, P]
             for f in ("oracle_route", "oracle_dispatch", "oracle_forward", "oracle_backward_tokens",
@@ -216,6 +218,11 @@ def e4m3_encode(v: float) -> int:
 
 def e4m3_decode(code: int) -> float:
     return float(lib().oracle_e4m3_decode(int(code)))
+
+
+def round_bf16(v: float) -> float:
+    """Nearest bf16 value (ties to even), as the fp8_bwd backward rounds its tensors."""
+    return float(lib().oracle_round_bf16(float(v)))
 
 
 def mx_scale_exp(amax: float) -> int:

@@ -10,7 +10,11 @@
     empty experts get exactly zero weight gradients, linearity in W_up/W_down
     and dy, expert relabelling equivariance;
   * the MXFP8 quantiser against a brute-force nearest-value search over all
-    E4M3 codes, and its scale rule against its defining inequality.
+    E4M3 codes, and its scale rule against its defining inequality;
+  * the bf16 rounding the fp8_bwd mode applies against torch's fp32 -> bf16
+    conversion, and the fp8_bwd backward against a numpy composition of the
+    pinned quantiser and rounding (which operands, along which axis, rounded
+    where).
 """
 import itertools
 
@@ -391,3 +395,79 @@ def test_fp8_bwd_mode_changes_backward_by_quantisation_error_only():
     qW = O.quant_weights(inp["W_gate"], inp["W_up"], inp["W_down"])
     again = O.mx_quantize_rows(f32_to_bf16_bits(qW[2]))[2]
     np.testing.assert_array_equal(again, qW[2])
+
+
+def test_round_bf16_matches_torch():
+    rng = np.random.default_rng(5)
+    v = np.concatenate([
+        (rng.standard_normal(4000) * np.exp2(rng.integers(-140, 127, 4000))).astype(np.float32),
+        np.float32([3.0e38, -3.39e38, 1e-45, -3e-41, 0.0, 1.0, 2.0 ** -126, 2.0 ** -127])])
+    # exact ties between two bf16 neighbours: both tie-to-even directions
+    base = f32_to_bf16_bits(rng.standard_normal(500).astype(np.float32)).astype(np.uint32) << 16
+    ties = (base | 0x8000).view(np.float32)
+    v = np.concatenate([v, ties])
+    ref = torch.from_numpy(v).to(torch.bfloat16).to(torch.float64).numpy()
+    got = np.array([O.round_bf16(float(a)) for a in v])
+    np.testing.assert_array_equal(got, ref)
+
+
+def _deq_cols(bits, seg, n, table):
+    codes, scales = O.mx_quantize_cols(bits, seg, n)
+    return (table[codes] * np.exp2(scales.astype(np.float64) - 127).repeat(32, axis=0))[:n]
+
+
+def test_fp8_bwd_composition():
+    """backward_tokens/dw_full in quant mode against the same chain written with
+    numpy matrix products over the oracle's pinned quantiser and bf16 rounding."""
+    shape = MoEShape(T=96, H=64, I=96, E=4, k=2)
+    inp = synth.make_inputs_shape(shape, 23, w_scale=0.3)
+    T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
+    idx, w = O.route(inp["logits"], k)
+    f = lambda b: bf16_bits_to_f32(b).astype(np.float64)
+    x, Wg, Wu, Wd, dy = (f(inp[n]) for n in ("x", "W_gate", "W_up", "W_down", "dy"))
+    qWg, qWu, qWd = (q.astype(np.float64) for q in O.quant_weights(inp["W_gate"], inp["W_up"], inp["W_down"]))
+    rb = np.vectorize(O.round_bf16)
+    table = np.array([O.e4m3_decode(c) for c in range(256)])
+    q_rows = lambda v: O.mx_quantize_rows(f32_to_bf16_bits(np.atleast_2d(v).astype(np.float32)))[2].astype(np.float64)
+    sig = lambda z: 1 / (1 + np.exp(-z))
+    dx = np.zeros((T, H))
+    rows = {e: [] for e in range(E)}
+    for t in range(T):
+        for j in range(k):
+            e, wt = idx[t, j], w[t, j]
+            g, u = x[t] @ Wg[e], x[t] @ Wu[e]
+            da = wt * (q_rows(dy[t])[0] @ qWd[e].T)
+            gb, ub = rb(g), rb(u)
+            dg = rb(da * ub * sig(gb) * (1 + gb * (1 - sig(gb))))
+            du = rb(da * gb * sig(gb))
+            dx[t] += q_rows(dg)[0] @ qWg[e].T + q_rows(du)[0] @ qWu[e].T
+            rows[e].append((t, rb(wt * g * sig(g) * u), dg, du))
+    ref_dx = O.backward_tokens(shape, inp["x"], inp["logits"], idx, w, inp["W_gate"], inp["W_up"],
+                               inp["W_down"], inp["dy"], quant=True)[0]
+    rel = lambda a, b: np.linalg.norm(a - b) / np.linalg.norm(b)
+    assert rel(dx, ref_dx) < 1e-12
+    dWg, dWu, dWd = O.dw_full(shape, inp["x"], idx, w, inp["W_gate"], inp["W_up"], inp["W_down"], inp["dy"],
+                              quant=True)
+    for e in range(E):
+        toks = [r[0] for r in rows[e]]
+        n = len(toks)
+        bits = lambda m: f32_to_bf16_bits(np.asarray(m, np.float32).reshape(n, -1))
+        Xq = _deq_cols(inp["x"][toks], 0, n, table)
+        DYq = _deq_cols(inp["dy"][toks], 0, n, table)
+        Aq = _deq_cols(bits([r[1] for r in rows[e]]), 0, n, table)
+        DGq = _deq_cols(bits([r[2] for r in rows[e]]), 0, n, table)
+        DUq = _deq_cols(bits([r[3] for r in rows[e]]), 0, n, table)
+        assert rel(Xq.T @ DGq, dWg[e]) < 1e-12
+        assert rel(Xq.T @ DUq, dWu[e]) < 1e-12
+        assert rel(Aq.T @ DYq, dWd[e]) < 1e-12
+    # the element-wise path agrees with the full one
+    rng = np.random.default_rng(3)
+    which = rng.integers(0, 3, 60).astype(np.int32)
+    ee = rng.integers(0, E, 60).astype(np.int32)
+    rr = np.where(which == 2, rng.integers(0, I, 60), rng.integers(0, H, 60)).astype(np.int32)
+    cc = np.where(which == 2, rng.integers(0, H, 60), rng.integers(0, I, 60)).astype(np.int32)
+    got = O.dw_elements(shape, inp["x"], idx, w, inp["W_gate"], inp["W_up"], inp["W_down"], inp["dy"],
+                        which, ee, rr, cc, quant=True)
+    full = np.stack([dWg, dWu])
+    exp = np.array([dWd[e, r, c] if wh == 2 else full[wh, e, r, c] for wh, e, r, c in zip(which, ee, rr, cc)])
+    np.testing.assert_allclose(got, exp, rtol=1e-12, atol=1e-14)
