@@ -42,6 +42,8 @@ struct Layout {
   size_t f_total;
   // backward scratch
   size_t b_dyp, b_dG, b_dU, b_dX, b_maps, b_total;
+  // fp8_bwd: quantised operands inside the backward scratch (zero otherwise)
+  moe_fp8_layout q;
 };
 
 bool shape_ok(const moe_config *c) {
@@ -50,8 +52,14 @@ bool shape_ok(const moe_config *c) {
   if (c->E < 1 || c->E > kMaxExperts || c->k < 1 || c->k > kMaxTopK || c->k > c->E) return false;
   if (static_cast<int64_t>(c->T) * c->k >= (int64_t{1} << 31)) return false;
   if (c->precision != MOE_PREC_BF16 && c->precision != MOE_PREC_FP8_BWD) return false;
+  // MXFP8 GEMMs stage K in 128-byte blocks and keep scale atoms of 128 rows
+  if (c->precision == MOE_PREC_FP8_BWD && (c->H % 128 || c->I % 128)) return false;
   return true;
 }
+
+// Padded token capacity of the fp8_bwd operands: every expert's rows rounded
+// up to a multiple of 128 fit in M + 127 E, itself rounded up to 128.
+inline size_t fp8_mpad(size_t M, size_t E) { return ((M + 127 * E + 127) / 128) * 128; }
 
 Layout layout_of(const moe_config *c) {
   Layout L{};
@@ -91,6 +99,39 @@ Layout layout_of(const moe_config *c) {
   o += align256(M * H * 2);
   L.b_maps = o;
   o += align256(E * kExpertMapBytes);
+  if (c->precision == MOE_PREC_FP8_BWD) {
+    const size_t Mp = fp8_mpad(M, E);
+    moe_fp8_layout &q = L.q;
+    q.m_pad = Mp;
+    auto take = [&o](size_t bytes) {
+      const size_t at = o;
+      o += align256(bytes);
+      return at;
+    };
+    q.pad_offsets = take((E + 1) * 4);
+    q.dy_q = take(Mp * H);
+    q.dy_sf = take(Mp * H / 32);
+    q.wd_q = take(E * I * H);
+    q.wd_sf = take(E * I * H / 32);
+    q.dg_q = take(Mp * I);
+    q.dg_sf = take(Mp * I / 32);
+    q.du_q = take(Mp * I);
+    q.du_sf = take(Mp * I / 32);
+    q.wg_q = take(E * H * I);
+    q.wg_sf = take(E * H * I / 32);
+    q.wu_q = take(E * H * I);
+    q.wu_sf = take(E * H * I / 32);
+    q.aw_t = take(I * Mp);
+    q.aw_t_sf = take(I * Mp / 32);
+    q.dy_t = take(H * Mp);
+    q.dy_t_sf = take(H * Mp / 32);
+    q.x_t = take(H * Mp);
+    q.x_t_sf = take(H * Mp / 32);
+    q.dg_t = take(I * Mp);
+    q.dg_t_sf = take(I * Mp / 32);
+    q.du_t = take(I * Mp);
+    q.du_t_sf = take(I * Mp / 32);
+  }
   L.b_total = o;
   return L;
 }
@@ -179,6 +220,119 @@ GemmArgs gemm_base(const moe_config *c, const moe_routing *r, int sms, int32_t *
   return g;
 }
 
+// The fp8_bwd backward after the router backward: each grouped GEMM's operands
+// are quantised to MXFP8 along that GEMM's K (weights along rows; activations
+// along features into a per-expert padded row space; token-axis operands
+// transposed, blocks of 32 tokens from each expert's first row), then the
+// block-scaled GEMMs run with the bf16 epilogues.
+struct Fp8Bwd {
+  const moe_config *cfg;
+  const moe_routing *r;
+  const moe_fp8_layout *q;
+  uint8_t *sc;
+  int sms;
+  int32_t *status;
+  const uint16_t *W_gate, *W_up, *W_down, *x_perm, *G, *U, *A_w;
+  uint16_t *dy_perm, *dG, *dU, *dX, *dx, *dW_gate, *dW_up, *dW_down;
+};
+
+moe_status backward_fp8(const Fp8Bwd &f, cudaStream_t s) {
+  const int T = f.cfg->T, H = f.cfg->H, I = f.cfg->I, E = f.cfg->E, k = f.cfg->k;
+  const int Mp = static_cast<int>(f.q->m_pad);
+  const moe_fp8_layout &q = *f.q;
+  uint8_t *sc = f.sc;
+  int32_t *pad_off = reinterpret_cast<int32_t *>(sc + q.pad_offsets);
+  const int32_t *off = f.r->offsets;
+  MOE_TRY(timed("mx_pad_offsets", s, [&] { return launch_pad_offsets(off, E, pad_off, s); }));
+  MxGemmArgs m{};
+  m.H = H;
+  m.I = I;
+  m.E = E;
+  m.Mpad = Mp;
+  m.offsets = off;
+  m.pad_off = pad_off;
+  m.G = f.G;
+  m.U = f.U;
+  m.w_row = f.r->w_row;
+  m.status = f.status;
+  m.num_sms = f.sms;
+  // dA = w (Q(dy) . Q(W_down)^T), K = H; dSwiGLU epilogue -> dG, dU
+  MOE_TRY(timed("mx_quant_rows", s, [&] {
+    return launch_quant_rows(f.dy_perm, Mp, H, off, pad_off, E, sc + q.dy_q, sc + q.dy_sf, s);
+  }));
+  MOE_TRY(timed("mx_quant_rows", s, [&] {
+    return launch_quant_rows(f.W_down, E * I, H, nullptr, nullptr, E, sc + q.wd_q, sc + q.wd_sf, s);
+  }));
+  m.a0 = sc + q.dy_q;
+  m.sfa0 = sc + q.dy_sf;
+  m.b0 = sc + q.wd_q;
+  m.sfb0 = sc + q.wd_sf;
+  m.o0 = f.dG;
+  m.o1 = f.dU;
+  MOE_TRY(timed("mx_gemm_dA_dswiglu", s, [&] { return launch_mx_gemm(kMxGemmDA, m, s); }));
+  // dX = Q(dG) . Q(W_gate)^T + Q(dU) . Q(W_up)^T, K = I
+  MOE_TRY(timed("mx_quant_rows", s, [&] {
+    return launch_quant_rows(f.dG, Mp, I, off, pad_off, E, sc + q.dg_q, sc + q.dg_sf, s);
+  }));
+  MOE_TRY(timed("mx_quant_rows", s, [&] {
+    return launch_quant_rows(f.dU, Mp, I, off, pad_off, E, sc + q.du_q, sc + q.du_sf, s);
+  }));
+  MOE_TRY(timed("mx_quant_rows", s, [&] {
+    return launch_quant_rows(f.W_gate, E * H, I, nullptr, nullptr, E, sc + q.wg_q, sc + q.wg_sf, s);
+  }));
+  MOE_TRY(timed("mx_quant_rows", s, [&] {
+    return launch_quant_rows(f.W_up, E * H, I, nullptr, nullptr, E, sc + q.wu_q, sc + q.wu_sf, s);
+  }));
+  m.a0 = sc + q.dg_q;
+  m.sfa0 = sc + q.dg_sf;
+  m.a1 = sc + q.du_q;
+  m.sfa1 = sc + q.du_sf;
+  m.b0 = sc + q.wg_q;
+  m.sfb0 = sc + q.wg_sf;
+  m.b1 = sc + q.wu_q;
+  m.sfb1 = sc + q.wu_sf;
+  m.o0 = f.dX;
+  m.o1 = nullptr;
+  MOE_TRY(timed("mx_gemm_dX", s, [&] { return launch_mx_gemm(kMxGemmDX, m, s); }));
+  MOE_TRY(timed("unpermute_sum", s, [&] {
+    return launch_gather_sum(f.dX, f.r->row_of_slot, nullptr, f.dx, T, H, k, s);
+  }));
+  // dW_down = Q(w a)^T . Q(dy), K = the expert's tokens
+  MOE_TRY(timed("mx_quant_cols", s, [&] {
+    return launch_quant_cols(f.A_w, I, Mp, off, pad_off, E, sc + q.aw_t, sc + q.aw_t_sf, s);
+  }));
+  MOE_TRY(timed("mx_quant_cols", s, [&] {
+    return launch_quant_cols(f.dy_perm, H, Mp, off, pad_off, E, sc + q.dy_t, sc + q.dy_t_sf, s);
+  }));
+  m.a0 = sc + q.aw_t;
+  m.sfa0 = sc + q.aw_t_sf;
+  m.b0 = sc + q.dy_t;
+  m.sfb0 = sc + q.dy_t_sf;
+  m.a1 = m.b1 = m.sfa1 = m.sfb1 = nullptr;
+  m.o0 = f.dW_down;
+  MOE_TRY(timed("mx_gemm_dW_down", s, [&] { return launch_mx_gemm(kMxGemmDWDown, m, s); }));
+  // dW_gate = Q(x)^T . Q(dG), dW_up = Q(x)^T . Q(dU), K = the expert's tokens
+  MOE_TRY(timed("mx_quant_cols", s, [&] {
+    return launch_quant_cols(f.x_perm, H, Mp, off, pad_off, E, sc + q.x_t, sc + q.x_t_sf, s);
+  }));
+  MOE_TRY(timed("mx_quant_cols", s, [&] {
+    return launch_quant_cols(f.dG, I, Mp, off, pad_off, E, sc + q.dg_t, sc + q.dg_t_sf, s);
+  }));
+  MOE_TRY(timed("mx_quant_cols", s, [&] {
+    return launch_quant_cols(f.dU, I, Mp, off, pad_off, E, sc + q.du_t, sc + q.du_t_sf, s);
+  }));
+  m.a0 = sc + q.x_t;
+  m.sfa0 = sc + q.x_t_sf;
+  m.b0 = sc + q.dg_t;
+  m.sfb0 = sc + q.dg_t_sf;
+  m.b1 = sc + q.du_t;
+  m.sfb1 = sc + q.du_t_sf;
+  m.o0 = f.dW_gate;
+  m.o1 = f.dW_up;
+  MOE_TRY(timed("mx_gemm_dW_gateup", s, [&] { return launch_mx_gemm(kMxGemmDWGateUp, m, s); }));
+  return MOE_OK;
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -206,6 +360,12 @@ moe_status moe_saved_offsets(const moe_config *cfg, moe_saved_layout *out) {
   out->A = L.s_A;
   out->Y = L.s_Y;
   out->A_w = L.s_Aw;
+  return MOE_OK;
+}
+
+moe_status moe_fp8_scratch_offsets(const moe_config *cfg, moe_fp8_layout *out) {
+  if (!shape_ok(cfg) || !out || cfg->precision != MOE_PREC_FP8_BWD) return MOE_ERR_INVALID_ARG;
+  *out = layout_of(cfg).q;
   return MOE_OK;
 }
 
@@ -321,7 +481,6 @@ moe_status moe_backward(const moe_config *cfg, const void *dy, const void *x,
     return MOE_ERR_ALIGNMENT;
   const Layout L = layout_of(cfg);
   if (saved_bytes < L.s_total || scratch_bytes < L.b_total) return MOE_ERR_WORKSPACE;
-  if (cfg->precision != MOE_PREC_BF16) return MOE_ERR_UNSUPPORTED;
   DevInfo di;
   MOE_TRY(device_info(&di));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -353,6 +512,31 @@ moe_status moe_backward(const moe_config *cfg, const void *dy, const void *x,
     return launch_router_bwd(static_cast<const uint16_t *>(dy), Y, r->row_of_slot, r->topk_idx,
                              r->topk_w, dy_perm, d_logits, d_topk_w, T, H, E, k, s);
   }));
+  if (cfg->precision == MOE_PREC_FP8_BWD) {
+    Fp8Bwd f;
+    f.cfg = cfg;
+    f.r = r;
+    f.q = &L.q;
+    f.sc = sc;
+    f.sms = di.sms;
+    f.status = status;
+    f.W_gate = static_cast<const uint16_t *>(W_gate);
+    f.W_up = static_cast<const uint16_t *>(W_up);
+    f.W_down = static_cast<const uint16_t *>(W_down);
+    f.x_perm = x_perm;
+    f.G = G;
+    f.U = U;
+    f.A_w = A_w;
+    f.dy_perm = dy_perm;
+    f.dG = dG;
+    f.dU = dU;
+    f.dX = dX;
+    f.dx = static_cast<uint16_t *>(dx);
+    f.dW_gate = static_cast<uint16_t *>(dW_gate);
+    f.dW_up = static_cast<uint16_t *>(dW_up);
+    f.dW_down = static_cast<uint16_t *>(dW_down);
+    return backward_fp8(f, s);
+  }
   GemmArgs g = gemm_base(cfg, r, di.sms, status);
   g.x_perm = x_perm;
   g.W_gate = static_cast<const uint16_t *>(W_gate);

@@ -1,0 +1,481 @@
+// gemm_mx.cu -- MXFP8 grouped GEMMs of the fp8_bwd backward on the 5th-generation
+// tensor core: tcgen05.mma kind::mxf8f6f4 with block scaling (E4M3 operands,
+// one UE8M0 scale per 32 elements of K, fp32 accumulation in TMEM).
+//
+// The four backward GEMMs (dA, dX, dW_down, dW_gate/up) read operands written
+// by the quantisers in mxfp8.cu: K-major E4M3 codes, scale factors in 512-byte
+// atoms, ragged operands in a per-expert row space padded to 128 rows (so tiles
+// and 32-element blocks along tokens never straddle two experts, and the padded
+// rows are zeros).  Outputs are bf16 and go through the same epilogues as the
+// bf16 engine (dSwiGLU for dA).
+//
+// One CTA per SM, persistent, static round-robin over 128 x 256 tiles:
+//   warp 0      producer: TMA boxes of codes (128-byte swizzle) and bulk copies
+//               of the scale atoms into a 4-stage ring
+//   warp 1      MMA issuer: per stage, tcgen05.cp of the scale atoms into a
+//               tensor-memory slot (32x128b.warpx4: row r's four block scales
+//               land in lane r%32, column r/32), then four K=32 MMAs selecting
+//               the block's scale byte with the descriptor's scale-factor ids
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator, bf16 stores
+// TMEM holds one 256-column accumulator and the scale slots.  Every wait is
+// bounded; on a timeout the kernel flags the status word and returns after
+// draining its copies and MMAs.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "epilogue.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128, BN = 256;
+constexpr int BKB = 128;  // K per stage in elements (= bytes): one 128-byte swizzle row
+constexpr int STAGES = 4;
+constexpr int kABytes = BM * BKB;        // 16 KB
+constexpr int kBBytes = BN * BKB;        // 32 KB
+constexpr int kSfBytes = 512 * 3;        // A atom + two B atoms
+constexpr int kStageBytes = kABytes + kBBytes;  // 48 KB: keeps every stage 1024-byte aligned
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;      // accumulator 0..255, scale slots from 256
+constexpr uint32_t kSfCol = 256, kSfSlotCols = 16;
+constexpr int kSmemBytes = STAGES * (kStageBytes + kSfBytes) + 1024 + 256 + 2 * (kMaxExperts + 1) * 4;
+
+enum MxMode : int { kMxDA = 0, kMxDX = 1, kMxDWDown = 2, kMxDWGateUp = 3 };
+
+struct MxParams {
+  int H, I, E;
+  int Mpad;                 // padded token count the token-axis operands were written with
+  const int32_t *offsets;   // [E+1] expert row offsets (unpadded)
+  const int32_t *pad_off;   // [E+1] padded offsets (multiples of 128)
+  const uint8_t *sfa0, *sfa1, *sfb0, *sfb1;  // scale atoms of the operands
+  const uint16_t *G, *U;
+  const float *w_row;
+  uint16_t *o0, *o1, *o2, *o3;
+  int32_t *status;
+  int n_tiles, m_tiles;
+};
+
+template <int MODE>
+struct MxTraits {
+  static constexpr bool kRaggedK = (MODE == kMxDWDown || MODE == kMxDWGateUp);
+  static constexpr int kEpi = MODE == kMxDA ? kBwdDA : MODE == kMxDX ? kBwdDX
+                              : MODE == kMxDWDown ? kBwdDWDown : kBwdDWGateUp;
+};
+
+// Block-scaled instruction descriptor: E4M3 x E4M3, fp32 D, UE8M0 scales,
+// scale-factor ids select the byte (K block within the 4-block word).
+__device__ __forceinline__ uint32_t idesc_mx(int sf_id) {
+  return (static_cast<uint32_t>(sf_id) << 4)       // B scale-factor id
+         | (static_cast<uint32_t>(BN >> 3) << 17)  // N / 8
+         | (1u << 23)                              // scale format: UE8M0
+         | (static_cast<uint32_t>(BM >> 4) << 24)  // M / 16
+         | (static_cast<uint32_t>(sf_id) << 29);   // A scale-factor id
+}
+
+__device__ __forceinline__ void tc_mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], "
+      "[%6], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
+// 32 rows x 16 bytes of scale atom (contiguous, no swizzle) into 4 TMEM columns,
+// replicated to all four lane quarters.
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, const void *smem_atom) {
+  uint64_t d = static_cast<uint64_t>((smem_addr(smem_atom) >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(1) << 16;    // leading byte offset (unused here) 16 B
+  d |= static_cast<uint64_t>(8) << 32;    // stride byte offset: 128 B per 8 rows
+  d |= 1ull << 46;                        // descriptor version
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(d) : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes,
+                                          uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool warp_wait_mx(uint64_t *bar, uint32_t parity, volatile int *abort) {
+  const int lane = threadIdx.x & 31;
+  int ok = 1;
+  if (lane == 0) ok = mbar_wait(bar, parity, abort) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok && lane != 0) {
+    for (int i = 0; i < (1 << 20) && !mbar_try_wait(bar, parity); ++i) {
+    }
+  }
+  return ok != 0;
+}
+
+struct MxTile {
+  Tile t;     // output placement (unpadded rows) for the shared epilogue
+  int arow;   // first row of A in its (padded) operand
+  int kb0;    // first 128-wide K block in the padded token axis (ragged K)
+};
+
+template <int MODE>
+__device__ __forceinline__ MxTile decode_mx(int tile, const MxParams &p, const int *s_off,
+                                            const int *s_pad) {
+  MxTile x;
+  Tile &t = x.t;
+  if constexpr (!MxTraits<MODE>::kRaggedK) {
+    const int mt_lin = tile / p.n_tiles, nt = tile % p.n_tiles;
+    const int prow = mt_lin * BM;  // padded row of the tile
+    int lo = 0, hi = p.E - 1;      // expert whose padded segment holds prow
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_pad[mid] <= prow)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    t.e = lo;
+    t.m0 = s_off[lo] + (prow - s_pad[lo]);
+    t.row_end = s_off[lo + 1];
+    t.n0 = nt * BN;
+    t.nkb = (MODE == kMxDA ? p.H : 2 * p.I) / BKB;
+    t.krow0 = 0;
+    t.kcount = 0;
+    x.arow = prow;
+    x.kb0 = 0;
+  } else {
+    const int per = p.m_tiles * p.n_tiles;
+    t.e = tile / per;
+    const int rem = tile % per;
+    t.m0 = (rem / p.n_tiles) * BM;
+    t.n0 = (rem % p.n_tiles) * (MODE == kMxDWGateUp ? BN / 2 : BN);  // B = [dG | dU] rows
+    t.krow0 = s_pad[t.e];
+    t.kcount = s_pad[t.e + 1] - s_pad[t.e];
+    t.nkb = t.kcount / BKB;  // padded: whole blocks, the rows past the expert's count are zero
+    t.row_end = 0;
+    x.arow = t.m0;
+    x.kb0 = t.krow0 / BKB;
+  }
+  return x;
+}
+
+// Scale atom of B rows [n0 + 128, n0 + 256) of a 256-row box: when those rows
+// lie past the operand's extent n (their output columns are never stored) the
+// first atom is loaded again, so no copy reads past the scale buffer.
+__device__ __forceinline__ size_t atom_hi(size_t atom_lo, int n0, int n) {
+  return n0 + 128 < n ? atom_lo + 1 : atom_lo;
+}
+
+template <int MODE>
+__device__ __forceinline__ void produce_mx(const MxTile &x, int kb, uint8_t *st, uint8_t *sf,
+                                           uint64_t *bar,
+                                           const MxParams &p, const CUtensorMap *a0,
+                                           const CUtensorMap *a1, const CUtensorMap *b0,
+                                           const CUtensorMap *b1) {
+  const Tile &t = x.t;
+  uint8_t *sa = st, *sb = st + kABytes;
+  if constexpr (MODE == kMxDA) {  // A = dy (padded rows, K = H); B = W_down rows e*I + n
+    const int K = p.H;
+    tma_load_2d(sa, a0, bar, kb * BKB, x.arow);
+    const int brow = t.e * p.I + t.n0;
+    tma_load_2d(sb, b0, bar, kb * BKB, brow);
+    bulk_load(sf, p.sfa0 + (static_cast<size_t>(x.arow / BM) * (K / 128) + kb) * 512, 512, bar);
+    const size_t b_lo = brow / BM, b_hi = atom_hi(b_lo, t.n0, p.I);
+    bulk_load(sf + 512, p.sfb0 + (b_lo * (K / 128) + kb) * 512, 512, bar);
+    bulk_load(sf + 1024, p.sfb0 + (b_hi * (K / 128) + kb) * 512, 512, bar);
+  } else if constexpr (MODE == kMxDX) {  // A = [dG | dU] (padded rows, K = I each); B = W_gate | W_up
+    const int K = p.I, kbi = p.I / BKB;
+    const bool first = kb < kbi;
+    const int k = first ? kb : kb - kbi;
+    const int brow = t.e * p.H + t.n0;
+    tma_load_2d(sa, first ? a0 : a1, bar, k * BKB, x.arow);
+    tma_load_2d(sb, first ? b0 : b1, bar, k * BKB, brow);
+    const uint8_t *sfa = first ? p.sfa0 : p.sfa1, *sfb = first ? p.sfb0 : p.sfb1;
+    bulk_load(sf, sfa + (static_cast<size_t>(x.arow / BM) * (K / 128) + k) * 512, 512, bar);
+    const size_t b_lo = brow / BM, b_hi = atom_hi(b_lo, t.n0, p.H);
+    bulk_load(sf + 512, sfb + (b_lo * (K / 128) + k) * 512, 512, bar);
+    bulk_load(sf + 1024, sfb + (b_hi * (K / 128) + k) * 512, 512, bar);
+  } else {  // ragged K: operands transposed, K = padded tokens
+    const int K = p.Mpad, kg = x.kb0 + kb;
+    tma_load_2d(sa, a0, bar, kg * BKB, x.arow);
+    bulk_load(sf, p.sfa0 + (static_cast<size_t>(x.arow / BM) * (K / 128) + kg) * 512, 512, bar);
+    if constexpr (MODE == kMxDWDown) {  // B = dy^T rows h
+      tma_load_2d(sb, b0, bar, kg * BKB, t.n0);
+      const size_t b_lo = t.n0 / BM, b_hi = atom_hi(b_lo, t.n0, p.H);
+      bulk_load(sf + 512, p.sfb0 + (b_lo * (K / 128) + kg) * 512, 512, bar);
+      bulk_load(sf + 1024, p.sfb0 + (b_hi * (K / 128) + kg) * 512, 512, bar);
+    } else {  // B = [dG^T rows i | dU^T rows i], 128 each
+      tma_load_2d(sb, b0, bar, kg * BKB, t.n0);
+      tma_load_2d(sb + kABytes, b1, bar, kg * BKB, t.n0);
+      bulk_load(sf + 512, p.sfb0 + (static_cast<size_t>(t.n0 / BM) * (K / 128) + kg) * 512, 512, bar);
+      bulk_load(sf + 1024, p.sfb1 + (static_cast<size_t>(t.n0 / BM) * (K / 128) + kg) * 512, 512, bar);
+    }
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA0,
+                           const __grid_constant__ CUtensorMap tmA1,
+                           const __grid_constant__ CUtensorMap tmB0,
+                           const __grid_constant__ CUtensorMap tmB1, const MxParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *stages = smem;                                  // [STAGES] A | B codes
+  uint8_t *sfs = smem + STAGES * kStageBytes;              // [STAGES] scale atoms
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sfs + STAGES * kSfBytes);
+  uint64_t *full = bars, *empty = bars + STAGES;
+  uint64_t *tfull = bars + 2 * STAGES, *tempty = tfull + 1, *drain = tempty + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  int *s_off = reinterpret_cast<int *>(sfs + STAGES * kSfBytes + 256);
+  int *s_pad = s_off + (kMaxExperts + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = p.E;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, 128);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA0);
+    tma_prefetch_desc(&tmA1);
+    tma_prefetch_desc(&tmB0);
+    tma_prefetch_desc(&tmB1);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  for (int e = threadIdx.x; e <= E; e += kThreads) {
+    s_off[e] = __ldg(p.offsets + e);
+    s_pad[e] = __ldg(p.pad_off + e);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = MxTraits<MODE>::kRaggedK ? E * p.m_tiles * p.n_tiles
+                                             : (s_pad[E] / BM) * p.n_tiles;
+  constexpr uint32_t kTx = kABytes + kBBytes + kSfBytes;
+
+  if (warp == 0) {
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t armed = 0, arm_par = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      const MxTile x = decode_mx<MODE>(tile, p, s_off, s_pad);
+      for (int kb = 0; kb < x.t.nkb; ++kb) {
+        if (!warp_wait_mx(&empty[stage], phase ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[stage], kTx);
+          produce_mx<MODE>(x, kb, stages + stage * kStageBytes, sfs + stage * kSfBytes,
+                           &full[stage], p, &tmA0, &tmA1, &tmB0, &tmB1);
+        }
+        armed |= 1u << stage;
+        arm_par = (arm_par & ~(1u << stage)) | (phase << stage);
+        __syncwarp();
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    if (*abort_flag && lane == 0) {
+      for (int s = 0; s < STAGES; ++s) {
+        if (!((armed >> s) & 1u)) continue;
+        for (int i = 0; i < (1 << 22) && !mbar_try_wait(&full[s], (arm_par >> s) & 1u); ++i) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    int stage = 0;
+    uint32_t phase = 0;
+    int it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+      const MxTile x = decode_mx<MODE>(tile, p, s_off, s_pad);
+      if (!warp_wait_mx(tempty, (it & 1) ^ 1, abort_flag)) break;  // single accumulator
+      tc_fence_after();
+      if (x.t.nkb == 0) {
+        if (lane == 0) mbar_arrive(tfull);
+        __syncwarp();
+        continue;
+      }
+      for (int kb = 0; kb < x.t.nkb; ++kb) {
+        if (!warp_wait_mx(&full[stage], phase, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          uint8_t *st = stages + stage * kStageBytes;
+          uint8_t *sf = sfs + stage * kSfBytes;
+          const uint32_t slot = tmem_base + kSfCol + kSfSlotCols * stage;
+          tc_cp_sf(slot, sf);            // A scales: columns slot .. slot+3
+          tc_cp_sf(slot + 4, sf + 512);  // B rows 0..127: slot+4 .. slot+7
+          tc_cp_sf(slot + 8, sf + 1024); // B rows 128..255: slot+8 .. slot+11
+          const uint32_t a_base = smem_addr(st), b_base = smem_addr(st + kABytes);
+#pragma unroll
+          for (int k32 = 0; k32 < BKB / 32; ++k32) {
+            const uint64_t adesc = smem_desc_sw128(a_base + k32 * 32, 16, 1024);
+            const uint64_t bdesc = smem_desc_sw128(b_base + k32 * 32, 16, 1024);
+            tc_mma_mx(tmem_base, adesc, bdesc, idesc_mx(k32), slot, slot + 4,
+                      (kb | k32) != 0 ? 1u : 0u);
+          }
+          tc_commit(&empty[stage]);
+        }
+        __syncwarp();
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) tc_commit(tfull);
+      __syncwarp();
+    }
+    if (*abort_flag && lane == 0) {
+      tc_commit(drain);
+      for (int i = 0; i < (1 << 22) && !mbar_try_wait(drain, 0); ++i) {
+      }
+    }
+  } else {
+    const int q = warp & 3;
+    const int rit = q * 32 + lane;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+      const MxTile x = decode_mx<MODE>(tile, p, s_off, s_pad);
+      if (!warp_wait_mx(tfull, it & 1, abort_flag)) break;
+      tc_fence_after();
+      epilogue_tile<MxTraits<MODE>::kEpi>(x.t, tmem_base + (static_cast<uint32_t>(q * 32) << 16),
+                                          rit, p);
+      tc_fence_before();
+      mbar_arrive(tempty);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) flag_status(p.status, kDevWaitTimeout);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// 2-D byte tensor map over row-major [rows, inner] codes, box {128, box_rows}.
+bool make_map_u8(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  auto fn = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder());
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MODE>
+cudaError_t launch_mx_mode(const MxGemmArgs &a, cudaStream_t s) {
+  CUtensorMap mA0, mA1, mB0, mB1;
+  MxParams p{};
+  p.H = a.H;
+  p.I = a.I;
+  p.E = a.E;
+  p.Mpad = a.Mpad;
+  p.offsets = a.offsets;
+  p.pad_off = a.pad_off;
+  p.G = a.G;
+  p.U = a.U;
+  p.w_row = a.w_row;
+  p.o0 = a.o0;
+  p.o1 = a.o1;
+  p.status = a.status;
+  const uint64_t H = a.H, I = a.I, E = a.E, Mp = a.Mpad;
+  bool ok = true;
+  switch (MODE) {
+    case kMxDA:
+      ok = make_map_u8(&mA0, a.a0, H, Mp, BM) && make_map_u8(&mB0, a.b0, H, E * I, BN);
+      mA1 = mA0;
+      mB1 = mB0;
+      p.sfa0 = a.sfa0;
+      p.sfb0 = a.sfb0;
+      p.n_tiles = (a.I + BN - 1) / BN;
+      break;
+    case kMxDX:
+      ok = make_map_u8(&mA0, a.a0, I, Mp, BM) && make_map_u8(&mA1, a.a1, I, Mp, BM) &&
+           make_map_u8(&mB0, a.b0, I, E * H, BN) && make_map_u8(&mB1, a.b1, I, E * H, BN);
+      p.sfa0 = a.sfa0;
+      p.sfa1 = a.sfa1;
+      p.sfb0 = a.sfb0;
+      p.sfb1 = a.sfb1;
+      p.n_tiles = (a.H + BN - 1) / BN;
+      break;
+    case kMxDWDown:
+      ok = make_map_u8(&mA0, a.a0, Mp, I, BM) && make_map_u8(&mB0, a.b0, Mp, H, BN);
+      mA1 = mA0;
+      mB1 = mB0;
+      p.sfa0 = a.sfa0;
+      p.sfb0 = a.sfb0;
+      p.m_tiles = (a.I + BM - 1) / BM;
+      p.n_tiles = (a.H + BN - 1) / BN;
+      break;
+    default:  // kMxDWGateUp
+      ok = make_map_u8(&mA0, a.a0, Mp, H, BM) && make_map_u8(&mB0, a.b0, Mp, I, BM) &&
+           make_map_u8(&mB1, a.b1, Mp, I, BM);
+      mA1 = mA0;
+      p.sfa0 = a.sfa0;
+      p.sfb0 = a.sfb0;
+      p.sfb1 = a.sfb1;
+      p.o1 = a.o1;
+      p.m_tiles = (a.H + BM - 1) / BM;
+      p.n_tiles = (a.I + BN / 2 - 1) / (BN / 2);
+      break;
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_mx_kernel<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  grouped_gemm_mx_kernel<MODE><<<a.num_sms, kThreads, kSmemBytes, s>>>(mA0, mA1, mB0, mB1, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_mx_gemm(int mode, const MxGemmArgs &a, cudaStream_t s) {
+  switch (mode) {
+    case 0: return launch_mx_mode<kMxDA>(a, s);
+    case 1: return launch_mx_mode<kMxDX>(a, s);
+    case 2: return launch_mx_mode<kMxDWDown>(a, s);
+    case 3: return launch_mx_mode<kMxDWGateUp>(a, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

@@ -84,6 +84,33 @@ constexpr size_t kExpertMapBytes = 3 * 128;  // per expert
 cudaError_t launch_grouped_gemm(GemmMode mode, const GemmArgs &a, cudaStream_t s);
 const char *gemm_mode_name(GemmMode mode);
 
+// ---- MXFP8 backward (mxfp8.cu, gemm_mx.cu)
+// pad_off[e] = sum over e' < e of ceil(count/128)*128
+cudaError_t launch_pad_offsets(const int32_t *offsets, int E, int32_t *pad_off, cudaStream_t s);
+// rows along K (K % 128 == 0): dense (offsets == nullptr, rows_out input rows) or
+// into the padded per-expert row space (rows_out = padded row capacity)
+cudaError_t launch_quant_rows(const uint16_t *src, int rows_out, int K, const int32_t *offsets,
+                              const int32_t *pad_off, int E, uint8_t *codes, uint8_t *sf,
+                              cudaStream_t s);
+// along tokens: [M, C] permuted rows -> codes [C, Mpad] (padded token axis)
+cudaError_t launch_quant_cols(const uint16_t *src, int C, int Mpad, const int32_t *offsets,
+                              const int32_t *pad_off, int E, uint8_t *codes, uint8_t *sf,
+                              cudaStream_t s);
+
+enum MxGemmMode : int { kMxGemmDA = 0, kMxGemmDX = 1, kMxGemmDWDown = 2, kMxGemmDWGateUp = 3 };
+struct MxGemmArgs {
+  int H, I, E, Mpad;
+  const int32_t *offsets, *pad_off;
+  const uint8_t *a0, *a1, *b0, *b1;          // E4M3 codes
+  const uint8_t *sfa0, *sfa1, *sfb0, *sfb1;  // scale atoms
+  const uint16_t *G, *U;
+  const float *w_row;
+  uint16_t *o0, *o1;
+  int32_t *status;
+  int num_sms;
+};
+cudaError_t launch_mx_gemm(int mode, const MxGemmArgs &a, cudaStream_t s);
+
 // driver entry point for tensor-map encoding (api.cu)
 void *tensor_map_encoder();
 

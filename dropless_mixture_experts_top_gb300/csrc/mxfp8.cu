@@ -1,0 +1,213 @@
+// mxfp8.cu -- MXFP8 quantisers for the fp8_bwd backward (E4M3 values, one
+// UE8M0 power-of-two scale per 32 consecutive elements along a GEMM's K).
+//
+// MXFP8 block scaling on Blackwell and group-aware quantisation are named in
+// the NVIDIA MoE article ("Que optimizaciones especificas exige el MoE sin
+// descartes": MXFP8 group quantisation, MXFP8 grouped GEMM); the fp8_bwd mode
+// (BF16 forward, FP8 backward) in the Prime Mega MoE write-ups.
+//
+// Scale rule: the smallest power of two 2^X with amax / 2^X <= 448, so no
+// element of a block saturates; X is clamped to [-127, 127] and stored as the
+// E8M0 code X + 127; an all-zero block gets code 0.  Values are scaled by 2^-X
+// (exact) and converted with CUDA's round-to-nearest-even, saturating E4M3
+// conversion.
+//
+// Output layouts are what the block-scaled tensor-core GEMM loads:
+//   codes  K-major: [rows][K] bytes;
+//   scales in 512-byte atoms, one per (128 rows, 128 K): atom (rb, kg) at
+//          ((rb * (K / 128)) + kg) * 512, holding the scale of row rb*128 +
+//          32 q + l and K block kg*4 + j at byte l*16 + q*4 + j -- the layout
+//          tcgen05.cp.32x128b.warpx4 copies into tensor memory for the MMA.
+// Ragged operands are written in a per-expert padded row space: expert e's
+// rows start at pad_off[e] = sum over e' < e of ceil(count/128)*128, the rows
+// past its count are zero codes with zero scales, so every 128-row tile and
+// every 32-element block along tokens starts inside one expert.
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+// E8M0 exponent of a block's scale from its (finite, non-negative) amax.
+__device__ __forceinline__ int mx_scale_exp(float amax) {
+  const uint32_t b = __float_as_uint(amax);
+  const int eb = static_cast<int>((b >> 23) & 0xFF);
+  if (amax <= 0.f) return -127;
+  if (eb == 0) return -127;  // below 2^-126: far under the smallest E4M3 step of any scale
+  int X = (eb - 127) - 8;    // amax = m 2^(eb-127), m in [1,2); 448 = 1.75 2^8
+  if ((b & 0x7FFFFFu) > 0x600000u) X += 1;  // m > 1.75
+  return X < -127 ? -127 : (X > 127 ? 127 : X);
+}
+
+__device__ __forceinline__ float pow2_neg(int X) {  // 2^-X for X in [-127, 126]
+  return __uint_as_float(static_cast<uint32_t>(127 - X) << 23);
+}
+
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  const uint32_t x0 = __nv_cvt_float_to_fp8(a, __NV_SATFINITE, __NV_E4M3);
+  const uint32_t x1 = __nv_cvt_float_to_fp8(b, __NV_SATFINITE, __NV_E4M3);
+  const uint32_t x2 = __nv_cvt_float_to_fp8(c, __NV_SATFINITE, __NV_E4M3);
+  const uint32_t x3 = __nv_cvt_float_to_fp8(d, __NV_SATFINITE, __NV_E4M3);
+  return x0 | (x1 << 8) | (x2 << 16) | (x3 << 24);
+}
+
+// Quantise 32 values held in registers; writes 32 code bytes; returns the E8M0 code.
+__device__ __forceinline__ uint8_t quant32(const float (&v)[32], uint4 *dst) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const int X = mx_scale_exp(amax);
+  const float s = pow2_neg(X);  // exact; an all-zero block stays zero
+  uint32_t w[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    w[q] = pack_e4m3x4(v[4 * q] * s, v[4 * q + 1] * s, v[4 * q + 2] * s, v[4 * q + 3] * s);
+  dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  return static_cast<uint8_t>(X + 127);
+}
+
+__device__ __forceinline__ size_t atom_byte(int row, int kblock, int K) {
+  const int rb = row >> 7, r = row & 127, kg = kblock >> 2;
+  return (static_cast<size_t>(rb) * (K >> 7) + kg) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (kblock & 3);
+}
+
+// Expert of padded row o (largest e with pad_off[e] <= o), from shared memory.
+__device__ __forceinline__ int expert_of(int o, const int *s_pad, int E) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_pad[mid] <= o)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+// One thread per (output row, 32-element block).  Rows are either the input
+// rows themselves (dense: weights) or the padded per-expert row space.
+__global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t *__restrict__ src, int K,
+                                                         int rows_out,
+                                                         const int32_t *__restrict__ offsets,
+                                                         const int32_t *__restrict__ pad_off, int E,
+                                                         uint8_t *__restrict__ codes,
+                                                         uint8_t *__restrict__ sf) {
+  __shared__ int s_off[kMaxExperts + 1], s_pad[kMaxExperts + 1];
+  if (offsets) {
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+      s_off[e] = __ldg(offsets + e);
+      s_pad[e] = __ldg(pad_off + e);
+    }
+    __syncthreads();
+  }
+  const int nb = K >> 5;
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<int64_t>(rows_out) * nb) return;
+  const int o = static_cast<int>(idx / nb), b = static_cast<int>(idx % nb);
+  int in_row = o;
+  if (offsets) {
+    const int e = expert_of(o, s_pad, E);
+    const int local = o - s_pad[e];
+    in_row = local < s_off[e + 1] - s_off[e] ? s_off[e] + local : -1;
+  }
+  float v[32];
+  if (in_row >= 0) {
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(src + static_cast<size_t>(in_row) * K + 32 * b);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 w = __ldg(s4 + q);
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        v[8 * q + 2 * h] = bf16_lo(ww[h]);
+        v[8 * q + 2 * h + 1] = bf16_hi(ww[h]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+  }
+  sf[atom_byte(o, b, K)] =
+      quant32(v, reinterpret_cast<uint4 *>(codes + static_cast<size_t>(o) * K + 32 * b));
+}
+
+// Token-axis quantisation: one thread per (column c, 32-token block of the
+// padded space).  Output is transposed: codes [C][Mpad] (tokens contiguous).
+__global__ void __launch_bounds__(256) quant_cols_kernel(const uint16_t *__restrict__ src, int C,
+                                                         int Mpad,
+                                                         const int32_t *__restrict__ offsets,
+                                                         const int32_t *__restrict__ pad_off, int E,
+                                                         uint8_t *__restrict__ codes,
+                                                         uint8_t *__restrict__ sf) {
+  __shared__ int s_off[kMaxExperts + 1], s_pad[kMaxExperts + 1];
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    s_off[e] = __ldg(offsets + e);
+    s_pad[e] = __ldg(pad_off + e);
+  }
+  __syncthreads();
+  const int nb = Mpad >> 5;
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<int64_t>(C) * nb) return;
+  const int c = static_cast<int>(idx % C), b = static_cast<int>(idx / C);  // columns fastest
+  const int o0 = 32 * b;
+  const int e = expert_of(o0, s_pad, E);
+  const int local0 = o0 - s_pad[e], count = s_off[e + 1] - s_off[e];
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int local = local0 + i;
+    v[i] = local < count ? __uint_as_float(static_cast<uint32_t>(src[static_cast<size_t>(s_off[e] + local) * C + c]) << 16)
+                         : 0.f;
+  }
+  sf[atom_byte(c, b, Mpad)] =
+      quant32(v, reinterpret_cast<uint4 *>(codes + static_cast<size_t>(c) * Mpad + o0));
+}
+
+// pad_off[e] = sum over e' < e of ceil(count/128)*128; pad_off[E] = padded total.
+__global__ void __launch_bounds__(32) pad_offsets_kernel(const int32_t *__restrict__ offsets, int E,
+                                                         int32_t *__restrict__ pad_off) {
+  const int lane = threadIdx.x;
+  int carry = 0;
+  for (int base = 0; base < E; base += 32) {
+    const int e = base + lane;
+    const int c = e < E ? ((offsets[e + 1] - offsets[e] + 127) / 128) * 128 : 0;
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (e < E) pad_off[e] = carry + incl - c;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) pad_off[E] = carry;
+}
+
+}  // namespace
+
+cudaError_t launch_pad_offsets(const int32_t *offsets, int E, int32_t *pad_off, cudaStream_t s) {
+  pad_offsets_kernel<<<1, 32, 0, s>>>(offsets, E, pad_off);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_rows(const uint16_t *src, int rows_out, int K, const int32_t *offsets,
+                              const int32_t *pad_off, int E, uint8_t *codes, uint8_t *sf,
+                              cudaStream_t s) {
+  const int64_t n = static_cast<int64_t>(rows_out) * (K / 32);
+  quant_rows_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(src, K, rows_out, offsets,
+                                                                            pad_off, E, codes, sf);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_cols(const uint16_t *src, int C, int Mpad, const int32_t *offsets,
+                              const int32_t *pad_off, int E, uint8_t *codes, uint8_t *sf,
+                              cudaStream_t s) {
+  const int64_t n = static_cast<int64_t>(C) * (Mpad / 32);
+  quant_cols_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(src, C, Mpad, offsets,
+                                                                            pad_off, E, codes, sf);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

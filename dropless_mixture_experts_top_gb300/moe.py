@@ -25,8 +25,8 @@ DEV_WAIT_TIMEOUT = 0x2
 _lib = None
 
 EXPORTED = [
-    "moe_query_workspace", "moe_saved_offsets", "moe_route", "moe_forward", "moe_backward",
-    "moe_get_device_status", "moe_status_string", "moe_timing_attach", "moe_timing_count",
+    "moe_query_workspace", "moe_saved_offsets", "moe_fp8_scratch_offsets", "moe_route",
+    "moe_forward", "moe_backward", "moe_get_device_status", "moe_status_string", "moe_timing_attach", "moe_timing_count",
     "moe_timing_label",
 ]
 
@@ -43,6 +43,13 @@ class Routing(ctypes.Structure):
 
 class SavedLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in ("x_perm", "G", "U", "A", "Y", "A_w")]
+
+
+class Fp8Layout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in (
+        "m_pad", "pad_offsets", "dy_q", "dy_sf", "wd_q", "wd_sf", "dg_q", "dg_sf", "du_q", "du_sf",
+        "wg_q", "wg_sf", "wu_q", "wu_sf", "aw_t", "aw_t_sf", "dy_t", "dy_t_sf", "x_t", "x_t_sf",
+        "dg_t", "dg_t_sf", "du_t", "du_t_sf")]
 
 
 class MoEError(RuntimeError):
@@ -66,6 +73,7 @@ def lib():
         P, sz = ctypes.c_void_p, ctypes.c_size_t
         L.moe_query_workspace.argtypes = [P, P, P, P, P]
         L.moe_saved_offsets.argtypes = [P, P]
+        L.moe_fp8_scratch_offsets.argtypes = [P, P]
         L.moe_route.argtypes = [P, P, P, P, sz, P]
         L.moe_forward.argtypes = [P, P, P, P, P, P, P, P, sz, P, sz, P]
         L.moe_backward.argtypes = [P, P, P, P, P, P, P, P, sz, P, P, P, P, P, P, P, sz, P]
@@ -77,7 +85,7 @@ def lib():
         L.moe_timing_count.restype = ctypes.c_int32
         L.moe_timing_label.argtypes = [ctypes.c_int32]
         L.moe_timing_label.restype = ctypes.c_char_p
-        for f in ("moe_query_workspace", "moe_saved_offsets", "moe_route", "moe_forward", "moe_backward",
+        for f in ("moe_query_workspace", "moe_saved_offsets", "moe_fp8_scratch_offsets", "moe_route", "moe_forward", "moe_backward",
                   "moe_get_device_status", "moe_timing_attach"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
@@ -119,6 +127,13 @@ def saved_offsets(cfg: Config) -> dict:
     lay = SavedLayout()
     _check(lib().moe_saved_offsets(ctypes.byref(cfg), ctypes.byref(lay)), "moe_saved_offsets")
     return {n: int(getattr(lay, n)) for n, _ in SavedLayout._fields_}
+
+
+def fp8_scratch_offsets(cfg: Config) -> dict:
+    lay = Fp8Layout()
+    _check(lib().moe_fp8_scratch_offsets(ctypes.byref(cfg), ctypes.byref(lay)),
+           "moe_fp8_scratch_offsets")
+    return {n: int(getattr(lay, n)) for n, _ in Fp8Layout._fields_}
 
 
 def make_routing(r: dict) -> Routing:
@@ -221,6 +236,26 @@ class MoELayer:
         off = self.saved_offsets[name]
         n = T * k * cols
         return self.saved[off:off + 2 * n].view(torch.int16).view(T * k, cols)
+
+    def fp8_tensor(self, name):
+        """A quantised operand left in the backward scratch (fp8_bwd only): uint8
+        codes [rows, K] for *_q and *_t, the raw scale-atom bytes for *_sf, int32
+        [E+1] for pad_offsets."""
+        lay = fp8_scratch_offsets(self.cfg)
+        s = self.shape
+        Mp = lay["m_pad"]
+        rows_k = {"dy_q": (Mp, s.H), "wd_q": (s.E * s.I, s.H), "dg_q": (Mp, s.I), "du_q": (Mp, s.I),
+                  "wg_q": (s.E * s.H, s.I), "wu_q": (s.E * s.H, s.I), "aw_t": (s.I, Mp),
+                  "dy_t": (s.H, Mp), "x_t": (s.H, Mp), "dg_t": (s.I, Mp), "du_t": (s.I, Mp)}
+        off = lay[name]
+        if name == "pad_offsets":
+            return self.bwd_scratch[off:off + 4 * (s.E + 1)].view(torch.int32)
+        if name.endswith("_sf"):
+            base = name[:-3] + "_q" if name[:-3] + "_q" in rows_k else name[:-3]
+            R, K = rows_k[base]
+            return self.bwd_scratch[off:off + R * K // 32]
+        R, K = rows_k[name]
+        return self.bwd_scratch[off:off + R * K].view(R, K)
 
     def route(self, logits, stream=None):
         route(self.cfg, logits, self.routing, self.route_scratch, stream)

@@ -33,7 +33,8 @@
  *     IEEE bfloat16 bit patterns.
  *   - Every device pointer must be 16-byte aligned.
  *   - Shapes: T >= 0, H % 64 == 0 and I % 64 == 0 (both >= 64), 1 <= E <= 256,
- *     1 <= k <= min(E, 16), T * k < 2^31.
+ *     1 <= k <= min(E, 16), T * k < 2^31; with MOE_PREC_FP8_BWD also
+ *     H % 128 == 0 and I % 128 == 0.
  *   - Errors found on the host (null pointer, bad shape, misalignment, a
  *     too-small workspace) return a negative moe_status with nothing launched.
  *     Anomalies found on the device (non-finite logits, a pipeline wait that
@@ -108,6 +109,27 @@ typedef struct {
   size_t x_perm, G, U, A, Y, A_w;
 } moe_saved_layout;
 moe_status moe_saved_offsets(const moe_config *cfg, moe_saved_layout *layout);
+
+/* MOE_PREC_FP8_BWD only: byte offsets, inside moe_backward's scratch, of the
+ * MXFP8 operands it writes, for inspection after the call.  m_pad is the padded
+ * token capacity (a multiple of 128): expert e's rows start at padded row
+ * pad_offsets[e] = sum over e' < e of ceil(count/128)*128 (int32 [E+1]); rows
+ * past an expert's count are zero codes with zero scale codes.
+ *   *_q     E4M3 codes, K-major: dy_q [m_pad,H] (padded rows), wd_q [E*I,H],
+ *           dg_q/du_q [m_pad,I], wg_q/wu_q [E*H,I];
+ *   *_t     token-axis operands transposed, tokens contiguous: aw_t (w*A) and
+ *           dg_t/du_t [I,m_pad], dy_t and x_t [H,m_pad];
+ *   *_sf    their UE8M0 scale codes (2^(code-127)), one per 32 elements along
+ *           K, in 512-byte atoms: for R rows and K columns the scale of row r,
+ *           K-block b sits at byte ((r/128)*(K/128) + b/4)*512 + (r%32)*16 +
+ *           ((r%128)/32)*4 + b%4 -- the order the tensor core reads them.
+ * Returns MOE_ERR_INVALID_ARG for other precisions or unsupported shapes. */
+typedef struct {
+  size_t m_pad, pad_offsets;
+  size_t dy_q, dy_sf, wd_q, wd_sf, dg_q, dg_sf, du_q, du_sf, wg_q, wg_sf, wu_q, wu_sf;
+  size_t aw_t, aw_t_sf, dy_t, dy_t_sf, x_t, x_t_sf, dg_t, dg_t_sf, du_t, du_t_sf;
+} moe_fp8_layout;
+moe_status moe_fp8_scratch_offsets(const moe_config *cfg, moe_fp8_layout *layout);
 
 /* Router and dispatch indices.  logits: device fp32 [T,E].  Writes every field
  * of *routing.  Per-expert counts, the scan and the permutation are computed

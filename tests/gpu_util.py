@@ -2,8 +2,9 @@
 inputs and compare with the fp64 oracle.
 
 Tolerances (floating point): relative L2 <= 5e-3 and max |diff| <= 2e-2 *
-max |ref| for bf16 outputs and gradients; router weights within 1e-6; integer
-routing and permutation bit-exact.
+max |ref| for bf16 outputs and gradients; 1e-2 and 5e-2 for the MXFP8 backward
+(fp8_bwd) gradients dx, dW_*, against the oracle's quantised backward; router
+weights within 1e-6; integer routing and permutation bit-exact.
 """
 import json
 import os
@@ -18,6 +19,13 @@ from oracle import oracle as O
 REL_L2 = 5e-3
 MAX_REL = 2e-2
 W_ATOL = 1e-6
+# fp8_bwd backward outputs against the oracle's quantised backward.  Both sides
+# decide every E4M3 code on the same bf16 tensors, so what remains is the bf16
+# rounding of the outputs and fp32 accumulation, as in the bf16 path, plus the
+# rare code that lands one step apart (one E4M3 step is 6-12% of an element)
+# where fp32 evaluation order moves a bf16 value across a rounding boundary.
+FP8_REL_L2 = 1e-2
+FP8_MAX_REL = 5e-2
 
 
 def to_dev(inp, dev="cuda"):
@@ -97,7 +105,7 @@ def check_full(shape, inp, layer, out, grads, precision="bf16", check_saved=True
                                    inp["W_down"], inp["dy"], quant=quant)
     dWg, dWu, dWd = O.dw_full(shape, inp["x"], idx, w, inp["W_gate"], inp["W_up"], inp["W_down"],
                               inp["dy"], quant=quant)
-    tol = dict(rel_l2=5e-2 if quant else REL_L2)
+    tol = dict(rel_l2=FP8_REL_L2, max_rel=FP8_MAX_REL) if quant else {}
     close("d_logits", grads["d_logits"].cpu().numpy(), dl)
     close("d_topk_w", grads["d_topk_w"].cpu().numpy(), gd)
     close("dx", bf(grads["dx"]), dx, **tol)

@@ -108,3 +108,31 @@ def test_status_strings(L):
         assert len(moe.status_string(code)) >= 2
     assert moe.status_string(-99) == "unknown status"
     assert L.moe_timing_count() == 0
+
+
+def test_fp8_shapes_and_layout(L):
+    # fp8_bwd stages K in 128-byte blocks: H and I multiples of 128
+    sz = ctypes.c_size_t()
+    for H, I in ((192, 128), (128, 192)):
+        assert L.moe_query_workspace(ctypes.byref(cfg(H=H, I=I, prec=1)), ctypes.byref(sz), None, None,
+                                     None) == -1
+    lay = moe.Fp8Layout()
+    assert L.moe_fp8_scratch_offsets(ctypes.byref(cfg(I=128)), ctypes.byref(lay)) == -1  # bf16 config
+    c = cfg(T=300, H=256, I=128, E=8, k=2, prec=1)
+    q = moe.fp8_scratch_offsets(c)
+    M, E, H, I = 600, 8, 256, 128
+    Mp = q["m_pad"]
+    assert Mp % 128 == 0 and Mp >= M + 127 * E
+    sizes = {"pad_offsets": 4 * (E + 1), "dy_q": Mp * H, "wd_q": E * I * H, "dg_q": Mp * I, "du_q": Mp * I,
+             "wg_q": E * H * I, "wu_q": E * H * I, "aw_t": I * Mp, "dy_t": H * Mp, "x_t": H * Mp,
+             "dg_t": I * Mp, "du_t": I * Mp}
+    for n in list(sizes):
+        if n != "pad_offsets":
+            sizes[(n[:-2] if n.endswith("_q") else n) + "_sf"] = sizes[n] // 32
+    spans = sorted((q[n], q[n] + b, n) for n, b in sizes.items())
+    for (a0, a1, n0), (b0, b1, n1) in zip(spans, spans[1:]):
+        assert a1 <= b0, (n0, n1)  # disjoint
+    assert all(q[n] % 256 == 0 for n in sizes)
+    _, _, _, bs = moe.query_workspace(c)
+    _, _, _, bs16 = moe.query_workspace(cfg(T=300, H=256, I=128, E=8, k=2, prec=0))
+    assert spans[0][0] >= bs16 - 256 and spans[-1][1] <= bs

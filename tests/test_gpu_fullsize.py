@@ -16,8 +16,8 @@ from tests import gpu_util as G
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
-BF16_WORKLOADS = ["qwen3_30b_a3b_layer_t16384", "qwen3_30b_a3b_layer_t16384_zipf",
-                  "qwen3_235b_a22b_layer_t16384"]
+WORKLOADS = ["qwen3_30b_a3b_layer_t16384", "qwen3_30b_a3b_layer_t16384_zipf",
+             "qwen3_235b_a22b_layer_t16384", "qwen3_30b_a3b_layer_t16384_fp8_bwd"]
 
 
 def sample_tokens(T, counts, idx, rng, n=64):
@@ -59,9 +59,12 @@ def run_workload(name):
     return w, shape, inp, layer, out, grads
 
 
-@pytest.mark.parametrize("name", BF16_WORKLOADS)
+@pytest.mark.parametrize("name", WORKLOADS)
 def test_fullsize_sampled_parity(name):
     w, shape, inp, layer, out, grads = run_workload(name)
+    quant = w.precision == "fp8_bwd"
+    tol = dict(rel_l2=G.FP8_REL_L2, max_rel=G.FP8_MAX_REL) if quant else {}
+    qW = O.quant_weights(inp["W_gate"], inp["W_up"], inp["W_down"]) if quant else None
     idx, wts, counts, offsets, ros, sor = G.check_routing(shape, inp, layer)
     assert counts.sum() == shape.T * shape.k
     if w.routing == "zipf":
@@ -71,14 +74,14 @@ def test_fullsize_sampled_parity(name):
     ref_out = O.forward(shape, inp["x"], idx, wts, inp["W_gate"], inp["W_up"], inp["W_down"], tokens=toks)
     G.close("out[sampled tokens]", G.bf(out[torch.from_numpy(toks).cuda()]), ref_out)
     dx, dl, gd = O.backward_tokens(shape, inp["x"], inp["logits"], idx, wts, inp["W_gate"], inp["W_up"],
-                                   inp["W_down"], inp["dy"], tokens=toks)
+                                   inp["W_down"], inp["dy"], tokens=toks, quant=quant, qW=qW)
     tk = torch.from_numpy(toks).cuda()
-    G.close("dx[sampled tokens]", G.bf(grads["dx"][tk]), dx)
+    G.close("dx[sampled tokens]", G.bf(grads["dx"][tk]), dx, **tol)
     G.close("d_logits[sampled tokens]", grads["d_logits"][tk].cpu().numpy(), dl)
     G.close("d_topk_w[sampled tokens]", grads["d_topk_w"][tk].cpu().numpy(), gd)
     which, ee, rr, cc, uni = sample_dw(shape, counts, rng)
     ref = O.dw_elements(shape, inp["x"], idx, wts, inp["W_gate"], inp["W_up"], inp["W_down"], inp["dy"],
-                        which, ee, rr, cc)
+                        which, ee, rr, cc, quant=quant, qW=qW)
     names = ["dW_gate", "dW_up", "dW_down"]
     for wh in range(3):
         m = which == wh
@@ -86,8 +89,8 @@ def test_fullsize_sampled_parity(name):
         got = G.bf(t[torch.from_numpy(ee[m]).long().cuda(), torch.from_numpy(rr[m]).long().cuda(),
                      torch.from_numpy(cc[m]).long().cuda()])
         u = uni[m]
-        G.close(f"{names[wh]}[uniform sample]", got[u], ref[m][u])
-        bound = G.MAX_REL * np.abs(ref[m]).max()
+        G.close(f"{names[wh]}[uniform sample]", got[u], ref[m][u], **tol)
+        bound = (G.FP8_MAX_REL if quant else G.MAX_REL) * np.abs(ref[m]).max()
         worst = np.abs(got[~u] - ref[m][~u]).max()
         assert worst <= bound, f"{names[wh]}[edge elements]: max|diff| {worst:.3e} > {bound:.3e}"
     for e in np.flatnonzero(counts == 0):
