@@ -257,10 +257,10 @@ moe_status backward_fp8(const Fp8Bwd &f, cudaStream_t s) {
   m.status = f.status;
   m.num_sms = f.sms;
   // dA = w (Q(dy) . Q(W_down)^T), K = H; dSwiGLU epilogue -> dG, dU
-  MOE_TRY(timed("mx_quant_rows", s, [&] {
+  MOE_TRY(timed("mx_quant_dy", s, [&] {
     return launch_quant_rows(f.dy_perm, Mp, H, off, pad_off, E, sc + q.dy_q, sc + q.dy_sf, s);
   }));
-  MOE_TRY(timed("mx_quant_rows", s, [&] {
+  MOE_TRY(timed("mx_quant_W_down", s, [&] {
     return launch_quant_rows(f.W_down, E * I, H, nullptr, nullptr, E, sc + q.wd_q, sc + q.wd_sf, s);
   }));
   m.a0 = sc + q.dy_q;
@@ -271,16 +271,16 @@ moe_status backward_fp8(const Fp8Bwd &f, cudaStream_t s) {
   m.o1 = f.dU;
   MOE_TRY(timed("mx_gemm_dA_dswiglu", s, [&] { return launch_mx_gemm(kMxGemmDA, m, s); }));
   // dX = Q(dG) . Q(W_gate)^T + Q(dU) . Q(W_up)^T, K = I
-  MOE_TRY(timed("mx_quant_rows", s, [&] {
+  MOE_TRY(timed("mx_quant_dG", s, [&] {
     return launch_quant_rows(f.dG, Mp, I, off, pad_off, E, sc + q.dg_q, sc + q.dg_sf, s);
   }));
-  MOE_TRY(timed("mx_quant_rows", s, [&] {
+  MOE_TRY(timed("mx_quant_dU", s, [&] {
     return launch_quant_rows(f.dU, Mp, I, off, pad_off, E, sc + q.du_q, sc + q.du_sf, s);
   }));
-  MOE_TRY(timed("mx_quant_rows", s, [&] {
+  MOE_TRY(timed("mx_quant_W_gate", s, [&] {
     return launch_quant_rows(f.W_gate, E * H, I, nullptr, nullptr, E, sc + q.wg_q, sc + q.wg_sf, s);
   }));
-  MOE_TRY(timed("mx_quant_rows", s, [&] {
+  MOE_TRY(timed("mx_quant_W_up", s, [&] {
     return launch_quant_rows(f.W_up, E * H, I, nullptr, nullptr, E, sc + q.wu_q, sc + q.wu_sf, s);
   }));
   m.a0 = sc + q.dg_q;
@@ -298,10 +298,10 @@ moe_status backward_fp8(const Fp8Bwd &f, cudaStream_t s) {
     return launch_gather_sum(f.dX, f.r->row_of_slot, nullptr, f.dx, T, H, k, s);
   }));
   // dW_down = Q(w a)^T . Q(dy), K = the expert's tokens
-  MOE_TRY(timed("mx_quant_cols", s, [&] {
+  MOE_TRY(timed("mx_quantT_A_w", s, [&] {
     return launch_quant_cols(f.A_w, I, Mp, off, pad_off, E, sc + q.aw_t, sc + q.aw_t_sf, s);
   }));
-  MOE_TRY(timed("mx_quant_cols", s, [&] {
+  MOE_TRY(timed("mx_quantT_dy", s, [&] {
     return launch_quant_cols(f.dy_perm, H, Mp, off, pad_off, E, sc + q.dy_t, sc + q.dy_t_sf, s);
   }));
   m.a0 = sc + q.aw_t;
@@ -312,13 +312,13 @@ moe_status backward_fp8(const Fp8Bwd &f, cudaStream_t s) {
   m.o0 = f.dW_down;
   MOE_TRY(timed("mx_gemm_dW_down", s, [&] { return launch_mx_gemm(kMxGemmDWDown, m, s); }));
   // dW_gate = Q(x)^T . Q(dG), dW_up = Q(x)^T . Q(dU), K = the expert's tokens
-  MOE_TRY(timed("mx_quant_cols", s, [&] {
+  MOE_TRY(timed("mx_quantT_x", s, [&] {
     return launch_quant_cols(f.x_perm, H, Mp, off, pad_off, E, sc + q.x_t, sc + q.x_t_sf, s);
   }));
-  MOE_TRY(timed("mx_quant_cols", s, [&] {
+  MOE_TRY(timed("mx_quantT_dG", s, [&] {
     return launch_quant_cols(f.dG, I, Mp, off, pad_off, E, sc + q.dg_t, sc + q.dg_t_sf, s);
   }));
-  MOE_TRY(timed("mx_quant_cols", s, [&] {
+  MOE_TRY(timed("mx_quantT_dU", s, [&] {
     return launch_quant_cols(f.dU, I, Mp, off, pad_off, E, sc + q.du_t, sc + q.du_t_sf, s);
   }));
   m.a0 = sc + q.x_t;
