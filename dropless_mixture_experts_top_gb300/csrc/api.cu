@@ -61,6 +61,12 @@ bool shape_ok(const moe_config *c) {
 // up to a multiple of 128 fit in M + 127 E, itself rounded up to 128.
 inline size_t fp8_mpad(size_t M, size_t E) { return ((M + 127 * E + 127) / 128) * 128; }
 
+// Scale-atom row grouping: A operands in plain 128-row blocks; B operands (the
+// GEMMs' N side) in 192-row groups restarting at every `seg` rows (an expert's
+// rows of a weight, or the whole transposed operand).
+inline SfLayout sf_a(size_t rows) { return SfLayout{static_cast<int>(rows), 128}; }
+inline SfLayout sf_b(size_t seg) { return SfLayout{static_cast<int>(seg), kMxBN}; }
+
 Layout layout_of(const moe_config *c) {
   Layout L{};
   const size_t T = c->T, H = c->H, I = c->I, E = c->E, k = c->k, M = T * k;
@@ -112,25 +118,25 @@ Layout layout_of(const moe_config *c) {
     q.dy_q = take(Mp * H);
     q.dy_sf = take(Mp * H / 32);
     q.wd_q = take(E * I * H);
-    q.wd_sf = take(E * I * H / 32);
+    q.wd_sf = take(sf_layout_bytes(E * I, H, sf_b(I)));
     q.dg_q = take(Mp * I);
     q.dg_sf = take(Mp * I / 32);
     q.du_q = take(Mp * I);
     q.du_sf = take(Mp * I / 32);
     q.wg_q = take(E * H * I);
-    q.wg_sf = take(E * H * I / 32);
+    q.wg_sf = take(sf_layout_bytes(E * H, I, sf_b(H)));
     q.wu_q = take(E * H * I);
-    q.wu_sf = take(E * H * I / 32);
+    q.wu_sf = take(sf_layout_bytes(E * H, I, sf_b(H)));
     q.aw_t = take(I * Mp);
     q.aw_t_sf = take(I * Mp / 32);
     q.dy_t = take(H * Mp);
-    q.dy_t_sf = take(H * Mp / 32);
+    q.dy_t_sf = take(sf_layout_bytes(H, Mp, sf_b(H)));
     q.x_t = take(H * Mp);
     q.x_t_sf = take(H * Mp / 32);
     q.dg_t = take(I * Mp);
-    q.dg_t_sf = take(I * Mp / 32);
+    q.dg_t_sf = take(sf_layout_bytes(I, Mp, sf_b(I)));
     q.du_t = take(I * Mp);
-    q.du_t_sf = take(I * Mp / 32);
+    q.du_t_sf = take(sf_layout_bytes(I, Mp, sf_b(I)));
   }
   L.b_total = o;
   return L;
@@ -258,10 +264,11 @@ moe_status backward_fp8(const Fp8Bwd &f, cudaStream_t s) {
   m.num_sms = f.sms;
   // dA = w (Q(dy) . Q(W_down)^T), K = H; dSwiGLU epilogue -> dG, dU
   MOE_TRY(timed("mx_quant_dy", s, [&] {
-    return launch_quant_rows(f.dy_perm, Mp, H, off, pad_off, E, sc + q.dy_q, sc + q.dy_sf, s);
+    return launch_quant_rows(f.dy_perm, Mp, H, off, pad_off, E, sc + q.dy_q, sc + q.dy_sf, sf_a(Mp), s);
   }));
   MOE_TRY(timed("mx_quant_W_down", s, [&] {
-    return launch_quant_rows(f.W_down, E * I, H, nullptr, nullptr, E, sc + q.wd_q, sc + q.wd_sf, s);
+    return launch_quant_rows(f.W_down, E * I, H, nullptr, nullptr, E, sc + q.wd_q, sc + q.wd_sf,
+                             sf_b(I), s);
   }));
   m.a0 = sc + q.dy_q;
   m.sfa0 = sc + q.dy_sf;
@@ -272,16 +279,18 @@ moe_status backward_fp8(const Fp8Bwd &f, cudaStream_t s) {
   MOE_TRY(timed("mx_gemm_dA_dswiglu", s, [&] { return launch_mx_gemm(kMxGemmDA, m, s); }));
   // dX = Q(dG) . Q(W_gate)^T + Q(dU) . Q(W_up)^T, K = I
   MOE_TRY(timed("mx_quant_dG", s, [&] {
-    return launch_quant_rows(f.dG, Mp, I, off, pad_off, E, sc + q.dg_q, sc + q.dg_sf, s);
+    return launch_quant_rows(f.dG, Mp, I, off, pad_off, E, sc + q.dg_q, sc + q.dg_sf, sf_a(Mp), s);
   }));
   MOE_TRY(timed("mx_quant_dU", s, [&] {
-    return launch_quant_rows(f.dU, Mp, I, off, pad_off, E, sc + q.du_q, sc + q.du_sf, s);
+    return launch_quant_rows(f.dU, Mp, I, off, pad_off, E, sc + q.du_q, sc + q.du_sf, sf_a(Mp), s);
   }));
   MOE_TRY(timed("mx_quant_W_gate", s, [&] {
-    return launch_quant_rows(f.W_gate, E * H, I, nullptr, nullptr, E, sc + q.wg_q, sc + q.wg_sf, s);
+    return launch_quant_rows(f.W_gate, E * H, I, nullptr, nullptr, E, sc + q.wg_q, sc + q.wg_sf,
+                             sf_b(H), s);
   }));
   MOE_TRY(timed("mx_quant_W_up", s, [&] {
-    return launch_quant_rows(f.W_up, E * H, I, nullptr, nullptr, E, sc + q.wu_q, sc + q.wu_sf, s);
+    return launch_quant_rows(f.W_up, E * H, I, nullptr, nullptr, E, sc + q.wu_q, sc + q.wu_sf,
+                             sf_b(H), s);
   }));
   m.a0 = sc + q.dg_q;
   m.sfa0 = sc + q.dg_sf;
@@ -299,10 +308,11 @@ moe_status backward_fp8(const Fp8Bwd &f, cudaStream_t s) {
   }));
   // dW_down = Q(w a)^T . Q(dy), K = the expert's tokens
   MOE_TRY(timed("mx_quantT_A_w", s, [&] {
-    return launch_quant_cols(f.A_w, I, Mp, off, pad_off, E, sc + q.aw_t, sc + q.aw_t_sf, s);
+    return launch_quant_cols(f.A_w, I, Mp, off, pad_off, E, sc + q.aw_t, sc + q.aw_t_sf, sf_a(I), s);
   }));
   MOE_TRY(timed("mx_quantT_dy", s, [&] {
-    return launch_quant_cols(f.dy_perm, H, Mp, off, pad_off, E, sc + q.dy_t, sc + q.dy_t_sf, s);
+    return launch_quant_cols(f.dy_perm, H, Mp, off, pad_off, E, sc + q.dy_t, sc + q.dy_t_sf, sf_b(H),
+                             s);
   }));
   m.a0 = sc + q.aw_t;
   m.sfa0 = sc + q.aw_t_sf;
@@ -313,13 +323,13 @@ moe_status backward_fp8(const Fp8Bwd &f, cudaStream_t s) {
   MOE_TRY(timed("mx_gemm_dW_down", s, [&] { return launch_mx_gemm(kMxGemmDWDown, m, s); }));
   // dW_gate = Q(x)^T . Q(dG), dW_up = Q(x)^T . Q(dU), K = the expert's tokens
   MOE_TRY(timed("mx_quantT_x", s, [&] {
-    return launch_quant_cols(f.x_perm, H, Mp, off, pad_off, E, sc + q.x_t, sc + q.x_t_sf, s);
+    return launch_quant_cols(f.x_perm, H, Mp, off, pad_off, E, sc + q.x_t, sc + q.x_t_sf, sf_a(H), s);
   }));
   MOE_TRY(timed("mx_quantT_dG", s, [&] {
-    return launch_quant_cols(f.dG, I, Mp, off, pad_off, E, sc + q.dg_t, sc + q.dg_t_sf, s);
+    return launch_quant_cols(f.dG, I, Mp, off, pad_off, E, sc + q.dg_t, sc + q.dg_t_sf, sf_b(I), s);
   }));
   MOE_TRY(timed("mx_quantT_dU", s, [&] {
-    return launch_quant_cols(f.dU, I, Mp, off, pad_off, E, sc + q.du_t, sc + q.du_t_sf, s);
+    return launch_quant_cols(f.dU, I, Mp, off, pad_off, E, sc + q.du_t, sc + q.du_t_sf, sf_b(I), s);
   }));
   m.a0 = sc + q.x_t;
   m.sfa0 = sc + q.x_t_sf;

@@ -35,8 +35,9 @@ __device__ __forceinline__ void store32_bf16(uint16_t *dst, const float (&v)[32]
 __device__ __forceinline__ float sigmoidf_(float z) { return 1.f / (1.f + __expf(-z)); }
 
 // Epilogue of one tile for one warp (32 rows).  tb: TMEM address of this
-// warp's lanes at the accumulator's first column.
-template <int MODE, class P>
+// warp's lanes at the accumulator's first column.  NCH: 32-column chunks in
+// the tile's unpaired accumulator (8 for 256 columns, 6 for 192).
+template <int MODE, class P, int NCH = 8>
 __device__ __forceinline__ void epilogue_tile(const Tile &t, uint32_t tb, int rit, const P &p) {
   uint32_t r0[32], r1[32];
   float v0[32], v1[32], v2[32];
@@ -70,7 +71,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, uint32_t tb, int ri
   } else if constexpr (MODE == kFwdDown || MODE == kBwdDX) {
     const int row = t.m0 + rit;
     const bool rv = row < t.row_end;
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 0; c < NCH; ++c) {
       const int col = t.n0 + 32 * c;
       if (col >= p.H) break;
       tmem_ld32(tb + 32 * c, r0);
@@ -95,10 +96,10 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, uint32_t tb, int ri
         uq[q] = __ldg(reinterpret_cast<const uint4 *>(p.U + rowoff + t.n0) + q);
       }
     }
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 0; c < NCH; ++c) {
       const int col = t.n0 + 32 * c;
       if (col >= p.I) break;
-      const bool next = c + 1 < 8 && col + 32 < p.I;
+      const bool next = c + 1 < NCH && col + 32 < p.I;
       if (rv && next) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -140,7 +141,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, uint32_t tb, int ri
   } else if constexpr (MODE == kBwdDWDown) {
     const int i_row = t.m0 + rit;
     const bool rv = i_row < p.I;
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 0; c < NCH; ++c) {
       const int col = t.n0 + 32 * c;
       if (col >= p.H) break;
       if (t.nkb > 0) {

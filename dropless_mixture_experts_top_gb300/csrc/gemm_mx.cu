@@ -9,17 +9,19 @@
 // rows are zeros).  Outputs are bf16 and go through the same epilogues as the
 // bf16 engine (dSwiGLU for dA).
 //
-// One CTA per SM, persistent, static round-robin over 128 x 256 tiles:
+// One CTA per SM, persistent, static round-robin over 128 x 192 tiles:
 //   warp 0      producer: TMA boxes of codes (128-byte swizzle) and bulk copies
-//               of the scale atoms into a 4-stage ring
+//               of the scale atoms into a 5-stage ring
 //   warp 1      MMA issuer: per stage, tcgen05.cp of the scale atoms into a
 //               tensor-memory slot (32x128b.warpx4: row r's four block scales
 //               land in lane r%32, column r/32), then four K=32 MMAs selecting
 //               the block's scale byte with the descriptor's scale-factor ids
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator, bf16 stores
-// TMEM holds one 256-column accumulator and the scale slots.  Every wait is
-// bounded; on a timeout the kernel flags the status word and returns after
-// draining its copies and MMAs.
+// TMEM holds two 192-column accumulators (the epilogue of one tile overlaps
+// the MMAs of the next) and a ring of scale slots.  B-operand scales are
+// grouped per 192 rows (two atoms, the second half used) so every tile's
+// scales start on an atom.  Every wait is bounded; on a timeout the kernel
+// flags the status word and returns after draining its copies and MMAs.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -28,17 +30,20 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128, BN = 256;
-constexpr int BKB = 128;  // K per stage in elements (= bytes): one 128-byte swizzle row
-constexpr int STAGES = 4;
-constexpr int kABytes = BM * BKB;        // 16 KB
-constexpr int kBBytes = BN * BKB;        // 32 KB
-constexpr int kSfBytes = 512 * 3;        // A atom + two B atoms
-constexpr int kStageBytes = kABytes + kBBytes;  // 48 KB: keeps every stage 1024-byte aligned
+constexpr int BM = 128, BN = kMxBN;  // 128 x 192 tiles
+constexpr int BKB = 128;             // K per stage in elements (= bytes): one 128-byte swizzle row
+constexpr int STAGES = 5;
+constexpr int kABytes = BM * BKB;    // 16 KB
+constexpr int kBBytes = BN * BKB;    // 24 KB
+constexpr int kSfBytes = 512 * 3;    // A atom + two B atoms
+constexpr int kStageBytes = kABytes + kBBytes;  // 40 KB: keeps every stage 1024-byte aligned
 constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 512;      // accumulator 0..255, scale slots from 256
-constexpr uint32_t kSfCol = 256, kSfSlotCols = 16;
-constexpr int kSmemBytes = STAGES * (kStageBytes + kSfBytes) + 1024 + 256 + 2 * (kMaxExperts + 1) * 4;
+constexpr uint32_t kTmemCols = 512;  // accumulators at 0 and BN, scale slots from 2*BN
+constexpr uint32_t kSfCol = 2 * BN, kSfSlotCols = 16;
+constexpr int kSmemBytes =
+    STAGES * (kStageBytes + kSfBytes) + 1024 + 256 + 2 * (kMaxExperts + 1) * 4;
+static_assert(kSfCol + STAGES * kSfSlotCols <= kTmemCols, "TMEM budget");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 enum MxMode : int { kMxDA = 0, kMxDX = 1, kMxDWDown = 2, kMxDWGateUp = 3 };
 
@@ -50,16 +55,26 @@ struct MxParams {
   const uint8_t *sfa0, *sfa1, *sfb0, *sfb1;  // scale atoms of the operands
   const uint16_t *G, *U;
   const float *w_row;
-  uint16_t *o0, *o1, *o2, *o3;
+  uint16_t *o0, *o1;
   int32_t *status;
   int n_tiles, m_tiles;
+  int b_gps;  // B scales: 192-row groups per segment
+};
+
+// What the shared epilogue reads: the layer's sizes and buffers, or for the
+// weight gradients of W_gate / W_up a [H rows, I columns] view of one of them.
+struct EpiView {
+  int H, I;
+  const uint16_t *G, *U;
+  const float *w_row;
+  uint16_t *o0, *o1, *o2, *o3;
 };
 
 template <int MODE>
 struct MxTraits {
   static constexpr bool kRaggedK = (MODE == kMxDWDown || MODE == kMxDWGateUp);
-  static constexpr int kEpi = MODE == kMxDA ? kBwdDA : MODE == kMxDX ? kBwdDX
-                              : MODE == kMxDWDown ? kBwdDWDown : kBwdDWGateUp;
+  // dW_gate and dW_up tiles use the dW_down epilogue on a transposed view
+  static constexpr int kEpi = MODE == kMxDA ? kBwdDA : MODE == kMxDX ? kBwdDX : kBwdDWDown;
 };
 
 // Block-scaled instruction descriptor: E4M3 x E4M3, fp32 D, UE8M0 scales,
@@ -116,9 +131,11 @@ __device__ __forceinline__ bool warp_wait_mx(uint64_t *bar, uint32_t parity, vol
 }
 
 struct MxTile {
-  Tile t;     // output placement (unpadded rows) for the shared epilogue
-  int arow;   // first row of A in its (padded) operand
-  int kb0;    // first 128-wide K block in the padded token axis (ragged K)
+  Tile t;       // output placement (unpadded rows) for the shared epilogue
+  int arow;     // first row of A in its (padded) operand
+  int kb0;      // first 128-wide K block in the padded token axis (ragged K)
+  int mat;      // dW_gate/up: 0 = gate, 1 = up
+  size_t bsf;   // row block of the first of the tile's two B scale atoms
 };
 
 template <int MODE>
@@ -126,6 +143,7 @@ __device__ __forceinline__ MxTile decode_mx(int tile, const MxParams &p, const i
                                             const int *s_pad) {
   MxTile x;
   Tile &t = x.t;
+  x.mat = 0;
   if constexpr (!MxTraits<MODE>::kRaggedK) {
     const int mt_lin = tile / p.n_tiles, nt = tile % p.n_tiles;
     const int prow = mt_lin * BM;  // padded row of the tile
@@ -146,74 +164,69 @@ __device__ __forceinline__ MxTile decode_mx(int tile, const MxParams &p, const i
     t.kcount = 0;
     x.arow = prow;
     x.kb0 = 0;
+    x.bsf = (static_cast<size_t>(lo) * p.b_gps + nt) * 2;  // B rows of expert lo, group nt
   } else {
+    if (MODE == kMxDWGateUp) {  // gate and up tiles of the same (e, m, n) are adjacent
+      x.mat = tile & 1;
+      tile >>= 1;
+    }
     const int per = p.m_tiles * p.n_tiles;
     t.e = tile / per;
     const int rem = tile % per;
+    const int nt = rem % p.n_tiles;
     t.m0 = (rem / p.n_tiles) * BM;
-    t.n0 = (rem % p.n_tiles) * (MODE == kMxDWGateUp ? BN / 2 : BN);  // B = [dG | dU] rows
+    t.n0 = nt * BN;
     t.krow0 = s_pad[t.e];
     t.kcount = s_pad[t.e + 1] - s_pad[t.e];
     t.nkb = t.kcount / BKB;  // padded: whole blocks, the rows past the expert's count are zero
     t.row_end = 0;
     x.arow = t.m0;
     x.kb0 = t.krow0 / BKB;
+    x.bsf = static_cast<size_t>(nt) * 2;  // one segment: the whole transposed operand
   }
   return x;
 }
 
-// Scale atom of B rows [n0 + 128, n0 + 256) of a 256-row box: when those rows
-// lie past the operand's extent n (their output columns are never stored) the
-// first atom is loaded again, so no copy reads past the scale buffer.
-__device__ __forceinline__ size_t atom_hi(size_t atom_lo, int n0, int n) {
-  return n0 + 128 < n ? atom_lo + 1 : atom_lo;
-}
-
+// One stage: A codes (128 rows), B codes (192 rows), the A scale atom and the
+// two B scale atoms of K block kb.
 template <int MODE>
 __device__ __forceinline__ void produce_mx(const MxTile &x, int kb, uint8_t *st, uint8_t *sf,
-                                           uint64_t *bar,
-                                           const MxParams &p, const CUtensorMap *a0,
-                                           const CUtensorMap *a1, const CUtensorMap *b0,
-                                           const CUtensorMap *b1) {
+                                           uint64_t *bar, const MxParams &p,
+                                           const CUtensorMap *a0, const CUtensorMap *a1,
+                                           const CUtensorMap *b0, const CUtensorMap *b1) {
   const Tile &t = x.t;
   uint8_t *sa = st, *sb = st + kABytes;
+  const uint8_t *sfa, *sfb;
+  int K, k;
   if constexpr (MODE == kMxDA) {  // A = dy (padded rows, K = H); B = W_down rows e*I + n
-    const int K = p.H;
-    tma_load_2d(sa, a0, bar, kb * BKB, x.arow);
-    const int brow = t.e * p.I + t.n0;
-    tma_load_2d(sb, b0, bar, kb * BKB, brow);
-    bulk_load(sf, p.sfa0 + (static_cast<size_t>(x.arow / BM) * (K / 128) + kb) * 512, 512, bar);
-    const size_t b_lo = brow / BM, b_hi = atom_hi(b_lo, t.n0, p.I);
-    bulk_load(sf + 512, p.sfb0 + (b_lo * (K / 128) + kb) * 512, 512, bar);
-    bulk_load(sf + 1024, p.sfb0 + (b_hi * (K / 128) + kb) * 512, 512, bar);
+    K = p.H;
+    k = kb;
+    tma_load_2d(sa, a0, bar, k * BKB, x.arow);
+    tma_load_2d(sb, b0, bar, k * BKB, t.e * p.I + t.n0);
+    sfa = p.sfa0;
+    sfb = p.sfb0;
   } else if constexpr (MODE == kMxDX) {  // A = [dG | dU] (padded rows, K = I each); B = W_gate | W_up
-    const int K = p.I, kbi = p.I / BKB;
+    K = p.I;
+    const int kbi = p.I / BKB;
     const bool first = kb < kbi;
-    const int k = first ? kb : kb - kbi;
-    const int brow = t.e * p.H + t.n0;
+    k = first ? kb : kb - kbi;
     tma_load_2d(sa, first ? a0 : a1, bar, k * BKB, x.arow);
-    tma_load_2d(sb, first ? b0 : b1, bar, k * BKB, brow);
-    const uint8_t *sfa = first ? p.sfa0 : p.sfa1, *sfb = first ? p.sfb0 : p.sfb1;
-    bulk_load(sf, sfa + (static_cast<size_t>(x.arow / BM) * (K / 128) + k) * 512, 512, bar);
-    const size_t b_lo = brow / BM, b_hi = atom_hi(b_lo, t.n0, p.H);
-    bulk_load(sf + 512, sfb + (b_lo * (K / 128) + k) * 512, 512, bar);
-    bulk_load(sf + 1024, sfb + (b_hi * (K / 128) + k) * 512, 512, bar);
+    tma_load_2d(sb, first ? b0 : b1, bar, k * BKB, t.e * p.H + t.n0);
+    sfa = first ? p.sfa0 : p.sfa1;
+    sfb = first ? p.sfb0 : p.sfb1;
   } else {  // ragged K: operands transposed, K = padded tokens
-    const int K = p.Mpad, kg = x.kb0 + kb;
-    tma_load_2d(sa, a0, bar, kg * BKB, x.arow);
-    bulk_load(sf, p.sfa0 + (static_cast<size_t>(x.arow / BM) * (K / 128) + kg) * 512, 512, bar);
-    if constexpr (MODE == kMxDWDown) {  // B = dy^T rows h
-      tma_load_2d(sb, b0, bar, kg * BKB, t.n0);
-      const size_t b_lo = t.n0 / BM, b_hi = atom_hi(b_lo, t.n0, p.H);
-      bulk_load(sf + 512, p.sfb0 + (b_lo * (K / 128) + kg) * 512, 512, bar);
-      bulk_load(sf + 1024, p.sfb0 + (b_hi * (K / 128) + kg) * 512, 512, bar);
-    } else {  // B = [dG^T rows i | dU^T rows i], 128 each
-      tma_load_2d(sb, b0, bar, kg * BKB, t.n0);
-      tma_load_2d(sb + kABytes, b1, bar, kg * BKB, t.n0);
-      bulk_load(sf + 512, p.sfb0 + (static_cast<size_t>(t.n0 / BM) * (K / 128) + kg) * 512, 512, bar);
-      bulk_load(sf + 1024, p.sfb1 + (static_cast<size_t>(t.n0 / BM) * (K / 128) + kg) * 512, 512, bar);
-    }
+    K = p.Mpad;
+    k = x.kb0 + kb;
+    tma_load_2d(sa, a0, bar, k * BKB, x.arow);
+    const bool up = MODE == kMxDWGateUp && x.mat;
+    tma_load_2d(sb, up ? b1 : b0, bar, k * BKB, t.n0);  // dy^T (dW_down) or dG^T / dU^T rows
+    sfa = p.sfa0;
+    sfb = up ? p.sfb1 : p.sfb0;
   }
+  const size_t kblocks = static_cast<size_t>(K / 128);
+  bulk_load(sf, sfa + (static_cast<size_t>(x.arow / BM) * kblocks + k) * 512, 512, bar);
+  bulk_load(sf + 512, sfb + (x.bsf * kblocks + k) * 512, 512, bar);
+  bulk_load(sf + 1024, sfb + ((x.bsf + 1) * kblocks + k) * 512, 512, bar);
 }
 
 template <int MODE>
@@ -229,7 +242,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *sfs = smem + STAGES * kStageBytes;              // [STAGES] scale atoms
   uint64_t *bars = reinterpret_cast<uint64_t *>(sfs + STAGES * kSfBytes);
   uint64_t *full = bars, *empty = bars + STAGES;
-  uint64_t *tfull = bars + 2 * STAGES, *tempty = tfull + 1, *drain = tempty + 1;
+  uint64_t *tfull = bars + 2 * STAGES;  // [2] accumulator ready
+  uint64_t *tempty = tfull + 2;         // [2] accumulator drained by the epilogue
+  uint64_t *drain = tempty + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *s_off = reinterpret_cast<int *>(sfs + STAGES * kSfBytes + 256);
@@ -242,8 +257,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(tfull, 1);
-    mbar_init(tempty, 128);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 128);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -263,11 +280,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int total = MxTraits<MODE>::kRaggedK ? E * p.m_tiles * p.n_tiles
-                                             : (s_pad[E] / BM) * p.n_tiles;
+  const int total = MODE == kMxDWGateUp ? 2 * E * p.m_tiles * p.n_tiles
+                    : MODE == kMxDWDown ? E * p.m_tiles * p.n_tiles
+                                        : (s_pad[E] / BM) * p.n_tiles;
   constexpr uint32_t kTx = kABytes + kBBytes + kSfBytes;
 
   if (warp == 0) {
+    // ---------------------------------------------------------------- producer
     int stage = 0;
     uint32_t phase = 0;
     uint32_t armed = 0, arm_par = 0;
@@ -293,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (*abort_flag && lane == 0) {
+    if (*abort_flag && lane == 0) {  // let the copies in flight land before the CTA exits
       for (int s = 0; s < STAGES; ++s) {
         if (!((armed >> s) & 1u)) continue;
         for (int i = 0; i < (1 << 22) && !mbar_try_wait(&full[s], (arm_par >> s) & 1u); ++i) {
@@ -301,16 +320,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
     int stage = 0;
     uint32_t phase = 0;
     int it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
       const MxTile x = decode_mx<MODE>(tile, p, s_off, s_pad);
-      if (!warp_wait_mx(tempty, (it & 1) ^ 1, abort_flag)) break;  // single accumulator
+      const int buf = it & 1;
+      const uint32_t use = (it >> 1) & 1;
+      if (!warp_wait_mx(&tempty[buf], use ^ 1, abort_flag)) break;
       tc_fence_after();
-      if (x.t.nkb == 0) {
-        if (lane == 0) mbar_arrive(tfull);
+      const uint32_t d_tmem = tmem_base + buf * BN;
+      if (x.t.nkb == 0) {  // empty expert: the epilogue writes zeros
+        if (lane == 0) mbar_arrive(&tfull[buf]);
         __syncwarp();
         continue;
       }
@@ -324,15 +347,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t *st = stages + stage * kStageBytes;
           uint8_t *sf = sfs + stage * kSfBytes;
           const uint32_t slot = tmem_base + kSfCol + kSfSlotCols * stage;
-          tc_cp_sf(slot, sf);            // A scales: columns slot .. slot+3
-          tc_cp_sf(slot + 4, sf + 512);  // B rows 0..127: slot+4 .. slot+7
-          tc_cp_sf(slot + 8, sf + 1024); // B rows 128..255: slot+8 .. slot+11
+          tc_cp_sf(slot, sf);             // A scales: columns slot .. slot+3
+          tc_cp_sf(slot + 4, sf + 512);   // B rows 0..127: slot+4 .. slot+7
+          tc_cp_sf(slot + 8, sf + 1024);  // B rows 128..191: slot+8, slot+9
           const uint32_t a_base = smem_addr(st), b_base = smem_addr(st + kABytes);
 #pragma unroll
           for (int k32 = 0; k32 < BKB / 32; ++k32) {
             const uint64_t adesc = smem_desc_sw128(a_base + k32 * 32, 16, 1024);
             const uint64_t bdesc = smem_desc_sw128(b_base + k32 * 32, 16, 1024);
-            tc_mma_mx(tmem_base, adesc, bdesc, idesc_mx(k32), slot, slot + 4,
+            tc_mma_mx(d_tmem, adesc, bdesc, idesc_mx(k32), slot, slot + 4,
                       (kb | k32) != 0 ? 1u : 0u);
           }
           tc_commit(&empty[stage]);
@@ -344,26 +367,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      if (lane == 0) tc_commit(tfull);
+      if (lane == 0) tc_commit(&tfull[buf]);
       __syncwarp();
     }
-    if (*abort_flag && lane == 0) {
+    if (*abort_flag && lane == 0) {  // wait for issued MMAs before TMEM is freed
       tc_commit(drain);
       for (int i = 0; i < (1 << 22) && !mbar_try_wait(drain, 0); ++i) {
       }
     }
   } else {
-    const int q = warp & 3;
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int rit = q * 32 + lane;
     int it = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
       const MxTile x = decode_mx<MODE>(tile, p, s_off, s_pad);
-      if (!warp_wait_mx(tfull, it & 1, abort_flag)) break;
+      const int buf = it & 1;
+      const uint32_t use = (it >> 1) & 1;
+      if (!warp_wait_mx(&tfull[buf], use, abort_flag)) break;
       tc_fence_after();
-      epilogue_tile<MxTraits<MODE>::kEpi>(x.t, tmem_base + (static_cast<uint32_t>(q * 32) << 16),
-                                          rit, p);
+      EpiView v{p.H, p.I, p.G, p.U, p.w_row, p.o0, p.o1, nullptr, nullptr};
+      if (MODE == kMxDWGateUp) {  // [H rows, I columns] of dW_gate or dW_up
+        v.H = p.I;
+        v.I = p.H;
+        v.o0 = x.mat ? p.o1 : p.o0;
+        v.o1 = nullptr;
+      }
+      epilogue_tile<MxTraits<MODE>::kEpi, EpiView, BN / 32>(
+          x.t, tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16), rit, v);
       tc_fence_before();
-      mbar_arrive(tempty);
+      mbar_arrive(&tempty[buf]);
     }
   }
 
@@ -394,6 +427,8 @@ bool make_map_u8(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t rows,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+inline int cdiv(int a, int b) { return (a + b - 1) / b; }
+
 template <int MODE>
 cudaError_t launch_mx_mode(const MxGemmArgs &a, cudaStream_t s) {
   CUtensorMap mA0, mA1, mB0, mB1;
@@ -410,45 +445,37 @@ cudaError_t launch_mx_mode(const MxGemmArgs &a, cudaStream_t s) {
   p.o0 = a.o0;
   p.o1 = a.o1;
   p.status = a.status;
+  p.sfa0 = a.sfa0;
+  p.sfa1 = a.sfa1;
+  p.sfb0 = a.sfb0;
+  p.sfb1 = a.sfb1;
   const uint64_t H = a.H, I = a.I, E = a.E, Mp = a.Mpad;
   bool ok = true;
   switch (MODE) {
-    case kMxDA:
+    case kMxDA:  // [Mp, H] x [E*I, H]^T
       ok = make_map_u8(&mA0, a.a0, H, Mp, BM) && make_map_u8(&mB0, a.b0, H, E * I, BN);
       mA1 = mA0;
       mB1 = mB0;
-      p.sfa0 = a.sfa0;
-      p.sfb0 = a.sfb0;
-      p.n_tiles = (a.I + BN - 1) / BN;
+      p.n_tiles = p.b_gps = cdiv(a.I, BN);
       break;
-    case kMxDX:
+    case kMxDX:  // [Mp, I] x [E*H, I]^T, twice
       ok = make_map_u8(&mA0, a.a0, I, Mp, BM) && make_map_u8(&mA1, a.a1, I, Mp, BM) &&
            make_map_u8(&mB0, a.b0, I, E * H, BN) && make_map_u8(&mB1, a.b1, I, E * H, BN);
-      p.sfa0 = a.sfa0;
-      p.sfa1 = a.sfa1;
-      p.sfb0 = a.sfb0;
-      p.sfb1 = a.sfb1;
-      p.n_tiles = (a.H + BN - 1) / BN;
+      p.n_tiles = p.b_gps = cdiv(a.H, BN);
       break;
-    case kMxDWDown:
+    case kMxDWDown:  // per expert: [I, tokens] x [H, tokens]^T
       ok = make_map_u8(&mA0, a.a0, Mp, I, BM) && make_map_u8(&mB0, a.b0, Mp, H, BN);
       mA1 = mA0;
       mB1 = mB0;
-      p.sfa0 = a.sfa0;
-      p.sfb0 = a.sfb0;
-      p.m_tiles = (a.I + BM - 1) / BM;
-      p.n_tiles = (a.H + BN - 1) / BN;
+      p.m_tiles = a.I / BM;
+      p.n_tiles = p.b_gps = cdiv(a.H, BN);
       break;
-    default:  // kMxDWGateUp
-      ok = make_map_u8(&mA0, a.a0, Mp, H, BM) && make_map_u8(&mB0, a.b0, Mp, I, BM) &&
-           make_map_u8(&mB1, a.b1, Mp, I, BM);
+    default:  // kMxDWGateUp, per expert: [H, tokens] x [I, tokens]^T for dG and for dU
+      ok = make_map_u8(&mA0, a.a0, Mp, H, BM) && make_map_u8(&mB0, a.b0, Mp, I, BN) &&
+           make_map_u8(&mB1, a.b1, Mp, I, BN);
       mA1 = mA0;
-      p.sfa0 = a.sfa0;
-      p.sfb0 = a.sfb0;
-      p.sfb1 = a.sfb1;
-      p.o1 = a.o1;
-      p.m_tiles = (a.H + BM - 1) / BM;
-      p.n_tiles = (a.I + BN / 2 - 1) / (BN / 2);
+      p.m_tiles = a.H / BM;
+      p.n_tiles = p.b_gps = cdiv(a.I, BN);
       break;
   }
   if (!ok) return cudaErrorInvalidValue;
@@ -470,10 +497,10 @@ cudaError_t launch_mx_mode(const MxGemmArgs &a, cudaStream_t s) {
 
 cudaError_t launch_mx_gemm(int mode, const MxGemmArgs &a, cudaStream_t s) {
   switch (mode) {
-    case 0: return launch_mx_mode<kMxDA>(a, s);
-    case 1: return launch_mx_mode<kMxDX>(a, s);
-    case 2: return launch_mx_mode<kMxDWDown>(a, s);
-    case 3: return launch_mx_mode<kMxDWGateUp>(a, s);
+    case kMxGemmDA: return launch_mx_mode<kMxDA>(a, s);
+    case kMxGemmDX: return launch_mx_mode<kMxDX>(a, s);
+    case kMxGemmDWDown: return launch_mx_mode<kMxDWDown>(a, s);
+    case kMxGemmDWGateUp: return launch_mx_mode<kMxDWGateUp>(a, s);
   }
   return cudaErrorInvalidValue;
 }

@@ -85,16 +85,28 @@ cudaError_t launch_grouped_gemm(GemmMode mode, const GemmArgs &a, cudaStream_t s
 const char *gemm_mode_name(GemmMode mode);
 
 // ---- MXFP8 backward (mxfp8.cu, gemm_mx.cu)
+// Row grouping of a scale-atom buffer: segments of `seg` rows, each cut into
+// groups of `group` rows (128, or kMxBN for B operands), each group spanning
+// ceil(group/128) 128-row atoms.
+constexpr int kMxBN = 192;  // N extent of an MXFP8 GEMM tile
+struct SfLayout {
+  int seg, group;
+};
+inline size_t sf_layout_bytes(size_t rows, size_t K, SfLayout L) {
+  const size_t nseg = (rows + L.seg - 1) / L.seg, gps = (L.seg + L.group - 1) / L.group;
+  const size_t apg = (L.group + 127) / 128;
+  return nseg * gps * apg * (K / 128) * 512;
+}
 // pad_off[e] = sum over e' < e of ceil(count/128)*128
 cudaError_t launch_pad_offsets(const int32_t *offsets, int E, int32_t *pad_off, cudaStream_t s);
 // rows along K (K % 128 == 0): dense (offsets == nullptr, rows_out input rows) or
 // into the padded per-expert row space (rows_out = padded row capacity)
 cudaError_t launch_quant_rows(const uint16_t *src, int rows_out, int K, const int32_t *offsets,
-                              const int32_t *pad_off, int E, uint8_t *codes, uint8_t *sf,
+                              const int32_t *pad_off, int E, uint8_t *codes, uint8_t *sf, SfLayout L,
                               cudaStream_t s);
 // along tokens: [M, C] permuted rows -> codes [C, Mpad] (padded token axis)
 cudaError_t launch_quant_cols(const uint16_t *src, int C, int Mpad, const int32_t *offsets,
-                              const int32_t *pad_off, int E, uint8_t *codes, uint8_t *sf,
+                              const int32_t *pad_off, int E, uint8_t *codes, uint8_t *sf, SfLayout L,
                               cudaStream_t s);
 
 enum MxGemmMode : int { kMxGemmDA = 0, kMxGemmDX = 1, kMxGemmDWDown = 2, kMxGemmDWGateUp = 3 };

@@ -14,10 +14,15 @@
 //
 // Output layouts are what the block-scaled tensor-core GEMM loads:
 //   codes  K-major: [rows][K] bytes;
-//   scales in 512-byte atoms, one per (128 rows, 128 K): atom (rb, kg) at
-//          ((rb * (K / 128)) + kg) * 512, holding the scale of row rb*128 +
-//          32 q + l and K block kg*4 + j at byte l*16 + q*4 + j -- the layout
+//   scales in 512-byte atoms of 128 rows x 128 K: atom (rb, kg) at
+//          ((rb * (K / 128)) + kg) * 512 holds the scale of its row 32 q + l
+//          and K block kg*4 + j at byte l*16 + q*4 + j -- the layout
 //          tcgen05.cp.32x128b.warpx4 copies into tensor memory for the MMA.
+//          Rows map to row blocks rb by an SfLayout: rows are cut into segments
+//          of `seg` rows (an expert's rows of a weight, or the whole operand),
+//          each segment into groups of `group` rows (128, or 192 for the
+//          GEMMs' 192-row B tiles), each group into ceil(group/128) atoms, so a
+//          tile's scales always start on an atom boundary.
 // Ragged operands are written in a per-expert padded row space: expert e's
 // rows start at pad_off[e] = sum over e' < e of ceil(count/128)*128, the rows
 // past its count are zero codes with zero scales, so every 128-row tile and
@@ -68,9 +73,13 @@ __device__ __forceinline__ uint8_t quant32(const float (&v)[32], uint4 *dst) {
   return static_cast<uint8_t>(X + 127);
 }
 
-__device__ __forceinline__ size_t atom_byte(int row, int kblock, int K) {
-  const int rb = row >> 7, r = row & 127, kg = kblock >> 2;
-  return (static_cast<size_t>(rb) * (K >> 7) + kg) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (kblock & 3);
+__device__ __forceinline__ size_t atom_byte(int row, int kblock, int K, SfLayout L) {
+  const int sg = row / L.seg, r = row - sg * L.seg;
+  const int g = r / L.group, rr = r - g * L.group;
+  const int gps = (L.seg + L.group - 1) / L.group, apg = (L.group + 127) >> 7;
+  const size_t rb = (static_cast<size_t>(sg) * gps + g) * apg + (rr >> 7);
+  const int w = rr & 127;
+  return (rb * (K >> 7) + (kblock >> 2)) * 512 + (w & 31) * 16 + (w >> 5) * 4 + (kblock & 3);
 }
 
 // Expert of padded row o (largest e with pad_off[e] <= o), from shared memory.
@@ -93,7 +102,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t *__restr
                                                          const int32_t *__restrict__ offsets,
                                                          const int32_t *__restrict__ pad_off, int E,
                                                          uint8_t *__restrict__ codes,
-                                                         uint8_t *__restrict__ sf) {
+                                                         uint8_t *__restrict__ sf, SfLayout L) {
   __shared__ int s_off[kMaxExperts + 1], s_pad[kMaxExperts + 1];
   if (offsets) {
     for (int e = threadIdx.x; e <= E; e += blockDim.x) {
@@ -106,6 +115,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t *__restr
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= static_cast<int64_t>(rows_out) * nb) return;
   const int o = static_cast<int>(idx / nb), b = static_cast<int>(idx % nb);
+  if (offsets && o >= s_pad[E]) return;  // past the padded total: never read
   int in_row = o;
   if (offsets) {
     const int e = expert_of(o, s_pad, E);
@@ -129,39 +139,62 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t *__restr
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = 0.f;
   }
-  sf[atom_byte(o, b, K)] =
+  sf[atom_byte(o, b, K, L)] =
       quant32(v, reinterpret_cast<uint4 *>(codes + static_cast<size_t>(o) * K + 32 * b));
 }
 
-// Token-axis quantisation: one thread per (column c, 32-token block of the
-// padded space).  Output is transposed: codes [C][Mpad] (tokens contiguous).
-__global__ void __launch_bounds__(256) quant_cols_kernel(const uint16_t *__restrict__ src, int C,
-                                                         int Mpad,
-                                                         const int32_t *__restrict__ offsets,
-                                                         const int32_t *__restrict__ pad_off, int E,
-                                                         uint8_t *__restrict__ codes,
-                                                         uint8_t *__restrict__ sf) {
-  __shared__ int s_off[kMaxExperts + 1], s_pad[kMaxExperts + 1];
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
-    s_off[e] = __ldg(offsets + e);
-    s_pad[e] = __ldg(pad_off + e);
+// Token-axis quantisation, output transposed: codes [C][Mpad] (tokens
+// contiguous).  A block takes 128 padded rows (one expert's, as segments are
+// 128-aligned) x 64 columns: coalesced 128-byte row loads into shared memory,
+// then one thread per (column, 32-token block) quantises down the column and
+// writes its 32 codes as two 16-byte stores.  Tiles past the padded total are
+// skipped (never read).
+constexpr int kQcRows = 128, kQcCols = 64, kQcThreads = 256;
+
+__global__ void __launch_bounds__(kQcThreads) quant_cols_kernel(const uint16_t *__restrict__ src, int C,
+                                                                int Mpad,
+                                                                const int32_t *__restrict__ offsets,
+                                                                const int32_t *__restrict__ pad_off, int E,
+                                                                uint8_t *__restrict__ codes,
+                                                                uint8_t *__restrict__ sf, SfLayout L) {
+  __shared__ int s_pad[kMaxExperts + 1];
+  __shared__ __align__(16) uint16_t tile[kQcRows * kQcCols];
+  __shared__ int s_seg[3];  // first source row, valid rows of this tile, skip flag
+  const int prow0 = blockIdx.x * kQcRows, c0 = blockIdx.y * kQcCols;
+  for (int e = threadIdx.x; e <= E; e += kQcThreads) s_pad[e] = __ldg(pad_off + e);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (prow0 >= s_pad[E]) {
+      s_seg[2] = 1;
+    } else {
+      const int e = expert_of(prow0, s_pad, E);
+      const int o = __ldg(offsets + e), count = __ldg(offsets + e + 1) - o;
+      const int local0 = prow0 - s_pad[e];
+      s_seg[0] = o + local0;
+      s_seg[1] = min(kQcRows, count - local0);
+      s_seg[2] = 0;
+    }
   }
   __syncthreads();
-  const int nb = Mpad >> 5;
-  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (idx >= static_cast<int64_t>(C) * nb) return;
-  const int c = static_cast<int>(idx % C), b = static_cast<int>(idx / C);  // columns fastest
-  const int o0 = 32 * b;
-  const int e = expert_of(o0, s_pad, E);
-  const int local0 = o0 - s_pad[e], count = s_off[e + 1] - s_off[e];
+  if (s_seg[2]) return;
+  const int row0 = s_seg[0], nvalid = s_seg[1];
+#pragma unroll
+  for (int j = 0; j < (kQcRows * kQcCols / 8) / kQcThreads; ++j) {
+    const int i = threadIdx.x + j * kQcThreads;
+    const int r = i >> 3, part = i & 7;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (r < nvalid)
+      v = __ldg(reinterpret_cast<const uint4 *>(src + static_cast<size_t>(row0 + r) * C + c0) + part);
+    *reinterpret_cast<uint4 *>(tile + r * kQcCols + part * 8) = v;
+  }
+  __syncthreads();
+  const int cc = threadIdx.x % kQcCols, b = threadIdx.x / kQcCols;  // 4 blocks of 32 tokens
   float v[32];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const int local = local0 + i;
-    v[i] = local < count ? __uint_as_float(static_cast<uint32_t>(src[static_cast<size_t>(s_off[e] + local) * C + c]) << 16)
-                         : 0.f;
-  }
-  sf[atom_byte(c, b, Mpad)] =
+  for (int i = 0; i < 32; ++i)
+    v[i] = __uint_as_float(static_cast<uint32_t>(tile[(32 * b + i) * kQcCols + cc]) << 16);
+  const int c = c0 + cc, o0 = prow0 + 32 * b;
+  sf[atom_byte(c, o0 >> 5, Mpad, L)] =
       quant32(v, reinterpret_cast<uint4 *>(codes + static_cast<size_t>(c) * Mpad + o0));
 }
 
@@ -193,20 +226,19 @@ cudaError_t launch_pad_offsets(const int32_t *offsets, int E, int32_t *pad_off, 
 }
 
 cudaError_t launch_quant_rows(const uint16_t *src, int rows_out, int K, const int32_t *offsets,
-                              const int32_t *pad_off, int E, uint8_t *codes, uint8_t *sf,
+                              const int32_t *pad_off, int E, uint8_t *codes, uint8_t *sf, SfLayout L,
                               cudaStream_t s) {
   const int64_t n = static_cast<int64_t>(rows_out) * (K / 32);
   quant_rows_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(src, K, rows_out, offsets,
-                                                                            pad_off, E, codes, sf);
+                                                                            pad_off, E, codes, sf, L);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quant_cols(const uint16_t *src, int C, int Mpad, const int32_t *offsets,
-                              const int32_t *pad_off, int E, uint8_t *codes, uint8_t *sf,
+                              const int32_t *pad_off, int E, uint8_t *codes, uint8_t *sf, SfLayout L,
                               cudaStream_t s) {
-  const int64_t n = static_cast<int64_t>(C) * (Mpad / 32);
-  quant_cols_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(src, C, Mpad, offsets,
-                                                                            pad_off, E, codes, sf);
+  const dim3 grid(static_cast<unsigned>(Mpad / kQcRows), static_cast<unsigned>(C / kQcCols));
+  quant_cols_kernel<<<grid, kQcThreads, 0, s>>>(src, C, Mpad, offsets, pad_off, E, codes, sf, L);
   return cudaGetLastError();
 }
 

@@ -136,6 +136,28 @@ def fp8_scratch_offsets(cfg: Config) -> dict:
     return {n: int(getattr(lay, n)) for n, _ in Fp8Layout._fields_}
 
 
+MX_BN = 192  # N extent of an MXFP8 GEMM tile: B-operand scales are grouped by it
+
+
+def sf_grouping(base: str, shape, m_pad: int):
+    """(segment rows, group rows) of a quantised operand's scale atoms."""
+    if base in ("wd_q",):
+        return shape.I, MX_BN
+    if base in ("wg_q", "wu_q"):
+        return shape.H, MX_BN
+    if base == "dy_t":
+        return shape.H, MX_BN
+    if base in ("dg_t", "du_t"):
+        return shape.I, MX_BN
+    rows = {"dy_q": m_pad, "dg_q": m_pad, "du_q": m_pad, "aw_t": shape.I, "x_t": shape.H}[base]
+    return rows, 128
+
+
+def sf_layout_bytes(rows: int, K: int, seg: int, group: int) -> int:
+    nseg, gps, apg = -(-rows // seg), -(-seg // group), -(-group // 128)
+    return nseg * gps * apg * (K // 128) * 512
+
+
 def make_routing(r: dict) -> Routing:
     return Routing(*[r[n].data_ptr() for n, _ in Routing._fields_])
 
@@ -253,7 +275,8 @@ class MoELayer:
         if name.endswith("_sf"):
             base = name[:-3] + "_q" if name[:-3] + "_q" in rows_k else name[:-3]
             R, K = rows_k[base]
-            return self.bwd_scratch[off:off + R * K // 32]
+            seg, group = sf_grouping(base, s, Mp)
+            return self.bwd_scratch[off:off + sf_layout_bytes(R, K, seg, group)]
         R, K = rows_k[name]
         return self.bwd_scratch[off:off + R * K].view(R, K)
 

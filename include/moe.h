@@ -114,15 +114,24 @@ moe_status moe_saved_offsets(const moe_config *cfg, moe_saved_layout *layout);
  * MXFP8 operands it writes, for inspection after the call.  m_pad is the padded
  * token capacity (a multiple of 128): expert e's rows start at padded row
  * pad_offsets[e] = sum over e' < e of ceil(count/128)*128 (int32 [E+1]); rows
- * past an expert's count are zero codes with zero scale codes.
+ * past an expert's count are zero codes with zero scale codes; padded rows at
+ * and past pad_offsets[E] are left unwritten.
  *   *_q     E4M3 codes, K-major: dy_q [m_pad,H] (padded rows), wd_q [E*I,H],
  *           dg_q/du_q [m_pad,I], wg_q/wu_q [E*H,I];
  *   *_t     token-axis operands transposed, tokens contiguous: aw_t (w*A) and
  *           dg_t/du_t [I,m_pad], dy_t and x_t [H,m_pad];
  *   *_sf    their UE8M0 scale codes (2^(code-127)), one per 32 elements along
- *           K, in 512-byte atoms: for R rows and K columns the scale of row r,
- *           K-block b sits at byte ((r/128)*(K/128) + b/4)*512 + (r%32)*16 +
- *           ((r%128)/32)*4 + b%4 -- the order the tensor core reads them.
+ *           K, in 512-byte atoms of 128 rows x 128 K, the order the tensor core
+ *           reads them: row w of atom row-block rb, K-block b, sits at byte
+ *           (rb*(K/128) + b/4)*512 + (w%32)*16 + (w/32)*4 + b%4.  For dy_q,
+ *           dg_q, du_q, aw_t and x_t (the GEMMs' M side) row r is row r%128 of
+ *           block r/128.  For wd_q, wg_q, wu_q, dy_t, dg_t and du_t (the N side,
+ *           read in 192-row tiles) rows are cut into segments of S rows (S = I
+ *           for wd_q, H for wg_q/wu_q, all rows for the transposed ones), each
+ *           segment into groups of 192 rows, each group into two blocks: row r
+ *           with s = r/S, g = (r%S)/192, j = (r%S)%192 is row j%128 of block
+ *           (s*ceil(S/192) + g)*2 + j/128.  Scale bytes of groups' rows past a
+ *           segment's end are left unwritten.
  * Returns MOE_ERR_INVALID_ARG for other precisions or unsupported shapes. */
 typedef struct {
   size_t m_pad, pad_offsets;

@@ -121,6 +121,8 @@ def test_fp8_shapes_and_layout(L):
     c = cfg(T=300, H=256, I=128, E=8, k=2, prec=1)
     q = moe.fp8_scratch_offsets(c)
     M, E, H, I = 600, 8, 256, 128
+    from dropless_mixture_experts_top_gb300.synth import MoEShape
+    moe_shape = MoEShape(T=300, H=H, I=I, E=E, k=2)
     Mp = q["m_pad"]
     assert Mp % 128 == 0 and Mp >= M + 127 * E
     sizes = {"pad_offsets": 4 * (E + 1), "dy_q": Mp * H, "wd_q": E * I * H, "dg_q": Mp * I, "du_q": Mp * I,
@@ -128,7 +130,12 @@ def test_fp8_shapes_and_layout(L):
              "dg_t": I * Mp, "du_t": I * Mp}
     for n in list(sizes):
         if n != "pad_offsets":
-            sizes[(n[:-2] if n.endswith("_q") else n) + "_sf"] = sizes[n] // 32
+            R, K = {"dy_q": (Mp, H), "wd_q": (E * I, H), "dg_q": (Mp, I), "du_q": (Mp, I), "wg_q": (E * H, I),
+                    "wu_q": (E * H, I), "aw_t": (I, Mp), "dy_t": (H, Mp), "x_t": (H, Mp), "dg_t": (I, Mp),
+                    "du_t": (I, Mp)}[n]
+            seg, group = moe.sf_grouping(n, moe_shape, Mp)
+            sizes[(n[:-2] if n.endswith("_q") else n) + "_sf"] = moe.sf_layout_bytes(R, K, seg, group)
+            assert sizes[(n[:-2] if n.endswith("_q") else n) + "_sf"] >= R * K // 32
     spans = sorted((q[n], q[n] + b, n) for n, b in sizes.items())
     for (a0, a1, n0), (b0, b1, n1) in zip(spans, spans[1:]):
         assert a1 <= b0, (n0, n1)  # disjoint

@@ -25,11 +25,21 @@ def _build():
     B.build()
 
 
-def atoms_to_scales(sf, R, K):
-    """[R, K/32] scale codes from the 512-byte atoms: byte l*16 + q*4 + j of atom
-    (rb, kg) is row rb*128 + 32q + l, K-block kg*4 + j."""
-    a = np.asarray(sf, np.uint8).reshape(R // 128, K // 128, 32, 4, 4)
-    return a.transpose(0, 3, 2, 1, 4).reshape(R, K // 32)
+def atoms_to_scales(sf, R, K, seg=None, group=128):
+    """[R, K/32] scale codes from the 512-byte atoms: row w of atom row-block rb,
+    K-block b at byte (rb*(K/128) + b/4)*512 + (w%32)*16 + (w/32)*4 + b%4; rows
+    map to (rb, w) through segments of `seg` rows cut into groups of `group`."""
+    seg = seg or R
+    r = np.arange(R)
+    s, j = r // seg, r % seg
+    g, jj = j // group, j % group
+    gps, apg = -(-seg // group), -(-group // 128)
+    rb = (s * gps + g) * apg + jj // 128
+    w = jj % 128
+    b = np.arange(K // 32)
+    idx = ((rb[:, None] * (K // 128) + b[None, :] // 4) * 512 + (w[:, None] % 32) * 16 + (w[:, None] // 32) * 4
+           + b[None, :] % 4)
+    return np.asarray(sf, np.uint8)[idx]
 
 
 def padded_rows(rows, offsets, pad, Mp):
@@ -44,7 +54,8 @@ def check_token_axis(layer, name, src_rows, offsets, pad, Mp):
     """Codes [C, Mp] and scales of an operand quantised along tokens, per expert."""
     C = src_rows.shape[1]
     got = layer.fp8_tensor(name).cpu().numpy()
-    got_sc = atoms_to_scales(layer.fp8_tensor(name + "_sf").cpu().numpy(), C, Mp)
+    seg, group = moe.sf_grouping(name, layer.shape, Mp)
+    got_sc = atoms_to_scales(layer.fp8_tensor(name + "_sf").cpu().numpy(), C, Mp, seg, group)
     exp = np.zeros((C, Mp), np.uint8)
     exp_sc = np.zeros((C, Mp // 32), np.uint8)
     for e in range(len(offsets) - 1):
@@ -54,8 +65,9 @@ def check_token_axis(layer, name, src_rows, offsets, pad, Mp):
         codes, sc = O.mx_quantize_cols(src_rows, int(offsets[e]), n)
         exp[:, pad[e]:pad[e] + codes.shape[0]] = codes.T
         exp_sc[:, pad[e] // 32:pad[e] // 32 + sc.shape[0]] = sc.T
-    np.testing.assert_array_equal(got, exp, err_msg=name)
-    np.testing.assert_array_equal(got_sc, exp_sc, err_msg=name + "_sf")
+    P = int(pad[-1])  # padded rows past the total are never read and left unwritten
+    np.testing.assert_array_equal(got[:, :P], exp[:, :P], err_msg=name)
+    np.testing.assert_array_equal(got_sc[:, :P // 32], exp_sc[:, :P // 32], err_msg=name + "_sf")
 
 
 def test_quantised_operands_bit_exact():
@@ -76,14 +88,18 @@ def test_quantised_operands_bit_exact():
                           ("wu", inp["W_up"], E * H, I)):
         codes, sc, _ = O.mx_quantize_rows(W.reshape(R, K))
         np.testing.assert_array_equal(layer.fp8_tensor(name + "_q").cpu().numpy(), codes, err_msg=name)
-        np.testing.assert_array_equal(atoms_to_scales(layer.fp8_tensor(name + "_sf").cpu().numpy(), R, K),
-                                      sc, err_msg=name + "_sf")
+        seg, group = moe.sf_grouping(name + "_q", shape, Mp)
+        np.testing.assert_array_equal(
+            atoms_to_scales(layer.fp8_tensor(name + "_sf").cpu().numpy(), R, K, seg, group), sc,
+            err_msg=name + "_sf")
     # dy in the padded row space (dA's A operand), along H
     dy_perm = inp["dy"][sor // k]
     codes, sc, _ = O.mx_quantize_rows(dy_perm)
-    np.testing.assert_array_equal(layer.fp8_tensor("dy_q").cpu().numpy(), padded_rows(codes, offsets, pad, Mp))
-    np.testing.assert_array_equal(atoms_to_scales(layer.fp8_tensor("dy_sf").cpu().numpy(), Mp, H),
-                                  padded_rows(sc, offsets, pad, Mp))
+    P = int(pad[-1])
+    np.testing.assert_array_equal(layer.fp8_tensor("dy_q").cpu().numpy()[:P],
+                                  padded_rows(codes, offsets, pad, Mp)[:P])
+    np.testing.assert_array_equal(atoms_to_scales(layer.fp8_tensor("dy_sf").cpu().numpy(), Mp, H)[:P],
+                                  padded_rows(sc, offsets, pad, Mp)[:P])
     # token-axis operands of the weight gradients: dy and x, blocks of 32 from each expert's first row
     check_token_axis(layer, "dy_t", dy_perm, offsets, pad, Mp)
     check_token_axis(layer, "x_t", inp["x"][sor // k], offsets, pad, Mp)
