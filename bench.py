@@ -87,10 +87,25 @@ def kernel_work(shape):
     }
 
 
-def source_hash():
+def kernel_source(label):
+    """The .cu file that defines the kernel behind a timing label."""
+    if label.startswith("mx_gemm_"):
+        return "gemm_mx.cu"
+    if label.startswith("gemm_"):
+        return "gemm.cu"
+    if label.startswith("mx_"):
+        return "mxfp8.cu"
+    if label.startswith("route_"):
+        return "route.cu"
+    return "gather.cu"  # permute_rows, combine, router_bwd, unpermute_sum
+
+
+def source_hash(label):
+    """Hash of a kernel's source and the headers it includes: a recorded traffic
+    figure is valid only while this is unchanged."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dropless_mixture_experts_top_gb300", "csrc")
-    for n in sorted(os.listdir(csrc)):
+    for n in (kernel_source(label), "common.cuh", "epilogue.cuh", "internal.h"):
         with open(os.path.join(csrc, n), "rb") as f:
             h.update(n.encode() + f.read())
     return h.hexdigest()[:16]
@@ -104,7 +119,7 @@ def committed_traffic(kernel, workload):
     with open(path) as f:
         rec = json.load(f)
     ent = rec.get(workload, {}).get(kernel)
-    if not ent or ent.get("source_hash") != source_hash():
+    if not ent or ent.get("source_hash") != source_hash(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
 

@@ -145,3 +145,31 @@ def test_fp8_empty_and_hot_experts():
 def test_fp8_rejects_unaligned_shape():
     with pytest.raises(moe.MoEError):
         moe.MoELayer(MoEShape(T=64, H=192, I=128, E=4, k=2), precision="fp8_bwd")
+
+
+def test_quantiser_sweeps_every_bf16_value():
+    """Every finite bf16 value through the GPU quantiser (CUDA's E4M3 conversion)
+    against the oracle's: blocks of 32 neighbouring magnitudes (each block's own
+    scale, so saturation, subnormals and ties all occur) plus blocks that mix
+    extremes."""
+    shape = MoEShape(T=64, H=256, I=512, E=2, k=1)
+    E, H, I = shape.E, shape.H, shape.I
+    rng = np.random.default_rng(61)
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    finite = bits[(bits & 0x7F80) != 0x7F80]                       # drop Inf / NaN
+    mag = synth.bf16_bits_to_f32(finite & 0x7FFF)
+    order = np.argsort(mag, kind="stable")
+    sweep = finite[order]                                          # neighbouring magnitudes together
+    n = E * I * H
+    assert len(sweep) <= n
+    vals = np.concatenate([sweep, rng.choice(finite, n - len(sweep))])  # then random blocks
+    W_down = vals.reshape(E, I, H)
+    inp = synth.make_inputs_shape(shape, 63)
+    inp["W_down"] = W_down
+    layer, out, grads = G.run_layer(shape, inp, precision="fp8_bwd")  # outputs may overflow: not compared
+    codes, sc, _ = O.mx_quantize_rows(W_down.reshape(E * I, H))
+    Mp = moe.fp8_scratch_offsets(layer.cfg)["m_pad"]
+    np.testing.assert_array_equal(layer.fp8_tensor("wd_q").cpu().numpy(), codes)
+    seg, group = moe.sf_grouping("wd_q", shape, Mp)
+    np.testing.assert_array_equal(atoms_to_scales(layer.fp8_tensor("wd_sf").cpu().numpy(), E * I, H, seg, group),
+                                  sc)
