@@ -3,11 +3,21 @@
 // SwiGLU for the forward gate/up GEMM, fused dSwiGLU for dA).  Shared by the
 // bf16 GEMM engine (gemm.cu) and the MXFP8 one (gemm_mx.cu).  `P` is any
 // parameter struct with the fields used below (H, I, G, U, w_row, o0..o3).
+//
+// A warp owns 32 rows (one per lane, as tcgen05.ld 32x32b delivers them) and
+// walks its columns in 32-column chunks.  Row-major global memory is touched
+// through a per-warp 2 KiB shared-memory tile: a lane writes its row's 64
+// bytes there, then each instruction moves 8 rows x 64 contiguous bytes
+// between the tile and global memory (4 lanes per row), instead of 32 rows x
+// 16 bytes.  The tile's 16-byte chunks are XOR-swizzled by row so that both
+// access patterns are free of bank conflicts.
 #pragma once
 
 #include "common.cuh"
 
 namespace moe {
+
+constexpr int kEpiTileBytes = 32 * 32 * 2;  // one warp's 32 x 32 bf16 staging tile
 
 struct Tile {
   int e;        // expert
@@ -19,8 +29,16 @@ struct Tile {
   int kcount;   // ragged K: expert's rows
 };
 
-__device__ __forceinline__ void store32_bf16(uint16_t *dst, const float (&v)[32]) {
-  uint4 *d = reinterpret_cast<uint4 *>(dst);
+// Byte offset of row r's 16-byte chunk q (of 4) in a staging tile.
+__device__ __forceinline__ uint32_t epi_swz(int r, int q) {
+  return static_cast<uint32_t>(r * 64 + ((q ^ ((r >> 1) & 3)) << 4));
+}
+
+// The warp's 32 rows x 32 columns, lane = row, to global rows [0, nvalid) at
+// g0 (row 0, first column), row stride ld elements.
+__device__ __forceinline__ void store_rows32(uint8_t *tile, uint16_t *g0, size_t ld, int nvalid,
+                                             const float (&v)[32]) {
+  const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     uint4 w;
@@ -28,136 +46,159 @@ __device__ __forceinline__ void store32_bf16(uint16_t *dst, const float (&v)[32]
     w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
     w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
     w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
-    d[q] = w;
+    *reinterpret_cast<uint4 *>(tile + epi_swz(lane, q)) = w;
   }
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = 8 * i + (lane >> 2), q = lane & 3;
+    const uint4 w = *reinterpret_cast<const uint4 *>(tile + epi_swz(r, q));
+    if (r < nvalid) *reinterpret_cast<uint4 *>(g0 + static_cast<size_t>(r) * ld + q * 8) = w;
+  }
+  __syncwarp();
+}
+
+// Coalesced loads of the warp's 32 rows x 32 bf16 columns (rows past nvalid
+// read as zero) into registers: issued early, consumed by rows32_to_lanes.
+__device__ __forceinline__ void load_rows32(const uint16_t *g0, size_t ld, int nvalid, uint4 (&w)[4]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = 8 * i + (lane >> 2), q = lane & 3;
+    w[i] = r < nvalid ? __ldg(reinterpret_cast<const uint4 *>(g0 + static_cast<size_t>(r) * ld) + q)
+                      : make_uint4(0, 0, 0, 0);
+  }
+}
+
+// Redistribute loaded rows through the staging tile: lane r gets row r's 32 values.
+__device__ __forceinline__ void rows32_to_lanes(uint8_t *tile, const uint4 (&w)[4], float (&v)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = 8 * i + (lane >> 2), q = lane & 3;
+    *reinterpret_cast<uint4 *>(tile + epi_swz(r, q)) = w[i];
+  }
+  __syncwarp();
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 x = *reinterpret_cast<const uint4 *>(tile + epi_swz(lane, q));
+    const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      v[8 * q + 2 * h] = bf16_lo(xw[h]);
+      v[8 * q + 2 * h + 1] = bf16_hi(xw[h]);
+    }
+  }
+  __syncwarp();
 }
 
 __device__ __forceinline__ float sigmoidf_(float z) { return 1.f / (1.f + __expf(-z)); }
 
-// Epilogue of one tile for one warp (32 rows).  tb: TMEM address of this
-// warp's lanes at the accumulator's first column.  NCH: 32-column chunks in
-// the tile's unpaired accumulator (8 for 256 columns, 6 for 192).
+__device__ __forceinline__ int clamp_rows(int n) { return n < 0 ? 0 : (n > 32 ? 32 : n); }
+
+// Epilogue of one tile for one warp: 32 rows, and the part-th of nparts column
+// ranges (nparts warps share each TMEM lane quarter).  tb: TMEM address of
+// this warp's lanes at the accumulator's first column; rit: this lane's row
+// within the tile; tile: the warp's staging tile.  NCH: 32-column chunks in
+// the tile's unpaired accumulator (8 for 256 columns, 6 for 192); the paired
+// modes (gate|up halves) have 4 chunks, each covering both halves.
 template <int MODE, class P, int NCH = 8>
-__device__ __forceinline__ void epilogue_tile(const Tile &t, uint32_t tb, int rit, const P &p) {
+__device__ __forceinline__ void epilogue_tile(const Tile &t, uint32_t tb, int rit, const P &p,
+                                              int part, int nparts, uint8_t *tile) {
+  constexpr int kPairChunks = 4;
+  const int cb4 = part * kPairChunks / nparts, ce4 = (part + 1) * kPairChunks / nparts;
+  const int cb = part * NCH / nparts, ce = (part + 1) * NCH / nparts;
+  const int lane = threadIdx.x & 31;
   uint32_t r0[32], r1[32];
   float v0[32], v1[32], v2[32];
   if constexpr (MODE == kFwdGateUp) {
-    const int row = t.m0 + rit;
-    const bool rv = row < t.row_end;
-    const float w = rv ? __ldg(p.w_row + row) : 0.f;
-    for (int c = 0; c < 4; ++c) {
+    const int row = t.m0 + rit, row0 = row - lane;
+    const int nvalid = clamp_rows(t.row_end - row0);
+    const float w = row < t.row_end ? __ldg(p.w_row + row) : 0.f;
+    for (int c = cb4; c < ce4; ++c) {
       const int col = t.n0 + 32 * c;
       if (col >= p.I) break;
       tmem_ld32(tb + 32 * c, r0);
       tmem_ld32(tb + 128 + 32 * c, r1);
       tmem_ld_wait();
-      if (rv) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float g = __uint_as_float(r0[i]), u = __uint_as_float(r1[i]);
-          v0[i] = g * sigmoidf_(g) * u;  // SwiGLU
-          v1[i] = g;
-          v2[i] = u;
-        }
-        const size_t off = static_cast<size_t>(row) * p.I + col;
-        store32_bf16(p.o0 + off, v0);
-        store32_bf16(p.o1 + off, v1);
-        store32_bf16(p.o2 + off, v2);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v0[i] *= w;  // A_w = w * A, the dW_down operand
-        store32_bf16(p.o3 + off, v0);
+      for (int i = 0; i < 32; ++i) {
+        const float g = __uint_as_float(r0[i]), u = __uint_as_float(r1[i]);
+        v0[i] = g * sigmoidf_(g) * u;  // SwiGLU
+        v1[i] = g;
+        v2[i] = u;
       }
+      const size_t off = static_cast<size_t>(row0) * p.I + col;
+      store_rows32(tile, p.o0 + off, p.I, nvalid, v0);
+      store_rows32(tile, p.o1 + off, p.I, nvalid, v1);
+      store_rows32(tile, p.o2 + off, p.I, nvalid, v2);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v0[i] *= w;  // A_w = w * A, the dW_down operand
+      store_rows32(tile, p.o3 + off, p.I, nvalid, v0);
     }
   } else if constexpr (MODE == kFwdDown || MODE == kBwdDX) {
-    const int row = t.m0 + rit;
-    const bool rv = row < t.row_end;
-    for (int c = 0; c < NCH; ++c) {
+    const int row0 = t.m0 + rit - lane;
+    const int nvalid = clamp_rows(t.row_end - row0);
+    for (int c = cb; c < ce; ++c) {
       const int col = t.n0 + 32 * c;
       if (col >= p.H) break;
       tmem_ld32(tb + 32 * c, r0);
       tmem_ld_wait();
-      if (rv) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v0[i] = __uint_as_float(r0[i]);
-        store32_bf16(p.o0 + static_cast<size_t>(row) * p.H + col, v0);
-      }
+      for (int i = 0; i < 32; ++i) v0[i] = __uint_as_float(r0[i]);
+      store_rows32(tile, p.o0 + static_cast<size_t>(row0) * p.H + col, p.H, nvalid, v0);
     }
   } else if constexpr (MODE == kBwdDA) {
-    const int row = t.m0 + rit;
-    const bool rv = row < t.row_end;
-    const float w = rv ? __ldg(p.w_row + row) : 0.f;  // dA = w * (dy . W_down^T)
+    const int row = t.m0 + rit, row0 = row - lane;
+    const int nvalid = clamp_rows(t.row_end - row0);
+    const float w = row < t.row_end ? __ldg(p.w_row + row) : 0.f;  // dA = w * (dy . W_down^T)
+    const size_t rowoff = static_cast<size_t>(row0) * p.I;
     // G and U of the next 32-column chunk are loaded while this chunk is computed
-    uint4 gq[4], uq[4], gn[4], un[4];
-    const size_t rowoff = static_cast<size_t>(rv ? row : 0) * p.I;
-    if (rv && t.n0 < p.I) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        gq[q] = __ldg(reinterpret_cast<const uint4 *>(p.G + rowoff + t.n0) + q);
-        uq[q] = __ldg(reinterpret_cast<const uint4 *>(p.U + rowoff + t.n0) + q);
-      }
+    uint4 gq[4], uq[4];
+    if (t.n0 + 32 * cb < p.I) {
+      load_rows32(p.G + rowoff + t.n0 + 32 * cb, p.I, nvalid, gq);
+      load_rows32(p.U + rowoff + t.n0 + 32 * cb, p.I, nvalid, uq);
     }
-    for (int c = 0; c < NCH; ++c) {
+    for (int c = cb; c < ce; ++c) {
       const int col = t.n0 + 32 * c;
       if (col >= p.I) break;
-      const bool next = c + 1 < NCH && col + 32 < p.I;
-      if (rv && next) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          gn[q] = __ldg(reinterpret_cast<const uint4 *>(p.G + rowoff + col + 32) + q);
-          un[q] = __ldg(reinterpret_cast<const uint4 *>(p.U + rowoff + col + 32) + q);
-        }
+      rows32_to_lanes(tile, gq, v1);
+      rows32_to_lanes(tile, uq, v2);
+      if (c + 1 < ce && col + 32 < p.I) {
+        load_rows32(p.G + rowoff + col + 32, p.I, nvalid, gq);
+        load_rows32(p.U + rowoff + col + 32, p.I, nvalid, uq);
       }
       tmem_ld32(tb + 32 * c, r0);
       tmem_ld_wait();
-      if (rv) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t gw[4] = {gq[q].x, gq[q].y, gq[q].z, gq[q].w};
-          const uint32_t uw[4] = {uq[q].x, uq[q].y, uq[q].z, uq[q].w};
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            v1[8 * q + 2 * h] = bf16_lo(gw[h]);
-            v1[8 * q + 2 * h + 1] = bf16_hi(gw[h]);
-            v2[8 * q + 2 * h] = bf16_lo(uw[h]);
-            v2[8 * q + 2 * h + 1] = bf16_hi(uw[h]);
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float da = w * __uint_as_float(r0[i]), g = v1[i], u = v2[i];
-          const float s = sigmoidf_(g);
-          v0[i] = da * u * s * (1.f + g * (1.f - s));  // dG
-          v1[i] = da * g * s;                          // dU = dA * silu(G)
-        }
-        store32_bf16(p.o0 + rowoff + col, v0);
-        store32_bf16(p.o1 + rowoff + col, v1);
+      for (int i = 0; i < 32; ++i) {  // in place: v1 G -> dU, v2 U -> dG
+        const float da = w * __uint_as_float(r0[i]), g = v1[i], u = v2[i];
+        const float s = sigmoidf_(g);
+        v2[i] = da * u * s * (1.f + g * (1.f - s));  // dG
+        v1[i] = da * g * s;                          // dU = dA * silu(G)
       }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        gq[q] = gn[q];
-        uq[q] = un[q];
-      }
+      store_rows32(tile, p.o0 + rowoff + col, p.I, nvalid, v2);
+      store_rows32(tile, p.o1 + rowoff + col, p.I, nvalid, v1);
     }
   } else if constexpr (MODE == kBwdDWDown) {
-    const int i_row = t.m0 + rit;
-    const bool rv = i_row < p.I;
-    for (int c = 0; c < NCH; ++c) {
+    const int i_row0 = t.m0 + rit - lane;
+    const int nvalid = clamp_rows(p.I - i_row0);
+    for (int c = cb; c < ce; ++c) {
       const int col = t.n0 + 32 * c;
       if (col >= p.H) break;
       if (t.nkb > 0) {
         tmem_ld32(tb + 32 * c, r0);
         tmem_ld_wait();
       }
-      if (rv) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v0[i] = t.nkb > 0 ? __uint_as_float(r0[i]) : 0.f;
-        store32_bf16(p.o0 + (static_cast<size_t>(t.e) * p.I + i_row) * p.H + col, v0);
-      }
+      for (int i = 0; i < 32; ++i) v0[i] = t.nkb > 0 ? __uint_as_float(r0[i]) : 0.f;
+      store_rows32(tile, p.o0 + (static_cast<size_t>(t.e) * p.I + i_row0) * p.H + col, p.H, nvalid,
+                   v0);
     }
   } else {  // kBwdDWGateUp
-    const int h_row = t.m0 + rit;
-    const bool rv = h_row < p.H;
-    for (int c = 0; c < 4; ++c) {
+    const int h_row0 = t.m0 + rit - lane;
+    const int nvalid = clamp_rows(p.H - h_row0);
+    for (int c = cb4; c < ce4; ++c) {
       const int col = t.n0 + 32 * c;
       if (col >= p.I) break;
       if (t.nkb > 0) {
@@ -165,16 +206,14 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, uint32_t tb, int ri
         tmem_ld32(tb + 128 + 32 * c, r1);
         tmem_ld_wait();
       }
-      if (rv) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          v0[i] = t.nkb > 0 ? __uint_as_float(r0[i]) : 0.f;
-          v1[i] = t.nkb > 0 ? __uint_as_float(r1[i]) : 0.f;
-        }
-        const size_t off = (static_cast<size_t>(t.e) * p.H + h_row) * p.I + col;
-        store32_bf16(p.o0 + off, v0);
-        store32_bf16(p.o1 + off, v1);
+      for (int i = 0; i < 32; ++i) {
+        v0[i] = t.nkb > 0 ? __uint_as_float(r0[i]) : 0.f;
+        v1[i] = t.nkb > 0 ? __uint_as_float(r1[i]) : 0.f;
       }
+      const size_t off = (static_cast<size_t>(t.e) * p.H + h_row0) * p.I + col;
+      store_rows32(tile, p.o0 + off, p.I, nvalid, v0);
+      store_rows32(tile, p.o1 + off, p.I, nvalid, v1);
     }
   }
 }

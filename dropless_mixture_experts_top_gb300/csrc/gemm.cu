@@ -23,9 +23,10 @@
 //   warp 0      TMA producer (both CTAs): 128B-swizzled boxes into its ring;
 //               both CTAs' copies complete on CTA 0's barrier
 //   warp 1      CTA 0: MMA issuer (CTA 1's warp 1 only shares the TMEM allocation)
-//   warps 2..5  epilogue (both CTAs): tcgen05.ld of its 128 rows from two
+//   warps 2..    epilogue (both CTAs): tcgen05.ld of its 128 rows from two
 //               double-buffered 256-column accumulators, fused SwiGLU /
-//               dSwiGLU, bf16 stores
+//               dSwiGLU, bf16 stores; 4 warps (one per TMEM lane quarter), 8
+//               for dA (two per quarter, one per column half)
 // Every wait is bounded; on a timeout the kernel flags the status word,
 // drains its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -45,10 +46,17 @@ constexpr int kBBytes = (BN / 2) * BK * 2;    // 16 KB: this CTA's columns of B
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kBox = 64 * 64 * 2;             // one 64x64 bf16 box (MN-major pieces)
 constexpr int kMapsPerExpert = 3;             // ragged K: A, B0, B1
-constexpr int kThreads = 192;
+// Warps: producer, MMA issuer, then 4 epilogue warps (one per TMEM lane
+// quarter), or 8 for dA, whose dSwiGLU epilogue (two loads, two stores per
+// element) outlasts the mainloop with 4; the others run slower with 8.
+__host__ __device__ constexpr int epi_warps(int mode) { return mode == kBwdDA ? 8 : 4; }
+__host__ __device__ constexpr int threads_of(int mode) { return 64 + 32 * epi_warps(mode); }
 constexpr uint32_t kTmemCols = 2 * BN;
-constexpr int kSmemBytes = STAGES * kStageBytes + 1024 /*align*/ + 512 /*barriers*/ +
-                           2 * (kMaxExperts + 1) * 4;
+constexpr int kEpiOff =  // after the barriers and the two [E+1] tables, 16-byte aligned
+    (STAGES * kStageBytes + 512 + 2 * (kMaxExperts + 1) * 4 + 15) / 16 * 16;
+constexpr int kSmemBytes = kEpiOff + 8 * kEpiTileBytes + 1024 /*align*/;
+static_assert(kEpiOff % 16 == 0, "staging tiles 16-byte aligned");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 struct Params {
   int M_rows, H, I, E;
@@ -99,7 +107,7 @@ __device__ __forceinline__ Tile decode_tile(int tile, const Params &p, const int
     t.kcount = 0;
   } else {
     const int per = p.m_tiles * p.n_tiles;
-    t.e = tile / per;
+    t.e = s_tp[tile / per];  // experts in decreasing order of rows
     const int rem = tile % per;
     t.m0 = (rem / p.n_tiles) * (2 * BM);
     t.n0 = (rem % p.n_tiles) * (Tr::kPair ? BN / 2 : BN);
@@ -183,7 +191,7 @@ __device__ __forceinline__ void produce_stage(const Tile &t, int kb, int rank, u
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_of(MODE), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                         const __grid_constant__ CUtensorMap tmA1,
                         const __grid_constant__ CUtensorMap tmB0,
@@ -201,12 +209,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *drain = tempty + 2;          // abort path: MMA completion
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  int *s_tp = reinterpret_cast<int *>(smem + STAGES * kStageBytes + 512);  // [E+1] tile prefix
+  // [E+1] ragged M: tile prefix over experts; ragged K: experts by decreasing row count
+  int *s_tp = reinterpret_cast<int *>(smem + STAGES * kStageBytes + 512);
   int *s_off = s_tp + (kMaxExperts + 1);                                    // [E+1] row offsets
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
   const int rank = static_cast<int>(cluster_ctarank());  // 0: issues the pair's MMAs
+  uint8_t *epi_tiles = smem + kEpiOff;  // [epilogue warp] 32 x 32 bf16 staging tiles
   const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
@@ -216,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 8);  // one arrival per epilogue warp of both CTAs
+      mbar_init(&tempty[b], 2 * epi_warps(MODE));  // one arrival per epilogue warp of both CTAs
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -229,9 +239,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmB1);
   }
   if (warp == 1) tmem_alloc_pair(tmem_slot, kTmemCols);
-  for (int e = threadIdx.x; e <= E; e += kThreads) s_off[e] = __ldg(p.offsets + e);
+  for (int e = threadIdx.x; e <= E; e += threads_of(MODE)) s_off[e] = __ldg(p.offsets + e);
   __syncthreads();
-  if (warp == 2) {  // tile prefix over experts: ceil(rows / 256)
+  if (Tr::kRaggedK) {
+    // Skewed routing (an expert with more than twice the mean rows): longest
+    // reductions first, so the static round-robin hands out the experts' tiles
+    // in decreasing order of work.  Balanced routing keeps the natural order.
+    int cmax = 0;
+    for (int f = 0; f < E; ++f) cmax = max(cmax, s_off[f + 1] - s_off[f]);
+    const bool skewed = static_cast<int64_t>(cmax) * E > 2 * static_cast<int64_t>(s_off[E] - s_off[0]);
+    for (int e = threadIdx.x; e < E; e += threads_of(MODE)) {
+      const int c = s_off[e + 1] - s_off[e];
+      int r = 0;
+      for (int f = 0; f < E; ++f) {
+        const int cf = s_off[f + 1] - s_off[f];
+        r += (cf > c || (cf == c && f < e)) ? 1 : 0;
+      }
+      s_tp[skewed ? r : e] = e;
+    }
+  } else if (warp == 2) {  // tile prefix over experts: ceil(rows / 256)
     int carry = 0;
     for (int base = 0; base < E; base += 32) {
       const int e = base + lane;
@@ -358,6 +384,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    // column range: warps 2..5 the first, 6..9 the second (a constant 0 with 4 warps)
+    const int part = epi_warps(MODE) == 8 ? (warp - 2) >> 2 : 0;
     const int rit = BM * rank + q * 32 + lane;  // row within the pair's 256-row tile
     const uint32_t tempty0 = peer_smem_addr(&tempty[0], 0);
     const uint32_t tempty1 = peer_smem_addr(&tempty[1], 0);
@@ -368,7 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t use = (it >> 1) & 1;
       if (!warp_wait(&tfull[buf], use, abort_flag)) break;
       tc_fence_after();
-      epilogue_tile<MODE>(t, tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16), rit, p);
+      epilogue_tile<MODE>(t, tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16), rit, p,
+                          part, epi_warps(MODE) / 4, epi_tiles + (warp - 2) * kEpiTileBytes);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(buf ? tempty1 : tempty0);
@@ -516,7 +545,7 @@ cudaError_t launch_mode(const GemmArgs &a, cudaStream_t s) {
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads_of(MODE));
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
   cfg.attrs = attr;

@@ -11,12 +11,13 @@
 //
 // One CTA per SM, persistent, static round-robin over 128 x 192 tiles:
 //   warp 0      producer: TMA boxes of codes (128-byte swizzle) and bulk copies
-//               of the scale atoms into a 5-stage ring
+//               of the scale atoms into a 5-stage ring (4 for dA)
 //   warp 1      MMA issuer: per stage, tcgen05.cp of the scale atoms into a
 //               tensor-memory slot (32x128b.warpx4: row r's four block scales
 //               land in lane r%32, column r/32), then four K=32 MMAs selecting
 //               the block's scale byte with the descriptor's scale-factor ids
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator, bf16 stores
+//   warps 2..   epilogue: tcgen05.ld of the accumulator, bf16 stores; 4 warps
+//               (one per TMEM lane quarter), 8 for dA (one per column half)
 // TMEM holds two 192-column accumulators (the epilogue of one tile overlaps
 // the MMAs of the next) and a ring of scale slots.  B-operand scales are
 // grouped per 192 rows (two atoms, the second half used) so every tile's
@@ -32,20 +33,31 @@ namespace {
 
 constexpr int BM = 128, BN = kMxBN;  // 128 x 192 tiles
 constexpr int BKB = 128;             // K per stage in elements (= bytes): one 128-byte swizzle row
-constexpr int STAGES = 5;
+// 5-stage ring; 4 for dA, whose 8 epilogue warps need 8 staging tiles
+__host__ __device__ constexpr int stages_of(int mode) { return mode == 0 ? 4 : 5; }
 constexpr int kABytes = BM * BKB;    // 16 KB
 constexpr int kBBytes = BN * BKB;    // 24 KB
 constexpr int kSfBytes = 512 * 3;    // A atom + two B atoms
 constexpr int kStageBytes = kABytes + kBBytes;  // 40 KB: keeps every stage 1024-byte aligned
-constexpr int kThreads = 192;
+// Warps: producer, MMA issuer, then 4 epilogue warps (one per TMEM lane
+// quarter), or 8 for dA (dSwiGLU epilogue; two warps per quarter).
+__host__ __device__ constexpr int epi_warps(int mode) { return mode == 0 ? 8 : 4; }
+__host__ __device__ constexpr int threads_of(int mode) { return 64 + 32 * epi_warps(mode); }
 constexpr uint32_t kTmemCols = 512;  // accumulators at 0 and BN, scale slots from 2*BN
 constexpr uint32_t kSfCol = 2 * BN, kSfSlotCols = 16;
-constexpr int kSmemBytes =
-    STAGES * (kStageBytes + kSfBytes) + 1024 + 256 + 2 * (kMaxExperts + 1) * 4;
-static_assert(kSfCol + STAGES * kSfSlotCols <= kTmemCols, "TMEM budget");
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+// Shared memory: code stages | scale atoms | barriers (256) | three [E+1]
+// tables | epilogue staging tiles, from a 1024-aligned base.
+__host__ __device__ constexpr int epi_off(int mode) {
+  return (stages_of(mode) * (kStageBytes + kSfBytes) + 256 + 3 * (kMaxExperts + 1) * 4 + 15) / 16 * 16;
+}
+__host__ __device__ constexpr int smem_bytes(int mode) {
+  return epi_off(mode) + epi_warps(mode) * kEpiTileBytes + 1024;
+}
+static_assert(smem_bytes(0) <= 227 * 1024 && smem_bytes(1) <= 227 * 1024, "shared memory budget");
+static_assert(kSfCol + 5 * kSfSlotCols <= kTmemCols, "TMEM budget");
 
 enum MxMode : int { kMxDA = 0, kMxDX = 1, kMxDWDown = 2, kMxDWGateUp = 3 };
+static_assert(kMxDA == 0, "epi_warps");
 
 struct MxParams {
   int H, I, E;
@@ -140,7 +152,7 @@ struct MxTile {
 
 template <int MODE>
 __device__ __forceinline__ MxTile decode_mx(int tile, const MxParams &p, const int *s_off,
-                                            const int *s_pad) {
+                                            const int *s_pad, const int *s_ord) {
   MxTile x;
   Tile &t = x.t;
   x.mat = 0;
@@ -171,7 +183,7 @@ __device__ __forceinline__ MxTile decode_mx(int tile, const MxParams &p, const i
       tile >>= 1;
     }
     const int per = p.m_tiles * p.n_tiles;
-    t.e = tile / per;
+    t.e = s_ord[tile / per];  // experts in decreasing order of rows
     const int rem = tile % per;
     const int nt = rem % p.n_tiles;
     t.m0 = (rem / p.n_tiles) * BM;
@@ -230,11 +242,12 @@ __device__ __forceinline__ void produce_mx(const MxTile &x, int kb, uint8_t *st,
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_of(MODE), 1)
     grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA0,
                            const __grid_constant__ CUtensorMap tmA1,
                            const __grid_constant__ CUtensorMap tmB0,
                            const __grid_constant__ CUtensorMap tmB1, const MxParams p) {
+  constexpr int STAGES = stages_of(MODE);
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -249,6 +262,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *s_off = reinterpret_cast<int *>(sfs + STAGES * kSfBytes + 256);
   int *s_pad = s_off + (kMaxExperts + 1);
+  int *s_ord = s_pad + (kMaxExperts + 1);  // ragged K: experts by decreasing row count
+  uint8_t *epi_tiles = smem + epi_off(MODE);  // [epilogue warp] 32 x 32 bf16 staging tiles
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
 
@@ -259,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 128);
+      mbar_init(&tempty[b], 32 * epi_warps(MODE));  // every epilogue thread
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -272,9 +287,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmB1);
   }
   if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
-  for (int e = threadIdx.x; e <= E; e += kThreads) {
+  for (int e = threadIdx.x; e <= E; e += threads_of(MODE)) {
     s_off[e] = __ldg(p.offsets + e);
     s_pad[e] = __ldg(p.pad_off + e);
+  }
+  __syncthreads();
+  if (MxTraits<MODE>::kRaggedK) {
+    // Skewed routing (an expert with more than twice the mean rows): longest
+    // reductions first, so the static round-robin hands out the experts' tiles
+    // in decreasing order of work.  Balanced routing keeps the natural order.
+    int cmax = 0;
+    for (int f = 0; f < E; ++f) cmax = max(cmax, s_pad[f + 1] - s_pad[f]);
+    const bool skewed = static_cast<int64_t>(cmax) * E > 2 * static_cast<int64_t>(s_pad[E]);
+    for (int e = threadIdx.x; e < E; e += threads_of(MODE)) {
+      const int c = s_pad[e + 1] - s_pad[e];
+      int r = 0;
+      for (int f = 0; f < E; ++f) {
+        const int cf = s_pad[f + 1] - s_pad[f];
+        r += (cf > c || (cf == c && f < e)) ? 1 : 0;
+      }
+      s_ord[skewed ? r : e] = e;
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -292,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t armed = 0, arm_par = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      const MxTile x = decode_mx<MODE>(tile, p, s_off, s_pad);
+      const MxTile x = decode_mx<MODE>(tile, p, s_off, s_pad, s_ord);
       for (int kb = 0; kb < x.t.nkb; ++kb) {
         if (!warp_wait_mx(&empty[stage], phase ^ 1, abort_flag)) {
           ok = false;
@@ -326,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
-      const MxTile x = decode_mx<MODE>(tile, p, s_off, s_pad);
+      const MxTile x = decode_mx<MODE>(tile, p, s_off, s_pad, s_ord);
       const int buf = it & 1;
       const uint32_t use = (it >> 1) & 1;
       if (!warp_wait_mx(&tempty[buf], use ^ 1, abort_flag)) break;
@@ -378,10 +411,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    // column range: warps 2..5 the first, 6..9 the second (a constant 0 with 4 warps)
+    const int part = epi_warps(MODE) == 8 ? (warp - 2) >> 2 : 0;
     const int rit = q * 32 + lane;
     int it = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
-      const MxTile x = decode_mx<MODE>(tile, p, s_off, s_pad);
+      const MxTile x = decode_mx<MODE>(tile, p, s_off, s_pad, s_ord);
       const int buf = it & 1;
       const uint32_t use = (it >> 1) & 1;
       if (!warp_wait_mx(&tfull[buf], use, abort_flag)) break;
@@ -394,7 +429,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         v.o1 = nullptr;
       }
       epilogue_tile<MxTraits<MODE>::kEpi, EpiView, BN / 32>(
-          x.t, tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16), rit, v);
+          x.t, tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16), rit, v, part,
+          epi_warps(MODE) / 4, epi_tiles + (warp - 2) * kEpiTileBytes);
       tc_fence_before();
       mbar_arrive(&tempty[buf]);
     }
@@ -485,11 +521,12 @@ cudaError_t launch_mx_mode(const MxGemmArgs &a, cudaStream_t s) {
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(grouped_gemm_mx_kernel<MODE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(MODE));
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  grouped_gemm_mx_kernel<MODE><<<a.num_sms, kThreads, kSmemBytes, s>>>(mA0, mA1, mB0, mB1, p);
+  grouped_gemm_mx_kernel<MODE><<<a.num_sms, threads_of(MODE), smem_bytes(MODE), s>>>(mA0, mA1, mB0,
+                                                                                    mB1, p);
   return cudaGetLastError();
 }
 
