@@ -9,9 +9,12 @@
 // see keep CUDA graphs usable).
 //
 // Two kernels:
-//   route_topk  : one warp per token.  Top-k by k rounds of warp arg-max
-//                 (ties -> lower expert), fp32 renormalised weights, then per
-//                 block of 128 tokens an expert histogram and every slot's
+//   route_topk  : the block's 128 tokens' logits staged in shared memory;
+//                 four threads per token each keep a sorted top-k list of a
+//                 quarter of the experts in registers (branch-free insertion,
+//                 ties -> lower expert), merged by two shuffle rounds; fp32
+//                 renormalised weights; then per block an expert histogram
+//                 and every slot's
 //                 rank inside its (block, expert) run.  The last block to
 //                 finish (atomic ticket, no spin-wait) scans the histograms:
 //                 counts, offsets, and the first row of every (block, expert)
@@ -28,65 +31,63 @@ namespace moe {
 namespace {
 
 constexpr int TB = kRouteTokensPerBlock;
-constexpr int NW = kRouteThreads / 32;
 
-// Top-k of one token's logits held 8 per lane (lane l holds experts l + 32 i):
-// k rounds of a warp arg-max, larger logit first, lower expert index on ties.
-// Two tokens are processed together so that their shuffle chains overlap.
-template <int NT>
-__device__ __forceinline__ void warp_topk(const float (&v)[NT][8], int npl, int E, int k, int lane,
-                                          int (&sel_i)[NT][kMaxTopK], float (&sel_v)[NT][kMaxTopK]) {
-  uint32_t taken[NT];
+constexpr int kQ = kRouteThreads / TB;  // threads per token (4): each scans a quarter of the experts
+
+// (x, xi) ranks before (tv, ti): larger logit first, lower expert index on
+// ties; an empty slot (ti == INT_MAX) ranks after everything.
+__device__ __forceinline__ bool ranks_before(float x, int xi, float tv, int ti) {
+  return x > tv || (x == tv && xi < ti);
+}
+
+// Insert (x, xi) into a list sorted by ranks_before, keeping its first KMAX
+// entries.  Branch-free: slot j takes slot j-1's entry if x ranks before it,
+// else x if x ranks before slot j's entry, else keeps its own.
+template <int KMAX>
+__device__ __forceinline__ void topk_insert(float (&tv)[KMAX], int (&ti)[KMAX], float x, int xi) {
+  bool before[KMAX];
 #pragma unroll
-  for (int q = 0; q < NT; ++q) taken[q] = 0;
+  for (int j = 0; j < KMAX; ++j) before[j] = ranks_before(x, xi, tv[j], ti[j]);
 #pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) {
-    if (j < k) {
-      float bv[NT];
-      int bi[NT];
-#pragma unroll
-      for (int q = 0; q < NT; ++q) {
-        bv[q] = -INFINITY;
-        bi[q] = INT_MAX;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int e = lane + 32 * i;
-          if (i < npl && e < E && !((taken[q] >> i) & 1u) &&
-              (v[q][i] > bv[q] || (v[q][i] == bv[q] && e < bi[q]))) {
-            bv[q] = v[q][i];
-            bi[q] = e;
-          }
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-        for (int q = 0; q < NT; ++q) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv[q], o);
-          const int oi = __shfl_xor_sync(0xffffffffu, bi[q], o);
-          if (ov > bv[q] || (ov == bv[q] && oi < bi[q])) {
-            bv[q] = ov;
-            bi[q] = oi;
-          }
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < NT; ++q) {
-        if ((bi[q] & 31) == lane) taken[q] |= 1u << (bi[q] >> 5);
-        sel_i[q][j] = bi[q];
-        sel_v[q][j] = bv[q];
-      }
+  for (int j = KMAX - 1; j > 0; --j) {
+    const float v = before[j - 1] ? tv[j - 1] : (before[j] ? x : tv[j]);
+    const int ix = before[j - 1] ? ti[j - 1] : (before[j] ? xi : ti[j]);
+    tv[j] = v;
+    ti[j] = ix;
+  }
+  if (before[0]) {
+    tv[0] = x;
+    ti[0] = xi;
+  }
+}
+
+// The block's logits [ntok, E] (contiguous in memory) into shared memory rows
+// of E + 1 floats (the pad keeps the per-token scans free of bank conflicts).
+__device__ __forceinline__ void stage_logits(const float *__restrict__ src, int n, int E, float *s_lg) {
+  for (int g = 4 * static_cast<int>(threadIdx.x); g < n; g += 4 * kRouteThreads) {
+    float v[4];
+    if (g + 4 <= n) {
+      const float4 q = __ldg(reinterpret_cast<const float4 *>(src + g));
+      v[0] = q.x, v[1] = q.y, v[2] = q.z, v[3] = q.w;
     } else {
 #pragma unroll
-      for (int q = 0; q < NT; ++q) {
-        sel_i[q][j] = 0;
-        sel_v[q][j] = -INFINITY;
+      for (int i = 0; i < 4; ++i) v[i] = g + i < n ? __ldg(src + g + i) : 0.f;
+    }
+    int r = g / E, c = g - r * E;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (g + i < n) s_lg[r * (E + 1) + c] = v[i];
+      if (++c == E) {
+        c = 0;
+        ++r;
       }
     }
   }
 }
 
+template <int KMAX>
 __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(RouteArgs a, int nblk) {
+  extern __shared__ float s_lg[];                     // [TB][E + 1] this block's logits
   __shared__ uint32_t s_mask[TB][kMaxExperts / 32];  // chosen experts of each token, as bits
   __shared__ uint8_t s_pos[TB][kMaxExperts];         // position j of expert e in the token's list
   __shared__ int32_t s_part[kRouteThreads];
@@ -99,57 +100,66 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(RouteArgs a, 
   const int E = a.E, k = a.k, T = a.T;
   const int t0 = blockIdx.x * TB;
   const int ntok = min(TB, T - t0);
-  const int npl = (E + 31) >> 5;  // logits per lane (<= 8)
   bool bad = false;
 
-  for (int tl0 = 2 * warp; tl0 < ntok; tl0 += 2 * NW) {
-    constexpr int NT = 2;
-    float v[NT][8];
+  stage_logits(a.logits + static_cast<size_t>(t0) * E, ntok * E, E, s_lg);
+  __syncthreads();
+
+  // Top-k: kQ threads per token (adjacent lanes), each keeps a sorted list of
+  // its quarter of the experts, then the lists merge by shuffles.
+  {
+    const int tl = threadIdx.x / kQ, qq = threadIdx.x % kQ;
+    const int per = (E + kQ - 1) / kQ;
+    const int e0 = qq * per, e1 = min(E, e0 + per);
+    float tv[KMAX];
+    int ti[KMAX];
 #pragma unroll
-    for (int q = 0; q < NT; ++q) {
-      const int tl = min(tl0 + q, ntok - 1);  // an odd tail repeats the last token
-      const float *lt = a.logits + static_cast<size_t>(t0 + tl) * E;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int e = lane + 32 * i;
-        float x = -INFINITY;
-        if (i < npl && e < E) {
-          x = __ldg(lt + e);
-          if (!isfinite(x)) {
-            bad = true;
-            if (isnan(x)) x = -INFINITY;  // keep the selection well defined
-          }
+    for (int j = 0; j < KMAX; ++j) {
+      tv[j] = -INFINITY;
+      ti[j] = INT_MAX;
+    }
+    if (tl < ntok) {
+      const float *row = s_lg + tl * (E + 1);
+      for (int e = e0; e < e1; ++e) {
+        float x = row[e];
+        if (!isfinite(x)) {
+          bad = true;
+          if (isnan(x)) x = -INFINITY;  // keep the selection well defined
         }
-        v[q][i] = x;
+        topk_insert<KMAX>(tv, ti, x, e);
       }
     }
-    int sel_i[NT][kMaxTopK];
-    float sel_v[NT][kMaxTopK];
-    warp_topk<NT>(v, npl, E, k, lane, sel_i, sel_v);
 #pragma unroll
-    for (int q = 0; q < NT; ++q) {
-      const int tl = tl0 + q;
-      if (tl >= ntok) break;
+    for (int o = 1; o < kQ; o <<= 1) {  // both partners merge the other's list: same result
+      float pv[KMAX];
+      int pi[KMAX];
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        pv[j] = __shfl_xor_sync(0xffffffffu, tv[j], o);
+        pi[j] = __shfl_xor_sync(0xffffffffu, ti[j], o);
+      }
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) topk_insert<KMAX>(tv, ti, pv[j], pi[j]);
+    }
+    if (tl < ntok && qq == 0) {
       const size_t sb = static_cast<size_t>(t0 + tl) * k;
       // renormalised weights: exp(l_j - l_max) / sum over the kept set
-      const float m = sel_v[q][0];
+      const float m = tv[0];
       float ssum = 0.f;
 #pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j)
-        if (j < k) ssum += expf(sel_v[q][j] - m);
-      uint32_t word = 0;
+      for (int j = 0; j < KMAX; ++j)
+        if (j < k) ssum += expf(tv[j] - m);
+      const int npl = (E + 31) >> 5;
+      for (int w = 0; w < npl; ++w) s_mask[tl][w] = 0;
 #pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j) {
+      for (int j = 0; j < KMAX; ++j) {
         if (j < k) {
-          if (lane == j) {
-            a.topk_idx[sb + j] = sel_i[q][j];
-            a.topk_w[sb + j] = expf(sel_v[q][j] - m) / ssum;
-            s_pos[tl][sel_i[q][j]] = static_cast<uint8_t>(j);
-          }
-          if ((sel_i[q][j] >> 5) == lane) word |= 1u << (sel_i[q][j] & 31);
+          a.topk_idx[sb + j] = ti[j];
+          a.topk_w[sb + j] = expf(tv[j] - m) / ssum;
+          s_pos[tl][ti[j]] = static_cast<uint8_t>(j);
+          s_mask[tl][ti[j] >> 5] |= 1u << (ti[j] & 31);
         }
       }
-      if (lane < npl) s_mask[tl][lane] = word;
     }
   }
   if (bad) flag_status(a.status, kDevNonfiniteLogit);
@@ -241,10 +251,27 @@ __global__ void __launch_bounds__(256) route_index_kernel(RouteArgs a) {
 
 int route_num_blocks(int T) { return (T + TB - 1) / TB; }
 
-cudaError_t launch_route_topk(const RouteArgs &a, cudaStream_t s) {
+template <int KMAX>
+cudaError_t launch_topk(const RouteArgs &a, cudaStream_t s) {
   const int nblk = route_num_blocks(a.T);
-  route_topk_kernel<<<nblk, kRouteThreads, 0, s>>>(a, nblk);
+  const size_t smem = static_cast<size_t>(TB) * (a.E + 1) * sizeof(float);
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {  // room for E = 256
+    const cudaError_t e = cudaFuncSetAttribute(route_topk_kernel<KMAX>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               TB * (kMaxExperts + 1) * static_cast<int>(sizeof(float)));
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  route_topk_kernel<KMAX><<<nblk, kRouteThreads, smem, s>>>(a, nblk);
   return cudaGetLastError();
+}
+
+cudaError_t launch_route_topk(const RouteArgs &a, cudaStream_t s) {
+  return a.k <= 8 ? launch_topk<8>(a, s) : launch_topk<kMaxTopK>(a, s);
 }
 
 cudaError_t launch_route_index(const RouteArgs &a, cudaStream_t s) {
