@@ -40,23 +40,40 @@ namespace {
 constexpr int BM = 128;   // rows per CTA (TMEM lanes); a tile is 2*BM rows
 constexpr int BN = 256;   // tile columns (TMEM columns per accumulator); BN/2 per CTA
 constexpr int BK = 64;    // K per stage: one 128-byte swizzle row of bf16
-constexpr int STAGES = 6;
 constexpr int kABytes = BM * BK * 2;          // 16 KB: this CTA's rows of A
 constexpr int kBBytes = (BN / 2) * BK * 2;    // 16 KB: this CTA's columns of B
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kBox = 64 * 64 * 2;             // one 64x64 bf16 box (MN-major pieces)
 constexpr int kMapsPerExpert = 3;             // ragged K: A, B0, B1
 // Warps: producer, MMA issuer, then 4 epilogue warps (one per TMEM lane
-// quarter), or 8 for dA, whose dSwiGLU epilogue (two loads, two stores per
-// element) outlasts the mainloop with 4; the others run slower with 8.
+// quarter).  dA's dSwiGLU epilogue reads G and U and writes dG and dU, so it
+// runs 8 epilogue warps (two per quarter, one per column half) and one more
+// warp that streams each tile's G and U into a shared-memory ring ahead of
+// them; its operand ring has 4 stages to make room.  The other modes run
+// slower with 8 epilogue warps.
+__host__ __device__ constexpr int stages_of(int mode) { return mode == kBwdDA ? 4 : 6; }
 __host__ __device__ constexpr int epi_warps(int mode) { return mode == kBwdDA ? 8 : 4; }
-__host__ __device__ constexpr int threads_of(int mode) { return 64 + 32 * epi_warps(mode); }
+__host__ __device__ constexpr int gu_warps(int mode) { return mode == kBwdDA ? 1 : 0; }
+__host__ __device__ constexpr int threads_of(int mode) {
+  return 64 + 32 * (epi_warps(mode) + gu_warps(mode));
+}
 constexpr uint32_t kTmemCols = 2 * BN;
-constexpr int kEpiOff =  // after the barriers and the two [E+1] tables, 16-byte aligned
-    (STAGES * kStageBytes + 512 + 2 * (kMaxExperts + 1) * 4 + 15) / 16 * 16;
-constexpr int kSmemBytes = kEpiOff + 8 * kEpiTileBytes + 1024 /*align*/;
-static_assert(kEpiOff % 16 == 0, "staging tiles 16-byte aligned");
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+constexpr int kGuSlots = 4;                   // dA: G/U ring of 32-column chunks
+constexpr int kGuHalfBytes = BM * 32 * 2;     // 128 rows x 32 bf16 columns of G (or U): 8 KB
+constexpr int kGuChunkBytes = 2 * kGuHalfBytes;
+// Shared memory (from a 1024-aligned base): operand stages | barriers (512) |
+// two [E+1] tables | epilogue staging tiles | dA: the G/U ring (1024-aligned).
+__host__ __device__ constexpr int epi_off(int mode) {
+  return (stages_of(mode) * kStageBytes + 512 + 2 * (kMaxExperts + 1) * 4 + 15) / 16 * 16;
+}
+__host__ __device__ constexpr int gu_off(int mode) {
+  return (epi_off(mode) + epi_warps(mode) * kEpiTileBytes + 1023) / 1024 * 1024;
+}
+__host__ __device__ constexpr int smem_bytes(int mode) {
+  return gu_off(mode) + gu_warps(mode) * kGuSlots * kGuChunkBytes + 1024 /*align*/;
+}
+static_assert(smem_bytes(kBwdDA) <= 227 * 1024 && smem_bytes(kFwdGateUp) <= 227 * 1024,
+              "shared memory budget");
 
 struct Params {
   int M_rows, H, I, E;
@@ -190,6 +207,64 @@ __device__ __forceinline__ void produce_stage(const Tile &t, int kb, int rank, u
   }
 }
 
+// dA's epilogue for one warp over one tile: its 32 rows, the chunks c of its
+// column half (c % 2 == part), G and U taken from the ring that the G/U warp
+// fills in chunk order (chunk g of the CTA's sequence sits in slot g %
+// kGuSlots; 64-byte rows with the TMA's 64-byte swizzle).  gbase: the CTA's
+// running chunk count, advanced past this tile.  Returns false if a wait gave up.
+__device__ __forceinline__ bool epilogue_da_ring(const Tile &t, uint32_t tb, int rit, int rloc,
+                                                 const Params &p, int part, uint8_t *tile,
+                                                 const uint8_t *ring, uint64_t *gu_full,
+                                                 uint64_t *gu_empty, int &gbase,
+                                                 volatile int *abort_flag) {
+  const int lane = threadIdx.x & 31;
+  const int row = t.m0 + rit, row0 = row - lane;
+  const int nvalid = clamp_rows(t.row_end - row0);
+  const float w = row < t.row_end ? __ldg(p.w_row + row) : 0.f;  // dA = w * (dy . W_down^T)
+  const size_t rowoff = static_cast<size_t>(row0) * p.I;
+  const int nch = min(BN / 32, (p.I - t.n0) / 32);
+  uint32_t r0[32];
+  float v1[32], v2[32];
+  bool ok = true;
+  for (int c = part; c < nch; c += 2) {
+    const int g = gbase + c, slot = g % kGuSlots;
+    if (!warp_wait(&gu_full[slot], static_cast<uint32_t>(g / kGuSlots) & 1u, abort_flag)) {
+      ok = false;
+      break;
+    }
+    const uint8_t *gs = ring + slot * kGuChunkBytes, *us = gs + kGuHalfBytes;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 xg = *reinterpret_cast<const uint4 *>(gs + epi_swz(rloc, q));
+      const uint4 xu = *reinterpret_cast<const uint4 *>(us + epi_swz(rloc, q));
+      const uint32_t wg[4] = {xg.x, xg.y, xg.z, xg.w}, wu[4] = {xu.x, xu.y, xu.z, xu.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        v1[8 * q + 2 * h] = bf16_lo(wg[h]);
+        v1[8 * q + 2 * h + 1] = bf16_hi(wg[h]);
+        v2[8 * q + 2 * h] = bf16_lo(wu[h]);
+        v2[8 * q + 2 * h + 1] = bf16_hi(wu[h]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&gu_empty[slot]);
+    const int col = t.n0 + 32 * c;
+    tmem_ld32(tb + 32 * c, r0);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {  // in place: v1 G -> dU, v2 U -> dG
+      const float da = w * __uint_as_float(r0[i]), gg = v1[i], u = v2[i];
+      const float sg = sigmoidf_(gg);
+      v2[i] = da * u * sg * (1.f + gg * (1.f - sg));  // dG
+      v1[i] = da * gg * sg;                           // dU = dA * silu(G)
+    }
+    store_rows32(tile, p.o0 + rowoff + col, p.I, nvalid, v2);
+    store_rows32(tile, p.o1 + rowoff + col, p.I, nvalid, v1);
+  }
+  gbase += nch;
+  return ok;
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(threads_of(MODE), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
@@ -197,6 +272,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
                         const __grid_constant__ CUtensorMap tmB0,
                         const __grid_constant__ CUtensorMap tmB1, const Params p) {
   using Tr = Traits<MODE>;
+  constexpr int STAGES = stages_of(MODE);
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -207,7 +283,9 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
   uint64_t *tfull = bars + 2 * STAGES;   // [2] accumulator ready (both CTAs)
   uint64_t *tempty = tfull + 2;          // [2] CTA 0 only: both CTAs' epilogues done
   uint64_t *drain = tempty + 2;          // abort path: MMA completion
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  uint64_t *gu_full = drain + 1;         // [kGuSlots] dA: a G/U chunk landed (this CTA)
+  uint64_t *gu_empty = gu_full + kGuSlots;  // [kGuSlots] dA: its 4 epilogue warps read it
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gu_empty + kGuSlots);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   // [E+1] ragged M: tile prefix over experts; ragged K: experts by decreasing row count
   int *s_tp = reinterpret_cast<int *>(smem + STAGES * kStageBytes + 512);
@@ -216,7 +294,8 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
   const int rank = static_cast<int>(cluster_ctarank());  // 0: issues the pair's MMAs
-  uint8_t *epi_tiles = smem + kEpiOff;  // [epilogue warp] 32 x 32 bf16 staging tiles
+  uint8_t *epi_tiles = smem + epi_off(MODE);  // [epilogue warp] 32 x 32 bf16 staging tiles
+  uint8_t *gu_ring = smem + gu_off(MODE);     // dA: [kGuSlots] G chunk | U chunk
   const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
@@ -229,6 +308,10 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
       mbar_init(&tempty[b], 2 * epi_warps(MODE));  // one arrival per epilogue warp of both CTAs
     }
     mbar_init(drain, 1);
+    for (int s = 0; s < kGuSlots; ++s) {
+      mbar_init(&gu_full[s], 1);
+      mbar_init(&gu_empty[s], 4);  // the four warps (lane quarters) of one column half
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -381,7 +464,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
       for (int i = 0; i < (1 << 22) && !mbar_try_wait(drain, 0); ++i) {
       }
     }
-  } else {
+  } else if (warp < 2 + epi_warps(MODE)) {
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     // column range: warps 2..5 the first, 6..9 the second (a constant 0 with 4 warps)
@@ -389,18 +472,60 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
     const int rit = BM * rank + q * 32 + lane;  // row within the pair's 256-row tile
     const uint32_t tempty0 = peer_smem_addr(&tempty[0], 0);
     const uint32_t tempty1 = peer_smem_addr(&tempty[1], 0);
-    int it = 0;
+    int it = 0, gbase = 0;
     for (int tile = cluster; tile < total; tile += nclusters, ++it) {
       const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off);
       const int buf = it & 1;
       const uint32_t use = (it >> 1) & 1;
       if (!warp_wait(&tfull[buf], use, abort_flag)) break;
       tc_fence_after();
-      epilogue_tile<MODE>(t, tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16), rit, p,
-                          part, epi_warps(MODE) / 4, epi_tiles + (warp - 2) * kEpiTileBytes);
+      const uint32_t tb = tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
+      uint8_t *stile = epi_tiles + (warp - 2) * kEpiTileBytes;
+      if constexpr (MODE == kBwdDA) {
+        if (!epilogue_da_ring(t, tb, rit, q * 32 + lane, p, part, stile, gu_ring, gu_full, gu_empty,
+                              gbase, abort_flag))
+          break;
+      } else {
+        epilogue_tile<MODE>(t, tb, rit, p, part, epi_warps(MODE) / 4, stile);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(buf ? tempty1 : tempty0);
+    }
+  } else {
+    // ------------------------------------------------------------ dA: G/U loader (both CTAs)
+    // Walks the tiles in the epilogue's order and loads each tile's G and U,
+    // this CTA's 128 rows, in 32-column chunks into the ring.
+    int g = 0;
+    uint32_t armed = 0, arm_par = 0;
+    bool ok = true;
+    for (int tile = cluster; tile < total && ok; tile += nclusters) {
+      const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off);
+      const int nch = min(BN / 32, (p.I - t.n0) / 32);
+      for (int c = 0; c < nch; ++c, ++g) {
+        const int slot = g % kGuSlots;
+        const uint32_t ph = static_cast<uint32_t>(g / kGuSlots) & 1u;
+        if (!warp_wait(&gu_empty[slot], ph ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          uint8_t *dst = gu_ring + slot * kGuChunkBytes;
+          mbar_arrive_expect_tx(&gu_full[slot], kGuChunkBytes);
+          tma_load_2d(dst, &tmA1, &gu_full[slot], t.n0 + 32 * c, t.m0 + BM * rank);  // G
+          tma_load_2d(dst + kGuHalfBytes, &tmB1, &gu_full[slot], t.n0 + 32 * c, t.m0 + BM * rank);  // U
+        }
+        armed |= 1u << slot;
+        arm_par = (arm_par & ~(1u << slot)) | (ph << slot);
+        __syncwarp();
+      }
+    }
+    if (*abort_flag && lane == 0) {  // let the copies in flight land before exit
+      for (int sl = 0; sl < kGuSlots; ++sl) {
+        if (!((armed >> sl) & 1u)) continue;
+        for (int i = 0; i < (1 << 22) && !mbar_try_wait(&gu_full[sl], (arm_par >> sl) & 1u); ++i) {
+        }
+      }
     }
   }
 
@@ -459,6 +584,20 @@ bool make_map(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t rows, ui
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D bf16 map over G or U [rows, I]: box {32, 128} (64-byte rows), 64-byte
+// swizzle, zero fill out of bounds.
+bool make_map_gu(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t rows) {
+  auto fn = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder());
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {32, static_cast<cuuint32_t>(BM)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int MODE>
 cudaError_t launch_mode(const GemmArgs &a, cudaStream_t s) {
   CUtensorMap mA0, mA1, mB0, mB1;
@@ -491,10 +630,9 @@ cudaError_t launch_mode(const GemmArgs &a, cudaStream_t s) {
       p.kdim = a.I;
       p.n_tiles = (a.H + 255) / 256;
       break;
-    case kBwdDA:
-      ok = make_map(&mA0, a.dy_perm, H, M, 128) && make_map(&mB0, a.W_down, H, E * I, 128);
-      mA1 = mA0;
-      mB1 = mB0;
+    case kBwdDA:  // A1, B1: G and U for the epilogue's ring (32 columns x 128 rows)
+      ok = make_map(&mA0, a.dy_perm, H, M, 128) && make_map(&mB0, a.W_down, H, E * I, 128) &&
+           make_map_gu(&mA1, a.G, I, M) && make_map_gu(&mB1, a.U, I, M);
       p.G = a.G;
       p.U = a.U;
       p.kdim = a.H;
@@ -546,13 +684,14 @@ cudaError_t launch_mode(const GemmArgs &a, cudaStream_t s) {
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.blockDim = dim3(threads_of(MODE));
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem_bytes(MODE);
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (!pair_grid[dev]) {
     cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         smem_bytes(MODE));
     if (e != cudaSuccess) return e;
     cfg.gridDim = dim3(a.num_sms & ~1);
     int clusters = 0;
