@@ -146,9 +146,10 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t *__restr
 // Token-axis quantisation, output transposed: codes [C][Mpad] (tokens
 // contiguous).  A block takes 128 padded rows (one expert's, as segments are
 // 128-aligned) x 64 columns: coalesced 128-byte row loads into shared memory,
-// then one thread per (column, 32-token block) quantises down the column and
-// writes its 32 codes as two 16-byte stores.  Tiles past the padded total are
-// skipped (never read).
+// one thread per (column, 32-token block) quantises down the column into a
+// shared output tile (64 rows of 128 codes, rows padded to 144 bytes against
+// bank conflicts), then the tile leaves as full 128-byte rows.  Tiles past the
+// padded total are skipped (never read).
 constexpr int kQcRows = 128, kQcCols = 64, kQcThreads = 256;
 
 __global__ void __launch_bounds__(kQcThreads) quant_cols_kernel(const uint16_t *__restrict__ src, int C,
@@ -159,8 +160,10 @@ __global__ void __launch_bounds__(kQcThreads) quant_cols_kernel(const uint16_t *
                                                                 uint8_t *__restrict__ sf, SfLayout L) {
   __shared__ int s_pad[kMaxExperts + 1];
   __shared__ __align__(16) uint16_t tile[kQcRows * kQcCols];
+  constexpr int kOutStride = kQcRows + 16;  // bytes per output row in shared memory
+  __shared__ __align__(16) uint8_t otile[kQcCols * kOutStride];
   __shared__ int s_seg[3];  // first source row, valid rows of this tile, skip flag
-  const int prow0 = blockIdx.x * kQcRows, c0 = blockIdx.y * kQcCols;
+  const int prow0 = blockIdx.x * kQcRows;
   for (int e = threadIdx.x; e <= E; e += kQcThreads) s_pad[e] = __ldg(pad_off + e);
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -178,24 +181,35 @@ __global__ void __launch_bounds__(kQcThreads) quant_cols_kernel(const uint16_t *
   __syncthreads();
   if (s_seg[2]) return;
   const int row0 = s_seg[0], nvalid = s_seg[1];
+  // the row tile's setup is shared by every column tile this block takes
+  for (int c0 = blockIdx.y * kQcCols; c0 < C; c0 += gridDim.y * kQcCols) {
 #pragma unroll
-  for (int j = 0; j < (kQcRows * kQcCols / 8) / kQcThreads; ++j) {
-    const int i = threadIdx.x + j * kQcThreads;
-    const int r = i >> 3, part = i & 7;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < nvalid)
-      v = __ldg(reinterpret_cast<const uint4 *>(src + static_cast<size_t>(row0 + r) * C + c0) + part);
-    *reinterpret_cast<uint4 *>(tile + r * kQcCols + part * 8) = v;
+    for (int j = 0; j < (kQcRows * kQcCols / 8) / kQcThreads; ++j) {
+      const int i = threadIdx.x + j * kQcThreads;
+      const int r = i >> 3, part = i & 7;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (r < nvalid)
+        v = __ldg(reinterpret_cast<const uint4 *>(src + static_cast<size_t>(row0 + r) * C + c0) + part);
+      *reinterpret_cast<uint4 *>(tile + r * kQcCols + part * 8) = v;
+    }
+    __syncthreads();
+    const int cc = threadIdx.x % kQcCols, b = threadIdx.x / kQcCols;  // 4 blocks of 32 tokens
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      v[i] = __uint_as_float(static_cast<uint32_t>(tile[(32 * b + i) * kQcCols + cc]) << 16);
+    const int c = c0 + cc, o0 = prow0 + 32 * b;
+    sf[atom_byte(c, o0 >> 5, Mpad, L)] = quant32(v, reinterpret_cast<uint4 *>(otile + cc * kOutStride + 32 * b));
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < (kQcCols * kQcRows / 16) / kQcThreads; ++j) {
+      const int i = threadIdx.x + j * kQcThreads;
+      const int r = i >> 3, part = i & 7;  // output row (column c0 + r), 16-byte piece
+      *reinterpret_cast<uint4 *>(codes + static_cast<size_t>(c0 + r) * Mpad + prow0 + part * 16) =
+          *reinterpret_cast<const uint4 *>(otile + r * kOutStride + part * 16);
+    }
+    __syncthreads();  // otile and tile are rewritten by the next column tile
   }
-  __syncthreads();
-  const int cc = threadIdx.x % kQcCols, b = threadIdx.x / kQcCols;  // 4 blocks of 32 tokens
-  float v[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i)
-    v[i] = __uint_as_float(static_cast<uint32_t>(tile[(32 * b + i) * kQcCols + cc]) << 16);
-  const int c = c0 + cc, o0 = prow0 + 32 * b;
-  sf[atom_byte(c, o0 >> 5, Mpad, L)] =
-      quant32(v, reinterpret_cast<uint4 *>(codes + static_cast<size_t>(c) * Mpad + o0));
 }
 
 // pad_off[e] = sum over e' < e of ceil(count/128)*128; pad_off[E] = padded total.
@@ -237,7 +251,8 @@ cudaError_t launch_quant_rows(const uint16_t *src, int rows_out, int K, const in
 cudaError_t launch_quant_cols(const uint16_t *src, int C, int Mpad, const int32_t *offsets,
                               const int32_t *pad_off, int E, uint8_t *codes, uint8_t *sf, SfLayout L,
                               cudaStream_t s) {
-  const dim3 grid(static_cast<unsigned>(Mpad / kQcRows), static_cast<unsigned>(C / kQcCols));
+  const int col_blocks = C / kQcCols < 4 ? C / kQcCols : 4;  // each loops over C / (64 * 4) column tiles
+  const dim3 grid(static_cast<unsigned>(Mpad / kQcRows), static_cast<unsigned>(col_blocks));
   quant_cols_kernel<<<grid, kQcThreads, 0, s>>>(src, C, Mpad, offsets, pad_off, E, codes, sf, L);
   return cudaGetLastError();
 }
