@@ -150,6 +150,15 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
   return ok != 0;
 }
 
+// Wait for a role whose single issuing lane (lane 0) acts on the barrier's
+// data: lane 0 waits, the result is broadcast, the other lanes do not test the
+// barrier (31 redundant tests cost about 1000 cycles per pipeline stage).
+__device__ __forceinline__ bool warp_wait_lane0(uint64_t *bar, uint32_t parity, volatile int *abort) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 // One box into this CTA's stage, completing on CTA 0's barrier for the stage.
 struct StageLoad {
   uint32_t bar_cl;  // CTA 0's full barrier for the stage (shared::cluster address)
@@ -380,7 +389,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
         __syncwarp();
       }
       for (int kb = 0; kb < t.nkb; ++kb) {
-        if (!warp_wait(&empty[stage], phase ^ 1, abort_flag)) {
+        if (!warp_wait_lane0(&empty[stage], phase ^ 1, abort_flag)) {
           ok = false;
           break;
         }
@@ -418,7 +427,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
       const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off);
       const int buf = it & 1;
       const uint32_t use = (it >> 1) & 1;
-      if (!warp_wait(&tempty[buf], use ^ 1, abort_flag)) break;
+      if (!warp_wait_lane0(&tempty[buf], use ^ 1, abort_flag)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + buf * BN;
       if (t.nkb == 0) {  // empty expert: both epilogues write zeros
@@ -430,7 +439,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
         continue;
       }
       for (int kb = 0; kb < t.nkb; ++kb) {
-        if (!warp_wait(&full[stage], phase, abort_flag)) {
+        if (!warp_wait_lane0(&full[stage], phase, abort_flag)) {
           ok = false;
           break;
         }
@@ -505,7 +514,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
       for (int c = 0; c < nch; ++c, ++g) {
         const int slot = g % kGuSlots;
         const uint32_t ph = static_cast<uint32_t>(g / kGuSlots) & 1u;
-        if (!warp_wait(&gu_empty[slot], ph ^ 1u, abort_flag)) {
+        if (!warp_wait_lane0(&gu_empty[slot], ph ^ 1u, abort_flag)) {
           ok = false;
           break;
         }

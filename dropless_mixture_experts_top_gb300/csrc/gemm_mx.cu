@@ -142,6 +142,15 @@ __device__ __forceinline__ bool warp_wait_mx(uint64_t *bar, uint32_t parity, vol
   return ok != 0;
 }
 
+// Wait for a role whose single issuing lane (lane 0) acts on the barrier's
+// data: lane 0 waits, the result is broadcast, the other lanes do not test the
+// barrier (31 redundant tests cost about 1000 cycles per pipeline stage).
+__device__ __forceinline__ bool warp_wait_mx_lane0(uint64_t *bar, uint32_t parity, volatile int *abort) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 struct MxTile {
   Tile t;       // output placement (unpadded rows) for the shared epilogue
   int arow;     // first row of A in its (padded) operand
@@ -327,7 +336,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       const MxTile x = decode_mx<MODE>(tile, p, s_off, s_pad, s_ord);
       for (int kb = 0; kb < x.t.nkb; ++kb) {
-        if (!warp_wait_mx(&empty[stage], phase ^ 1, abort_flag)) {
+        if (!warp_wait_mx_lane0(&empty[stage], phase ^ 1, abort_flag)) {
           ok = false;
           break;
         }
@@ -362,7 +371,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
       const MxTile x = decode_mx<MODE>(tile, p, s_off, s_pad, s_ord);
       const int buf = it & 1;
       const uint32_t use = (it >> 1) & 1;
-      if (!warp_wait_mx(&tempty[buf], use ^ 1, abort_flag)) break;
+      if (!warp_wait_mx_lane0(&tempty[buf], use ^ 1, abort_flag)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + buf * BN;
       if (x.t.nkb == 0) {  // empty expert: the epilogue writes zeros
@@ -371,7 +380,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
         continue;
       }
       for (int kb = 0; kb < x.t.nkb; ++kb) {
-        if (!warp_wait_mx(&full[stage], phase, abort_flag)) {
+        if (!warp_wait_mx_lane0(&full[stage], phase, abort_flag)) {
           ok = false;
           break;
         }
