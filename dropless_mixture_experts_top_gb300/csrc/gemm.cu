@@ -46,13 +46,16 @@ constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kBox = 64 * 64 * 2;             // one 64x64 bf16 box (MN-major pieces)
 constexpr int kMapsPerExpert = 3;             // ragged K: A, B0, B1
 // Warps: producer, MMA issuer, then 4 epilogue warps (one per TMEM lane
-// quarter).  dA's dSwiGLU epilogue reads G and U and writes dG and dU, so it
-// runs 8 epilogue warps (two per quarter, one per column half) and one more
-// warp that streams each tile's G and U into a shared-memory ring ahead of
-// them; its operand ring has 4 stages to make room.  The other modes run
-// slower with 8 epilogue warps.
+// quarter).  The two epilogue-heavy modes run 8 (two per quarter, one per
+// column half): gate/up writes four outputs per element, and dA's dSwiGLU
+// reads G and U and writes dG and dU -- dA also has a warp that streams each
+// tile's G and U into a shared-memory ring ahead of its epilogue, and an
+// operand ring of 4 stages to make room.  The other modes run slower with 8
+// epilogue warps.
 __host__ __device__ constexpr int stages_of(int mode) { return mode == kBwdDA ? 4 : 6; }
-__host__ __device__ constexpr int epi_warps(int mode) { return mode == kBwdDA ? 8 : 4; }
+__host__ __device__ constexpr int epi_warps(int mode) {
+  return (mode == kBwdDA || mode == kFwdGateUp) ? 8 : 4;
+}
 __host__ __device__ constexpr int gu_warps(int mode) { return mode == kBwdDA ? 1 : 0; }
 __host__ __device__ constexpr int threads_of(int mode) {
   return 64 + 32 * (epi_warps(mode) + gu_warps(mode));
