@@ -50,9 +50,9 @@ constexpr int kMapsPerExpert = 3;             // ragged K: A, B0, B1
 // column half): gate/up writes four outputs per element, and dA's dSwiGLU
 // reads G and U and writes dG and dU -- dA also has a warp that streams each
 // tile's G and U into a shared-memory ring ahead of its epilogue, and an
-// operand ring of 4 stages to make room.  The other modes run slower with 8
+// operand ring of 5 stages to make room.  The other modes run slower with 8
 // epilogue warps.
-__host__ __device__ constexpr int stages_of(int mode) { return mode == kBwdDA ? 4 : 6; }
+__host__ __device__ constexpr int stages_of(int mode) { return mode == kBwdDA ? 5 : 6; }
 __host__ __device__ constexpr int epi_warps(int mode) {
   return (mode == kBwdDA || mode == kFwdGateUp) ? 8 : 4;
 }
@@ -61,7 +61,7 @@ __host__ __device__ constexpr int threads_of(int mode) {
   return 64 + 32 * (epi_warps(mode) + gu_warps(mode));
 }
 constexpr uint32_t kTmemCols = 2 * BN;
-constexpr int kGuSlots = 4;                   // dA: G/U ring of 32-column chunks
+constexpr int kGuSlots = 2;                   // dA: G/U ring of 32-column chunks (one per column half)
 constexpr int kGuHalfBytes = BM * 32 * 2;     // 128 rows x 32 bf16 columns of G (or U): 8 KB
 constexpr int kGuChunkBytes = 2 * kGuHalfBytes;
 // Shared memory (from a 1024-aligned base): operand stages | barriers (512) |
@@ -139,23 +139,10 @@ __device__ __forceinline__ Tile decode_tile(int tile, const Params &p, const int
   return t;
 }
 
-// Warp-uniform bounded wait: lane 0 polls, the result is broadcast, then the
-// other lanes observe the completed phase themselves (acquire).
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
-  const int lane = threadIdx.x & 31;
-  int ok = 1;
-  if (lane == 0) ok = mbar_wait(bar, parity, abort) ? 1 : 0;
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  if (ok && lane != 0) {
-    for (int i = 0; i < (1 << 20) && !mbar_try_wait(bar, parity); ++i) {
-    }
-  }
-  return ok != 0;
-}
-
-// Wait for a role whose single issuing lane (lane 0) acts on the barrier's
-// data: lane 0 waits, the result is broadcast, the other lanes do not test the
-// barrier (31 redundant tests cost about 1000 cycles per pipeline stage).
+// Bounded wait by lane 0 alone; the result is broadcast to the warp.  The
+// other lanes never test the barrier themselves (31 redundant tests of a
+// completed phase cost about 1000 cycles per pipeline stage); lanes that read
+// the barrier's data follow with __syncwarp().
 __device__ __forceinline__ bool warp_wait_lane0(uint64_t *bar, uint32_t parity, volatile int *abort) {
   int ok = 1;
   if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort) ? 1 : 0;
@@ -240,10 +227,11 @@ __device__ __forceinline__ bool epilogue_da_ring(const Tile &t, uint32_t tb, int
   bool ok = true;
   for (int c = part; c < nch; c += 2) {
     const int g = gbase + c, slot = g % kGuSlots;
-    if (!warp_wait(&gu_full[slot], static_cast<uint32_t>(g / kGuSlots) & 1u, abort_flag)) {
+    if (!warp_wait_lane0(&gu_full[slot], static_cast<uint32_t>(g / kGuSlots) & 1u, abort_flag)) {
       ok = false;
       break;
     }
+    __syncwarp();  // the other lanes read the chunk after lane 0 saw it land
     const uint8_t *gs = ring + slot * kGuChunkBytes, *us = gs + kGuHalfBytes;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -489,7 +477,8 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
       const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off);
       const int buf = it & 1;
       const uint32_t use = (it >> 1) & 1;
-      if (!warp_wait(&tfull[buf], use, abort_flag)) break;
+      if (!warp_wait_lane0(&tfull[buf], use, abort_flag)) break;
+      __syncwarp();  // every lane reads the accumulator after lane 0 saw it complete
       tc_fence_after();
       const uint32_t tb = tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
       uint8_t *stile = epi_tiles + (warp - 2) * kEpiTileBytes;

@@ -130,21 +130,10 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint
       : "memory");
 }
 
-__device__ __forceinline__ bool warp_wait_mx(uint64_t *bar, uint32_t parity, volatile int *abort) {
-  const int lane = threadIdx.x & 31;
-  int ok = 1;
-  if (lane == 0) ok = mbar_wait(bar, parity, abort) ? 1 : 0;
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  if (ok && lane != 0) {
-    for (int i = 0; i < (1 << 20) && !mbar_try_wait(bar, parity); ++i) {
-    }
-  }
-  return ok != 0;
-}
-
-// Wait for a role whose single issuing lane (lane 0) acts on the barrier's
-// data: lane 0 waits, the result is broadcast, the other lanes do not test the
-// barrier (31 redundant tests cost about 1000 cycles per pipeline stage).
+// Bounded wait by lane 0 alone; the result is broadcast to the warp.  The
+// other lanes never test the barrier themselves (31 redundant tests of a
+// completed phase cost about 1000 cycles per pipeline stage); lanes that read
+// the barrier's data follow with __syncwarp().
 __device__ __forceinline__ bool warp_wait_mx_lane0(uint64_t *bar, uint32_t parity, volatile int *abort) {
   int ok = 1;
   if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort) ? 1 : 0;
@@ -428,7 +417,8 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
       const MxTile x = decode_mx<MODE>(tile, p, s_off, s_pad, s_ord);
       const int buf = it & 1;
       const uint32_t use = (it >> 1) & 1;
-      if (!warp_wait_mx(&tfull[buf], use, abort_flag)) break;
+      if (!warp_wait_mx_lane0(&tfull[buf], use, abort_flag)) break;
+      __syncwarp();  // every lane reads the accumulator after lane 0 saw it complete
       tc_fence_after();
       EpiView v{p.H, p.I, p.G, p.U, p.w_row, p.o0, p.o1, nullptr, nullptr};
       if (MODE == kMxDWGateUp) {  // [H rows, I columns] of dW_gate or dW_up
