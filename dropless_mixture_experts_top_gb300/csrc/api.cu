@@ -255,6 +255,7 @@ moe_status backward_fp8(const Fp8Bwd &f, cudaStream_t s) {
   m.I = I;
   m.E = E;
   m.Mpad = Mp;
+  m.M = T * k;
   m.offsets = off;
   m.pad_off = pad_off;
   m.G = f.G;

@@ -86,6 +86,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
   }
 }
 
+// Bounded wait by lane 0 alone; the result is broadcast to the warp.  The
+// other lanes never test the barrier themselves (31 redundant tests of a
+// completed phase cost about 1000 cycles per pipeline stage); lanes that read
+// the barrier's data follow with __syncwarp().
+__device__ __forceinline__ bool wait_lane0(uint64_t *bar, uint32_t parity, volatile int *abort) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {

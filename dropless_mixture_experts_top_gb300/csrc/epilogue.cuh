@@ -218,4 +218,72 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, uint32_t tb, int ri
   }
 }
 
+// dA's G/U ring (both GEMM engines): a loader warp streams each tile's G and U,
+// the CTA's 128 rows, in 32-column chunks (64-byte rows, TMA 64-byte swizzle)
+// into kGuSlots slots; the two column halves of epilogue warps take alternate
+// chunks, so each half owns one slot.
+constexpr int kGuSlots = 2;
+constexpr int kGuHalfBytes = 128 * 32 * 2;  // 128 rows x 32 bf16 columns of G (or U): 8 KB
+constexpr int kGuChunkBytes = 2 * kGuHalfBytes;
+
+// dA's epilogue for one warp over one tile: its 32 rows, the chunks c of its
+// column half (c % 2 == part), G and U taken from the ring that the G/U warp
+// fills in chunk order (chunk g of the CTA's sequence sits in slot g %
+// kGuSlots; 64-byte rows with the TMA's 64-byte swizzle).  gbase: the CTA's
+// running chunk count, advanced past this tile.  Returns false if a wait gave up.
+template <class P, int NCH>
+__device__ __forceinline__ bool epilogue_da_ring(const Tile &t, uint32_t tb, int rit, int rloc,
+                                                 const P &p, int part, uint8_t *tile,
+                                                 const uint8_t *ring, uint64_t *gu_full,
+                                                 uint64_t *gu_empty, int &gbase,
+                                                 volatile int *abort_flag) {
+  const int lane = threadIdx.x & 31;
+  const int row = t.m0 + rit, row0 = row - lane;
+  const int nvalid = clamp_rows(t.row_end - row0);
+  const float w = row < t.row_end ? __ldg(p.w_row + row) : 0.f;  // dA = w * (dy . W_down^T)
+  const size_t rowoff = static_cast<size_t>(row0) * p.I;
+  const int nch = min(NCH, (p.I - t.n0) / 32);
+  uint32_t r0[32];
+  float v1[32], v2[32];
+  bool ok = true;
+  for (int c = part; c < nch; c += 2) {
+    const int g = gbase + c, slot = g % kGuSlots;
+    if (!wait_lane0(&gu_full[slot], static_cast<uint32_t>(g / kGuSlots) & 1u, abort_flag)) {
+      ok = false;
+      break;
+    }
+    __syncwarp();  // the other lanes read the chunk after lane 0 saw it land
+    const uint8_t *gs = ring + slot * kGuChunkBytes, *us = gs + kGuHalfBytes;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 xg = *reinterpret_cast<const uint4 *>(gs + epi_swz(rloc, q));
+      const uint4 xu = *reinterpret_cast<const uint4 *>(us + epi_swz(rloc, q));
+      const uint32_t wg[4] = {xg.x, xg.y, xg.z, xg.w}, wu[4] = {xu.x, xu.y, xu.z, xu.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        v1[8 * q + 2 * h] = bf16_lo(wg[h]);
+        v1[8 * q + 2 * h + 1] = bf16_hi(wg[h]);
+        v2[8 * q + 2 * h] = bf16_lo(wu[h]);
+        v2[8 * q + 2 * h + 1] = bf16_hi(wu[h]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&gu_empty[slot]);
+    const int col = t.n0 + 32 * c;
+    tmem_ld32(tb + 32 * c, r0);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {  // in place: v1 G -> dU, v2 U -> dG
+      const float da = w * __uint_as_float(r0[i]), gg = v1[i], u = v2[i];
+      const float sg = sigmoidf_(gg);
+      v2[i] = da * u * sg * (1.f + gg * (1.f - sg));  // dG
+      v1[i] = da * gg * sg;                           // dU = dA * silu(G)
+    }
+    store_rows32(tile, p.o0 + rowoff + col, p.I, nvalid, v2);
+    store_rows32(tile, p.o1 + rowoff + col, p.I, nvalid, v1);
+  }
+  gbase += nch;
+  return ok;
+}
+
 }  // namespace moe

@@ -61,9 +61,6 @@ __host__ __device__ constexpr int threads_of(int mode) {
   return 64 + 32 * (epi_warps(mode) + gu_warps(mode));
 }
 constexpr uint32_t kTmemCols = 2 * BN;
-constexpr int kGuSlots = 2;                   // dA: G/U ring of 32-column chunks (one per column half)
-constexpr int kGuHalfBytes = BM * 32 * 2;     // 128 rows x 32 bf16 columns of G (or U): 8 KB
-constexpr int kGuChunkBytes = 2 * kGuHalfBytes;
 // Shared memory (from a 1024-aligned base): operand stages | barriers (512) |
 // two [E+1] tables | epilogue staging tiles | dA: the G/U ring (1024-aligned).
 __host__ __device__ constexpr int epi_off(int mode) {
@@ -139,16 +136,6 @@ __device__ __forceinline__ Tile decode_tile(int tile, const Params &p, const int
   return t;
 }
 
-// Bounded wait by lane 0 alone; the result is broadcast to the warp.  The
-// other lanes never test the barrier themselves (31 redundant tests of a
-// completed phase cost about 1000 cycles per pipeline stage); lanes that read
-// the barrier's data follow with __syncwarp().
-__device__ __forceinline__ bool warp_wait_lane0(uint64_t *bar, uint32_t parity, volatile int *abort) {
-  int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort) ? 1 : 0;
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
-}
-
 // One box into this CTA's stage, completing on CTA 0's barrier for the stage.
 struct StageLoad {
   uint32_t bar_cl;  // CTA 0's full barrier for the stage (shared::cluster address)
@@ -204,65 +191,6 @@ __device__ __forceinline__ void produce_stage(const Tile &t, int kb, int rank, u
     ld(sb, g, t.n0, r);
     ld(sb + kBox, g, t.n0 + 64, r);
   }
-}
-
-// dA's epilogue for one warp over one tile: its 32 rows, the chunks c of its
-// column half (c % 2 == part), G and U taken from the ring that the G/U warp
-// fills in chunk order (chunk g of the CTA's sequence sits in slot g %
-// kGuSlots; 64-byte rows with the TMA's 64-byte swizzle).  gbase: the CTA's
-// running chunk count, advanced past this tile.  Returns false if a wait gave up.
-__device__ __forceinline__ bool epilogue_da_ring(const Tile &t, uint32_t tb, int rit, int rloc,
-                                                 const Params &p, int part, uint8_t *tile,
-                                                 const uint8_t *ring, uint64_t *gu_full,
-                                                 uint64_t *gu_empty, int &gbase,
-                                                 volatile int *abort_flag) {
-  const int lane = threadIdx.x & 31;
-  const int row = t.m0 + rit, row0 = row - lane;
-  const int nvalid = clamp_rows(t.row_end - row0);
-  const float w = row < t.row_end ? __ldg(p.w_row + row) : 0.f;  // dA = w * (dy . W_down^T)
-  const size_t rowoff = static_cast<size_t>(row0) * p.I;
-  const int nch = min(BN / 32, (p.I - t.n0) / 32);
-  uint32_t r0[32];
-  float v1[32], v2[32];
-  bool ok = true;
-  for (int c = part; c < nch; c += 2) {
-    const int g = gbase + c, slot = g % kGuSlots;
-    if (!warp_wait_lane0(&gu_full[slot], static_cast<uint32_t>(g / kGuSlots) & 1u, abort_flag)) {
-      ok = false;
-      break;
-    }
-    __syncwarp();  // the other lanes read the chunk after lane 0 saw it land
-    const uint8_t *gs = ring + slot * kGuChunkBytes, *us = gs + kGuHalfBytes;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint4 xg = *reinterpret_cast<const uint4 *>(gs + epi_swz(rloc, q));
-      const uint4 xu = *reinterpret_cast<const uint4 *>(us + epi_swz(rloc, q));
-      const uint32_t wg[4] = {xg.x, xg.y, xg.z, xg.w}, wu[4] = {xu.x, xu.y, xu.z, xu.w};
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        v1[8 * q + 2 * h] = bf16_lo(wg[h]);
-        v1[8 * q + 2 * h + 1] = bf16_hi(wg[h]);
-        v2[8 * q + 2 * h] = bf16_lo(wu[h]);
-        v2[8 * q + 2 * h + 1] = bf16_hi(wu[h]);
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&gu_empty[slot]);
-    const int col = t.n0 + 32 * c;
-    tmem_ld32(tb + 32 * c, r0);
-    tmem_ld_wait();
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {  // in place: v1 G -> dU, v2 U -> dG
-      const float da = w * __uint_as_float(r0[i]), gg = v1[i], u = v2[i];
-      const float sg = sigmoidf_(gg);
-      v2[i] = da * u * sg * (1.f + gg * (1.f - sg));  // dG
-      v1[i] = da * gg * sg;                           // dU = dA * silu(G)
-    }
-    store_rows32(tile, p.o0 + rowoff + col, p.I, nvalid, v2);
-    store_rows32(tile, p.o1 + rowoff + col, p.I, nvalid, v1);
-  }
-  gbase += nch;
-  return ok;
 }
 
 template <int MODE>
@@ -380,7 +308,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
         __syncwarp();
       }
       for (int kb = 0; kb < t.nkb; ++kb) {
-        if (!warp_wait_lane0(&empty[stage], phase ^ 1, abort_flag)) {
+        if (!wait_lane0(&empty[stage], phase ^ 1, abort_flag)) {
           ok = false;
           break;
         }
@@ -418,7 +346,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
       const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off);
       const int buf = it & 1;
       const uint32_t use = (it >> 1) & 1;
-      if (!warp_wait_lane0(&tempty[buf], use ^ 1, abort_flag)) break;
+      if (!wait_lane0(&tempty[buf], use ^ 1, abort_flag)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + buf * BN;
       if (t.nkb == 0) {  // empty expert: both epilogues write zeros
@@ -430,7 +358,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
         continue;
       }
       for (int kb = 0; kb < t.nkb; ++kb) {
-        if (!warp_wait_lane0(&full[stage], phase, abort_flag)) {
+        if (!wait_lane0(&full[stage], phase, abort_flag)) {
           ok = false;
           break;
         }
@@ -477,14 +405,14 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
       const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off);
       const int buf = it & 1;
       const uint32_t use = (it >> 1) & 1;
-      if (!warp_wait_lane0(&tfull[buf], use, abort_flag)) break;
+      if (!wait_lane0(&tfull[buf], use, abort_flag)) break;
       __syncwarp();  // every lane reads the accumulator after lane 0 saw it complete
       tc_fence_after();
       const uint32_t tb = tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
       uint8_t *stile = epi_tiles + (warp - 2) * kEpiTileBytes;
       if constexpr (MODE == kBwdDA) {
-        if (!epilogue_da_ring(t, tb, rit, q * 32 + lane, p, part, stile, gu_ring, gu_full, gu_empty,
-                              gbase, abort_flag))
+        if (!epilogue_da_ring<Params, BN / 32>(t, tb, rit, q * 32 + lane, p, part, stile, gu_ring,
+                                               gu_full, gu_empty, gbase, abort_flag))
           break;
       } else {
         epilogue_tile<MODE>(t, tb, rit, p, part, epi_warps(MODE) / 4, stile);
@@ -506,7 +434,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
       for (int c = 0; c < nch; ++c, ++g) {
         const int slot = g % kGuSlots;
         const uint32_t ph = static_cast<uint32_t>(g / kGuSlots) & 1u;
-        if (!warp_wait_lane0(&gu_empty[slot], ph ^ 1u, abort_flag)) {
+        if (!wait_lane0(&gu_empty[slot], ph ^ 1u, abort_flag)) {
           ok = false;
           break;
         }

@@ -40,18 +40,26 @@ constexpr int kBBytes = BN * BKB;    // 24 KB
 constexpr int kSfBytes = 512 * 3;    // A atom + two B atoms
 constexpr int kStageBytes = kABytes + kBBytes;  // 40 KB: keeps every stage 1024-byte aligned
 // Warps: producer, MMA issuer, then 4 epilogue warps (one per TMEM lane
-// quarter), or 8 for dA (dSwiGLU epilogue; two warps per quarter).
+// quarter), or for dA 8 (dSwiGLU epilogue; two warps per quarter) and a
+// loader warp that streams G and U into a shared-memory ring ahead of them.
 __host__ __device__ constexpr int epi_warps(int mode) { return mode == 0 ? 8 : 4; }
-__host__ __device__ constexpr int threads_of(int mode) { return 64 + 32 * epi_warps(mode); }
+__host__ __device__ constexpr int gu_warps(int mode) { return mode == 0 ? 1 : 0; }
+__host__ __device__ constexpr int threads_of(int mode) {
+  return 64 + 32 * (epi_warps(mode) + gu_warps(mode));
+}
 constexpr uint32_t kTmemCols = 512;  // accumulators at 0 and BN, scale slots from 2*BN
 constexpr uint32_t kSfCol = 2 * BN, kSfSlotCols = 16;
 // Shared memory: code stages | scale atoms | barriers (256) | three [E+1]
-// tables | epilogue staging tiles, from a 1024-aligned base.
+// tables | epilogue staging tiles | dA: the G/U ring (1024-aligned), from a
+// 1024-aligned base.
 __host__ __device__ constexpr int epi_off(int mode) {
   return (stages_of(mode) * (kStageBytes + kSfBytes) + 256 + 3 * (kMaxExperts + 1) * 4 + 15) / 16 * 16;
 }
+__host__ __device__ constexpr int gu_off(int mode) {
+  return (epi_off(mode) + epi_warps(mode) * kEpiTileBytes + 1023) / 1024 * 1024;
+}
 __host__ __device__ constexpr int smem_bytes(int mode) {
-  return epi_off(mode) + epi_warps(mode) * kEpiTileBytes + 1024;
+  return gu_off(mode) + gu_warps(mode) * kGuSlots * kGuChunkBytes + 1024;
 }
 static_assert(smem_bytes(0) <= 227 * 1024 && smem_bytes(1) <= 227 * 1024, "shared memory budget");
 static_assert(kSfCol + 5 * kSfSlotCols <= kTmemCols, "TMEM budget");
@@ -128,16 +136,6 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint
           smem_addr(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
-}
-
-// Bounded wait by lane 0 alone; the result is broadcast to the warp.  The
-// other lanes never test the barrier themselves (31 redundant tests of a
-// completed phase cost about 1000 cycles per pipeline stage); lanes that read
-// the barrier's data follow with __syncwarp().
-__device__ __forceinline__ bool warp_wait_mx_lane0(uint64_t *bar, uint32_t parity, volatile int *abort) {
-  int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort) ? 1 : 0;
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
 struct MxTile {
@@ -256,12 +254,15 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
   uint64_t *tfull = bars + 2 * STAGES;  // [2] accumulator ready
   uint64_t *tempty = tfull + 2;         // [2] accumulator drained by the epilogue
   uint64_t *drain = tempty + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  uint64_t *gu_full = drain + 1;            // [kGuSlots] dA: a G/U chunk landed
+  uint64_t *gu_empty = gu_full + kGuSlots;  // [kGuSlots] dA: its 4 epilogue warps read it
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gu_empty + kGuSlots);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *s_off = reinterpret_cast<int *>(sfs + STAGES * kSfBytes + 256);
   int *s_pad = s_off + (kMaxExperts + 1);
   int *s_ord = s_pad + (kMaxExperts + 1);  // ragged K: experts by decreasing row count
   uint8_t *epi_tiles = smem + epi_off(MODE);  // [epilogue warp] 32 x 32 bf16 staging tiles
+  uint8_t *gu_ring = smem + gu_off(MODE);     // dA: [kGuSlots] G chunk | U chunk
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
 
@@ -275,6 +276,10 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
       mbar_init(&tempty[b], 32 * epi_warps(MODE));  // every epilogue thread
     }
     mbar_init(drain, 1);
+    for (int s = 0; s < kGuSlots; ++s) {
+      mbar_init(&gu_full[s], 1);
+      mbar_init(&gu_empty[s], 4);  // the four warps (lane quarters) of one column half
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -325,7 +330,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       const MxTile x = decode_mx<MODE>(tile, p, s_off, s_pad, s_ord);
       for (int kb = 0; kb < x.t.nkb; ++kb) {
-        if (!warp_wait_mx_lane0(&empty[stage], phase ^ 1, abort_flag)) {
+        if (!wait_lane0(&empty[stage], phase ^ 1, abort_flag)) {
           ok = false;
           break;
         }
@@ -360,7 +365,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
       const MxTile x = decode_mx<MODE>(tile, p, s_off, s_pad, s_ord);
       const int buf = it & 1;
       const uint32_t use = (it >> 1) & 1;
-      if (!warp_wait_mx_lane0(&tempty[buf], use ^ 1, abort_flag)) break;
+      if (!wait_lane0(&tempty[buf], use ^ 1, abort_flag)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + buf * BN;
       if (x.t.nkb == 0) {  // empty expert: the epilogue writes zeros
@@ -369,7 +374,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
         continue;
       }
       for (int kb = 0; kb < x.t.nkb; ++kb) {
-        if (!warp_wait_mx_lane0(&full[stage], phase, abort_flag)) {
+        if (!wait_lane0(&full[stage], phase, abort_flag)) {
           ok = false;
           break;
         }
@@ -406,18 +411,18 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
       for (int i = 0; i < (1 << 22) && !mbar_try_wait(drain, 0); ++i) {
       }
     }
-  } else {
+  } else if (warp < 2 + epi_warps(MODE)) {
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     // column range: warps 2..5 the first, 6..9 the second (a constant 0 with 4 warps)
     const int part = epi_warps(MODE) == 8 ? (warp - 2) >> 2 : 0;
     const int rit = q * 32 + lane;
-    int it = 0;
+    int it = 0, gbase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
       const MxTile x = decode_mx<MODE>(tile, p, s_off, s_pad, s_ord);
       const int buf = it & 1;
       const uint32_t use = (it >> 1) & 1;
-      if (!warp_wait_mx_lane0(&tfull[buf], use, abort_flag)) break;
+      if (!wait_lane0(&tfull[buf], use, abort_flag)) break;
       __syncwarp();  // every lane reads the accumulator after lane 0 saw it complete
       tc_fence_after();
       EpiView v{p.H, p.I, p.G, p.U, p.w_row, p.o0, p.o1, nullptr, nullptr};
@@ -427,11 +432,53 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
         v.o0 = x.mat ? p.o1 : p.o0;
         v.o1 = nullptr;
       }
-      epilogue_tile<MxTraits<MODE>::kEpi, EpiView, BN / 32>(
-          x.t, tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16), rit, v, part,
-          epi_warps(MODE) / 4, epi_tiles + (warp - 2) * kEpiTileBytes);
+      const uint32_t tb = tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
+      uint8_t *stile = epi_tiles + (warp - 2) * kEpiTileBytes;
+      if constexpr (MODE == kMxDA) {
+        if (!epilogue_da_ring<EpiView, BN / 32>(x.t, tb, rit, rit, v, part, stile, gu_ring, gu_full,
+                                                gu_empty, gbase, abort_flag))
+          break;
+      } else {
+        epilogue_tile<MxTraits<MODE>::kEpi, EpiView, BN / 32>(x.t, tb, rit, v, part,
+                                                              epi_warps(MODE) / 4, stile);
+      }
       tc_fence_before();
       mbar_arrive(&tempty[buf]);
+    }
+  } else {
+    // ---------------------------------------------------------------- dA: G/U loader
+    // Walks the tiles in the epilogue's order and loads each tile's G and U
+    // (128 rows from the tile's first unpadded row) in 32-column chunks.
+    int g = 0;
+    uint32_t armed = 0, arm_par = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      const MxTile x = decode_mx<MODE>(tile, p, s_off, s_pad, s_ord);
+      const int nch = min(BN / 32, (p.I - x.t.n0) / 32);
+      for (int c = 0; c < nch; ++c, ++g) {
+        const int slot = g % kGuSlots;
+        const uint32_t ph = static_cast<uint32_t>(g / kGuSlots) & 1u;
+        if (!wait_lane0(&gu_empty[slot], ph ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          uint8_t *dst = gu_ring + slot * kGuChunkBytes;
+          mbar_arrive_expect_tx(&gu_full[slot], kGuChunkBytes);
+          tma_load_2d(dst, &tmA1, &gu_full[slot], x.t.n0 + 32 * c, x.t.m0);                 // G
+          tma_load_2d(dst + kGuHalfBytes, &tmB1, &gu_full[slot], x.t.n0 + 32 * c, x.t.m0);  // U
+        }
+        armed |= 1u << slot;
+        arm_par = (arm_par & ~(1u << slot)) | (ph << slot);
+        __syncwarp();
+      }
+    }
+    if (*abort_flag && lane == 0) {  // let the copies in flight land before exit
+      for (int sl = 0; sl < kGuSlots; ++sl) {
+        if (!((armed >> sl) & 1u)) continue;
+        for (int i = 0; i < (1 << 22) && !mbar_try_wait(&gu_full[sl], (arm_par >> sl) & 1u); ++i) {
+        }
+      }
     }
   }
 
@@ -462,6 +509,20 @@ bool make_map_u8(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t rows,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D bf16 map over G or U [rows, I]: box {32, 128} (64-byte rows), 64-byte
+// swizzle, zero fill out of bounds.
+bool make_map_gu_bf16(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t rows) {
+  auto fn = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder());
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {32, static_cast<cuuint32_t>(BM)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 template <int MODE>
@@ -487,10 +548,9 @@ cudaError_t launch_mx_mode(const MxGemmArgs &a, cudaStream_t s) {
   const uint64_t H = a.H, I = a.I, E = a.E, Mp = a.Mpad;
   bool ok = true;
   switch (MODE) {
-    case kMxDA:  // [Mp, H] x [E*I, H]^T
-      ok = make_map_u8(&mA0, a.a0, H, Mp, BM) && make_map_u8(&mB0, a.b0, H, E * I, BN);
-      mA1 = mA0;
-      mB1 = mB0;
+    case kMxDA:  // [Mp, H] x [E*I, H]^T; A1, B1: G and U [M, I] for the epilogue's ring
+      ok = make_map_u8(&mA0, a.a0, H, Mp, BM) && make_map_u8(&mB0, a.b0, H, E * I, BN) &&
+           make_map_gu_bf16(&mA1, a.G, I, a.M) && make_map_gu_bf16(&mB1, a.U, I, a.M);
       p.n_tiles = p.b_gps = cdiv(a.I, BN);
       break;
     case kMxDX:  // [Mp, I] x [E*H, I]^T, twice

@@ -112,6 +112,7 @@ cudaError_t launch_quant_cols(const uint16_t *src, int C, int Mpad, const int32_
 enum MxGemmMode : int { kMxGemmDA = 0, kMxGemmDX = 1, kMxGemmDWDown = 2, kMxGemmDWGateUp = 3 };
 struct MxGemmArgs {
   int H, I, E, Mpad;
+  int M;  // permuted rows T*k (rows of G and U)
   const int32_t *offsets, *pad_off;
   const uint8_t *a0, *a1, *b0, *b1;          // E4M3 codes
   const uint8_t *sfa0, *sfa1, *sfb0, *sfb1;  // scale atoms

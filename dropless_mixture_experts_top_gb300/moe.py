@@ -26,8 +26,9 @@ _lib = None
 
 EXPORTED = [
     "moe_query_workspace", "moe_saved_offsets", "moe_fp8_scratch_offsets", "moe_route",
-    "moe_forward", "moe_backward", "moe_get_device_status", "moe_status_string", "moe_timing_attach", "moe_timing_count",
-    "moe_timing_label",
+    "moe_route_static_scratch", "moe_forward", "moe_backward", "moe_get_device_status",
+    "moe_status_string", "moe_timing_attach", "moe_timing_count", "moe_timing_label",
+    "moe_selftest_wait_timeout",
 ]
 
 
@@ -78,6 +79,8 @@ def lib():
         L.moe_forward.argtypes = [P, P, P, P, P, P, P, P, sz, P, sz, P]
         L.moe_backward.argtypes = [P, P, P, P, P, P, P, P, sz, P, P, P, P, P, P, P, sz, P]
         L.moe_get_device_status.argtypes = [P, P, P]
+        L.moe_selftest_wait_timeout.argtypes = [P, P]
+        L.moe_selftest_wait_timeout.restype = ctypes.c_int
         L.moe_status_string.argtypes = [ctypes.c_int]
         L.moe_status_string.restype = ctypes.c_char_p
         L.moe_timing_attach.argtypes = [P, ctypes.c_int32]
@@ -191,6 +194,11 @@ def get_device_status(scratch, stream=None) -> int:
     if rc not in (MOE_OK, -6):
         _check(rc, "moe_get_device_status")
     return int(code.value)
+
+
+def selftest_wait_timeout(status, stream=None):
+    """Launch the bounded-wait diagnostic; `status` is a device int32 tensor."""
+    _check(lib().moe_selftest_wait_timeout(_ptr(status), _stream(stream)), "moe_selftest_wait_timeout")
 
 
 def timing_attach(events):

@@ -191,6 +191,16 @@ moe_status moe_route_static_scratch(const moe_config *cfg, const float *logits,
                                     const moe_routing *routing, int32_t *device_status,
                                     void *stream);
 
+/* Diagnostic with no counterpart in the paper: launches one kernel that waits,
+ * through the same bounded wait every pipeline stage of the library uses, on
+ * an mbarrier nothing arrives at.  The wait gives up after about two seconds
+ * of SM clock and the kernel sets MOE_DEV_WAIT_TIMEOUT in *device_status
+ * (device int32, 4-byte aligned, zeroed on `stream` first).  It shows that a
+ * lost arrival is reported as a status instead of hanging the GPU, and that
+ * the context stays usable afterwards.  Returns MOE_ERR_INVALID_ARG for a
+ * NULL pointer; asynchronous on `stream`. */
+moe_status moe_selftest_wait_timeout(int32_t *device_status, void *stream);
+
 /* Waits for `stream`, then reads the status word at the start of `scratch` (a
  * scratch buffer previously passed to moe_route, moe_forward or moe_backward).
  * *host_code receives the MOE_DEV_* flags; returns MOE_OK when they are zero,
