@@ -294,79 +294,76 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
-    const uint32_t full_cl0 = peer_smem_addr(&full[0], 0);  // CTA 0's full[] (direct mode)
-    int stage = 0;
-    uint32_t phase = 0;
-    uint32_t armed = 0, arm_par = 0;  // per stage: armed at least once, parity of last arm
-    bool ok = true;
-    for (int tile = cluster; tile < total && ok; tile += nclusters) {
-      const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off);
-      if constexpr (Tr::kRaggedK) {  // this expert's maps were written by the preceding launch;
-        // the thread that issues the copies acquires every map it will use
-        if (lane == 0 && t.nkb > 0)
-          for (int j = 0; j < kMapsPerExpert; ++j) tmap_acquire(p.expert_maps + t.e * kMapsPerExpert + j);
-        __syncwarp();
-      }
-      for (int kb = 0; kb < t.nkb; ++kb) {
-        if (!wait_lane0(&empty[stage], phase ^ 1, abort_flag)) {
-          ok = false;
-          break;
+    // Lane 0 runs the loop alone: no warp collective per stage.
+    if (lane == 0) {
+      const uint32_t full_cl0 = peer_smem_addr(&full[0], 0);  // CTA 0's full[] (direct mode)
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, arm_par = 0;  // per stage: armed at least once, parity of last arm
+      bool ok = true;
+      for (int tile = cluster; tile < total && ok; tile += nclusters) {
+        const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off);
+        if constexpr (Tr::kRaggedK) {  // this expert's maps were written by the preceding
+          // launch; the thread that issues the copies acquires every map it will use
+          if (t.nkb > 0)
+            for (int j = 0; j < kMapsPerExpert; ++j) tmap_acquire(p.expert_maps + t.e * kMapsPerExpert + j);
         }
-        if (lane == 0) {
+        for (int kb = 0; kb < t.nkb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
           uint8_t *sa = stages + stage * kStageBytes;
           if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);  // both CTAs' bytes
           const StageLoad ld{full_cl0 + 8u * stage};
           produce_stage<MODE>(t, kb, rank, sa, sa + kABytes, ld, p, &tmA0, &tmA1, &tmB0, &tmB1);
+          armed |= 1u << stage;
+          arm_par = (arm_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
         }
-        armed |= 1u << stage;
-        arm_par = (arm_par & ~(1u << stage)) | (phase << stage);
-        __syncwarp();
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1;
+      }
+      if (*abort_flag && rank == 0) {  // let the pair's copies land before exit
+        for (int s = 0; s < STAGES; ++s) {
+          if (!((armed >> s) & 1u)) continue;
+          for (int i = 0; i < (1 << 22) && !mbar_try_wait(&full[s], (arm_par >> s) & 1u); ++i) {
+          }
         }
       }
     }
-    if (*abort_flag && lane == 0 && rank == 0) {  // let the pair's copies land before exit
-      for (int s = 0; s < STAGES; ++s) {
-        if (!((armed >> s) & 1u)) continue;
-        for (int i = 0; i < (1 << 22) && !mbar_try_wait(&full[s], (arm_par >> s) & 1u); ++i) {
-        }
-      }
-    }
+    __syncwarp();
   } else if (warp == 1 && rank == 1) {
     // CTA 1's warp 1 holds the pair's TMEM allocation with CTA 0's warp 1
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (CTA 0)
-    int stage = 0;
-    uint32_t phase = 0;
-    int it = 0;
-    bool ok = true;
-    for (int tile = cluster; tile < total && ok; tile += nclusters, ++it) {
-      const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off);
-      const int buf = it & 1;
-      const uint32_t use = (it >> 1) & 1;
-      if (!wait_lane0(&tempty[buf], use ^ 1, abort_flag)) break;
-      tc_fence_after();
-      const uint32_t d_tmem = tmem_base + buf * BN;
-      if (t.nkb == 0) {  // empty expert: both epilogues write zeros
-        if (lane == 0) {
+    // Lane 0 runs the loop alone: no warp collective per stage.
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int tile = cluster; tile < total && ok; tile += nclusters, ++it) {
+        const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off);
+        const int buf = it & 1;
+        const uint32_t use = (it >> 1) & 1;
+        if (!mbar_wait(&tempty[buf], use ^ 1, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * BN;
+        if (t.nkb == 0) {  // empty expert: both epilogues write zeros
           mbar_arrive(&tfull[buf]);
           mbar_arrive_cluster(peer_smem_addr(&tfull[buf], 1));
+          continue;
         }
-        __syncwarp();
-        continue;
-      }
-      for (int kb = 0; kb < t.nkb; ++kb) {
-        if (!wait_lane0(&full[stage], phase, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        uint8_t *sa = stages + stage * kStageBytes;
-        uint8_t *sb = sa + kABytes;
-        if (lane == 0) {
-          const uint32_t a_base = smem_addr(sa), b_base = smem_addr(sb);
+        for (int kb = 0; kb < t.nkb; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_addr(stages + stage * kStageBytes);
+          const uint32_t b_base = a_base + kABytes;
 #pragma unroll
           for (int k16 = 0; k16 < BK / 16; ++k16) {
             const uint64_t adesc = Tr::kAMN ? smem_desc_sw128(a_base + k16 * 2048, kBox, 1024)
@@ -376,22 +373,21 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
             tc_mma_f16_pair(d_tmem, adesc, bdesc, Tr::kIdesc, (kb | k16) != 0 ? 1u : 0u);
           }
           tc_commit_pair(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
         }
-        __syncwarp();
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1;
+        if (!ok) break;
+        tc_commit_pair(&tfull[buf]);
+      }
+      if (*abort_flag) {  // wait for the pair's MMAs before TMEM is freed
+        tc_commit_pair(drain);
+        for (int i = 0; i < (1 << 22) && !mbar_try_wait(drain, 0); ++i) {
         }
       }
-      if (!ok) break;
-      if (lane == 0) tc_commit_pair(&tfull[buf]);
-      __syncwarp();
     }
-    if (*abort_flag && lane == 0) {  // wait for the pair's MMAs before TMEM is freed
-      tc_commit_pair(drain);
-      for (int i = 0; i < (1 << 22) && !mbar_try_wait(drain, 0); ++i) {
-      }
-    }
+    __syncwarp();
   } else if (warp < 2 + epi_warps(MODE)) {
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -424,38 +420,38 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
   } else {
     // ------------------------------------------------------------ dA: G/U loader (both CTAs)
     // Walks the tiles in the epilogue's order and loads each tile's G and U,
-    // this CTA's 128 rows, in 32-column chunks into the ring.
-    int g = 0;
-    uint32_t armed = 0, arm_par = 0;
-    bool ok = true;
-    for (int tile = cluster; tile < total && ok; tile += nclusters) {
-      const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off);
-      const int nch = min(BN / 32, (p.I - t.n0) / 32);
-      for (int c = 0; c < nch; ++c, ++g) {
-        const int slot = g % kGuSlots;
-        const uint32_t ph = static_cast<uint32_t>(g / kGuSlots) & 1u;
-        if (!wait_lane0(&gu_empty[slot], ph ^ 1u, abort_flag)) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) {
+    // this CTA's 128 rows, in 32-column chunks into the ring (lane 0 alone).
+    if (lane == 0) {
+      int g = 0;
+      uint32_t armed = 0, arm_par = 0;
+      bool ok = true;
+      for (int tile = cluster; tile < total && ok; tile += nclusters) {
+        const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off);
+        const int nch = min(BN / 32, (p.I - t.n0) / 32);
+        for (int c = 0; c < nch; ++c, ++g) {
+          const int slot = g % kGuSlots;
+          const uint32_t ph = static_cast<uint32_t>(g / kGuSlots) & 1u;
+          if (!mbar_wait(&gu_empty[slot], ph ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
           uint8_t *dst = gu_ring + slot * kGuChunkBytes;
           mbar_arrive_expect_tx(&gu_full[slot], kGuChunkBytes);
           tma_load_2d(dst, &tmA1, &gu_full[slot], t.n0 + 32 * c, t.m0 + BM * rank);  // G
           tma_load_2d(dst + kGuHalfBytes, &tmB1, &gu_full[slot], t.n0 + 32 * c, t.m0 + BM * rank);  // U
-        }
-        armed |= 1u << slot;
-        arm_par = (arm_par & ~(1u << slot)) | (ph << slot);
-        __syncwarp();
-      }
-    }
-    if (*abort_flag && lane == 0) {  // let the copies in flight land before exit
-      for (int sl = 0; sl < kGuSlots; ++sl) {
-        if (!((armed >> sl) & 1u)) continue;
-        for (int i = 0; i < (1 << 22) && !mbar_try_wait(&gu_full[sl], (arm_par >> sl) & 1u); ++i) {
+          armed |= 1u << slot;
+          arm_par = (arm_par & ~(1u << slot)) | (ph << slot);
         }
       }
+      if (*abort_flag) {  // let the copies in flight land before exit
+        for (int sl = 0; sl < kGuSlots; ++sl) {
+          if (!((armed >> sl) & 1u)) continue;
+          for (int i = 0; i < (1 << 22) && !mbar_try_wait(&gu_full[sl], (arm_par >> sl) & 1u); ++i) {
+          }
+        }
+      }
     }
+    __syncwarp();
   }
 
   tc_fence_before();

@@ -323,63 +323,64 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
-    int stage = 0;
-    uint32_t phase = 0;
-    uint32_t armed = 0, arm_par = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      const MxTile x = decode_mx<MODE>(tile, p, s_off, s_pad, s_ord);
-      for (int kb = 0; kb < x.t.nkb; ++kb) {
-        if (!wait_lane0(&empty[stage], phase ^ 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) {
+    // Lane 0 runs the loop alone: no warp collective per stage.
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, arm_par = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const MxTile x = decode_mx<MODE>(tile, p, s_off, s_pad, s_ord);
+        for (int kb = 0; kb < x.t.nkb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
           mbar_arrive_expect_tx(&full[stage], kTx);
-          produce_mx<MODE>(x, kb, stages + stage * kStageBytes, sfs + stage * kSfBytes,
-                           &full[stage], p, &tmA0, &tmA1, &tmB0, &tmB1);
+          produce_mx<MODE>(x, kb, stages + stage * kStageBytes, sfs + stage * kSfBytes, &full[stage],
+                           p, &tmA0, &tmA1, &tmB0, &tmB1);
+          armed |= 1u << stage;
+          arm_par = (arm_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
         }
-        armed |= 1u << stage;
-        arm_par = (arm_par & ~(1u << stage)) | (phase << stage);
-        __syncwarp();
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1;
+      }
+      if (*abort_flag) {  // let the copies in flight land before the CTA exits
+        for (int s = 0; s < STAGES; ++s) {
+          if (!((armed >> s) & 1u)) continue;
+          for (int i = 0; i < (1 << 22) && !mbar_try_wait(&full[s], (arm_par >> s) & 1u); ++i) {
+          }
         }
       }
     }
-    if (*abort_flag && lane == 0) {  // let the copies in flight land before the CTA exits
-      for (int s = 0; s < STAGES; ++s) {
-        if (!((armed >> s) & 1u)) continue;
-        for (int i = 0; i < (1 << 22) && !mbar_try_wait(&full[s], (arm_par >> s) & 1u); ++i) {
-        }
-      }
-    }
+    __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
-    int stage = 0;
-    uint32_t phase = 0;
-    int it = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
-      const MxTile x = decode_mx<MODE>(tile, p, s_off, s_pad, s_ord);
-      const int buf = it & 1;
-      const uint32_t use = (it >> 1) & 1;
-      if (!wait_lane0(&tempty[buf], use ^ 1, abort_flag)) break;
-      tc_fence_after();
-      const uint32_t d_tmem = tmem_base + buf * BN;
-      if (x.t.nkb == 0) {  // empty expert: the epilogue writes zeros
-        if (lane == 0) mbar_arrive(&tfull[buf]);
-        __syncwarp();
-        continue;
-      }
-      for (int kb = 0; kb < x.t.nkb; ++kb) {
-        if (!wait_lane0(&full[stage], phase, abort_flag)) {
-          ok = false;
-          break;
-        }
+    // Lane 0 runs the loop alone: no warp collective per stage.
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+        const MxTile x = decode_mx<MODE>(tile, p, s_off, s_pad, s_ord);
+        const int buf = it & 1;
+        const uint32_t use = (it >> 1) & 1;
+        if (!mbar_wait(&tempty[buf], use ^ 1, abort_flag)) break;
         tc_fence_after();
-        if (lane == 0) {
+        const uint32_t d_tmem = tmem_base + buf * BN;
+        if (x.t.nkb == 0) {  // empty expert: the epilogue writes zeros
+          mbar_arrive(&tfull[buf]);
+          continue;
+        }
+        for (int kb = 0; kb < x.t.nkb; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
           uint8_t *st = stages + stage * kStageBytes;
           uint8_t *sf = sfs + stage * kSfBytes;
           const uint32_t slot = tmem_base + kSfCol + kSfSlotCols * stage;
@@ -391,26 +392,24 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
           for (int k32 = 0; k32 < BKB / 32; ++k32) {
             const uint64_t adesc = smem_desc_sw128(a_base + k32 * 32, 16, 1024);
             const uint64_t bdesc = smem_desc_sw128(b_base + k32 * 32, 16, 1024);
-            tc_mma_mx(d_tmem, adesc, bdesc, idesc_mx(k32), slot, slot + 4,
-                      (kb | k32) != 0 ? 1u : 0u);
+            tc_mma_mx(d_tmem, adesc, bdesc, idesc_mx(k32), slot, slot + 4, (kb | k32) != 0 ? 1u : 0u);
           }
           tc_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
         }
-        __syncwarp();
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1;
+        if (!ok) break;
+        tc_commit(&tfull[buf]);
+      }
+      if (*abort_flag) {  // wait for issued MMAs before TMEM is freed
+        tc_commit(drain);
+        for (int i = 0; i < (1 << 22) && !mbar_try_wait(drain, 0); ++i) {
         }
       }
-      if (!ok) break;
-      if (lane == 0) tc_commit(&tfull[buf]);
-      __syncwarp();
     }
-    if (*abort_flag && lane == 0) {  // wait for issued MMAs before TMEM is freed
-      tc_commit(drain);
-      for (int i = 0; i < (1 << 22) && !mbar_try_wait(drain, 0); ++i) {
-      }
-    }
+    __syncwarp();
   } else if (warp < 2 + epi_warps(MODE)) {
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -448,38 +447,39 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
   } else {
     // ---------------------------------------------------------------- dA: G/U loader
     // Walks the tiles in the epilogue's order and loads each tile's G and U
-    // (128 rows from the tile's first unpadded row) in 32-column chunks.
-    int g = 0;
-    uint32_t armed = 0, arm_par = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      const MxTile x = decode_mx<MODE>(tile, p, s_off, s_pad, s_ord);
-      const int nch = min(BN / 32, (p.I - x.t.n0) / 32);
-      for (int c = 0; c < nch; ++c, ++g) {
-        const int slot = g % kGuSlots;
-        const uint32_t ph = static_cast<uint32_t>(g / kGuSlots) & 1u;
-        if (!wait_lane0(&gu_empty[slot], ph ^ 1u, abort_flag)) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) {
+    // (128 rows from the tile's first unpadded row) in 32-column chunks
+    // (lane 0 alone).
+    if (lane == 0) {
+      int g = 0;
+      uint32_t armed = 0, arm_par = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const MxTile x = decode_mx<MODE>(tile, p, s_off, s_pad, s_ord);
+        const int nch = min(BN / 32, (p.I - x.t.n0) / 32);
+        for (int c = 0; c < nch; ++c, ++g) {
+          const int slot = g % kGuSlots;
+          const uint32_t ph = static_cast<uint32_t>(g / kGuSlots) & 1u;
+          if (!mbar_wait(&gu_empty[slot], ph ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
           uint8_t *dst = gu_ring + slot * kGuChunkBytes;
           mbar_arrive_expect_tx(&gu_full[slot], kGuChunkBytes);
           tma_load_2d(dst, &tmA1, &gu_full[slot], x.t.n0 + 32 * c, x.t.m0);                 // G
           tma_load_2d(dst + kGuHalfBytes, &tmB1, &gu_full[slot], x.t.n0 + 32 * c, x.t.m0);  // U
-        }
-        armed |= 1u << slot;
-        arm_par = (arm_par & ~(1u << slot)) | (ph << slot);
-        __syncwarp();
-      }
-    }
-    if (*abort_flag && lane == 0) {  // let the copies in flight land before exit
-      for (int sl = 0; sl < kGuSlots; ++sl) {
-        if (!((armed >> sl) & 1u)) continue;
-        for (int i = 0; i < (1 << 22) && !mbar_try_wait(&gu_full[sl], (arm_par >> sl) & 1u); ++i) {
+          armed |= 1u << slot;
+          arm_par = (arm_par & ~(1u << slot)) | (ph << slot);
         }
       }
+      if (*abort_flag) {  // let the copies in flight land before exit
+        for (int sl = 0; sl < kGuSlots; ++sl) {
+          if (!((armed >> sl) & 1u)) continue;
+          for (int i = 0; i < (1 << 22) && !mbar_try_wait(&gu_full[sl], (arm_par >> sl) & 1u); ++i) {
+          }
+        }
+      }
     }
+    __syncwarp();
   }
 
   tc_fence_before();
