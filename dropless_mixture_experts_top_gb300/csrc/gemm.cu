@@ -39,10 +39,14 @@ namespace {
 
 constexpr int BM = 128;   // rows per CTA (TMEM lanes); a tile is 2*BM rows
 constexpr int BN = 256;   // tile columns (TMEM columns per accumulator); BN/2 per CTA
-constexpr int BK = 64;    // K per stage: one 128-byte swizzle row of bf16
-constexpr int kABytes = BM * BK * 2;          // 16 KB: this CTA's rows of A
-constexpr int kBBytes = (BN / 2) * BK * 2;    // 16 KB: this CTA's columns of B
-constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int BK = 64;    // K per operand box: one 128-byte swizzle row of bf16
+constexpr int kABox = BM * BK * 2;            // 16 KB: this CTA's rows of A for 64 of K
+constexpr int kBBox = (BN / 2) * BK * 2;      // 16 KB: this CTA's columns of B for 64 of K
+// A pipeline stage holds HALVES consecutive 64-wide K blocks of both operands
+// ([A k0 | A k1 | B k0 | B k1]): 128 of K, so eight MMAs per barrier round
+// trip; dA keeps 64 (its shared memory also holds the G/U ring).
+__host__ __device__ constexpr int halves_of(int mode) { return mode == kBwdDA ? 1 : 2; }
+__host__ __device__ constexpr int stage_bytes(int mode) { return halves_of(mode) * (kABox + kBBox); }
 constexpr int kBox = 64 * 64 * 2;             // one 64x64 bf16 box (MN-major pieces)
 constexpr int kMapsPerExpert = 3;             // ragged K: A, B0, B1
 // Warps: producer, MMA issuer, then 4 epilogue warps (one per TMEM lane
@@ -52,7 +56,7 @@ constexpr int kMapsPerExpert = 3;             // ragged K: A, B0, B1
 // tile's G and U into a shared-memory ring ahead of its epilogue, and an
 // operand ring of 5 stages to make room.  The other modes run slower with 8
 // epilogue warps.
-__host__ __device__ constexpr int stages_of(int mode) { return mode == kBwdDA ? 5 : 6; }
+__host__ __device__ constexpr int stages_of(int mode) { return mode == kBwdDA ? 5 : 3; }
 __host__ __device__ constexpr int epi_warps(int mode) {
   return (mode == kBwdDA || mode == kFwdGateUp) ? 8 : 4;
 }
@@ -64,7 +68,7 @@ constexpr uint32_t kTmemCols = 2 * BN;
 // Shared memory (from a 1024-aligned base): operand stages | barriers (512) |
 // two [E+1] tables | epilogue staging tiles | dA: the G/U ring (1024-aligned).
 __host__ __device__ constexpr int epi_off(int mode) {
-  return (stages_of(mode) * kStageBytes + 512 + 2 * (kMaxExperts + 1) * 4 + 15) / 16 * 16;
+  return (stages_of(mode) * stage_bytes(mode) + 512 + 2 * (kMaxExperts + 1) * 4 + 15) / 16 * 16;
 }
 __host__ __device__ constexpr int gu_off(int mode) {
   return (epi_off(mode) + epi_warps(mode) * kEpiTileBytes + 1023) / 1024 * 1024;
@@ -200,7 +204,8 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
                         const __grid_constant__ CUtensorMap tmB0,
                         const __grid_constant__ CUtensorMap tmB1, const Params p) {
   using Tr = Traits<MODE>;
-  constexpr int STAGES = stages_of(MODE);
+  constexpr int STAGES = stages_of(MODE), HALVES = halves_of(MODE);
+  constexpr int kStageBytes = stage_bytes(MODE), kABytes = HALVES * kABox;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -308,7 +313,8 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
           if (t.nkb > 0)
             for (int j = 0; j < kMapsPerExpert; ++j) tmap_acquire(p.expert_maps + t.e * kMapsPerExpert + j);
         }
-        for (int kb = 0; kb < t.nkb; ++kb) {
+        const int nstage = (t.nkb + HALVES - 1) / HALVES;
+        for (int ks = 0; ks < nstage; ++ks) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
             ok = false;
             break;
@@ -316,7 +322,12 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
           uint8_t *sa = stages + stage * kStageBytes;
           if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);  // both CTAs' bytes
           const StageLoad ld{full_cl0 + 8u * stage};
-          produce_stage<MODE>(t, kb, rank, sa, sa + kABytes, ld, p, &tmA0, &tmA1, &tmB0, &tmB1);
+          // a K block past the end (odd count of 64-blocks) loads zero fill or rows
+          // that no MMA reads, so every stage carries the same bytes
+#pragma unroll
+          for (int h = 0; h < HALVES; ++h)
+            produce_stage<MODE>(t, ks * HALVES + h, rank, sa + h * kABox, sa + kABytes + h * kBBox, ld,
+                                p, &tmA0, &tmA1, &tmB0, &tmB1);
           armed |= 1u << stage;
           arm_par = (arm_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -356,7 +367,8 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
           mbar_arrive_cluster(peer_smem_addr(&tfull[buf], 1));
           continue;
         }
-        for (int kb = 0; kb < t.nkb; ++kb) {
+        const int nstage = (t.nkb + HALVES - 1) / HALVES;
+        for (int ks = 0; ks < nstage; ++ks) {
           if (!mbar_wait(&full[stage], phase, abort_flag)) {
             ok = false;
             break;
@@ -364,13 +376,18 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
           tc_fence_after();
           const uint32_t a_base = smem_addr(stages + stage * kStageBytes);
           const uint32_t b_base = a_base + kABytes;
+          const int nk16 = (BK / 16) * min(HALVES, t.nkb - ks * HALVES);  // K steps inside K
 #pragma unroll
-          for (int k16 = 0; k16 < BK / 16; ++k16) {
-            const uint64_t adesc = Tr::kAMN ? smem_desc_sw128(a_base + k16 * 2048, kBox, 1024)
-                                            : smem_desc_sw128(a_base + k16 * 32, 16, 1024);
-            const uint64_t bdesc = Tr::kBMN ? smem_desc_sw128(b_base + k16 * 2048, kBox, 1024)
-                                            : smem_desc_sw128(b_base + k16 * 32, 16, 1024);
-            tc_mma_f16_pair(d_tmem, adesc, bdesc, Tr::kIdesc, (kb | k16) != 0 ? 1u : 0u);
+          for (int k16 = 0; k16 < HALVES * (BK / 16); ++k16) {
+            if (k16 < nk16) {
+              const int h = k16 / (BK / 16), j = k16 % (BK / 16);
+              const uint32_t ab = a_base + h * kABox, bb = b_base + h * kBBox;
+              const uint64_t adesc = Tr::kAMN ? smem_desc_sw128(ab + j * 2048, kBox, 1024)
+                                              : smem_desc_sw128(ab + j * 32, 16, 1024);
+              const uint64_t bdesc = Tr::kBMN ? smem_desc_sw128(bb + j * 2048, kBox, 1024)
+                                              : smem_desc_sw128(bb + j * 32, 16, 1024);
+              tc_mma_f16_pair(d_tmem, adesc, bdesc, Tr::kIdesc, (ks | k16) != 0 ? 1u : 0u);
+            }
           }
           tc_commit_pair(&empty[stage]);
           if (++stage == STAGES) {
