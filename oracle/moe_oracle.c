@@ -704,3 +704,53 @@ EXPORT int oracle_dw_elements(const oracle_shape *sh, const uint16_t *x, const i
   }
   return bad ? -1 : 0;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Router projection: the learned router's linear layer, logits = x . W_r.    */
+/* ------------------------------------------------------------------------- */
+
+/* logits[t, e] = sum_h x[t, h] W_r[h, e]; x [T,H] and W_r [H,E] bf16; fp64 out. */
+EXPORT int oracle_router_forward(int64_t T, int32_t H, int32_t E, const uint16_t *x,
+                                 const uint16_t *Wr, double *logits) {
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < T; ++t) {
+    double *lt = logits + t * E;
+    for (int e = 0; e < E; ++e) lt[e] = 0.0;
+    for (int h = 0; h < H; ++h) {
+      const double xv = bf(x[t * H + h]);
+      const uint16_t *w = Wr + (int64_t)h * E;
+      for (int e = 0; e < E; ++e) lt[e] += xv * bf(w[e]);
+    }
+  }
+  return 0;
+}
+
+/* Backward of the router projection for an upstream gradient d_logits [T,E]:
+ *   dW_r[h, e] = sum_t x[t, h] d_logits[t, e]     (fp64, [H,E])
+ *   dx[t, h]   = sum_e d_logits[t, e] W_r[h, e]   (fp64, [T,H]; the router's
+ *                contribution to the layer input's gradient). */
+EXPORT int oracle_router_backward(int64_t T, int32_t H, int32_t E, const uint16_t *x,
+                                  const uint16_t *Wr, const double *d_logits, double *dWr,
+                                  double *dx) {
+#pragma omp parallel for schedule(static)
+  for (int h = 0; h < H; ++h) {
+    double *dw = dWr + (int64_t)h * E;
+    for (int e = 0; e < E; ++e) dw[e] = 0.0;
+    for (int64_t t = 0; t < T; ++t) {
+      const double xv = bf(x[t * H + h]);
+      const double *g = d_logits + t * E;
+      for (int e = 0; e < E; ++e) dw[e] += xv * g[e];
+    }
+  }
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < T; ++t) {
+    const double *g = d_logits + t * E;
+    for (int h = 0; h < H; ++h) {
+      const uint16_t *w = Wr + (int64_t)h * E;
+      double acc = 0.0;
+      for (int e = 0; e < E; ++e) acc += g[e] * bf(w[e]);
+      dx[t * H + h] = acc;
+    }
+  }
+  return 0;
+}

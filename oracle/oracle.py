@@ -59,6 +59,8 @@ def lib():
             L.oracle_e4m3_decode.restype = ctypes.c_double
             L.oracle_mx_scale_exp.argtypes = [ctypes.c_double]
             L.oracle_mx_scale_exp.restype = ctypes.c_int
+            L.oracle_router_forward.argtypes = [i64, i32, i32, P, P, P]
+            L.oracle_router_backward.argtypes = [i64, i32, i32, P, P, P, P, P]
             L.oracle_round_bf16.argtypes = [ctypes.c_double]
             L.oracle_round_bf16.restype = ctypes.c_double
             L.oracle_mx_quantize_rows_bf16.argtypes = [i64, i64, P, P, P, P]
@@ -66,7 +68,7 @@ def lib():
             for f in ("oracle_route", "oracle_dispatch", "oracle_forward", "oracle_backward_tokens",
                       "oracle_expert_rows",
                       "oracle_dw_full", "oracle_dw_elements", "oracle_mx_quantize_rows_bf16",
-                      "oracle_mx_quantize_cols_bf16"):
+                      "oracle_mx_quantize_cols_bf16", "oracle_router_forward", "oracle_router_backward"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -218,6 +220,30 @@ def e4m3_encode(v: float) -> int:
 
 def e4m3_decode(code: int) -> float:
     return float(lib().oracle_e4m3_decode(int(code)))
+
+
+def router_forward(x, W_r):
+    """logits [T,E] (fp64) = x [T,H] . W_r [H,E] (bf16 bit patterns)."""
+    x = _c(x, np.uint16)
+    W_r = _c(W_r, np.uint16)
+    T, H = x.shape
+    E = W_r.shape[1]
+    out = np.empty((T, E), np.float64)
+    _check(lib().oracle_router_forward(T, H, E, _p(x), _p(W_r), _p(out)), "router_forward")
+    return out
+
+
+def router_backward(x, W_r, d_logits):
+    """dW_r [H,E] and the router's dx [T,H] (fp64) for an upstream d_logits [T,E]."""
+    x = _c(x, np.uint16)
+    W_r = _c(W_r, np.uint16)
+    g = _c(d_logits, np.float64)
+    T, H = x.shape
+    E = W_r.shape[1]
+    dW = np.empty((H, E), np.float64)
+    dx = np.empty((T, H), np.float64)
+    _check(lib().oracle_router_backward(T, H, E, _p(x), _p(W_r), _p(g), _p(dW), _p(dx)), "router_backward")
+    return dW, dx
 
 
 def round_bf16(v: float) -> float:

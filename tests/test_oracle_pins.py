@@ -471,3 +471,52 @@ def test_fp8_bwd_composition():
     full = np.stack([dWg, dWu])
     exp = np.array([dWd[e, r, c] if wh == 2 else full[wh, e, r, c] for wh, e, r, c in zip(which, ee, rr, cc)])
     np.testing.assert_allclose(got, exp, rtol=1e-12, atol=1e-14)
+
+
+# ----------------------------------------------------------------------------- router projection
+
+def test_router_forward_exact_on_integers():
+    """Small-integer bf16 inputs: every product and partial sum is exact, so the
+    oracle's logits equal an integer matrix product exactly."""
+    rng = np.random.default_rng(12)
+    xi = rng.integers(-8, 9, (37, 96))
+    wi = rng.integers(-8, 9, (96, 24))
+    x = f32_to_bf16_bits(xi.astype(np.float32))
+    W = f32_to_bf16_bits(wi.astype(np.float32))
+    np.testing.assert_array_equal(O.router_forward(x, W), (xi @ wi).astype(np.float64))
+
+
+def test_router_backward_through_the_layer_matches_torch_autograd():
+    """The router projection in front of the layer: torch autograd through
+    logits = x . W_r and the whole MoE layer (fp64) gives d(W_r) and the total dx;
+    the oracle composes router_forward, backward_tokens and router_backward."""
+    shape = MoEShape(T=40, H=32, I=16, E=6, k=2)
+    inp = small_inputs(shape, c=13)
+    rng = np.random.default_rng(14)
+    # x on a 1/64 grid and W_r on a 1/256 grid: every logit is exact in fp32, so
+    # routing on fp32 logits and differentiating in fp64 see the same numbers
+    inp["x"] = f32_to_bf16_bits((rng.integers(-64, 65, (shape.T, shape.H)) / 64.0).astype(np.float32))
+    W_r = f32_to_bf16_bits((rng.integers(-128, 129, (shape.H, shape.E)) / 256.0).astype(np.float32))
+    logits64 = O.router_forward(inp["x"], W_r)
+    inp["logits"] = logits64.astype(np.float32)
+    assert np.array_equal(inp["logits"].astype(np.float64), logits64)
+    idx, w = O.route(inp["logits"], shape.k)
+    srt = np.sort(logits64, axis=1)[:, ::-1]
+    assert np.all(srt[:, shape.k - 1] - srt[:, shape.k] > 1e-4)  # no near tie at the cut
+    dx, dl, _ = O.backward_tokens(shape, inp["x"], inp["logits"], idx, w, inp["W_gate"], inp["W_up"],
+                                  inp["W_down"], inp["dy"])
+    dWr, dx_router = O.router_backward(inp["x"], W_r, dl)
+    # torch: the same layer with the logits computed from x and W_r inside the graph
+    f = lambda b: torch.from_numpy(bf16_bits_to_f32(b).astype(np.float64)).requires_grad_(True)
+    x, Wg, Wu, Wd, Wr = (f(a) for a in (inp["x"], inp["W_gate"], inp["W_up"], inp["W_down"], W_r))
+    dy = torch.from_numpy(bf16_bits_to_f32(inp["dy"]).astype(np.float64))
+    sel = torch.from_numpy(idx.astype(np.int64))
+    p = torch.softmax(x @ Wr, dim=1)
+    ps = torch.gather(p, 1, sel)
+    wt = ps / ps.sum(1, keepdim=True)
+    g = torch.einsum("th,tkhi->tki", x, Wg[sel])
+    u = torch.einsum("th,tkhi->tki", x, Wu[sel])
+    y = torch.einsum("tki,tkih->tkh", torch.nn.functional.silu(g) * u, Wd[sel])
+    ((wt.unsqueeze(-1) * y).sum(1) * dy).sum().backward()
+    np.testing.assert_allclose(dWr, Wr.grad.numpy(), rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(dx + dx_router, x.grad.numpy(), rtol=1e-10, atol=1e-13)
