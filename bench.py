@@ -402,6 +402,31 @@ def run_ours(args):
             c_ends[i].record(stream)
     torch.cuda.synchronize()
     ckpt_ms = statistics.mean(c_starts[i].elapsed_time(c_ends[i]) for i in range(K))
+    # the router projection in front of the layer (logits = x . W_r, and its backward)
+    router_ms = None
+    if shape.E % 8 == 0:
+        rgen = np.random.default_rng(3300)
+        W_r = torch.from_numpy((rgen.standard_normal((shape.H, shape.E), dtype=np.float32) * 0.02)
+                               .astype(np.float32)).to(dev).to(torch.bfloat16).view(torch.int16)
+        router = moe.Router(shape, device=dev)
+        logits_r = torch.empty((shape.T, shape.E), dtype=torch.float32, device=dev)
+        dW_r = torch.empty((shape.H, shape.E), dtype=torch.float32, device=dev)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3 * K)]
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                flush.zero_()
+                ev[3 * i].record(stream)
+                router.forward(d["x"], W_r, logits_r, stream=stream)
+                ev[3 * i + 1].record(stream)
+                router.backward(d["x"], W_r, grads["d_logits"], grads["dx"], dW_r, stream=stream)
+                ev[3 * i + 2].record(stream)
+        torch.cuda.synchronize()
+        if any(router.status(stream).values()):
+            raise RuntimeError(f"router status: {router.status(stream)}")
+        router_ms = {"fwd_ms": statistics.mean(ev[3 * i].elapsed_time(ev[3 * i + 1]) for i in range(K)),
+                     "bwd_ms": statistics.mean(ev[3 * i + 1].elapsed_time(ev[3 * i + 2]) for i in range(K)),
+                     "flop_per_step": 3 * 2.0 * shape.T * shape.H * shape.E}
     st = layer.status(stream)
     if any(st.values()):
         raise RuntimeError(f"device status after timed steps: {st}")
@@ -450,6 +475,7 @@ def run_ours(args):
         "e2e": {"value": world_tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": nk, "clocks": clk.summary(),
+        "router_projection": router_ms,
     }
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(w, inp)

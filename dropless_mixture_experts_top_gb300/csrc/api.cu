@@ -581,6 +581,100 @@ moe_status moe_backward(const moe_config *cfg, const void *dy, const void *x,
   return MOE_OK;
 }
 
+// ---- router projection (logits = x . W_r and its backward)
+
+namespace {
+bool router_shape_ok(const moe_config *c) {
+  if (!c) return false;
+  if (c->T < 0 || c->H < 64 || c->H % 64) return false;
+  if (c->E < 8 || c->E > kMaxExperts || c->E % 8) return false;  // 16-byte rows for the TMA
+  return true;
+}
+constexpr size_t kRouterOff = kHeader;            // int32 {0, T}: the single segment
+constexpr size_t kRouterMaps = kHeader + 256;     // 3 tensor maps for the weight gradient
+constexpr size_t kRouterDlog = kRouterMaps + 512; // bf16 d_logits [T,E]
+}  // namespace
+
+moe_status moe_router_workspace(const moe_config *cfg, size_t *fwd_scratch, size_t *bwd_scratch) {
+  if (!router_shape_ok(cfg)) return MOE_ERR_INVALID_ARG;
+  if (fwd_scratch) *fwd_scratch = kRouterMaps;
+  if (bwd_scratch) *bwd_scratch = kRouterDlog + align256(static_cast<size_t>(cfg->T) * cfg->E * 2);
+  return MOE_OK;
+}
+
+moe_status moe_router_forward(const moe_config *cfg, const void *x, const void *W_r, float *logits,
+                              void *scratch, size_t scratch_bytes, void *stream) {
+  if (!router_shape_ok(cfg)) return MOE_ERR_INVALID_ARG;
+  if (!W_r || !scratch || (cfg->T > 0 && (!x || !logits))) return MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(W_r) || !al16(logits) || !al16(scratch)) return MOE_ERR_ALIGNMENT;
+  if (scratch_bytes < kRouterMaps) return MOE_ERR_WORKSPACE;
+  DevInfo di;
+  MOE_TRY(device_info(&di));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t *sc = static_cast<uint8_t *>(scratch);
+  if (cudaMemsetAsync(sc, 0, kHeader, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cfg->T == 0) return MOE_OK;
+  int32_t *seg = reinterpret_cast<int32_t *>(sc + kRouterOff);
+  MOE_TRY(timed("router_segment", s, [&] { return launch_one_segment(seg, cfg->T, s); }));
+  GemmArgs g{};
+  g.M_rows = cfg->T;
+  g.H = cfg->H;
+  g.E = cfg->E;
+  g.offsets = seg;
+  g.r_x = static_cast<const uint16_t *>(x);
+  g.r_w = static_cast<const uint16_t *>(W_r);
+  g.r_out = logits;
+  g.status = reinterpret_cast<int32_t *>(sc);
+  g.num_sms = di.sms;
+  MOE_TRY(timed(gemm_mode_name(kRouterFwd), s, [&] { return launch_grouped_gemm(kRouterFwd, g, s); }));
+  return MOE_OK;
+}
+
+moe_status moe_router_backward(const moe_config *cfg, const void *x, const void *W_r,
+                               const float *d_logits, void *dx, float *dW_r, void *scratch,
+                               size_t scratch_bytes, void *stream) {
+  if (!router_shape_ok(cfg)) return MOE_ERR_INVALID_ARG;
+  if (!W_r || !dW_r || !scratch || (cfg->T > 0 && (!x || !d_logits || !dx)))
+    return MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(W_r) || !al16(d_logits) || !al16(dx) || !al16(dW_r) || !al16(scratch))
+    return MOE_ERR_ALIGNMENT;
+  size_t need = 0;
+  moe_router_workspace(cfg, nullptr, &need);
+  if (scratch_bytes < need) return MOE_ERR_WORKSPACE;
+  DevInfo di;
+  MOE_TRY(device_info(&di));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t *sc = static_cast<uint8_t *>(scratch);
+  if (cudaMemsetAsync(sc, 0, kHeader, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cfg->T == 0) {  // no tokens: dW_r = 0, dx untouched
+    if (cudaMemsetAsync(dW_r, 0, sizeof(float) * cfg->H * cfg->E, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  int32_t *seg = reinterpret_cast<int32_t *>(sc + kRouterOff);
+  uint16_t *dlog = reinterpret_cast<uint16_t *>(sc + kRouterDlog);
+  MOE_TRY(timed("router_segment", s, [&] { return launch_one_segment(seg, cfg->T, s); }));
+  MOE_TRY(timed("router_dlogits_bf16", s, [&] {
+    return launch_to_bf16(d_logits, dlog, static_cast<int64_t>(cfg->T) * cfg->E, s);
+  }));
+  GemmArgs g{};
+  g.M_rows = cfg->T;
+  g.H = cfg->H;
+  g.E = cfg->E;
+  g.offsets = seg;
+  g.r_x = static_cast<const uint16_t *>(x);
+  g.r_w = static_cast<const uint16_t *>(W_r);
+  g.r_dlog = dlog;
+  g.o0 = static_cast<uint16_t *>(dx);
+  g.r_out = dW_r;
+  g.map_scratch = sc + kRouterMaps;
+  g.status = reinterpret_cast<int32_t *>(sc);
+  g.num_sms = di.sms;
+  MOE_TRY(timed(gemm_mode_name(kRouterDX), s, [&] { return launch_grouped_gemm(kRouterDX, g, s); }));
+  MOE_TRY(timed(gemm_mode_name(kRouterDW), s, [&] { return launch_grouped_gemm(kRouterDW, g, s); }));
+  return MOE_OK;
+}
+
 moe_status moe_get_device_status(const void *scratch, void *stream, int32_t *host_code) {
   if (!scratch || !host_code) return MOE_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;

@@ -195,6 +195,48 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, uint32_t tb, int ri
       store_rows32(tile, p.o0 + (static_cast<size_t>(t.e) * p.I + i_row0) * p.H + col, p.H, nvalid,
                    v0);
     }
+  } else if constexpr (MODE == kRouterFwd || MODE == kRouterDW) {
+    // fp32 output [rows, n_out]: logits (rows = tokens, bounded by the segment's
+    // end) or dW_r (rows = H, no token ends them; an empty reduction writes 0)
+    const int row = t.m0 + rit;
+    const bool rv = MODE == kRouterFwd ? row < t.row_end : row < p.H;
+    for (int c = cb; c < ce; ++c) {
+      const int col = t.n0 + 32 * c;
+      if (col >= p.n_out) break;
+      if (MODE == kRouterFwd || t.nkb > 0) {
+        tmem_ld32(tb + 32 * c, r0);
+        tmem_ld_wait();
+      }
+      if (rv) {
+        float *dst = p.of + static_cast<size_t>(row) * p.n_out + col;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (col + 4 * q < p.n_out) {  // n_out is a multiple of 8
+            const bool z = MODE == kRouterDW && t.nkb == 0;
+            *reinterpret_cast<float4 *>(dst + 4 * q) =
+                z ? make_float4(0.f, 0.f, 0.f, 0.f)
+                  : make_float4(__uint_as_float(r0[4 * q]), __uint_as_float(r0[4 * q + 1]),
+                                __uint_as_float(r0[4 * q + 2]), __uint_as_float(r0[4 * q + 3]));
+          }
+        }
+      }
+    }
+  } else if constexpr (MODE == kRouterDX) {  // dx [rows, H] bf16 += accumulator
+    const int row0 = t.m0 + rit - lane;
+    const int nvalid = clamp_rows(t.row_end - row0);
+    for (int c = cb; c < ce; ++c) {
+      const int col = t.n0 + 32 * c;
+      if (col >= p.H) break;
+      uint4 w[4];
+      uint16_t *g0 = p.o0 + static_cast<size_t>(row0) * p.H + col;
+      load_rows32(g0, p.H, nvalid, w);
+      rows32_to_lanes(tile, w, v1);
+      tmem_ld32(tb + 32 * c, r0);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v0[i] = v1[i] + __uint_as_float(r0[i]);
+      store_rows32(tile, g0, p.H, nvalid, v0);
+    }
   } else {  // kBwdDWGateUp
     const int h_row0 = t.m0 + rit - lane;
     const int nvalid = clamp_rows(p.H - h_row0);

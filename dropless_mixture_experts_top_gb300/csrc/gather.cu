@@ -217,6 +217,41 @@ cudaError_t launch_gather_sum(const uint16_t *rows, const int32_t *row_of_slot, 
   return cudaGetLastError();
 }
 
+namespace {
+
+// Router projection backward: d_logits rounded to bf16 (nearest even) for the
+// two bf16 tensor-core products; four floats per thread.
+__global__ void __launch_bounds__(256) to_bf16_kernel(const float4 *__restrict__ in, uint2 *__restrict__ out,
+                                                      int64_t n4) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n4) return;
+  const float4 v = __ldg(in + i);
+  out[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+}
+
+// The router projection's single "expert": offsets {0, T}.
+__global__ void one_segment_kernel(int32_t *offsets, int T) {
+  if (threadIdx.x == 0) {
+    offsets[0] = 0;
+    offsets[1] = T;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_to_bf16(const float *in, uint16_t *out, int64_t n, cudaStream_t s) {
+  const int64_t n4 = n / 4;  // n is a multiple of 8 (E % 8 == 0)
+  if (n4 == 0) return cudaSuccess;
+  to_bf16_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, s>>>(
+      reinterpret_cast<const float4 *>(in), reinterpret_cast<uint2 *>(out), n4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_one_segment(int32_t *offsets, int T, cudaStream_t s) {
+  one_segment_kernel<<<1, 32, 0, s>>>(offsets, T);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_router_bwd(const uint16_t *dy, const uint16_t *Y, const int32_t *row_of_slot,
                               const int32_t *topk_idx, const float *topk_w, uint16_t *dy_perm,
                               float *d_logits, float *d_topk_w, int T, int H, int E, int k,

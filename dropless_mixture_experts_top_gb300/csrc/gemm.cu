@@ -85,6 +85,8 @@ struct Params {
   const uint16_t *G, *U;  // dSwiGLU epilogue inputs
   const float *w_row;     // router weight of each permuted row
   uint16_t *o0, *o1, *o2, *o3;
+  float *of;   // router projection: fp32 output
+  int n_out;   // router projection: output columns (E)
   int32_t *status;
   const CUtensorMap *expert_maps;  // ragged K: [E][kMapsPerExpert] maps ending at each expert's end
   int kdim;     // ragged M: the fixed reduction length
@@ -94,9 +96,10 @@ struct Params {
 
 template <int MODE>
 struct Traits {
-  static constexpr bool kRaggedK = (MODE == kBwdDWDown || MODE == kBwdDWGateUp);
+  static constexpr bool kRaggedK = (MODE == kBwdDWDown || MODE == kBwdDWGateUp || MODE == kRouterDW);
   static constexpr int kAMN = kRaggedK ? 1 : 0;  // A operand MN-major in smem
-  static constexpr int kBMN = (MODE == kFwdGateUp || MODE == kFwdDown || kRaggedK) ? 1 : 0;
+  static constexpr int kBMN =
+      (MODE == kFwdGateUp || MODE == kFwdDown || MODE == kRouterFwd || kRaggedK) ? 1 : 0;
   // column tile = [first source | second source], 128 columns each (gate | up):
   // CTA 0 holds the first source's columns, CTA 1 the second's
   static constexpr bool kPair = (MODE == kFwdGateUp || MODE == kBwdDWGateUp);
@@ -162,12 +165,12 @@ __device__ __forceinline__ void produce_stage(const Tile &t, int kb, int rank, u
     const int wrow = t.e * p.H + kb * BK;
     ld(sb, w, t.n0, wrow);
     ld(sb + kBox, w, t.n0 + 64, wrow);
-  } else if constexpr (MODE == kFwdDown) {
+  } else if constexpr (MODE == kFwdDown || MODE == kRouterFwd) {
     ld(sa, a0, kb * BK, arow);
     const int wrow = t.e * p.I + kb * BK;
     ld(sb, b0, bcol, wrow);
     ld(sb + kBox, b0, bcol + 64, wrow);
-  } else if constexpr (MODE == kBwdDA) {
+  } else if constexpr (MODE == kBwdDA || MODE == kRouterDX) {
     ld(sa, a0, kb * BK, arow);
     ld(sb, b0, kb * BK, t.e * p.I + bcol);
   } else if constexpr (MODE == kBwdDX) {
@@ -179,7 +182,7 @@ __device__ __forceinline__ void produce_stage(const Tile &t, int kb, int rank, u
       ld(sa, a1, (kb - kbi) * BK, arow);
       ld(sb, b1, (kb - kbi) * BK, t.e * p.H + bcol);
     }
-  } else if constexpr (MODE == kBwdDWDown) {
+  } else if constexpr (MODE == kBwdDWDown || MODE == kRouterDW) {
     const CUtensorMap *em = p.expert_maps + t.e * kMapsPerExpert;  // rows end at the expert's end
     const int r = t.krow0 + kb * BK;
     ld(sa, em + 0, t.m0 + BM * rank, r);
@@ -556,6 +559,12 @@ cudaError_t launch_mode(const GemmArgs &a, cudaStream_t s) {
   p.w_row = a.w_row;
   p.status = a.status;
   const uint64_t M = static_cast<uint64_t>(a.M_rows), H = a.H, I = a.I, E = a.E;
+  // router modes: a.E is the router's output width, the GEMM sees one expert
+  const uint64_t E_out = a.E;
+  const bool router = MODE == kRouterFwd || MODE == kRouterDX || MODE == kRouterDW;
+  p.E = router ? 1 : a.E;
+  p.of = a.r_out;
+  p.n_out = a.E;
   bool ok = true;
   switch (MODE) {
     case kFwdGateUp:
@@ -593,6 +602,27 @@ cudaError_t launch_mode(const GemmArgs &a, cudaStream_t s) {
       p.m_tiles = (a.I + 2 * BM - 1) / (2 * BM);
       p.n_tiles = (a.H + 255) / 256;
       break;
+    case kRouterFwd:  // x [T,H] . W_r [H,E]: one expert, K = H, N = E
+      ok = make_map(&mA0, a.r_x, H, M, 128) && make_map(&mB0, a.r_w, E_out, H, 64);
+      mA1 = mA0;
+      mB1 = mB0;
+      p.kdim = a.H;
+      p.n_tiles = (a.E + 255) / 256;
+      break;
+    case kRouterDX:  // bf16(d_logits) [T,E] . W_r^T: K = E (zero-filled to 64s), N = H
+      ok = make_map(&mA0, a.r_dlog, E_out, M, 128) && make_map(&mB0, a.r_w, E_out, H, 128);
+      mA1 = mA0;
+      mB1 = mB0;
+      p.kdim = (a.E + BK - 1) / BK * BK;
+      p.n_tiles = (a.H + 255) / 256;
+      break;
+    case kRouterDW:  // x^T [H,T] . bf16(d_logits) [T,E]: K = T, M = H, N = E
+      ok = make_map(&mA0, a.r_x, H, M, 64) && make_map(&mB0, a.r_dlog, E_out, M, 64);
+      mA1 = mA0;
+      mB1 = mB0;
+      p.m_tiles = (a.H + 2 * BM - 1) / (2 * BM);
+      p.n_tiles = (a.E + 255) / 256;
+      break;
     default:  // kBwdDWGateUp
       ok = make_map(&mA0, a.x_perm, H, M, 64) && make_map(&mB0, a.dG, I, M, 64) &&
            make_map(&mB1, a.dU, I, M, 64);
@@ -609,7 +639,7 @@ cudaError_t launch_mode(const GemmArgs &a, cudaStream_t s) {
     tm.m[1] = mB0;
     tm.m[2] = mB1;
     CUtensorMap *maps = static_cast<CUtensorMap *>(a.map_scratch);
-    expert_maps_kernel<<<(a.E + 255) / 256, 256, 0, s>>>(tm, a.offsets, a.E, maps);
+    expert_maps_kernel<<<(p.E + 255) / 256, 256, 0, s>>>(tm, a.offsets, p.E, maps);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     p.expert_maps = maps;
@@ -658,6 +688,9 @@ cudaError_t launch_grouped_gemm(GemmMode mode, const GemmArgs &a, cudaStream_t s
     case kBwdDX: return launch_mode<kBwdDX>(a, s);
     case kBwdDWDown: return launch_mode<kBwdDWDown>(a, s);
     case kBwdDWGateUp: return launch_mode<kBwdDWGateUp>(a, s);
+    case kRouterFwd: return launch_mode<kRouterFwd>(a, s);
+    case kRouterDX: return launch_mode<kRouterDX>(a, s);
+    case kRouterDW: return launch_mode<kRouterDW>(a, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -670,6 +703,9 @@ const char *gemm_mode_name(GemmMode mode) {
     case kBwdDX: return "gemm_dX";
     case kBwdDWDown: return "gemm_dW_down";
     case kBwdDWGateUp: return "gemm_dW_gateup";
+    case kRouterFwd: return "router_gemm_logits";
+    case kRouterDX: return "router_gemm_dx";
+    case kRouterDW: return "router_gemm_dW";
   }
   return "?";
 }

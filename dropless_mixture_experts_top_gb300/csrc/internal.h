@@ -47,6 +47,8 @@ cudaError_t launch_permute_rows(const uint16_t *x, const int32_t *row_of_slot, u
 cudaError_t launch_gather_sum(const uint16_t *rows, const int32_t *row_of_slot, const float *w,
                               uint16_t *out, int T, int H, int k, cudaStream_t s);
 // dy_perm[row(t,j)] = dy[t]; g[t,j] = <dy[t], Y[row]>; d_logits; d_topk_w (nullable)
+cudaError_t launch_to_bf16(const float *in, uint16_t *out, int64_t n, cudaStream_t s);
+cudaError_t launch_one_segment(int32_t *offsets, int T, cudaStream_t s);
 cudaError_t launch_router_bwd(const uint16_t *dy, const uint16_t *Y, const int32_t *row_of_slot,
                               const int32_t *topk_idx, const float *topk_w, uint16_t *dy_perm,
                               float *d_logits, float *d_topk_w, int T, int H, int E, int k,
@@ -59,7 +61,11 @@ enum GemmMode : int {
   kBwdDA = 2,       // dy_perm . W_down^T, times w -> dSwiGLU epilogue: dG, dU      (ragged M)
   kBwdDX = 3,       // [dG | dU] . [W_gate | W_up]^T -> dX_perm                     (ragged M)
   kBwdDWDown = 4,   // A_w^T . dy_perm            -> dW_down                        (ragged K)
-  kBwdDWGateUp = 5  // x_perm^T . [dG | dU]       -> dW_gate, dW_up                 (ragged K)
+  kBwdDWGateUp = 5, // x_perm^T . [dG | dU]       -> dW_gate, dW_up                 (ragged K)
+  // router projection: one "expert" spanning all T tokens
+  kRouterFwd = 6,   // x . W_r                    -> logits fp32                    (ragged M)
+  kRouterDX = 7,    // bf16(d_logits) . W_r^T     -> dx += (bf16, in place)         (ragged M)
+  kRouterDW = 8     // x^T . bf16(d_logits)       -> dW_r fp32                      (ragged K)
 };
 
 struct GemmArgs {
@@ -76,6 +82,9 @@ struct GemmArgs {
   const float *w_row;       // [M] router weight per permuted row
   // outputs (device, bf16)
   uint16_t *o0, *o1, *o2, *o3;
+  // router projection: x [T,H], W_r [H,E], d_logits as bf16 [T,E]; fp32 output, its columns
+  const uint16_t *r_x, *r_w, *r_dlog;
+  float *r_out;
   int32_t *status;
   void *map_scratch;  // ragged K: device scratch for E * 3 tensor maps (128 B each, 128-B aligned)
   int num_sms;

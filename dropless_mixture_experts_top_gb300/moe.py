@@ -28,7 +28,7 @@ EXPORTED = [
     "moe_query_workspace", "moe_saved_offsets", "moe_fp8_scratch_offsets", "moe_route",
     "moe_route_static_scratch", "moe_forward", "moe_backward", "moe_get_device_status",
     "moe_status_string", "moe_timing_attach", "moe_timing_count", "moe_timing_label",
-    "moe_selftest_wait_timeout",
+    "moe_selftest_wait_timeout", "moe_router_workspace", "moe_router_forward", "moe_router_backward",
 ]
 
 
@@ -81,6 +81,11 @@ def lib():
         L.moe_get_device_status.argtypes = [P, P, P]
         L.moe_selftest_wait_timeout.argtypes = [P, P]
         L.moe_selftest_wait_timeout.restype = ctypes.c_int
+        L.moe_router_workspace.argtypes = [P, P, P]
+        L.moe_router_forward.argtypes = [P, P, P, P, P, sz, P]
+        L.moe_router_backward.argtypes = [P, P, P, P, P, P, P, sz, P]
+        for f in ("moe_router_workspace", "moe_router_forward", "moe_router_backward"):
+            getattr(L, f).restype = ctypes.c_int
         L.moe_status_string.argtypes = [ctypes.c_int]
         L.moe_status_string.restype = ctypes.c_char_p
         L.moe_timing_attach.argtypes = [P, ctypes.c_int32]
@@ -194,6 +199,47 @@ def get_device_status(scratch, stream=None) -> int:
     if rc not in (MOE_OK, -6):
         _check(rc, "moe_get_device_status")
     return int(code.value)
+
+
+def router_workspace(cfg: Config):
+    f, b = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().moe_router_workspace(ctypes.byref(cfg), ctypes.byref(f), ctypes.byref(b)),
+           "moe_router_workspace")
+    return int(f.value), int(b.value)
+
+
+class Router:
+    """The router projection logits = x . W_r (bf16 in, fp32 logits) and its
+    backward, over scratch buffers sized for one configuration."""
+
+    def __init__(self, shape, device="cuda"):
+        self.shape = shape
+        self.cfg = make_config(shape)
+        fs, bs = router_workspace(self.cfg)
+        self.fwd_scratch = torch.empty(fs, dtype=torch.uint8, device=device)
+        self.bwd_scratch = torch.empty(bs, dtype=torch.uint8, device=device)
+        self.device = device
+
+    def forward(self, x, W_r, logits=None, stream=None):
+        if logits is None:
+            logits = torch.empty((self.shape.T, self.shape.E), dtype=torch.float32, device=self.device)
+        _check(lib().moe_router_forward(ctypes.byref(self.cfg), _ptr(x), _ptr(W_r), _ptr(logits),
+                                        _ptr(self.fwd_scratch), self.fwd_scratch.numel(), _stream(stream)),
+               "moe_router_forward")
+        return logits
+
+    def backward(self, x, W_r, d_logits, dx, dW_r=None, stream=None):
+        """dx (bf16 [T,H]) is updated in place; returns dW_r (fp32 [H,E])."""
+        if dW_r is None:
+            dW_r = torch.empty((self.shape.H, self.shape.E), dtype=torch.float32, device=self.device)
+        _check(lib().moe_router_backward(ctypes.byref(self.cfg), _ptr(x), _ptr(W_r), _ptr(d_logits), _ptr(dx),
+                                         _ptr(dW_r), _ptr(self.bwd_scratch), self.bwd_scratch.numel(),
+                                         _stream(stream)), "moe_router_backward")
+        return dW_r
+
+    def status(self, stream=None) -> dict:
+        return {n: get_device_status(b, stream) for n, b in (("forward", self.fwd_scratch),
+                                                             ("backward", self.bwd_scratch))}
 
 
 def selftest_wait_timeout(status, stream=None):

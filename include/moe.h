@@ -168,6 +168,23 @@ moe_status moe_backward(const moe_config *cfg, const void *dy, const void *x,
                         void *dW_gate, void *dW_up, void *dW_down, float *d_logits,
                         float *d_topk_w, void *scratch, size_t scratch_bytes, void *stream);
 
+/* Router projection: the learned router's linear layer in front of moe_route,
+ *   logits [T,E] fp32 = x [T,H] bf16 . W_r [H,E] bf16   (fp32 accumulation),
+ * and its backward for the d_logits moe_backward returns,
+ *   dW_r [H,E] fp32 = x^T . d_logits,   dx [T,H] bf16 += d_logits . W_r^T
+ * (dx is updated in place: pass the dx moe_backward wrote to get the layer
+ * input's full gradient).  d_logits enters both products rounded to bf16 (the
+ * tensor cores' operand type); accumulation is fp32.  cfg->k and cfg->I are not
+ * used; requires E % 8 == 0 (8 <= E <= 256) and H % 64 == 0.  Scratch sizes from
+ * moe_router_workspace; a status header at the start of the scratch as for the
+ * other calls.  With T == 0, logits is untouched and dW_r is zeroed. */
+moe_status moe_router_workspace(const moe_config *cfg, size_t *fwd_scratch, size_t *bwd_scratch);
+moe_status moe_router_forward(const moe_config *cfg, const void *x, const void *W_r, float *logits,
+                              void *scratch, size_t scratch_bytes, void *stream);
+moe_status moe_router_backward(const moe_config *cfg, const void *x, const void *W_r,
+                               const float *d_logits, void *dx, float *dW_r, void *scratch,
+                               size_t scratch_bytes, void *stream);
+
 /* Routing without a caller-provided scratch buffer.  The paper has no
  * counterpart: it exists for callers that cannot allocate device memory --
  * code running while a CUDA graph is captured (cudaMalloc is not allowed

@@ -143,3 +143,11 @@ def test_fp8_shapes_and_layout(L):
     _, _, _, bs = moe.query_workspace(c)
     _, _, _, bs16 = moe.query_workspace(cfg(T=300, H=256, I=128, E=8, k=2, prec=0))
     assert spans[0][0] >= bs16 - 256 and spans[-1][1] <= bs
+
+
+def test_router_workspace_and_shapes(L):
+    f, b = moe.router_workspace(moe.Config(300, 256, 64, 16, 2, 0))
+    assert f >= 512 and b >= f + 300 * 16 * 2
+    for bad in (dict(E=12), dict(E=4), dict(H=96)):  # E % 8, E >= 8, H % 64
+        c = moe.Config(300, bad.get("H", 256), 64, bad.get("E", 16), 2, 0)
+        assert L.moe_router_workspace(ctypes.byref(c), None, None) == -1
