@@ -97,10 +97,12 @@ Layout layout_of(const moe_config *c) {
   o = kHeader;
   L.b_dyp = o;
   o += align256(M * H * 2);
-  L.b_dG = o;
-  o += align256(M * I * 2);
-  L.b_dU = o;
-  o += align256(M * I * 2);
+  if (c->precision == MOE_PREC_BF16) {  // fp8_bwd: dG and dU exist only quantised
+    L.b_dG = o;
+    o += align256(M * I * 2);
+    L.b_dU = o;
+    o += align256(M * I * 2);
+  }
   L.b_dX = o;
   o += align256(M * H * 2);
   L.b_maps = o;
@@ -239,7 +241,7 @@ struct Fp8Bwd {
   int sms;
   int32_t *status;
   const uint16_t *W_gate, *W_up, *W_down, *x_perm, *G, *U, *A_w;
-  uint16_t *dy_perm, *dG, *dU, *dX, *dx, *dW_gate, *dW_up, *dW_down;
+  uint16_t *dy_perm, *dX, *dx, *dW_gate, *dW_up, *dW_down;
 };
 
 moe_status backward_fp8(const Fp8Bwd &f, cudaStream_t s) {
@@ -263,7 +265,7 @@ moe_status backward_fp8(const Fp8Bwd &f, cudaStream_t s) {
   m.w_row = f.r->w_row;
   m.status = f.status;
   m.num_sms = f.sms;
-  // dA = w (Q(dy) . Q(W_down)^T), K = H; dSwiGLU epilogue -> dG, dU
+  // dA = w (Q(dy) . Q(W_down)^T), K = H; dSwiGLU epilogue -> Q(dG), Q(dU) on both axes
   MOE_TRY(timed("mx_quant_dy", s, [&] {
     return launch_quant_rows(f.dy_perm, Mp, H, off, pad_off, E, sc + q.dy_q, sc + q.dy_sf, sf_a(Mp), s);
   }));
@@ -275,16 +277,19 @@ moe_status backward_fp8(const Fp8Bwd &f, cudaStream_t s) {
   m.sfa0 = sc + q.dy_sf;
   m.b0 = sc + q.wd_q;
   m.sfb0 = sc + q.wd_sf;
-  m.o0 = f.dG;
-  m.o1 = f.dU;
+  // dA's epilogue writes dG and dU quantised along I (for dX) and along tokens
+  // (for dW_gate/up); they are never stored in bf16
+  m.o0 = m.o1 = nullptr;
+  m.dg_q = sc + q.dg_q;
+  m.dg_sf = sc + q.dg_sf;
+  m.du_q = sc + q.du_q;
+  m.du_sf = sc + q.du_sf;
+  m.dg_t = sc + q.dg_t;
+  m.dg_t_sf = sc + q.dg_t_sf;
+  m.du_t = sc + q.du_t;
+  m.du_t_sf = sc + q.du_t_sf;
   MOE_TRY(timed("mx_gemm_dA_dswiglu", s, [&] { return launch_mx_gemm(kMxGemmDA, m, s); }));
   // dX = Q(dG) . Q(W_gate)^T + Q(dU) . Q(W_up)^T, K = I
-  MOE_TRY(timed("mx_quant_dG", s, [&] {
-    return launch_quant_rows(f.dG, Mp, I, off, pad_off, E, sc + q.dg_q, sc + q.dg_sf, sf_a(Mp), s);
-  }));
-  MOE_TRY(timed("mx_quant_dU", s, [&] {
-    return launch_quant_rows(f.dU, Mp, I, off, pad_off, E, sc + q.du_q, sc + q.du_sf, sf_a(Mp), s);
-  }));
   MOE_TRY(timed("mx_quant_W_gate", s, [&] {
     return launch_quant_rows(f.W_gate, E * H, I, nullptr, nullptr, E, sc + q.wg_q, sc + q.wg_sf,
                              sf_b(H), s);
@@ -325,12 +330,6 @@ moe_status backward_fp8(const Fp8Bwd &f, cudaStream_t s) {
   // dW_gate = Q(x)^T . Q(dG), dW_up = Q(x)^T . Q(dU), K = the expert's tokens
   MOE_TRY(timed("mx_quantT_x", s, [&] {
     return launch_quant_cols(f.x_perm, H, Mp, off, pad_off, E, sc + q.x_t, sc + q.x_t_sf, sf_a(H), s);
-  }));
-  MOE_TRY(timed("mx_quantT_dG", s, [&] {
-    return launch_quant_cols(f.dG, I, Mp, off, pad_off, E, sc + q.dg_t, sc + q.dg_t_sf, sf_b(I), s);
-  }));
-  MOE_TRY(timed("mx_quantT_dU", s, [&] {
-    return launch_quant_cols(f.dU, I, Mp, off, pad_off, E, sc + q.du_t, sc + q.du_t_sf, sf_b(I), s);
   }));
   m.a0 = sc + q.x_t;
   m.sfa0 = sc + q.x_t_sf;
@@ -539,8 +538,6 @@ moe_status moe_backward(const moe_config *cfg, const void *dy, const void *x,
     f.U = U;
     f.A_w = A_w;
     f.dy_perm = dy_perm;
-    f.dG = dG;
-    f.dU = dU;
     f.dX = dX;
     f.dx = static_cast<uint16_t *>(dx);
     f.dW_gate = static_cast<uint16_t *>(dW_gate);

@@ -6,8 +6,13 @@
 // by the quantisers in mxfp8.cu: K-major E4M3 codes, scale factors in 512-byte
 // atoms, ragged operands in a per-expert row space padded to 128 rows (so tiles
 // and 32-element blocks along tokens never straddle two experts, and the padded
-// rows are zeros).  Outputs are bf16 and go through the same epilogues as the
-// bf16 engine (dSwiGLU for dA).
+// rows are zeros).  dX and the weight gradients write bf16 through the same
+// epilogues as the bf16 engine.  dA's epilogue computes dSwiGLU and quantises
+// its dG and dU itself, in the form the two GEMMs that read them load: along
+// I (a lane's 32 consecutive columns are one block of its row) and along
+// tokens (a warp's 32 rows are one 32-token block of the padded row space,
+// transposed through the warp's staging tile), from the bf16-rounded values a
+// bf16 tensor would hold; dG and dU never exist in bf16.
 //
 // One CTA per SM, persistent, static round-robin over 128 x 192 tiles:
 //   warp 0      producer: TMA boxes of codes (128-byte swizzle) and bulk copies
@@ -27,14 +32,18 @@
 
 #include "common.cuh"
 #include "epilogue.cuh"
+#include "mxfp8.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int BM = 128, BN = kMxBN;  // 128 x 192 tiles
 constexpr int BKB = 128;             // K per stage in elements (= bytes): one 128-byte swizzle row
-// 5-stage ring; 4 for dA, whose 8 epilogue warps need 8 staging tiles
-__host__ __device__ constexpr int stages_of(int mode) { return mode == 0 ? 4 : 5; }
+// 5-stage ring; 3 for dA, whose shared memory also holds 8 staging tiles and a
+// 4-slot G/U ring (two slots per column half, so a half's next chunk lands
+// while it works on the current one)
+__host__ __device__ constexpr int stages_of(int mode) { return mode == 0 ? 3 : 5; }
+constexpr int kMxGuSlots = 4;
 constexpr int kABytes = BM * BKB;    // 16 KB
 constexpr int kBBytes = BN * BKB;    // 24 KB
 constexpr int kSfBytes = 512 * 3;    // A atom + two B atoms
@@ -59,7 +68,7 @@ __host__ __device__ constexpr int gu_off(int mode) {
   return (epi_off(mode) + epi_warps(mode) * kEpiTileBytes + 1023) / 1024 * 1024;
 }
 __host__ __device__ constexpr int smem_bytes(int mode) {
-  return gu_off(mode) + gu_warps(mode) * kGuSlots * kGuChunkBytes + 1024;
+  return gu_off(mode) + gu_warps(mode) * kMxGuSlots * kGuChunkBytes + 1024;
 }
 static_assert(smem_bytes(0) <= 227 * 1024 && smem_bytes(1) <= 227 * 1024, "shared memory budget");
 static_assert(kSfCol + 5 * kSfSlotCols <= kTmemCols, "TMEM budget");
@@ -76,6 +85,7 @@ struct MxParams {
   const uint16_t *G, *U;
   const float *w_row;
   uint16_t *o0, *o1;
+  uint8_t *dg_q, *du_q, *dg_sf, *du_sf, *dg_t, *du_t, *dg_t_sf, *du_t_sf;  // dA's quantised outputs
   int32_t *status;
   int n_tiles, m_tiles;
   int b_gps;  // B scales: 192-row groups per segment
@@ -94,7 +104,8 @@ template <int MODE>
 struct MxTraits {
   static constexpr bool kRaggedK = (MODE == kMxDWDown || MODE == kMxDWGateUp);
   // dW_gate and dW_up tiles use the dW_down epilogue on a transposed view
-  static constexpr int kEpi = MODE == kMxDA ? kBwdDA : MODE == kMxDX ? kBwdDX : kBwdDWDown;
+  // (dA has its own epilogue, epilogue_da_mx)
+  static constexpr int kEpi = MODE == kMxDX ? kBwdDX : kBwdDWDown;
 };
 
 // Block-scaled instruction descriptor: E4M3 x E4M3, fp32 D, UE8M0 scales,
@@ -195,6 +206,121 @@ __device__ __forceinline__ MxTile decode_mx(int tile, const MxParams &p, const i
   return x;
 }
 
+// sigmoid with the approximate (branch-free) reciprocal: within a few fp32
+// ulp of 1 / (1 + e^-z), far below the bf16 rounding that follows.
+__device__ __forceinline__ float sigmoid_approx(float z) { return __fdividef(1.f, 1.f + __expf(-z)); }
+
+// The value a bf16 tensor would hold (nearest even), as fp32.
+__device__ __forceinline__ float round_bf16(float v) {
+  return __uint_as_float(static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v))) << 16);
+}
+
+// A warp's 32 x 32 values (lane = row, bf16-exact) quantised down the rows:
+// written to the staging tile as bf16, then lane j takes column j's 32 values
+// (one 32-token block) and writes its 32 codes at codes + (col0 + j) * ld +
+// tok0 and their scale code at sf_byte (its own column's byte).
+__device__ __forceinline__ void quant_down_rows32(uint8_t *tile, const float (&v)[32], uint8_t *codes,
+                                                  size_t ld, int col0, int tok0, uint8_t *sf_byte) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 w;
+    w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+    w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+    w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+    w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+    *reinterpret_cast<uint4 *>(tile + epi_swz(lane, q)) = w;
+  }
+  __syncwarp();
+  float c[32];
+  const int qc = lane >> 3, within = (lane & 7) * 2;
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    c[i] = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(
+                               tile + epi_swz(i, qc) + within))
+                           << 16);
+  __syncwarp();  // the tile is rewritten by the next call
+  *sf_byte = quant32(c, reinterpret_cast<uint4 *>(codes + static_cast<size_t>(col0 + lane) * ld + tok0));
+}
+
+// dA's epilogue in the fp8_bwd backward: ring, dSwiGLU and the weighting as
+// in the bf16 engine's dA, then dG and dU rounded to bf16 (zero in the padded
+// rows past the expert's count) and quantised along I and along tokens.
+template <int NCH>
+__device__ __forceinline__ bool epilogue_da_mx(const MxTile &x, uint32_t tb, int rit, const MxParams &p,
+                                               int part, uint8_t *tile, const uint8_t *ring,
+                                               uint64_t *gu_full, uint64_t *gu_empty, int &gbase,
+                                               volatile int *abort_flag) {
+  const Tile &t = x.t;
+  const int lane = threadIdx.x & 31;
+  const int row = t.m0 + rit;  // unpadded row
+  const bool valid = row < t.row_end;
+  const int prow = x.arow + rit, prow0 = prow - lane;  // padded rows; prow0 starts a 32-token block
+  const float w = valid ? __ldg(p.w_row + row) : 0.f;  // dA = w * (dy . W_down^T)
+  const int nch = min(NCH, (p.I - t.n0) / 32);
+  // Scale bytes (atom_byte without its divisions).  Along I: 128-row atoms of
+  // the padded rows, K = I; this lane's row prow, K block col/32.  Along
+  // tokens: rows = columns of dG, grouped per 192 (the tile's n index is the
+  // group, as tiles are 192 wide), K = Mpad; this lane's column n0 + 32c + lane,
+  // K block prow0/32.
+  const int wi = prow & 127;
+  const size_t sfi_base = static_cast<size_t>(prow >> 7) * (p.I >> 7) * 512 + (wi & 31) * 16 + (wi >> 5) * 4;
+  const int kbt = prow0 >> 5, nt = t.n0 / kMxBN;
+  const size_t kblocks_t = static_cast<size_t>(p.Mpad >> 7);
+  uint32_t r0[32];
+  float v1[32], v2[32];
+  bool ok = true;
+  for (int c = part; c < nch; c += 2) {
+    const int g = gbase + c, slot = g % kMxGuSlots;
+    if (!wait_lane0(&gu_full[slot], static_cast<uint32_t>(g / kMxGuSlots) & 1u, abort_flag)) {
+      ok = false;
+      break;
+    }
+    __syncwarp();  // the other lanes read the chunk after lane 0 saw it land
+    const uint8_t *gs = ring + slot * kGuChunkBytes, *us = gs + kGuHalfBytes;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 xg = *reinterpret_cast<const uint4 *>(gs + epi_swz(rit, q));
+      const uint4 xu = *reinterpret_cast<const uint4 *>(us + epi_swz(rit, q));
+      const uint32_t wg[4] = {xg.x, xg.y, xg.z, xg.w}, wu[4] = {xu.x, xu.y, xu.z, xu.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        v1[8 * q + 2 * h] = bf16_lo(wg[h]);
+        v1[8 * q + 2 * h + 1] = bf16_hi(wg[h]);
+        v2[8 * q + 2 * h] = bf16_lo(wu[h]);
+        v2[8 * q + 2 * h + 1] = bf16_hi(wu[h]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&gu_empty[slot]);
+    const int col = t.n0 + 32 * c;
+    tmem_ld32(tb + 32 * c, r0);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {  // in place: v1 G -> dU, v2 U -> dG
+      const float da = w * __uint_as_float(r0[i]), gg = v1[i], u = v2[i];
+      const float sg = sigmoid_approx(gg);
+      const float dg = da * u * sg * (1.f + gg * (1.f - sg));
+      const float du = da * gg * sg;  // dA * silu(G)
+      v2[i] = valid ? round_bf16(dg) : 0.f;
+      v1[i] = valid ? round_bf16(du) : 0.f;
+    }
+    // along I (dX's A operand): this lane's 32 values are one block of its row
+    const int kbi = col >> 5;
+    const size_t sfi = sfi_base + (kbi >> 2) * 512 + (kbi & 3);
+    p.dg_sf[sfi] = quant32(v2, reinterpret_cast<uint4 *>(p.dg_q + static_cast<size_t>(prow) * p.I + col));
+    p.du_sf[sfi] = quant32(v1, reinterpret_cast<uint4 *>(p.du_q + static_cast<size_t>(prow) * p.I + col));
+    // along tokens (dW_gate/up's B operand): the warp's 32 rows are one block
+    const int rr = 32 * c + lane, wt = rr & 127;
+    const size_t sft = ((2 * nt + (rr >> 7)) * kblocks_t + (kbt >> 2)) * 512 + (wt & 31) * 16 +
+                       (wt >> 5) * 4 + (kbt & 3);
+    quant_down_rows32(tile, v2, p.dg_t, static_cast<size_t>(p.Mpad), col, prow0, p.dg_t_sf + sft);
+    quant_down_rows32(tile, v1, p.du_t, static_cast<size_t>(p.Mpad), col, prow0, p.du_t_sf + sft);
+  }
+  gbase += nch;
+  return ok;
+}
+
 // One stage: A codes (128 rows), B codes (192 rows), the A scale atom and the
 // two B scale atoms of K block kb.
 template <int MODE>
@@ -254,15 +380,15 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
   uint64_t *tfull = bars + 2 * STAGES;  // [2] accumulator ready
   uint64_t *tempty = tfull + 2;         // [2] accumulator drained by the epilogue
   uint64_t *drain = tempty + 2;
-  uint64_t *gu_full = drain + 1;            // [kGuSlots] dA: a G/U chunk landed
-  uint64_t *gu_empty = gu_full + kGuSlots;  // [kGuSlots] dA: its 4 epilogue warps read it
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gu_empty + kGuSlots);
+  uint64_t *gu_full = drain + 1;            // [kMxGuSlots] dA: a G/U chunk landed
+  uint64_t *gu_empty = gu_full + kMxGuSlots;  // [kMxGuSlots] dA: its 4 epilogue warps read it
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gu_empty + kMxGuSlots);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *s_off = reinterpret_cast<int *>(sfs + STAGES * kSfBytes + 256);
   int *s_pad = s_off + (kMaxExperts + 1);
   int *s_ord = s_pad + (kMaxExperts + 1);  // ragged K: experts by decreasing row count
   uint8_t *epi_tiles = smem + epi_off(MODE);  // [epilogue warp] 32 x 32 bf16 staging tiles
-  uint8_t *gu_ring = smem + gu_off(MODE);     // dA: [kGuSlots] G chunk | U chunk
+  uint8_t *gu_ring = smem + gu_off(MODE);     // dA: [kMxGuSlots] G chunk | U chunk
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
 
@@ -276,7 +402,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
       mbar_init(&tempty[b], 32 * epi_warps(MODE));  // every epilogue thread
     }
     mbar_init(drain, 1);
-    for (int s = 0; s < kGuSlots; ++s) {
+    for (int s = 0; s < kMxGuSlots; ++s) {
       mbar_init(&gu_full[s], 1);
       mbar_init(&gu_empty[s], 4);  // the four warps (lane quarters) of one column half
     }
@@ -434,8 +560,8 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
       const uint32_t tb = tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
       uint8_t *stile = epi_tiles + (warp - 2) * kEpiTileBytes;
       if constexpr (MODE == kMxDA) {
-        if (!epilogue_da_ring<EpiView, BN / 32>(x.t, tb, rit, rit, v, part, stile, gu_ring, gu_full,
-                                                gu_empty, gbase, abort_flag))
+        if (!epilogue_da_mx<BN / 32>(x, tb, rit, p, part, stile, gu_ring, gu_full, gu_empty, gbase,
+                                     abort_flag))
           break;
       } else {
         epilogue_tile<MxTraits<MODE>::kEpi, EpiView, BN / 32>(x.t, tb, rit, v, part,
@@ -457,8 +583,8 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
         const MxTile x = decode_mx<MODE>(tile, p, s_off, s_pad, s_ord);
         const int nch = min(BN / 32, (p.I - x.t.n0) / 32);
         for (int c = 0; c < nch; ++c, ++g) {
-          const int slot = g % kGuSlots;
-          const uint32_t ph = static_cast<uint32_t>(g / kGuSlots) & 1u;
+          const int slot = g % kMxGuSlots;
+          const uint32_t ph = static_cast<uint32_t>(g / kMxGuSlots) & 1u;
           if (!mbar_wait(&gu_empty[slot], ph ^ 1u, abort_flag)) {
             ok = false;
             break;
@@ -472,7 +598,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
         }
       }
       if (*abort_flag) {  // let the copies in flight land before exit
-        for (int sl = 0; sl < kGuSlots; ++sl) {
+        for (int sl = 0; sl < kMxGuSlots; ++sl) {
           if (!((armed >> sl) & 1u)) continue;
           for (int i = 0; i < (1 << 22) && !mbar_try_wait(&gu_full[sl], (arm_par >> sl) & 1u); ++i) {
           }
@@ -540,6 +666,14 @@ cudaError_t launch_mx_mode(const MxGemmArgs &a, cudaStream_t s) {
   p.w_row = a.w_row;
   p.o0 = a.o0;
   p.o1 = a.o1;
+  p.dg_q = a.dg_q;
+  p.du_q = a.du_q;
+  p.dg_sf = a.dg_sf;
+  p.du_sf = a.du_sf;
+  p.dg_t = a.dg_t;
+  p.du_t = a.du_t;
+  p.dg_t_sf = a.dg_t_sf;
+  p.du_t_sf = a.du_t_sf;
   p.status = a.status;
   p.sfa0 = a.sfa0;
   p.sfa1 = a.sfa1;

@@ -128,6 +128,10 @@ struct MxGemmArgs {
   const uint16_t *G, *U;
   const float *w_row;
   uint16_t *o0, *o1;
+  // dA: its epilogue quantises dG and dU for the next two GEMMs -- along I
+  // (codes [Mpad, I], 128-row scale atoms: dX's A operand) and along tokens
+  // (codes [I, Mpad], 192-row scale groups: dW_gate/up's B operand)
+  uint8_t *dg_q, *du_q, *dg_sf, *du_sf, *dg_t, *du_t, *dg_t_sf, *du_t_sf;
   int32_t *status;
   int num_sms;
 };

@@ -6,11 +6,8 @@
 // descartes": MXFP8 group quantisation, MXFP8 grouped GEMM); the fp8_bwd mode
 // (BF16 forward, FP8 backward) in the Prime Mega MoE write-ups.
 //
-// Scale rule: the smallest power of two 2^X with amax / 2^X <= 448, so no
-// element of a block saturates; X is clamped to [-127, 127] and stored as the
-// E8M0 code X + 127; an all-zero block gets code 0.  Values are scaled by 2^-X
-// (exact) and converted with CUDA's round-to-nearest-even, saturating E4M3
-// conversion.
+// The scale rule and the E4M3 conversion are in mxfp8.cuh (shared with the
+// block-scaled dA GEMM, whose epilogue quantises dG and dU itself).
 //
 // Output layouts are what the block-scaled tensor-core GEMM loads:
 //   codes  K-major: [rows][K] bytes;
@@ -27,60 +24,10 @@
 // rows start at pad_off[e] = sum over e' < e of ceil(count/128)*128, the rows
 // past its count are zero codes with zero scales, so every 128-row tile and
 // every 32-element block along tokens starts inside one expert.
-#include <cuda_fp8.h>
-
-#include "common.cuh"
+#include "mxfp8.cuh"
 
 namespace moe {
 namespace {
-
-// E8M0 exponent of a block's scale from its (finite, non-negative) amax.
-__device__ __forceinline__ int mx_scale_exp(float amax) {
-  const uint32_t b = __float_as_uint(amax);
-  const int eb = static_cast<int>((b >> 23) & 0xFF);
-  if (amax <= 0.f) return -127;
-  if (eb == 0) return -127;  // below 2^-126: far under the smallest E4M3 step of any scale
-  int X = (eb - 127) - 8;    // amax = m 2^(eb-127), m in [1,2); 448 = 1.75 2^8
-  if ((b & 0x7FFFFFu) > 0x600000u) X += 1;  // m > 1.75
-  return X < -127 ? -127 : (X > 127 ? 127 : X);
-}
-
-__device__ __forceinline__ float pow2_neg(int X) {  // 2^-X for X in [-127, 126]
-  return __uint_as_float(static_cast<uint32_t>(127 - X) << 23);
-}
-
-__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
-  const uint32_t x0 = __nv_cvt_float_to_fp8(a, __NV_SATFINITE, __NV_E4M3);
-  const uint32_t x1 = __nv_cvt_float_to_fp8(b, __NV_SATFINITE, __NV_E4M3);
-  const uint32_t x2 = __nv_cvt_float_to_fp8(c, __NV_SATFINITE, __NV_E4M3);
-  const uint32_t x3 = __nv_cvt_float_to_fp8(d, __NV_SATFINITE, __NV_E4M3);
-  return x0 | (x1 << 8) | (x2 << 16) | (x3 << 24);
-}
-
-// Quantise 32 values held in registers; writes 32 code bytes; returns the E8M0 code.
-__device__ __forceinline__ uint8_t quant32(const float (&v)[32], uint4 *dst) {
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  const int X = mx_scale_exp(amax);
-  const float s = pow2_neg(X);  // exact; an all-zero block stays zero
-  uint32_t w[8];
-#pragma unroll
-  for (int q = 0; q < 8; ++q)
-    w[q] = pack_e4m3x4(v[4 * q] * s, v[4 * q + 1] * s, v[4 * q + 2] * s, v[4 * q + 3] * s);
-  dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-  dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-  return static_cast<uint8_t>(X + 127);
-}
-
-__device__ __forceinline__ size_t atom_byte(int row, int kblock, int K, SfLayout L) {
-  const int sg = row / L.seg, r = row - sg * L.seg;
-  const int g = r / L.group, rr = r - g * L.group;
-  const int gps = (L.seg + L.group - 1) / L.group, apg = (L.group + 127) >> 7;
-  const size_t rb = (static_cast<size_t>(sg) * gps + g) * apg + (rr >> 7);
-  const int w = rr & 127;
-  return (rb * (K >> 7) + (kblock >> 2)) * 512 + (w & 31) * 16 + (w >> 5) * 4 + (kblock & 3);
-}
 
 // Expert of padded row o (largest e with pad_off[e] <= o), from shared memory.
 __device__ __forceinline__ int expert_of(int o, const int *s_pad, int E) {
