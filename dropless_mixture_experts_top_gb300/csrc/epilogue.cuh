@@ -92,7 +92,10 @@ __device__ __forceinline__ void rows32_to_lanes(uint8_t *tile, const uint4 (&w)[
   __syncwarp();
 }
 
-__device__ __forceinline__ float sigmoidf_(float z) { return 1.f / (1.f + __expf(-z)); }
+// sigmoid with the approximate (branch-free) reciprocal: within a few fp32 ulp
+// of 1 / (1 + e^-z), far below the bf16 rounding of every output it feeds; the
+// IEEE division's special-case branch stalled the epilogue warps.
+__device__ __forceinline__ float sigmoidf_(float z) { return __fdividef(1.f, 1.f + __expf(-z)); }
 
 __device__ __forceinline__ int clamp_rows(int n) { return n < 0 ? 0 : (n > 32 ? 32 : n); }
 

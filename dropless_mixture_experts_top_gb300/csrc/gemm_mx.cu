@@ -206,10 +206,6 @@ __device__ __forceinline__ MxTile decode_mx(int tile, const MxParams &p, const i
   return x;
 }
 
-// sigmoid with the approximate (branch-free) reciprocal: within a few fp32
-// ulp of 1 / (1 + e^-z), far below the bf16 rounding that follows.
-__device__ __forceinline__ float sigmoid_approx(float z) { return __fdividef(1.f, 1.f + __expf(-z)); }
-
 // The value a bf16 tensor would hold (nearest even), as fp32.
 __device__ __forceinline__ float round_bf16(float v) {
   return __uint_as_float(static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v))) << 16);
@@ -299,7 +295,7 @@ __device__ __forceinline__ bool epilogue_da_mx(const MxTile &x, uint32_t tb, int
 #pragma unroll
     for (int i = 0; i < 32; ++i) {  // in place: v1 G -> dU, v2 U -> dG
       const float da = w * __uint_as_float(r0[i]), gg = v1[i], u = v2[i];
-      const float sg = sigmoid_approx(gg);
+      const float sg = sigmoidf_(gg);
       const float dg = da * u * sg * (1.f + gg * (1.f - sg));
       const float du = da * gg * sg;  // dA * silu(G)
       v2[i] = valid ? round_bf16(dg) : 0.f;
