@@ -64,10 +64,10 @@ def kernel_work(shape):
     q = lambda n: ("hbm", n * (2 + 1 + 1 / 32), "B")
     return {
         "mx_pad_offsets": ("hbm", (E + 1) * 8.0, "B"),
-        "mx_quant_dy": q(M * H), "mx_quant_W_down": q(E * I * H), "mx_quant_dG": q(M * I),
-        "mx_quant_dU": q(M * I), "mx_quant_W_gate": q(E * H * I), "mx_quant_W_up": q(E * H * I),
-        "mx_quantT_A_w": q(M * I), "mx_quantT_dy": q(M * H), "mx_quantT_x": q(M * H),
-        "mx_quantT_dG": q(M * I), "mx_quantT_dU": q(M * I),
+        # dy quantised along H and along tokens from one read
+        "mx_quant_dy_both": ("hbm", M * H * (2 + 2 * (1 + 1 / 32)), "B"),
+        "mx_quant_W_down": q(E * I * H), "mx_quant_W_gate": q(E * H * I), "mx_quant_W_up": q(E * H * I),
+        "mx_quantT_A_w": q(M * I), "mx_quantT_x": q(M * H),
         "mx_gemm_dA_dswiglu": ("tensor_fp8", 2 * MHI, "flop"),
         "mx_gemm_dX": ("tensor_fp8", 4 * MHI, "flop"),
         "mx_gemm_dW_down": ("tensor_fp8", 2 * MHI, "flop"),

@@ -265,9 +265,11 @@ moe_status backward_fp8(const Fp8Bwd &f, cudaStream_t s) {
   m.w_row = f.r->w_row;
   m.status = f.status;
   m.num_sms = f.sms;
-  // dA = w (Q(dy) . Q(W_down)^T), K = H; dSwiGLU epilogue -> Q(dG), Q(dU) on both axes
-  MOE_TRY(timed("mx_quant_dy", s, [&] {
-    return launch_quant_rows(f.dy_perm, Mp, H, off, pad_off, E, sc + q.dy_q, sc + q.dy_sf, sf_a(Mp), s);
+  // dA = w (Q(dy) . Q(W_down)^T), K = H; dSwiGLU epilogue -> Q(dG), Q(dU) on both axes.
+  // dy is quantised along H (dA) and along tokens (dW_down) from one read.
+  MOE_TRY(timed("mx_quant_dy_both", s, [&] {
+    return launch_quant_cols(f.dy_perm, H, Mp, off, pad_off, E, sc + q.dy_t, sc + q.dy_t_sf, sf_b(H),
+                             RowCodes{sc + q.dy_q, sc + q.dy_sf, sf_a(Mp)}, s);
   }));
   MOE_TRY(timed("mx_quant_W_down", s, [&] {
     return launch_quant_rows(f.W_down, E * I, H, nullptr, nullptr, E, sc + q.wd_q, sc + q.wd_sf,
@@ -314,11 +316,8 @@ moe_status backward_fp8(const Fp8Bwd &f, cudaStream_t s) {
   }));
   // dW_down = Q(w a)^T . Q(dy), K = the expert's tokens
   MOE_TRY(timed("mx_quantT_A_w", s, [&] {
-    return launch_quant_cols(f.A_w, I, Mp, off, pad_off, E, sc + q.aw_t, sc + q.aw_t_sf, sf_a(I), s);
-  }));
-  MOE_TRY(timed("mx_quantT_dy", s, [&] {
-    return launch_quant_cols(f.dy_perm, H, Mp, off, pad_off, E, sc + q.dy_t, sc + q.dy_t_sf, sf_b(H),
-                             s);
+    return launch_quant_cols(f.A_w, I, Mp, off, pad_off, E, sc + q.aw_t, sc + q.aw_t_sf, sf_a(I),
+                             RowCodes{}, s);
   }));
   m.a0 = sc + q.aw_t;
   m.sfa0 = sc + q.aw_t_sf;
@@ -329,7 +328,8 @@ moe_status backward_fp8(const Fp8Bwd &f, cudaStream_t s) {
   MOE_TRY(timed("mx_gemm_dW_down", s, [&] { return launch_mx_gemm(kMxGemmDWDown, m, s); }));
   // dW_gate = Q(x)^T . Q(dG), dW_up = Q(x)^T . Q(dU), K = the expert's tokens
   MOE_TRY(timed("mx_quantT_x", s, [&] {
-    return launch_quant_cols(f.x_perm, H, Mp, off, pad_off, E, sc + q.x_t, sc + q.x_t_sf, sf_a(H), s);
+    return launch_quant_cols(f.x_perm, H, Mp, off, pad_off, E, sc + q.x_t, sc + q.x_t_sf, sf_a(H),
+                             RowCodes{}, s);
   }));
   m.a0 = sc + q.x_t;
   m.sfa0 = sc + q.x_t_sf;

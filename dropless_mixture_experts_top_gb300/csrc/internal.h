@@ -113,10 +113,15 @@ cudaError_t launch_pad_offsets(const int32_t *offsets, int E, int32_t *pad_off, 
 cudaError_t launch_quant_rows(const uint16_t *src, int rows_out, int K, const int32_t *offsets,
                               const int32_t *pad_off, int E, uint8_t *codes, uint8_t *sf, SfLayout L,
                               cudaStream_t s);
-// along tokens: [M, C] permuted rows -> codes [C, Mpad] (padded token axis)
+// along tokens: [M, C] permuted rows -> codes [C, Mpad] (padded token axis);
+// with rows.codes set, also along C into the padded row space: codes [Mpad, C]
+struct RowCodes {
+  uint8_t *codes, *sf;
+  SfLayout L;
+};
 cudaError_t launch_quant_cols(const uint16_t *src, int C, int Mpad, const int32_t *offsets,
                               const int32_t *pad_off, int E, uint8_t *codes, uint8_t *sf, SfLayout L,
-                              cudaStream_t s);
+                              RowCodes rows, cudaStream_t s);
 
 enum MxGemmMode : int { kMxGemmDA = 0, kMxGemmDX = 1, kMxGemmDWDown = 2, kMxGemmDWGateUp = 3 };
 struct MxGemmArgs {

@@ -92,19 +92,24 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t *__restr
 
 // Token-axis quantisation, output transposed: codes [C][Mpad] (tokens
 // contiguous).  A block takes 128 padded rows (one expert's, as segments are
-// 128-aligned) x 64 columns: coalesced 128-byte row loads into shared memory,
-// one thread per (column, 32-token block) quantises down the column into a
-// shared output tile (64 rows of 128 codes, rows padded to 144 bytes against
-// bank conflicts), then the tile leaves as full 128-byte rows.  Tiles past the
-// padded total are skipped (never read).
+// 128-aligned) x 64 columns: coalesced 128-byte row loads into shared memory
+// (16-byte chunks XOR-swizzled by row, so that both a column walk and a row
+// walk are free of bank conflicts), one thread per (column, 32-token block)
+// quantises down the column into a shared output tile (64 rows of 128 codes,
+// rows padded to 144 bytes against bank conflicts), then the tile leaves as
+// full 128-byte rows.  Optionally the same tile is also quantised along its
+// rows (one thread per (row, 32-column block)) into the padded row space, so
+// an operand needed on both axes (dy) is read once.  Tiles past the padded
+// total are skipped (never read).
 constexpr int kQcRows = 128, kQcCols = 64, kQcThreads = 256;
 
-__global__ void __launch_bounds__(kQcThreads) quant_cols_kernel(const uint16_t *__restrict__ src, int C,
+__global__ void __launch_bounds__(kQcThreads, 3) quant_cols_kernel(const uint16_t *__restrict__ src, int C,
                                                                 int Mpad,
                                                                 const int32_t *__restrict__ offsets,
                                                                 const int32_t *__restrict__ pad_off, int E,
                                                                 uint8_t *__restrict__ codes,
-                                                                uint8_t *__restrict__ sf, SfLayout L) {
+                                                                uint8_t *__restrict__ sf, SfLayout L,
+                                                                RowCodes rows) {
   __shared__ int s_pad[kMaxExperts + 1];
   __shared__ __align__(16) uint16_t tile[kQcRows * kQcCols];
   constexpr int kOutStride = kQcRows + 16;  // bytes per output row in shared memory
@@ -128,23 +133,56 @@ __global__ void __launch_bounds__(kQcThreads) quant_cols_kernel(const uint16_t *
   __syncthreads();
   if (s_seg[2]) return;
   const int row0 = s_seg[0], nvalid = s_seg[1];
-  // the row tile's setup is shared by every column tile this block takes
-  for (int c0 = blockIdx.y * kQcCols; c0 < C; c0 += gridDim.y * kQcCols) {
+  // the row tile's setup is shared by every column tile this block takes; the
+  // next column tile's loads are issued before the current one is quantised
+  constexpr int kLoads = (kQcRows * kQcCols / 8) / kQcThreads;  // 16-byte pieces per thread
+  uint4 nxt[kLoads];
+  auto load_tile = [&](int c0) {
 #pragma unroll
-    for (int j = 0; j < (kQcRows * kQcCols / 8) / kQcThreads; ++j) {
+    for (int j = 0; j < kLoads; ++j) {
       const int i = threadIdx.x + j * kQcThreads;
       const int r = i >> 3, part = i & 7;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (r < nvalid)
-        v = __ldg(reinterpret_cast<const uint4 *>(src + static_cast<size_t>(row0 + r) * C + c0) + part);
-      *reinterpret_cast<uint4 *>(tile + r * kQcCols + part * 8) = v;
+      nxt[j] = r < nvalid ? __ldg(reinterpret_cast<const uint4 *>(src + static_cast<size_t>(row0 + r) * C + c0) +
+                                  part)
+                          : make_uint4(0, 0, 0, 0);
     }
+  };
+  const int cstep = gridDim.y * kQcCols;
+  if (blockIdx.y * kQcCols < C) load_tile(blockIdx.y * kQcCols);
+  for (int c0 = blockIdx.y * kQcCols; c0 < C; c0 += cstep) {
+#pragma unroll
+    for (int j = 0; j < kLoads; ++j) {
+      const int i = threadIdx.x + j * kQcThreads;
+      const int r = i >> 3, part = i & 7;
+      *reinterpret_cast<uint4 *>(tile + r * kQcCols + ((part ^ (r & 7)) << 3)) = nxt[j];
+    }
+    if (c0 + cstep < C) load_tile(c0 + cstep);
     __syncthreads();
+    if (rows.codes) {  // along the rows: thread = (row, 32-column block); zero rows past the count
+      const int r = threadIdx.x >> 1, bb = threadIdx.x & 1;
+      float v[32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(tile + r * kQcCols + (((4 * bb + q) ^ (r & 7)) << 3));
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          v[8 * q + 2 * h] = bf16_lo(ww[h]);
+          v[8 * q + 2 * h + 1] = bf16_hi(ww[h]);
+        }
+      }
+      const int prow = prow0 + r, kb = (c0 >> 5) + bb;
+      rows.sf[atom_byte(prow, kb, C, rows.L)] =
+          quant32(v, reinterpret_cast<uint4 *>(rows.codes + static_cast<size_t>(prow) * C + c0 + 32 * bb));
+    }
     const int cc = threadIdx.x % kQcCols, b = threadIdx.x / kQcCols;  // 4 blocks of 32 tokens
     float v[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      v[i] = __uint_as_float(static_cast<uint32_t>(tile[(32 * b + i) * kQcCols + cc]) << 16);
+    for (int i = 0; i < 32; ++i) {
+      const int r = 32 * b + i;
+      v[i] = __uint_as_float(static_cast<uint32_t>(tile[r * kQcCols + (((cc >> 3) ^ (r & 7)) << 3) + (cc & 7)])
+                             << 16);
+    }
     const int c = c0 + cc, o0 = prow0 + 32 * b;
     sf[atom_byte(c, o0 >> 5, Mpad, L)] = quant32(v, reinterpret_cast<uint4 *>(otile + cc * kOutStride + 32 * b));
     __syncthreads();
@@ -197,10 +235,10 @@ cudaError_t launch_quant_rows(const uint16_t *src, int rows_out, int K, const in
 
 cudaError_t launch_quant_cols(const uint16_t *src, int C, int Mpad, const int32_t *offsets,
                               const int32_t *pad_off, int E, uint8_t *codes, uint8_t *sf, SfLayout L,
-                              cudaStream_t s) {
+                              RowCodes rows, cudaStream_t s) {
   const int col_blocks = C / kQcCols < 4 ? C / kQcCols : 4;  // each loops over C / (64 * 4) column tiles
   const dim3 grid(static_cast<unsigned>(Mpad / kQcRows), static_cast<unsigned>(col_blocks));
-  quant_cols_kernel<<<grid, kQcThreads, 0, s>>>(src, C, Mpad, offsets, pad_off, E, codes, sf, L);
+  quant_cols_kernel<<<grid, kQcThreads, 0, s>>>(src, C, Mpad, offsets, pad_off, E, codes, sf, L, rows);
   return cudaGetLastError();
 }
 
