@@ -37,6 +37,12 @@
  *     reads them, and dg, du and w*a are rounded to bf16 (nearest-even) before
  *     they are quantised.  Where floating point decides an integer code, both
  *     this oracle and the GPU take the decision on the same bf16 values.
+ *   - mxfp8 (the forward GEMMs in MXFP8 as well): x along H and W_gate/W_up
+ *     along H (their reduction dimension) for GEMM1; a = silu(g) u, rounded to
+ *     bf16 (the forward's bf16 tensor), and W_down along I for GEMM2.  g and u
+ *     are the products of the dequantised operands (not rounded: the backward
+ *     reads them as bf16 through the fp8_bwd rule above); the backward of this
+ *     mode is the fp8_bwd backward on these forward values.
  *
  * Arithmetic: fp64 throughout; bf16 inputs are widened exactly.  The oracle
  * never rounds intermediates.  Loops run in a fixed order; OpenMP only splits
@@ -289,9 +295,19 @@ typedef struct {
   /* fp8_bwd: dequantised weights (quantised along each backward GEMM's K):
    * Wd along H, Wg/Wu along I.  NULL when not quantising. */
   const float *qWg, *qWu, *qWd;
+  /* mxfp8 forward: dequantised weights quantised along each forward GEMM's K:
+   * Wg/Wu along H, Wd along I.  NULL for the exact forward. */
+  const float *fWg, *fWu, *fWd;
 } ctx_t;
 
+static void expert_fwd_mx(const ctx_t *c, int64_t t, int e, double *g, double *u, double *a,
+                          double *y);
+
 static void expert_fwd(const ctx_t *c, int64_t t, int e, double *g, double *u, double *a, double *y) {
+  if (c->fWg) {
+    expert_fwd_mx(c, t, e, g, u, a, y);
+    return;
+  }
   const int H = c->sh->H, I = c->sh->I;
   const uint16_t *xt = c->x + t * H;
   const uint16_t *wg = c->Wg + (int64_t)e * H * I, *wu = c->Wu + (int64_t)e * H * I;
@@ -312,6 +328,35 @@ static void expert_fwd(const ctx_t *c, int64_t t, int e, double *g, double *u, d
   }
 }
 
+/* The same expert with its forward GEMMs in MXFP8: g = Q(x_t) . Q(W_gate[e])
+ * (x along H, W along H), u likewise; a = silu(g) u; y = Q(bf16(a)) . Q(W_down[e])
+ * (both along I). */
+static void expert_fwd_mx(const ctx_t *c, int64_t t, int e, double *g, double *u, double *a,
+                          double *y) {
+  const int H = c->sh->H, I = c->sh->I;
+  double *xq = malloc(sizeof(double) * (size_t)(H + I));
+  double *aq = xq + H;
+  for (int h = 0; h < H; ++h) xq[h] = bf(c->x[t * H + h]);
+  mx_vec(xq, H, 1);
+  const float *wg = c->fWg + (int64_t)e * H * I, *wu = c->fWu + (int64_t)e * H * I;
+  for (int i = 0; i < I; ++i) g[i] = u[i] = 0.0;
+  for (int h = 0; h < H; ++h)
+    for (int i = 0; i < I; ++i) {
+      g[i] += xq[h] * (double)wg[(int64_t)h * I + i];
+      u[i] += xq[h] * (double)wu[(int64_t)h * I + i];
+    }
+  for (int i = 0; i < I; ++i) a[i] = silu(g[i]) * u[i];
+  if (y) {
+    const float *wd = c->fWd + (int64_t)e * I * H;
+    for (int i = 0; i < I; ++i) aq[i] = oracle_round_bf16(a[i]);
+    mx_vec(aq, I, 1);
+    for (int h = 0; h < H; ++h) y[h] = 0.0;
+    for (int i = 0; i < I; ++i)
+      for (int h = 0; h < H; ++h) y[h] += aq[i] * (double)wd[(int64_t)i * H + h];
+  }
+  free(xq);
+}
+
 static void ctx_init(ctx_t *c, const oracle_shape *sh, const uint16_t *x, const uint16_t *Wg,
                      const uint16_t *Wu, const uint16_t *Wd, const uint16_t *dy, const float *qWg,
                      const float *qWu, const float *qWd) {
@@ -324,17 +369,30 @@ static void ctx_init(ctx_t *c, const oracle_shape *sh, const uint16_t *x, const 
   c->qWg = qWg;
   c->qWu = qWu;
   c->qWd = qWd;
+  c->fWg = c->fWu = c->fWd = NULL;
+}
+
+/* Forward-quantised weights (mxfp8): all three or none. */
+static int ctx_forward_quant(ctx_t *c, const float *fWg, const float *fWu, const float *fWd) {
+  if (!fWg && !fWu && !fWd) return 0;
+  if (!fWg || !fWu || !fWd || c->sh->H % 32 || c->sh->I % 32) return -1;
+  c->fWg = fWg;
+  c->fWu = fWu;
+  c->fWd = fWd;
+  return 0;
 }
 
 /* Forward for a list of tokens: out[n] = sum_j w_j * y(t, S_j).  Optionally the
- * per-choice expert outputs y [n, k, H]. */
+ * per-choice expert outputs y [n, k, H].  fWg/fWu/fWd: forward-quantised
+ * weights (mxfp8) or NULL. */
 EXPORT int oracle_forward(const oracle_shape *sh, const uint16_t *x, const int32_t *topk_idx,
                           const double *topk_w, const uint16_t *Wg, const uint16_t *Wu,
-                          const uint16_t *Wd, int64_t ntok, const int64_t *tokens, double *out,
-                          double *y_all) {
+                          const uint16_t *Wd, const float *fWg, const float *fWu, const float *fWd,
+                          int64_t ntok, const int64_t *tokens, double *out, double *y_all) {
   const int H = sh->H, I = sh->I, k = sh->k;
   ctx_t c;
   ctx_init(&c, sh, x, Wg, Wu, Wd, NULL, NULL, NULL, NULL);
+  if (ctx_forward_quant(&c, fWg, fWu, fWd)) return -1;
   int bad = 0;
 #pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
   for (int64_t n = 0; n < ntok; ++n) {
@@ -360,11 +418,13 @@ EXPORT int oracle_forward(const oracle_shape *sh, const uint16_t *x, const int32
 /* Expert intermediates of listed (token, expert) pairs, for localising a
  * mismatch: g, u, a [n, I] and y [n, H] of expert e on token t. */
 EXPORT int oracle_expert_rows(const oracle_shape *sh, const uint16_t *x, const uint16_t *Wg,
-                              const uint16_t *Wu, const uint16_t *Wd, int64_t n,
+                              const uint16_t *Wu, const uint16_t *Wd, const float *fWg,
+                              const float *fWu, const float *fWd, int64_t n,
                               const int64_t *tokens, const int32_t *experts, double *g, double *u,
                               double *a, double *y) {
   ctx_t c;
   ctx_init(&c, sh, x, Wg, Wu, Wd, NULL, NULL, NULL, NULL);
+  if (ctx_forward_quant(&c, fWg, fWu, fWd)) return -1;
   int bad = 0;
 #pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
   for (int64_t q = 0; q < n; ++q) {
@@ -394,12 +454,14 @@ EXPORT int oracle_backward_tokens(const oracle_shape *sh, const uint16_t *x, con
                                   const int32_t *topk_idx, const double *topk_w, const uint16_t *Wg,
                                   const uint16_t *Wu, const uint16_t *Wd, const uint16_t *dy,
                                   int32_t quant, const float *qWg, const float *qWu,
-                                  const float *qWd, int64_t ntok, const int64_t *tokens, double *dx,
+                                  const float *qWd, const float *fWg, const float *fWu,
+                                  const float *fWd, int64_t ntok, const int64_t *tokens, double *dx,
                                   double *d_logits, double *gdot_out) {
   const int H = sh->H, I = sh->I, E = sh->E, k = sh->k;
   if (quant && (!qWg || !qWu || !qWd || H % 32 || I % 32)) return -1;
   ctx_t c;
   ctx_init(&c, sh, x, Wg, Wu, Wd, dy, qWg, qWu, qWd);
+  if (ctx_forward_quant(&c, fWg, fWu, fWd)) return -1;
   int bad = 0;
 #pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
   for (int64_t n = 0; n < ntok; ++n) {
@@ -564,11 +626,12 @@ static void expert_rows_bwd(const ctx_t *c, int e, int64_t n, const int64_t *tok
 EXPORT int oracle_dw_full(const oracle_shape *sh, const uint16_t *x, const int32_t *topk_idx,
                           const double *topk_w, const uint16_t *Wg, const uint16_t *Wu,
                           const uint16_t *Wd, const uint16_t *dy, int32_t quant, const float *qWg,
-                          const float *qWu, const float *qWd, double *dWg, double *dWu,
-                          double *dWd) {
+                          const float *qWu, const float *qWd, const float *fWg, const float *fWu,
+                          const float *fWd, double *dWg, double *dWu, double *dWd) {
   const int H = sh->H, I = sh->I, E = sh->E;
   ctx_t c;
   ctx_init(&c, sh, x, Wg, Wu, Wd, dy, qWg, qWu, qWd);
+  if (ctx_forward_quant(&c, fWg, fWu, fWd)) return -1;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int e = 0; e < E; ++e) {
     int64_t *tok = malloc(sizeof(int64_t) * (size_t)sh->T);
@@ -625,12 +688,14 @@ EXPORT int oracle_dw_full(const oracle_shape *sh, const uint16_t *x, const int32
 EXPORT int oracle_dw_elements(const oracle_shape *sh, const uint16_t *x, const int32_t *topk_idx,
                               const double *topk_w, const uint16_t *Wg, const uint16_t *Wu,
                               const uint16_t *Wd, const uint16_t *dy, int32_t quant,
-                              const float *qWg, const float *qWu, const float *qWd, int64_t nel,
+                              const float *qWg, const float *qWu, const float *qWd,
+                              const float *fWg, const float *fWu, const float *fWd, int64_t nel,
                               const int32_t *which, const int32_t *ee, const int32_t *rr,
                               const int32_t *cc, double *val) {
   const int H = sh->H, I = sh->I, k = sh->k;
   ctx_t c;
   ctx_init(&c, sh, x, Wg, Wu, Wd, dy, qWg, qWu, qWd);
+  if (ctx_forward_quant(&c, fWg, fWu, fWd)) return -1;
   int bad = 0;
 #pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
   for (int64_t q = 0; q < nel; ++q) {
@@ -644,19 +709,30 @@ EXPORT int oracle_dw_elements(const oracle_shape *sh, const uint16_t *x, const i
     int64_t n = expert_rows(sh, topk_idx, e, tok, ch);
     double *L = malloc(sizeof(double) * (size_t)(n + 1));
     double *R = malloc(sizeof(double) * (size_t)(n + 1));
-    double *dyw = malloc(sizeof(double) * (size_t)H);
+    double *dyw = malloc(sizeof(double) * (size_t)(2 * H));
+    double *xq = dyw + H;
     /* only column ci of g and u is needed: the same sums over h, in the same
-     * order, as expert_fwd computes for every column */
+     * order, as expert_fwd (or expert_fwd_mx) computes for every column */
     const int ci = (wh == 2) ? r0 : c0;
     const uint16_t *wg = Wg + (int64_t)e * H * I, *wu = Wu + (int64_t)e * H * I;
     for (int64_t r = 0; r < n; ++r) {
       int64_t t = tok[r];
       double w = topk_w[t * k + ch[r]];
       double gi = 0.0, ui = 0.0;
-      for (int h = 0; h < H; ++h) {
-        double xv = bf(x[t * H + h]);
-        gi += xv * bf(wg[(int64_t)h * I + ci]);
-        ui += xv * bf(wu[(int64_t)h * I + ci]);
+      if (c.fWg) {
+        const float *fg = c.fWg + (int64_t)e * H * I, *fu = c.fWu + (int64_t)e * H * I;
+        for (int h = 0; h < H; ++h) xq[h] = bf(x[t * H + h]);
+        mx_vec(xq, H, 1);
+        for (int h = 0; h < H; ++h) {
+          gi += xq[h] * (double)fg[(int64_t)h * I + ci];
+          ui += xq[h] * (double)fu[(int64_t)h * I + ci];
+        }
+      } else {
+        for (int h = 0; h < H; ++h) {
+          double xv = bf(x[t * H + h]);
+          gi += xv * bf(wg[(int64_t)h * I + ci]);
+          ui += xv * bf(wu[(int64_t)h * I + ci]);
+        }
       }
       if (wh == 2) { /* dW_down[e, i=r0, h=c0] = sum a_i * (w dy)_h */
         if (quant) { /* operands w*a (a bf16 tensor) and dy */

@@ -48,11 +48,13 @@ def lib():
             i64, i32 = ctypes.c_int64, ctypes.c_int32
             L.oracle_route.argtypes = [i64, i32, i32, P, P, P]
             L.oracle_dispatch.argtypes = [i64, i32, i32, P, P, P, P, P]
-            L.oracle_forward.argtypes = [P, P, P, P, P, P, P, i64, P, P, P]
-            L.oracle_backward_tokens.argtypes = [P, P, P, P, P, P, P, P, P, i32, P, P, P, i64, P, P, P, P]
-            L.oracle_dw_full.argtypes = [P, P, P, P, P, P, P, P, i32, P, P, P, P, P, P]
-            L.oracle_dw_elements.argtypes = [P, P, P, P, P, P, P, P, i32, P, P, P, i64, P, P, P, P, P]
-            L.oracle_expert_rows.argtypes = [P, P, P, P, P, i64, P, P, P, P, P, P]
+            L.oracle_forward.argtypes = [P, P, P, P, P, P, P, P, P, P, i64, P, P, P]
+            L.oracle_backward_tokens.argtypes = [P, P, P, P, P, P, P, P, P, i32, P, P, P, P, P, P, i64, P, P,
+                                                 P, P]
+            L.oracle_dw_full.argtypes = [P, P, P, P, P, P, P, P, i32, P, P, P, P, P, P, P, P, P]
+            L.oracle_dw_elements.argtypes = [P, P, P, P, P, P, P, P, i32, P, P, P, P, P, P, i64, P, P, P, P,
+                                             P]
+            L.oracle_expert_rows.argtypes = [P, P, P, P, P, P, P, P, i64, P, P, P, P, P, P]
             L.oracle_e4m3_encode.argtypes = [ctypes.c_double]
             L.oracle_e4m3_encode.restype = ctypes.c_uint8
             L.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
@@ -114,21 +116,31 @@ def dispatch(topk_idx: np.ndarray, E: int):
     return counts, offsets, ros, sor
 
 
-def forward(shape, x, topk_idx, topk_w, W_gate, W_up, W_down, tokens=None, want_y=False):
-    """out [n,H] fp64 for the listed tokens (all tokens by default); optionally y [n,k,H]."""
+def _fq(fwd_quant, fW, W_gate, W_up, W_down):
+    """Pointers to the forward-quantised weights (mxfp8 mode) or three NULLs."""
+    if not fwd_quant:
+        return None, None, None
+    return fW if fW is not None else quant_weights_fwd(W_gate, W_up, W_down)
+
+
+def forward(shape, x, topk_idx, topk_w, W_gate, W_up, W_down, tokens=None, want_y=False,
+            fwd_quant=False, fW=None):
+    """out [n,H] fp64 for the listed tokens (all tokens by default); optionally y [n,k,H].
+    fwd_quant: the mxfp8 mode's forward (both forward GEMMs' operands quantised)."""
     tokens = np.arange(shape.T, dtype=np.int64) if tokens is None else _c(tokens, np.int64)
     n = len(tokens)
     out = np.empty((n, shape.H), np.float64)
     y = np.empty((n, shape.k, shape.H), np.float64) if want_y else None
+    fg, fu, fd = _fq(fwd_quant, fW, W_gate, W_up, W_down)
     sh = _shape(shape)
     _check(lib().oracle_forward(ctypes.byref(sh), _p(_c(x, np.uint16)), _p(_c(topk_idx, np.int32)),
                                 _p(_c(topk_w, np.float64)), _p(_c(W_gate, np.uint16)),
-                                _p(_c(W_up, np.uint16)), _p(_c(W_down, np.uint16)), n, _p(tokens),
-                                _p(out), _p(y)), "forward")
+                                _p(_c(W_up, np.uint16)), _p(_c(W_down, np.uint16)), _p(fg), _p(fu), _p(fd),
+                                n, _p(tokens), _p(out), _p(y)), "forward")
     return (out, y) if want_y else out
 
 
-def expert_rows(shape, x, W_gate, W_up, W_down, tokens, experts):
+def expert_rows(shape, x, W_gate, W_up, W_down, tokens, experts, fwd_quant=False, fW=None):
     """g, u, a [n,I] and y [n,H] (fp64) of expert experts[q] applied to token tokens[q]."""
     tokens = _c(tokens, np.int64)
     experts = _c(experts, np.int32)
@@ -137,10 +149,12 @@ def expert_rows(shape, x, W_gate, W_up, W_down, tokens, experts):
     u = np.empty((n, shape.I))
     a = np.empty((n, shape.I))
     y = np.empty((n, shape.H))
+    fg, fu, fd = _fq(fwd_quant, fW, W_gate, W_up, W_down)
     sh = _shape(shape)
     _check(lib().oracle_expert_rows(ctypes.byref(sh), _p(_c(x, np.uint16)), _p(_c(W_gate, np.uint16)),
-                                    _p(_c(W_up, np.uint16)), _p(_c(W_down, np.uint16)), n, _p(tokens),
-                                    _p(experts), _p(g), _p(u), _p(a), _p(y)), "expert_rows")
+                                    _p(_c(W_up, np.uint16)), _p(_c(W_down, np.uint16)), _p(fg), _p(fu),
+                                    _p(fd), n, _p(tokens), _p(experts), _p(g), _p(u), _p(a), _p(y)),
+           "expert_rows")
     return g, u, a, y
 
 
@@ -158,8 +172,24 @@ def quant_weights(W_gate, W_up, W_down):
     return tuple(res)
 
 
+def quant_weights_fwd(W_gate, W_up, W_down):
+    """Dequantised MXFP8 copies of the weights as the mxfp8 forward GEMMs see
+    them: W_gate/W_up along H and W_down along I (each one's middle axis, the
+    forward GEMM's reduction dimension)."""
+    res = []
+    for W in (W_gate, W_up, W_down):
+        W = _c(W, np.uint16)
+        E, R, C = W.shape
+        Wt = np.ascontiguousarray(W.transpose(0, 2, 1))  # [E, C, R]: the reduction axis last
+        deq = np.empty(Wt.shape, np.float32)
+        _check(lib().oracle_mx_quantize_rows_bf16(E * C, R, _p(Wt), None, None, _p(deq)),
+               "mx_quantize_rows")
+        res.append(np.ascontiguousarray(deq.transpose(0, 2, 1)))
+    return tuple(res)
+
+
 def backward_tokens(shape, x, logits, topk_idx, topk_w, W_gate, W_up, W_down, dy, tokens=None,
-                    quant=False, qW=None):
+                    quant=False, qW=None, fwd_quant=False, fW=None):
     """dx [n,H], d_logits [n,E], gdot [n,k] (fp64) for the listed tokens."""
     tokens = np.arange(shape.T, dtype=np.int64) if tokens is None else _c(tokens, np.int64)
     n = len(tokens)
@@ -169,16 +199,18 @@ def backward_tokens(shape, x, logits, topk_idx, topk_w, W_gate, W_up, W_down, dy
     if quant and qW is None:
         qW = quant_weights(W_gate, W_up, W_down)
     qg, qu, qd = qW if quant else (None, None, None)
+    fg, fu, fd = _fq(fwd_quant, fW, W_gate, W_up, W_down)
     sh = _shape(shape)
     _check(lib().oracle_backward_tokens(
         ctypes.byref(sh), _p(_c(x, np.uint16)), _p(_c(logits, np.float32)), _p(_c(topk_idx, np.int32)),
         _p(_c(topk_w, np.float64)), _p(_c(W_gate, np.uint16)), _p(_c(W_up, np.uint16)),
         _p(_c(W_down, np.uint16)), _p(_c(dy, np.uint16)), int(bool(quant)), _p(qg), _p(qu), _p(qd),
-        n, _p(tokens), _p(dx), _p(dl), _p(gd)), "backward_tokens")
+        _p(fg), _p(fu), _p(fd), n, _p(tokens), _p(dx), _p(dl), _p(gd)), "backward_tokens")
     return dx, dl, gd
 
 
-def dw_full(shape, x, topk_idx, topk_w, W_gate, W_up, W_down, dy, quant=False, qW=None):
+def dw_full(shape, x, topk_idx, topk_w, W_gate, W_up, W_down, dy, quant=False, qW=None,
+            fwd_quant=False, fW=None):
     """dW_gate, dW_up [E,H,I] and dW_down [E,I,H] (fp64)."""
     E, H, I = shape.E, shape.H, shape.I
     dWg = np.empty((E, H, I), np.float64)
@@ -187,17 +219,18 @@ def dw_full(shape, x, topk_idx, topk_w, W_gate, W_up, W_down, dy, quant=False, q
     if quant and qW is None:
         qW = quant_weights(W_gate, W_up, W_down)
     qg, qu, qd = qW if quant else (None, None, None)
+    fg, fu, fd = _fq(fwd_quant, fW, W_gate, W_up, W_down)
     sh = _shape(shape)
     _check(lib().oracle_dw_full(
         ctypes.byref(sh), _p(_c(x, np.uint16)), _p(_c(topk_idx, np.int32)), _p(_c(topk_w, np.float64)),
         _p(_c(W_gate, np.uint16)), _p(_c(W_up, np.uint16)), _p(_c(W_down, np.uint16)),
-        _p(_c(dy, np.uint16)), int(bool(quant)), _p(qg), _p(qu), _p(qd), _p(dWg), _p(dWu), _p(dWd)),
-        "dw_full")
+        _p(_c(dy, np.uint16)), int(bool(quant)), _p(qg), _p(qu), _p(qd), _p(fg), _p(fu), _p(fd),
+        _p(dWg), _p(dWu), _p(dWd)), "dw_full")
     return dWg, dWu, dWd
 
 
 def dw_elements(shape, x, topk_idx, topk_w, W_gate, W_up, W_down, dy, which, e, r, c, quant=False,
-                qW=None):
+                qW=None, fwd_quant=False, fW=None):
     """Selected weight-gradient elements: which 0 = dW_gate[e,r,c], 1 = dW_up[e,r,c],
     2 = dW_down[e,r,c]."""
     which, e, r, c = (_c(a, np.int32) for a in (which, e, r, c))
@@ -205,12 +238,13 @@ def dw_elements(shape, x, topk_idx, topk_w, W_gate, W_up, W_down, dy, which, e, 
     if quant and qW is None:
         qW = quant_weights(W_gate, W_up, W_down)
     qg, qu, qd = qW if quant else (None, None, None)
+    fg, fu, fd = _fq(fwd_quant, fW, W_gate, W_up, W_down)
     sh = _shape(shape)
     _check(lib().oracle_dw_elements(
         ctypes.byref(sh), _p(_c(x, np.uint16)), _p(_c(topk_idx, np.int32)), _p(_c(topk_w, np.float64)),
         _p(_c(W_gate, np.uint16)), _p(_c(W_up, np.uint16)), _p(_c(W_down, np.uint16)),
-        _p(_c(dy, np.uint16)), int(bool(quant)), _p(qg), _p(qu), _p(qd), len(which), _p(which), _p(e),
-        _p(r), _p(c), _p(val)), "dw_elements")
+        _p(_c(dy, np.uint16)), int(bool(quant)), _p(qg), _p(qu), _p(qd), _p(fg), _p(fu), _p(fd),
+        len(which), _p(which), _p(e), _p(r), _p(c), _p(val)), "dw_elements")
     return val
 
 

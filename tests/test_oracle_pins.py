@@ -14,7 +14,10 @@
   * the bf16 rounding the fp8_bwd mode applies against torch's fp32 -> bf16
     conversion, and the fp8_bwd backward against a numpy composition of the
     pinned quantiser and rounding (which operands, along which axis, rounded
-    where).
+    where);
+  * the mxfp8 mode's forward (both forward GEMMs in MXFP8) and its backward
+    against the same kind of composition, with the weights quantised through
+    the column quantiser (a different routine from the one the oracle uses).
 """
 import itertools
 
@@ -520,3 +523,123 @@ def test_router_backward_through_the_layer_matches_torch_autograd():
     ((wt.unsqueeze(-1) * y).sum(1) * dy).sum().backward()
     np.testing.assert_allclose(dWr, Wr.grad.numpy(), rtol=1e-10, atol=1e-13)
     np.testing.assert_allclose(dx + dx_router, x.grad.numpy(), rtol=1e-10, atol=1e-13)
+
+
+# ----------------------------------------------------------------------------- mxfp8 forward
+
+
+def _fwd_weights_by_cols(W, table):
+    """Dequantised W [E, R, C] quantised along R (blocks of 32 rows of each
+    column) through the column quantiser."""
+    E, R, C = W.shape
+    return np.stack([_deq_cols(W[e], 0, R, table) for e in range(E)])
+
+
+def _mxfp8_chain(inp, shape, idx, w):
+    """The mxfp8 forward written out with numpy products: Q(x) . Q(W_gate) (both
+    along H), a = silu(g) u, y = Q(bf16(a)) . Q(W_down) (both along I)."""
+    T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
+    table = np.array([O.e4m3_decode(c) for c in range(256)])
+    f = lambda b: bf16_bits_to_f32(b).astype(np.float64)
+    q_rows = lambda v: O.mx_quantize_rows(f32_to_bf16_bits(np.atleast_2d(v).astype(np.float32)))[2].astype(np.float64)
+    rb = np.vectorize(O.round_bf16)
+    xq = O.mx_quantize_rows(inp["x"])[2].astype(np.float64)
+    Wg, Wu, Wd = (_fwd_weights_by_cols(inp[n], table) for n in ("W_gate", "W_up", "W_down"))
+    sig = lambda z: 1 / (1 + np.exp(-z))
+    out = np.zeros((T, H))
+    per = {}
+    for t in range(T):
+        for j in range(k):
+            e = idx[t, j]
+            g, u = xq[t] @ Wg[e], xq[t] @ Wu[e]
+            a = g * sig(g) * u
+            y = q_rows(rb(a))[0] @ Wd[e]
+            out[t] += w[t, j] * y
+            per[(t, j)] = (g, u, a, y)
+    return out, per
+
+
+def test_mxfp8_forward_composition():
+    shape = MoEShape(T=96, H=64, I=96, E=4, k=2)
+    inp = synth.make_inputs_shape(shape, 31, w_scale=0.3)
+    idx, w = O.route(inp["logits"], shape.k)
+    ref, per = _mxfp8_chain(inp, shape, idx, w)
+    got, y = O.forward(shape, inp["x"], idx, w, inp["W_gate"], inp["W_up"], inp["W_down"], want_y=True,
+                       fwd_quant=True)
+    rel = lambda a, b: np.linalg.norm(a - b) / np.linalg.norm(b)
+    assert rel(got, ref) < 1e-12
+    toks = np.repeat(np.arange(shape.T), shape.k)
+    g, u, a, yy = O.expert_rows(shape, inp["x"], inp["W_gate"], inp["W_up"], inp["W_down"], toks, idx.ravel(),
+                                fwd_quant=True)
+    for q, (t, j) in enumerate(zip(toks, np.tile(np.arange(shape.k), shape.T))):
+        for got_v, ref_v in zip((g[q], u[q], a[q], yy[q], y[t, j]), per[(t, j)] + (per[(t, j)][3],)):
+            np.testing.assert_allclose(got_v, ref_v, rtol=1e-12, atol=1e-12)
+    # the quantised forward differs from the exact one by quantisation error only
+    exact = O.forward(shape, inp["x"], idx, w, inp["W_gate"], inp["W_up"], inp["W_down"])
+    assert 5e-3 < rel(got, exact) < 1.2e-1
+    # the forward-quantised weights sit on the E4M3 x 2^X grid along the reduction axis
+    fWg, fWu, fWd = O.quant_weights_fwd(inp["W_gate"], inp["W_up"], inp["W_down"])
+    table = np.array([O.e4m3_decode(c) for c in range(256)])
+    np.testing.assert_array_equal(fWg, _fwd_weights_by_cols(inp["W_gate"], table).astype(np.float32))
+    np.testing.assert_array_equal(fWd, _fwd_weights_by_cols(inp["W_down"], table).astype(np.float32))
+
+
+def test_mxfp8_backward_composition():
+    """The mxfp8 mode's backward is the fp8_bwd backward on the quantised forward's
+    values: gdot = <dy, y_q>, dSwiGLU on bf16(g_q), bf16(u_q), dW_down's operand
+    bf16(w a_q)."""
+    shape = MoEShape(T=96, H=64, I=96, E=4, k=2)
+    inp = synth.make_inputs_shape(shape, 33, w_scale=0.3)
+    T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
+    idx, w = O.route(inp["logits"], k)
+    _, per = _mxfp8_chain(inp, shape, idx, w)
+    f = lambda b: bf16_bits_to_f32(b).astype(np.float64)
+    dy = f(inp["dy"])
+    qWg, qWu, qWd = (q.astype(np.float64) for q in O.quant_weights(inp["W_gate"], inp["W_up"], inp["W_down"]))
+    rb = np.vectorize(O.round_bf16)
+    q_rows = lambda v: O.mx_quantize_rows(f32_to_bf16_bits(np.atleast_2d(v).astype(np.float32)))[2].astype(np.float64)
+    sig = lambda z: 1 / (1 + np.exp(-z))
+    dx = np.zeros((T, H))
+    gd = np.zeros((T, k))
+    rows = {e: [] for e in range(E)}
+    for t in range(T):
+        for j in range(k):
+            e, wt = idx[t, j], w[t, j]
+            g, u, a, y = per[(t, j)]
+            gd[t, j] = dy[t] @ y
+            da = wt * (q_rows(dy[t])[0] @ qWd[e].T)
+            gb, ub = rb(g), rb(u)
+            dg = rb(da * ub * sig(gb) * (1 + gb * (1 - sig(gb))))
+            du = rb(da * gb * sig(gb))
+            dx[t] += q_rows(dg)[0] @ qWg[e].T + q_rows(du)[0] @ qWu[e].T
+            rows[e].append((t, rb(wt * a), dg, du))
+    got_dx, got_dl, got_gd = O.backward_tokens(shape, inp["x"], inp["logits"], idx, w, inp["W_gate"], inp["W_up"],
+                                               inp["W_down"], inp["dy"], quant=True, fwd_quant=True)
+    rel = lambda a, b: np.linalg.norm(a - b) / np.linalg.norm(b)
+    assert rel(got_dx, dx) < 1e-12
+    assert rel(got_gd, gd) < 1e-12
+    dWg, dWu, dWd = O.dw_full(shape, inp["x"], idx, w, inp["W_gate"], inp["W_up"], inp["W_down"], inp["dy"],
+                              quant=True, fwd_quant=True)
+    table = np.array([O.e4m3_decode(c) for c in range(256)])
+    for e in range(E):
+        toks = [r[0] for r in rows[e]]
+        n = len(toks)
+        bits = lambda m: f32_to_bf16_bits(np.asarray(m, np.float32).reshape(n, -1))
+        Xq = _deq_cols(inp["x"][toks], 0, n, table)
+        DYq = _deq_cols(inp["dy"][toks], 0, n, table)
+        Aq = _deq_cols(bits([r[1] for r in rows[e]]), 0, n, table)
+        DGq = _deq_cols(bits([r[2] for r in rows[e]]), 0, n, table)
+        DUq = _deq_cols(bits([r[3] for r in rows[e]]), 0, n, table)
+        assert rel(Xq.T @ DGq, dWg[e]) < 1e-12
+        assert rel(Xq.T @ DUq, dWu[e]) < 1e-12
+        assert rel(Aq.T @ DYq, dWd[e]) < 1e-12
+    rng = np.random.default_rng(4)
+    which = rng.integers(0, 3, 60).astype(np.int32)
+    ee = rng.integers(0, E, 60).astype(np.int32)
+    rr = np.where(which == 2, rng.integers(0, I, 60), rng.integers(0, H, 60)).astype(np.int32)
+    cc = np.where(which == 2, rng.integers(0, H, 60), rng.integers(0, I, 60)).astype(np.int32)
+    got = O.dw_elements(shape, inp["x"], idx, w, inp["W_gate"], inp["W_up"], inp["W_down"], inp["dy"],
+                        which, ee, rr, cc, quant=True, fwd_quant=True)
+    full = np.stack([dWg, dWu])
+    exp = np.array([dWd[e, r, c] if wh == 2 else full[wh, e, r, c] for wh, e, r, c in zip(which, ee, rr, cc)])
+    np.testing.assert_allclose(got, exp, rtol=1e-12, atol=1e-14)
