@@ -64,6 +64,11 @@ def kernel_work(shape):
     q = lambda n: ("hbm", n * (2 + 1 + 1 / 32), "B")
     return {
         "mx_pad_offsets": ("hbm", (E + 1) * 8.0, "B"),
+        "mx_pad_offsets_fwd": ("hbm", (E + 1) * 8.0, "B"),
+        # mxfp8 forward: x along H; the weights along their middle axis (gate and up, down)
+        "mx_quant_x": q(M * H), "mx_quant_W_gateup_fwd": q(2 * E * H * I), "mx_quant_W_down_fwd": q(E * I * H),
+        "mx_gemm_gateup_swiglu": ("tensor_fp8", 4 * MHI, "flop"),
+        "mx_gemm_down": ("tensor_fp8", 2 * MHI, "flop"),
         # dy quantised along H and along tokens from one read
         "mx_quant_dy_both": ("hbm", M * H * (2 + 2 * (1 + 1 / 32)), "B"),
         "mx_quant_W_down": q(E * I * H), "mx_quant_W_gate": q(E * H * I), "mx_quant_W_up": q(E * H * I),
@@ -189,13 +194,16 @@ def oracle_sub_batch_step(O, w, inp, S):
     t0 = time.perf_counter()
     idx, wts = O.route(inp["logits"][:S], shape.k)
     O.dispatch(idx, shape.E)
-    O.forward(sub, inp["x"][:S], idx, wts, inp["W_gate"], inp["W_up"], inp["W_down"])
-    quant = w.precision == "fp8_bwd"
+    O.forward(sub, inp["x"][:S], idx, wts, inp["W_gate"], inp["W_up"], inp["W_down"],
+              fwd_quant=w.precision == "mxfp8")
+    quant = w.precision in ("fp8_bwd", "mxfp8")
+    fq = w.precision == "mxfp8"
     qW = O.quant_weights(inp["W_gate"], inp["W_up"], inp["W_down"]) if quant else None
+    fW = O.quant_weights_fwd(inp["W_gate"], inp["W_up"], inp["W_down"]) if fq else None
     O.backward_tokens(sub, inp["x"][:S], inp["logits"][:S], idx, wts, inp["W_gate"], inp["W_up"],
-                      inp["W_down"], inp["dy"][:S], quant=quant, qW=qW)
+                      inp["W_down"], inp["dy"][:S], quant=quant, qW=qW, fwd_quant=fq, fW=fW)
     O.dw_full(sub, inp["x"][:S], idx, wts, inp["W_gate"], inp["W_up"], inp["W_down"], inp["dy"][:S],
-              quant=quant, qW=qW)
+              quant=quant, qW=qW, fwd_quant=fq, fW=fW)
     return time.perf_counter() - t0
 
 
@@ -462,7 +470,8 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": world_tokens / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16" if w.precision == "bf16" else "bf16 fwd + mxfp8 bwd GEMMs",
+        "vs_baseline": None, "dtype": {"bf16": "bf16", "fp8_bwd": "bf16 fwd + mxfp8 bwd GEMMs",
+                                            "mxfp8": "mxfp8 fwd + bwd GEMMs"}[w.precision],
         "data": "synthetic (seeded normals; Qwen3-shaped layer)",
         "config": {"workload": w.name, "T": shape.T, "H": shape.H, "I": shape.I, "E": shape.E, "k": shape.k,
                    "precision": w.precision, "parallelism": "replicas" if world > 1 else "single GPU",

@@ -42,8 +42,10 @@ struct Layout {
   size_t f_total;
   // backward scratch
   size_t b_dyp, b_dG, b_dU, b_dX, b_maps, b_total;
-  // fp8_bwd: quantised operands inside the backward scratch (zero otherwise)
+  // fp8_bwd and mxfp8: quantised operands inside the backward scratch (zero otherwise)
   moe_fp8_layout q;
+  // mxfp8: quantised operands of the forward GEMMs inside the forward scratch
+  moe_mxfp8_fwd_layout fq;
 };
 
 bool shape_ok(const moe_config *c) {
@@ -51,9 +53,11 @@ bool shape_ok(const moe_config *c) {
   if (c->T < 0 || c->H < 64 || c->I < 64 || c->H % 64 || c->I % 64) return false;
   if (c->E < 1 || c->E > kMaxExperts || c->k < 1 || c->k > kMaxTopK || c->k > c->E) return false;
   if (static_cast<int64_t>(c->T) * c->k >= (int64_t{1} << 31)) return false;
-  if (c->precision != MOE_PREC_BF16 && c->precision != MOE_PREC_FP8_BWD) return false;
+  if (c->precision != MOE_PREC_BF16 && c->precision != MOE_PREC_FP8_BWD &&
+      c->precision != MOE_PREC_MXFP8)
+    return false;
   // MXFP8 GEMMs stage K in 128-byte blocks and keep scale atoms of 128 rows
-  if (c->precision == MOE_PREC_FP8_BWD && (c->H % 128 || c->I % 128)) return false;
+  if (c->precision != MOE_PREC_BF16 && (c->H % 128 || c->I % 128)) return false;
   return true;
 }
 
@@ -93,7 +97,27 @@ Layout layout_of(const moe_config *c) {
   L.s_Aw = o;
   o += align256(M * I * 2);
   L.s_total = o > 0 ? o : 256;
-  L.f_total = kHeader;
+  o = kHeader;
+  if (c->precision == MOE_PREC_MXFP8) {
+    const size_t Mp = fp8_mpad(M, E);
+    moe_mxfp8_fwd_layout &f = L.fq;
+    auto take = [&o](size_t bytes) {
+      const size_t at = o;
+      o += align256(bytes);
+      return at;
+    };
+    f.m_pad = Mp;
+    f.pad_offsets = take((E + 1) * 4);
+    f.x_q = take(Mp * H);
+    f.x_sf = take(Mp * H / 32);
+    f.a_q = take(Mp * I);
+    f.a_sf = take(Mp * I / 32);
+    f.wgu_q = take(E * 2 * I * H);
+    f.wgu_sf = take(sf_layout_bytes(E * 2 * I, H, sf_b(2 * I)));
+    f.wdt_q = take(E * H * I);
+    f.wdt_sf = take(sf_layout_bytes(E * H, I, sf_b(H)));
+  }
+  L.f_total = o;
   o = kHeader;
   L.b_dyp = o;
   o += align256(M * H * 2);
@@ -107,7 +131,7 @@ Layout layout_of(const moe_config *c) {
   o += align256(M * H * 2);
   L.b_maps = o;
   o += align256(E * kExpertMapBytes);
-  if (c->precision == MOE_PREC_FP8_BWD) {
+  if (c->precision != MOE_PREC_BF16) {
     const size_t Mp = fp8_mpad(M, E);
     moe_fp8_layout &q = L.q;
     q.m_pad = Mp;
@@ -343,6 +367,74 @@ moe_status backward_fp8(const Fp8Bwd &f, cudaStream_t s) {
   return MOE_OK;
 }
 
+// The mxfp8 forward after the permute: both grouped GEMMs in MXFP8.  x_perm
+// along H into the padded row space; the weights along their middle axis,
+// transposed (W_gate | W_up interleaved by 32 columns, so one 192-row B tile
+// holds 96 gate and the same 96 up columns); GEMM1's epilogue writes the bf16
+// activations and A quantised along I; GEMM2 writes Y.
+struct Mx8Fwd {
+  const moe_config *cfg;
+  const moe_routing *r;
+  const moe_mxfp8_fwd_layout *q;
+  uint8_t *sc;
+  int sms;
+  int32_t *status;
+  const uint16_t *x_perm, *W_gate, *W_up, *W_down;
+  uint16_t *A, *G, *U, *A_w, *Y;
+};
+
+moe_status forward_mx(const Mx8Fwd &f, cudaStream_t s) {
+  const int T = f.cfg->T, H = f.cfg->H, I = f.cfg->I, E = f.cfg->E, k = f.cfg->k;
+  const int Mp = static_cast<int>(f.q->m_pad);
+  const moe_mxfp8_fwd_layout &q = *f.q;
+  uint8_t *sc = f.sc;
+  int32_t *pad_off = reinterpret_cast<int32_t *>(sc + q.pad_offsets);
+  const int32_t *off = f.r->offsets;
+  MOE_TRY(timed("mx_pad_offsets_fwd", s, [&] { return launch_pad_offsets(off, E, pad_off, s); }));
+  MOE_TRY(timed("mx_quant_x", s, [&] {
+    return launch_quant_rows(f.x_perm, Mp, H, off, pad_off, E, sc + q.x_q, sc + q.x_sf, sf_a(Mp), s);
+  }));
+  MOE_TRY(timed("mx_quant_W_gateup_fwd", s, [&] {
+    const cudaError_t e = launch_quant_wT(f.W_gate, E, H, I, 1, 0, sc + q.wgu_q, sc + q.wgu_sf, sf_b(2 * I), s);
+    if (e != cudaSuccess) return e;
+    return launch_quant_wT(f.W_up, E, H, I, 1, 1, sc + q.wgu_q, sc + q.wgu_sf, sf_b(2 * I), s);
+  }));
+  MxGemmArgs m{};
+  m.H = H;
+  m.I = I;
+  m.E = E;
+  m.Mpad = Mp;
+  m.M = T * k;
+  m.offsets = off;
+  m.pad_off = pad_off;
+  m.w_row = f.r->w_row;
+  m.status = f.status;
+  m.num_sms = f.sms;
+  m.a0 = sc + q.x_q;
+  m.sfa0 = sc + q.x_sf;
+  m.b0 = sc + q.wgu_q;
+  m.sfb0 = sc + q.wgu_sf;
+  m.o0 = f.A;
+  m.o1 = f.G;
+  m.o2 = f.U;
+  m.o3 = f.A_w;
+  m.aq = sc + q.a_q;
+  m.aq_sf = sc + q.a_sf;
+  MOE_TRY(timed("mx_gemm_gateup_swiglu", s, [&] { return launch_mx_gemm(kMxGemmGateUp, m, s); }));
+  MOE_TRY(timed("mx_quant_W_down_fwd", s, [&] {
+    return launch_quant_wT(f.W_down, E, I, H, 0, 0, sc + q.wdt_q, sc + q.wdt_sf, sf_b(H), s);
+  }));
+  m.a0 = sc + q.a_q;
+  m.sfa0 = sc + q.a_sf;
+  m.b0 = sc + q.wdt_q;
+  m.sfb0 = sc + q.wdt_sf;
+  m.o0 = f.Y;
+  m.o1 = m.o2 = m.o3 = nullptr;
+  m.aq = m.aq_sf = nullptr;
+  MOE_TRY(timed("mx_gemm_down", s, [&] { return launch_mx_gemm(kMxGemmDown, m, s); }));
+  return MOE_OK;
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -373,8 +465,14 @@ moe_status moe_saved_offsets(const moe_config *cfg, moe_saved_layout *out) {
   return MOE_OK;
 }
 
+moe_status moe_mxfp8_forward_offsets(const moe_config *cfg, moe_mxfp8_fwd_layout *out) {
+  if (!shape_ok(cfg) || !out || cfg->precision != MOE_PREC_MXFP8) return MOE_ERR_INVALID_ARG;
+  *out = layout_of(cfg).fq;
+  return MOE_OK;
+}
+
 moe_status moe_fp8_scratch_offsets(const moe_config *cfg, moe_fp8_layout *out) {
-  if (!shape_ok(cfg) || !out || cfg->precision != MOE_PREC_FP8_BWD) return MOE_ERR_INVALID_ARG;
+  if (!shape_ok(cfg) || !out || cfg->precision == MOE_PREC_BF16) return MOE_ERR_INVALID_ARG;
   *out = layout_of(cfg).q;
   return MOE_OK;
 }
@@ -453,21 +551,41 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const moe_routing *
     return launch_permute_rows(static_cast<const uint16_t *>(x), r->row_of_slot, x_perm, T, H, k,
                                s);
   }));
-  GemmArgs g = gemm_base(cfg, r, di.sms, status);
-  g.x_perm = x_perm;
-  g.W_gate = static_cast<const uint16_t *>(W_gate);
-  g.W_up = static_cast<const uint16_t *>(W_up);
-  g.W_down = static_cast<const uint16_t *>(W_down);
-  g.w_row = r->w_row;
-  g.o0 = A;
-  g.o1 = G;
-  g.o2 = U;
-  g.o3 = A_w;
-  MOE_TRY(timed(gemm_mode_name(kFwdGateUp), s, [&] { return launch_grouped_gemm(kFwdGateUp, g, s); }));
-  g.act = A;
-  g.o0 = Y;
-  g.o1 = g.o2 = g.o3 = nullptr;
-  MOE_TRY(timed(gemm_mode_name(kFwdDown), s, [&] { return launch_grouped_gemm(kFwdDown, g, s); }));
+  if (cfg->precision == MOE_PREC_MXFP8) {
+    Mx8Fwd f;
+    f.cfg = cfg;
+    f.r = r;
+    f.q = &L.fq;
+    f.sc = sc;
+    f.sms = di.sms;
+    f.status = status;
+    f.x_perm = x_perm;
+    f.W_gate = static_cast<const uint16_t *>(W_gate);
+    f.W_up = static_cast<const uint16_t *>(W_up);
+    f.W_down = static_cast<const uint16_t *>(W_down);
+    f.A = A;
+    f.G = G;
+    f.U = U;
+    f.A_w = A_w;
+    f.Y = Y;
+    MOE_TRY(forward_mx(f, s));
+  } else {
+    GemmArgs g = gemm_base(cfg, r, di.sms, status);
+    g.x_perm = x_perm;
+    g.W_gate = static_cast<const uint16_t *>(W_gate);
+    g.W_up = static_cast<const uint16_t *>(W_up);
+    g.W_down = static_cast<const uint16_t *>(W_down);
+    g.w_row = r->w_row;
+    g.o0 = A;
+    g.o1 = G;
+    g.o2 = U;
+    g.o3 = A_w;
+    MOE_TRY(timed(gemm_mode_name(kFwdGateUp), s, [&] { return launch_grouped_gemm(kFwdGateUp, g, s); }));
+    g.act = A;
+    g.o0 = Y;
+    g.o1 = g.o2 = g.o3 = nullptr;
+    MOE_TRY(timed(gemm_mode_name(kFwdDown), s, [&] { return launch_grouped_gemm(kFwdDown, g, s); }));
+  }
   MOE_TRY(timed("combine", s, [&] {
     return launch_gather_sum(Y, r->row_of_slot, r->topk_w, static_cast<uint16_t *>(out), T, H, k,
                              s);
@@ -522,7 +640,7 @@ moe_status moe_backward(const moe_config *cfg, const void *dy, const void *x,
     return launch_router_bwd(static_cast<const uint16_t *>(dy), Y, r->row_of_slot, r->topk_idx,
                              r->topk_w, dy_perm, d_logits, d_topk_w, T, H, E, k, s);
   }));
-  if (cfg->precision == MOE_PREC_FP8_BWD) {
+  if (cfg->precision != MOE_PREC_BF16) {
     Fp8Bwd f;
     f.cfg = cfg;
     f.r = r;

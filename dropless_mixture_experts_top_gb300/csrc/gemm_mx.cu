@@ -14,6 +14,11 @@
 // transposed through the warp's staging tile), from the bf16-rounded values a
 // bf16 tensor would hold; dG and dU never exist in bf16.
 //
+// The mxfp8 mode adds the two forward GEMMs: gate|up (its B rows interleave
+// 32 columns of W_gate and the same 32 of W_up, so a 192-row tile yields 96
+// output columns and the epilogue computes SwiGLU, writes the bf16 A, G, U,
+// A_w and quantises A along I for the down GEMM), and down (plain bf16 Y).
+//
 // One CTA per SM, persistent, static round-robin over 128 x 192 tiles:
 //   warp 0      producer: TMA boxes of codes (128-byte swizzle) and bulk copies
 //               of the scale atoms into a 5-stage ring (4 for dA)
@@ -42,16 +47,17 @@ constexpr int BKB = 128;             // K per stage in elements (= bytes): one 1
 // 5-stage ring; 3 for dA, whose shared memory also holds 8 staging tiles and a
 // 4-slot G/U ring (two slots per column half, so a half's next chunk lands
 // while it works on the current one)
-__host__ __device__ constexpr int stages_of(int mode) { return mode == 0 ? 3 : 5; }
+__host__ __device__ constexpr int stages_of(int mode) { return mode == 0 ? 3 : mode == 4 ? 4 : 5; }
 constexpr int kMxGuSlots = 4;
 constexpr int kABytes = BM * BKB;    // 16 KB
 constexpr int kBBytes = BN * BKB;    // 24 KB
 constexpr int kSfBytes = 512 * 3;    // A atom + two B atoms
 constexpr int kStageBytes = kABytes + kBBytes;  // 40 KB: keeps every stage 1024-byte aligned
 // Warps: producer, MMA issuer, then 4 epilogue warps (one per TMEM lane
-// quarter), or for dA 8 (dSwiGLU epilogue; two warps per quarter) and a
-// loader warp that streams G and U into a shared-memory ring ahead of them.
-__host__ __device__ constexpr int epi_warps(int mode) { return mode == 0 ? 8 : 4; }
+// quarter), or 8 (two per quarter) for the epilogue-heavy dA (dSwiGLU, and a
+// loader warp that streams G and U into a shared-memory ring ahead of them)
+// and gate|up (SwiGLU, four bf16 outputs and A's quantisation; 4 stages).
+__host__ __device__ constexpr int epi_warps(int mode) { return (mode == 0 || mode == 4) ? 8 : 4; }
 __host__ __device__ constexpr int gu_warps(int mode) { return mode == 0 ? 1 : 0; }
 __host__ __device__ constexpr int threads_of(int mode) {
   return 64 + 32 * (epi_warps(mode) + gu_warps(mode));
@@ -70,11 +76,12 @@ __host__ __device__ constexpr int gu_off(int mode) {
 __host__ __device__ constexpr int smem_bytes(int mode) {
   return gu_off(mode) + gu_warps(mode) * kMxGuSlots * kGuChunkBytes + 1024;
 }
-static_assert(smem_bytes(0) <= 227 * 1024 && smem_bytes(1) <= 227 * 1024, "shared memory budget");
+static_assert(smem_bytes(0) <= 227 * 1024 && smem_bytes(1) <= 227 * 1024 && smem_bytes(4) <= 227 * 1024,
+              "shared memory budget");
 static_assert(kSfCol + 5 * kSfSlotCols <= kTmemCols, "TMEM budget");
 
-enum MxMode : int { kMxDA = 0, kMxDX = 1, kMxDWDown = 2, kMxDWGateUp = 3 };
-static_assert(kMxDA == 0, "epi_warps");
+enum MxMode : int { kMxDA = 0, kMxDX = 1, kMxDWDown = 2, kMxDWGateUp = 3, kMxGateUp = 4, kMxDown = 5 };
+static_assert(kMxDA == 0 && kMxGateUp == 4, "stages_of, epi_warps");
 
 struct MxParams {
   int H, I, E;
@@ -84,7 +91,8 @@ struct MxParams {
   const uint8_t *sfa0, *sfa1, *sfb0, *sfb1;  // scale atoms of the operands
   const uint16_t *G, *U;
   const float *w_row;
-  uint16_t *o0, *o1;
+  uint16_t *o0, *o1, *o2, *o3;
+  uint8_t *aq, *aq_sf;  // gate|up: A quantised along I
   uint8_t *dg_q, *du_q, *dg_sf, *du_sf, *dg_t, *du_t, *dg_t_sf, *du_t_sf;  // dA's quantised outputs
   int32_t *status;
   int n_tiles, m_tiles;
@@ -104,8 +112,15 @@ template <int MODE>
 struct MxTraits {
   static constexpr bool kRaggedK = (MODE == kMxDWDown || MODE == kMxDWGateUp);
   // dW_gate and dW_up tiles use the dW_down epilogue on a transposed view
-  // (dA has its own epilogue, epilogue_da_mx)
-  static constexpr int kEpi = MODE == kMxDX ? kBwdDX : kBwdDWDown;
+  // (dA and gate|up have their own epilogues; down stores Y like dX stores dX)
+  static constexpr int kEpi = (MODE == kMxDX || MODE == kMxDown) ? kBwdDX : kBwdDWDown;
+  // ragged M: the reduction length and the B rows of one expert
+  __host__ __device__ static int kdim(const MxParams &p) {
+    return MODE == kMxDX ? 2 * p.I : MODE == kMxDown ? p.I : p.H;
+  }
+  __host__ __device__ static int brows(const MxParams &p) {
+    return MODE == kMxDA ? p.I : MODE == kMxGateUp ? 2 * p.I : p.H;
+  }
 };
 
 // Block-scaled instruction descriptor: E4M3 x E4M3, fp32 D, UE8M0 scales,
@@ -178,7 +193,7 @@ __device__ __forceinline__ MxTile decode_mx(int tile, const MxParams &p, const i
     t.m0 = s_off[lo] + (prow - s_pad[lo]);
     t.row_end = s_off[lo + 1];
     t.n0 = nt * BN;
-    t.nkb = (MODE == kMxDA ? p.H : 2 * p.I) / BKB;
+    t.nkb = MxTraits<MODE>::kdim(p) / BKB;
     t.krow0 = 0;
     t.kcount = 0;
     x.arow = prow;
@@ -317,6 +332,54 @@ __device__ __forceinline__ bool epilogue_da_mx(const MxTile &x, uint32_t tb, int
   return ok;
 }
 
+// The mxfp8 gate|up epilogue: accumulator columns [gate 32 | up 32] x 3 are
+// the output columns n0/2 + 32 j (pair j); SwiGLU as in the bf16 engine (A, G,
+// U and A_w = w A in bf16, rows past the expert's count not stored), and A
+// quantised along I into the padded row space for the down GEMM, from the
+// bf16 value A holds (zero in the padded rows past the count).
+template <int NCH>
+__device__ __forceinline__ void epilogue_gateup_mx(const MxTile &x, uint32_t tb, int rit, const MxParams &p,
+                                                   int part, uint8_t *tile) {
+  const Tile &t = x.t;
+  const int lane = threadIdx.x & 31;
+  const int row = t.m0 + rit, row0 = row - lane;
+  const bool valid = row < t.row_end;
+  const int nvalid = clamp_rows(t.row_end - row0);
+  const int prow = x.arow + rit;
+  const float w = valid ? __ldg(p.w_row + row) : 0.f;
+  const int ocol0 = t.n0 / 2;
+  const int npair = min(NCH / 2, (p.I - ocol0) / 32);
+  const int wi = prow & 127;  // A's scale byte (along I: 128-row atoms of the padded rows, K = I)
+  const size_t sfi_base = static_cast<size_t>(prow >> 7) * (p.I >> 7) * 512 + (wi & 31) * 16 + (wi >> 5) * 4;
+  uint32_t r0[32], r1[32];
+  float v0[32], v1[32], v2[32];
+  for (int j = part; j < npair; j += 2) {
+    tmem_ld32(tb + 64 * j, r0);
+    tmem_ld32(tb + 64 * j + 32, r1);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float g = __uint_as_float(r0[i]), u = __uint_as_float(r1[i]);
+      v0[i] = g * sigmoidf_(g) * u;  // SwiGLU
+      v1[i] = g;
+      v2[i] = u;
+    }
+    const int col = ocol0 + 32 * j;
+    const size_t off = static_cast<size_t>(row0) * p.I + col;
+    store_rows32(tile, p.o0 + off, p.I, nvalid, v0);
+    store_rows32(tile, p.o1 + off, p.I, nvalid, v1);
+    store_rows32(tile, p.o2 + off, p.I, nvalid, v2);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v1[i] = valid ? round_bf16(v0[i]) : 0.f;
+    const int kb = col >> 5;
+    p.aq_sf[sfi_base + (kb >> 2) * 512 + (kb & 3)] =
+        quant32(v1, reinterpret_cast<uint4 *>(p.aq + static_cast<size_t>(prow) * p.I + col));
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v0[i] *= w;  // A_w = w * A, the dW_down operand
+    store_rows32(tile, p.o3 + off, p.I, nvalid, v0);
+  }
+}
+
 // One stage: A codes (128 rows), B codes (192 rows), the A scale atom and the
 // two B scale atoms of K block kb.
 template <int MODE>
@@ -328,11 +391,14 @@ __device__ __forceinline__ void produce_mx(const MxTile &x, int kb, uint8_t *st,
   uint8_t *sa = st, *sb = st + kABytes;
   const uint8_t *sfa, *sfb;
   int K, k;
-  if constexpr (MODE == kMxDA) {  // A = dy (padded rows, K = H); B = W_down rows e*I + n
-    K = p.H;
+  if constexpr (MODE == kMxDA || MODE == kMxGateUp || MODE == kMxDown) {
+    // dA: A = dy (padded rows, K = H), B = W_down rows e*I + n;  gate|up: A = x
+    // (K = H), B = interleaved gate|up rows e*2I + n;  down: A = A (K = I), B =
+    // W_down^T rows e*H + n
+    K = MxTraits<MODE>::kdim(p);
     k = kb;
     tma_load_2d(sa, a0, bar, k * BKB, x.arow);
-    tma_load_2d(sb, b0, bar, k * BKB, t.e * p.I + t.n0);
+    tma_load_2d(sb, b0, bar, k * BKB, t.e * MxTraits<MODE>::brows(p) + t.n0);
     sfa = p.sfa0;
     sfb = p.sfb0;
   } else if constexpr (MODE == kMxDX) {  // A = [dG | dU] (padded rows, K = I each); B = W_gate | W_up
@@ -559,6 +625,8 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
         if (!epilogue_da_mx<BN / 32>(x, tb, rit, p, part, stile, gu_ring, gu_full, gu_empty, gbase,
                                      abort_flag))
           break;
+      } else if constexpr (MODE == kMxGateUp) {
+        epilogue_gateup_mx<BN / 32>(x, tb, rit, p, part, stile);
       } else {
         epilogue_tile<MxTraits<MODE>::kEpi, EpiView, BN / 32>(x.t, tb, rit, v, part,
                                                               epi_warps(MODE) / 4, stile);
@@ -662,6 +730,10 @@ cudaError_t launch_mx_mode(const MxGemmArgs &a, cudaStream_t s) {
   p.w_row = a.w_row;
   p.o0 = a.o0;
   p.o1 = a.o1;
+  p.o2 = a.o2;
+  p.o3 = a.o3;
+  p.aq = a.aq;
+  p.aq_sf = a.aq_sf;
   p.dg_q = a.dg_q;
   p.du_q = a.du_q;
   p.dg_sf = a.dg_sf;
@@ -693,6 +765,18 @@ cudaError_t launch_mx_mode(const MxGemmArgs &a, cudaStream_t s) {
       mA1 = mA0;
       mB1 = mB0;
       p.m_tiles = a.I / BM;
+      p.n_tiles = p.b_gps = cdiv(a.H, BN);
+      break;
+    case kMxGateUp:  // [Mp, H] x [E*2I, H]^T (gate|up rows interleaved by 32)
+      ok = make_map_u8(&mA0, a.a0, H, Mp, BM) && make_map_u8(&mB0, a.b0, H, E * 2 * I, BN);
+      mA1 = mA0;
+      mB1 = mB0;
+      p.n_tiles = p.b_gps = cdiv(2 * a.I, BN);
+      break;
+    case kMxDown:  // [Mp, I] x [E*H, I]^T
+      ok = make_map_u8(&mA0, a.a0, I, Mp, BM) && make_map_u8(&mB0, a.b0, I, E * H, BN);
+      mA1 = mA0;
+      mB1 = mB0;
       p.n_tiles = p.b_gps = cdiv(a.H, BN);
       break;
     default:  // kMxDWGateUp, per expert: [H, tokens] x [I, tokens]^T for dG and for dU
@@ -727,6 +811,8 @@ cudaError_t launch_mx_gemm(int mode, const MxGemmArgs &a, cudaStream_t s) {
     case kMxGemmDX: return launch_mx_mode<kMxDX>(a, s);
     case kMxGemmDWDown: return launch_mx_mode<kMxDWDown>(a, s);
     case kMxGemmDWGateUp: return launch_mx_mode<kMxDWGateUp>(a, s);
+    case kMxGemmGateUp: return launch_mx_mode<kMxGateUp>(a, s);
+    case kMxGemmDown: return launch_mx_mode<kMxDown>(a, s);
   }
   return cudaErrorInvalidValue;
 }

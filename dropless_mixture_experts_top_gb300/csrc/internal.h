@@ -123,7 +123,21 @@ cudaError_t launch_quant_cols(const uint16_t *src, int C, int Mpad, const int32_
                               const int32_t *pad_off, int E, uint8_t *codes, uint8_t *sf, SfLayout L,
                               RowCodes rows, cudaStream_t s);
 
-enum MxGemmMode : int { kMxGemmDA = 0, kMxGemmDX = 1, kMxGemmDWDown = 2, kMxGemmDWGateUp = 3 };
+// Weights [E, R, C] quantised along R (R % 128 == 0, C % 64 == 0), transposed:
+// codes [E * C, R] (interleave 0) or the gate|up interleave of the mxfp8 GEMM1
+// (interleave 1, codes [E * 2C, R]: row e*2C + (c/32)*64 + half*32 + c%32).
+cudaError_t launch_quant_wT(const uint16_t *W, int E, int R, int C, int interleave, int half,
+                            uint8_t *codes, uint8_t *sf, SfLayout L, cudaStream_t s);
+
+// MXFP8 grouped GEMMs: the fp8_bwd backward's four, and the mxfp8 forward's two
+enum MxGemmMode : int {
+  kMxGemmDA = 0,
+  kMxGemmDX = 1,
+  kMxGemmDWDown = 2,
+  kMxGemmDWGateUp = 3,
+  kMxGemmGateUp = 4,  // Q(x) . Q(W_gate | W_up)^T (interleaved B rows) -> SwiGLU: A, G, U, A_w, Q(A)
+  kMxGemmDown = 5     // Q(A) . Q(W_down)^T -> Y
+};
 struct MxGemmArgs {
   int H, I, E, Mpad;
   int M;  // permuted rows T*k (rows of G and U)
@@ -132,7 +146,9 @@ struct MxGemmArgs {
   const uint8_t *sfa0, *sfa1, *sfb0, *sfb1;  // scale atoms
   const uint16_t *G, *U;
   const float *w_row;
-  uint16_t *o0, *o1;
+  uint16_t *o0, *o1, *o2, *o3;
+  // mxfp8 GEMM1: A quantised along I for the down GEMM (codes [Mpad, I], 128-row atoms)
+  uint8_t *aq, *aq_sf;
   // dA: its epilogue quantises dG and dU for the next two GEMMs -- along I
   // (codes [Mpad, I], 128-row scale atoms: dX's A operand) and along tokens
   // (codes [I, Mpad], 192-row scale groups: dW_gate/up's B operand)

@@ -197,6 +197,57 @@ __global__ void __launch_bounds__(kQcThreads, 3) quant_cols_kernel(const uint16_
   }
 }
 
+// Weights quantised along their middle axis (the mxfp8 forward GEMMs' K),
+// written transposed: W [E, R, C] bf16 (R the reduction axis, R % 128 == 0)
+// -> codes [rows, R] with output row (e, c) = e * C + c (W_down: the down
+// GEMM's B rows), or, interleaved for gate|up tiles, e * 2C + (c / 32) * 64 +
+// half * 32 + c % 32 (W_gate half 0, W_up half 1: every 64 B rows hold 32
+// gate columns then the same 32 up columns).  Same staging as the token-axis
+// quantiser: 128 x 64 tiles, one thread per (column, 32-row block), codes
+// leaving through a shared output tile as 128-byte rows.
+__global__ void __launch_bounds__(kQcThreads, 3) quant_wT_kernel(const uint16_t *__restrict__ src, int R,
+                                                                 int C, int interleave, int half,
+                                                                 uint8_t *__restrict__ codes,
+                                                                 uint8_t *__restrict__ sf, SfLayout L) {
+  __shared__ __align__(16) uint16_t tile[kQcRows * kQcCols];
+  constexpr int kOutStride = kQcRows + 16;
+  __shared__ __align__(16) uint8_t otile[kQcCols * kOutStride];
+  const int grow0 = blockIdx.x * kQcRows;  // first source row (of E * R)
+  const int e = grow0 / R, r0 = grow0 - e * R;
+  auto out_row = [&](int c) {
+    return interleave ? e * 2 * C + (c >> 5) * 64 + half * 32 + (c & 31) : e * C + c;
+  };
+  for (int c0 = blockIdx.y * kQcCols; c0 < C; c0 += gridDim.y * kQcCols) {
+#pragma unroll
+    for (int j = 0; j < (kQcRows * kQcCols / 8) / kQcThreads; ++j) {
+      const int i = threadIdx.x + j * kQcThreads;
+      const int r = i >> 3, part = i & 7;
+      const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src + static_cast<size_t>(grow0 + r) * C + c0) + part);
+      *reinterpret_cast<uint4 *>(tile + r * kQcCols + ((part ^ (r & 7)) << 3)) = v;
+    }
+    __syncthreads();
+    const int cc = threadIdx.x % kQcCols, b = threadIdx.x / kQcCols;  // 4 blocks of 32 rows
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int r = 32 * b + i;
+      v[i] = __uint_as_float(static_cast<uint32_t>(tile[r * kQcCols + (((cc >> 3) ^ (r & 7)) << 3) + (cc & 7)])
+                             << 16);
+    }
+    sf[atom_byte(out_row(c0 + cc), (r0 >> 5) + b, R, L)] =
+        quant32(v, reinterpret_cast<uint4 *>(otile + cc * kOutStride + 32 * b));
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < (kQcCols * kQcRows / 16) / kQcThreads; ++j) {
+      const int i = threadIdx.x + j * kQcThreads;
+      const int r = i >> 3, part = i & 7;  // output row (column c0 + r), 16-byte piece
+      *reinterpret_cast<uint4 *>(codes + static_cast<size_t>(out_row(c0 + r)) * R + r0 + part * 16) =
+          *reinterpret_cast<const uint4 *>(otile + r * kOutStride + part * 16);
+    }
+    __syncthreads();
+  }
+}
+
 // pad_off[e] = sum over e' < e of ceil(count/128)*128; pad_off[E] = padded total.
 __global__ void __launch_bounds__(32) pad_offsets_kernel(const int32_t *__restrict__ offsets, int E,
                                                          int32_t *__restrict__ pad_off) {
@@ -239,6 +290,14 @@ cudaError_t launch_quant_cols(const uint16_t *src, int C, int Mpad, const int32_
   const int col_blocks = C / kQcCols < 4 ? C / kQcCols : 4;  // each loops over C / (64 * 4) column tiles
   const dim3 grid(static_cast<unsigned>(Mpad / kQcRows), static_cast<unsigned>(col_blocks));
   quant_cols_kernel<<<grid, kQcThreads, 0, s>>>(src, C, Mpad, offsets, pad_off, E, codes, sf, L, rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_wT(const uint16_t *W, int E, int R, int C, int interleave, int half,
+                            uint8_t *codes, uint8_t *sf, SfLayout L, cudaStream_t s) {
+  const int col_blocks = C / kQcCols < 4 ? C / kQcCols : 4;
+  const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(E) * R / kQcRows), static_cast<unsigned>(col_blocks));
+  quant_wT_kernel<<<grid, kQcThreads, 0, s>>>(W, R, C, interleave, half, codes, sf, L);
   return cudaGetLastError();
 }
 

@@ -18,14 +18,15 @@ import torch
 from . import _build
 
 MOE_OK = 0
-PRECISIONS = {"bf16": 0, "fp8_bwd": 1}
+PRECISIONS = {"bf16": 0, "fp8_bwd": 1, "mxfp8": 2}
 DEV_NONFINITE_LOGIT = 0x1
 DEV_WAIT_TIMEOUT = 0x2
 
 _lib = None
 
 EXPORTED = [
-    "moe_query_workspace", "moe_saved_offsets", "moe_fp8_scratch_offsets", "moe_route",
+    "moe_query_workspace", "moe_saved_offsets", "moe_fp8_scratch_offsets", "moe_mxfp8_forward_offsets",
+    "moe_route",
     "moe_route_static_scratch", "moe_forward", "moe_backward", "moe_get_device_status",
     "moe_status_string", "moe_timing_attach", "moe_timing_count", "moe_timing_label",
     "moe_selftest_wait_timeout", "moe_router_workspace", "moe_router_forward", "moe_router_backward",
@@ -53,6 +54,11 @@ class Fp8Layout(ctypes.Structure):
         "dg_t", "dg_t_sf", "du_t", "du_t_sf")]
 
 
+class Mx8FwdLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in (
+        "m_pad", "pad_offsets", "x_q", "x_sf", "a_q", "a_sf", "wgu_q", "wgu_sf", "wdt_q", "wdt_sf")]
+
+
 class MoEError(RuntimeError):
     def __init__(self, what, code):
         super().__init__(f"{what}: {status_string(code)} ({code})")
@@ -75,6 +81,7 @@ def lib():
         L.moe_query_workspace.argtypes = [P, P, P, P, P]
         L.moe_saved_offsets.argtypes = [P, P]
         L.moe_fp8_scratch_offsets.argtypes = [P, P]
+        L.moe_mxfp8_forward_offsets.argtypes = [P, P]
         L.moe_route.argtypes = [P, P, P, P, sz, P]
         L.moe_forward.argtypes = [P, P, P, P, P, P, P, P, sz, P, sz, P]
         L.moe_backward.argtypes = [P, P, P, P, P, P, P, P, sz, P, P, P, P, P, P, P, sz, P]
@@ -93,7 +100,8 @@ def lib():
         L.moe_timing_count.restype = ctypes.c_int32
         L.moe_timing_label.argtypes = [ctypes.c_int32]
         L.moe_timing_label.restype = ctypes.c_char_p
-        for f in ("moe_query_workspace", "moe_saved_offsets", "moe_fp8_scratch_offsets", "moe_route", "moe_forward", "moe_backward",
+        for f in ("moe_query_workspace", "moe_saved_offsets", "moe_fp8_scratch_offsets",
+                  "moe_mxfp8_forward_offsets", "moe_route", "moe_forward", "moe_backward",
                   "moe_get_device_status", "moe_timing_attach"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
@@ -144,6 +152,13 @@ def fp8_scratch_offsets(cfg: Config) -> dict:
     return {n: int(getattr(lay, n)) for n, _ in Fp8Layout._fields_}
 
 
+def mxfp8_forward_offsets(cfg: Config) -> dict:
+    lay = Mx8FwdLayout()
+    _check(lib().moe_mxfp8_forward_offsets(ctypes.byref(cfg), ctypes.byref(lay)),
+           "moe_mxfp8_forward_offsets")
+    return {n: int(getattr(lay, n)) for n, _ in Mx8FwdLayout._fields_}
+
+
 MX_BN = 192  # N extent of an MXFP8 GEMM tile: B-operand scales are grouped by it
 
 
@@ -157,7 +172,12 @@ def sf_grouping(base: str, shape, m_pad: int):
         return shape.H, MX_BN
     if base in ("dg_t", "du_t"):
         return shape.I, MX_BN
-    rows = {"dy_q": m_pad, "dg_q": m_pad, "du_q": m_pad, "aw_t": shape.I, "x_t": shape.H}[base]
+    if base == "wgu_q":
+        return 2 * shape.I, MX_BN
+    if base == "wdt_q":
+        return shape.H, MX_BN
+    rows = {"dy_q": m_pad, "dg_q": m_pad, "du_q": m_pad, "aw_t": shape.I, "x_t": shape.H,
+            "x_q": m_pad, "a_q": m_pad}[base]
     return rows, 128
 
 
@@ -333,6 +353,25 @@ class MoELayer:
             return self.bwd_scratch[off:off + sf_layout_bytes(R, K, seg, group)]
         R, K = rows_k[name]
         return self.bwd_scratch[off:off + R * K].view(R, K)
+
+    def fwd_fp8_tensor(self, name):
+        """A quantised operand of the mxfp8 forward left in the forward scratch:
+        uint8 codes [rows, K] for *_q, raw scale-atom bytes for *_sf, int32 [E+1]
+        for pad_offsets."""
+        lay = mxfp8_forward_offsets(self.cfg)
+        s = self.shape
+        Mp = lay["m_pad"]
+        rows_k = {"x_q": (Mp, s.H), "a_q": (Mp, s.I), "wgu_q": (s.E * 2 * s.I, s.H), "wdt_q": (s.E * s.H, s.I)}
+        off = lay[name]
+        if name == "pad_offsets":
+            return self.fwd_scratch[off:off + 4 * (s.E + 1)].view(torch.int32)
+        if name.endswith("_sf"):
+            base = name[:-3] + "_q"
+            R, K = rows_k[base]
+            seg, group = sf_grouping(base, s, Mp)
+            return self.fwd_scratch[off:off + sf_layout_bytes(R, K, seg, group)]
+        R, K = rows_k[name]
+        return self.fwd_scratch[off:off + R * K].view(R, K)
 
     def route(self, logits, stream=None):
         route(self.cfg, logits, self.routing, self.route_scratch, stream)

@@ -64,7 +64,7 @@ class Workload:
     shape: MoEShape
     seed_index: int          # selects the seed family (x 1000+c, logits 2000+c, ...)
     routing: str             # "uniform" or "zipf"
-    precision: str           # "bf16" or "fp8_bwd"
+    precision: str           # "bf16", "fp8_bwd" or "mxfp8"
     description: str
 
 
@@ -85,6 +85,8 @@ WORKLOADS: dict[str, Workload] = {
                  "Qwen3-235B-A22B-shaped layer, T=16384 H=4096 I=1536 E=128 top-8, uniform routing"),
         Workload("qwen3_30b_a3b_layer_t16384_fp8_bwd", _Q30, 2, "uniform", "fp8_bwd",
                  "30B shape, BF16 forward, MXFP8 backward grouped GEMMs (same inputs as the uniform 30B case)"),
+        Workload("qwen3_30b_a3b_layer_t16384_mxfp8", _Q30, 2, "uniform", "mxfp8",
+                 "30B shape, forward and backward grouped GEMMs in MXFP8 (same inputs as the uniform 30B case)"),
     ]
 }
 

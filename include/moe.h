@@ -33,8 +33,8 @@
  *     IEEE bfloat16 bit patterns.
  *   - Every device pointer must be 16-byte aligned.
  *   - Shapes: T >= 0, H % 64 == 0 and I % 64 == 0 (both >= 64), 1 <= E <= 256,
- *     1 <= k <= min(E, 16), T * k < 2^31; with MOE_PREC_FP8_BWD also
- *     H % 128 == 0 and I % 128 == 0.
+ *     1 <= k <= min(E, 16), T * k < 2^31; with MOE_PREC_FP8_BWD or
+ *     MOE_PREC_MXFP8 also H % 128 == 0 and I % 128 == 0.
  *   - Errors found on the host (null pointer, bad shape, misalignment, a
  *     too-small workspace) return a negative moe_status with nothing launched.
  *     Anomalies found on the device (non-finite logits, a pipeline wait that
@@ -65,8 +65,12 @@ typedef enum {
 
 typedef enum {
   MOE_PREC_BF16 = 0,    /* bf16 operands, fp32 accumulation, everywhere */
-  MOE_PREC_FP8_BWD = 1  /* bf16 forward; backward grouped GEMMs in MXFP8 (E4M3 values,
+  MOE_PREC_FP8_BWD = 1, /* bf16 forward; backward grouped GEMMs in MXFP8 (E4M3 values,
                            one UE8M0 scale per 32 elements along each GEMM's K) */
+  MOE_PREC_MXFP8 = 2    /* the forward grouped GEMMs in MXFP8 too ("mxfp8" in the Prime
+                           Mega MoE write-ups' precision switch): x and W_gate/W_up
+                           along H, A (as bf16) and W_down along I; the activations the
+                           forward saves stay bf16; the backward is fp8_bwd's */
 } moe_precision;
 
 /* Device status flags (moe_get_device_status *host_code). */
@@ -110,7 +114,7 @@ typedef struct {
 } moe_saved_layout;
 moe_status moe_saved_offsets(const moe_config *cfg, moe_saved_layout *layout);
 
-/* MOE_PREC_FP8_BWD only: byte offsets, inside moe_backward's scratch, of the
+/* MOE_PREC_FP8_BWD and MOE_PREC_MXFP8: byte offsets, inside moe_backward's scratch, of the
  * MXFP8 operands it writes, for inspection after the call.  m_pad is the padded
  * token capacity (a multiple of 128): expert e's rows start at padded row
  * pad_offsets[e] = sum over e' < e of ceil(count/128)*128 (int32 [E+1]); rows
@@ -139,6 +143,22 @@ typedef struct {
   size_t aw_t, aw_t_sf, dy_t, dy_t_sf, x_t, x_t_sf, dg_t, dg_t_sf, du_t, du_t_sf;
 } moe_fp8_layout;
 moe_status moe_fp8_scratch_offsets(const moe_config *cfg, moe_fp8_layout *layout);
+
+/* MOE_PREC_MXFP8 only: byte offsets, inside moe_forward's scratch, of the MXFP8
+ * operands of the two forward GEMMs, for inspection after the call (padded row
+ * space, pad_offsets, codes and 512-byte scale atoms as in moe_fp8_layout):
+ *   x_q   [m_pad,H]  the permuted x along H (M side: row r in block r/128);
+ *   a_q   [m_pad,I]  A along I, from its bf16 value (M side);
+ *   wgu_q [E*2I,H]   W_gate and W_up along H, transposed and interleaved by 32:
+ *                    row e*2I + (i/32)*64 + i%32 holds W_gate[e][:, i] and the
+ *                    row 32 after it W_up[e][:, i] (N side, segments of 2I rows);
+ *   wdt_q [E*H,I]    W_down along I, transposed: row e*H + h holds W_down[e][:, h]
+ *                    (N side, segments of H rows).
+ * Returns MOE_ERR_INVALID_ARG for other precisions or unsupported shapes. */
+typedef struct {
+  size_t m_pad, pad_offsets, x_q, x_sf, a_q, a_sf, wgu_q, wgu_sf, wdt_q, wdt_sf;
+} moe_mxfp8_fwd_layout;
+moe_status moe_mxfp8_forward_offsets(const moe_config *cfg, moe_mxfp8_fwd_layout *layout);
 
 /* Router and dispatch indices.  logits: device fp32 [T,E].  Writes every field
  * of *routing.  Per-expert counts, the scan and the permutation are computed

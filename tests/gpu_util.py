@@ -3,7 +3,8 @@ inputs and compare with the fp64 oracle.
 
 Tolerances (floating point): relative L2 <= 5e-3 and max |diff| <= 2e-2 *
 max |ref| for bf16 outputs and gradients; 1e-2 and 5e-2 for the MXFP8 backward
-(fp8_bwd) gradients dx, dW_*, against the oracle's quantised backward; router
+(fp8_bwd) gradients dx, dW_*, against the oracle's quantised backward, and in
+the mxfp8 mode for every output (its forward is quantised too); router
 weights within 1e-6; integer routing and permutation bit-exact.
 """
 import json
@@ -26,6 +27,31 @@ W_ATOL = 1e-6
 # where fp32 evaluation order moves a bf16 value across a rounding boundary.
 FP8_REL_L2 = 1e-2
 FP8_MAX_REL = 5e-2
+
+
+def atoms_to_scales(sf, R, K, seg=None, group=128):
+    """[R, K/32] scale codes from the 512-byte atoms: row w of atom row-block rb,
+    K-block b at byte (rb*(K/128) + b/4)*512 + (w%32)*16 + (w/32)*4 + b%4; rows
+    map to (rb, w) through segments of `seg` rows cut into groups of `group`."""
+    seg = seg or R
+    r = np.arange(R)
+    s, j = r // seg, r % seg
+    g, jj = j // group, j % group
+    gps, apg = -(-seg // group), -(-group // 128)
+    rb = (s * gps + g) * apg + jj // 128
+    w = jj % 128
+    b = np.arange(K // 32)
+    idx = ((rb[:, None] * (K // 128) + b[None, :] // 4) * 512 + (w[:, None] % 32) * 16 + (w[:, None] // 32) * 4
+           + b[None, :] % 4)
+    return np.asarray(sf, np.uint8)[idx]
+
+
+def padded_rows(rows, offsets, pad, Mp):
+    out = np.zeros((Mp,) + rows.shape[1:], rows.dtype)
+    for e in range(len(offsets) - 1):
+        n = offsets[e + 1] - offsets[e]
+        out[pad[e]:pad[e] + n] = rows[offsets[e]:offsets[e + 1]]
+    return out
 
 
 def to_dev(inp, dev="cuda"):
@@ -87,27 +113,31 @@ def check_routing(shape, inp, layer):
 def check_full(shape, inp, layer, out, grads, precision="bf16", check_saved=True):
     """Every output element against the oracle (small shapes)."""
     idx, w, counts, offsets, ros, sor = check_routing(shape, inp, layer)
-    quant = precision == "fp8_bwd"
+    quant = precision in ("fp8_bwd", "mxfp8")
+    fq = precision == "mxfp8"  # the forward GEMMs quantised too
+    fW = O.quant_weights_fwd(inp["W_gate"], inp["W_up"], inp["W_down"]) if fq else None
+    tol = dict(rel_l2=FP8_REL_L2, max_rel=FP8_MAX_REL) if quant else {}
+    ftol = tol if fq else {}
     if check_saved:
         xp = layer.saved_tensor("x_perm").cpu().numpy().view(np.uint16)
         np.testing.assert_array_equal(xp, inp["x"][sor // shape.k])
         toks = sor // shape.k
         experts = idx.ravel()[sor]
-        g, u, a, y = O.expert_rows(shape, inp["x"], inp["W_gate"], inp["W_up"], inp["W_down"], toks, experts)
-        close("G", bf(layer.saved_tensor("G")), g)
-        close("U", bf(layer.saved_tensor("U")), u)
-        close("A", bf(layer.saved_tensor("A")), a)
-        close("Y", bf(layer.saved_tensor("Y")), y)
-        close("A_w", bf(layer.saved_tensor("A_w")), a * w.ravel()[sor][:, None])
-    ref = O.forward(shape, inp["x"], idx, w, inp["W_gate"], inp["W_up"], inp["W_down"])
-    close("out", bf(out), ref)
+        g, u, a, y = O.expert_rows(shape, inp["x"], inp["W_gate"], inp["W_up"], inp["W_down"], toks, experts,
+                                   fwd_quant=fq, fW=fW)
+        close("G", bf(layer.saved_tensor("G")), g, **ftol)
+        close("U", bf(layer.saved_tensor("U")), u, **ftol)
+        close("A", bf(layer.saved_tensor("A")), a, **ftol)
+        close("Y", bf(layer.saved_tensor("Y")), y, **ftol)
+        close("A_w", bf(layer.saved_tensor("A_w")), a * w.ravel()[sor][:, None], **ftol)
+    ref = O.forward(shape, inp["x"], idx, w, inp["W_gate"], inp["W_up"], inp["W_down"], fwd_quant=fq, fW=fW)
+    close("out", bf(out), ref, **ftol)
     dx, dl, gd = O.backward_tokens(shape, inp["x"], inp["logits"], idx, w, inp["W_gate"], inp["W_up"],
-                                   inp["W_down"], inp["dy"], quant=quant)
+                                   inp["W_down"], inp["dy"], quant=quant, fwd_quant=fq, fW=fW)
     dWg, dWu, dWd = O.dw_full(shape, inp["x"], idx, w, inp["W_gate"], inp["W_up"], inp["W_down"],
-                              inp["dy"], quant=quant)
-    tol = dict(rel_l2=FP8_REL_L2, max_rel=FP8_MAX_REL) if quant else {}
-    close("d_logits", grads["d_logits"].cpu().numpy(), dl)
-    close("d_topk_w", grads["d_topk_w"].cpu().numpy(), gd)
+                              inp["dy"], quant=quant, fwd_quant=fq, fW=fW)
+    close("d_logits", grads["d_logits"].cpu().numpy(), dl, **ftol)
+    close("d_topk_w", grads["d_topk_w"].cpu().numpy(), gd, **ftol)
     close("dx", bf(grads["dx"]), dx, **tol)
     close("dW_gate", bf(grads["dW_gate"]), dWg, **tol)
     close("dW_up", bf(grads["dW_up"]), dWu, **tol)

@@ -153,3 +153,35 @@ def test_router_workspace_and_shapes(L):
     for bad in (dict(E=12), dict(E=4), dict(H=96)):  # E % 8, E >= 8, H % 64
         c = moe.Config(300, bad.get("H", 256), 64, bad.get("E", 16), 2, 0)
         assert L.moe_router_workspace(ctypes.byref(c), None, None) == -1
+
+
+def test_mxfp8_shapes_and_forward_layout(L):
+    sz = ctypes.c_size_t()
+    for H, I in ((192, 128), (128, 192)):  # K staged in 128-byte blocks
+        assert L.moe_query_workspace(ctypes.byref(cfg(H=H, I=I, prec=2)), ctypes.byref(sz), None, None,
+                                     None) == -1
+    lay = moe.Mx8FwdLayout()
+    for prec in (0, 1):
+        assert L.moe_mxfp8_forward_offsets(ctypes.byref(cfg(I=128, prec=prec)), ctypes.byref(lay)) == -1
+    T, H, I, E, k = 300, 256, 128, 8, 2
+    c = cfg(T=T, H=H, I=I, E=E, k=k, prec=2)
+    f = moe.mxfp8_forward_offsets(c)
+    M = T * k
+    Mp = f["m_pad"]
+    assert Mp % 128 == 0 and Mp >= M + 127 * E
+    from dropless_mixture_experts_top_gb300.synth import MoEShape
+    shape = MoEShape(T=T, H=H, I=I, E=E, k=k)
+    sizes = {"pad_offsets": 4 * (E + 1), "x_q": Mp * H, "a_q": Mp * I, "wgu_q": E * 2 * I * H, "wdt_q": E * H * I}
+    for n, (R, K) in {"x_q": (Mp, H), "a_q": (Mp, I), "wgu_q": (E * 2 * I, H), "wdt_q": (E * H, I)}.items():
+        seg, group = moe.sf_grouping(n, shape, Mp)
+        sizes[n[:-2] + "_sf"] = moe.sf_layout_bytes(R, K, seg, group)
+        assert sizes[n[:-2] + "_sf"] >= R * K // 32
+    spans = sorted((f[n], f[n] + b, n) for n, b in sizes.items())
+    for (a0, a1, n0), (b0, b1, n1) in zip(spans, spans[1:]):
+        assert a1 <= b0, (n0, n1)
+    assert all(f[n] % 256 == 0 for n in sizes)
+    _, _, fs, bs = moe.query_workspace(c)
+    assert spans[0][0] >= 256 and spans[-1][1] <= fs  # after the status header, inside the forward scratch
+    # the backward is fp8_bwd's: same backward scratch and quantised-operand layout
+    c1 = cfg(T=T, H=H, I=I, E=E, k=k, prec=1)
+    assert moe.query_workspace(c1)[3] == bs and moe.fp8_scratch_offsets(c1) == moe.fp8_scratch_offsets(c)

@@ -15,6 +15,7 @@ from dropless_mixture_experts_top_gb300 import moe, synth
 from dropless_mixture_experts_top_gb300.synth import MoEShape
 from oracle import oracle as O
 from tests import gpu_util as G
+from tests.gpu_util import atoms_to_scales, padded_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -23,31 +24,6 @@ pytestmark = pytest.mark.gpu
 def _build():
     from dropless_mixture_experts_top_gb300 import _build as B
     B.build()
-
-
-def atoms_to_scales(sf, R, K, seg=None, group=128):
-    """[R, K/32] scale codes from the 512-byte atoms: row w of atom row-block rb,
-    K-block b at byte (rb*(K/128) + b/4)*512 + (w%32)*16 + (w/32)*4 + b%4; rows
-    map to (rb, w) through segments of `seg` rows cut into groups of `group`."""
-    seg = seg or R
-    r = np.arange(R)
-    s, j = r // seg, r % seg
-    g, jj = j // group, j % group
-    gps, apg = -(-seg // group), -(-group // 128)
-    rb = (s * gps + g) * apg + jj // 128
-    w = jj % 128
-    b = np.arange(K // 32)
-    idx = ((rb[:, None] * (K // 128) + b[None, :] // 4) * 512 + (w[:, None] % 32) * 16 + (w[:, None] // 32) * 4
-           + b[None, :] % 4)
-    return np.asarray(sf, np.uint8)[idx]
-
-
-def padded_rows(rows, offsets, pad, Mp):
-    out = np.zeros((Mp,) + rows.shape[1:], rows.dtype)
-    for e in range(len(offsets) - 1):
-        n = offsets[e + 1] - offsets[e]
-        out[pad[e]:pad[e] + n] = rows[offsets[e]:offsets[e + 1]]
-    return out
 
 
 def check_token_axis(layer, name, src_rows, offsets, pad, Mp):
