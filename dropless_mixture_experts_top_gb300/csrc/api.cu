@@ -96,6 +96,20 @@ Layout layout_of(const moe_config *c) {
   o += align256(M * H * 2);
   L.s_Aw = o;
   o += align256(M * I * 2);
+  if (c->precision == MOE_PREC_MXFP8) {  // the backward's weight operands, written by the forward
+    moe_mxfp8_fwd_layout &f = L.fq;
+    auto take = [&o](size_t bytes) {
+      const size_t at = o;
+      o += align256(bytes);
+      return at;
+    };
+    f.bwd_wd_q = take(E * I * H);
+    f.bwd_wd_sf = take(sf_layout_bytes(E * I, H, sf_b(I)));
+    f.bwd_wg_q = take(E * H * I);
+    f.bwd_wg_sf = take(sf_layout_bytes(E * H, I, sf_b(H)));
+    f.bwd_wu_q = take(E * H * I);
+    f.bwd_wu_sf = take(sf_layout_bytes(E * H, I, sf_b(H)));
+  }
   L.s_total = o > 0 ? o : 256;
   o = kHeader;
   if (c->precision == MOE_PREC_MXFP8) {
@@ -143,16 +157,21 @@ Layout layout_of(const moe_config *c) {
     q.pad_offsets = take((E + 1) * 4);
     q.dy_q = take(Mp * H);
     q.dy_sf = take(Mp * H / 32);
-    q.wd_q = take(E * I * H);
-    q.wd_sf = take(sf_layout_bytes(E * I, H, sf_b(I)));
+    const bool wq = c->precision == MOE_PREC_FP8_BWD;  // mxfp8: the weights' codes are in `saved`
+    if (wq) {
+      q.wd_q = take(E * I * H);
+      q.wd_sf = take(sf_layout_bytes(E * I, H, sf_b(I)));
+    }
     q.dg_q = take(Mp * I);
     q.dg_sf = take(Mp * I / 32);
     q.du_q = take(Mp * I);
     q.du_sf = take(Mp * I / 32);
-    q.wg_q = take(E * H * I);
-    q.wg_sf = take(sf_layout_bytes(E * H, I, sf_b(H)));
-    q.wu_q = take(E * H * I);
-    q.wu_sf = take(sf_layout_bytes(E * H, I, sf_b(H)));
+    if (wq) {
+      q.wg_q = take(E * H * I);
+      q.wg_sf = take(sf_layout_bytes(E * H, I, sf_b(H)));
+      q.wu_q = take(E * H * I);
+      q.wu_sf = take(sf_layout_bytes(E * H, I, sf_b(H)));
+    }
     q.aw_t = take(I * Mp);
     q.aw_t_sf = take(I * Mp / 32);
     q.dy_t = take(H * Mp);
@@ -266,6 +285,10 @@ struct Fp8Bwd {
   int32_t *status;
   const uint16_t *W_gate, *W_up, *W_down, *x_perm, *G, *U, *A_w;
   uint16_t *dy_perm, *dX, *dx, *dW_gate, *dW_up, *dW_down;
+  // the weights' codes for the three GEMMs that read them: quantised here
+  // (fp8_bwd, into the scratch) or already by the forward (mxfp8, in `saved`)
+  bool quantise_weights;
+  uint8_t *wd_q, *wd_sf, *wg_q, *wg_sf, *wu_q, *wu_sf;
 };
 
 moe_status backward_fp8(const Fp8Bwd &f, cudaStream_t s) {
@@ -295,14 +318,14 @@ moe_status backward_fp8(const Fp8Bwd &f, cudaStream_t s) {
     return launch_quant_cols(f.dy_perm, H, Mp, off, pad_off, E, sc + q.dy_t, sc + q.dy_t_sf, sf_b(H),
                              RowCodes{sc + q.dy_q, sc + q.dy_sf, sf_a(Mp)}, s);
   }));
-  MOE_TRY(timed("mx_quant_W_down", s, [&] {
-    return launch_quant_rows(f.W_down, E * I, H, nullptr, nullptr, E, sc + q.wd_q, sc + q.wd_sf,
-                             sf_b(I), s);
-  }));
+  if (f.quantise_weights)
+    MOE_TRY(timed("mx_quant_W_down", s, [&] {
+      return launch_quant_rows(f.W_down, E * I, H, nullptr, nullptr, E, f.wd_q, f.wd_sf, sf_b(I), s);
+    }));
   m.a0 = sc + q.dy_q;
   m.sfa0 = sc + q.dy_sf;
-  m.b0 = sc + q.wd_q;
-  m.sfb0 = sc + q.wd_sf;
+  m.b0 = f.wd_q;
+  m.sfb0 = f.wd_sf;
   // dA's epilogue writes dG and dU quantised along I (for dX) and along tokens
   // (for dW_gate/up); they are never stored in bf16
   m.o0 = m.o1 = nullptr;
@@ -316,22 +339,22 @@ moe_status backward_fp8(const Fp8Bwd &f, cudaStream_t s) {
   m.du_t_sf = sc + q.du_t_sf;
   MOE_TRY(timed("mx_gemm_dA_dswiglu", s, [&] { return launch_mx_gemm(kMxGemmDA, m, s); }));
   // dX = Q(dG) . Q(W_gate)^T + Q(dU) . Q(W_up)^T, K = I
-  MOE_TRY(timed("mx_quant_W_gate", s, [&] {
-    return launch_quant_rows(f.W_gate, E * H, I, nullptr, nullptr, E, sc + q.wg_q, sc + q.wg_sf,
-                             sf_b(H), s);
-  }));
-  MOE_TRY(timed("mx_quant_W_up", s, [&] {
-    return launch_quant_rows(f.W_up, E * H, I, nullptr, nullptr, E, sc + q.wu_q, sc + q.wu_sf,
-                             sf_b(H), s);
-  }));
+  if (f.quantise_weights) {
+    MOE_TRY(timed("mx_quant_W_gate", s, [&] {
+      return launch_quant_rows(f.W_gate, E * H, I, nullptr, nullptr, E, f.wg_q, f.wg_sf, sf_b(H), s);
+    }));
+    MOE_TRY(timed("mx_quant_W_up", s, [&] {
+      return launch_quant_rows(f.W_up, E * H, I, nullptr, nullptr, E, f.wu_q, f.wu_sf, sf_b(H), s);
+    }));
+  }
   m.a0 = sc + q.dg_q;
   m.sfa0 = sc + q.dg_sf;
   m.a1 = sc + q.du_q;
   m.sfa1 = sc + q.du_sf;
-  m.b0 = sc + q.wg_q;
-  m.sfb0 = sc + q.wg_sf;
-  m.b1 = sc + q.wu_q;
-  m.sfb1 = sc + q.wu_sf;
+  m.b0 = f.wg_q;
+  m.sfb0 = f.wg_sf;
+  m.b1 = f.wu_q;
+  m.sfb1 = f.wu_sf;
   m.o0 = f.dX;
   m.o1 = nullptr;
   MOE_TRY(timed("mx_gemm_dX", s, [&] { return launch_mx_gemm(kMxGemmDX, m, s); }));
@@ -367,8 +390,8 @@ moe_status backward_fp8(const Fp8Bwd &f, cudaStream_t s) {
   return MOE_OK;
 }
 
-// The mxfp8 forward after the permute: both grouped GEMMs in MXFP8.  x_perm
-// along H into the padded row space; the weights along their middle axis,
+// The mxfp8 forward: both grouped GEMMs in MXFP8.  The permute also quantises
+// x along H into the padded row space; the weights along their middle axis,
 // transposed (W_gate | W_up interleaved by 32 columns, so one 192-row B tile
 // holds 96 gate and the same 96 up columns); GEMM1's epilogue writes the bf16
 // activations and A quantised along I; GEMM2 writes Y.
@@ -379,8 +402,9 @@ struct Mx8Fwd {
   uint8_t *sc;
   int sms;
   int32_t *status;
-  const uint16_t *x_perm, *W_gate, *W_up, *W_down;
-  uint16_t *A, *G, *U, *A_w, *Y;
+  const uint16_t *x, *W_gate, *W_up, *W_down;
+  uint16_t *x_perm, *A, *G, *U, *A_w, *Y;
+  uint8_t *saved;  // the backward's weight codes go here
 };
 
 moe_status forward_mx(const Mx8Fwd &f, cudaStream_t s) {
@@ -391,13 +415,21 @@ moe_status forward_mx(const Mx8Fwd &f, cudaStream_t s) {
   int32_t *pad_off = reinterpret_cast<int32_t *>(sc + q.pad_offsets);
   const int32_t *off = f.r->offsets;
   MOE_TRY(timed("mx_pad_offsets_fwd", s, [&] { return launch_pad_offsets(off, E, pad_off, s); }));
-  MOE_TRY(timed("mx_quant_x", s, [&] {
-    return launch_quant_rows(f.x_perm, Mp, H, off, pad_off, E, sc + q.x_q, sc + q.x_sf, sf_a(Mp), s);
+  MOE_TRY(timed("permute_quant_x", s, [&] {
+    return launch_permute_quant(f.x, f.r->row_of_slot, f.r->topk_idx, off, pad_off, f.x_perm, sc + q.x_q,
+                                sc + q.x_sf, sf_a(Mp), T, H, k, s);
   }));
+  MOE_TRY(timed("mx_zero_pad_rows", s, [&] {
+    return launch_zero_pad_rows(off, pad_off, E, H, sc + q.x_q, sc + q.x_sf, sf_a(Mp), s);
+  }));
+  // each weight read once: along H for GEMM1 (transposed, interleaved) and
+  // along I for the backward's dX (row by row, into `saved`)
   MOE_TRY(timed("mx_quant_W_gateup_fwd", s, [&] {
-    const cudaError_t e = launch_quant_wT(f.W_gate, E, H, I, 1, 0, sc + q.wgu_q, sc + q.wgu_sf, sf_b(2 * I), s);
+    const cudaError_t e = launch_quant_wT(f.W_gate, E, H, I, 1, 0, sc + q.wgu_q, sc + q.wgu_sf, sf_b(2 * I),
+                                          RowCodes{f.saved + q.bwd_wg_q, f.saved + q.bwd_wg_sf, sf_b(H)}, s);
     if (e != cudaSuccess) return e;
-    return launch_quant_wT(f.W_up, E, H, I, 1, 1, sc + q.wgu_q, sc + q.wgu_sf, sf_b(2 * I), s);
+    return launch_quant_wT(f.W_up, E, H, I, 1, 1, sc + q.wgu_q, sc + q.wgu_sf, sf_b(2 * I),
+                           RowCodes{f.saved + q.bwd_wu_q, f.saved + q.bwd_wu_sf, sf_b(H)}, s);
   }));
   MxGemmArgs m{};
   m.H = H;
@@ -422,7 +454,9 @@ moe_status forward_mx(const Mx8Fwd &f, cudaStream_t s) {
   m.aq_sf = sc + q.a_sf;
   MOE_TRY(timed("mx_gemm_gateup_swiglu", s, [&] { return launch_mx_gemm(kMxGemmGateUp, m, s); }));
   MOE_TRY(timed("mx_quant_W_down_fwd", s, [&] {
-    return launch_quant_wT(f.W_down, E, I, H, 0, 0, sc + q.wdt_q, sc + q.wdt_sf, sf_b(H), s);
+    // along I for GEMM2 (transposed) and along H for the backward's dA (row by row, into `saved`)
+    return launch_quant_wT(f.W_down, E, I, H, 0, 0, sc + q.wdt_q, sc + q.wdt_sf, sf_b(H),
+                           RowCodes{f.saved + q.bwd_wd_q, f.saved + q.bwd_wd_sf, sf_b(I)}, s);
   }));
   m.a0 = sc + q.a_q;
   m.sfa0 = sc + q.a_sf;
@@ -547,10 +581,6 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const moe_routing *
   uint16_t *Y = reinterpret_cast<uint16_t *>(sv + L.s_Y);
   uint16_t *A_w = reinterpret_cast<uint16_t *>(sv + L.s_Aw);
 
-  MOE_TRY(timed("permute_rows", s, [&] {
-    return launch_permute_rows(static_cast<const uint16_t *>(x), r->row_of_slot, x_perm, T, H, k,
-                               s);
-  }));
   if (cfg->precision == MOE_PREC_MXFP8) {
     Mx8Fwd f;
     f.cfg = cfg;
@@ -559,6 +589,7 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const moe_routing *
     f.sc = sc;
     f.sms = di.sms;
     f.status = status;
+    f.x = static_cast<const uint16_t *>(x);
     f.x_perm = x_perm;
     f.W_gate = static_cast<const uint16_t *>(W_gate);
     f.W_up = static_cast<const uint16_t *>(W_up);
@@ -568,8 +599,12 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const moe_routing *
     f.U = U;
     f.A_w = A_w;
     f.Y = Y;
+    f.saved = sv;
     MOE_TRY(forward_mx(f, s));
   } else {
+    MOE_TRY(timed("permute_rows", s, [&] {
+      return launch_permute_rows(static_cast<const uint16_t *>(x), r->row_of_slot, x_perm, T, H, k, s);
+    }));
     GemmArgs g = gemm_base(cfg, r, di.sms, status);
     g.x_perm = x_perm;
     g.W_gate = static_cast<const uint16_t *>(W_gate);
@@ -661,6 +696,20 @@ moe_status moe_backward(const moe_config *cfg, const void *dy, const void *x,
     f.dW_gate = static_cast<uint16_t *>(dW_gate);
     f.dW_up = static_cast<uint16_t *>(dW_up);
     f.dW_down = static_cast<uint16_t *>(dW_down);
+    f.quantise_weights = cfg->precision == MOE_PREC_FP8_BWD;
+    uint8_t *wb = f.quantise_weights ? sc : const_cast<uint8_t *>(sv);  // read only when in `saved`
+    const size_t o_wd = f.quantise_weights ? L.q.wd_q : L.fq.bwd_wd_q;
+    const size_t o_wd_sf = f.quantise_weights ? L.q.wd_sf : L.fq.bwd_wd_sf;
+    const size_t o_wg = f.quantise_weights ? L.q.wg_q : L.fq.bwd_wg_q;
+    const size_t o_wg_sf = f.quantise_weights ? L.q.wg_sf : L.fq.bwd_wg_sf;
+    const size_t o_wu = f.quantise_weights ? L.q.wu_q : L.fq.bwd_wu_q;
+    const size_t o_wu_sf = f.quantise_weights ? L.q.wu_sf : L.fq.bwd_wu_sf;
+    f.wd_q = wb + o_wd;
+    f.wd_sf = wb + o_wd_sf;
+    f.wg_q = wb + o_wg;
+    f.wg_sf = wb + o_wg_sf;
+    f.wu_q = wb + o_wu;
+    f.wu_sf = wb + o_wu_sf;
     return backward_fp8(f, s);
   }
   GemmArgs g = gemm_base(cfg, r, di.sms, status);

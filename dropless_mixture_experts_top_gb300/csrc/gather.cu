@@ -16,6 +16,7 @@
 //                  g_tj = <dy[t], Y[row(t,j)]>                 (d w_tj)
 //                  d_logits[t, S_tj] = w_tj (g_tj - sum_i w_ti g_ti), 0 elsewhere
 #include "common.cuh"
+#include "mxfp8.cuh"
 
 namespace moe {
 namespace {
@@ -71,6 +72,87 @@ __global__ void __launch_bounds__(kWarps * 32) permute_rows_kernel(const uint4 *
       }
     }
   }
+}
+
+// The permute with the mxfp8 forward's quantisation of x fused: x_perm as
+// above, and each token's row quantised along H once (a 32-element block is
+// four consecutive 16-byte vectors, i.e. four neighbouring lanes) with its
+// codes and scale written to the padded row of each of its k permuted rows
+// (expert e's rows start at pad_off[e]).
+__global__ void __launch_bounds__(kWarps * 32) permute_quant_kernel(
+    const uint4 *__restrict__ x, const int32_t *__restrict__ ros, const int32_t *__restrict__ topk_idx,
+    const int32_t *__restrict__ offsets, const int32_t *__restrict__ pad_off, uint4 *__restrict__ xp,
+    uint8_t *__restrict__ codes, uint8_t *__restrict__ sf, SfLayout L, int T, int nv, int k) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const int H = nv * 8;
+  int myrow = 0, myprow = 0;
+  if (lane < k) {
+    myrow = __ldg(ros + static_cast<size_t>(t) * k + lane);
+    const int e = __ldg(topk_idx + static_cast<size_t>(t) * k + lane);
+    myprow = __ldg(pad_off + e) + myrow - __ldg(offsets + e);
+  }
+  for (int v0 = 0; v0 < nv; v0 += 32 * kVecPerLane) {
+    uint4 buf[kVecPerLane];
+    uint2 q[kVecPerLane];
+    uint8_t scode[kVecPerLane];
+#pragma unroll
+    for (int u = 0; u < kVecPerLane; ++u) {
+      const int v = v0 + u * 32 + lane;
+      buf[u] = v < nv ? __ldcs(x + static_cast<size_t>(t) * nv + v) : make_uint4(0, 0, 0, 0);
+      const uint32_t w[4] = {buf[u].x, buf[u].y, buf[u].z, buf[u].w};
+      float f[8];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        f[2 * h] = bf16_lo(w[h]);
+        f[2 * h + 1] = bf16_hi(w[h]);
+      }
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));  // the block's four lanes
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      const int X = mx_scale_exp(amax);
+      const float s = pow2_neg(X);
+      q[u] = make_uint2(pack_e4m3x4(f[0] * s, f[1] * s, f[2] * s, f[3] * s),
+                        pack_e4m3x4(f[4] * s, f[5] * s, f[6] * s, f[7] * s));
+      scode[u] = static_cast<uint8_t>(X + 127);
+    }
+    for (int j = 0; j < k; ++j) {
+      const int row = __shfl_sync(0xffffffffu, myrow, j);
+      const int prow = __shfl_sync(0xffffffffu, myprow, j);
+      uint4 *dst = xp + static_cast<size_t>(row) * nv;
+      uint2 *cdst = reinterpret_cast<uint2 *>(codes + static_cast<size_t>(prow) * H);
+#pragma unroll
+      for (int u = 0; u < kVecPerLane; ++u) {
+        const int v = v0 + u * 32 + lane;
+        if (v < nv) {
+          dst[v] = buf[u];
+          cdst[v] = q[u];
+          if ((lane & 3) == 0) sf[atom_byte(prow, v >> 2, H, L)] = scode[u];
+        }
+      }
+    }
+  }
+}
+
+// Padded rows past each expert's count (up to the next 128-row boundary): zero
+// codes and zero scale codes.  One block per expert.
+__global__ void __launch_bounds__(256) zero_pad_rows_kernel(const int32_t *__restrict__ offsets,
+                                                            const int32_t *__restrict__ pad_off, int K,
+                                                            uint8_t *__restrict__ codes,
+                                                            uint8_t *__restrict__ sf, SfLayout L) {
+  const int e = blockIdx.x;
+  const int first = __ldg(pad_off + e) + (__ldg(offsets + e + 1) - __ldg(offsets + e));
+  const int end = __ldg(pad_off + e + 1);
+  const int per_row = K / 16;
+  for (int i = threadIdx.x; i < (end - first) * per_row; i += blockDim.x) {
+    const int r = first + i / per_row, c = i % per_row;
+    reinterpret_cast<uint4 *>(codes + static_cast<size_t>(r) * K)[c] = make_uint4(0, 0, 0, 0);
+  }
+  for (int i = threadIdx.x; i < (end - first) * (K / 32); i += blockDim.x)
+    sf[atom_byte(first + i / (K / 32), i % (K / 32), K, L)] = 0;
 }
 
 template <bool kWeighted>
@@ -259,6 +341,21 @@ cudaError_t launch_router_bwd(const uint16_t *dy, const uint16_t *Y, const int32
   router_bwd_kernel<<<blocks_for(T), kWarps * 32, 0, s>>>(
       reinterpret_cast<const uint4 *>(dy), reinterpret_cast<const uint4 *>(Y), row_of_slot,
       topk_idx, topk_w, reinterpret_cast<uint4 *>(dy_perm), d_logits, d_topk_w, T, H / 8, E, k);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute_quant(const uint16_t *x, const int32_t *row_of_slot, const int32_t *topk_idx,
+                                 const int32_t *offsets, const int32_t *pad_off, uint16_t *x_perm,
+                                 uint8_t *codes, uint8_t *sf, SfLayout L, int T, int H, int k, cudaStream_t s) {
+  permute_quant_kernel<<<blocks_for(T), kWarps * 32, 0, s>>>(
+      reinterpret_cast<const uint4 *>(x), row_of_slot, topk_idx, offsets, pad_off,
+      reinterpret_cast<uint4 *>(x_perm), codes, sf, L, T, H / 8, k);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_zero_pad_rows(const int32_t *offsets, const int32_t *pad_off, int E, int K, uint8_t *codes,
+                                 uint8_t *sf, SfLayout L, cudaStream_t s) {
+  zero_pad_rows_kernel<<<E, 256, 0, s>>>(offsets, pad_off, K, codes, sf, L);
   return cudaGetLastError();
 }
 

@@ -123,11 +123,21 @@ cudaError_t launch_quant_cols(const uint16_t *src, int C, int Mpad, const int32_
                               const int32_t *pad_off, int E, uint8_t *codes, uint8_t *sf, SfLayout L,
                               RowCodes rows, cudaStream_t s);
 
+// mxfp8 forward: the permute with x quantised along H fused (codes and scales
+// to the padded row of every permuted row; H % 128 == 0), and zero codes and
+// scales for the padded rows past each expert's count
+cudaError_t launch_permute_quant(const uint16_t *x, const int32_t *row_of_slot, const int32_t *topk_idx,
+                                 const int32_t *offsets, const int32_t *pad_off, uint16_t *x_perm,
+                                 uint8_t *codes, uint8_t *sf, SfLayout L, int T, int H, int k, cudaStream_t s);
+cudaError_t launch_zero_pad_rows(const int32_t *offsets, const int32_t *pad_off, int E, int K, uint8_t *codes,
+                                 uint8_t *sf, SfLayout L, cudaStream_t s);
+
 // Weights [E, R, C] quantised along R (R % 128 == 0, C % 64 == 0), transposed:
 // codes [E * C, R] (interleave 0) or the gate|up interleave of the mxfp8 GEMM1
-// (interleave 1, codes [E * 2C, R]: row e*2C + (c/32)*64 + half*32 + c%32).
+// (interleave 1, codes [E * 2C, R]: row e*2C + (c/32)*64 + half*32 + c%32);
+// with rows.codes set, also along C row by row: codes [E * R, C].
 cudaError_t launch_quant_wT(const uint16_t *W, int E, int R, int C, int interleave, int half,
-                            uint8_t *codes, uint8_t *sf, SfLayout L, cudaStream_t s);
+                            uint8_t *codes, uint8_t *sf, SfLayout L, RowCodes rows, cudaStream_t s);
 
 // MXFP8 grouped GEMMs: the fp8_bwd backward's four, and the mxfp8 forward's two
 enum MxGemmMode : int {

@@ -202,13 +202,17 @@ __global__ void __launch_bounds__(kQcThreads, 3) quant_cols_kernel(const uint16_
 // -> codes [rows, R] with output row (e, c) = e * C + c (W_down: the down
 // GEMM's B rows), or, interleaved for gate|up tiles, e * 2C + (c / 32) * 64 +
 // half * 32 + c % 32 (W_gate half 0, W_up half 1: every 64 B rows hold 32
-// gate columns then the same 32 up columns).  Same staging as the token-axis
-// quantiser: 128 x 64 tiles, one thread per (column, 32-row block), codes
-// leaving through a shared output tile as 128-byte rows.
+// gate columns then the same 32 up columns).  Optionally the same staged tile
+// is also quantised along C, row by row (the backward GEMMs' weight operand,
+// codes [E * R, C]), so each weight is read once for both.  Same staging as
+// the token-axis quantiser: 128 x 64 tiles (chunks XOR-swizzled by row), the
+// next column tile prefetched into registers, one thread per (column, 32-row
+// block), codes leaving through a shared output tile as 128-byte rows.
 __global__ void __launch_bounds__(kQcThreads, 3) quant_wT_kernel(const uint16_t *__restrict__ src, int R,
                                                                  int C, int interleave, int half,
                                                                  uint8_t *__restrict__ codes,
-                                                                 uint8_t *__restrict__ sf, SfLayout L) {
+                                                                 uint8_t *__restrict__ sf, SfLayout L,
+                                                                 RowCodes rows) {
   __shared__ __align__(16) uint16_t tile[kQcRows * kQcCols];
   constexpr int kOutStride = kQcRows + 16;
   __shared__ __align__(16) uint8_t otile[kQcCols * kOutStride];
@@ -217,15 +221,43 @@ __global__ void __launch_bounds__(kQcThreads, 3) quant_wT_kernel(const uint16_t 
   auto out_row = [&](int c) {
     return interleave ? e * 2 * C + (c >> 5) * 64 + half * 32 + (c & 31) : e * C + c;
   };
-  for (int c0 = blockIdx.y * kQcCols; c0 < C; c0 += gridDim.y * kQcCols) {
+  constexpr int kLoads = (kQcRows * kQcCols / 8) / kQcThreads;
+  uint4 nxt[kLoads];
+  auto load_tile = [&](int c0) {
 #pragma unroll
-    for (int j = 0; j < (kQcRows * kQcCols / 8) / kQcThreads; ++j) {
+    for (int j = 0; j < kLoads; ++j) {
+      const int i = threadIdx.x + j * kQcThreads;
+      nxt[j] = __ldg(reinterpret_cast<const uint4 *>(src + static_cast<size_t>(grow0 + (i >> 3)) * C + c0) + (i & 7));
+    }
+  };
+  const int cstep = gridDim.y * kQcCols;
+  if (blockIdx.y * kQcCols < C) load_tile(blockIdx.y * kQcCols);
+  for (int c0 = blockIdx.y * kQcCols; c0 < C; c0 += cstep) {
+#pragma unroll
+    for (int j = 0; j < kLoads; ++j) {
       const int i = threadIdx.x + j * kQcThreads;
       const int r = i >> 3, part = i & 7;
-      const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src + static_cast<size_t>(grow0 + r) * C + c0) + part);
-      *reinterpret_cast<uint4 *>(tile + r * kQcCols + ((part ^ (r & 7)) << 3)) = v;
+      *reinterpret_cast<uint4 *>(tile + r * kQcCols + ((part ^ (r & 7)) << 3)) = nxt[j];
     }
+    if (c0 + cstep < C) load_tile(c0 + cstep);
     __syncthreads();
+    if (rows.codes) {  // along C: thread = (row, 32-column block)
+      const int r = threadIdx.x >> 1, bb = threadIdx.x & 1;
+      float v[32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(tile + r * kQcCols + (((4 * bb + q) ^ (r & 7)) << 3));
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          v[8 * q + 2 * h] = bf16_lo(ww[h]);
+          v[8 * q + 2 * h + 1] = bf16_hi(ww[h]);
+        }
+      }
+      const int grow = grow0 + r;
+      rows.sf[atom_byte(grow, (c0 >> 5) + bb, C, rows.L)] =
+          quant32(v, reinterpret_cast<uint4 *>(rows.codes + static_cast<size_t>(grow) * C + c0 + 32 * bb));
+    }
     const int cc = threadIdx.x % kQcCols, b = threadIdx.x / kQcCols;  // 4 blocks of 32 rows
     float v[32];
 #pragma unroll
@@ -294,10 +326,10 @@ cudaError_t launch_quant_cols(const uint16_t *src, int C, int Mpad, const int32_
 }
 
 cudaError_t launch_quant_wT(const uint16_t *W, int E, int R, int C, int interleave, int half,
-                            uint8_t *codes, uint8_t *sf, SfLayout L, cudaStream_t s) {
+                            uint8_t *codes, uint8_t *sf, SfLayout L, RowCodes rows, cudaStream_t s) {
   const int col_blocks = C / kQcCols < 4 ? C / kQcCols : 4;
   const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(E) * R / kQcRows), static_cast<unsigned>(col_blocks));
-  quant_wT_kernel<<<grid, kQcThreads, 0, s>>>(W, R, C, interleave, half, codes, sf, L);
+  quant_wT_kernel<<<grid, kQcThreads, 0, s>>>(W, R, C, interleave, half, codes, sf, L, rows);
   return cudaGetLastError();
 }
 

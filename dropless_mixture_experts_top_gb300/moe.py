@@ -56,7 +56,8 @@ class Fp8Layout(ctypes.Structure):
 
 class Mx8FwdLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
-        "m_pad", "pad_offsets", "x_q", "x_sf", "a_q", "a_sf", "wgu_q", "wgu_sf", "wdt_q", "wdt_sf")]
+        "m_pad", "pad_offsets", "x_q", "x_sf", "a_q", "a_sf", "wgu_q", "wgu_sf", "wdt_q", "wdt_sf",
+        "bwd_wd_q", "bwd_wd_sf", "bwd_wg_q", "bwd_wg_sf", "bwd_wu_q", "bwd_wu_sf")]
 
 
 class MoEError(RuntimeError):
@@ -355,23 +356,25 @@ class MoELayer:
         return self.bwd_scratch[off:off + R * K].view(R, K)
 
     def fwd_fp8_tensor(self, name):
-        """A quantised operand of the mxfp8 forward left in the forward scratch:
-        uint8 codes [rows, K] for *_q, raw scale-atom bytes for *_sf, int32 [E+1]
-        for pad_offsets."""
+        """A quantised operand of the mxfp8 forward: in the forward scratch, or for
+        bwd_* (the backward's weight operands) in `saved`.  uint8 codes [rows, K]
+        for *_q, raw scale-atom bytes for *_sf, int32 [E+1] for pad_offsets."""
         lay = mxfp8_forward_offsets(self.cfg)
         s = self.shape
         Mp = lay["m_pad"]
-        rows_k = {"x_q": (Mp, s.H), "a_q": (Mp, s.I), "wgu_q": (s.E * 2 * s.I, s.H), "wdt_q": (s.E * s.H, s.I)}
+        rows_k = {"x_q": (Mp, s.H), "a_q": (Mp, s.I), "wgu_q": (s.E * 2 * s.I, s.H), "wdt_q": (s.E * s.H, s.I),
+                  "bwd_wd_q": (s.E * s.I, s.H), "bwd_wg_q": (s.E * s.H, s.I), "bwd_wu_q": (s.E * s.H, s.I)}
+        buf = self.saved if name.startswith("bwd_") else self.fwd_scratch
         off = lay[name]
         if name == "pad_offsets":
-            return self.fwd_scratch[off:off + 4 * (s.E + 1)].view(torch.int32)
+            return buf[off:off + 4 * (s.E + 1)].view(torch.int32)
         if name.endswith("_sf"):
             base = name[:-3] + "_q"
             R, K = rows_k[base]
-            seg, group = sf_grouping(base, s, Mp)
-            return self.fwd_scratch[off:off + sf_layout_bytes(R, K, seg, group)]
+            seg, group = sf_grouping(base[4:] if base.startswith("bwd_") else base, s, Mp)
+            return buf[off:off + sf_layout_bytes(R, K, seg, group)]
         R, K = rows_k[name]
-        return self.fwd_scratch[off:off + R * K].view(R, K)
+        return buf[off:off + R * K].view(R, K)
 
     def route(self, logits, stream=None):
         route(self.cfg, logits, self.routing, self.route_scratch, stream)

@@ -154,9 +154,15 @@ moe_status moe_fp8_scratch_offsets(const moe_config *cfg, moe_fp8_layout *layout
  *                    row 32 after it W_up[e][:, i] (N side, segments of 2I rows);
  *   wdt_q [E*H,I]    W_down along I, transposed: row e*H + h holds W_down[e][:, h]
  *                    (N side, segments of H rows).
+ * The same passes over the weights also write the backward GEMMs' weight
+ * operands, which in this mode live in `saved` (moe_backward does not quantise
+ * the weights again; moe_fp8_scratch_offsets reports 0 for them):
+ *   bwd_wd_q [E*I,H], bwd_wg_q and bwd_wu_q [E*H,I] and their scales, laid
+ *   out as moe_fp8_layout's wd_q, wg_q, wu_q (offsets inside `saved`).
  * Returns MOE_ERR_INVALID_ARG for other precisions or unsupported shapes. */
 typedef struct {
   size_t m_pad, pad_offsets, x_q, x_sf, a_q, a_sf, wgu_q, wgu_sf, wdt_q, wdt_sf;
+  size_t bwd_wd_q, bwd_wd_sf, bwd_wg_q, bwd_wg_sf, bwd_wu_q, bwd_wu_sf;
 } moe_mxfp8_fwd_layout;
 moe_status moe_mxfp8_forward_offsets(const moe_config *cfg, moe_mxfp8_fwd_layout *layout);
 

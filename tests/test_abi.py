@@ -182,6 +182,18 @@ def test_mxfp8_shapes_and_forward_layout(L):
     assert all(f[n] % 256 == 0 for n in sizes)
     _, _, fs, bs = moe.query_workspace(c)
     assert spans[0][0] >= 256 and spans[-1][1] <= fs  # after the status header, inside the forward scratch
-    # the backward is fp8_bwd's: same backward scratch and quantised-operand layout
+    # the backward's weight codes are written by the forward into `saved`, after the activations
+    rs, sv, _, _ = moe.query_workspace(c)
+    so = moe.saved_offsets(c)
+    wsz = {"bwd_wd_q": E * I * H, "bwd_wg_q": E * H * I, "bwd_wu_q": E * H * I}
+    for n, (R, K, seg) in {"bwd_wd_q": (E * I, H, I), "bwd_wg_q": (E * H, I, H), "bwd_wu_q": (E * H, I, H)}.items():
+        wsz[n[:-2] + "_sf"] = moe.sf_layout_bytes(R, K, seg, moe.MX_BN)
+    wspans = sorted((f[n], f[n] + b, n) for n, b in wsz.items())
+    for (a0, a1, n0), (b0, b1, n1) in zip(wspans, wspans[1:]):
+        assert a1 <= b0, (n0, n1)
+    assert wspans[0][0] >= so["A_w"] + M * I * 2 and wspans[-1][1] <= sv
+    # the rest of the backward is fp8_bwd's; its scratch holds no weight codes in this mode
+    q = moe.fp8_scratch_offsets(c)
+    assert all(q[n] == 0 for n in ("wd_q", "wd_sf", "wg_q", "wg_sf", "wu_q", "wu_sf"))
     c1 = cfg(T=T, H=H, I=I, E=E, k=k, prec=1)
-    assert moe.query_workspace(c1)[3] == bs and moe.fp8_scratch_offsets(c1) == moe.fp8_scratch_offsets(c)
+    assert bs < moe.query_workspace(c1)[3]

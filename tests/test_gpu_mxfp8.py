@@ -116,3 +116,22 @@ def test_mxfp8_empty_and_hot_experts():
 def test_mxfp8_rejects_unaligned_shape():
     with pytest.raises(moe.MoEError):
         moe.MoELayer(MoEShape(T=64, H=192, I=128, E=4, k=2), precision="mxfp8")
+
+
+def test_backward_weight_codes_from_the_forward():
+    """In this mode the forward's passes over the weights also write the
+    backward GEMMs' weight operands (into `saved`): W_down along H, W_gate and
+    W_up along I, bit-exact against the oracle's quantiser."""
+    shape = MoEShape(T=300, H=256, I=384, E=4, k=2)
+    inp = synth.make_inputs_shape(shape, 67)
+    layer, out, grads = G.run_layer(shape, inp, precision="mxfp8")
+    assert layer.status() == {"route": 0, "forward": 0, "backward": 0}
+    E, H, I = shape.E, shape.H, shape.I
+    Mp = moe.mxfp8_forward_offsets(layer.cfg)["m_pad"]
+    for name, W, R, K, seg in (("bwd_wd", inp["W_down"], E * I, H, I), ("bwd_wg", inp["W_gate"], E * H, I, H),
+                               ("bwd_wu", inp["W_up"], E * H, I, H)):
+        codes, sc, _ = O.mx_quantize_rows(W.reshape(R, K))
+        np.testing.assert_array_equal(layer.fwd_fp8_tensor(name + "_q").cpu().numpy(), codes, err_msg=name)
+        np.testing.assert_array_equal(
+            atoms_to_scales(layer.fwd_fp8_tensor(name + "_sf").cpu().numpy(), R, K, seg, moe.MX_BN), sc,
+            err_msg=name + "_sf")
