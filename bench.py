@@ -89,6 +89,9 @@ def kernel_work(shape):
         "gemm_down": ("tensor", 2 * MHI, "flop"),
         "combine": ("hbm", M * H * 2 + T * H * 2.0 + M * 8, "B"),
         "router_bwd": ("hbm", T * H * 2 + 2 * M * H * 2.0 + T * E * 4 + M * 12, "B"),
+        # bf16 backward: dy permuted (as x), the router gradient from the dA GEMM's partials
+        "permute_dy": ("hbm", T * H * 2 + M * H * 2.0 + M * 4, "B"),
+        "router_grad": ("hbm", M * 2 * ((I + 255) // 256) * 4.0 + T * E * 4 + M * 16, "B"),
         "gemm_dA_dswiglu": ("tensor", 2 * MHI, "flop"),
         "gemm_dX": ("tensor", 4 * MHI, "flop"),
         "unpermute_sum": ("hbm", M * H * 2 + T * H * 2.0 + M * 4, "B"),
@@ -107,7 +110,7 @@ def kernel_source(label):
         return "mxfp8.cu"
     if label.startswith("route_"):
         return "route.cu"
-    return "gather.cu"  # permute_rows, combine, router_bwd, unpermute_sum
+    return "gather.cu"  # permute_rows, permute_dy, combine, router_bwd, router_grad, unpermute_sum
 
 
 def source_hash(label):

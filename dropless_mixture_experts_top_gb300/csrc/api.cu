@@ -41,7 +41,7 @@ struct Layout {
   // forward scratch
   size_t f_total;
   // backward scratch
-  size_t b_dyp, b_dG, b_dU, b_dX, b_maps, b_total;
+  size_t b_dyp, b_dG, b_dU, b_dX, b_maps, b_gpart, b_total;
   // fp8_bwd and mxfp8: quantised operands inside the backward scratch (zero otherwise)
   moe_fp8_layout q;
   // mxfp8: quantised operands of the forward GEMMs inside the forward scratch
@@ -64,6 +64,10 @@ bool shape_ok(const moe_config *c) {
 // Padded token capacity of the fp8_bwd operands: every expert's rows rounded
 // up to a multiple of 128 fit in M + 127 E, itself rounded up to 128.
 inline size_t fp8_mpad(size_t M, size_t E) { return ((M + 127 * E + 127) / 128) * 128; }
+
+// Partials per row of the router weight's gradient that the bf16 dA GEMM
+// writes: one per column half of each 256-column tile.
+inline int router_grad_parts(int I) { return 2 * ((I + 255) / 256); }
 
 // Scale-atom row grouping: A operands in plain 128-row blocks; B operands (the
 // GEMMs' N side) in 192-row groups restarting at every `seg` rows (an expert's
@@ -145,6 +149,10 @@ Layout layout_of(const moe_config *c) {
   o += align256(M * H * 2);
   L.b_maps = o;
   o += align256(E * kExpertMapBytes);
+  if (c->precision == MOE_PREC_BF16) {  // the router weight's gradient, partials from the dA GEMM
+    L.b_gpart = o;
+    o += align256(M * router_grad_parts(c->I) * 4);
+  }
   if (c->precision != MOE_PREC_BF16) {
     const size_t Mp = fp8_mpad(M, E);
     moe_fp8_layout &q = L.q;
@@ -671,11 +679,13 @@ moe_status moe_backward(const moe_config *cfg, const void *dy, const void *x,
   uint16_t *dU = reinterpret_cast<uint16_t *>(sc + L.b_dU);
   uint16_t *dX = reinterpret_cast<uint16_t *>(sc + L.b_dX);
 
-  MOE_TRY(timed("router_bwd", s, [&] {
-    return launch_router_bwd(static_cast<const uint16_t *>(dy), Y, r->row_of_slot, r->topk_idx,
-                             r->topk_w, dy_perm, d_logits, d_topk_w, T, H, E, k, s);
-  }));
   if (cfg->precision != MOE_PREC_BF16) {
+    // g_tj = <dy_t, Y_tj> from the saved Y: the MXFP8 dA's accumulator carries
+    // dy's and W_down's quantisation error, so the router gradient is not taken from it
+    MOE_TRY(timed("router_bwd", s, [&] {
+      return launch_router_bwd(static_cast<const uint16_t *>(dy), Y, r->row_of_slot, r->topk_idx,
+                               r->topk_w, dy_perm, d_logits, d_topk_w, T, H, E, k, s);
+    }));
     Fp8Bwd f;
     f.cfg = cfg;
     f.r = r;
@@ -712,12 +722,20 @@ moe_status moe_backward(const moe_config *cfg, const void *dy, const void *x,
     f.wu_sf = wb + o_wu_sf;
     return backward_fp8(f, s);
   }
+  // bf16: dy is permuted; the router weight's gradient g_tj = <dy_t . W_down^T,
+  // A_r> comes from the dA GEMM's epilogue (Y is not read again)
+  MOE_TRY(timed("permute_dy", s, [&] {
+    return launch_permute_rows(static_cast<const uint16_t *>(dy), r->row_of_slot, dy_perm, T, H, k, s);
+  }));
+  (void)Y;
+  float *g_part = reinterpret_cast<float *>(sc + L.b_gpart);
   GemmArgs g = gemm_base(cfg, r, di.sms, status);
   g.x_perm = x_perm;
   g.W_gate = static_cast<const uint16_t *>(W_gate);
   g.W_up = static_cast<const uint16_t *>(W_up);
   g.W_down = static_cast<const uint16_t *>(W_down);
   g.act = A;
+  g.g_part = g_part;
   g.G = G;
   g.U = U;
   g.dy_perm = dy_perm;
@@ -729,6 +747,11 @@ moe_status moe_backward(const moe_config *cfg, const void *dy, const void *x,
   g.o0 = dG;
   g.o1 = dU;
   MOE_TRY(timed(gemm_mode_name(kBwdDA), s, [&] { return launch_grouped_gemm(kBwdDA, g, s); }));
+  g.g_part = nullptr;
+  MOE_TRY(timed("router_grad", s, [&] {
+    return launch_router_grad(r->row_of_slot, r->topk_idx, r->topk_w, g_part, router_grad_parts(I), d_logits,
+                              d_topk_w, T, E, k, s);
+  }));
   g.o0 = dX;
   g.o1 = nullptr;
   MOE_TRY(timed(gemm_mode_name(kBwdDX), s, [&] { return launch_grouped_gemm(kBwdDX, g, s); }));

@@ -275,7 +275,11 @@ constexpr int kGuChunkBytes = 2 * kGuHalfBytes;
 // column half (c % 2 == part), G and U taken from the ring that the G/U warp
 // fills in chunk order (chunk g of the CTA's sequence sits in slot g %
 // kGuSlots; 64-byte rows with the TMA's 64-byte swizzle).  gbase: the CTA's
-// running chunk count, advanced past this tile.  Returns false if a wait gave up.
+// running chunk count, advanced past this tile.  With p.g_part set it also
+// accumulates the router weight's gradient g_r = <dy_t, Y_r> = <dy_t . W_down^T,
+// A_r> over the half's columns (A recomputed from the bf16 G and U, the
+// accumulator taken before the router weight) and stores it as partial
+// (tile column index, half) of row r.  Returns false if a wait gave up.
 template <class P, int NCH>
 __device__ __forceinline__ bool epilogue_da_ring(const Tile &t, uint32_t tb, int rit, int rloc,
                                                  const P &p, int part, uint8_t *tile,
@@ -290,6 +294,7 @@ __device__ __forceinline__ bool epilogue_da_ring(const Tile &t, uint32_t tb, int
   const int nch = min(NCH, (p.I - t.n0) / 32);
   uint32_t r0[32];
   float v1[32], v2[32];
+  float gp = 0.f;  // this row's partial router-weight gradient
   bool ok = true;
   for (int c = part; c < nch; c += 2) {
     const int g = gbase + c, slot = g % kGuSlots;
@@ -319,14 +324,19 @@ __device__ __forceinline__ bool epilogue_da_ring(const Tile &t, uint32_t tb, int
     tmem_ld_wait();
 #pragma unroll
     for (int i = 0; i < 32; ++i) {  // in place: v1 G -> dU, v2 U -> dG
-      const float da = w * __uint_as_float(r0[i]), gg = v1[i], u = v2[i];
+      const float acc = __uint_as_float(r0[i]), gg = v1[i], u = v2[i];
+      const float da = w * acc;
       const float sg = sigmoidf_(gg);
+      const float silu = gg * sg;
+      gp = fmaf(acc, silu * u, gp);                   // <dy . W_down^T, A>
       v2[i] = da * u * sg * (1.f + gg * (1.f - sg));  // dG
-      v1[i] = da * gg * sg;                           // dU = dA * silu(G)
+      v1[i] = da * silu;                              // dU = dA * silu(G)
     }
     store_rows32(tile, p.o0 + rowoff + col, p.I, nvalid, v2);
     store_rows32(tile, p.o1 + rowoff + col, p.I, nvalid, v1);
   }
+  if (ok && p.g_part && row < t.row_end)
+    p.g_part[static_cast<size_t>(row) * p.g_np + (t.n0 >> 8) * 2 + part] = gp;
   gbase += nch;
   return ok;
 }

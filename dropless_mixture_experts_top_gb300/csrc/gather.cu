@@ -203,6 +203,31 @@ __global__ void __launch_bounds__(kWarps * 32) gather_sum_kernel(const uint4 *__
   }
 }
 
+// Router gradients of token t from g_tj (lane j < k holds g, w, expert of
+// choice j): d_topk_w = g, and d_logits[t, S_tj] = w_j (g_j - sum_i w_i g_i),
+// written as w_j sum_i w_i (g_j - g_i) (the weights sum to one): no
+// cancellation when one weight is close to 1; zero for the other experts.
+__device__ __forceinline__ void router_grads(float myg, float myw, int mye, size_t t, int k, int E,
+                                             float *__restrict__ d_logits, float *__restrict__ d_topk_w) {
+  const int lane = threadIdx.x & 31;
+  if (d_topk_w && lane < k) d_topk_w[t * k + lane] = myg;
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < kMaxTopK; ++i)
+    if (i < k) acc = fmaf(__shfl_sync(0xffffffffu, myw, i), myg - __shfl_sync(0xffffffffu, myg, i), acc);
+  const float mydl = myw * acc;
+  for (int e0 = 0; e0 < E; e0 += 32) {
+    const int e = e0 + lane;
+    float val = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int ej = __shfl_sync(0xffffffffu, mye, j);
+      const float dj = __shfl_sync(0xffffffffu, mydl, j);
+      if (ej == e) val = dj;
+    }
+    if (e < E) d_logits[t * E + e] = val;
+  }
+}
+
 __global__ void __launch_bounds__(kWarps * 32) router_bwd_kernel(
     const uint4 *__restrict__ dy, const uint4 *__restrict__ Y, const int32_t *__restrict__ ros,
     const int32_t *__restrict__ topk_idx, const float *__restrict__ topk_w, uint4 *__restrict__ dyp,
@@ -254,24 +279,29 @@ __global__ void __launch_bounds__(kWarps * 32) router_bwd_kernel(
 #pragma unroll
   for (int j = 0; j < kMaxTopK; ++j)
     if (j == lane) myg = dot[j];
-  if (d_topk_w && lane < k) d_topk_w[sb + lane] = myg;
-  // w_j (g_j - sum_i w_i g_i) written as w_j sum_i w_i (g_j - g_i) (the weights
-  // sum to one): no cancellation when one weight is close to 1.
-  float acc = 0.f;
-#pragma unroll
-  for (int i = 0; i < kMaxTopK; ++i)
-    if (i < k) acc = fmaf(__shfl_sync(0xffffffffu, myw, i), myg - dot[i], acc);
-  const float mydl = myw * acc;
-  for (int e0 = 0; e0 < E; e0 += 32) {
-    const int e = e0 + lane;
-    float val = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const int ej = __shfl_sync(0xffffffffu, mye, j);
-      const float dj = __shfl_sync(0xffffffffu, mydl, j);
-      if (ej == e) val = dj;
-    }
-    if (e < E) d_logits[static_cast<size_t>(t) * E + e] = val;
+  router_grads(myg, myw, mye, static_cast<size_t>(t), k, E, d_logits, d_topk_w);
+}
+
+// d_logits and d_topk_w of a token from g_tj computed by the bf16 dA GEMM's
+// epilogue: g_tj = <dy_t, Y_tj> = <dy_t . W_down^T, A_r>, summed here over the
+// np column partials of row r = row(t,j) in a fixed order.
+__global__ void __launch_bounds__(kWarps * 32) router_grad_kernel(
+    const int32_t *__restrict__ ros, const int32_t *__restrict__ topk_idx, const float *__restrict__ topk_w,
+    const float *__restrict__ g_part, int np, float *__restrict__ d_logits, float *__restrict__ d_topk_w,
+    int T, int E, int k) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const size_t sb = static_cast<size_t>(t) * k;
+  float myg = 0.f, myw = 0.f;
+  int mye = -1;
+  if (lane < k) {
+    const float *gp = g_part + static_cast<size_t>(__ldg(ros + sb + lane)) * np;
+    for (int p = 0; p < np; ++p) myg += __ldg(gp + p);
+    myw = __ldg(topk_w + sb + lane);
+    mye = __ldg(topk_idx + sb + lane);
   }
+  router_grads(myg, myw, mye, static_cast<size_t>(t), k, E, d_logits, d_topk_w);
 }
 
 inline int blocks_for(int T) { return (T + kWarps - 1) / kWarps; }
@@ -356,6 +386,14 @@ cudaError_t launch_permute_quant(const uint16_t *x, const int32_t *row_of_slot, 
 cudaError_t launch_zero_pad_rows(const int32_t *offsets, const int32_t *pad_off, int E, int K, uint8_t *codes,
                                  uint8_t *sf, SfLayout L, cudaStream_t s) {
   zero_pad_rows_kernel<<<E, 256, 0, s>>>(offsets, pad_off, K, codes, sf, L);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_grad(const int32_t *row_of_slot, const int32_t *topk_idx, const float *topk_w,
+                               const float *g_part, int np, float *d_logits, float *d_topk_w, int T, int E, int k,
+                               cudaStream_t s) {
+  router_grad_kernel<<<blocks_for(T), kWarps * 32, 0, s>>>(row_of_slot, topk_idx, topk_w, g_part, np, d_logits,
+                                                           d_topk_w, T, E, k);
   return cudaGetLastError();
 }
 

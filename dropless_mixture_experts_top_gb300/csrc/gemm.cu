@@ -84,6 +84,8 @@ struct Params {
   const int32_t *offsets;
   const uint16_t *G, *U;  // dSwiGLU epilogue inputs
   const float *w_row;     // router weight of each permuted row
+  float *g_part;          // dA: partial router-weight gradients [M][g_np] (or null)
+  int g_np;               // dA: partials per row (2 per 256-column tile)
   uint16_t *o0, *o1, *o2, *o3;
   float *of;   // router projection: fp32 output
   int n_out;   // router projection: output columns (E)
@@ -557,6 +559,8 @@ cudaError_t launch_mode(const GemmArgs &a, cudaStream_t s) {
   p.o2 = a.o2;
   p.o3 = a.o3;
   p.w_row = a.w_row;
+  p.g_part = a.g_part;
+  p.g_np = 2 * ((a.I + 255) / 256);
   p.status = a.status;
   const uint64_t M = static_cast<uint64_t>(a.M_rows), H = a.H, I = a.I, E = a.E;
   // router modes: a.E is the router's output width, the GEMM sees one expert

@@ -46,9 +46,15 @@ cudaError_t launch_permute_rows(const uint16_t *x, const int32_t *row_of_slot, u
 // out[t] = sum_j w[t,j] * rows[row_of_slot[t,j]]   (w == nullptr: plain sum)
 cudaError_t launch_gather_sum(const uint16_t *rows, const int32_t *row_of_slot, const float *w,
                               uint16_t *out, int T, int H, int k, cudaStream_t s);
-// dy_perm[row(t,j)] = dy[t]; g[t,j] = <dy[t], Y[row]>; d_logits; d_topk_w (nullable)
+// router projection: fp32 -> bf16 (nearest even), n % 4 == 0; offsets {0, T}
 cudaError_t launch_to_bf16(const float *in, uint16_t *out, int64_t n, cudaStream_t s);
 cudaError_t launch_one_segment(int32_t *offsets, int T, cudaStream_t s);
+// d_logits and d_topk_w from g computed in the bf16 dA epilogue: g[r] = the sum
+// of the np partials g_part[r * np + p]
+cudaError_t launch_router_grad(const int32_t *row_of_slot, const int32_t *topk_idx, const float *topk_w,
+                               const float *g_part, int np, float *d_logits, float *d_topk_w, int T, int E, int k,
+                               cudaStream_t s);
+// dy_perm[row(t,j)] = dy[t]; g[t,j] = <dy[t], Y[row]>; d_logits; d_topk_w (nullable)
 cudaError_t launch_router_bwd(const uint16_t *dy, const uint16_t *Y, const int32_t *row_of_slot,
                               const int32_t *topk_idx, const float *topk_w, uint16_t *dy_perm,
                               float *d_logits, float *d_topk_w, int T, int H, int E, int k,
@@ -80,6 +86,7 @@ struct GemmArgs {
   const uint16_t *dy_perm;  // dy rows in permuted order [M,H]
   const uint16_t *dG, *dU;
   const float *w_row;       // [M] router weight per permuted row
+  float *g_part;            // dA: the router weight's gradient, 2 partials per 256-column tile [M][np]
   // outputs (device, bf16)
   uint16_t *o0, *o1, *o2, *o3;
   // router projection: x [T,H], W_r [H,E], d_logits as bf16 [T,E]; fp32 output, its columns

@@ -17,7 +17,8 @@ from tests import gpu_util as G
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 WORKLOADS = ["qwen3_30b_a3b_layer_t16384", "qwen3_30b_a3b_layer_t16384_zipf",
-             "qwen3_235b_a22b_layer_t16384", "qwen3_30b_a3b_layer_t16384_fp8_bwd"]
+             "qwen3_235b_a22b_layer_t16384", "qwen3_30b_a3b_layer_t16384_fp8_bwd",
+             "qwen3_30b_a3b_layer_t16384_mxfp8"]
 
 
 def sample_tokens(T, counts, idx, rng, n=64):
@@ -62,26 +63,31 @@ def run_workload(name):
 @pytest.mark.parametrize("name", WORKLOADS)
 def test_fullsize_sampled_parity(name):
     w, shape, inp, layer, out, grads = run_workload(name)
-    quant = w.precision == "fp8_bwd"
+    quant = w.precision in ("fp8_bwd", "mxfp8")
+    fq = w.precision == "mxfp8"  # the forward quantised too
     tol = dict(rel_l2=G.FP8_REL_L2, max_rel=G.FP8_MAX_REL) if quant else {}
+    ftol = tol if fq else {}
     qW = O.quant_weights(inp["W_gate"], inp["W_up"], inp["W_down"]) if quant else None
+    fW = O.quant_weights_fwd(inp["W_gate"], inp["W_up"], inp["W_down"]) if fq else None
     idx, wts, counts, offsets, ros, sor = G.check_routing(shape, inp, layer)
     assert counts.sum() == shape.T * shape.k
     if w.routing == "zipf":
         assert (counts == 0).sum() >= 1 and counts.max() > 8 * counts[counts > 0].min()
     rng = np.random.default_rng(7)
     toks = sample_tokens(shape.T, counts, idx, rng)
-    ref_out = O.forward(shape, inp["x"], idx, wts, inp["W_gate"], inp["W_up"], inp["W_down"], tokens=toks)
-    G.close("out[sampled tokens]", G.bf(out[torch.from_numpy(toks).cuda()]), ref_out)
+    ref_out = O.forward(shape, inp["x"], idx, wts, inp["W_gate"], inp["W_up"], inp["W_down"], tokens=toks,
+                        fwd_quant=fq, fW=fW)
+    G.close("out[sampled tokens]", G.bf(out[torch.from_numpy(toks).cuda()]), ref_out, **ftol)
     dx, dl, gd = O.backward_tokens(shape, inp["x"], inp["logits"], idx, wts, inp["W_gate"], inp["W_up"],
-                                   inp["W_down"], inp["dy"], tokens=toks, quant=quant, qW=qW)
+                                   inp["W_down"], inp["dy"], tokens=toks, quant=quant, qW=qW, fwd_quant=fq,
+                                   fW=fW)
     tk = torch.from_numpy(toks).cuda()
     G.close("dx[sampled tokens]", G.bf(grads["dx"][tk]), dx, **tol)
-    G.close("d_logits[sampled tokens]", grads["d_logits"][tk].cpu().numpy(), dl)
-    G.close("d_topk_w[sampled tokens]", grads["d_topk_w"][tk].cpu().numpy(), gd)
+    G.close("d_logits[sampled tokens]", grads["d_logits"][tk].cpu().numpy(), dl, **ftol)
+    G.close("d_topk_w[sampled tokens]", grads["d_topk_w"][tk].cpu().numpy(), gd, **ftol)
     which, ee, rr, cc, uni = sample_dw(shape, counts, rng)
     ref = O.dw_elements(shape, inp["x"], idx, wts, inp["W_gate"], inp["W_up"], inp["W_down"], inp["dy"],
-                        which, ee, rr, cc, quant=quant, qW=qW)
+                        which, ee, rr, cc, quant=quant, qW=qW, fwd_quant=fq, fW=fW)
     names = ["dW_gate", "dW_up", "dW_down"]
     for wh in range(3):
         m = which == wh
