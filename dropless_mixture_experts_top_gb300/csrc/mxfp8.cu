@@ -92,16 +92,96 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t *__restr
 
 // Token-axis quantisation, output transposed: codes [C][Mpad] (tokens
 // contiguous).  A block takes 128 padded rows (one expert's, as segments are
-// 128-aligned) x 64 columns: coalesced 128-byte row loads into shared memory
-// (16-byte chunks XOR-swizzled by row, so that both a column walk and a row
-// walk are free of bank conflicts), one thread per (column, 32-token block)
-// quantises down the column into a shared output tile (64 rows of 128 codes,
-// rows padded to 144 bytes against bank conflicts), then the tile leaves as
-// full 128-byte rows.  Optionally the same tile is also quantised along its
-// rows (one thread per (row, 32-column block)) into the padded row space, so
-// an operand needed on both axes (dy) is read once.  Tiles past the padded
-// total are skipped (never read).
+// 128-aligned) and walks their columns in 64-wide tiles.  The tiles are staged
+// in shared memory by cp.async, kQcRing of them in flight (16-byte chunks
+// XOR-swizzled by row, so that both a column walk and a row walk are free of
+// bank conflicts); one thread per (column, 32-token block) quantises down the
+// column into a shared output tile (64 rows of 128 codes, rows padded to 144
+// bytes against bank conflicts), which leaves as full 128-byte rows.
+// Optionally the same tile is also quantised along its rows (one thread per
+// (row, 32-column block)) into the padded row space, so an operand needed on
+// both axes (dy) is read once.  Tiles past the padded total are skipped.
 constexpr int kQcRows = 128, kQcCols = 64, kQcThreads = 256;
+constexpr int kQcRing = 4;                         // staged tiles in flight per block
+constexpr int kQcTileElems = kQcRows * kQcCols;   // bf16 per staged tile (16 KB)
+constexpr int kQcOutStride = kQcRows + 16;         // bytes per output row in shared memory
+constexpr int kQcSmem = kQcRing * kQcTileElems * 2 + kQcCols * kQcOutStride;  // dynamic shared memory
+constexpr int kQcLoads = (kQcRows * kQcCols / 8) / kQcThreads;  // 16-byte pieces per thread per tile
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most n of this thread's cp.async groups are still pending (n < kQcRing).
+__device__ __forceinline__ void cp_async_wait_pending(int n) {
+  if (n <= 0)
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+  else if (n == 1)
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+  else if (n == 2)
+    asm volatile("cp.async.wait_group 2;" ::: "memory");
+  else
+    asm volatile("cp.async.wait_group 3;" ::: "memory");
+}
+
+// Element (r, c) of a staged tile.
+__device__ __forceinline__ int qc_idx(int r, int c) { return r * kQcCols + (((c >> 3) ^ (r & 7)) << 3) + (c & 7); }
+
+// Issue one 128 x 64 tile: source row r at row_ptr(r) (nullptr: a zero row),
+// columns c0 .. c0 + 63; one cp.async group per call.
+template <class RowPtr>
+__device__ __forceinline__ void qc_issue(uint16_t *dst, int c0, const RowPtr &row_ptr) {
+#pragma unroll
+  for (int j = 0; j < kQcLoads; ++j) {
+    const int i = threadIdx.x + j * kQcThreads;
+    const int r = i >> 3, part = i & 7;
+    uint16_t *d = dst + r * kQcCols + ((part ^ (r & 7)) << 3);
+    const uint16_t *sp = row_ptr(r);
+    if (sp)
+      cp_async16(d, sp + c0 + part * 8);
+    else
+      *reinterpret_cast<uint4 *>(d) = make_uint4(0, 0, 0, 0);
+  }
+  cp_async_commit();
+}
+
+// 32 bf16 values of a staged tile: row r, columns 32 bb .. 32 bb + 31.
+__device__ __forceinline__ void qc_row32(const uint16_t *tile, int r, int bb, float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 w = *reinterpret_cast<const uint4 *>(tile + r * kQcCols + (((4 * bb + q) ^ (r & 7)) << 3));
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      v[8 * q + 2 * h] = bf16_lo(ww[h]);
+      v[8 * q + 2 * h + 1] = bf16_hi(ww[h]);
+    }
+  }
+}
+
+// 32 bf16 values of a staged tile down column c: rows 32 b .. 32 b + 31.
+__device__ __forceinline__ void qc_col32(const uint16_t *tile, int c, int b, float (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(static_cast<uint32_t>(tile[qc_idx(32 * b + i, c)]) << 16);
+}
+
+// The column-tile walk shared by both transposing quantisers: tiles c0 =
+// first, first + step, ... < C, kQcRing - 1 of them issued ahead; work(tile,
+// c0) runs on each once it has landed, between two block barriers.
+template <class RowPtr, class Work>
+__device__ __forceinline__ void qc_walk(uint16_t *ring, int first, int step, int C, const RowPtr &row_ptr,
+                                        const Work &work) {
+  const int nt = first < C ? (C - first + step - 1) / step : 0;
+  for (int i = 0; i < kQcRing - 1 && i < nt; ++i) qc_issue(ring + i * kQcTileElems, first + i * step, row_ptr);
+  for (int it = 0; it < nt; ++it) {
+    const int ahead = it + kQcRing - 1;
+    if (ahead < nt) qc_issue(ring + (ahead % kQcRing) * kQcTileElems, first + ahead * step, row_ptr);
+    cp_async_wait_pending(min(nt - 1, ahead) - it);  // this tile's group has landed
+    __syncthreads();
+    work(ring + (it % kQcRing) * kQcTileElems, first + it * step);
+    __syncthreads();  // the tile's slot and the output tile are reused
+  }
+}
 
 __global__ void __launch_bounds__(kQcThreads, 3) quant_cols_kernel(const uint16_t *__restrict__ src, int C,
                                                                 int Mpad,
@@ -110,10 +190,10 @@ __global__ void __launch_bounds__(kQcThreads, 3) quant_cols_kernel(const uint16_
                                                                 uint8_t *__restrict__ codes,
                                                                 uint8_t *__restrict__ sf, SfLayout L,
                                                                 RowCodes rows) {
+  extern __shared__ __align__(16) uint8_t qc_smem[];
+  uint16_t *ring = reinterpret_cast<uint16_t *>(qc_smem);
+  uint8_t *otile = qc_smem + kQcRing * kQcTileElems * 2;
   __shared__ int s_pad[kMaxExperts + 1];
-  __shared__ __align__(16) uint16_t tile[kQcRows * kQcCols];
-  constexpr int kOutStride = kQcRows + 16;  // bytes per output row in shared memory
-  __shared__ __align__(16) uint8_t otile[kQcCols * kOutStride];
   __shared__ int s_seg[3];  // first source row, valid rows of this tile, skip flag
   const int prow0 = blockIdx.x * kQcRows;
   for (int e = threadIdx.x; e <= E; e += kQcThreads) s_pad[e] = __ldg(pad_off + e);
@@ -133,68 +213,32 @@ __global__ void __launch_bounds__(kQcThreads, 3) quant_cols_kernel(const uint16_
   __syncthreads();
   if (s_seg[2]) return;
   const int row0 = s_seg[0], nvalid = s_seg[1];
-  // the row tile's setup is shared by every column tile this block takes; the
-  // next column tile's loads are issued before the current one is quantised
-  constexpr int kLoads = (kQcRows * kQcCols / 8) / kQcThreads;  // 16-byte pieces per thread
-  uint4 nxt[kLoads];
-  auto load_tile = [&](int c0) {
-#pragma unroll
-    for (int j = 0; j < kLoads; ++j) {
-      const int i = threadIdx.x + j * kQcThreads;
-      const int r = i >> 3, part = i & 7;
-      nxt[j] = r < nvalid ? __ldg(reinterpret_cast<const uint4 *>(src + static_cast<size_t>(row0 + r) * C + c0) +
-                                  part)
-                          : make_uint4(0, 0, 0, 0);
-    }
+  auto row_ptr = [&](int r) -> const uint16_t * {
+    return r < nvalid ? src + static_cast<size_t>(row0 + r) * C : nullptr;
   };
-  const int cstep = gridDim.y * kQcCols;
-  if (blockIdx.y * kQcCols < C) load_tile(blockIdx.y * kQcCols);
-  for (int c0 = blockIdx.y * kQcCols; c0 < C; c0 += cstep) {
-#pragma unroll
-    for (int j = 0; j < kLoads; ++j) {
-      const int i = threadIdx.x + j * kQcThreads;
-      const int r = i >> 3, part = i & 7;
-      *reinterpret_cast<uint4 *>(tile + r * kQcCols + ((part ^ (r & 7)) << 3)) = nxt[j];
-    }
-    if (c0 + cstep < C) load_tile(c0 + cstep);
-    __syncthreads();
+  qc_walk(ring, blockIdx.y * kQcCols, gridDim.y * kQcCols, C, row_ptr, [&](const uint16_t *tile, int c0) {
     if (rows.codes) {  // along the rows: thread = (row, 32-column block); zero rows past the count
       const int r = threadIdx.x >> 1, bb = threadIdx.x & 1;
       float v[32];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 w = *reinterpret_cast<const uint4 *>(tile + r * kQcCols + (((4 * bb + q) ^ (r & 7)) << 3));
-        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          v[8 * q + 2 * h] = bf16_lo(ww[h]);
-          v[8 * q + 2 * h + 1] = bf16_hi(ww[h]);
-        }
-      }
+      qc_row32(tile, r, bb, v);
       const int prow = prow0 + r, kb = (c0 >> 5) + bb;
       rows.sf[atom_byte(prow, kb, C, rows.L)] =
           quant32(v, reinterpret_cast<uint4 *>(rows.codes + static_cast<size_t>(prow) * C + c0 + 32 * bb));
     }
     const int cc = threadIdx.x % kQcCols, b = threadIdx.x / kQcCols;  // 4 blocks of 32 tokens
     float v[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int r = 32 * b + i;
-      v[i] = __uint_as_float(static_cast<uint32_t>(tile[r * kQcCols + (((cc >> 3) ^ (r & 7)) << 3) + (cc & 7)])
-                             << 16);
-    }
-    const int c = c0 + cc, o0 = prow0 + 32 * b;
-    sf[atom_byte(c, o0 >> 5, Mpad, L)] = quant32(v, reinterpret_cast<uint4 *>(otile + cc * kOutStride + 32 * b));
+    qc_col32(tile, cc, b, v);
+    sf[atom_byte(c0 + cc, (prow0 >> 5) + b, Mpad, L)] =
+        quant32(v, reinterpret_cast<uint4 *>(otile + cc * kQcOutStride + 32 * b));
     __syncthreads();
 #pragma unroll
     for (int j = 0; j < (kQcCols * kQcRows / 16) / kQcThreads; ++j) {
       const int i = threadIdx.x + j * kQcThreads;
       const int r = i >> 3, part = i & 7;  // output row (column c0 + r), 16-byte piece
       *reinterpret_cast<uint4 *>(codes + static_cast<size_t>(c0 + r) * Mpad + prow0 + part * 16) =
-          *reinterpret_cast<const uint4 *>(otile + r * kOutStride + part * 16);
+          *reinterpret_cast<const uint4 *>(otile + r * kQcOutStride + part * 16);
     }
-    __syncthreads();  // otile and tile are rewritten by the next column tile
-  }
+  });
 }
 
 // Weights quantised along their middle axis (the mxfp8 forward GEMMs' K),
@@ -204,80 +248,45 @@ __global__ void __launch_bounds__(kQcThreads, 3) quant_cols_kernel(const uint16_
 // half * 32 + c % 32 (W_gate half 0, W_up half 1: every 64 B rows hold 32
 // gate columns then the same 32 up columns).  Optionally the same staged tile
 // is also quantised along C, row by row (the backward GEMMs' weight operand,
-// codes [E * R, C]), so each weight is read once for both.  Same staging as
-// the token-axis quantiser: 128 x 64 tiles (chunks XOR-swizzled by row), the
-// next column tile prefetched into registers, one thread per (column, 32-row
-// block), codes leaving through a shared output tile as 128-byte rows.
+// codes [E * R, C]), so each weight is read once for both.  Same staging and
+// column walk as the token-axis quantiser.
 __global__ void __launch_bounds__(kQcThreads, 3) quant_wT_kernel(const uint16_t *__restrict__ src, int R,
                                                                  int C, int interleave, int half,
                                                                  uint8_t *__restrict__ codes,
                                                                  uint8_t *__restrict__ sf, SfLayout L,
                                                                  RowCodes rows) {
-  __shared__ __align__(16) uint16_t tile[kQcRows * kQcCols];
-  constexpr int kOutStride = kQcRows + 16;
-  __shared__ __align__(16) uint8_t otile[kQcCols * kOutStride];
+  extern __shared__ __align__(16) uint8_t qc_smem[];
+  uint16_t *ring = reinterpret_cast<uint16_t *>(qc_smem);
+  uint8_t *otile = qc_smem + kQcRing * kQcTileElems * 2;
   const int grow0 = blockIdx.x * kQcRows;  // first source row (of E * R)
   const int e = grow0 / R, r0 = grow0 - e * R;
   auto out_row = [&](int c) {
     return interleave ? e * 2 * C + (c >> 5) * 64 + half * 32 + (c & 31) : e * C + c;
   };
-  constexpr int kLoads = (kQcRows * kQcCols / 8) / kQcThreads;
-  uint4 nxt[kLoads];
-  auto load_tile = [&](int c0) {
-#pragma unroll
-    for (int j = 0; j < kLoads; ++j) {
-      const int i = threadIdx.x + j * kQcThreads;
-      nxt[j] = __ldg(reinterpret_cast<const uint4 *>(src + static_cast<size_t>(grow0 + (i >> 3)) * C + c0) + (i & 7));
-    }
-  };
-  const int cstep = gridDim.y * kQcCols;
-  if (blockIdx.y * kQcCols < C) load_tile(blockIdx.y * kQcCols);
-  for (int c0 = blockIdx.y * kQcCols; c0 < C; c0 += cstep) {
-#pragma unroll
-    for (int j = 0; j < kLoads; ++j) {
-      const int i = threadIdx.x + j * kQcThreads;
-      const int r = i >> 3, part = i & 7;
-      *reinterpret_cast<uint4 *>(tile + r * kQcCols + ((part ^ (r & 7)) << 3)) = nxt[j];
-    }
-    if (c0 + cstep < C) load_tile(c0 + cstep);
-    __syncthreads();
+  auto row_ptr = [&](int r) -> const uint16_t * { return src + static_cast<size_t>(grow0 + r) * C; };
+  qc_walk(ring, blockIdx.y * kQcCols, gridDim.y * kQcCols, C, row_ptr, [&](const uint16_t *tile, int c0) {
     if (rows.codes) {  // along C: thread = (row, 32-column block)
       const int r = threadIdx.x >> 1, bb = threadIdx.x & 1;
       float v[32];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 w = *reinterpret_cast<const uint4 *>(tile + r * kQcCols + (((4 * bb + q) ^ (r & 7)) << 3));
-        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          v[8 * q + 2 * h] = bf16_lo(ww[h]);
-          v[8 * q + 2 * h + 1] = bf16_hi(ww[h]);
-        }
-      }
+      qc_row32(tile, r, bb, v);
       const int grow = grow0 + r;
       rows.sf[atom_byte(grow, (c0 >> 5) + bb, C, rows.L)] =
           quant32(v, reinterpret_cast<uint4 *>(rows.codes + static_cast<size_t>(grow) * C + c0 + 32 * bb));
     }
     const int cc = threadIdx.x % kQcCols, b = threadIdx.x / kQcCols;  // 4 blocks of 32 rows
     float v[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int r = 32 * b + i;
-      v[i] = __uint_as_float(static_cast<uint32_t>(tile[r * kQcCols + (((cc >> 3) ^ (r & 7)) << 3) + (cc & 7)])
-                             << 16);
-    }
+    qc_col32(tile, cc, b, v);
     sf[atom_byte(out_row(c0 + cc), (r0 >> 5) + b, R, L)] =
-        quant32(v, reinterpret_cast<uint4 *>(otile + cc * kOutStride + 32 * b));
+        quant32(v, reinterpret_cast<uint4 *>(otile + cc * kQcOutStride + 32 * b));
     __syncthreads();
 #pragma unroll
     for (int j = 0; j < (kQcCols * kQcRows / 16) / kQcThreads; ++j) {
       const int i = threadIdx.x + j * kQcThreads;
       const int r = i >> 3, part = i & 7;  // output row (column c0 + r), 16-byte piece
       *reinterpret_cast<uint4 *>(codes + static_cast<size_t>(out_row(c0 + r)) * R + r0 + part * 16) =
-          *reinterpret_cast<const uint4 *>(otile + r * kOutStride + part * 16);
+          *reinterpret_cast<const uint4 *>(otile + r * kQcOutStride + part * 16);
     }
-    __syncthreads();
-  }
+  });
 }
 
 // pad_off[e] = sum over e' < e of ceil(count/128)*128; pad_off[E] = padded total.
@@ -321,7 +330,13 @@ cudaError_t launch_quant_cols(const uint16_t *src, int C, int Mpad, const int32_
                               RowCodes rows, cudaStream_t s) {
   const int col_blocks = C / kQcCols < 4 ? C / kQcCols : 4;  // each loops over C / (64 * 4) column tiles
   const dim3 grid(static_cast<unsigned>(Mpad / kQcRows), static_cast<unsigned>(col_blocks));
-  quant_cols_kernel<<<grid, kQcThreads, 0, s>>>(src, C, Mpad, offsets, pad_off, E, codes, sf, L, rows);
+  static bool attr_set = false;  // dynamic shared memory above 48 KB (set once per process)
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(quant_cols_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQcSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  quant_cols_kernel<<<grid, kQcThreads, kQcSmem, s>>>(src, C, Mpad, offsets, pad_off, E, codes, sf, L, rows);
   return cudaGetLastError();
 }
 
@@ -329,7 +344,13 @@ cudaError_t launch_quant_wT(const uint16_t *W, int E, int R, int C, int interlea
                             uint8_t *codes, uint8_t *sf, SfLayout L, RowCodes rows, cudaStream_t s) {
   const int col_blocks = C / kQcCols < 4 ? C / kQcCols : 4;
   const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(E) * R / kQcRows), static_cast<unsigned>(col_blocks));
-  quant_wT_kernel<<<grid, kQcThreads, 0, s>>>(W, R, C, interleave, half, codes, sf, L, rows);
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(quant_wT_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQcSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  quant_wT_kernel<<<grid, kQcThreads, kQcSmem, s>>>(W, R, C, interleave, half, codes, sf, L, rows);
   return cudaGetLastError();
 }
 
