@@ -1,8 +1,11 @@
 // epilogue.cuh -- epilogues of the grouped GEMMs: read one warp's 32 TMEM lanes
 // of a 128 x 256 fp32 accumulator and write the layer's bf16 outputs (fused
-// SwiGLU for the forward gate/up GEMM, fused dSwiGLU for dA).  Shared by the
-// bf16 GEMM engine (gemm.cu) and the MXFP8 one (gemm_mx.cu).  `P` is any
-// parameter struct with the fields used below (H, I, G, U, w_row, o0..o3).
+// SwiGLU for the forward gate/up GEMM, fused dSwiGLU for dA through the G/U
+// ring, plain stores for the others, the router projection's fp32 modes).
+// epilogue_tile serves both GEMM engines (gemm.cu, and gemm_mx.cu for dX, down
+// and the weight gradients; the MXFP8 dA and gate/up epilogues, which also
+// quantise, live in gemm_mx.cu).  `P` is any parameter struct with the fields
+// used below.
 //
 // A warp owns 32 rows (one per lane, as tcgen05.ld 32x32b delivers them) and
 // walks its columns in 32-column chunks.  Row-major global memory is touched
@@ -150,38 +153,6 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, uint32_t tb, int ri
 #pragma unroll
       for (int i = 0; i < 32; ++i) v0[i] = __uint_as_float(r0[i]);
       store_rows32(tile, p.o0 + static_cast<size_t>(row0) * p.H + col, p.H, nvalid, v0);
-    }
-  } else if constexpr (MODE == kBwdDA) {
-    const int row = t.m0 + rit, row0 = row - lane;
-    const int nvalid = clamp_rows(t.row_end - row0);
-    const float w = row < t.row_end ? __ldg(p.w_row + row) : 0.f;  // dA = w * (dy . W_down^T)
-    const size_t rowoff = static_cast<size_t>(row0) * p.I;
-    // G and U of the next 32-column chunk are loaded while this chunk is computed
-    uint4 gq[4], uq[4];
-    if (t.n0 + 32 * cb < p.I) {
-      load_rows32(p.G + rowoff + t.n0 + 32 * cb, p.I, nvalid, gq);
-      load_rows32(p.U + rowoff + t.n0 + 32 * cb, p.I, nvalid, uq);
-    }
-    for (int c = cb; c < ce; ++c) {
-      const int col = t.n0 + 32 * c;
-      if (col >= p.I) break;
-      rows32_to_lanes(tile, gq, v1);
-      rows32_to_lanes(tile, uq, v2);
-      if (c + 1 < ce && col + 32 < p.I) {
-        load_rows32(p.G + rowoff + col + 32, p.I, nvalid, gq);
-        load_rows32(p.U + rowoff + col + 32, p.I, nvalid, uq);
-      }
-      tmem_ld32(tb + 32 * c, r0);
-      tmem_ld_wait();
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {  // in place: v1 G -> dU, v2 U -> dG
-        const float da = w * __uint_as_float(r0[i]), g = v1[i], u = v2[i];
-        const float s = sigmoidf_(g);
-        v2[i] = da * u * s * (1.f + g * (1.f - s));  // dG
-        v1[i] = da * g * s;                          // dU = dA * silu(G)
-      }
-      store_rows32(tile, p.o0 + rowoff + col, p.I, nvalid, v2);
-      store_rows32(tile, p.o1 + rowoff + col, p.I, nvalid, v1);
     }
   } else if constexpr (MODE == kBwdDWDown) {
     const int i_row0 = t.m0 + rit - lane;
