@@ -62,19 +62,22 @@ def test_all_tokens_one_expert_tail():
     G.check_full(shape, inp, layer, out, grads)
 
 
-def test_zero_tokens():
-    shape = MoEShape(T=0, H=128, I=64, E=4, k=2)
-    layer = moe.MoELayer(shape)
+PRECISIONS = ["bf16", "fp8_bwd", "mxfp8"]
+
+
+@pytest.mark.parametrize("precision", PRECISIONS)
+def test_zero_tokens(precision):
+    shape = MoEShape(T=0, H=128, I=128, E=4, k=2)
+    layer = moe.MoELayer(shape, precision=precision)
     dev = "cuda"
     logits = torch.empty((0, 4), dtype=torch.float32, device=dev)
     x = torch.empty((0, 128), dtype=torch.int16, device=dev)
-    W = [torch.ones((4, 128, 64), dtype=torch.int16, device=dev)] * 2 + \
-        [torch.ones((4, 64, 128), dtype=torch.int16, device=dev)]
+    W = [torch.ones((4, 128, 128), dtype=torch.int16, device=dev)] * 3
     layer.route(logits)
     out = layer.forward(x, *W)
-    grads = {"dx": x.clone(), "dW_gate": torch.full((4, 128, 64), 7, dtype=torch.int16, device=dev),
-             "dW_up": torch.full((4, 128, 64), 7, dtype=torch.int16, device=dev),
-             "dW_down": torch.full((4, 64, 128), 7, dtype=torch.int16, device=dev),
+    grads = {"dx": x.clone(), "dW_gate": torch.full((4, 128, 128), 7, dtype=torch.int16, device=dev),
+             "dW_up": torch.full((4, 128, 128), 7, dtype=torch.int16, device=dev),
+             "dW_down": torch.full((4, 128, 128), 7, dtype=torch.int16, device=dev),
              "d_logits": logits.clone(), "d_topk_w": torch.empty((0, 2), dtype=torch.float32, device=dev)}
     layer.backward(x, x, *W, grads=grads)
     torch.cuda.synchronize()
@@ -106,21 +109,23 @@ def test_nonfinite_logits_flagged_not_trapped():
     assert moe.get_device_status(layer.route_scratch) == 0
 
 
-def test_deterministic_bitwise():
-    shape = MoEShape(T=700, H=256, I=192, E=6, k=2)
+@pytest.mark.parametrize("precision", PRECISIONS)
+def test_deterministic_bitwise(precision):
+    shape = MoEShape(T=700, H=256, I=256, E=6, k=2)
     inp = synth.make_inputs_shape(shape, 53)
-    _, out1, g1 = G.run_layer(shape, inp)
-    _, out2, g2 = G.run_layer(shape, inp)
+    _, out1, g1 = G.run_layer(shape, inp, precision=precision)
+    _, out2, g2 = G.run_layer(shape, inp, precision=precision)
     assert torch.equal(out1, out2)
     for n in g1:
         assert torch.equal(g1[n], g2[n]), n
 
 
-def test_cuda_graph_capture_and_replay_with_new_routing():
+@pytest.mark.parametrize("precision", PRECISIONS)
+def test_cuda_graph_capture_and_replay_with_new_routing(precision):
     shape = MoEShape(T=512, H=128, I=128, E=8, k=2)
     inp = synth.make_inputs_shape(shape, 59)
     t = G.to_dev(inp)
-    layer = moe.MoELayer(shape)
+    layer = moe.MoELayer(shape, precision=precision)
     s = torch.cuda.Stream()
     out = torch.empty((shape.T, shape.H), dtype=torch.int16, device="cuda")
     grads = None
@@ -142,4 +147,4 @@ def test_cuda_graph_capture_and_replay_with_new_routing():
     t["logits"].copy_(torch.from_numpy(lg).cuda())
     g.replay()
     torch.cuda.synchronize()
-    G.check_full(shape, inp2, layer, out, grads)
+    G.check_full(shape, inp2, layer, out, grads, precision=precision)
