@@ -100,6 +100,35 @@ def kernel_work(shape):
     }
 
 
+def gemm_bytes(shape):
+    """Algorithmic HBM bytes per launch of each grouped GEMM: every operand read
+    once and every output written once (bf16 2 B; MXFP8 one code byte per element
+    plus one scale byte per 32).  Against the measured HBM bandwidth this gives a
+    GEMM's second roof: the one that binds is the larger of flops / tensor peak and
+    bytes / HBM bandwidth (the fused dSwiGLU GEMM, which reads G and U and writes
+    dG and dU, is HBM-bound at the 30B shape)."""
+    T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
+    M = float(T * k)
+    W = float(E) * H * I  # one expert weight tensor's elements
+    c = 1 + 1 / 32
+    np_ = 2 * ((I + 255) // 256)
+    return {
+        "gemm_gateup_swiglu": M * H * 2 + 2 * W * 2 + 4 * M * I * 2,
+        "gemm_down": M * I * 2 + W * 2 + M * H * 2,
+        "gemm_dA_dswiglu": M * H * 2 + W * 2 + 2 * M * I * 2 + 2 * M * I * 2 + M * np_ * 4,
+        "gemm_dX": 2 * M * I * 2 + 2 * W * 2 + M * H * 2,
+        "gemm_dW_down": M * I * 2 + M * H * 2 + W * 2,
+        "gemm_dW_gateup": M * H * 2 + 2 * M * I * 2 + 2 * W * 2,
+        "mx_gemm_gateup_swiglu": M * H * c + 2 * W * c + 4 * M * I * 2 + M * I * c,
+        "mx_gemm_down": M * I * c + W * c + M * H * 2,
+        # codes of dG and dU along I and along tokens
+        "mx_gemm_dA_dswiglu": M * H * c + W * c + 2 * M * I * 2 + 4 * M * I * c,
+        "mx_gemm_dX": 2 * M * I * c + 2 * W * c + M * H * 2,
+        "mx_gemm_dW_down": M * I * c + M * H * c + W * 2,
+        "mx_gemm_dW_gateup": M * H * c + 2 * M * I * c + 2 * W * 2,
+    }
+
+
 def kernel_source(label):
     """The .cu file that defines the kernel behind a timing label."""
     if label.startswith("mx_gemm_"):
@@ -464,7 +493,6 @@ def run_ours(args):
     with torch.cuda.stream(stream):
         for i in range(K):
             n_starts[i].record(stream)
-            ev_mid = torch.cuda.Event(enable_timing=True)
             step()
             n_ends[i].record(stream)
     torch.cuda.synchronize()
@@ -504,6 +532,7 @@ def run_ours(args):
 
     peaks, peak_src = load_peaks()
     work = kernel_work(shape)
+    gbytes = gemm_bytes(shape)
     fwd_fl, bwd_fl = shape.gemm_flops()
     kernels = {}
     for lab, ts in kern.items():
@@ -517,6 +546,12 @@ def run_ours(args):
             ach, pk, u = amount / (avg * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
         kernels[lab] = {"launches": len(ts), "avg_ms": avg, "share": sum(ts) / sum(sum(v) for v in kern.values()),
                         "bound": bound, "achieved": ach, "unit": u, "peak": pk, "frac": ach / pk}
+        if lab in gbytes:  # a GEMM's HBM roof beside its tensor roof; the larger floor binds
+            gb = gbytes[lab] / (avg * 1e-3) / 1e9
+            t_tensor, t_hbm = amount / (pk * 1e12), gbytes[lab] / (peaks["hbm_gbs"] * 1e9)
+            kernels[lab].update({"hbm_bytes": gbytes[lab], "hbm_achieved_gbs": gb, "hbm_frac": gb / peaks["hbm_gbs"],
+                                 "binding_roof": "tensor" if t_tensor >= t_hbm else "hbm",
+                                 "binding_frac": max(t_tensor, t_hbm) / (avg * 1e-3)})
     top = max(kernels, key=lambda n: kernels[n]["share"])
     kt = kernels[top]
     src = {"tensor": "bf16 burst", "tensor_fp8": f"bf16 burst x {FP8_OVER_BF16:g} (nominal fp8/bf16 ratio)",

@@ -29,13 +29,13 @@ void *tensor_map_encoder() {
 
 namespace {
 
-constexpr size_t kHeader = 256;  // status word (offset 0) + route ticket (offset 4)
+constexpr size_t kHeader = 256;  // status word at offset 0
 
 inline size_t align256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
 
 struct Layout {
   // route scratch
-  size_t r_lrank, r_hist, r_base, r_total;
+  size_t r_lrank, r_hist, r_total;
   // saved
   size_t s_xperm, s_G, s_U, s_A, s_Y, s_Aw, s_total;
   // forward scratch
@@ -83,8 +83,6 @@ Layout layout_of(const moe_config *c) {
   L.r_lrank = o;
   o += align256(M * 4);
   L.r_hist = o;
-  o += align256(nblk * E * 4);
-  L.r_base = o;
   o += align256(nblk * E * 4);
   L.r_total = o;
   o = 0;
@@ -552,8 +550,6 @@ moe_status moe_route(const moe_config *cfg, const float *logits, const moe_routi
   a.w_row = r->w_row;
   a.lrank = reinterpret_cast<int32_t *>(sc + L.r_lrank);
   a.hist = reinterpret_cast<int32_t *>(sc + L.r_hist);
-  a.block_base = reinterpret_cast<int32_t *>(sc + L.r_base);
-  a.ticket = reinterpret_cast<uint32_t *>(sc + 4);
   a.status = reinterpret_cast<int32_t *>(sc);
   MOE_TRY(timed("route_topk", s, [&] { return launch_route_topk(a, s); }));
   MOE_TRY(timed("route_index", s, [&] { return launch_route_index(a, s); }));

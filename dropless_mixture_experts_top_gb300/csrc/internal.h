@@ -31,8 +31,6 @@ struct RouteArgs {
   float *w_row;         // [T*k]
   int32_t *lrank;       // [T*k] scratch: rank of a slot among its block's slots of the same expert
   int32_t *hist;        // [nblk,E] scratch: per-block expert histogram
-  int32_t *block_base;  // [nblk,E] scratch: first row of each (block, expert) run
-  uint32_t *ticket;     // scratch: blocks finished (zeroed before launch)
   int32_t *status;      // scratch status word
 };
 int route_num_blocks(int T);

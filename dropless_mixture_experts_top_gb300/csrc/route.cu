@@ -9,18 +9,23 @@
 // see keep CUDA graphs usable).
 //
 // Two kernels:
-//   route_topk  : the block's 128 tokens' logits staged in shared memory;
-//                 four threads per token each keep a sorted top-k list of a
-//                 quarter of the experts in registers (branch-free insertion,
-//                 ties -> lower expert), merged by two shuffle rounds; fp32
-//                 renormalised weights; then per block an expert histogram
-//                 and every slot's
-//                 rank inside its (block, expert) run.  The last block to
-//                 finish (atomic ticket, no spin-wait) scans the histograms:
-//                 counts, offsets, and the first row of every (block, expert)
-//                 run.  Single pass over the logits.
-//   route_index : one thread per slot: row = run base + rank; writes
-//                 row_of_slot, slot_of_row and w_row.
+//   route_topk  : the block's 128 tokens' logits staged in shared memory (all
+//                 of a thread's loads issued before the first store);
+//                 four threads per token each take every fourth expert, sort
+//                 them KMAX at a time with a bitonic network and keep the best
+//                 KMAX (bitonic top-k merge); the four lists merge by two
+//                 shuffle rounds.  Ties -> lower expert.  fp32 renormalised
+//                 weights.  Every token's chosen experts set one bit in a
+//                 per-expert bitmask over the block's tokens, so a slot's rank
+//                 inside its (block, expert) run, in token order, is a
+//                 popcount and the block's expert histogram a sum of them.
+//                 Single pass over the logits.
+//   route_index : one block per route block: every block sums the histogram
+//                 columns (below its own row, and in total), scans the totals
+//                 over experts (counts, offsets; block 0 writes them), and
+//                 writes its slots' rows: row = offsets[e] + the rows of
+//                 expert e in earlier blocks + rank; row_of_slot, slot_of_row,
+//                 w_row.  The kernel boundary is the only grid-wide wait.
 // The resulting permutation is expert-major and token-ascending inside an
 // expert, so it is unique and reproducible bit for bit.
 #include <math.h>
@@ -32,85 +37,156 @@ namespace {
 
 constexpr int TB = kRouteTokensPerBlock;
 
-constexpr int kQ = kRouteThreads / TB;  // threads per token (4): each scans a quarter of the experts
+constexpr int kQ = kRouteThreads / TB;      // threads per token (4): each takes every kQ-th expert
+constexpr int kTokPerWarp = 32 / kQ;        // tokens of one warp (8); a token's threads are kTokPerWarp lanes apart
+constexpr int kMaskWords = TB / 32;         // words of a per-expert token bitmask
+constexpr int kLoadBatch = 8;               // float4 loads a thread has in flight while staging
+constexpr int kHistLoads = 32;              // histogram loads a route_index thread has in flight
 
-// (x, xi) ranks before (tv, ti): larger logit first, lower expert index on
-// ties; an empty slot (ti == INT_MAX) ranks after everything.
-__device__ __forceinline__ bool ranks_before(float x, int xi, float tv, int ti) {
-  return x > tv || (x == tv && xi < ti);
+// (x, xi) ranks before (y, yi): larger logit first, lower expert index on
+// ties; an empty slot (index INT_MAX, value -inf) ranks after everything.
+__device__ __forceinline__ bool ranks_before(float x, int xi, float y, int yi) {
+  return x > y || (x == y && xi < yi);
 }
 
-// Insert (x, xi) into a list sorted by ranks_before, keeping its first KMAX
-// entries.  Branch-free: slot j takes slot j-1's entry if x ranks before it,
-// else x if x ranks before slot j's entry, else keeps its own.
-template <int KMAX>
-__device__ __forceinline__ void topk_insert(float (&tv)[KMAX], int (&ti)[KMAX], float x, int xi) {
-  bool before[KMAX];
-#pragma unroll
-  for (int j = 0; j < KMAX; ++j) before[j] = ranks_before(x, xi, tv[j], ti[j]);
-#pragma unroll
-  for (int j = KMAX - 1; j > 0; --j) {
-    const float v = before[j - 1] ? tv[j - 1] : (before[j] ? x : tv[j]);
-    const int ix = before[j - 1] ? ti[j - 1] : (before[j] ? xi : ti[j]);
-    tv[j] = v;
-    ti[j] = ix;
-  }
-  if (before[0]) {
-    tv[0] = x;
-    ti[0] = xi;
-  }
+// Order the pair so that slot a ranks before slot b.
+__device__ __forceinline__ void order_pair(float &av, int &ai, float &bv, int &bi) {
+  const bool sw = ranks_before(bv, bi, av, ai);
+  const float tv = sw ? bv : av;
+  const int ti = sw ? bi : ai;
+  bv = sw ? av : bv;
+  bi = sw ? ai : bi;
+  av = tv;
+  ai = ti;
 }
 
-// The block's logits [ntok, E] (contiguous in memory) into shared memory rows
-// of E + 1 floats (the pad keeps the per-token scans free of bank conflicts).
-__device__ __forceinline__ void stage_logits(const float *__restrict__ src, int n, int E, float *s_lg) {
-  for (int g = 4 * static_cast<int>(threadIdx.x); g < n; g += 4 * kRouteThreads) {
-    float v[4];
-    if (g + 4 <= n) {
-      const float4 q = __ldg(reinterpret_cast<const float4 *>(src + g));
-      v[0] = q.x, v[1] = q.y, v[2] = q.z, v[3] = q.w;
-    } else {
+// Bitonic sorting network over N (a power of two) entries: afterwards entry 0
+// ranks first.  Blocks of `size` entries alternate direction until the last
+// stage, where every pair orders first-before-second.
+template <int N>
+__device__ __forceinline__ void bitonic_sort(float (&v)[N], int (&ix)[N]) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) v[i] = g + i < n ? __ldg(src + g + i) : 0.f;
-    }
-    int r = g / E, c = g - r * E;
+  for (int size = 2; size <= N; size <<= 1) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (g + i < n) s_lg[r * (E + 1) + c] = v[i];
-      if (++c == E) {
-        c = 0;
-        ++r;
+    for (int st = size >> 1; st > 0; st >>= 1) {
+#pragma unroll
+      for (int i = 0; i < N; ++i) {
+        if ((i & st) == 0) {
+          if ((i & size) == 0)
+            order_pair(v[i], ix[i], v[i + st], ix[i + st]);
+          else
+            order_pair(v[i + st], ix[i + st], v[i], ix[i]);
+        }
       }
     }
   }
 }
 
+// a <- the best N of a and b, sorted; both sorted on entry.  Entry i of a
+// against entry N-1-i of b keeps the better one: the result holds the N best
+// of both and is bitonic, and a cascade of half-cleaners sorts it.
+template <int N>
+__device__ __forceinline__ void merge_best(float (&av)[N], int (&ai)[N], const float (&bv)[N],
+                                           const int (&bi)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const bool tb = ranks_before(bv[N - 1 - i], bi[N - 1 - i], av[i], ai[i]);
+    av[i] = tb ? bv[N - 1 - i] : av[i];
+    ai[i] = tb ? bi[N - 1 - i] : ai[i];
+  }
+#pragma unroll
+  for (int st = N >> 1; st > 0; st >>= 1) {
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+      if ((i & st) == 0) order_pair(av[i], ai[i], av[i + st], ai[i + st]);
+  }
+}
+
+// The block's logits [n / E, E] (contiguous in memory, 16-byte aligned: the
+// block's first token is a multiple of 128) into shared memory rows of S
+// floats.  Each thread issues kLoadBatch 16-byte loads before its first
+// store, so the block waits for one round trip to memory, not one per load.
+// A NaN is staged as -inf (the selection stays well defined); returns whether
+// this thread saw a non-finite logit.
+__device__ __forceinline__ float nan_to_ninf(float x, bool &bad) {
+  bad |= !isfinite(x);
+  return x != x ? -INFINITY : x;
+}
+
+__device__ __forceinline__ bool stage_logits(const float *__restrict__ src, int n, int E, int S,
+                                             float *s_lg) {
+  bool bad = false;
+  for (int base = 0; base < n; base += 4 * kRouteThreads * kLoadBatch) {
+    float4 q[kLoadBatch];
+#pragma unroll
+    for (int u = 0; u < kLoadBatch; ++u) {
+      const int g = base + 4 * (static_cast<int>(threadIdx.x) + u * kRouteThreads);
+      if (g + 4 <= n) {
+        q[u] = __ldg(reinterpret_cast<const float4 *>(src + g));
+      } else {
+        q[u].x = g < n ? __ldg(src + g) : 0.f;
+        q[u].y = g + 1 < n ? __ldg(src + g + 1) : 0.f;
+        q[u].z = g + 2 < n ? __ldg(src + g + 2) : 0.f;
+        q[u].w = g + 3 < n ? __ldg(src + g + 3) : 0.f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kLoadBatch; ++u) {
+      q[u].x = nan_to_ninf(q[u].x, bad);
+      q[u].y = nan_to_ninf(q[u].y, bad);
+      q[u].z = nan_to_ninf(q[u].z, bad);
+      q[u].w = nan_to_ninf(q[u].w, bad);
+    }
+#pragma unroll
+    for (int u = 0; u < kLoadBatch; ++u) {
+      const int g = base + 4 * (static_cast<int>(threadIdx.x) + u * kRouteThreads);
+      if (g >= n) break;
+      int r = g / E, c = g - r * E;
+      if ((E & 3) == 0) {  // the four stay in one row; rows start 16-byte aligned
+        *reinterpret_cast<float4 *>(s_lg + r * S + c) = q[u];
+      } else {
+        const float v[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (g + i < n) s_lg[r * S + c] = v[i];
+          if (++c == E) {
+            c = 0;
+            ++r;
+          }
+        }
+      }
+    }
+  }
+  return bad;
+}
+
+// Shared-memory row stride of the staged logits: E + 4 floats keeps rows
+// 16-byte aligned and puts the 8 tokens x 4 quarters of a warp's reads
+// (token tl, expert q + 4m) on distinct banks when E is a multiple of 32.
+__host__ __device__ constexpr int logit_stride(int E) { return E + 4; }
+
 template <int KMAX>
-__global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(RouteArgs a, int nblk) {
-  extern __shared__ float s_lg[];                     // [TB][E + 1] this block's logits
-  __shared__ uint32_t s_mask[TB][kMaxExperts / 32];  // chosen experts of each token, as bits
-  __shared__ uint8_t s_pos[TB][kMaxExperts];         // position j of expert e in the token's list
-  __shared__ int32_t s_part[kRouteThreads];
-  __shared__ int32_t s_start[kRouteThreads];
-  __shared__ int32_t s_cnt[kMaxExperts];
-  __shared__ int32_t s_off[kMaxExperts + 1];
-  __shared__ int s_last;
+__global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(RouteArgs a) {
+  extern __shared__ __align__(16) float s_lg[];           // [TB][E + 4] this block's logits
+  __shared__ uint32_t s_emask[kMaxExperts][kMaskWords];  // tokens of this block that chose expert e
+  __shared__ uint8_t s_slot_e[TB * kMaxTopK];            // expert of each of the block's slots
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = a.E, k = a.k, T = a.T;
+  const int S = logit_stride(E);
   const int t0 = blockIdx.x * TB;
   const int ntok = min(TB, T - t0);
-  bool bad = false;
 
-  stage_logits(a.logits + static_cast<size_t>(t0) * E, ntok * E, E, s_lg);
+  for (int i = threadIdx.x; i < E * kMaskWords; i += kRouteThreads) (&s_emask[0][0])[i] = 0u;
+  const bool bad = stage_logits(a.logits + static_cast<size_t>(t0) * E, ntok * E, E, S, s_lg);
   __syncthreads();
 
-  // Top-k: kQ threads per token (adjacent lanes), each keeps a sorted list of
-  // its quarter of the experts, then the lists merge by shuffles.
+  // Top-k of token tl by its kQ threads (lanes kTokPerWarp apart): quarter qq
+  // takes experts qq, qq + kQ, qq + 2kQ, ...
   {
-    const int tl = threadIdx.x / kQ, qq = threadIdx.x % kQ;
-    const int per = (E + kQ - 1) / kQ;
-    const int e0 = qq * per, e1 = min(E, e0 + per);
+    const int tl = warp * kTokPerWarp + lane % kTokPerWarp, qq = lane / kTokPerWarp;
+    const int nm = tl < ntok ? (E - qq + kQ - 1) / kQ : 0;  // this quarter's experts
+    const float *row = s_lg + tl * S;
     float tv[KMAX];
     int ti[KMAX];
 #pragma unroll
@@ -118,19 +194,28 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(RouteArgs a, 
       tv[j] = -INFINITY;
       ti[j] = INT_MAX;
     }
-    if (tl < ntok) {
-      const float *row = s_lg + tl * (E + 1);
-      for (int e = e0; e < e1; ++e) {
-        float x = row[e];
-        if (!isfinite(x)) {
-          bad = true;
-          if (isnan(x)) x = -INFINITY;  // keep the selection well defined
+    for (int m0 = 0; m0 < nm; m0 += KMAX) {
+      float cv[KMAX];
+      int ci[KMAX];
+#pragma unroll
+      for (int u = 0; u < KMAX; ++u) {
+        const int m = m0 + u, e = qq + kQ * m;
+        cv[u] = m < nm ? row[e] : -INFINITY;
+        ci[u] = m < nm ? e : INT_MAX;
+      }
+      bitonic_sort<KMAX>(cv, ci);
+      if (m0 == 0) {  // the first chunk is the running list
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+          tv[j] = cv[j];
+          ti[j] = ci[j];
         }
-        topk_insert<KMAX>(tv, ti, x, e);
+      } else {
+        merge_best<KMAX>(tv, ti, cv, ci);
       }
     }
 #pragma unroll
-    for (int o = 1; o < kQ; o <<= 1) {  // both partners merge the other's list: same result
+    for (int o = kTokPerWarp; o < 32; o <<= 1) {  // both partners merge the same two lists
       float pv[KMAX];
       int pi[KMAX];
 #pragma unroll
@@ -138,10 +223,9 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(RouteArgs a, 
         pv[j] = __shfl_xor_sync(0xffffffffu, tv[j], o);
         pi[j] = __shfl_xor_sync(0xffffffffu, ti[j], o);
       }
-#pragma unroll
-      for (int j = 0; j < KMAX; ++j) topk_insert<KMAX>(tv, ti, pv[j], pi[j]);
+      merge_best<KMAX>(tv, ti, pv, pi);
     }
-    if (tl < ntok && qq == 0) {
+    if (tl < ntok) {
       const size_t sb = static_cast<size_t>(t0 + tl) * k;
       // renormalised weights: exp(l_j - l_max) / sum over the kept set
       const float m = tv[0];
@@ -149,15 +233,13 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(RouteArgs a, 
 #pragma unroll
       for (int j = 0; j < KMAX; ++j)
         if (j < k) ssum += expf(tv[j] - m);
-      const int npl = (E + 31) >> 5;
-      for (int w = 0; w < npl; ++w) s_mask[tl][w] = 0;
 #pragma unroll
       for (int j = 0; j < KMAX; ++j) {
-        if (j < k) {
+        if (j < k && j % kQ == qq) {  // the token's kQ threads share its k slots
           a.topk_idx[sb + j] = ti[j];
           a.topk_w[sb + j] = expf(tv[j] - m) / ssum;
-          s_pos[tl][ti[j]] = static_cast<uint8_t>(j);
-          s_mask[tl][ti[j] >> 5] |= 1u << (ti[j] & 31);
+          s_slot_e[tl * k + j] = static_cast<uint8_t>(ti[j]);
+          atomicOr(&s_emask[ti[j]][tl >> 5], 1u << (tl & 31));
         }
       }
     }
@@ -165,45 +247,62 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(RouteArgs a, 
   if (bad) flag_status(a.status, kDevNonfiniteLogit);
   __syncthreads();
 
-  // per-(block, expert) histogram and ranks, in token order
-  if (threadIdx.x < E) {
-    const int e = threadIdx.x, w = e >> 5, b = e & 31;
-    int cnt = 0;
-#pragma unroll 8
-    for (int tl = 0; tl < ntok; ++tl) {
-      if ((s_mask[tl][w] >> b) & 1u)
-        a.lrank[static_cast<size_t>(t0 + tl) * k + s_pos[tl][e]] = cnt++;
-    }
-    a.hist[static_cast<size_t>(blockIdx.x) * E + e] = cnt;
+  // rank of every slot inside its (block, expert) run: the run's tokens before it
+  for (int sl = threadIdx.x; sl < ntok * k; sl += kRouteThreads) {
+    const int tl = sl / k;
+    const uint32_t *mk = s_emask[s_slot_e[sl]];
+    int r = __popc(mk[tl >> 5] & ((1u << (tl & 31)) - 1u));
+    for (int w = 0; w < (tl >> 5); ++w) r += __popc(mk[w]);
+    a.lrank[static_cast<size_t>(t0) * k + sl] = r;
   }
+  if (threadIdx.x < E) {
+    int c = 0;
+#pragma unroll
+    for (int w = 0; w < kMaskWords; ++w) c += __popc(s_emask[threadIdx.x][w]);
+    a.hist[static_cast<size_t>(blockIdx.x) * E + threadIdx.x] = c;
+  }
+}
 
-  // last block to finish scans all histograms
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_last = (atomicAdd(a.ticket, 1u) == static_cast<unsigned>(nblk - 1));
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
+__global__ void __launch_bounds__(kRouteThreads) route_index_kernel(RouteArgs a, int nblk) {
+  __shared__ int32_t s_below[kRouteThreads];  // per (partial p, expert e): rows of e in earlier blocks
+  __shared__ int32_t s_total[kRouteThreads];  // per (p, e): rows of e in all blocks
+  __shared__ int32_t s_base[kMaxExperts];
+  __shared__ int32_t s_cnt[kMaxExperts];
+  __shared__ int32_t s_off[kMaxExperts + 1];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int E = a.E, k = a.k, b = blockIdx.x;
 
+  // thread (p, e) sums histogram rows [b0, b1) of column e, kHistLoads loads in flight
   const int P = kRouteThreads / E;  // partial sums per expert (>= 2)
   const int chunk = (nblk + P - 1) / P;
   const int e = threadIdx.x % E, p = threadIdx.x / E;
-  const int b0 = p * chunk, b1 = min(nblk, b0 + chunk);
   if (p < P) {
-    int s = 0;
-#pragma unroll 8
-    for (int b = b0; b < b1; ++b) s += __ldcg(a.hist + static_cast<size_t>(b) * E + e);
-    s_part[p * E + e] = s;
+    const int b0 = p * chunk, b1 = min(nblk, b0 + chunk);
+    int below = 0, total = 0;
+    for (int bb = b0; bb < b1; bb += kHistLoads) {
+      int hv[kHistLoads];
+#pragma unroll
+      for (int u = 0; u < kHistLoads; ++u)
+        hv[u] = bb + u < b1 ? __ldg(a.hist + static_cast<size_t>(bb + u) * E + e) : 0;
+#pragma unroll
+      for (int u = 0; u < kHistLoads; ++u) {
+        total += hv[u];
+        below += bb + u < b ? hv[u] : 0;
+      }
+    }
+    s_below[p * E + e] = below;
+    s_total[p * E + e] = total;
   }
   __syncthreads();
   if (threadIdx.x < E) {
-    int run = 0;
+    int below = 0, total = 0;
     for (int q = 0; q < P; ++q) {
-      s_start[q * E + threadIdx.x] = run;
-      run += s_part[q * E + threadIdx.x];
+      below += s_below[q * E + threadIdx.x];
+      total += s_total[q * E + threadIdx.x];
     }
-    s_cnt[threadIdx.x] = run;
-    a.counts[threadIdx.x] = run;
+    s_base[threadIdx.x] = below;
+    s_cnt[threadIdx.x] = total;
+    if (b == 0) a.counts[threadIdx.x] = total;
   }
   __syncthreads();
   if (warp == 0) {  // exclusive scan of counts over experts
@@ -223,28 +322,18 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(RouteArgs a, 
     if (lane == 0) s_off[E] = carry;
   }
   __syncthreads();
-  if (threadIdx.x <= E) a.offsets[threadIdx.x] = s_off[threadIdx.x];
-  if (p < P) {
-    int run = s_off[e] + s_start[p * E + e];
-#pragma unroll 8
-    for (int b = b0; b < b1; ++b) {
-      a.block_base[static_cast<size_t>(b) * E + e] = run;
-      run += __ldcg(a.hist + static_cast<size_t>(b) * E + e);
-    }
-  }
-}
+  if (b == 0 && threadIdx.x <= E) a.offsets[threadIdx.x] = s_off[threadIdx.x];
 
-__global__ void __launch_bounds__(256) route_index_kernel(RouteArgs a) {
-  const int s = blockIdx.x * blockDim.x + threadIdx.x;
-  const int nslots = a.T * a.k;
-  if (s >= nslots) return;
-  const int t = s / a.k;
-  const int b = t / TB;
-  const int e = a.topk_idx[s];
-  const int row = a.block_base[static_cast<size_t>(b) * a.E + e] + a.lrank[s];
-  a.row_of_slot[s] = row;
-  a.slot_of_row[row] = s;
-  a.w_row[row] = a.topk_w[s];
+  // this block's slots: row = start of expert e + rows of e in earlier blocks + rank
+  const int t0 = b * TB, ntok = min(TB, a.T - t0);
+  for (int sl = threadIdx.x; sl < ntok * k; sl += kRouteThreads) {
+    const size_t s = static_cast<size_t>(t0) * k + sl;
+    const int ee = a.topk_idx[s];
+    const int row = s_off[ee] + s_base[ee] + a.lrank[s];
+    a.row_of_slot[s] = row;
+    a.slot_of_row[row] = static_cast<int32_t>(s);
+    a.w_row[row] = a.topk_w[s];
+  }
 }
 
 }  // namespace
@@ -254,7 +343,7 @@ int route_num_blocks(int T) { return (T + TB - 1) / TB; }
 template <int KMAX>
 cudaError_t launch_topk(const RouteArgs &a, cudaStream_t s) {
   const int nblk = route_num_blocks(a.T);
-  const size_t smem = static_cast<size_t>(TB) * (a.E + 1) * sizeof(float);
+  const size_t smem = static_cast<size_t>(TB) * logit_stride(a.E) * sizeof(float);
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -262,11 +351,11 @@ cudaError_t launch_topk(const RouteArgs &a, cudaStream_t s) {
   if (!attr_set[dev]) {  // room for E = 256
     const cudaError_t e = cudaFuncSetAttribute(route_topk_kernel<KMAX>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               TB * (kMaxExperts + 1) * static_cast<int>(sizeof(float)));
+                                               TB * logit_stride(kMaxExperts) * static_cast<int>(sizeof(float)));
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  route_topk_kernel<KMAX><<<nblk, kRouteThreads, smem, s>>>(a, nblk);
+  route_topk_kernel<KMAX><<<nblk, kRouteThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -275,8 +364,8 @@ cudaError_t launch_route_topk(const RouteArgs &a, cudaStream_t s) {
 }
 
 cudaError_t launch_route_index(const RouteArgs &a, cudaStream_t s) {
-  const int n = a.T * a.k;
-  route_index_kernel<<<(n + 255) / 256, 256, 0, s>>>(a);
+  const int nblk = route_num_blocks(a.T);
+  route_index_kernel<<<nblk, kRouteThreads, 0, s>>>(a, nblk);
   return cudaGetLastError();
 }
 

@@ -19,8 +19,8 @@ namespace moe {
 namespace {
 
 // Room for any configuration with T <= 32768 tokens (k <= 16, E <= 256): per-slot
-// ranks (2 MiB at the limit), two per-block expert histograms (256 KiB each) and
-// the status header -- 2.5 MiB + 4 KiB.
+// ranks (2 MiB at the limit), the per-block expert histogram (256 KiB) and the
+// status header, with room to spare -- 2.5 MiB + 4 KiB.
 constexpr size_t kStaticRouteScratchBytes = (size_t{5} << 19) + 4096;
 
 static __device__ __align__(256) uint8_t g_route_scratch[kStaticRouteScratchBytes];
