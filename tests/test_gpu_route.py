@@ -30,6 +30,7 @@ CASES = [
     ("E64_k8_one_past_a_block", 129, 64, 8),
     ("E256_k8_long_scan", 9000, 256, 8),   # 71 blocks, 2 partial sums per expert: 36 blocks each
     ("E8_k2_many_blocks", 20000, 8, 2),    # 157 blocks, 64 partial sums per expert
+    ("E128_k8_t16384", 16384, 128, 8),     # the 30B-shaped layer's routing, in full
 ]
 
 
