@@ -147,7 +147,7 @@ def source_hash(label):
     figure is valid only while this is unchanged."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dropless_mixture_experts_top_gb300", "csrc")
-    for n in (kernel_source(label), "common.cuh", "epilogue.cuh", "internal.h"):
+    for n in (kernel_source(label), "common.cuh", "epilogue.cuh", "internal.h", "mxfp8.cuh"):
         with open(os.path.join(csrc, n), "rb") as f:
             h.update(n.encode() + f.read())
     return h.hexdigest()[:16]
