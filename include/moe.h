@@ -168,8 +168,9 @@ moe_status moe_mxfp8_forward_offsets(const moe_config *cfg, moe_mxfp8_fwd_layout
 
 /* Router and dispatch indices.  logits: device fp32 [T,E].  Writes every field
  * of *routing.  Per-expert counts, the scan and the permutation are computed
- * on the device in one pass over the tokens (per-block expert histograms; the
- * last block to finish scans them).  Non-finite logits set
+ * on the device in one pass over the logits (two kernels: per-block expert
+ * histograms and ranks, then every block scans the histograms itself and
+ * writes its slots' rows).  Non-finite logits set
  * MOE_DEV_NONFINITE_LOGIT; the indices written are still in range. */
 moe_status moe_route(const moe_config *cfg, const float *logits, const moe_routing *routing,
                      void *scratch, size_t scratch_bytes, void *stream);
