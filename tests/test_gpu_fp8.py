@@ -86,6 +86,7 @@ FP8_SHAPES = [
     ("ragged_half_boxes", MoEShape(T=700, H=384, I=384, E=6, k=2)),  # 256-row B boxes half past the operand
     ("wide", MoEShape(T=300, H=640, I=256, E=16, k=4)),
     ("single_expert", MoEShape(T=333, H=128, I=256, E=1, k=1)),
+    ("E256_k16_max", MoEShape(T=300, H=256, I=128, E=256, k=16)),  # padded row space ~8x the rows
 ]
 
 

@@ -45,6 +45,7 @@ SHAPES = [
     ("ragged", MoEShape(T=700, H=384, I=384, E=6, k=2)),   # 2I = 768: four 192-row gate|up tiles
     ("partial_tiles", MoEShape(T=300, H=256, I=128, E=8, k=2)),  # 2I = 256: a 192-row tile half past it
     ("wide", MoEShape(T=300, H=640, I=256, E=16, k=4)),
+    ("E256_k16_max", MoEShape(T=300, H=256, I=128, E=256, k=16)),
 ]
 
 

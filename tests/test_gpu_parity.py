@@ -17,6 +17,7 @@ SHAPES = [
     ("k1", MoEShape(T=200, H=128, I=128, E=4, k=1)),
     ("k_eq_E", MoEShape(T=130, H=128, I=64, E=3, k=3)),
     ("single_expert", MoEShape(T=333, H=192, I=128, E=1, k=1)),
+    ("E256_k16_max", MoEShape(T=300, H=128, I=128, E=256, k=16)),  # the largest E and k: most experts empty
 ]
 
 

@@ -31,6 +31,7 @@ CASES = [
     ("E256_k8_long_scan", 9000, 256, 8),   # 71 blocks, 2 partial sums per expert: 36 blocks each
     ("E8_k2_many_blocks", 20000, 8, 2),    # 157 blocks, 64 partial sums per expert
     ("E128_k8_t16384", 16384, 128, 8),     # the 30B-shaped layer's routing, in full
+    ("E256_k16_t131072", 131072, 256, 16),  # 2 M slots, 1024 blocks: 16 register batches per scan
 ]
 
 
