@@ -201,10 +201,10 @@ struct DevInfo {
 };
 
 moe_status device_info(DevInfo *out) {
-  static DevInfo cache[64];
-  static std::once_flag flags[64];
+  static DevInfo cache[kMaxDevices];
+  static std::once_flag flags[kMaxDevices];
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
   std::call_once(flags[dev], [dev] {
     int maj = 0, min = 0, sms = 0;
     cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev);

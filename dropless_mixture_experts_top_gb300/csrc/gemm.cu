@@ -649,10 +649,7 @@ cudaError_t launch_mode(const GemmArgs &a, cudaStream_t s) {
     p.expert_maps = maps;
   }
   // once per device: the shared-memory opt-in, and how many CTA pairs fit at once
-  static int pair_grid[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  static DeviceOnce once;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -664,20 +661,25 @@ cudaError_t launch_mode(const GemmArgs &a, cudaStream_t s) {
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (!pair_grid[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         smem_bytes(MODE));
-    if (e != cudaSuccess) return e;
-    cfg.gridDim = dim3(a.num_sms & ~1);
-    int clusters = 0;
-    e = cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_kernel<MODE>, &cfg);
-    if (e != cudaSuccess) return e;
-    if (clusters < 1) return cudaErrorInvalidConfiguration;
-    pair_grid[dev] = 2 * (clusters < a.num_sms / 2 ? clusters : a.num_sms / 2);
-  }
-  cfg.gridDim = dim3(pair_grid[dev]);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE>, mA0, mA1, mB0, mB1, p);
+  int pair_grid = 0;
+  cudaError_t e = once.get(
+      [&](int *grid) {
+        cudaError_t r = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(MODE));
+        if (r != cudaSuccess) return r;
+        cudaLaunchConfig_t q = cfg;
+        q.gridDim = dim3(a.num_sms & ~1);
+        int clusters = 0;
+        r = cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_kernel<MODE>, &q);
+        if (r != cudaSuccess) return r;
+        if (clusters < 1) return cudaErrorInvalidConfiguration;
+        *grid = 2 * (clusters < a.num_sms / 2 ? clusters : a.num_sms / 2);
+        return cudaSuccess;
+      },
+      &pair_grid);
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3(pair_grid);
+  e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE>, mA0, mA1, mB0, mB1, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -788,16 +788,12 @@ cudaError_t launch_mx_mode(const MxGemmArgs &a, cudaStream_t s) {
       break;
   }
   if (!ok) return cudaErrorInvalidValue;
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_mx_kernel<MODE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(MODE));
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
+  static DeviceOnce once;  // the shared-memory opt-in, once per device
+  const cudaError_t e = once.get([](int *) {
+    return cudaFuncSetAttribute(grouped_gemm_mx_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                smem_bytes(MODE));
+  });
+  if (e != cudaSuccess) return e;
   grouped_gemm_mx_kernel<MODE><<<a.num_sms, threads_of(MODE), smem_bytes(MODE), s>>>(mA0, mA1, mB0,
                                                                                     mB1, p);
   return cudaGetLastError();

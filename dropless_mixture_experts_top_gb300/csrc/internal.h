@@ -6,10 +6,31 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace moe {
 
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 16;
+
+// Per-device one-time setup of a launcher (a kernel's shared-memory opt-in, an
+// occupancy query): setup(&value) runs once per device under std::call_once,
+// so concurrent first calls from several host threads are safe, and its
+// result and value are returned on every later call for that device.
+constexpr int kMaxDevices = 64;
+struct DeviceOnce {
+  std::once_flag flag[kMaxDevices];
+  cudaError_t err[kMaxDevices] = {};
+  int value[kMaxDevices] = {};
+  template <class Setup>
+  cudaError_t get(Setup &&setup, int *out = nullptr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::call_once(flag[dev], [&] { err[dev] = setup(&value[dev]); });
+    if (out) *out = value[dev];
+    return err[dev];
+  }
+};
 
 // Status flags written by kernels into the scratch status word.
 constexpr int32_t kDevNonfiniteLogit = 0x1;

@@ -330,12 +330,11 @@ cudaError_t launch_quant_cols(const uint16_t *src, int C, int Mpad, const int32_
                               RowCodes rows, cudaStream_t s) {
   const int col_blocks = C / kQcCols < 4 ? C / kQcCols : 4;  // each loops over C / (64 * 4) column tiles
   const dim3 grid(static_cast<unsigned>(Mpad / kQcRows), static_cast<unsigned>(col_blocks));
-  static bool attr_set = false;  // dynamic shared memory above 48 KB (set once per process)
-  if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(quant_cols_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQcSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static DeviceOnce once;  // dynamic shared memory above 48 KB, opted in once per device
+  const cudaError_t e = once.get([](int *) {
+    return cudaFuncSetAttribute(quant_cols_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQcSmem);
+  });
+  if (e != cudaSuccess) return e;
   quant_cols_kernel<<<grid, kQcThreads, kQcSmem, s>>>(src, C, Mpad, offsets, pad_off, E, codes, sf, L, rows);
   return cudaGetLastError();
 }
@@ -344,12 +343,11 @@ cudaError_t launch_quant_wT(const uint16_t *W, int E, int R, int C, int interlea
                             uint8_t *codes, uint8_t *sf, SfLayout L, RowCodes rows, cudaStream_t s) {
   const int col_blocks = C / kQcCols < 4 ? C / kQcCols : 4;
   const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(E) * R / kQcRows), static_cast<unsigned>(col_blocks));
-  static bool attr_set = false;
-  if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(quant_wT_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQcSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static DeviceOnce once;
+  const cudaError_t e = once.get([](int *) {
+    return cudaFuncSetAttribute(quant_wT_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQcSmem);
+  });
+  if (e != cudaSuccess) return e;
   quant_wT_kernel<<<grid, kQcThreads, kQcSmem, s>>>(W, R, C, interleave, half, codes, sf, L, rows);
   return cudaGetLastError();
 }

@@ -344,17 +344,12 @@ template <int KMAX>
 cudaError_t launch_topk(const RouteArgs &a, cudaStream_t s) {
   const int nblk = route_num_blocks(a.T);
   const size_t smem = static_cast<size_t>(TB) * logit_stride(a.E) * sizeof(float);
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {  // room for E = 256
-    const cudaError_t e = cudaFuncSetAttribute(route_topk_kernel<KMAX>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               TB * logit_stride(kMaxExperts) * static_cast<int>(sizeof(float)));
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
+  static DeviceOnce once;  // the shared-memory opt-in (room for E = 256), once per device
+  const cudaError_t e = once.get([](int *) {
+    return cudaFuncSetAttribute(route_topk_kernel<KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                TB * logit_stride(kMaxExperts) * static_cast<int>(sizeof(float)));
+  });
+  if (e != cudaSuccess) return e;
   route_topk_kernel<KMAX><<<nblk, kRouteThreads, smem, s>>>(a);
   return cudaGetLastError();
 }

@@ -27,7 +27,6 @@ static __device__ __align__(256) uint8_t g_route_scratch[kStaticRouteScratchByte
 
 // In host code g_route_scratch names a host-side stand-in, not a device address.
 // The device address is looked up once per device, with that device current.
-constexpr int kMaxDevices = 64;
 void *g_scratch_addr[kMaxDevices];
 cudaError_t g_scratch_err[kMaxDevices];
 std::once_flag g_scratch_once[kMaxDevices];
