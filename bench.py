@@ -469,8 +469,9 @@ def run_ours(args):
     if not torch.equal(host_dl.to(dev), grads["d_logits"]):
         raise RuntimeError("pipelined end-to-end step disagrees with the device-resident step")
     e2e_ms = max_over_ranks(e2e_start.elapsed_time(e2e_end) / K, dist, dev)
-    # activation-checkpointed layer step (the pages' "2 fwd + bwd"): route, forward,
-    # then in the backward pass the forward again (recompute) followed by the backward
+    # activation-checkpointed layer step (the pages' "2 fwd + bwd"): route, a forward
+    # that keeps no activations (out only), then in the backward pass the recompute of
+    # what the backward reads, followed by the backward
     c_starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     c_ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     torch.cuda.synchronize()
@@ -479,8 +480,8 @@ def run_ours(args):
             flush.zero_()
             c_starts[i].record(stream)
             layer.route(d["logits"], stream)
-            layer.forward(d["x"], d["W_gate"], d["W_up"], d["W_down"], out=out, stream=stream)
-            layer.forward(d["x"], d["W_gate"], d["W_up"], d["W_down"], out=out, stream=stream)
+            layer.forward(d["x"], d["W_gate"], d["W_up"], d["W_down"], out=out, stream=stream, save=False)
+            layer.recompute(d["x"], d["W_gate"], d["W_up"], d["W_down"], stream=stream)
             grads = layer.backward(d["dy"], d["x"], d["W_gate"], d["W_up"], d["W_down"], grads=grads,
                                    stream=stream)
             c_ends[i].record(stream)

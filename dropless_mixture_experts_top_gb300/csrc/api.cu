@@ -480,6 +480,100 @@ moe_status forward_mx(const Mx8Fwd &f, cudaStream_t s) {
 
 using namespace moe;
 
+namespace moe {
+namespace {
+
+// What a forward call leaves behind.  Full: out and everything the backward
+// reads (in `saved`).  NoSave: out only (`saved` is used as scratch; a
+// checkpointed layer's first pass).  Recompute: what the backward reads, not
+// out (a checkpointed layer's second pass, just before the backward).
+enum FwdKind { kFwdFull, kFwdNoSave, kFwdRecompute };
+
+moe_status forward_impl(FwdKind kind, const moe_config *cfg, const void *x, const moe_routing *r,
+                        const void *W_gate, const void *W_up, const void *W_down, void *out,
+                        void *saved, size_t saved_bytes, void *scratch, size_t scratch_bytes,
+                        void *stream) {
+  const bool need_out = kind != kFwdRecompute;
+  if (!shape_ok(cfg)) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_routing(r, cfg->T));
+  if (!W_gate || !W_up || !W_down || !saved || !scratch || (cfg->T > 0 && (!x || (need_out && !out))))
+    return MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(W_gate) || !al16(W_up) || !al16(W_down) || (need_out && !al16(out)) ||
+      !al16(saved) || !al16(scratch))
+    return MOE_ERR_ALIGNMENT;
+  const Layout L = layout_of(cfg);
+  if (saved_bytes < L.s_total || scratch_bytes < L.f_total) return MOE_ERR_WORKSPACE;
+  DevInfo di;
+  MOE_TRY(device_info(&di));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t *sc = static_cast<uint8_t *>(scratch);
+  uint8_t *sv = static_cast<uint8_t *>(saved);
+  if (cudaMemsetAsync(sc, 0, kHeader, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cfg->T == 0) return MOE_OK;
+  const int T = cfg->T, H = cfg->H, k = cfg->k;
+  int32_t *status = reinterpret_cast<int32_t *>(sc);
+  uint16_t *x_perm = reinterpret_cast<uint16_t *>(sv + L.s_xperm);
+  uint16_t *G = reinterpret_cast<uint16_t *>(sv + L.s_G);
+  uint16_t *U = reinterpret_cast<uint16_t *>(sv + L.s_U);
+  uint16_t *A = reinterpret_cast<uint16_t *>(sv + L.s_A);
+  uint16_t *Y = reinterpret_cast<uint16_t *>(sv + L.s_Y);
+  uint16_t *A_w = reinterpret_cast<uint16_t *>(sv + L.s_Aw);
+
+  if (cfg->precision == MOE_PREC_MXFP8) {
+    Mx8Fwd f;
+    f.cfg = cfg;
+    f.r = r;
+    f.q = &L.fq;
+    f.sc = sc;
+    f.sms = di.sms;
+    f.status = status;
+    f.x = static_cast<const uint16_t *>(x);
+    f.x_perm = x_perm;
+    f.W_gate = static_cast<const uint16_t *>(W_gate);
+    f.W_up = static_cast<const uint16_t *>(W_up);
+    f.W_down = static_cast<const uint16_t *>(W_down);
+    f.A = A;
+    f.G = G;
+    f.U = U;
+    f.A_w = A_w;
+    f.Y = Y;
+    f.saved = sv;
+    MOE_TRY(forward_mx(f, s));
+  } else {
+    MOE_TRY(timed("permute_rows", s, [&] {
+      return launch_permute_rows(static_cast<const uint16_t *>(x), r->row_of_slot, x_perm, T, H, k, s);
+    }));
+    GemmArgs g = gemm_base(cfg, r, di.sms, status);
+    g.x_perm = x_perm;
+    g.W_gate = static_cast<const uint16_t *>(W_gate);
+    g.W_up = static_cast<const uint16_t *>(W_up);
+    g.W_down = static_cast<const uint16_t *>(W_down);
+    g.w_row = r->w_row;
+    g.o0 = A;
+    const bool keep = kind != kFwdNoSave;  // G, U and A_w are only the backward's
+    g.o1 = keep ? G : nullptr;
+    g.o2 = keep ? U : nullptr;
+    g.o3 = keep ? A_w : nullptr;
+    MOE_TRY(timed(gemm_mode_name(kFwdGateUp), s, [&] { return launch_grouped_gemm(kFwdGateUp, g, s); }));
+    // the bf16 backward never reads Y (its router gradient comes from the dA GEMM),
+    // so a recompute for it stops after GEMM1; the fp8 modes' backward reads Y
+    if (kind == kFwdRecompute && cfg->precision == MOE_PREC_BF16) return MOE_OK;
+    g.act = A;
+    g.o0 = Y;
+    g.o1 = g.o2 = g.o3 = nullptr;
+    MOE_TRY(timed(gemm_mode_name(kFwdDown), s, [&] { return launch_grouped_gemm(kFwdDown, g, s); }));
+  }
+  if (kind == kFwdRecompute) return MOE_OK;
+  MOE_TRY(timed("combine", s, [&] {
+    return launch_gather_sum(Y, r->row_of_slot, r->topk_w, static_cast<uint16_t *>(out), T, H, k,
+                             s);
+  }));
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
 extern "C" {
 
 moe_status moe_query_workspace(const moe_config *cfg, size_t *route_scratch, size_t *saved,
@@ -560,76 +654,23 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const moe_routing *
                        const void *W_gate, const void *W_up, const void *W_down, void *out,
                        void *saved, size_t saved_bytes, void *scratch, size_t scratch_bytes,
                        void *stream) {
-  if (!shape_ok(cfg)) return MOE_ERR_INVALID_ARG;
-  MOE_TRY(check_routing(r, cfg->T));
-  if (!W_gate || !W_up || !W_down || !saved || !scratch || (cfg->T > 0 && (!x || !out)))
-    return MOE_ERR_INVALID_ARG;
-  if (!al16(x) || !al16(W_gate) || !al16(W_up) || !al16(W_down) || !al16(out) || !al16(saved) ||
-      !al16(scratch))
-    return MOE_ERR_ALIGNMENT;
-  const Layout L = layout_of(cfg);
-  if (saved_bytes < L.s_total || scratch_bytes < L.f_total) return MOE_ERR_WORKSPACE;
-  DevInfo di;
-  MOE_TRY(device_info(&di));
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint8_t *sc = static_cast<uint8_t *>(scratch);
-  uint8_t *sv = static_cast<uint8_t *>(saved);
-  if (cudaMemsetAsync(sc, 0, kHeader, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (cfg->T == 0) return MOE_OK;
-  const int T = cfg->T, H = cfg->H, k = cfg->k;
-  int32_t *status = reinterpret_cast<int32_t *>(sc);
-  uint16_t *x_perm = reinterpret_cast<uint16_t *>(sv + L.s_xperm);
-  uint16_t *G = reinterpret_cast<uint16_t *>(sv + L.s_G);
-  uint16_t *U = reinterpret_cast<uint16_t *>(sv + L.s_U);
-  uint16_t *A = reinterpret_cast<uint16_t *>(sv + L.s_A);
-  uint16_t *Y = reinterpret_cast<uint16_t *>(sv + L.s_Y);
-  uint16_t *A_w = reinterpret_cast<uint16_t *>(sv + L.s_Aw);
+  return moe::forward_impl(moe::kFwdFull, cfg, x, r, W_gate, W_up, W_down, out, saved, saved_bytes, scratch,
+                           scratch_bytes, stream);
+}
 
-  if (cfg->precision == MOE_PREC_MXFP8) {
-    Mx8Fwd f;
-    f.cfg = cfg;
-    f.r = r;
-    f.q = &L.fq;
-    f.sc = sc;
-    f.sms = di.sms;
-    f.status = status;
-    f.x = static_cast<const uint16_t *>(x);
-    f.x_perm = x_perm;
-    f.W_gate = static_cast<const uint16_t *>(W_gate);
-    f.W_up = static_cast<const uint16_t *>(W_up);
-    f.W_down = static_cast<const uint16_t *>(W_down);
-    f.A = A;
-    f.G = G;
-    f.U = U;
-    f.A_w = A_w;
-    f.Y = Y;
-    f.saved = sv;
-    MOE_TRY(forward_mx(f, s));
-  } else {
-    MOE_TRY(timed("permute_rows", s, [&] {
-      return launch_permute_rows(static_cast<const uint16_t *>(x), r->row_of_slot, x_perm, T, H, k, s);
-    }));
-    GemmArgs g = gemm_base(cfg, r, di.sms, status);
-    g.x_perm = x_perm;
-    g.W_gate = static_cast<const uint16_t *>(W_gate);
-    g.W_up = static_cast<const uint16_t *>(W_up);
-    g.W_down = static_cast<const uint16_t *>(W_down);
-    g.w_row = r->w_row;
-    g.o0 = A;
-    g.o1 = G;
-    g.o2 = U;
-    g.o3 = A_w;
-    MOE_TRY(timed(gemm_mode_name(kFwdGateUp), s, [&] { return launch_grouped_gemm(kFwdGateUp, g, s); }));
-    g.act = A;
-    g.o0 = Y;
-    g.o1 = g.o2 = g.o3 = nullptr;
-    MOE_TRY(timed(gemm_mode_name(kFwdDown), s, [&] { return launch_grouped_gemm(kFwdDown, g, s); }));
-  }
-  MOE_TRY(timed("combine", s, [&] {
-    return launch_gather_sum(Y, r->row_of_slot, r->topk_w, static_cast<uint16_t *>(out), T, H, k,
-                             s);
-  }));
-  return MOE_OK;
+moe_status moe_forward_nosave(const moe_config *cfg, const void *x, const moe_routing *r,
+                              const void *W_gate, const void *W_up, const void *W_down, void *out,
+                              void *saved, size_t saved_bytes, void *scratch, size_t scratch_bytes,
+                              void *stream) {
+  return moe::forward_impl(moe::kFwdNoSave, cfg, x, r, W_gate, W_up, W_down, out, saved, saved_bytes, scratch,
+                           scratch_bytes, stream);
+}
+
+moe_status moe_forward_recompute(const moe_config *cfg, const void *x, const moe_routing *r,
+                                 const void *W_gate, const void *W_up, const void *W_down, void *saved,
+                                 size_t saved_bytes, void *scratch, size_t scratch_bytes, void *stream) {
+  return moe::forward_impl(moe::kFwdRecompute, cfg, x, r, W_gate, W_up, W_down, nullptr, saved, saved_bytes,
+                           scratch, scratch_bytes, stream);
 }
 
 moe_status moe_backward(const moe_config *cfg, const void *dy, const void *x,

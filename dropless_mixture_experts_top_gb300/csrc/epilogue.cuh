@@ -136,11 +136,13 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, uint32_t tb, int ri
       }
       const size_t off = static_cast<size_t>(row0) * p.I + col;
       store_rows32(tile, p.o0 + off, p.I, nvalid, v0);
-      store_rows32(tile, p.o1 + off, p.I, nvalid, v1);
-      store_rows32(tile, p.o2 + off, p.I, nvalid, v2);
+      if (p.o1) {  // G, U and A_w are the backward's; a forward that saves nothing skips them
+        store_rows32(tile, p.o1 + off, p.I, nvalid, v1);
+        store_rows32(tile, p.o2 + off, p.I, nvalid, v2);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v0[i] *= w;  // A_w = w * A, the dW_down operand
-      store_rows32(tile, p.o3 + off, p.I, nvalid, v0);
+        for (int i = 0; i < 32; ++i) v0[i] *= w;  // A_w = w * A, the dW_down operand
+        store_rows32(tile, p.o3 + off, p.I, nvalid, v0);
+      }
     }
   } else if constexpr (MODE == kFwdDown || MODE == kBwdDX) {
     const int row0 = t.m0 + rit - lane;

@@ -27,7 +27,8 @@ _lib = None
 EXPORTED = [
     "moe_query_workspace", "moe_saved_offsets", "moe_fp8_scratch_offsets", "moe_mxfp8_forward_offsets",
     "moe_route",
-    "moe_route_static_scratch", "moe_forward", "moe_backward", "moe_get_device_status",
+    "moe_route_static_scratch", "moe_forward", "moe_forward_nosave", "moe_forward_recompute", "moe_backward",
+    "moe_get_device_status",
     "moe_status_string", "moe_timing_attach", "moe_timing_count", "moe_timing_label",
     "moe_selftest_wait_timeout", "moe_router_workspace", "moe_router_forward", "moe_router_backward",
 ]
@@ -85,6 +86,8 @@ def lib():
         L.moe_mxfp8_forward_offsets.argtypes = [P, P]
         L.moe_route.argtypes = [P, P, P, P, sz, P]
         L.moe_forward.argtypes = [P, P, P, P, P, P, P, P, sz, P, sz, P]
+        L.moe_forward_nosave.argtypes = [P, P, P, P, P, P, P, P, sz, P, sz, P]
+        L.moe_forward_recompute.argtypes = [P, P, P, P, P, P, P, sz, P, sz, P]
         L.moe_backward.argtypes = [P, P, P, P, P, P, P, P, sz, P, P, P, P, P, P, P, sz, P]
         L.moe_get_device_status.argtypes = [P, P, P]
         L.moe_selftest_wait_timeout.argtypes = [P, P]
@@ -197,11 +200,19 @@ def route(cfg, logits, routing: dict, scratch, stream=None):
                            scratch.numel(), _stream(stream)), "moe_route")
 
 
-def forward(cfg, x, routing: dict, W_gate, W_up, W_down, out, saved, scratch, stream=None):
+def forward(cfg, x, routing: dict, W_gate, W_up, W_down, out, saved, scratch, stream=None, save=True):
+    """moe_forward, or moe_forward_nosave when save is False (out only)."""
     rt = make_routing(routing)
-    _check(lib().moe_forward(ctypes.byref(cfg), _ptr(x), ctypes.byref(rt), _ptr(W_gate), _ptr(W_up),
-                             _ptr(W_down), _ptr(out), _ptr(saved), saved.numel(), _ptr(scratch),
-                             scratch.numel(), _stream(stream)), "moe_forward")
+    fn, name = (lib().moe_forward, "moe_forward") if save else (lib().moe_forward_nosave, "moe_forward_nosave")
+    _check(fn(ctypes.byref(cfg), _ptr(x), ctypes.byref(rt), _ptr(W_gate), _ptr(W_up), _ptr(W_down), _ptr(out),
+              _ptr(saved), saved.numel(), _ptr(scratch), scratch.numel(), _stream(stream)), name)
+
+
+def forward_recompute(cfg, x, routing: dict, W_gate, W_up, W_down, saved, scratch, stream=None):
+    rt = make_routing(routing)
+    _check(lib().moe_forward_recompute(ctypes.byref(cfg), _ptr(x), ctypes.byref(rt), _ptr(W_gate), _ptr(W_up),
+                                       _ptr(W_down), _ptr(saved), saved.numel(), _ptr(scratch), scratch.numel(),
+                                       _stream(stream)), "moe_forward_recompute")
 
 
 def backward(cfg, dy, x, routing: dict, W_gate, W_up, W_down, saved, dx, dW_gate, dW_up, dW_down,
@@ -379,11 +390,18 @@ class MoELayer:
     def route(self, logits, stream=None):
         route(self.cfg, logits, self.routing, self.route_scratch, stream)
 
-    def forward(self, x, W_gate, W_up, W_down, out=None, stream=None):
+    def forward(self, x, W_gate, W_up, W_down, out=None, stream=None, save=True):
+        """save=False: a checkpointed layer's first pass (out only; call recompute
+        before backward)."""
         if out is None:
             out = torch.empty((self.shape.T, self.shape.H), dtype=torch.int16, device=self.device)
-        forward(self.cfg, x, self.routing, W_gate, W_up, W_down, out, self.saved, self.fwd_scratch, stream)
+        forward(self.cfg, x, self.routing, W_gate, W_up, W_down, out, self.saved, self.fwd_scratch, stream,
+                save=save)
         return out
+
+    def recompute(self, x, W_gate, W_up, W_down, stream=None):
+        """What backward reads, rebuilt from the same inputs (no out)."""
+        forward_recompute(self.cfg, x, self.routing, W_gate, W_up, W_down, self.saved, self.fwd_scratch, stream)
 
     def backward(self, dy, x, W_gate, W_up, W_down, grads=None, stream=None):
         s = self.shape

@@ -184,6 +184,25 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const moe_routing *
                        void *saved, size_t saved_bytes, void *scratch, size_t scratch_bytes,
                        void *stream);
 
+/* Activation checkpointing (the pages' "2 fwd + bwd" layer step: the forward
+ * runs once without keeping its activations and again just before the
+ * backward).  Same arguments and errors as moe_forward.
+ * moe_forward_nosave writes out like moe_forward but skips what only the
+ * backward reads (bf16 and fp8_bwd: GEMM1's G, U and w*A are not written;
+ * mxfp8: the same work as moe_forward); `saved` is used as scratch and is not
+ * valid for moe_backward afterwards.  out is bit-identical to moe_forward's.
+ * moe_forward_recompute writes everything moe_backward reads into `saved`,
+ * and not out (bf16: the permute and GEMM1 only -- the bf16 backward never
+ * reads Y; the fp8 modes: GEMM2's Y too, no combine).  moe_backward after it
+ * gives results bit-identical to moe_backward after moe_forward. */
+moe_status moe_forward_nosave(const moe_config *cfg, const void *x, const moe_routing *routing,
+                              const void *W_gate, const void *W_up, const void *W_down, void *out,
+                              void *saved, size_t saved_bytes, void *scratch, size_t scratch_bytes,
+                              void *stream);
+moe_status moe_forward_recompute(const moe_config *cfg, const void *x, const moe_routing *routing,
+                                 const void *W_gate, const void *W_up, const void *W_down, void *saved,
+                                 size_t saved_bytes, void *scratch, size_t scratch_bytes, void *stream);
+
 /* Backward.  dy: device bf16 [T,H] (gradient of out); x: the forward's input
  * (must be unchanged); routing and saved as left by moe_route/moe_forward.
  * Outputs (device): dx bf16 [T,H]; dW_gate, dW_up bf16 [E,H,I]; dW_down bf16

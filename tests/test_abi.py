@@ -81,6 +81,12 @@ res["fwd_small_saved"] = L.moe_forward(ctypes.byref(c), a[0], ctypes.byref(r), a
                                        sv - 16, a[6], fs, None)
 res["fwd_misaligned"] = L.moe_forward(ctypes.byref(c), P(0x100008), ctypes.byref(r), a[1], a[2], a[3], a[4],
                                       a[5], sv, a[6], fs, None)
+res["nosave_null_out"] = L.moe_forward_nosave(ctypes.byref(c), a[0], ctypes.byref(r), a[1], a[2], a[3], None,
+                                              a[5], sv, a[6], fs, None)
+res["recompute_misaligned"] = L.moe_forward_recompute(ctypes.byref(c), P(0x100008), ctypes.byref(r), a[1], a[2],
+                                                      a[3], a[5], sv, a[6], fs, None)
+res["recompute_small_scratch"] = L.moe_forward_recompute(ctypes.byref(c), a[0], ctypes.byref(r), a[1], a[2],
+                                                         a[3], a[5], sv, a[6], fs - 16, None)
 res["bwd_null_dlogits"] = L.moe_backward(ctypes.byref(c), a[0], a[1], ctypes.byref(r), a[2], a[3], a[4], a[5],
                                          sv, a[6], a[7], a[8], a[9], None, None, a[10], bs, None)
 res["bwd_small_scratch"] = L.moe_backward(ctypes.byref(c), a[0], a[1], ctypes.byref(r), a[2], a[3], a[4], a[5],
@@ -89,7 +95,8 @@ print(repr(res))
 """
 
 EXPECTED = {"route_null_member": -1, "route_misaligned": -2, "route_small_scratch": -3,
-            "fwd_small_saved": -3, "fwd_misaligned": -2, "bwd_null_dlogits": -1, "bwd_small_scratch": -3}
+            "fwd_small_saved": -3, "fwd_misaligned": -2, "nosave_null_out": -1, "recompute_misaligned": -2,
+            "recompute_small_scratch": -3, "bwd_null_dlogits": -1, "bwd_small_scratch": -3}
 
 
 def test_validation_rejects_before_launch(L):
