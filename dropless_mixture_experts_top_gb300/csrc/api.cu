@@ -411,6 +411,7 @@ struct Mx8Fwd {
   const uint16_t *x, *W_gate, *W_up, *W_down;
   uint16_t *x_perm, *A, *G, *U, *A_w, *Y;
   uint8_t *saved;  // the backward's weight codes go here
+  bool keep;       // write what the backward reads (the bf16 activations, the weight codes)
 };
 
 moe_status forward_mx(const Mx8Fwd &f, cudaStream_t s) {
@@ -431,11 +432,11 @@ moe_status forward_mx(const Mx8Fwd &f, cudaStream_t s) {
   // each weight read once: along H for GEMM1 (transposed, interleaved) and
   // along I for the backward's dX (row by row, into `saved`)
   MOE_TRY(timed("mx_quant_W_gateup_fwd", s, [&] {
-    const cudaError_t e = launch_quant_wT(f.W_gate, E, H, I, 1, 0, sc + q.wgu_q, sc + q.wgu_sf, sf_b(2 * I),
-                                          RowCodes{f.saved + q.bwd_wg_q, f.saved + q.bwd_wg_sf, sf_b(H)}, s);
+    const RowCodes wg = f.keep ? RowCodes{f.saved + q.bwd_wg_q, f.saved + q.bwd_wg_sf, sf_b(H)} : RowCodes{};
+    const RowCodes wu = f.keep ? RowCodes{f.saved + q.bwd_wu_q, f.saved + q.bwd_wu_sf, sf_b(H)} : RowCodes{};
+    const cudaError_t e = launch_quant_wT(f.W_gate, E, H, I, 1, 0, sc + q.wgu_q, sc + q.wgu_sf, sf_b(2 * I), wg, s);
     if (e != cudaSuccess) return e;
-    return launch_quant_wT(f.W_up, E, H, I, 1, 1, sc + q.wgu_q, sc + q.wgu_sf, sf_b(2 * I),
-                           RowCodes{f.saved + q.bwd_wu_q, f.saved + q.bwd_wu_sf, sf_b(H)}, s);
+    return launch_quant_wT(f.W_up, E, H, I, 1, 1, sc + q.wgu_q, sc + q.wgu_sf, sf_b(2 * I), wu, s);
   }));
   MxGemmArgs m{};
   m.H = H;
@@ -452,17 +453,17 @@ moe_status forward_mx(const Mx8Fwd &f, cudaStream_t s) {
   m.sfa0 = sc + q.x_sf;
   m.b0 = sc + q.wgu_q;
   m.sfb0 = sc + q.wgu_sf;
-  m.o0 = f.A;
-  m.o1 = f.G;
-  m.o2 = f.U;
-  m.o3 = f.A_w;
+  m.o0 = f.keep ? f.A : nullptr;
+  m.o1 = f.keep ? f.G : nullptr;
+  m.o2 = f.keep ? f.U : nullptr;
+  m.o3 = f.keep ? f.A_w : nullptr;
   m.aq = sc + q.a_q;
   m.aq_sf = sc + q.a_sf;
   MOE_TRY(timed("mx_gemm_gateup_swiglu", s, [&] { return launch_mx_gemm(kMxGemmGateUp, m, s); }));
   MOE_TRY(timed("mx_quant_W_down_fwd", s, [&] {
     // along I for GEMM2 (transposed) and along H for the backward's dA (row by row, into `saved`)
     return launch_quant_wT(f.W_down, E, I, H, 0, 0, sc + q.wdt_q, sc + q.wdt_sf, sf_b(H),
-                           RowCodes{f.saved + q.bwd_wd_q, f.saved + q.bwd_wd_sf, sf_b(I)}, s);
+                           f.keep ? RowCodes{f.saved + q.bwd_wd_q, f.saved + q.bwd_wd_sf, sf_b(I)} : RowCodes{}, s);
   }));
   m.a0 = sc + q.a_q;
   m.sfa0 = sc + q.a_sf;
@@ -538,6 +539,7 @@ moe_status forward_impl(FwdKind kind, const moe_config *cfg, const void *x, cons
     f.A_w = A_w;
     f.Y = Y;
     f.saved = sv;
+    f.keep = kind != kFwdNoSave;
     MOE_TRY(forward_mx(f, s));
   } else {
     MOE_TRY(timed("permute_rows", s, [&] {

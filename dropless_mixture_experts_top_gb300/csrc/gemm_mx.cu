@@ -366,17 +366,22 @@ __device__ __forceinline__ void epilogue_gateup_mx(const MxTile &x, uint32_t tb,
     }
     const int col = ocol0 + 32 * j;
     const size_t off = static_cast<size_t>(row0) * p.I + col;
-    store_rows32(tile, p.o0 + off, p.I, nvalid, v0);
-    store_rows32(tile, p.o1 + off, p.I, nvalid, v1);
-    store_rows32(tile, p.o2 + off, p.I, nvalid, v2);
+    const bool keep = p.o0 != nullptr;  // the bf16 A, G, U, A_w are the backward's only
+    if (keep) {
+      store_rows32(tile, p.o0 + off, p.I, nvalid, v0);
+      store_rows32(tile, p.o1 + off, p.I, nvalid, v1);
+      store_rows32(tile, p.o2 + off, p.I, nvalid, v2);
+    }
 #pragma unroll
     for (int i = 0; i < 32; ++i) v1[i] = valid ? round_bf16(v0[i]) : 0.f;
     const int kb = col >> 5;
     p.aq_sf[sfi_base + (kb >> 2) * 512 + (kb & 3)] =
         quant32(v1, reinterpret_cast<uint4 *>(p.aq + static_cast<size_t>(prow) * p.I + col));
+    if (keep) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v0[i] *= w;  // A_w = w * A, the dW_down operand
-    store_rows32(tile, p.o3 + off, p.I, nvalid, v0);
+      for (int i = 0; i < 32; ++i) v0[i] *= w;  // A_w = w * A, the dW_down operand
+      store_rows32(tile, p.o3 + off, p.I, nvalid, v0);
+    }
   }
 }
 

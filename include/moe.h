@@ -189,7 +189,9 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const moe_routing *
  * backward).  Same arguments and errors as moe_forward.
  * moe_forward_nosave writes out like moe_forward but skips what only the
  * backward reads (bf16 and fp8_bwd: GEMM1's G, U and w*A are not written;
- * mxfp8: the same work as moe_forward); `saved` is used as scratch and is not
+ * mxfp8: GEMM1 writes only A's codes, not the bf16 A, G, U, w*A, and the
+ * weights are quantised for the forward GEMMs only); `saved` is used as
+ * scratch and is not
  * valid for moe_backward afterwards.  out is bit-identical to moe_forward's.
  * moe_forward_recompute writes everything moe_backward reads into `saved`,
  * and not out (bf16: the permute and GEMM1 only -- the bf16 backward never
