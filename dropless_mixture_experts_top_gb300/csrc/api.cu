@@ -816,15 +816,28 @@ bool router_shape_ok(const moe_config *c) {
   if (c->E < 8 || c->E > kMaxExperts || c->E % 8) return false;  // 16-byte rows for the TMA
   return true;
 }
-constexpr size_t kRouterOff = kHeader;            // int32 {0, T}: the single segment
-constexpr size_t kRouterMaps = kHeader + 256;     // 3 tensor maps for the weight gradient
-constexpr size_t kRouterDlog = kRouterMaps + 512; // bf16 d_logits [T,E]
+constexpr size_t kRouterSplit = kHeader;          // int32 [S + 1]: the weight gradient's token segments
+constexpr size_t kRouterMaps = kHeader + 256;     // 3 tensor maps per segment for the weight gradient
+// Backward scratch after the maps: fp32 partials [S][H][E] of the weight
+// gradient when it is split (S > 1), then bf16 d_logits [T,E].
+struct RouterBwdLayout {
+  int S;
+  size_t parts, dlog, total;
+};
+RouterBwdLayout router_bwd_layout(const moe_config *c) {
+  RouterBwdLayout L{};
+  L.S = router_dw_segments(c->T, c->H, c->E);
+  L.parts = kRouterMaps + align256(static_cast<size_t>(L.S) * kExpertMapBytes);
+  L.dlog = L.parts + (L.S > 1 ? align256(static_cast<size_t>(L.S) * c->H * c->E * 4) : 0);
+  L.total = L.dlog + align256(static_cast<size_t>(c->T) * c->E * 2);
+  return L;
+}
 }  // namespace
 
 moe_status moe_router_workspace(const moe_config *cfg, size_t *fwd_scratch, size_t *bwd_scratch) {
   if (!router_shape_ok(cfg)) return MOE_ERR_INVALID_ARG;
   if (fwd_scratch) *fwd_scratch = kRouterMaps;
-  if (bwd_scratch) *bwd_scratch = kRouterDlog + align256(static_cast<size_t>(cfg->T) * cfg->E * 2);
+  if (bwd_scratch) *bwd_scratch = router_bwd_layout(cfg).total;
   return MOE_OK;
 }
 
@@ -840,13 +853,10 @@ moe_status moe_router_forward(const moe_config *cfg, const void *x, const void *
   uint8_t *sc = static_cast<uint8_t *>(scratch);
   if (cudaMemsetAsync(sc, 0, kHeader, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (cfg->T == 0) return MOE_OK;
-  int32_t *seg = reinterpret_cast<int32_t *>(sc + kRouterOff);
-  MOE_TRY(timed("router_segment", s, [&] { return launch_one_segment(seg, cfg->T, s); }));
-  GemmArgs g{};
+  GemmArgs g{};  // no offsets: one segment of T rows
   g.M_rows = cfg->T;
   g.H = cfg->H;
   g.E = cfg->E;
-  g.offsets = seg;
   g.r_x = static_cast<const uint16_t *>(x);
   g.r_w = static_cast<const uint16_t *>(W_r);
   g.r_out = logits;
@@ -877,17 +887,17 @@ moe_status moe_router_backward(const moe_config *cfg, const void *x, const void 
       return MOE_ERR_CUDA;
     return MOE_OK;
   }
-  int32_t *seg = reinterpret_cast<int32_t *>(sc + kRouterOff);
-  uint16_t *dlog = reinterpret_cast<uint16_t *>(sc + kRouterDlog);
-  MOE_TRY(timed("router_segment", s, [&] { return launch_one_segment(seg, cfg->T, s); }));
+  const RouterBwdLayout RL = router_bwd_layout(cfg);
+  int32_t *split = reinterpret_cast<int32_t *>(sc + kRouterSplit);
+  uint16_t *dlog = reinterpret_cast<uint16_t *>(sc + RL.dlog);
+  float *parts = reinterpret_cast<float *>(sc + RL.parts);
   MOE_TRY(timed("router_dlogits_bf16", s, [&] {
-    return launch_to_bf16(d_logits, dlog, static_cast<int64_t>(cfg->T) * cfg->E, s);
+    return launch_router_dlogits(d_logits, dlog, static_cast<int64_t>(cfg->T) * cfg->E, split, cfg->T, RL.S, s);
   }));
-  GemmArgs g{};
+  GemmArgs g{};  // dx: no offsets, one segment of T rows
   g.M_rows = cfg->T;
   g.H = cfg->H;
   g.E = cfg->E;
-  g.offsets = seg;
   g.r_x = static_cast<const uint16_t *>(x);
   g.r_w = static_cast<const uint16_t *>(W_r);
   g.r_dlog = dlog;
@@ -897,7 +907,16 @@ moe_status moe_router_backward(const moe_config *cfg, const void *x, const void 
   g.status = reinterpret_cast<int32_t *>(sc);
   g.num_sms = di.sms;
   MOE_TRY(timed(gemm_mode_name(kRouterDX), s, [&] { return launch_grouped_gemm(kRouterDX, g, s); }));
+  // the weight gradient reduces over all T tokens into only ceil(H/256) x ceil(E/256)
+  // tiles: split the tokens into S segments (partials), then add them in order
+  g.offsets = split;
+  g.r_segments = RL.S;
+  g.r_out = RL.S > 1 ? parts : dW_r;
   MOE_TRY(timed(gemm_mode_name(kRouterDW), s, [&] { return launch_grouped_gemm(kRouterDW, g, s); }));
+  if (RL.S > 1)
+    MOE_TRY(timed("router_dW_sum", s, [&] {
+      return launch_sum_segments(parts, RL.S, static_cast<int64_t>(cfg->H) * cfg->E, dW_r, s);
+    }));
   return MOE_OK;
 }
 

@@ -183,8 +183,9 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, uint32_t tb, int ri
         tmem_ld32(tb + 32 * c, r0);
         tmem_ld_wait();
       }
-      if (rv) {
-        float *dst = p.of + static_cast<size_t>(row) * p.n_out + col;
+      if (rv) {  // dW_r split over token segments: segment t.e's partial at t.e * H rows
+        const size_t orow = MODE == kRouterDW ? static_cast<size_t>(t.e) * p.H + row : static_cast<size_t>(row);
+        float *dst = p.of + orow * p.n_out + col;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           if (col + 4 * q < p.n_out) {  // n_out is a multiple of 8
@@ -198,14 +199,19 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, uint32_t tb, int ri
       }
     }
   } else if constexpr (MODE == kRouterDX) {  // dx [rows, H] bf16 += accumulator
+    // K = E is short, so the tile's time is this read-modify-write of dx: the
+    // next chunk's rows (other columns) are loaded while this one is processed
     const int row0 = t.m0 + rit - lane;
     const int nvalid = clamp_rows(t.row_end - row0);
+    uint16_t *grow = p.o0 + static_cast<size_t>(row0) * p.H;
+    uint4 wn[4];
+    if (cb < ce && t.n0 + 32 * cb < p.H) load_rows32(grow + t.n0 + 32 * cb, p.H, nvalid, wn);
     for (int c = cb; c < ce; ++c) {
       const int col = t.n0 + 32 * c;
       if (col >= p.H) break;
-      uint4 w[4];
-      uint16_t *g0 = p.o0 + static_cast<size_t>(row0) * p.H + col;
-      load_rows32(g0, p.H, nvalid, w);
+      uint4 w[4] = {wn[0], wn[1], wn[2], wn[3]};
+      uint16_t *g0 = grow + col;
+      if (c + 1 < ce && col + 32 < p.H) load_rows32(g0 + 32, p.H, nvalid, wn);
       rows32_to_lanes(tile, w, v1);
       tmem_ld32(tb + 32 * c, r0);
       tmem_ld_wait();

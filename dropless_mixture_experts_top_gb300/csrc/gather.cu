@@ -332,35 +332,52 @@ cudaError_t launch_gather_sum(const uint16_t *rows, const int32_t *row_of_slot, 
 namespace {
 
 // Router projection backward: d_logits rounded to bf16 (nearest even) for the
-// two bf16 tensor-core products; four floats per thread.
-__global__ void __launch_bounds__(256) to_bf16_kernel(const float4 *__restrict__ in, uint2 *__restrict__ out,
-                                                      int64_t n4) {
+// two bf16 tensor-core products, four floats per thread; the first block also
+// writes the weight gradient's S token segments (S + 1 offsets, segment i =
+// tokens [T i / S, T (i+1) / S)).
+__global__ void __launch_bounds__(256) router_dlogits_kernel(const float4 *__restrict__ in, uint2 *__restrict__ out,
+                                                             int64_t n4, int32_t *split, int T, int S) {
+  if (blockIdx.x == 0 && static_cast<int>(threadIdx.x) <= S)
+    split[threadIdx.x] = static_cast<int32_t>(static_cast<int64_t>(T) * threadIdx.x / S);
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n4) return;
   const float4 v = __ldg(in + i);
   out[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
 }
 
-// The router projection's single "expert": offsets {0, T}.
-__global__ void one_segment_kernel(int32_t *offsets, int T) {
-  if (threadIdx.x == 0) {
-    offsets[0] = 0;
-    offsets[1] = T;
+// out[i] = sum over s of parts[s][i], s ascending (a fixed order: deterministic).
+__global__ void __launch_bounds__(256) sum_segments_kernel(const float4 *__restrict__ parts, int S, int64_t n4,
+                                                           float4 *__restrict__ out) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n4) return;
+  float4 a = __ldg(parts + i);
+  for (int s = 1; s < S; ++s) {
+    const float4 b = __ldg(parts + static_cast<int64_t>(s) * n4 + i);
+    a.x += b.x;
+    a.y += b.y;
+    a.z += b.z;
+    a.w += b.w;
   }
+  out[i] = a;
 }
 
 }  // namespace
 
-cudaError_t launch_to_bf16(const float *in, uint16_t *out, int64_t n, cudaStream_t s) {
-  const int64_t n4 = n / 4;  // n is a multiple of 8 (E % 8 == 0)
-  if (n4 == 0) return cudaSuccess;
-  to_bf16_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, s>>>(
-      reinterpret_cast<const float4 *>(in), reinterpret_cast<uint2 *>(out), n4);
+cudaError_t launch_router_dlogits(const float *d_logits, uint16_t *out, int64_t n, int32_t *split, int T, int S,
+                                  cudaStream_t s) {
+  if (S < 1 || S > 63) return cudaErrorInvalidValue;
+  const int64_t n4 = n / 4;  // n = T * E, a multiple of 8 (E % 8 == 0)
+  const int64_t blocks = (n4 + 255) / 256;
+  router_dlogits_kernel<<<static_cast<unsigned>(blocks > 0 ? blocks : 1), 256, 0, s>>>(
+      reinterpret_cast<const float4 *>(d_logits), reinterpret_cast<uint2 *>(out), n4, split, T, S);
   return cudaGetLastError();
 }
 
-cudaError_t launch_one_segment(int32_t *offsets, int T, cudaStream_t s) {
-  one_segment_kernel<<<1, 32, 0, s>>>(offsets, T);
+cudaError_t launch_sum_segments(const float *parts, int S, int64_t n, float *out, cudaStream_t s) {
+  const int64_t n4 = n / 4;  // n = H * E, a multiple of 8
+  if (n4 == 0) return cudaSuccess;
+  sum_segments_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, s>>>(
+      reinterpret_cast<const float4 *>(parts), S, n4, reinterpret_cast<float4 *>(out));
   return cudaGetLastError();
 }
 

@@ -50,15 +50,16 @@ __host__ __device__ constexpr int stage_bytes(int mode) { return halves_of(mode)
 constexpr int kBox = 64 * 64 * 2;             // one 64x64 bf16 box (MN-major pieces)
 constexpr int kMapsPerExpert = 3;             // ragged K: A, B0, B1
 // Warps: producer, MMA issuer, then 4 epilogue warps (one per TMEM lane
-// quarter).  The two epilogue-heavy modes run 8 (two per quarter, one per
-// column half): gate/up writes four outputs per element, and dA's dSwiGLU
-// reads G and U and writes dG and dU -- dA also has a warp that streams each
+// quarter).  The epilogue-heavy modes run 8 (two per quarter, one per column
+// half): gate/up writes four outputs per element, dA's dSwiGLU reads G and U
+// and writes dG and dU, and the router's dx reads and rewrites dx after a
+// K = E reduction too short to hide it -- dA also has a warp that streams each
 // tile's G and U into a shared-memory ring ahead of its epilogue, and an
 // operand ring of 5 stages to make room.  The other modes run slower with 8
 // epilogue warps.
 __host__ __device__ constexpr int stages_of(int mode) { return mode == kBwdDA ? 5 : 3; }
 __host__ __device__ constexpr int epi_warps(int mode) {
-  return (mode == kBwdDA || mode == kFwdGateUp) ? 8 : 4;
+  return (mode == kBwdDA || mode == kFwdGateUp || mode == kRouterDX) ? 8 : 4;
 }
 __host__ __device__ constexpr int gu_warps(int mode) { return mode == kBwdDA ? 1 : 0; }
 __host__ __device__ constexpr int threads_of(int mode) {
@@ -260,7 +261,9 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
     tma_prefetch_desc(&tmB1);
   }
   if (warp == 1) tmem_alloc_pair(tmem_slot, kTmemCols);
-  for (int e = threadIdx.x; e <= E; e += threads_of(MODE)) s_off[e] = __ldg(p.offsets + e);
+  // no offsets: one segment of all M_rows rows (the router projection's logits and dx)
+  for (int e = threadIdx.x; e <= E; e += threads_of(MODE))
+    s_off[e] = p.offsets ? __ldg(p.offsets + e) : (e == 0 ? 0 : p.M_rows);
   __syncthreads();
   if (Tr::kRaggedK) {
     // Skewed routing (an expert with more than twice the mean rows): longest
@@ -566,7 +569,7 @@ cudaError_t launch_mode(const GemmArgs &a, cudaStream_t s) {
   // router modes: a.E is the router's output width, the GEMM sees one expert
   const uint64_t E_out = a.E;
   const bool router = MODE == kRouterFwd || MODE == kRouterDX || MODE == kRouterDW;
-  p.E = router ? 1 : a.E;
+  p.E = router ? (MODE == kRouterDW ? (a.r_segments > 0 ? a.r_segments : 1) : 1) : a.E;
   p.of = a.r_out;
   p.n_out = a.E;
   bool ok = true;
@@ -699,6 +702,15 @@ cudaError_t launch_grouped_gemm(GemmMode mode, const GemmArgs &a, cudaStream_t s
     case kRouterDW: return launch_mode<kRouterDW>(a, s);
   }
   return cudaErrorInvalidValue;
+}
+
+int router_dw_segments(int T, int H, int E) {
+  constexpr int kPairs = 76;  // CTA pairs of a 152-SM part
+  const int tiles = ((H + 2 * BM - 1) / (2 * BM)) * ((E + 255) / 256);
+  int S = kPairs / (tiles > 0 ? tiles : 1);
+  S = S < T / 1024 ? S : T / 1024;
+  S = S < 32 ? S : 32;
+  return S > 1 ? S : 1;
 }
 
 const char *gemm_mode_name(GemmMode mode) {

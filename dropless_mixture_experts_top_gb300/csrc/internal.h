@@ -66,8 +66,12 @@ cudaError_t launch_permute_rows(const uint16_t *x, const int32_t *row_of_slot, u
 cudaError_t launch_gather_sum(const uint16_t *rows, const int32_t *row_of_slot, const float *w,
                               uint16_t *out, int T, int H, int k, cudaStream_t s);
 // router projection: fp32 -> bf16 (nearest even), n % 4 == 0; offsets {0, T}
-cudaError_t launch_to_bf16(const float *in, uint16_t *out, int64_t n, cudaStream_t s);
-cudaError_t launch_one_segment(int32_t *offsets, int T, cudaStream_t s);
+// the router's d_logits [T,E] fp32 -> bf16 (n = T * E), and split = the S + 1
+// offsets of S equal token segments for the weight gradient (S <= 63)
+cudaError_t launch_router_dlogits(const float *d_logits, uint16_t *out, int64_t n, int32_t *split, int T, int S,
+                                  cudaStream_t s);
+// out [n] = sum over s of parts [S][n], in order of s (n a multiple of 8)
+cudaError_t launch_sum_segments(const float *parts, int S, int64_t n, float *out, cudaStream_t s);
 // d_logits and d_topk_w from g computed in the bf16 dA epilogue: g[r] = the sum
 // of the np partials g_part[r * np + p]
 cudaError_t launch_router_grad(const int32_t *row_of_slot, const int32_t *topk_idx, const float *topk_w,
@@ -111,12 +115,16 @@ struct GemmArgs {
   // router projection: x [T,H], W_r [H,E], d_logits as bf16 [T,E]; fp32 output, its columns
   const uint16_t *r_x, *r_w, *r_dlog;
   float *r_out;
+  int r_segments;  // dW_r: token segments reduced separately (offsets[0..S]), partials [S][H][E] in r_out
   int32_t *status;
   void *map_scratch;  // ragged K: device scratch for E * 3 tensor maps (128 B each, 128-B aligned)
   int num_sms;
 };
 constexpr size_t kExpertMapBytes = 3 * 128;  // per expert
 cudaError_t launch_grouped_gemm(GemmMode mode, const GemmArgs &a, cudaStream_t s);
+// dW_r = x^T . d_logits split over the tokens: how many segments keep every CTA
+// pair of the part (152 SMs) busy, at least 1024 tokens each; 1 = no split.
+int router_dw_segments(int T, int H, int E);
 const char *gemm_mode_name(GemmMode mode);
 
 // ---- MXFP8 backward (mxfp8.cu, gemm_mx.cu)

@@ -27,10 +27,11 @@ def dev16(a):
 
 SHAPES = [MoEShape(T=1000, H=256, I=64, E=64, k=2),   # several M tiles, E below one tile
           MoEShape(T=333, H=192, I=64, E=136, k=4),   # H with an odd count of 64-blocks, E % 64 != 0
-          MoEShape(T=4096, H=2048, I=64, E=128, k=8)]  # the 30B router's width and depth
+          MoEShape(T=4096, H=2048, I=64, E=128, k=8),  # the 30B router's width and depth (dW_r in 4 segments)
+          MoEShape(T=5000, H=256, I=64, E=64, k=2)]    # dW_r in 4 segments of 1250 tokens (ragged K tails)
 
 
-@pytest.mark.parametrize("shape", SHAPES, ids=["t1000_e64", "t333_e136", "t4096_h2048"])
+@pytest.mark.parametrize("shape", SHAPES, ids=["t1000_e64", "t333_e136", "t4096_h2048", "t5000_split4"])
 def test_router_projection_matches_oracle(shape):
     rng = np.random.default_rng(81)
     x = f32_to_bf16_bits(rng.standard_normal((shape.T, shape.H)).astype(np.float32))
