@@ -44,6 +44,11 @@ def test_router_projection_matches_oracle(shape):
     dW = r.backward(dev16(x), dev16(W_r), torch.from_numpy(d_logits).cuda(), dx)
     torch.cuda.synchronize()
     assert r.status() == {"forward": 0, "backward": 0}
+    # dW_r does not read dx: a second backward gives the same bits (split
+    # weight gradients are added in a fixed order)
+    dW2 = r.backward(dev16(x), dev16(W_r), torch.from_numpy(d_logits).cuda(), dev16(dx0))
+    torch.cuda.synchronize()
+    assert torch.equal(dW2, dW)
     ref_lg = O.router_forward(x, W_r)
     G.close("logits", lg.cpu().numpy(), ref_lg, rel_l2=1e-5, max_rel=1e-4)
     ref_dW, ref_dx = O.router_backward(x, W_r, d_logits.astype(np.float64))
