@@ -518,11 +518,26 @@ def run_ours(args):
                 router.backward(d["x"], W_r, grads["d_logits"], grads["dx"], dW_r, stream=stream)
                 ev[3 * i + 2].record(stream)
         torch.cuda.synchronize()
+        # a second pass with per-kernel events (they add gaps, so not in the totals above)
+        rkev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * 8 * K)]
+        moe.timing_attach(rkev)
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                flush.zero_()
+                router.forward(d["x"], W_r, logits_r, stream=stream)
+                router.backward(d["x"], W_r, grads["d_logits"], grads["dx"], dW_r, stream=stream)
+        torch.cuda.synchronize()
+        rlabels = [moe.timing_label(i) for i in range(moe.timing_count())]
+        moe.timing_attach(None)
+        rk = {}
+        for i, lab in enumerate(rlabels):
+            rk.setdefault(lab, []).append(rkev[2 * i].elapsed_time(rkev[2 * i + 1]))
         if any(router.status(stream).values()):
             raise RuntimeError(f"router status: {router.status(stream)}")
         router_ms = {"fwd_ms": statistics.mean(ev[3 * i].elapsed_time(ev[3 * i + 1]) for i in range(K)),
                      "bwd_ms": statistics.mean(ev[3 * i + 1].elapsed_time(ev[3 * i + 2]) for i in range(K)),
-                     "flop_per_step": 3 * 2.0 * shape.T * shape.H * shape.E}
+                     "flop_per_step": 3 * 2.0 * shape.T * shape.H * shape.E,
+                     "kernels_avg_ms": {lab: statistics.mean(v) for lab, v in rk.items()}}
     st = layer.status(stream)
     if any(st.values()):
         raise RuntimeError(f"device status after timed steps: {st}")
