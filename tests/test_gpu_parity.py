@@ -149,3 +149,37 @@ def test_cuda_graph_capture_and_replay_with_new_routing(precision):
     g.replay()
     torch.cuda.synchronize()
     G.check_full(shape, inp2, layer, out, grads, precision=precision)
+
+
+@pytest.mark.parametrize("precision", ["bf16", "fp8_bwd", "mxfp8"])
+def test_cuda_graph_checkpointed_step(precision):
+    """The activation-checkpointed sequence (route, forward without saving,
+    recompute, backward) captured once and replayed with new routing."""
+    shape = MoEShape(T=512, H=128, I=128, E=8, k=2)
+    inp = synth.make_inputs_shape(shape, 61)
+    t = G.to_dev(inp)
+    layer = moe.MoELayer(shape, precision=precision)
+    s = torch.cuda.Stream()
+    out = torch.empty((shape.T, shape.H), dtype=torch.int16, device="cuda")
+
+    def step(grads=None):
+        layer.route(t["logits"], s)
+        layer.forward(t["x"], t["W_gate"], t["W_up"], t["W_down"], out=out, stream=s, save=False)
+        layer.recompute(t["x"], t["W_gate"], t["W_up"], t["W_down"], stream=s)
+        return layer.backward(t["dy"], t["x"], t["W_gate"], t["W_up"], t["W_down"], grads=grads, stream=s)
+
+    with torch.cuda.stream(s):  # warm-up outside capture (first-call attribute setup)
+        grads = step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step(grads)
+    inp2 = dict(inp)
+    lg = np.random.default_rng(6).standard_normal(inp["logits"].shape).astype(np.float32)
+    lg[:, 5] -= 50.0  # an empty expert
+    inp2["logits"] = lg
+    t["logits"].copy_(torch.from_numpy(lg).cuda())
+    g.replay()
+    torch.cuda.synchronize()
+    assert layer.status() == {"route": 0, "forward": 0, "backward": 0}
+    G.check_full(shape, inp2, layer, out, grads, precision=precision, check_saved=False)
