@@ -159,6 +159,14 @@ def test_fp8_shapes_and_layout(L):
 def test_router_workspace_and_shapes(L):
     f, b = moe.router_workspace(moe.Config(300, 256, 64, 16, 2, 0))
     assert f >= 512 and b >= f + 300 * 16 * 2
+    # the weight gradient of a long batch is split over token segments: its fp32
+    # partials are part of the backward workspace (9 of [H,E] at the 30B shape,
+    # filling the 76 CTA pairs with 8 tiles each; none below 2048 tokens)
+    T, H, E = 16384, 2048, 128
+    _, b_split = moe.router_workspace(moe.Config(T, H, 64, E, 8, 0))
+    assert b_split >= 9 * H * E * 4 + T * E * 2
+    _, b_short = moe.router_workspace(moe.Config(2047, H, 64, E, 8, 0))
+    assert b_short < H * E * 4 + 2047 * E * 2 + 16384
     for bad in (dict(E=12), dict(E=4), dict(H=96)):  # E % 8, E >= 8, H % 64
         c = moe.Config(300, bad.get("H", 256), 64, bad.get("E", 16), 2, 0)
         assert L.moe_router_workspace(ctypes.byref(c), None, None) == -1
