@@ -11,7 +11,11 @@ inside the timed region).  Each timed step is bracketed by CUDA events on the
 library's stream; an L2 flush (256 MiB write) runs between steps, outside the
 events.  `roofline` covers the kernel with the largest share of step time, timed
 live with per-kernel events.  `cpu_baseline` is the fp64 oracle timed on this
-host's cores on a bounded sub-batch.
+host's cores on a bounded sub-batch.  Also reported: `ckpt_2f_plus_b_ms`, the
+activation-checkpointed step (route, a forward that keeps no activations, the
+recompute of what the backward reads, the backward); `no_l2_flush`, the step
+without the flush; `router_projection`, the router's linear layer in front of
+the layer (logits = x . W_r and its backward), totals and per kernel.
 
 --impl reference times that oracle alone (the only reference this method has:
 the pages publish no runnable code), on bounded sub-batches of the same workload.
