@@ -16,17 +16,20 @@
 //
 // Kernel structure: clusters of two CTAs (a CTA pair on two SMs), persistent,
 // static round-robin over 256x256 output tiles.  Each CTA holds 128 rows of A
-// and 128 columns of B in a 6-stage shared-memory ring, so each SM reads half
-// the B operand it would need alone; the pair's MMAs (cta_group::2, M=256,
-// N=256, K=16, bf16 in, fp32 accumulate) are issued by the first CTA and write
-// each CTA's 128 accumulator rows into its own TMEM.
+// and 128 columns of B in a shared-memory ring (3 stages of 128 of K; dA: 5
+// stages of 64 of K, its shared memory also holding a G/U ring), so each SM
+// reads half the B operand it would need alone; the pair's MMAs (cta_group::2,
+// M=256, N=256, K=16, bf16 in, fp32 accumulate) are issued by the first CTA and
+// write each CTA's 128 accumulator rows into its own TMEM.
 //   warp 0      TMA producer (both CTAs): 128B-swizzled boxes into its ring;
 //               both CTAs' copies complete on CTA 0's barrier
 //   warp 1      CTA 0: MMA issuer (CTA 1's warp 1 only shares the TMEM allocation)
 //   warps 2..    epilogue (both CTAs): tcgen05.ld of its 128 rows from two
 //               double-buffered 256-column accumulators, fused SwiGLU /
 //               dSwiGLU, bf16 stores; 4 warps (one per TMEM lane quarter), 8
-//               for dA (two per quarter, one per column half)
+//               (two per quarter, one per column half) for the modes with the
+//               heaviest epilogues: gate/up, dA and the router's dx
+//   dA only     one more warp streams each tile's G and U into the G/U ring
 // Every wait is bounded; on a timeout the kernel flags the status word,
 // drains its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>

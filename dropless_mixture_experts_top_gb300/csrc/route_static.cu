@@ -26,19 +26,25 @@ constexpr size_t kStaticRouteScratchBytes = (size_t{5} << 19) + 4096;
 static __device__ __align__(256) uint8_t g_route_scratch[kStaticRouteScratchBytes];
 
 // In host code g_route_scratch names a host-side stand-in, not a device address.
-// The device address is looked up once per device, with that device current.
+// The device address is looked up with the device current and cached per
+// device only once a lookup has succeeded; a failed lookup (for example a first
+// call made while the stream is being captured) is retried by the next call.
+std::mutex g_scratch_mu;
 void *g_scratch_addr[kMaxDevices];
-cudaError_t g_scratch_err[kMaxDevices];
-std::once_flag g_scratch_once[kMaxDevices];
 
 cudaError_t static_scratch(int dev, void **out) {
-  std::call_once(g_scratch_once[dev], [dev] {
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
     void *p = nullptr;
-    g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_route_scratch);
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_route_scratch);
+    if (e != cudaSuccess || !p) {
+      cudaGetLastError();  // leave no error behind for the next launcher to report
+      return e != cudaSuccess ? e : cudaErrorInvalidSymbol;
+    }
     g_scratch_addr[dev] = p;
-  });
+  }
   *out = g_scratch_addr[dev];
-  return g_scratch_err[dev];
+  return cudaSuccess;
 }
 
 }  // namespace

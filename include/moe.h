@@ -41,7 +41,9 @@
  *     ran out of time) set flags in a status word at the start of the call's
  *     scratch buffer; kernels never trap.  Read it with moe_get_device_status.
  *   - The library holds no per-call state; calls on different streams with
- *     disjoint buffers may run concurrently.
+ *     disjoint buffers may run concurrently.  Two exceptions, both opt-in:
+ *     the per-kernel timing hook (moe_timing_attach, process-wide while
+ *     attached) and moe_route_static_scratch's one shared scratch array.
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H
@@ -98,7 +100,11 @@ typedef struct {
   float *w_row;         /* [M]    router weight of permuted row r */
 } moe_routing;
 
-/* Byte sizes of the caller-provided buffers for a configuration:
+/* Byte sizes of the caller-provided buffers for a configuration.  The fused
+ * kernel of the pages works through preallocated GPU scratch space instead of
+ * allocating intermediates per call (the MarkTechPost article in Thai
+ * translation, "how the fused kernel works"); here the caller allocates that
+ * space once, sized by this call, and passes it to every call:
  *   route_scratch: moe_route's scratch;
  *   saved:        activations moe_forward keeps for moe_backward (layout below);
  *   fwd_scratch:  moe_forward's scratch;  bwd_scratch: moe_backward's scratch.
@@ -167,7 +173,11 @@ typedef struct {
 moe_status moe_mxfp8_forward_offsets(const moe_config *cfg, moe_mxfp8_fwd_layout *layout);
 
 /* Router and dispatch indices.  logits: device fp32 [T,E].  Writes every field
- * of *routing.  Per-expert counts, the scan and the permutation are computed
+ * of *routing.  Dropless routing gives per-expert group sizes that change
+ * every step; they stay on the device and the grouped GEMMs read them there,
+ * so no host copy breaks CUDA-graph capture (NVIDIA article "DeepSeek-V3 MoE
+ * from 103 to 1,068 TFLOPS", "optimisations dropless needs" and "grouped
+ * GEMM").  Per-expert counts, the scan and the permutation are computed
  * on the device in one pass over the logits (two kernels: per-block expert
  * histograms and ranks, then every block scans the histograms itself and
  * writes its slots' rows).  Non-finite logits set
@@ -247,9 +257,11 @@ moe_status moe_router_backward(const moe_config *cfg, const void *x, const void 
  * allocating library call).
  * device_status: optional device int32 that receives the call's MOE_DEV_* flags
  * (copied on `stream` after the routing kernels); NULL to skip.
- * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture.  All calls share the one array and it keeps the last call's
+ * The first call on a device looks up the array's device address (with that
+ * device current) and keeps it for the process; make that first call before
+ * any stream capture.  If the lookup fails the call returns MOE_ERR_CUDA with
+ * nothing launched and no CUDA error left pending, and the next call on that
+ * device looks the address up again.  All calls share the one array and it keeps the last call's
  * contents: calls that overlap on the GPU (for example on two streams) race,
  * so serialise them. */
 moe_status moe_route_static_scratch(const moe_config *cfg, const float *logits,
