@@ -34,8 +34,8 @@ constexpr size_t kHeader = 256;  // status word at offset 0
 inline size_t align256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
 
 struct Layout {
-  // route scratch
-  size_t r_lrank, r_hist, r_total;
+  // route scratch (r_zero: bytes from the start that each call zeroes: header and tickets)
+  size_t r_tickets, r_lrank, r_hist, r_gpref, r_zero, r_total;
   // saved
   size_t s_xperm, s_G, s_U, s_A, s_Y, s_Aw, s_total;
   // forward scratch
@@ -79,11 +79,17 @@ Layout layout_of(const moe_config *c) {
   Layout L{};
   const size_t T = c->T, H = c->H, I = c->I, E = c->E, k = c->k, M = T * k;
   const size_t nblk = static_cast<size_t>(route_num_blocks(c->T));
+  const size_t ngroups = static_cast<size_t>(route_scan_groups(c->T));
   size_t o = kHeader;
+  L.r_tickets = o;
+  o += align256((1 + ngroups) * 4);
+  L.r_zero = o;
   L.r_lrank = o;
-  o += align256(M * 4);
+  o += align256(M);
   L.r_hist = o;
   o += align256(nblk * E * 4);
+  L.r_gpref = o;
+  o += align256(ngroups * E * 4);
   L.r_total = o;
   o = 0;
   L.s_xperm = o;
@@ -625,7 +631,7 @@ moe_status moe_route(const moe_config *cfg, const float *logits, const moe_routi
   MOE_TRY(device_info(&di));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t *sc = static_cast<uint8_t *>(scratch);
-  if (cudaMemsetAsync(sc, 0, kHeader, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(sc, 0, L.r_zero, s) != cudaSuccess) return MOE_ERR_CUDA;  // status and scan tickets
   if (cfg->T == 0) {  // no tokens: empty groups
     if (cudaMemsetAsync(r->counts, 0, sizeof(int32_t) * cfg->E, s) != cudaSuccess ||
         cudaMemsetAsync(r->offsets, 0, sizeof(int32_t) * (cfg->E + 1), s) != cudaSuccess)
@@ -644,8 +650,10 @@ moe_status moe_route(const moe_config *cfg, const float *logits, const moe_routi
   a.row_of_slot = r->row_of_slot;
   a.slot_of_row = r->slot_of_row;
   a.w_row = r->w_row;
-  a.lrank = reinterpret_cast<int32_t *>(sc + L.r_lrank);
+  a.lrank = sc + L.r_lrank;
   a.hist = reinterpret_cast<int32_t *>(sc + L.r_hist);
+  a.gpref = reinterpret_cast<int32_t *>(sc + L.r_gpref);
+  a.tickets = reinterpret_cast<int32_t *>(sc + L.r_tickets);
   a.status = reinterpret_cast<int32_t *>(sc);
   MOE_TRY(timed("route_topk", s, [&] { return launch_route_topk(a, s); }));
   MOE_TRY(timed("route_index", s, [&] { return launch_route_index(a, s); }));

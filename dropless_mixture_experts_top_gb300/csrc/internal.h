@@ -37,8 +37,8 @@ constexpr int32_t kDevNonfiniteLogit = 0x1;
 constexpr int32_t kDevWaitTimeout = 0x2;
 
 // ---- routing (route.cu)
-constexpr int kRouteTokensPerBlock = 128;  // tokens per route block (one histogram row)
-constexpr int kRouteThreads = 512;
+constexpr int kRouteTokensPerBlock = 64;  // tokens per route block (one histogram row)
+constexpr int kRouteThreads = 256;        // four per token; at least kMaxExperts
 
 struct RouteArgs {
   const float *logits;  // [T,E]
@@ -50,11 +50,14 @@ struct RouteArgs {
   int32_t *row_of_slot; // [T*k]
   int32_t *slot_of_row; // [T*k]
   float *w_row;         // [T*k]
-  int32_t *lrank;       // [T*k] scratch: rank of a slot among its block's slots of the same expert
-  int32_t *hist;        // [nblk,E] scratch: per-block expert histogram
+  uint8_t *lrank;       // [T*k] scratch: rank of a slot among its block's slots of the same expert
+  int32_t *hist;        // [nblk,E] scratch: per-block expert histogram, then its prefix inside its scan group
+  int32_t *gpref;       // [ngroups,E] scratch: group totals, then their exclusive prefix over groups
+  int32_t *tickets;     // [1 + ngroups] scratch, zero on entry: arrival counters of the scan
   int32_t *status;      // scratch status word
 };
 int route_num_blocks(int T);
+int route_scan_groups(int T);
 cudaError_t launch_route_topk(const RouteArgs &a, cudaStream_t s);
 cudaError_t launch_route_index(const RouteArgs &a, cudaStream_t s);
 

@@ -9,23 +9,31 @@
 // see keep CUDA graphs usable).
 //
 // Two kernels:
-//   route_topk  : the block's 128 tokens' logits staged in shared memory (all
-//                 of a thread's loads issued before the first store);
-//                 four threads per token each take every fourth expert, sort
-//                 them KMAX at a time with a bitonic network and keep the best
-//                 KMAX (bitonic top-k merge); the four lists merge by two
-//                 shuffle rounds.  Ties -> lower expert.  fp32 renormalised
+//   route_topk  : the block's 64 tokens' logits staged in shared memory (all
+//                 of a thread's loads issued before the first store); four
+//                 threads per token, each taking every fourth expert.  Each
+//                 thread keeps the KMAX/4 largest of its logits (values only,
+//                 two min/max per logit); the smallest of those over the four
+//                 threads is a threshold with at least KMAX >= k logits at or
+//                 above it, so the top k are among them.  Only those
+//                 candidates (typically a tenth of the row) enter a sorted
+//                 KMAX list per thread; the four lists merge by two shuffle
+//                 rounds (bitonic).  Ties -> lower expert.  fp32 renormalised
 //                 weights.  Every token's chosen experts set one bit in a
 //                 per-expert bitmask over the block's tokens, so a slot's rank
-//                 inside its (block, expert) run, in token order, is a
-//                 popcount and the block's expert histogram a sum of them.
-//                 Single pass over the logits.
-//   route_index : one block per route block: every block sums the histogram
-//                 columns (below its own row, and in total), scans the totals
-//                 over experts (counts, offsets; block 0 writes them), and
-//                 writes its slots' rows: row = offsets[e] + the rows of
-//                 expert e in earlier blocks + rank; row_of_slot, slot_of_row,
-//                 w_row.  The kernel boundary is the only grid-wide wait.
+//                 in its (block, expert) run is a popcount (one byte per slot)
+//                 and the block's histogram row the masks' popcounts.  The
+//                 scan over blocks runs in the same launch without any block
+//                 waiting for another: the last block of each group of 32 to
+//                 finish (an atomic ticket) turns the group's histogram rows
+//                 into exclusive prefixes inside the group and writes the
+//                 group's totals; the last group to finish scans the group
+//                 totals over groups (exclusive) and the expert totals over
+//                 experts (counts, offsets).  Every histogram entry is read
+//                 twice, so the scan is linear in T.
+//   route_index : one thread per slot: row = offsets[e] + the prefix of its
+//                 group + the prefix of its block inside the group + its rank;
+//                 row_of_slot, slot_of_row, w_row.
 // The resulting permutation is expert-major and token-ascending inside an
 // expert, so it is unique and reproducible bit for bit.
 #include <math.h>
@@ -41,7 +49,7 @@ constexpr int kQ = kRouteThreads / TB;      // threads per token (4): each takes
 constexpr int kTokPerWarp = 32 / kQ;        // tokens of one warp (8); a token's threads are kTokPerWarp lanes apart
 constexpr int kMaskWords = TB / 32;         // words of a per-expert token bitmask
 constexpr int kLoadBatch = 8;               // float4 loads a thread has in flight while staging
-constexpr int kHistLoads = 32;              // histogram loads a route_index thread has in flight
+constexpr int kScanGroup = 32;              // route blocks per scan group (one load each in flight)
 
 // (x, xi) ranks before (y, yi): larger logit first, lower expert index on
 // ties; an empty slot (index INT_MAX, value -inf) ranks after everything.
@@ -103,7 +111,7 @@ __device__ __forceinline__ void merge_best(float (&av)[N], int (&ai)[N], const f
 }
 
 // The block's logits [n / E, E] (contiguous in memory, 16-byte aligned: the
-// block's first token is a multiple of 128) into shared memory rows of S
+// block's first token is a multiple of 64) into shared memory rows of S
 // floats.  Each thread issues kLoadBatch 16-byte loads before its first
 // store, so the block waits for one round trip to memory, not one per load.
 // A NaN is staged as -inf (the selection stays well defined); returns whether
@@ -170,11 +178,13 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(RouteArgs a) 
   extern __shared__ __align__(16) float s_lg[];           // [TB][E + 4] this block's logits
   __shared__ uint32_t s_emask[kMaxExperts][kMaskWords];  // tokens of this block that chose expert e
   __shared__ uint8_t s_slot_e[TB * kMaxTopK];            // expert of each of the block's slots
+  __shared__ int s_last;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = a.E, k = a.k, T = a.T;
   const int S = logit_stride(E);
-  const int t0 = blockIdx.x * TB;
+  const int b = blockIdx.x, nblk = gridDim.x;
+  const int t0 = b * TB;
   const int ntok = min(TB, T - t0);
 
   for (int i = threadIdx.x; i < E * kMaskWords; i += kRouteThreads) (&s_emask[0][0])[i] = 0u;
@@ -185,8 +195,27 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(RouteArgs a) 
   // takes experts qq, qq + kQ, qq + 2kQ, ...
   {
     const int tl = warp * kTokPerWarp + lane % kTokPerWarp, qq = lane / kTokPerWarp;
-    const int nm = tl < ntok ? (E - qq + kQ - 1) / kQ : 0;  // this quarter's experts
+    const int nm = tl < ntok ? (E - qq + kQ - 1) / kQ : 0;  // this quarter's experts (<= 64)
     const float *row = s_lg + tl * S;
+    // the quarter's MQ largest logits, descending (-inf while it has fewer)
+    constexpr int MQ = KMAX / kQ;
+    float qmax[MQ];
+#pragma unroll
+    for (int j = 0; j < MQ; ++j) qmax[j] = -INFINITY;
+    for (int m = 0; m < nm; ++m) {
+      const float v = row[qq + kQ * m];
+#pragma unroll
+      for (int j = MQ - 1; j > 0; --j) qmax[j] = fmaxf(qmax[j], fminf(qmax[j - 1], v));
+      qmax[0] = fmaxf(qmax[0], v);
+    }
+    // every quarter holds MQ logits >= its qmax[MQ-1] (or has fewer, and then
+    // tau is -inf): at least kQ * MQ = KMAX >= k logits are >= tau, so the k-th
+    // largest is too, and every logit of the top k is a candidate
+    float tau = qmax[MQ - 1];
+#pragma unroll
+    for (int o = kTokPerWarp; o < 32; o <<= 1) tau = fminf(tau, __shfl_xor_sync(0xffffffffu, tau, o));
+    uint64_t cand = 0;
+    for (int m = 0; m < nm; ++m) cand |= static_cast<uint64_t>(row[qq + kQ * m] >= tau) << m;
     float tv[KMAX];
     int ti[KMAX];
 #pragma unroll
@@ -194,25 +223,23 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(RouteArgs a) 
       tv[j] = -INFINITY;
       ti[j] = INT_MAX;
     }
-    for (int m0 = 0; m0 < nm; m0 += KMAX) {
-      float cv[KMAX];
-      int ci[KMAX];
+    while (cand) {  // insert each candidate into the sorted list
+      const int m = __ffsll(static_cast<long long>(cand)) - 1;
+      cand &= cand - 1;
+      const float v = row[qq + kQ * m];
+      const int e = qq + kQ * m;
+      // its position p = the entries that rank before it (independent compares);
+      // the entries from p on move down one place and the last drops out
+      int p = 0;
 #pragma unroll
-      for (int u = 0; u < KMAX; ++u) {
-        const int m = m0 + u, e = qq + kQ * m;
-        cv[u] = m < nm ? row[e] : -INFINITY;
-        ci[u] = m < nm ? e : INT_MAX;
-      }
-      bitonic_sort<KMAX>(cv, ci);
-      if (m0 == 0) {  // the first chunk is the running list
+      for (int j = 0; j < KMAX; ++j) p += ranks_before(tv[j], ti[j], v, e) ? 1 : 0;
 #pragma unroll
-        for (int j = 0; j < KMAX; ++j) {
-          tv[j] = cv[j];
-          ti[j] = ci[j];
-        }
-      } else {
-        merge_best<KMAX>(tv, ti, cv, ci);
+      for (int j = KMAX - 1; j > 0; --j) {
+        tv[j] = j > p ? tv[j - 1] : (j == p ? v : tv[j]);
+        ti[j] = j > p ? ti[j - 1] : (j == p ? e : ti[j]);
       }
+      tv[0] = p == 0 ? v : tv[0];
+      ti[0] = p == 0 ? e : ti[0];
     }
 #pragma unroll
     for (int o = kTokPerWarp; o < 32; o <<= 1) {  // both partners merge the same two lists
@@ -252,57 +279,74 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(RouteArgs a) 
     const int tl = sl / k;
     const uint32_t *mk = s_emask[s_slot_e[sl]];
     int r = __popc(mk[tl >> 5] & ((1u << (tl & 31)) - 1u));
-    for (int w = 0; w < (tl >> 5); ++w) r += __popc(mk[w]);
-    a.lrank[static_cast<size_t>(t0) * k + sl] = r;
+#pragma unroll
+    for (int w = 0; w < kMaskWords - 1; ++w) r += w < (tl >> 5) ? __popc(mk[w]) : 0;
+    a.lrank[static_cast<size_t>(t0) * k + sl] = static_cast<uint8_t>(r);
   }
+  // the block's histogram row (kRouteThreads >= E)
   if (threadIdx.x < E) {
     int c = 0;
 #pragma unroll
     for (int w = 0; w < kMaskWords; ++w) c += __popc(s_emask[threadIdx.x][w]);
-    a.hist[static_cast<size_t>(blockIdx.x) * E + threadIdx.x] = c;
+    a.hist[static_cast<size_t>(b) * E + threadIdx.x] = c;
   }
-}
 
-__global__ void __launch_bounds__(kRouteThreads) route_index_kernel(RouteArgs a, int nblk) {
-  __shared__ int32_t s_below[kRouteThreads];  // per (partial p, expert e): rows of e in earlier blocks
-  __shared__ int32_t s_total[kRouteThreads];  // per (p, e): rows of e in all blocks
-  __shared__ int32_t s_base[kMaxExperts];
-  __shared__ int32_t s_cnt[kMaxExperts];
-  __shared__ int32_t s_off[kMaxExperts + 1];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int E = a.E, k = a.k, b = blockIdx.x;
-
-  // thread (p, e) sums histogram rows [b0, b1) of column e, kHistLoads loads in flight
-  const int P = kRouteThreads / E;  // partial sums per expert (>= 2)
-  const int chunk = (nblk + P - 1) / P;
-  const int e = threadIdx.x % E, p = threadIdx.x / E;
-  if (p < P) {
-    const int b0 = p * chunk, b1 = min(nblk, b0 + chunk);
-    int below = 0, total = 0;
-    for (int bb = b0; bb < b1; bb += kHistLoads) {
-      int hv[kHistLoads];
-#pragma unroll
-      for (int u = 0; u < kHistLoads; ++u)
-        hv[u] = bb + u < b1 ? __ldg(a.hist + static_cast<size_t>(bb + u) * E + e) : 0;
-#pragma unroll
-      for (int u = 0; u < kHistLoads; ++u) {
-        total += hv[u];
-        below += bb + u < b ? hv[u] : 0;
-      }
-    }
-    s_below[p * E + e] = below;
-    s_total[p * E + e] = total;
+  // ---- scan over blocks: the last block of the group to arrive takes the group
+  const int g = b / kScanGroup, ngroups = (nblk + kScanGroup - 1) / kScanGroup;
+  const int gb0 = g * kScanGroup, gn = min(kScanGroup, nblk - gb0);
+  // one thread per block fences and takes the ticket: the barrier orders the
+  // block's writes before its fence, so they are visible before the ticket
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const bool last = atomicAdd(a.tickets + 1 + g, 1) == gn - 1;
+    if (last) __threadfence();  // the group's rows, seen through the ticket, before they are read
+    s_last = last;
   }
   __syncthreads();
-  if (threadIdx.x < E) {
-    int below = 0, total = 0;
-    for (int q = 0; q < P; ++q) {
-      below += s_below[q * E + threadIdx.x];
-      total += s_total[q * E + threadIdx.x];
+  if (!s_last) return;
+  if (threadIdx.x < E) {  // column e: exclusive prefix of the group's rows, in place; the group total
+    const int e = threadIdx.x;
+    int h[kScanGroup];
+#pragma unroll
+    for (int i = 0; i < kScanGroup; ++i)
+      h[i] = i < gn ? __ldcg(a.hist + static_cast<size_t>(gb0 + i) * E + e) : 0;
+    int run = 0;
+#pragma unroll
+    for (int i = 0; i < kScanGroup; ++i) {
+      if (i < gn) a.hist[static_cast<size_t>(gb0 + i) * E + e] = run;
+      run += h[i];
     }
-    s_base[threadIdx.x] = below;
-    s_cnt[threadIdx.x] = total;
-    if (b == 0) a.counts[threadIdx.x] = total;
+    a.gpref[static_cast<size_t>(g) * E + e] = run;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const bool last = atomicAdd(a.tickets, 1) == ngroups - 1;
+    if (last) __threadfence();
+    s_last = last;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  // the last group: exclusive prefix of the group totals over groups (in place),
+  // expert totals (counts), and their exclusive scan over experts (offsets)
+  __shared__ int32_t s_cnt[kMaxExperts];
+  if (threadIdx.x < E) {
+    const int e = threadIdx.x;
+    int run = 0;
+    for (int g0 = 0; g0 < ngroups; g0 += kScanGroup) {
+      int h[kScanGroup];
+#pragma unroll
+      for (int i = 0; i < kScanGroup; ++i)
+        h[i] = g0 + i < ngroups ? __ldcg(a.gpref + static_cast<size_t>(g0 + i) * E + e) : 0;
+#pragma unroll
+      for (int i = 0; i < kScanGroup; ++i) {
+        if (g0 + i < ngroups) a.gpref[static_cast<size_t>(g0 + i) * E + e] = run;
+        run += h[i];
+      }
+    }
+    s_cnt[e] = run;
+    a.counts[e] = run;
   }
   __syncthreads();
   if (warp == 0) {  // exclusive scan of counts over experts
@@ -316,29 +360,30 @@ __global__ void __launch_bounds__(kRouteThreads) route_index_kernel(RouteArgs a,
         const int y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
       }
-      if (ee < E) s_off[ee] = carry + incl - c;
+      if (ee < E) a.offsets[ee] = carry + incl - c;
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (lane == 0) s_off[E] = carry;
+    if (lane == 0) a.offsets[E] = carry;
   }
-  __syncthreads();
-  if (b == 0 && threadIdx.x <= E) a.offsets[threadIdx.x] = s_off[threadIdx.x];
+}
 
-  // this block's slots: row = start of expert e + rows of e in earlier blocks + rank
-  const int t0 = b * TB, ntok = min(TB, a.T - t0);
-  for (int sl = threadIdx.x; sl < ntok * k; sl += kRouteThreads) {
-    const size_t s = static_cast<size_t>(t0) * k + sl;
-    const int ee = a.topk_idx[s];
-    const int row = s_off[ee] + s_base[ee] + a.lrank[s];
-    a.row_of_slot[s] = row;
-    a.slot_of_row[row] = static_cast<int32_t>(s);
-    a.w_row[row] = a.topk_w[s];
-  }
+__global__ void __launch_bounds__(256) route_index_kernel(RouteArgs a) {
+  const int s = blockIdx.x * 256 + threadIdx.x;  // slot t * k + j
+  if (s >= a.T * a.k) return;
+  const int e = __ldg(a.topk_idx + s), r = __ldg(a.lrank + s);
+  const float w = __ldg(a.topk_w + s);
+  const int b = s / a.k / TB, E = a.E;
+  const int row = __ldg(a.offsets + e) + __ldg(a.gpref + static_cast<size_t>(b / kScanGroup) * E + e) +
+                  __ldg(a.hist + static_cast<size_t>(b) * E + e) + r;
+  a.row_of_slot[s] = row;
+  a.slot_of_row[row] = s;
+  a.w_row[row] = w;
 }
 
 }  // namespace
 
 int route_num_blocks(int T) { return (T + TB - 1) / TB; }
+int route_scan_groups(int T) { return (route_num_blocks(T) + kScanGroup - 1) / kScanGroup; }
 
 template <int KMAX>
 cudaError_t launch_topk(const RouteArgs &a, cudaStream_t s) {
@@ -359,8 +404,8 @@ cudaError_t launch_route_topk(const RouteArgs &a, cudaStream_t s) {
 }
 
 cudaError_t launch_route_index(const RouteArgs &a, cudaStream_t s) {
-  const int nblk = route_num_blocks(a.T);
-  route_index_kernel<<<nblk, kRouteThreads, 0, s>>>(a, nblk);
+  const int slots = a.T * a.k;
+  route_index_kernel<<<(slots + 255) / 256, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -177,11 +177,12 @@ moe_status moe_mxfp8_forward_offsets(const moe_config *cfg, moe_mxfp8_fwd_layout
  * every step; they stay on the device and the grouped GEMMs read them there,
  * so no host copy breaks CUDA-graph capture (NVIDIA article "DeepSeek-V3 MoE
  * from 103 to 1,068 TFLOPS", "optimisations dropless needs" and "grouped
- * GEMM").  Per-expert counts, the scan and the permutation are computed
- * on the device in one pass over the logits (two kernels: per-block expert
- * histograms and ranks, then every block scans the histograms itself and
- * writes its slots' rows).  Non-finite logits set
- * MOE_DEV_NONFINITE_LOGIT; the indices written are still in range. */
+ * GEMM").  Two kernels: the first reads the logits once and writes the top k,
+ * the per-block expert histograms and every slot's rank, and its last blocks
+ * to finish scan the histograms (counts, offsets, per-block bases); the second
+ * writes every slot's row.  Work and scratch grow linearly with T.
+ * Non-finite logits set MOE_DEV_NONFINITE_LOGIT; the indices written are still
+ * in range. */
 moe_status moe_route(const moe_config *cfg, const float *logits, const moe_routing *routing,
                      void *scratch, size_t scratch_bytes, void *stream);
 

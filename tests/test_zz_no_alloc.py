@@ -105,9 +105,10 @@ def test_static_scratch_reports_nonfinite_logits(L):
 
 
 def test_static_scratch_rejects_oversized_configuration(L):
-    # route scratch needed: T*k*4 bytes of ranks alone = 3.84 MB > the 2.5 MiB array.
-    # Real device buffers throughout, so nothing could fault even if the check were missing.
-    shape = synth.MoEShape(T=60000, H=128, I=64, E=256, k=16)
+    # route scratch needed: one rank byte per slot and the per-block expert histograms, 3.2 MB >
+    # the 2.5 MiB array.  Real device buffers throughout, so nothing could fault even if the
+    # check were missing.
+    shape = synth.MoEShape(T=100000, H=128, I=64, E=256, k=16)
     cfg = moe.make_config(shape)
     assert moe.query_workspace(cfg)[0] > (5 << 19) + 4096
     logits = torch.zeros((shape.T, shape.E), dtype=torch.float32, device="cuda")
