@@ -78,8 +78,9 @@ def kernel_work(shape):
         "mx_quant_W_down_fwd": ("hbm", E * I * H * (2 + 2 * (1 + 1 / 32)), "B"),
         "mx_gemm_gateup_swiglu": ("tensor_fp8", 4 * MHI, "flop"),
         "mx_gemm_down": ("tensor_fp8", 2 * MHI, "flop"),
-        # dy quantised along H and along tokens from one read
-        "mx_quant_dy_both": ("hbm", M * H * (2 + 2 * (1 + 1 / 32)), "B"),
+        # dy read once (through each permuted row's token), Y read for the router
+        # gradient, codes and scales written along H and along tokens, g in partials
+        "mx_dy_quant_gdot": ("hbm", T * H * 2 + M * H * 2 + 2 * M * H * (1 + 1 / 32) + M * 4 * 4.0, "B"),
         "mx_quant_W_down": q(E * I * H), "mx_quant_W_gate": q(E * H * I), "mx_quant_W_up": q(E * H * I),
         "mx_quantT_A_w": q(M * I), "mx_quantT_x": q(M * H),
         "mx_gemm_dA_dswiglu": ("tensor_fp8", 2 * MHI, "flop"),
@@ -92,7 +93,6 @@ def kernel_work(shape):
         "gemm_gateup_swiglu": ("tensor", 4 * MHI, "flop"),
         "gemm_down": ("tensor", 2 * MHI, "flop"),
         "combine": ("hbm", M * H * 2 + T * H * 2.0 + M * 8, "B"),
-        "router_bwd": ("hbm", T * H * 2 + 2 * M * H * 2.0 + T * E * 4 + M * 12, "B"),
         # bf16 backward: dy permuted (as x), the router gradient from the dA GEMM's partials
         "permute_dy": ("hbm", T * H * 2 + M * H * 2.0 + M * 4, "B"),
         "router_grad": ("hbm", M * 2 * ((I + 255) // 256) * 4.0 + T * E * 4 + M * 16, "B"),
@@ -143,7 +143,7 @@ def kernel_source(label):
         return "mxfp8.cu"
     if label.startswith("route_"):
         return "route.cu"
-    return "gather.cu"  # permute_rows, permute_dy, combine, router_bwd, router_grad, unpermute_sum
+    return "gather.cu"  # permute_rows, permute_dy, combine, router_grad, unpermute_sum
 
 
 def source_hash(label):

@@ -141,8 +141,10 @@ Layout layout_of(const moe_config *c) {
   }
   L.f_total = o;
   o = kHeader;
-  L.b_dyp = o;
-  o += align256(M * H * 2);
+  if (c->precision == MOE_PREC_BF16) {  // the fp8 modes quantise dy straight from dy (no bf16 copy)
+    L.b_dyp = o;
+    o += align256(M * H * 2);
+  }
   if (c->precision == MOE_PREC_BF16) {  // fp8_bwd: dG and dU exist only quantised
     L.b_dG = o;
     o += align256(M * I * 2);
@@ -153,10 +155,10 @@ Layout layout_of(const moe_config *c) {
   o += align256(M * H * 2);
   L.b_maps = o;
   o += align256(E * kExpertMapBytes);
-  if (c->precision == MOE_PREC_BF16) {  // the router weight's gradient, partials from the dA GEMM
-    L.b_gpart = o;
-    o += align256(M * router_grad_parts(c->I) * 4);
-  }
+  // the router weight's gradient in partial sums per row: from the bf16 dA GEMM's
+  // epilogue, or from the fp8 modes' pass over dy
+  L.b_gpart = o;
+  o += align256(M * (c->precision == MOE_PREC_BF16 ? router_grad_parts(c->I) : dy_quant_col_blocks(c->H)) * 4);
   if (c->precision != MOE_PREC_BF16) {
     const size_t Mp = fp8_mpad(M, E);
     moe_fp8_layout &q = L.q;
@@ -295,8 +297,9 @@ struct Fp8Bwd {
   uint8_t *sc;
   int sms;
   int32_t *status;
-  const uint16_t *W_gate, *W_up, *W_down, *x_perm, *G, *U, *A_w;
-  uint16_t *dy_perm, *dX, *dx, *dW_gate, *dW_up, *dW_down;
+  const uint16_t *W_gate, *W_up, *W_down, *x_perm, *G, *U, *A_w, *Y, *dy;
+  uint16_t *dX, *dx, *dW_gate, *dW_up, *dW_down;
+  float *g_part, *d_logits, *d_topk_w;
   // the weights' codes for the three GEMMs that read them: quantised here
   // (fp8_bwd, into the scratch) or already by the forward (mxfp8, in `saved`)
   bool quantise_weights;
@@ -324,12 +327,21 @@ moe_status backward_fp8(const Fp8Bwd &f, cudaStream_t s) {
   m.w_row = f.r->w_row;
   m.status = f.status;
   m.num_sms = f.sms;
-  // dA = w (Q(dy) . Q(W_down)^T), K = H; dSwiGLU epilogue -> Q(dG), Q(dU) on both axes.
-  // dy is quantised along H (dA) and along tokens (dW_down) from one read.
-  MOE_TRY(timed("mx_quant_dy_both", s, [&] {
-    return launch_quant_cols(f.dy_perm, H, Mp, off, pad_off, E, sc + q.dy_t, sc + q.dy_t_sf, sf_b(H),
-                             RowCodes{sc + q.dy_q, sc + q.dy_sf, sf_a(Mp)}, s);
+  // One pass over dy, read through each permuted row's token: quantised along H
+  // (dA's A operand) and along tokens (dW_down's B operand), and g_tj = <dy_t,
+  // Y_tj> from the saved Y in partial sums (the MXFP8 dA's accumulator carries
+  // dy's and W_down's quantisation error, so the router gradient is not taken
+  // from it); the router gradients follow from g.
+  const int gcb = dy_quant_col_blocks(H);
+  MOE_TRY(timed("mx_dy_quant_gdot", s, [&] {
+    return launch_dy_quant(f.dy, f.Y, f.r->slot_of_row, k, H, Mp, off, pad_off, E, sc + q.dy_t, sc + q.dy_t_sf,
+                           sf_b(H), RowCodes{sc + q.dy_q, sc + q.dy_sf, sf_a(Mp)}, f.g_part, gcb, s);
   }));
+  MOE_TRY(timed("router_grad", s, [&] {
+    return launch_router_grad(f.r->row_of_slot, f.r->topk_idx, f.r->topk_w, f.g_part, gcb, f.d_logits,
+                              f.d_topk_w, T, E, k, s);
+  }));
+  // dA = w (Q(dy) . Q(W_down)^T), K = H; dSwiGLU epilogue -> Q(dG), Q(dU) on both axes.
   if (f.quantise_weights)
     MOE_TRY(timed("mx_quant_W_down", s, [&] {
       return launch_quant_rows(f.W_down, E * I, H, nullptr, nullptr, E, f.wd_q, f.wd_sf, sf_b(I), s);
@@ -721,18 +733,13 @@ moe_status moe_backward(const moe_config *cfg, const void *dy, const void *x,
   const uint16_t *A = reinterpret_cast<const uint16_t *>(sv + L.s_A);
   const uint16_t *Y = reinterpret_cast<const uint16_t *>(sv + L.s_Y);
   const uint16_t *A_w = reinterpret_cast<const uint16_t *>(sv + L.s_Aw);
-  uint16_t *dy_perm = reinterpret_cast<uint16_t *>(sc + L.b_dyp);
+  uint16_t *dy_perm = reinterpret_cast<uint16_t *>(sc + L.b_dyp);  // bf16 only
+  float *g_part = reinterpret_cast<float *>(sc + L.b_gpart);
   uint16_t *dG = reinterpret_cast<uint16_t *>(sc + L.b_dG);
   uint16_t *dU = reinterpret_cast<uint16_t *>(sc + L.b_dU);
   uint16_t *dX = reinterpret_cast<uint16_t *>(sc + L.b_dX);
 
   if (cfg->precision != MOE_PREC_BF16) {
-    // g_tj = <dy_t, Y_tj> from the saved Y: the MXFP8 dA's accumulator carries
-    // dy's and W_down's quantisation error, so the router gradient is not taken from it
-    MOE_TRY(timed("router_bwd", s, [&] {
-      return launch_router_bwd(static_cast<const uint16_t *>(dy), Y, r->row_of_slot, r->topk_idx,
-                               r->topk_w, dy_perm, d_logits, d_topk_w, T, H, E, k, s);
-    }));
     Fp8Bwd f;
     f.cfg = cfg;
     f.r = r;
@@ -747,7 +754,11 @@ moe_status moe_backward(const moe_config *cfg, const void *dy, const void *x,
     f.G = G;
     f.U = U;
     f.A_w = A_w;
-    f.dy_perm = dy_perm;
+    f.Y = Y;
+    f.dy = static_cast<const uint16_t *>(dy);
+    f.g_part = g_part;
+    f.d_logits = d_logits;
+    f.d_topk_w = d_topk_w;
     f.dX = dX;
     f.dx = static_cast<uint16_t *>(dx);
     f.dW_gate = static_cast<uint16_t *>(dW_gate);
@@ -775,7 +786,6 @@ moe_status moe_backward(const moe_config *cfg, const void *dy, const void *x,
     return launch_permute_rows(static_cast<const uint16_t *>(dy), r->row_of_slot, dy_perm, T, H, k, s);
   }));
   (void)Y;
-  float *g_part = reinterpret_cast<float *>(sc + L.b_gpart);
   GemmArgs g = gemm_base(cfg, r, di.sms, status);
   g.x_perm = x_perm;
   g.W_gate = static_cast<const uint16_t *>(W_gate);

@@ -11,9 +11,8 @@
 //   permute_rows : x_perm[row(t,j)] = x[t]                      (dispatch)
 //   gather_sum   : out[t] = sum_j w_tj * Y[row(t,j)]           (combine)
 //                  dx[t]  = sum_j dX_perm[row(t,j)]            (un-permute)
-//   router_bwd   : dy_perm[row(t,j)] = dy[t]                   (dy dispatch; the
-//                  router weight is applied later in fp32, so dy is never rounded)
-//                  g_tj = <dy[t], Y[row(t,j)]>                 (d w_tj)
+//   router_grad  : from g_tj = <dy[t], Y[row(t,j)]> (d w_tj) in partial sums
+//                  per permuted row: d_topk_w and
 //                  d_logits[t, S_tj] = w_tj (g_tj - sum_i w_ti g_ti), 0 elsewhere
 #include "common.cuh"
 #include "mxfp8.cuh"
@@ -228,63 +227,10 @@ __device__ __forceinline__ void router_grads(float myg, float myw, int mye, size
   }
 }
 
-__global__ void __launch_bounds__(kWarps * 32) router_bwd_kernel(
-    const uint4 *__restrict__ dy, const uint4 *__restrict__ Y, const int32_t *__restrict__ ros,
-    const int32_t *__restrict__ topk_idx, const float *__restrict__ topk_w, uint4 *__restrict__ dyp,
-    float *__restrict__ d_logits, float *__restrict__ d_topk_w, int T, int nv, int E, int k) {
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
-  if (t >= T) return;
-  const size_t sb = static_cast<size_t>(t) * k;
-  const int myrow = lane < k ? __ldg(ros + sb + lane) : 0;
-  const float myw = lane < k ? __ldg(topk_w + sb + lane) : 0.f;
-  const int mye = lane < k ? __ldg(topk_idx + sb + lane) : -1;
-  float dot[kMaxTopK];
-#pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) dot[j] = 0.f;
-  for (int v0 = 0; v0 < nv; v0 += 32 * kVecPerLane) {
-    uint4 d[kVecPerLane];
-#pragma unroll
-    for (int u = 0; u < kVecPerLane; ++u) {
-      const int v = v0 + u * 32 + lane;
-      if (v < nv) d[u] = __ldcs(dy + static_cast<size_t>(t) * nv + v);
-    }
-#pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
-      if (j < k) {
-        const int row = __shfl_sync(0xffffffffu, myrow, j);
-        const uint4 *src = Y + static_cast<size_t>(row) * nv;
-        uint4 *dst = dyp + static_cast<size_t>(row) * nv;
-        uint4 q[kVecPerLane];
-#pragma unroll
-        for (int u = 0; u < kVecPerLane; ++u) {
-          const int v = v0 + u * 32 + lane;
-          if (v < nv) q[u] = __ldcs(src + v);
-        }
-#pragma unroll
-        for (int u = 0; u < kVecPerLane; ++u) {
-          const int v = v0 + u * 32 + lane;
-          if (v < nv) {
-            dot[j] += dot8(d[u], q[u]);
-            dst[v] = d[u];
-          }
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j)
-    if (j < k) dot[j] = warp_sum(dot[j]);
-  float myg = 0.f;
-#pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j)
-    if (j == lane) myg = dot[j];
-  router_grads(myg, myw, mye, static_cast<size_t>(t), k, E, d_logits, d_topk_w);
-}
-
-// d_logits and d_topk_w of a token from g_tj computed by the bf16 dA GEMM's
-// epilogue: g_tj = <dy_t, Y_tj> = <dy_t . W_down^T, A_r>, summed here over the
-// np column partials of row r = row(t,j) in a fixed order.
+// d_logits and d_topk_w of a token from g_tj in np partial sums per permuted
+// row (the bf16 dA GEMM's epilogue: g_tj = <dy_t . W_down^T, A_r>; the fp8
+// modes' pass over dy: <dy_t, Y_r>), added here for row r = row(t,j) in a fixed
+// order.
 __global__ void __launch_bounds__(kWarps * 32) router_grad_kernel(
     const int32_t *__restrict__ ros, const int32_t *__restrict__ topk_idx, const float *__restrict__ topk_w,
     const float *__restrict__ g_part, int np, float *__restrict__ d_logits, float *__restrict__ d_topk_w,
@@ -378,16 +324,6 @@ cudaError_t launch_sum_segments(const float *parts, int S, int64_t n, float *out
   if (n4 == 0) return cudaSuccess;
   sum_segments_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, s>>>(
       reinterpret_cast<const float4 *>(parts), S, n4, reinterpret_cast<float4 *>(out));
-  return cudaGetLastError();
-}
-
-cudaError_t launch_router_bwd(const uint16_t *dy, const uint16_t *Y, const int32_t *row_of_slot,
-                              const int32_t *topk_idx, const float *topk_w, uint16_t *dy_perm,
-                              float *d_logits, float *d_topk_w, int T, int H, int E, int k,
-                              cudaStream_t s) {
-  router_bwd_kernel<<<blocks_for(T), kWarps * 32, 0, s>>>(
-      reinterpret_cast<const uint4 *>(dy), reinterpret_cast<const uint4 *>(Y), row_of_slot,
-      topk_idx, topk_w, reinterpret_cast<uint4 *>(dy_perm), d_logits, d_topk_w, T, H / 8, E, k);
   return cudaGetLastError();
 }
 

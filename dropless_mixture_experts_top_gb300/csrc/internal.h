@@ -80,12 +80,6 @@ cudaError_t launch_sum_segments(const float *parts, int S, int64_t n, float *out
 cudaError_t launch_router_grad(const int32_t *row_of_slot, const int32_t *topk_idx, const float *topk_w,
                                const float *g_part, int np, float *d_logits, float *d_topk_w, int T, int E, int k,
                                cudaStream_t s);
-// dy_perm[row(t,j)] = dy[t]; g[t,j] = <dy[t], Y[row]>; d_logits; d_topk_w (nullable)
-cudaError_t launch_router_bwd(const uint16_t *dy, const uint16_t *Y, const int32_t *row_of_slot,
-                              const int32_t *topk_idx, const float *topk_w, uint16_t *dy_perm,
-                              float *d_logits, float *d_topk_w, int T, int H, int E, int k,
-                              cudaStream_t s);
-
 // ---- grouped GEMMs (gemm.cu)
 enum GemmMode : int {
   kFwdGateUp = 0,   // [x_perm] . [W_gate | W_up]  -> SwiGLU epilogue: A, G, U, A_w  (ragged M)
@@ -159,6 +153,16 @@ struct RowCodes {
 cudaError_t launch_quant_cols(const uint16_t *src, int C, int Mpad, const int32_t *offsets,
                               const int32_t *pad_off, int E, uint8_t *codes, uint8_t *sf, SfLayout L,
                               RowCodes rows, cudaStream_t s);
+
+// The MXFP8 backward's one pass over dy: dy rows gathered by token for every
+// permuted row, quantised along H into the padded row space (rows) and along
+// tokens (codes_t [H, Mpad]), and g = <dy_t, Y_r> in col_blocks partial sums per
+// row (g_part [M][col_blocks], added in order by launch_router_grad).
+cudaError_t launch_dy_quant(const uint16_t *dy, const uint16_t *Y, const int32_t *slot_of_row, int k, int H,
+                            int Mpad, const int32_t *offsets, const int32_t *pad_off, int E, uint8_t *codes_t,
+                            uint8_t *sf_t, SfLayout Lt, RowCodes rows, float *g_part, int col_blocks,
+                            cudaStream_t s);
+int dy_quant_col_blocks(int H);  // column blocks of that pass (its partials per row)
 
 // mxfp8 forward: the permute with x quantised along H fused (codes and scales
 // to the padded row of every permuted row; H % 128 == 0), and zero codes and

@@ -130,7 +130,7 @@ __device__ __forceinline__ int qc_idx(int r, int c) { return r * kQcCols + (((c 
 // Issue one 128 x 64 tile: source row r at row_ptr(r) (nullptr: a zero row),
 // columns c0 .. c0 + 63; one cp.async group per call.
 template <class RowPtr>
-__device__ __forceinline__ void qc_issue(uint16_t *dst, int c0, const RowPtr &row_ptr) {
+__device__ __forceinline__ void qc_issue(uint16_t *dst, int c0, const RowPtr &row_ptr, bool commit = true) {
 #pragma unroll
   for (int j = 0; j < kQcLoads; ++j) {
     const int i = threadIdx.x + j * kQcThreads;
@@ -142,7 +142,7 @@ __device__ __forceinline__ void qc_issue(uint16_t *dst, int c0, const RowPtr &ro
     else
       *reinterpret_cast<uint4 *>(d) = make_uint4(0, 0, 0, 0);
   }
-  cp_async_commit();
+  if (commit) cp_async_commit();
 }
 
 // 32 bf16 values of a staged tile: row r, columns 32 bb .. 32 bb + 31.
@@ -239,6 +239,102 @@ __global__ void __launch_bounds__(kQcThreads, 3) quant_cols_kernel(const uint16_
           *reinterpret_cast<const uint4 *>(otile + r * kQcOutStride + part * 16);
     }
   });
+}
+
+// The MXFP8 backward's pass over dy (one read, no bf16 copy): for 128 padded
+// rows of one expert (a block) and 64-column tiles of H, the rows of dy the
+// permuted rows come from (gathered by token: slot_of_row / k) and the same
+// rows of Y are staged by cp.async, kDyRing tiles of each in flight.  Each
+// tile is quantised along H (thread = row, 32-column block; into the padded
+// row space: dA's A operand) and along tokens (thread = column, 32-token
+// block; transposed: dW_down's B operand), and every row accumulates its part
+// of g = <dy_t, Y_r> over the block's columns; the part of block column
+// y of row r goes to g_part[r * gridDim.y + y], added in order by the router
+// gradient kernel.
+constexpr int kDyRing = 3;
+constexpr int kDySmem = kDyRing * 2 * kQcTileElems * 2 + kQcCols * kQcOutStride;
+
+__global__ void __launch_bounds__(kQcThreads, 2) dy_quant_kernel(const uint16_t *__restrict__ dy,
+                                                                 const uint16_t *__restrict__ Y,
+                                                                 const int32_t *__restrict__ slot_of_row, int k,
+                                                                 int H, int Mpad, const int32_t *__restrict__ offsets,
+                                                                 const int32_t *__restrict__ pad_off, int E,
+                                                                 uint8_t *__restrict__ codes_t, uint8_t *__restrict__ sf_t,
+                                                                 SfLayout Lt, RowCodes rows, float *__restrict__ g_part) {
+  extern __shared__ __align__(16) uint8_t qc_smem[];
+  uint16_t *ring = reinterpret_cast<uint16_t *>(qc_smem);  // [kDyRing][dy tile | Y tile]
+  uint8_t *otile = qc_smem + kDyRing * 2 * kQcTileElems * 2;
+  __shared__ int s_pad[kMaxExperts + 1];
+  __shared__ int s_seg[3];  // first source row, valid rows of this tile, skip flag
+  __shared__ int s_tok[kQcRows];
+  const int prow0 = blockIdx.x * kQcRows;
+  for (int e = threadIdx.x; e <= E; e += kQcThreads) s_pad[e] = __ldg(pad_off + e);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (prow0 >= s_pad[E]) {
+      s_seg[2] = 1;
+    } else {
+      const int e = expert_of(prow0, s_pad, E);
+      const int o = __ldg(offsets + e), count = __ldg(offsets + e + 1) - o;
+      const int local0 = prow0 - s_pad[e];
+      s_seg[0] = o + local0;
+      s_seg[1] = min(kQcRows, count - local0);
+      s_seg[2] = 0;
+    }
+  }
+  __syncthreads();
+  if (s_seg[2]) return;
+  const int row0 = s_seg[0], nvalid = s_seg[1];
+  for (int r = threadIdx.x; r < nvalid; r += kQcThreads) s_tok[r] = __ldg(slot_of_row + row0 + r) / k;
+  __syncthreads();
+  auto dy_ptr = [&](int r) -> const uint16_t * {
+    return r < nvalid ? dy + static_cast<size_t>(s_tok[r]) * H : nullptr;
+  };
+  auto y_ptr = [&](int r) -> const uint16_t * { return r < nvalid ? Y + static_cast<size_t>(row0 + r) * H : nullptr; };
+  const int first = blockIdx.y * kQcCols, step = gridDim.y * kQcCols;
+  const int nt = first < H ? (H - first + step - 1) / step : 0;
+  auto issue = [&](int i) {
+    uint16_t *slot = ring + (i % kDyRing) * 2 * kQcTileElems;
+    qc_issue(slot, first + i * step, dy_ptr, false);
+    qc_issue(slot + kQcTileElems, first + i * step, y_ptr, true);  // one group per tile: both sources
+  };
+  const int r = threadIdx.x >> 1, bb = threadIdx.x & 1;  // row pass: row, 32-column block
+  float gpart = 0.f;
+  for (int i = 0; i < kDyRing - 1 && i < nt; ++i) issue(i);
+  for (int it = 0; it < nt; ++it) {
+    const int ahead = it + kDyRing - 1;
+    if (ahead < nt) issue(ahead);
+    cp_async_wait_pending(min(nt - 1, ahead) - it);  // this tile's group has landed
+    __syncthreads();
+    const uint16_t *tile = ring + (it % kDyRing) * 2 * kQcTileElems, *ytile = tile + kQcTileElems;
+    const int c0 = first + it * step;
+    {
+      float v[32], yv[32];
+      qc_row32(tile, r, bb, v);
+      qc_row32(ytile, r, bb, yv);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) gpart = fmaf(v[i], yv[i], gpart);
+      const int prow = prow0 + r, kb = (c0 >> 5) + bb;
+      rows.sf[atom_byte(prow, kb, H, rows.L)] =
+          quant32(v, reinterpret_cast<uint4 *>(rows.codes + static_cast<size_t>(prow) * H + c0 + 32 * bb));
+    }
+    const int cc = threadIdx.x % kQcCols, b = threadIdx.x / kQcCols;  // 4 blocks of 32 tokens
+    float v[32];
+    qc_col32(tile, cc, b, v);
+    sf_t[atom_byte(c0 + cc, (prow0 >> 5) + b, Mpad, Lt)] =
+        quant32(v, reinterpret_cast<uint4 *>(otile + cc * kQcOutStride + 32 * b));
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < (kQcCols * kQcRows / 16) / kQcThreads; ++j) {
+      const int i = threadIdx.x + j * kQcThreads;
+      const int orow = i >> 3, part = i & 7;  // output row (column c0 + orow), 16-byte piece
+      *reinterpret_cast<uint4 *>(codes_t + static_cast<size_t>(c0 + orow) * Mpad + prow0 + part * 16) =
+          *reinterpret_cast<const uint4 *>(otile + orow * kQcOutStride + part * 16);
+    }
+    __syncthreads();  // the tile's slot and the output tile are reused
+  }
+  gpart += __shfl_xor_sync(0xffffffffu, gpart, 1);  // the row's two 32-column halves
+  if (bb == 0 && r < nvalid) g_part[static_cast<size_t>(row0 + r) * gridDim.y + blockIdx.y] = gpart;
 }
 
 // Weights quantised along their middle axis (the mxfp8 forward GEMMs' K),
@@ -338,6 +434,23 @@ cudaError_t launch_quant_cols(const uint16_t *src, int C, int Mpad, const int32_
   quant_cols_kernel<<<grid, kQcThreads, kQcSmem, s>>>(src, C, Mpad, offsets, pad_off, E, codes, sf, L, rows);
   return cudaGetLastError();
 }
+
+cudaError_t launch_dy_quant(const uint16_t *dy, const uint16_t *Y, const int32_t *slot_of_row, int k, int H,
+                            int Mpad, const int32_t *offsets, const int32_t *pad_off, int E, uint8_t *codes_t,
+                            uint8_t *sf_t, SfLayout Lt, RowCodes rows, float *g_part, int col_blocks,
+                            cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>(Mpad / kQcRows), static_cast<unsigned>(col_blocks));
+  static DeviceOnce once;  // dynamic shared memory above 48 KB, opted in once per device
+  const cudaError_t e = once.get([](int *) {
+    return cudaFuncSetAttribute(dy_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDySmem);
+  });
+  if (e != cudaSuccess) return e;
+  dy_quant_kernel<<<grid, kQcThreads, kDySmem, s>>>(dy, Y, slot_of_row, k, H, Mpad, offsets, pad_off, E, codes_t,
+                                                     sf_t, Lt, rows, g_part);
+  return cudaGetLastError();
+}
+
+int dy_quant_col_blocks(int H) { return H / kQcCols < 4 ? H / kQcCols : 4; }
 
 cudaError_t launch_quant_wT(const uint16_t *W, int E, int R, int C, int interleave, int half,
                             uint8_t *codes, uint8_t *sf, SfLayout L, RowCodes rows, cudaStream_t s) {
