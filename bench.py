@@ -82,7 +82,7 @@ def kernel_work(shape):
         # gradient, codes and scales written along H and along tokens, g in partials
         "mx_dy_quant_gdot": ("hbm", T * H * 2 + M * H * 2 + 2 * M * H * (1 + 1 / 32) + M * 4 * 4.0, "B"),
         "mx_quant_W_down": q(E * I * H), "mx_quant_W_gate": q(E * H * I), "mx_quant_W_up": q(E * H * I),
-        "mx_quantT_A_w": q(M * I), "mx_quantT_x": q(M * H),
+        "mx_quantT_x": q(M * H),
         "mx_gemm_dA_dswiglu": ("tensor_fp8", 2 * MHI, "flop"),
         "mx_gemm_dX": ("tensor_fp8", 4 * MHI, "flop"),
         "mx_gemm_dW_down": ("tensor_fp8", 2 * MHI, "flop"),

@@ -104,6 +104,16 @@ Layout layout_of(const moe_config *c) {
   o += align256(M * H * 2);
   L.s_Aw = o;
   o += align256(M * I * 2);
+  if (c->precision != MOE_PREC_BF16) {
+    // an MXFP8 backward's dW_down operand, w * A along tokens, written by the
+    // forward's gate/up epilogue (instead of the bf16 A_w)
+    const size_t Mp = fp8_mpad(M, E);
+    L.q.m_pad = Mp;
+    L.q.aw_t = o;
+    o += align256(I * Mp);
+    L.q.aw_t_sf = o;
+    o += align256(I * Mp / 32);
+  }
   if (c->precision == MOE_PREC_MXFP8) {  // the backward's weight operands, written by the forward
     moe_mxfp8_fwd_layout &f = L.fq;
     auto take = [&o](size_t bytes) {
@@ -186,8 +196,6 @@ Layout layout_of(const moe_config *c) {
       q.wu_q = take(E * H * I);
       q.wu_sf = take(sf_layout_bytes(E * H, I, sf_b(H)));
     }
-    q.aw_t = take(I * Mp);
-    q.aw_t_sf = take(I * Mp / 32);
     q.dy_t = take(H * Mp);
     q.dy_t_sf = take(sf_layout_bytes(H, Mp, sf_b(H)));
     q.x_t = take(H * Mp);
@@ -297,7 +305,8 @@ struct Fp8Bwd {
   uint8_t *sc;
   int sms;
   int32_t *status;
-  const uint16_t *W_gate, *W_up, *W_down, *x_perm, *G, *U, *A_w, *Y, *dy;
+  const uint16_t *W_gate, *W_up, *W_down, *x_perm, *G, *U, *Y, *dy;
+  const uint8_t *aw_t, *aw_t_sf;  // w * A along tokens, from the forward (in `saved`)
   uint16_t *dX, *dx, *dW_gate, *dW_up, *dW_down;
   float *g_part, *d_logits, *d_topk_w;
   // the weights' codes for the three GEMMs that read them: quantised here
@@ -385,13 +394,10 @@ moe_status backward_fp8(const Fp8Bwd &f, cudaStream_t s) {
   MOE_TRY(timed("unpermute_sum", s, [&] {
     return launch_gather_sum(f.dX, f.r->row_of_slot, nullptr, f.dx, T, H, k, s);
   }));
-  // dW_down = Q(w a)^T . Q(dy), K = the expert's tokens
-  MOE_TRY(timed("mx_quantT_A_w", s, [&] {
-    return launch_quant_cols(f.A_w, I, Mp, off, pad_off, E, sc + q.aw_t, sc + q.aw_t_sf, sf_a(I),
-                             RowCodes{}, s);
-  }));
-  m.a0 = sc + q.aw_t;
-  m.sfa0 = sc + q.aw_t_sf;
+  // dW_down = Q(w a)^T . Q(dy), K = the expert's tokens; Q(w a) along tokens comes
+  // from the forward's gate/up epilogue
+  m.a0 = f.aw_t;
+  m.sfa0 = f.aw_t_sf;
   m.b0 = sc + q.dy_t;
   m.sfb0 = sc + q.dy_t_sf;
   m.a1 = m.b1 = m.sfa1 = m.sfb1 = nullptr;
@@ -429,6 +435,7 @@ struct Mx8Fwd {
   const uint16_t *x, *W_gate, *W_up, *W_down;
   uint16_t *x_perm, *A, *G, *U, *A_w, *Y;
   uint8_t *saved;  // the backward's weight codes go here
+  uint8_t *aw_t, *aw_t_sf;  // and w * A along tokens
   bool keep;       // write what the backward reads (the bf16 activations, the weight codes)
 };
 
@@ -474,9 +481,11 @@ moe_status forward_mx(const Mx8Fwd &f, cudaStream_t s) {
   m.o0 = f.keep ? f.A : nullptr;
   m.o1 = f.keep ? f.G : nullptr;
   m.o2 = f.keep ? f.U : nullptr;
-  m.o3 = f.keep ? f.A_w : nullptr;
+  m.o3 = nullptr;  // the backward reads w * A quantised along tokens, not in bf16
   m.aq = sc + q.a_q;
   m.aq_sf = sc + q.a_sf;
+  m.aw_t = f.keep ? f.aw_t : nullptr;
+  m.aw_t_sf = f.keep ? f.aw_t_sf : nullptr;
   MOE_TRY(timed("mx_gemm_gateup_swiglu", s, [&] { return launch_mx_gemm(kMxGemmGateUp, m, s); }));
   MOE_TRY(timed("mx_quant_W_down_fwd", s, [&] {
     // along I for GEMM2 (transposed) and along H for the backward's dA (row by row, into `saved`)
@@ -489,7 +498,7 @@ moe_status forward_mx(const Mx8Fwd &f, cudaStream_t s) {
   m.sfb0 = sc + q.wdt_sf;
   m.o0 = f.Y;
   m.o1 = m.o2 = m.o3 = nullptr;
-  m.aq = m.aq_sf = nullptr;
+  m.aq = m.aq_sf = m.aw_t = m.aw_t_sf = nullptr;
   MOE_TRY(timed("mx_gemm_down", s, [&] { return launch_mx_gemm(kMxGemmDown, m, s); }));
   return MOE_OK;
 }
@@ -554,9 +563,12 @@ moe_status forward_impl(FwdKind kind, const moe_config *cfg, const void *x, cons
     f.A = A;
     f.G = G;
     f.U = U;
-    f.A_w = A_w;
+    f.aw_t = sv + L.q.aw_t;
+    f.aw_t_sf = sv + L.q.aw_t_sf;
     f.Y = Y;
     f.saved = sv;
+    f.aw_t = sv + L.q.aw_t;
+    f.aw_t_sf = sv + L.q.aw_t_sf;
     f.keep = kind != kFwdNoSave;
     MOE_TRY(forward_mx(f, s));
   } else {
@@ -570,10 +582,14 @@ moe_status forward_impl(FwdKind kind, const moe_config *cfg, const void *x, cons
     g.W_down = static_cast<const uint16_t *>(W_down);
     g.w_row = r->w_row;
     g.o0 = A;
-    const bool keep = kind != kFwdNoSave;  // G, U and A_w are only the backward's
+    const bool keep = kind != kFwdNoSave;  // G, U and w * A are only the backward's
+    const bool fp8b = cfg->precision == MOE_PREC_FP8_BWD;  // its dW_down reads w * A quantised along tokens
     g.o1 = keep ? G : nullptr;
     g.o2 = keep ? U : nullptr;
-    g.o3 = keep ? A_w : nullptr;
+    g.o3 = keep && !fp8b ? A_w : nullptr;
+    g.aw_t = keep && fp8b ? sv + L.q.aw_t : nullptr;
+    g.aw_t_sf = keep && fp8b ? sv + L.q.aw_t_sf : nullptr;
+    g.Mpad = static_cast<int>(L.q.m_pad);
     MOE_TRY(timed(gemm_mode_name(kFwdGateUp), s, [&] { return launch_grouped_gemm(kFwdGateUp, g, s); }));
     // the bf16 backward never reads Y (its router gradient comes from the dA GEMM),
     // so a recompute for it stops after GEMM1; the fp8 modes' backward reads Y
@@ -581,6 +597,7 @@ moe_status forward_impl(FwdKind kind, const moe_config *cfg, const void *x, cons
     g.act = A;
     g.o0 = Y;
     g.o1 = g.o2 = g.o3 = nullptr;
+    g.aw_t = g.aw_t_sf = nullptr;
     MOE_TRY(timed(gemm_mode_name(kFwdDown), s, [&] { return launch_grouped_gemm(kFwdDown, g, s); }));
   }
   if (kind == kFwdRecompute) return MOE_OK;
@@ -753,7 +770,8 @@ moe_status moe_backward(const moe_config *cfg, const void *dy, const void *x,
     f.x_perm = x_perm;
     f.G = G;
     f.U = U;
-    f.A_w = A_w;
+    f.aw_t = sv + L.q.aw_t;
+    f.aw_t_sf = sv + L.q.aw_t_sf;
     f.Y = Y;
     f.dy = static_cast<const uint16_t *>(dy);
     f.g_part = g_part;

@@ -17,6 +17,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "mxfp8.cuh"
 
 namespace moe {
 
@@ -28,8 +29,8 @@ struct Tile {
   int row_end;  // ragged M: end of the expert's rows
   int n0;       // first output column
   int nkb;      // K blocks
-  int krow0;    // ragged K: expert's first row
-  int kcount;   // ragged K: expert's rows
+  int krow0;    // ragged K: expert's first row; ragged M: padded row of m0 (128-aligned segments)
+  int kcount;   // ragged K: expert's rows; ragged M: end of the expert's padded segment
 };
 
 // Byte offset of row r's 16-byte chunk q (of 4) in a staging tile.
@@ -95,6 +96,39 @@ __device__ __forceinline__ void rows32_to_lanes(uint8_t *tile, const uint4 (&w)[
   __syncwarp();
 }
 
+// The value a bf16 tensor would hold (nearest even), as fp32.
+__device__ __forceinline__ float round_bf16(float v) {
+  return __uint_as_float(static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v))) << 16);
+}
+
+// A warp's 32 x 32 values (lane = row, bf16-exact) quantised down the rows:
+// written to the staging tile as bf16, then lane j takes column j's 32 values
+// (one 32-token block) and writes its 32 codes at codes + (col0 + j) * ld +
+// tok0 and their scale code at sf_byte (its own column's byte).
+__device__ __forceinline__ void quant_down_rows32(uint8_t *tile, const float (&v)[32], uint8_t *codes,
+                                                  size_t ld, int col0, int tok0, uint8_t *sf_byte) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 w;
+    w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+    w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+    w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+    w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+    *reinterpret_cast<uint4 *>(tile + epi_swz(lane, q)) = w;
+  }
+  __syncwarp();
+  float c[32];
+  const int qc = lane >> 3, within = (lane & 7) * 2;
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    c[i] = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(
+                               tile + epi_swz(i, qc) + within))
+                           << 16);
+  __syncwarp();  // the tile is rewritten by the next call
+  *sf_byte = quant32(c, reinterpret_cast<uint4 *>(codes + static_cast<size_t>(col0 + lane) * ld + tok0));
+}
+
 // sigmoid with the approximate (branch-free) reciprocal: within a few fp32 ulp
 // of 1 / (1 + e^-z), far below the bf16 rounding of every output it feeds; the
 // IEEE division's special-case branch stalled the epilogue warps.
@@ -121,6 +155,11 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, uint32_t tb, int ri
     const int row = t.m0 + rit, row0 = row - lane;
     const int nvalid = clamp_rows(t.row_end - row0);
     const float w = row < t.row_end ? __ldg(p.w_row + row) : 0.f;
+    // for an MXFP8 backward: w * A quantised along tokens -- the warp's 32 rows
+    // are one 32-token block of the padded token axis when they start inside
+    // the expert's padded segment (rows past its count are zeros)
+    const int prow0 = t.krow0 + (rit - lane);
+    const bool qtok = p.aw_t != nullptr && prow0 < t.kcount;
     for (int c = cb4; c < ce4; ++c) {
       const int col = t.n0 + 32 * c;
       if (col >= p.I) break;
@@ -136,12 +175,23 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, uint32_t tb, int ri
       }
       const size_t off = static_cast<size_t>(row0) * p.I + col;
       store_rows32(tile, p.o0 + off, p.I, nvalid, v0);
-      if (p.o1) {  // G, U and A_w are the backward's; a forward that saves nothing skips them
+      if (p.o1) {  // G, U and w * A are the backward's; a forward that saves nothing skips them
         store_rows32(tile, p.o1 + off, p.I, nvalid, v1);
         store_rows32(tile, p.o2 + off, p.I, nvalid, v2);
+      }
+      if (p.o3 || qtok) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) v0[i] *= w;  // A_w = w * A, the dW_down operand
-        store_rows32(tile, p.o3 + off, p.I, nvalid, v0);
+        if (p.o3) store_rows32(tile, p.o3 + off, p.I, nvalid, v0);
+        if (qtok) {  // from the bf16 value the tensor would hold; lane j takes column col + j
+          // rows past the count are +0 (0 * A may be -0, whose E4M3 code is not 0)
+          const bool valid = row < t.row_end;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v1[i] = valid ? round_bf16(v0[i]) : 0.f;
+          const int ccol = col + lane;
+          const size_t sfb = atom_byte(ccol, prow0 >> 5, p.Mpad, SfLayout{p.I, 128});
+          quant_down_rows32(tile, v1, p.aw_t, static_cast<size_t>(p.Mpad), col, prow0, p.aw_t_sf + sfb);
+        }
       }
     }
   } else if constexpr (MODE == kFwdDown || MODE == kBwdDX) {

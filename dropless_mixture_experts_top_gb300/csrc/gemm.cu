@@ -70,9 +70,9 @@ __host__ __device__ constexpr int threads_of(int mode) {
 }
 constexpr uint32_t kTmemCols = 2 * BN;
 // Shared memory (from a 1024-aligned base): operand stages | barriers (512) |
-// two [E+1] tables | epilogue staging tiles | dA: the G/U ring (1024-aligned).
+// three [E+1] tables | epilogue staging tiles | dA: the G/U ring (1024-aligned).
 __host__ __device__ constexpr int epi_off(int mode) {
-  return (stages_of(mode) * stage_bytes(mode) + 512 + 2 * (kMaxExperts + 1) * 4 + 15) / 16 * 16;
+  return (stages_of(mode) * stage_bytes(mode) + 512 + 3 * (kMaxExperts + 1) * 4 + 15) / 16 * 16;
 }
 __host__ __device__ constexpr int gu_off(int mode) {
   return (epi_off(mode) + epi_warps(mode) * kEpiTileBytes + 1023) / 1024 * 1024;
@@ -91,6 +91,8 @@ struct Params {
   float *g_part;          // dA: partial router-weight gradients [M][g_np] (or null)
   int g_np;               // dA: partials per row (2 per 256-column tile)
   uint16_t *o0, *o1, *o2, *o3;
+  uint8_t *aw_t, *aw_t_sf;  // gate/up for an MXFP8 backward: w * A along tokens [I, Mpad] (or null)
+  int Mpad;
   float *of;   // router projection: fp32 output
   int n_out;   // router projection: output columns (E)
   int32_t *status;
@@ -115,7 +117,7 @@ struct Traits {
 
 template <int MODE>
 __device__ __forceinline__ Tile decode_tile(int tile, const Params &p, const int *s_tp,
-                                            const int *s_off) {
+                                            const int *s_off, const int *s_pad) {
   using Tr = Traits<MODE>;
   Tile t;
   if constexpr (!Tr::kRaggedK) {
@@ -133,8 +135,9 @@ __device__ __forceinline__ Tile decode_tile(int tile, const Params &p, const int
     t.row_end = s_off[lo + 1];
     t.n0 = nt * (Tr::kPair ? BN / 2 : BN);
     t.nkb = p.kdim / BK;
-    t.krow0 = 0;
-    t.kcount = 0;
+    // the padded token axis of an MXFP8 backward (each expert from a multiple of 128)
+    t.krow0 = s_pad[lo] + (t.m0 - s_off[lo]);
+    t.kcount = s_pad[lo] + (s_off[lo + 1] - s_off[lo] + 127) / 128 * 128;
   } else {
     const int per = p.m_tiles * p.n_tiles;
     t.e = s_tp[tile / per];  // experts in decreasing order of rows
@@ -232,6 +235,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
   // [E+1] ragged M: tile prefix over experts; ragged K: experts by decreasing row count
   int *s_tp = reinterpret_cast<int *>(smem + STAGES * kStageBytes + 512);
   int *s_off = s_tp + (kMaxExperts + 1);                                    // [E+1] row offsets
+  int *s_pad = s_off + (kMaxExperts + 1);  // [E+1] ragged M: padded offsets (128-aligned segments)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
@@ -300,6 +304,22 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
     }
     if (lane == 0) s_tp[E] = carry;
   }
+  if (!Tr::kRaggedK && warp == 3) {  // padded offsets: ceil(rows / 128) * 128 per expert
+    int carry = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      const int c = e < E ? (s_off[e + 1] - s_off[e] + 127) / 128 * 128 : 0;
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (e < E) s_pad[e] = carry + incl - c;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) s_pad[E] = carry;
+  }
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // both CTAs' barriers initialised before any remote arrival
@@ -318,7 +338,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
       uint32_t armed = 0, arm_par = 0;  // per stage: armed at least once, parity of last arm
       bool ok = true;
       for (int tile = cluster; tile < total && ok; tile += nclusters) {
-        const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off);
+        const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off, s_pad);
         if constexpr (Tr::kRaggedK) {  // this expert's maps were written by the preceding
           // launch; the thread that issues the copies acquires every map it will use
           if (t.nkb > 0)
@@ -367,7 +387,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
       int it = 0;
       bool ok = true;
       for (int tile = cluster; tile < total && ok; tile += nclusters, ++it) {
-        const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off);
+        const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off, s_pad);
         const int buf = it & 1;
         const uint32_t use = (it >> 1) & 1;
         if (!mbar_wait(&tempty[buf], use ^ 1, abort_flag)) break;
@@ -426,7 +446,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
     const uint32_t tempty1 = peer_smem_addr(&tempty[1], 0);
     int it = 0, gbase = 0;
     for (int tile = cluster; tile < total; tile += nclusters, ++it) {
-      const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off);
+      const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off, s_pad);
       const int buf = it & 1;
       const uint32_t use = (it >> 1) & 1;
       if (!wait_lane0(&tfull[buf], use, abort_flag)) break;
@@ -454,7 +474,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
       uint32_t armed = 0, arm_par = 0;
       bool ok = true;
       for (int tile = cluster; tile < total && ok; tile += nclusters) {
-        const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off);
+        const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off, s_pad);
         const int nch = min(BN / 32, (p.I - t.n0) / 32);
         for (int c = 0; c < nch; ++c, ++g) {
           const int slot = g % kGuSlots;
@@ -565,6 +585,9 @@ cudaError_t launch_mode(const GemmArgs &a, cudaStream_t s) {
   p.o2 = a.o2;
   p.o3 = a.o3;
   p.w_row = a.w_row;
+  p.aw_t = a.aw_t;
+  p.aw_t_sf = a.aw_t_sf;
+  p.Mpad = a.Mpad;
   p.g_part = a.g_part;
   p.g_np = 2 * ((a.I + 255) / 256);
   p.status = a.status;

@@ -93,6 +93,7 @@ struct MxParams {
   const float *w_row;
   uint16_t *o0, *o1, *o2, *o3;
   uint8_t *aq, *aq_sf;  // gate|up: A quantised along I
+  uint8_t *aw_t, *aw_t_sf;  // gate|up: w * A along tokens for the backward (or null)
   uint8_t *dg_q, *du_q, *dg_sf, *du_sf, *dg_t, *du_t, *dg_t_sf, *du_t_sf;  // dA's quantised outputs
   int32_t *status;
   int n_tiles, m_tiles;
@@ -221,39 +222,6 @@ __device__ __forceinline__ MxTile decode_mx(int tile, const MxParams &p, const i
   return x;
 }
 
-// The value a bf16 tensor would hold (nearest even), as fp32.
-__device__ __forceinline__ float round_bf16(float v) {
-  return __uint_as_float(static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v))) << 16);
-}
-
-// A warp's 32 x 32 values (lane = row, bf16-exact) quantised down the rows:
-// written to the staging tile as bf16, then lane j takes column j's 32 values
-// (one 32-token block) and writes its 32 codes at codes + (col0 + j) * ld +
-// tok0 and their scale code at sf_byte (its own column's byte).
-__device__ __forceinline__ void quant_down_rows32(uint8_t *tile, const float (&v)[32], uint8_t *codes,
-                                                  size_t ld, int col0, int tok0, uint8_t *sf_byte) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 w;
-    w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
-    w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
-    w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
-    w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
-    *reinterpret_cast<uint4 *>(tile + epi_swz(lane, q)) = w;
-  }
-  __syncwarp();
-  float c[32];
-  const int qc = lane >> 3, within = (lane & 7) * 2;
-#pragma unroll
-  for (int i = 0; i < 32; ++i)
-    c[i] = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(
-                               tile + epi_swz(i, qc) + within))
-                           << 16);
-  __syncwarp();  // the tile is rewritten by the next call
-  *sf_byte = quant32(c, reinterpret_cast<uint4 *>(codes + static_cast<size_t>(col0 + lane) * ld + tok0));
-}
-
 // dA's epilogue in the fp8_bwd backward: ring, dSwiGLU and the weighting as
 // in the bf16 engine's dA, then dG and dU rounded to bf16 (zero in the padded
 // rows past the expert's count) and quantised along I and along tokens.
@@ -333,10 +301,11 @@ __device__ __forceinline__ bool epilogue_da_mx(const MxTile &x, uint32_t tb, int
 }
 
 // The mxfp8 gate|up epilogue: accumulator columns [gate 32 | up 32] x 3 are
-// the output columns n0/2 + 32 j (pair j); SwiGLU as in the bf16 engine (A, G,
-// U and A_w = w A in bf16, rows past the expert's count not stored), and A
-// quantised along I into the padded row space for the down GEMM, from the
-// bf16 value A holds (zero in the padded rows past the count).
+// the output columns n0/2 + 32 j (pair j); SwiGLU as in the bf16 engine (A, G
+// and U in bf16, rows past the expert's count not stored), A quantised along I
+// into the padded row space for the down GEMM, from the bf16 value A holds
+// (zero in the padded rows past the count), and w * A quantised along tokens
+// for the backward's dW_down (its bf16 value; zero past the count).
 template <int NCH>
 __device__ __forceinline__ void epilogue_gateup_mx(const MxTile &x, uint32_t tb, int rit, const MxParams &p,
                                                    int part, uint8_t *tile) {
@@ -377,10 +346,17 @@ __device__ __forceinline__ void epilogue_gateup_mx(const MxTile &x, uint32_t tb,
     const int kb = col >> 5;
     p.aq_sf[sfi_base + (kb >> 2) * 512 + (kb & 3)] =
         quant32(v1, reinterpret_cast<uint4 *>(p.aq + static_cast<size_t>(prow) * p.I + col));
-    if (keep) {
+    if (p.o3 || p.aw_t) {
 #pragma unroll
       for (int i = 0; i < 32; ++i) v0[i] *= w;  // A_w = w * A, the dW_down operand
-      store_rows32(tile, p.o3 + off, p.I, nvalid, v0);
+      if (p.o3) store_rows32(tile, p.o3 + off, p.I, nvalid, v0);
+      if (p.aw_t) {  // along tokens from its bf16 value: the warp's 32 rows are one block (+0 past the count)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v1[i] = valid ? round_bf16(v0[i]) : 0.f;
+        const int prow0 = prow - lane;
+        const size_t sfb = atom_byte(col + lane, prow0 >> 5, p.Mpad, SfLayout{p.I, 128});
+        quant_down_rows32(tile, v1, p.aw_t, static_cast<size_t>(p.Mpad), col, prow0, p.aw_t_sf + sfb);
+      }
     }
   }
 }
@@ -739,6 +715,8 @@ cudaError_t launch_mx_mode(const MxGemmArgs &a, cudaStream_t s) {
   p.o3 = a.o3;
   p.aq = a.aq;
   p.aq_sf = a.aq_sf;
+  p.aw_t = a.aw_t;
+  p.aw_t_sf = a.aw_t_sf;
   p.dg_q = a.dg_q;
   p.du_q = a.du_q;
   p.dg_sf = a.dg_sf;

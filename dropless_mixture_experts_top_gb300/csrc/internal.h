@@ -109,6 +109,10 @@ struct GemmArgs {
   float *g_part;            // dA: the router weight's gradient, 2 partials per 256-column tile [M][np]
   // outputs (device, bf16)
   uint16_t *o0, *o1, *o2, *o3;
+  // gate/up for an MXFP8 backward: w * A quantised along tokens into the padded
+  // token axis (codes [I, Mpad], scales in 128-row atoms over K = Mpad), or null
+  uint8_t *aw_t, *aw_t_sf;
+  int Mpad;
   // router projection: x [T,H], W_r [H,E], d_logits as bf16 [T,E]; fp32 output, its columns
   const uint16_t *r_x, *r_w, *r_dlog;
   float *r_out;
@@ -198,8 +202,9 @@ struct MxGemmArgs {
   const uint16_t *G, *U;
   const float *w_row;
   uint16_t *o0, *o1, *o2, *o3;
-  // mxfp8 GEMM1: A quantised along I for the down GEMM (codes [Mpad, I], 128-row atoms)
-  uint8_t *aq, *aq_sf;
+  // mxfp8 GEMM1: A quantised along I for the down GEMM (codes [Mpad, I], 128-row atoms),
+  // and (or null) w * A along tokens for the backward's dW_down (codes [I, Mpad])
+  uint8_t *aq, *aq_sf, *aw_t, *aw_t_sf;
   // dA: its epilogue quantises dG and dU for the next two GEMMs -- along I
   // (codes [Mpad, I], 128-row scale atoms: dX's A operand) and along tokens
   // (codes [I, Mpad], 192-row scale groups: dW_gate/up's B operand)

@@ -346,9 +346,10 @@ class MoELayer:
         return self.saved[off:off + 2 * n].view(torch.int16).view(T * k, cols)
 
     def fp8_tensor(self, name):
-        """A quantised operand left in the backward scratch (fp8_bwd only): uint8
-        codes [rows, K] for *_q and *_t, the raw scale-atom bytes for *_sf, int32
-        [E+1] for pad_offsets."""
+        """A quantised operand left in the backward scratch (the fp8 modes), or for
+        aw_t / aw_t_sf (w * A along tokens, written by the forward) in `saved`:
+        uint8 codes [rows, K] for *_q and *_t, the raw scale-atom bytes for *_sf,
+        int32 [E+1] for pad_offsets."""
         lay = fp8_scratch_offsets(self.cfg)
         s = self.shape
         Mp = lay["m_pad"]
@@ -356,15 +357,16 @@ class MoELayer:
                   "wg_q": (s.E * s.H, s.I), "wu_q": (s.E * s.H, s.I), "aw_t": (s.I, Mp),
                   "dy_t": (s.H, Mp), "x_t": (s.H, Mp), "dg_t": (s.I, Mp), "du_t": (s.I, Mp)}
         off = lay[name]
+        buf = self.saved if name.startswith("aw_t") else self.bwd_scratch  # w * A: written by the forward
         if name == "pad_offsets":
-            return self.bwd_scratch[off:off + 4 * (s.E + 1)].view(torch.int32)
+            return buf[off:off + 4 * (s.E + 1)].view(torch.int32)
         if name.endswith("_sf"):
             base = name[:-3] + "_q" if name[:-3] + "_q" in rows_k else name[:-3]
             R, K = rows_k[base]
             seg, group = sf_grouping(base, s, Mp)
-            return self.bwd_scratch[off:off + sf_layout_bytes(R, K, seg, group)]
+            return buf[off:off + sf_layout_bytes(R, K, seg, group)]
         R, K = rows_k[name]
-        return self.bwd_scratch[off:off + R * K].view(R, K)
+        return buf[off:off + R * K].view(R, K)
 
     def fwd_fp8_tensor(self, name):
         """A quantised operand of the mxfp8 forward: in the forward scratch, or for

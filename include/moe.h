@@ -114,7 +114,9 @@ moe_status moe_query_workspace(const moe_config *cfg, size_t *route_scratch, siz
 
 /* Offsets (bytes) of the saved activations inside `saved`, for inspection:
  * x_perm [M,H], G [M,I], U [M,I], A [M,I], Y [M,H] (unweighted), A_w [M,I]
- * (A times the row's router weight: the weight-gradient operand), all bf16. */
+ * (A times the row's router weight: the weight-gradient operand), all bf16.
+ * A_w is written in MOE_PREC_BF16 only: the MXFP8 backwards read w * A
+ * quantised along tokens instead (moe_fp8_layout's aw_t, also in `saved`). */
 typedef struct {
   size_t x_perm, G, U, A, Y, A_w;
 } moe_saved_layout;
@@ -129,7 +131,9 @@ moe_status moe_saved_offsets(const moe_config *cfg, moe_saved_layout *layout);
  *   *_q     E4M3 codes, K-major: dy_q [m_pad,H] (padded rows), wd_q [E*I,H],
  *           dg_q/du_q [m_pad,I], wg_q/wu_q [E*H,I];
  *   *_t     token-axis operands transposed, tokens contiguous: aw_t (w*A) and
- *           dg_t/du_t [I,m_pad], dy_t and x_t [H,m_pad];
+ *           dg_t/du_t [I,m_pad], dy_t and x_t [H,m_pad]; aw_t and aw_t_sf are
+ *           offsets inside `saved`, not the scratch: the forward's gate/up
+ *           epilogue writes them (moe_forward and moe_forward_recompute);
  *   *_sf    their UE8M0 scale codes (2^(code-127)), one per 32 elements along
  *           K, in 512-byte atoms of 128 rows x 128 K, the order the tensor core
  *           reads them: row w of atom row-block rb, K-block b, sits at byte

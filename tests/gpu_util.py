@@ -110,6 +110,37 @@ def check_routing(shape, inp, layer):
     return idx, w, counts, offsets, ros, sor
 
 
+_E4M3 = None
+
+
+def e4m3_values():
+    global _E4M3
+    if _E4M3 is None:
+        _E4M3 = np.array([O.e4m3_decode(c) for c in range(256)], np.float64)
+    return _E4M3
+
+
+def check_aw_t(shape, layer, aw, offsets):
+    """w * A quantised along tokens [I, m_pad] (from its bf16 value, in the GPU's
+    fp32 arithmetic, so not bit-comparable with the oracle): dequantised, within
+    MXFP8 error of the oracle's w * a in every expert's tokens, and exactly zero
+    in the padded tokens past each expert's count."""
+    Mp = moe.fp8_scratch_offsets(layer.cfg)["m_pad"]
+    I = shape.I
+    codes = layer.fp8_tensor("aw_t").cpu().numpy()
+    sc = atoms_to_scales(layer.fp8_tensor("aw_t_sf").cpu().numpy(), I, Mp, I, 128).astype(np.int64)
+    deq = e4m3_values()[codes] * np.exp2(np.repeat(sc, 32, axis=1) - 127.0)
+    counts = np.diff(offsets)
+    pad = np.concatenate([[0], np.cumsum((counts + 127) // 128 * 128)]).astype(np.int64)
+    ref = np.zeros((I, Mp))
+    for e in range(len(counts)):
+        n = int(counts[e])
+        ref[:, pad[e]:pad[e] + n] = aw[offsets[e]:offsets[e] + n].T
+        assert np.all(codes[:, pad[e] + n:pad[e + 1]] == 0), e
+    P = int(pad[-1])
+    close("aw_t", deq[:, :P], ref[:, :P], rel_l2=5e-2, max_rel=8e-2)
+
+
 def check_full(shape, inp, layer, out, grads, precision="bf16", check_saved=True):
     """Every output element against the oracle (small shapes)."""
     idx, w, counts, offsets, ros, sor = check_routing(shape, inp, layer)
@@ -129,7 +160,10 @@ def check_full(shape, inp, layer, out, grads, precision="bf16", check_saved=True
         close("U", bf(layer.saved_tensor("U")), u, **ftol)
         close("A", bf(layer.saved_tensor("A")), a, **ftol)
         close("Y", bf(layer.saved_tensor("Y")), y, **ftol)
-        close("A_w", bf(layer.saved_tensor("A_w")), a * w.ravel()[sor][:, None], **ftol)
+        if quant:  # w * A exists only quantised along tokens, written by the forward's gate/up epilogue
+            check_aw_t(shape, layer, a * w.ravel()[sor][:, None], offsets)
+        else:
+            close("A_w", bf(layer.saved_tensor("A_w")), a * w.ravel()[sor][:, None], **ftol)
     ref = O.forward(shape, inp["x"], idx, w, inp["W_gate"], inp["W_up"], inp["W_down"], fwd_quant=fq, fW=fW)
     close("out", bf(out), ref, **ftol)
     dx, dl, gd = O.backward_tokens(shape, inp["x"], inp["logits"], idx, w, inp["W_gate"], inp["W_up"],
