@@ -70,8 +70,8 @@ def kernel_work(shape):
         "mx_pad_offsets": ("hbm", (E + 1) * 8.0, "B"),
         "mx_pad_offsets_fwd": ("hbm", (E + 1) * 8.0, "B"),
         # mxfp8 forward: x along H; the weights along their middle axis (gate and up, down)
-        # the permute with x quantised along H: reads x, writes x_perm and its codes
-        "permute_quant_x": ("hbm", T * H * 2 + M * H * (2 + 1 + 1 / 32) + M * 4, "B"),
+        # the dispatch with x quantised along H: reads x, writes its codes to every permuted row
+        "permute_quant_x": ("hbm", T * H * 2 + M * H * (1 + 1 / 32) + M * 4, "B"),
         "mx_zero_pad_rows": ("hbm", 127 * E * H * (1 + 1 / 32) / 2, "B"),
         # each weight read once, written along both axes
         "mx_quant_W_gateup_fwd": ("hbm", 2 * E * H * I * (2 + 2 * (1 + 1 / 32)), "B"),

@@ -305,7 +305,7 @@ struct Fp8Bwd {
   uint8_t *sc;
   int sms;
   int32_t *status;
-  const uint16_t *W_gate, *W_up, *W_down, *x_perm, *G, *U, *Y, *dy;
+  const uint16_t *W_gate, *W_up, *W_down, *x, *G, *U, *Y, *dy;
   const uint8_t *aw_t, *aw_t_sf;  // w * A along tokens, from the forward (in `saved`)
   uint16_t *dX, *dx, *dW_gate, *dW_up, *dW_down;
   float *g_part, *d_logits, *d_topk_w;
@@ -404,9 +404,9 @@ moe_status backward_fp8(const Fp8Bwd &f, cudaStream_t s) {
   m.o0 = f.dW_down;
   MOE_TRY(timed("mx_gemm_dW_down", s, [&] { return launch_mx_gemm(kMxGemmDWDown, m, s); }));
   // dW_gate = Q(x)^T . Q(dG), dW_up = Q(x)^T . Q(dU), K = the expert's tokens
-  MOE_TRY(timed("mx_quantT_x", s, [&] {
-    return launch_quant_cols(f.x_perm, H, Mp, off, pad_off, E, sc + q.x_t, sc + q.x_t_sf, sf_a(H),
-                             RowCodes{}, s);
+  MOE_TRY(timed("mx_quantT_x", s, [&] {  // gathered from x by token, not re-read from x_perm
+    return launch_quant_cols(f.x, H, Mp, off, pad_off, E, sc + q.x_t, sc + q.x_t_sf, sf_a(H), RowCodes{}, s,
+                             f.r->slot_of_row, k);
   }));
   m.a0 = sc + q.x_t;
   m.sfa0 = sc + q.x_t_sf;
@@ -448,7 +448,7 @@ moe_status forward_mx(const Mx8Fwd &f, cudaStream_t s) {
   const int32_t *off = f.r->offsets;
   MOE_TRY(timed("mx_pad_offsets_fwd", s, [&] { return launch_pad_offsets(off, E, pad_off, s); }));
   MOE_TRY(timed("permute_quant_x", s, [&] {
-    return launch_permute_quant(f.x, f.r->row_of_slot, f.r->topk_idx, off, pad_off, f.x_perm, sc + q.x_q,
+    return launch_permute_quant(f.x, f.r->row_of_slot, f.r->topk_idx, off, pad_off, nullptr, sc + q.x_q,
                                 sc + q.x_sf, sf_a(Mp), T, H, k, s);
   }));
   MOE_TRY(timed("mx_zero_pad_rows", s, [&] {
@@ -767,7 +767,7 @@ moe_status moe_backward(const moe_config *cfg, const void *dy, const void *x,
     f.W_gate = static_cast<const uint16_t *>(W_gate);
     f.W_up = static_cast<const uint16_t *>(W_up);
     f.W_down = static_cast<const uint16_t *>(W_down);
-    f.x_perm = x_perm;
+    f.x = static_cast<const uint16_t *>(x);
     f.G = G;
     f.U = U;
     f.aw_t = sv + L.q.aw_t;

@@ -73,11 +73,11 @@ __global__ void __launch_bounds__(kWarps * 32) permute_rows_kernel(const uint4 *
   }
 }
 
-// The permute with the mxfp8 forward's quantisation of x fused: x_perm as
-// above, and each token's row quantised along H once (a 32-element block is
-// four consecutive 16-byte vectors, i.e. four neighbouring lanes) with its
-// codes and scale written to the padded row of each of its k permuted rows
-// (expert e's rows start at pad_off[e]).
+// The mxfp8 forward's dispatch: each token's row quantised along H once (a
+// 32-element block is four consecutive 16-byte vectors, i.e. four neighbouring
+// lanes) with its codes and scale written to the padded row of each of its k
+// permuted rows (expert e's rows start at pad_off[e]); x_perm as above only
+// when xp is set (the mxfp8 GEMMs read the codes, and its backward gathers x).
 __global__ void __launch_bounds__(kWarps * 32) permute_quant_kernel(
     const uint4 *__restrict__ x, const int32_t *__restrict__ ros, const int32_t *__restrict__ topk_idx,
     const int32_t *__restrict__ offsets, const int32_t *__restrict__ pad_off, uint4 *__restrict__ xp,
@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(kWarps * 32) permute_quant_kernel(
       for (int u = 0; u < kVecPerLane; ++u) {
         const int v = v0 + u * 32 + lane;
         if (v < nv) {
-          dst[v] = buf[u];
+          if (xp) dst[v] = buf[u];
           cdst[v] = q[u];
           if ((lane & 3) == 0) sf[atom_byte(prow, v >> 2, H, L)] = scode[u];
         }

@@ -154,9 +154,11 @@ struct RowCodes {
   uint8_t *codes, *sf;
   SfLayout L;
 };
+// With slot_of_row set, src is token-major ([T, C]) and permuted row r reads
+// token slot_of_row[r] / k.
 cudaError_t launch_quant_cols(const uint16_t *src, int C, int Mpad, const int32_t *offsets,
                               const int32_t *pad_off, int E, uint8_t *codes, uint8_t *sf, SfLayout L,
-                              RowCodes rows, cudaStream_t s);
+                              RowCodes rows, cudaStream_t s, const int32_t *slot_of_row = nullptr, int k = 1);
 
 // The MXFP8 backward's one pass over dy: dy rows gathered by token for every
 // permuted row, quantised along H into the padded row space (rows) and along

@@ -100,7 +100,9 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t *__restr
 // bytes against bank conflicts), which leaves as full 128-byte rows.
 // Optionally the same tile is also quantised along its rows (one thread per
 // (row, 32-column block)) into the padded row space, so an operand needed on
-// both axes (dy) is read once.  Tiles past the padded total are skipped.
+// both axes is read once; and the rows may be gathered from a token-major
+// source (permuted row r reads token slot_of_row[r] / k) instead of read from
+// a permuted copy.  Tiles past the padded total are skipped.
 constexpr int kQcRows = 128, kQcCols = 64, kQcThreads = 256;
 constexpr int kQcRing = 4;                         // staged tiles in flight per block
 constexpr int kQcTileElems = kQcRows * kQcCols;   // bf16 per staged tile (16 KB)
@@ -189,7 +191,8 @@ __global__ void __launch_bounds__(kQcThreads, 3) quant_cols_kernel(const uint16_
                                                                 const int32_t *__restrict__ pad_off, int E,
                                                                 uint8_t *__restrict__ codes,
                                                                 uint8_t *__restrict__ sf, SfLayout L,
-                                                                RowCodes rows) {
+                                                                RowCodes rows,
+                                                                const int32_t *__restrict__ slot_of_row, int k) {
   extern __shared__ __align__(16) uint8_t qc_smem[];
   uint16_t *ring = reinterpret_cast<uint16_t *>(qc_smem);
   uint8_t *otile = qc_smem + kQcRing * kQcTileElems * 2;
@@ -213,8 +216,12 @@ __global__ void __launch_bounds__(kQcThreads, 3) quant_cols_kernel(const uint16_
   __syncthreads();
   if (s_seg[2]) return;
   const int row0 = s_seg[0], nvalid = s_seg[1];
+  __shared__ int s_src[kQcRows];  // source row of each permuted row (its token's, when gathering)
+  for (int r = threadIdx.x; r < nvalid; r += kQcThreads)
+    s_src[r] = slot_of_row ? __ldg(slot_of_row + row0 + r) / k : row0 + r;
+  __syncthreads();
   auto row_ptr = [&](int r) -> const uint16_t * {
-    return r < nvalid ? src + static_cast<size_t>(row0 + r) * C : nullptr;
+    return r < nvalid ? src + static_cast<size_t>(s_src[r]) * C : nullptr;
   };
   qc_walk(ring, blockIdx.y * kQcCols, gridDim.y * kQcCols, C, row_ptr, [&](const uint16_t *tile, int c0) {
     if (rows.codes) {  // along the rows: thread = (row, 32-column block); zero rows past the count
@@ -423,7 +430,7 @@ cudaError_t launch_quant_rows(const uint16_t *src, int rows_out, int K, const in
 
 cudaError_t launch_quant_cols(const uint16_t *src, int C, int Mpad, const int32_t *offsets,
                               const int32_t *pad_off, int E, uint8_t *codes, uint8_t *sf, SfLayout L,
-                              RowCodes rows, cudaStream_t s) {
+                              RowCodes rows, cudaStream_t s, const int32_t *slot_of_row, int k) {
   const int col_blocks = C / kQcCols < 4 ? C / kQcCols : 4;  // each loops over C / (64 * 4) column tiles
   const dim3 grid(static_cast<unsigned>(Mpad / kQcRows), static_cast<unsigned>(col_blocks));
   static DeviceOnce once;  // dynamic shared memory above 48 KB, opted in once per device
@@ -431,7 +438,8 @@ cudaError_t launch_quant_cols(const uint16_t *src, int C, int Mpad, const int32_
     return cudaFuncSetAttribute(quant_cols_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQcSmem);
   });
   if (e != cudaSuccess) return e;
-  quant_cols_kernel<<<grid, kQcThreads, kQcSmem, s>>>(src, C, Mpad, offsets, pad_off, E, codes, sf, L, rows);
+  quant_cols_kernel<<<grid, kQcThreads, kQcSmem, s>>>(src, C, Mpad, offsets, pad_off, E, codes, sf, L, rows,
+                                                       slot_of_row, k);
   return cudaGetLastError();
 }
 

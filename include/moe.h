@@ -116,7 +116,9 @@ moe_status moe_query_workspace(const moe_config *cfg, size_t *route_scratch, siz
  * x_perm [M,H], G [M,I], U [M,I], A [M,I], Y [M,H] (unweighted), A_w [M,I]
  * (A times the row's router weight: the weight-gradient operand), all bf16.
  * A_w is written in MOE_PREC_BF16 only: the MXFP8 backwards read w * A
- * quantised along tokens instead (moe_fp8_layout's aw_t, also in `saved`). */
+ * quantised along tokens instead (moe_fp8_layout's aw_t, also in `saved`).
+ * x_perm is not written in MOE_PREC_MXFP8, whose GEMMs read x's codes and whose
+ * backward reads x itself. */
 typedef struct {
   size_t x_perm, G, U, A, Y, A_w;
 } moe_saved_layout;

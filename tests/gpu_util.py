@@ -150,8 +150,9 @@ def check_full(shape, inp, layer, out, grads, precision="bf16", check_saved=True
     tol = dict(rel_l2=FP8_REL_L2, max_rel=FP8_MAX_REL) if quant else {}
     ftol = tol if fq else {}
     if check_saved:
-        xp = layer.saved_tensor("x_perm").cpu().numpy().view(np.uint16)
-        np.testing.assert_array_equal(xp, inp["x"][sor // shape.k])
+        if not fq:  # the mxfp8 mode keeps x only quantised (its backward reads x itself)
+            xp = layer.saved_tensor("x_perm").cpu().numpy().view(np.uint16)
+            np.testing.assert_array_equal(xp, inp["x"][sor // shape.k])
         toks = sor // shape.k
         experts = idx.ravel()[sor]
         g, u, a, y = O.expert_rows(shape, inp["x"], inp["W_gate"], inp["W_up"], inp["W_down"], toks, experts,
