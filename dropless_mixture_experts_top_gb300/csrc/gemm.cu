@@ -272,13 +272,16 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
   for (int e = threadIdx.x; e <= E; e += threads_of(MODE))
     s_off[e] = p.offsets ? __ldg(p.offsets + e) : (e == 0 ? 0 : p.M_rows);
   __syncthreads();
+  bool skewed = false;
   if (Tr::kRaggedK) {
     // Skewed routing (an expert with more than twice the mean rows): longest
-    // reductions first, so the static round-robin hands out the experts' tiles
-    // in decreasing order of work.  Balanced routing keeps the natural order.
+    // reductions first, and the tiles go out in a snake over the CTA pairs
+    // (round r to pairs 0, 1, ... when r is even, to pairs ..., 1, 0 when odd),
+    // which balances decreasing work much better than a plain round-robin.
+    // Balanced routing keeps the natural order and the round-robin.
     int cmax = 0;
     for (int f = 0; f < E; ++f) cmax = max(cmax, s_off[f + 1] - s_off[f]);
-    const bool skewed = static_cast<int64_t>(cmax) * E > 2 * static_cast<int64_t>(s_off[E] - s_off[0]);
+    skewed = static_cast<int64_t>(cmax) * E > 2 * static_cast<int64_t>(s_off[E] - s_off[0]);
     for (int e = threadIdx.x; e < E; e += threads_of(MODE)) {
       const int c = s_off[e + 1] - s_off[e];
       int r = 0;
@@ -327,6 +330,11 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
   const uint32_t tmem_base = *tmem_slot;
 
   const int total = Tr::kRaggedK ? E * p.m_tiles * p.n_tiles : s_tp[E] * p.n_tiles;
+  // the it-th tile of this CTA pair (>= total: none left)
+  auto tile_at = [&](int it) {
+    const int c = (skewed && (it & 1)) ? nclusters - 1 - cluster : cluster;
+    return it * nclusters + c;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
@@ -337,7 +345,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
       uint32_t phase = 0;
       uint32_t armed = 0, arm_par = 0;  // per stage: armed at least once, parity of last arm
       bool ok = true;
-      for (int tile = cluster; tile < total && ok; tile += nclusters) {
+      for (int it = 0, tile = tile_at(0); tile < total && ok; tile = tile_at(++it)) {
         const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off, s_pad);
         if constexpr (Tr::kRaggedK) {  // this expert's maps were written by the preceding
           // launch; the thread that issues the copies acquires every map it will use
@@ -386,7 +394,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
-      for (int tile = cluster; tile < total && ok; tile += nclusters, ++it) {
+      for (int tile = tile_at(0); tile < total && ok; tile = tile_at(++it)) {
         const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off, s_pad);
         const int buf = it & 1;
         const uint32_t use = (it >> 1) & 1;
@@ -445,7 +453,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
     const uint32_t tempty0 = peer_smem_addr(&tempty[0], 0);
     const uint32_t tempty1 = peer_smem_addr(&tempty[1], 0);
     int it = 0, gbase = 0;
-    for (int tile = cluster; tile < total; tile += nclusters, ++it) {
+    for (int tile = tile_at(0); tile < total; tile = tile_at(++it)) {
       const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off, s_pad);
       const int buf = it & 1;
       const uint32_t use = (it >> 1) & 1;
@@ -473,7 +481,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
       int g = 0;
       uint32_t armed = 0, arm_par = 0;
       bool ok = true;
-      for (int tile = cluster; tile < total && ok; tile += nclusters) {
+      for (int it = 0, tile = tile_at(0); tile < total && ok; tile = tile_at(++it)) {
         const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off, s_pad);
         const int nch = min(BN / 32, (p.I - t.n0) / 32);
         for (int c = 0; c < nch; ++c, ++g) {

@@ -63,6 +63,35 @@ def test_all_tokens_one_expert_tail():
     G.check_full(shape, inp, layer, out, grads)
 
 
+def test_hot_experts_weight_gradients_bitwise():
+    """Skewed routing (the weight gradients' longest-first order and snake assignment of
+    tiles to CTA pairs): every element against the oracle, and a second step gives the
+    same bits."""
+    shape = MoEShape(T=2048, H=256, I=256, E=16, k=2)  # mean 256 rows per expert
+    inp = synth.make_inputs_shape(shape, 61)
+    inp["logits"][:, 3] += 6.0   # in nearly every token's top 2: ~8x the mean
+    inp["logits"][:, 11] += 2.0  # a second hot expert
+    layer, out, grads = G.run_layer(shape, inp)
+    G.check_full(shape, inp, layer, out, grads)
+    counts = layer.routing["counts"].cpu().numpy()
+    assert counts[3] > 6 * counts.mean() and counts[11] > 2 * counts.mean()
+    first = {n: grads[n].clone() for n in ("dW_gate", "dW_up", "dW_down")}
+    _, _, grads2 = G.run_layer(shape, inp, layer=layer)
+    for n, v in first.items():
+        assert torch.equal(grads2[n], v), n
+
+
+def test_many_hot_experts():
+    """Twenty hot experts among sixty-four: every element against the oracle."""
+    shape = MoEShape(T=2048, H=128, I=128, E=64, k=4)  # mean 128 rows per expert
+    inp = synth.make_inputs_shape(shape, 67)
+    inp["logits"][:, :20] += 4.0  # each of the twenty takes about 3x the mean
+    layer, out, grads = G.run_layer(shape, inp)
+    G.check_full(shape, inp, layer, out, grads)
+    counts = layer.routing["counts"].cpu().numpy()
+    assert (counts > 2 * counts.mean()).sum() > 16
+
+
 PRECISIONS = ["bf16", "fp8_bwd", "mxfp8"]
 
 
