@@ -133,6 +133,16 @@ def gemm_bytes(shape):
     }
 
 
+def launches_in_timed_region(labels, steps_hooked, steps):
+    """Kernels the library launched in the timed region: the timing hook's labels of
+    the hooked steps, scaled to all steps (every step launches the same kernels).
+    Four labels cover two kernels each: the ragged-K GEMMs (their per-expert tensor
+    maps, then the GEMM) and the mxfp8 forward's gate and up weight quantisers."""
+    per_label = {"gemm_dW_down": 2, "gemm_dW_gateup": 2, "router_gemm_dW": 2, "mx_quant_W_gateup_fwd": 2}
+    n = sum(per_label.get(lab, 1) for lab in labels)
+    return n * steps // max(steps_hooked, 1)
+
+
 def kernel_source(label):
     """The .cu file that defines the kernel behind a timing label."""
     if label.startswith("mx_gemm_"):
@@ -380,20 +390,24 @@ def run_ours(args):
     if any(st.values()):
         raise RuntimeError(f"device status after warm-up: {st}")
 
-    # timed region: per-step events, per-kernel events through the library's timing hook
+    # timed region: per-step events; per-kernel events through the library's
+    # timing hook on the last KH steps only (two events around every kernel are
+    # stream work a user does not pay for; the other steps run without them)
     K = args.steps
+    KH = min(K, 2)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     mids = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    cap = 64 * K
+    cap = 64 * KH
     kev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * cap)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        moe.timing_attach(kev)
         with torch.cuda.stream(stream):
             for i in range(K):
+                if i == K - KH:
+                    moe.timing_attach(kev)
                 flush.zero_()
                 starts[i].record(stream)
                 ev_mid = mids[i]
@@ -601,7 +615,7 @@ def run_ours(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "pipeline": "K steps; inputs copied in on one stream, results out on another, "
                             "double-buffered around the compute stream; no L2 flush (inputs exceed L2)"},
-        "gpu_launches": nk, "clocks": clk.summary(),
+        "gpu_launches": launches_in_timed_region(labels, KH, K), "clocks": clk.summary(),
         "router_projection": router_ms,
     }
     if not args.no_cpu_baseline and world == 1:
