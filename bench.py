@@ -81,7 +81,6 @@ def kernel_work(shape):
         # dy read once (through each permuted row's token), Y read for the router
         # gradient, codes and scales written along H and along tokens, g in partials
         "mx_dy_quant_gdot": ("hbm", T * H * 2 + M * H * 2 + 2 * M * H * (1 + 1 / 32) + M * 4 * 4.0, "B"),
-        "mx_quant_W_down": q(E * I * H), "mx_quant_W_gate": q(E * H * I), "mx_quant_W_up": q(E * H * I),
         "mx_quantT_x": q(M * H),
         "mx_gemm_dA_dswiglu": ("tensor_fp8", 2 * MHI, "flop"),
         "mx_gemm_dX": ("tensor_fp8", 4 * MHI, "flop"),
@@ -104,21 +103,24 @@ def kernel_work(shape):
     }
 
 
-def gemm_bytes(shape):
+def gemm_bytes(shape, precision="bf16"):
     """Algorithmic HBM bytes per launch of each grouped GEMM: every operand read
     once and every output written once (bf16 2 B; MXFP8 one code byte per element
     plus one scale byte per 32).  Against the measured HBM bandwidth this gives a
     GEMM's second roof: the one that binds is the larger of flops / tensor peak and
     bytes / HBM bandwidth (the fused dSwiGLU GEMM, which reads G and U and writes
-    dG and dU, is HBM-bound at the 30B shape)."""
+    dG and dU, is HBM-bound at the 30B shape).  Before an MXFP8 backward the two
+    bf16 forward GEMMs also write the weights' codes, and GEMM1 w * A as codes
+    along tokens instead of bf16."""
     T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
     M = float(T * k)
     W = float(E) * H * I  # one expert weight tensor's elements
     c = 1 + 1 / 32
     np_ = 2 * ((I + 255) // 256)
+    fp8b = precision == "fp8_bwd"
     return {
-        "gemm_gateup_swiglu": M * H * 2 + 2 * W * 2 + 4 * M * I * 2,
-        "gemm_down": M * I * 2 + W * 2 + M * H * 2,
+        "gemm_gateup_swiglu": M * H * 2 + 2 * W * 2 + (3 * M * I * 2 + M * I * c + 2 * W * c if fp8b else 4 * M * I * 2),
+        "gemm_down": M * I * 2 + W * 2 + M * H * 2 + (W * c if fp8b else 0.0),
         "gemm_dA_dswiglu": M * H * 2 + W * 2 + 2 * M * I * 2 + 2 * M * I * 2 + M * np_ * 4,
         "gemm_dX": 2 * M * I * 2 + 2 * W * 2 + M * H * 2,
         "gemm_dW_down": M * I * 2 + M * H * 2 + W * 2,
@@ -566,7 +568,7 @@ def run_ours(args):
 
     peaks, peak_src = load_peaks()
     work = kernel_work(shape)
-    gbytes = gemm_bytes(shape)
+    gbytes = gemm_bytes(shape, w.precision)
     fwd_fl, bwd_fl = shape.gemm_flops()
     kernels = {}
     for lab, ts in kern.items():

@@ -114,19 +114,30 @@ Layout layout_of(const moe_config *c) {
     L.q.aw_t_sf = o;
     o += align256(I * Mp / 32);
   }
-  if (c->precision == MOE_PREC_MXFP8) {  // the backward's weight operands, written by the forward
-    moe_mxfp8_fwd_layout &f = L.fq;
+  if (c->precision != MOE_PREC_BF16) {
+    // the backward's weight operands, written by the forward: in fp8_bwd by the
+    // bf16 GEMMs as the weights pass through them, in mxfp8 by its weight passes
+    moe_fp8_layout &q = L.q;
     auto take = [&o](size_t bytes) {
       const size_t at = o;
       o += align256(bytes);
       return at;
     };
-    f.bwd_wd_q = take(E * I * H);
-    f.bwd_wd_sf = take(sf_layout_bytes(E * I, H, sf_b(I)));
-    f.bwd_wg_q = take(E * H * I);
-    f.bwd_wg_sf = take(sf_layout_bytes(E * H, I, sf_b(H)));
-    f.bwd_wu_q = take(E * H * I);
-    f.bwd_wu_sf = take(sf_layout_bytes(E * H, I, sf_b(H)));
+    q.wd_q = take(E * I * H);
+    q.wd_sf = take(sf_layout_bytes(E * I, H, sf_b(I)));
+    q.wg_q = take(E * H * I);
+    q.wg_sf = take(sf_layout_bytes(E * H, I, sf_b(H)));
+    q.wu_q = take(E * H * I);
+    q.wu_sf = take(sf_layout_bytes(E * H, I, sf_b(H)));
+    if (c->precision == MOE_PREC_MXFP8) {
+      moe_mxfp8_fwd_layout &f = L.fq;
+      f.bwd_wd_q = q.wd_q;
+      f.bwd_wd_sf = q.wd_sf;
+      f.bwd_wg_q = q.wg_q;
+      f.bwd_wg_sf = q.wg_sf;
+      f.bwd_wu_q = q.wu_q;
+      f.bwd_wu_sf = q.wu_sf;
+    }
   }
   L.s_total = o > 0 ? o : 256;
   o = kHeader;
@@ -181,21 +192,10 @@ Layout layout_of(const moe_config *c) {
     q.pad_offsets = take((E + 1) * 4);
     q.dy_q = take(Mp * H);
     q.dy_sf = take(Mp * H / 32);
-    const bool wq = c->precision == MOE_PREC_FP8_BWD;  // mxfp8: the weights' codes are in `saved`
-    if (wq) {
-      q.wd_q = take(E * I * H);
-      q.wd_sf = take(sf_layout_bytes(E * I, H, sf_b(I)));
-    }
     q.dg_q = take(Mp * I);
     q.dg_sf = take(Mp * I / 32);
     q.du_q = take(Mp * I);
     q.du_sf = take(Mp * I / 32);
-    if (wq) {
-      q.wg_q = take(E * H * I);
-      q.wg_sf = take(sf_layout_bytes(E * H, I, sf_b(H)));
-      q.wu_q = take(E * H * I);
-      q.wu_sf = take(sf_layout_bytes(E * H, I, sf_b(H)));
-    }
     q.dy_t = take(H * Mp);
     q.dy_t_sf = take(sf_layout_bytes(H, Mp, sf_b(H)));
     q.x_t = take(H * Mp);
@@ -305,14 +305,13 @@ struct Fp8Bwd {
   uint8_t *sc;
   int sms;
   int32_t *status;
-  const uint16_t *W_gate, *W_up, *W_down, *x, *G, *U, *Y, *dy;
+  const uint16_t *x, *G, *U, *Y, *dy;
   const uint8_t *aw_t, *aw_t_sf;  // w * A along tokens, from the forward (in `saved`)
   uint16_t *dX, *dx, *dW_gate, *dW_up, *dW_down;
   float *g_part, *d_logits, *d_topk_w;
-  // the weights' codes for the three GEMMs that read them: quantised here
-  // (fp8_bwd, into the scratch) or already by the forward (mxfp8, in `saved`)
-  bool quantise_weights;
-  uint8_t *wd_q, *wd_sf, *wg_q, *wg_sf, *wu_q, *wu_sf;
+  // the weights' codes for the three GEMMs that read them, written by the
+  // forward (in `saved`)
+  const uint8_t *wd_q, *wd_sf, *wg_q, *wg_sf, *wu_q, *wu_sf;
 };
 
 moe_status backward_fp8(const Fp8Bwd &f, cudaStream_t s) {
@@ -351,10 +350,6 @@ moe_status backward_fp8(const Fp8Bwd &f, cudaStream_t s) {
                               f.d_topk_w, T, E, k, s);
   }));
   // dA = w (Q(dy) . Q(W_down)^T), K = H; dSwiGLU epilogue -> Q(dG), Q(dU) on both axes.
-  if (f.quantise_weights)
-    MOE_TRY(timed("mx_quant_W_down", s, [&] {
-      return launch_quant_rows(f.W_down, E * I, H, nullptr, nullptr, E, f.wd_q, f.wd_sf, sf_b(I), s);
-    }));
   m.a0 = sc + q.dy_q;
   m.sfa0 = sc + q.dy_sf;
   m.b0 = f.wd_q;
@@ -372,14 +367,6 @@ moe_status backward_fp8(const Fp8Bwd &f, cudaStream_t s) {
   m.du_t_sf = sc + q.du_t_sf;
   MOE_TRY(timed("mx_gemm_dA_dswiglu", s, [&] { return launch_mx_gemm(kMxGemmDA, m, s); }));
   // dX = Q(dG) . Q(W_gate)^T + Q(dU) . Q(W_up)^T, K = I
-  if (f.quantise_weights) {
-    MOE_TRY(timed("mx_quant_W_gate", s, [&] {
-      return launch_quant_rows(f.W_gate, E * H, I, nullptr, nullptr, E, f.wg_q, f.wg_sf, sf_b(H), s);
-    }));
-    MOE_TRY(timed("mx_quant_W_up", s, [&] {
-      return launch_quant_rows(f.W_up, E * H, I, nullptr, nullptr, E, f.wu_q, f.wu_sf, sf_b(H), s);
-    }));
-  }
   m.a0 = sc + q.dg_q;
   m.sfa0 = sc + q.dg_sf;
   m.a1 = sc + q.du_q;
@@ -590,6 +577,12 @@ moe_status forward_impl(FwdKind kind, const moe_config *cfg, const void *x, cons
     g.aw_t = keep && fp8b ? sv + L.q.aw_t : nullptr;
     g.aw_t_sf = keep && fp8b ? sv + L.q.aw_t_sf : nullptr;
     g.Mpad = static_cast<int>(L.q.m_pad);
+    if (keep && fp8b) {  // the backward's W_gate and W_up codes, quantised as they pass through GEMM1
+      g.wq[0] = sv + L.q.wg_q;
+      g.wq_sf[0] = sv + L.q.wg_sf;
+      g.wq[1] = sv + L.q.wu_q;
+      g.wq_sf[1] = sv + L.q.wu_sf;
+    }
     MOE_TRY(timed(gemm_mode_name(kFwdGateUp), s, [&] { return launch_grouped_gemm(kFwdGateUp, g, s); }));
     // the bf16 backward never reads Y (its router gradient comes from the dA GEMM),
     // so a recompute for it stops after GEMM1; the fp8 modes' backward reads Y
@@ -598,6 +591,9 @@ moe_status forward_impl(FwdKind kind, const moe_config *cfg, const void *x, cons
     g.o0 = Y;
     g.o1 = g.o2 = g.o3 = nullptr;
     g.aw_t = g.aw_t_sf = nullptr;
+    g.wq[0] = keep && fp8b ? sv + L.q.wd_q : nullptr;  // and W_down's, through GEMM2
+    g.wq_sf[0] = keep && fp8b ? sv + L.q.wd_sf : nullptr;
+    g.wq[1] = g.wq_sf[1] = nullptr;
     MOE_TRY(timed(gemm_mode_name(kFwdDown), s, [&] { return launch_grouped_gemm(kFwdDown, g, s); }));
   }
   if (kind == kFwdRecompute) return MOE_OK;
@@ -764,9 +760,6 @@ moe_status moe_backward(const moe_config *cfg, const void *dy, const void *x,
     f.sc = sc;
     f.sms = di.sms;
     f.status = status;
-    f.W_gate = static_cast<const uint16_t *>(W_gate);
-    f.W_up = static_cast<const uint16_t *>(W_up);
-    f.W_down = static_cast<const uint16_t *>(W_down);
     f.x = static_cast<const uint16_t *>(x);
     f.G = G;
     f.U = U;
@@ -782,20 +775,12 @@ moe_status moe_backward(const moe_config *cfg, const void *dy, const void *x,
     f.dW_gate = static_cast<uint16_t *>(dW_gate);
     f.dW_up = static_cast<uint16_t *>(dW_up);
     f.dW_down = static_cast<uint16_t *>(dW_down);
-    f.quantise_weights = cfg->precision == MOE_PREC_FP8_BWD;
-    uint8_t *wb = f.quantise_weights ? sc : const_cast<uint8_t *>(sv);  // read only when in `saved`
-    const size_t o_wd = f.quantise_weights ? L.q.wd_q : L.fq.bwd_wd_q;
-    const size_t o_wd_sf = f.quantise_weights ? L.q.wd_sf : L.fq.bwd_wd_sf;
-    const size_t o_wg = f.quantise_weights ? L.q.wg_q : L.fq.bwd_wg_q;
-    const size_t o_wg_sf = f.quantise_weights ? L.q.wg_sf : L.fq.bwd_wg_sf;
-    const size_t o_wu = f.quantise_weights ? L.q.wu_q : L.fq.bwd_wu_q;
-    const size_t o_wu_sf = f.quantise_weights ? L.q.wu_sf : L.fq.bwd_wu_sf;
-    f.wd_q = wb + o_wd;
-    f.wd_sf = wb + o_wd_sf;
-    f.wg_q = wb + o_wg;
-    f.wg_sf = wb + o_wg_sf;
-    f.wu_q = wb + o_wu;
-    f.wu_sf = wb + o_wu_sf;
+    f.wd_q = sv + L.q.wd_q;
+    f.wd_sf = sv + L.q.wd_sf;
+    f.wg_q = sv + L.q.wg_q;
+    f.wg_sf = sv + L.q.wg_sf;
+    f.wu_q = sv + L.q.wu_q;
+    f.wu_sf = sv + L.q.wu_sf;
     return backward_fp8(f, s);
   }
   // bf16: dy is permuted; the router weight's gradient g_tj = <dy_t . W_down^T,

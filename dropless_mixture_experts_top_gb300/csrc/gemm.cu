@@ -30,6 +30,9 @@
 //               (two per quarter, one per column half) for the modes with the
 //               heaviest epilogues: gate/up, dA and the router's dx
 //   dA only     one more warp streams each tile's G and U into the G/U ring
+//   forward GEMMs of an MXFP8 backward: after each tile's epilogue, the
+//               epilogue warps quantise part of the weights into the backward's
+//               weight codes (8 epilogue warps for the down GEMM too)
 // Every wait is bounded; on a timeout the kernel flags the status word,
 // drains its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -61,12 +64,12 @@ constexpr int kMapsPerExpert = 3;             // ragged K: A, B0, B1
 // operand ring of 5 stages to make room.  The other modes run slower with 8
 // epilogue warps.
 __host__ __device__ constexpr int stages_of(int mode) { return mode == kBwdDA ? 5 : 3; }
-__host__ __device__ constexpr int epi_warps(int mode) {
-  return (mode == kBwdDA || mode == kFwdGateUp || mode == kRouterDX) ? 8 : 4;
+__host__ __device__ constexpr int epi_warps(int mode, bool wq = false) {
+  return (mode == kBwdDA || mode == kFwdGateUp || mode == kRouterDX || (mode == kFwdDown && wq)) ? 8 : 4;
 }
 __host__ __device__ constexpr int gu_warps(int mode) { return mode == kBwdDA ? 1 : 0; }
-__host__ __device__ constexpr int threads_of(int mode) {
-  return 64 + 32 * (epi_warps(mode) + gu_warps(mode));
+__host__ __device__ constexpr int threads_of(int mode, bool wq = false) {
+  return 64 + 32 * (epi_warps(mode, wq) + gu_warps(mode));
 }
 constexpr uint32_t kTmemCols = 2 * BN;
 // Shared memory (from a 1024-aligned base): operand stages | barriers (512) |
@@ -74,13 +77,14 @@ constexpr uint32_t kTmemCols = 2 * BN;
 __host__ __device__ constexpr int epi_off(int mode) {
   return (stages_of(mode) * stage_bytes(mode) + 512 + 3 * (kMaxExperts + 1) * 4 + 15) / 16 * 16;
 }
-__host__ __device__ constexpr int gu_off(int mode) {
-  return (epi_off(mode) + epi_warps(mode) * kEpiTileBytes + 1023) / 1024 * 1024;
+__host__ __device__ constexpr int gu_off(int mode, bool wq = false) {
+  return (epi_off(mode) + epi_warps(mode, wq) * kEpiTileBytes + 1023) / 1024 * 1024;
 }
-__host__ __device__ constexpr int smem_bytes(int mode) {
-  return gu_off(mode) + gu_warps(mode) * kGuSlots * kGuChunkBytes + 1024 /*align*/;
+__host__ __device__ constexpr int smem_bytes(int mode, bool wq = false) {
+  return gu_off(mode, wq) + gu_warps(mode) * kGuSlots * kGuChunkBytes + 1024 /*align*/;
 }
-static_assert(smem_bytes(kBwdDA) <= 227 * 1024 && smem_bytes(kFwdGateUp) <= 227 * 1024,
+static_assert(smem_bytes(kBwdDA) <= 227 * 1024 && smem_bytes(kFwdGateUp) <= 227 * 1024 &&
+                  smem_bytes(kFwdDown, true) <= 227 * 1024,
               "shared memory budget");
 
 struct Params {
@@ -93,6 +97,10 @@ struct Params {
   uint16_t *o0, *o1, *o2, *o3;
   uint8_t *aw_t, *aw_t_sf;  // gate/up for an MXFP8 backward: w * A along tokens [I, Mpad] (or null)
   int Mpad;
+  // forward GEMMs for an MXFP8 backward: the bf16 weights ([E*H, I] gate (0) and
+  // up (1), or [E*I, H] down (0)) and their codes along the last axis with scale atoms
+  const uint16_t *wsrc[2];
+  uint8_t *wq[2], *wq_sf[2];
   float *of;   // router projection: fp32 output
   int n_out;   // router projection: output columns (E)
   int32_t *status;
@@ -209,14 +217,84 @@ __device__ __forceinline__ void produce_stage(const Tile &t, int kb, int rank, u
   }
 }
 
-template <int MODE>
-__global__ void __launch_bounds__(threads_of(MODE), 1)
+// The backward's weight codes for 32 rows x 128 columns of a bf16 weight
+// ([rows, ld] row-major, row0 a multiple of 32, col0 of 128): E4M3 codes and
+// UE8M0 scales in blocks of 32 along the rows, the quantiser's rule
+// (mxfp8.cuh).  One warp: four rows per step, eight lanes per row, sixteen
+// columns per lane, so a block's amax takes one exchange between lane pairs and
+// each row leaves as one 128-byte line of codes and one 4-byte word of scales.
+// The 32 rows lie in one 128-row scale atom (segments and groups are multiples
+// of 64 rows), so the scale words are the atom's base plus the row's offset.
+// Each batch of kBatch steps issues its loads together (all eight where the
+// kernel's registers allow).
+template <int kBatch>
+__device__ __forceinline__ void quant_weight_rows(const uint16_t *__restrict__ w, int row0, int col0, int ld,
+                                                  uint8_t *__restrict__ codes, uint8_t *__restrict__ sf,
+                                                  SfLayout L, int lane) {
+  const int sub = lane & 7, r4 = lane >> 3;
+  const size_t base = atom_byte(row0, col0 >> 5, ld, L);  // word of the block's first row
+  const int w0 = (row0 - (row0 / L.seg) * L.seg) % L.group & 127;  // its row within the atom
+  const uint4 *src = reinterpret_cast<const uint4 *>(w + static_cast<size_t>(row0 + r4) * ld + col0 + sub * 16);
+  uint8_t *dst = codes + static_cast<size_t>(row0 + r4) * ld + col0 + sub * 16;
+  const size_t step = static_cast<size_t>(4) * ld;  // four rows, in elements and in code bytes
+#pragma unroll 1
+  for (int bt = 0; bt < 8 / kBatch; ++bt) {
+    uint4 in[kBatch][2];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const size_t off = (bt * kBatch + j) * step / 8;
+      in[j][0] = __ldg(src + off);
+      in[j][1] = __ldg(src + off + 1);
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int i = bt * kBatch + j;  // step: rows 4i .. 4i+3 of the 32
+      const uint32_t u[8] = {in[j][0].x, in[j][0].y, in[j][0].z, in[j][0].w,
+                             in[j][1].x, in[j][1].y, in[j][1].z, in[j][1].w};
+      float v[16];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        v[2 * q] = bf16_lo(u[q]);
+        v[2 * q + 1] = bf16_hi(u[q]);
+      }
+      float m[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        m[q] = fmaxf(fmaxf(fabsf(v[q]), fabsf(v[q + 4])), fmaxf(fabsf(v[q + 8]), fabsf(v[q + 12])));
+      float amax = fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));  // the other half of the block
+      const int X = mx_scale_exp(amax);
+      const float sc = pow2_neg(X);
+      uint4 o;
+      o.x = pack_e4m3x4(v[0] * sc, v[1] * sc, v[2] * sc, v[3] * sc);
+      o.y = pack_e4m3x4(v[4] * sc, v[5] * sc, v[6] * sc, v[7] * sc);
+      o.z = pack_e4m3x4(v[8] * sc, v[9] * sc, v[10] * sc, v[11] * sc);
+      o.w = pack_e4m3x4(v[12] * sc, v[13] * sc, v[14] * sc, v[15] * sc);
+      *reinterpret_cast<uint4 *>(dst + i * step) = o;
+      // the row's four blocks: scale codes of lanes 0, 2, 4, 6 of its eight, one word
+      const uint32_t x0 = static_cast<uint32_t>(X + 127);
+      const uint32_t x1 = __shfl_down_sync(0xffffffffu, x0, 2);
+      const uint32_t x2 = __shfl_down_sync(0xffffffffu, x0, 4);
+      const uint32_t x3 = __shfl_down_sync(0xffffffffu, x0, 6);
+      if (sub == 0) {
+        const int wr = w0 + 4 * i + r4;  // the row within its atom
+        *reinterpret_cast<uint32_t *>(sf + base + (wr & 31) * 16 + (wr >> 5) * 4 - (w0 & 31) * 16 - (w0 >> 5) * 4) =
+            x0 | (x1 << 8) | (x2 << 16) | (x3 << 24);
+      }
+    }
+  }
+}
+
+template <int MODE, bool WQ>
+__global__ void __launch_bounds__(threads_of(MODE, WQ), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                         const __grid_constant__ CUtensorMap tmA1,
                         const __grid_constant__ CUtensorMap tmB0,
                         const __grid_constant__ CUtensorMap tmB1, const Params p) {
   using Tr = Traits<MODE>;
+  static_assert(!WQ || MODE == kFwdGateUp || MODE == kFwdDown, "weight codes come from the forward GEMMs");
   constexpr int STAGES = stages_of(MODE), HALVES = halves_of(MODE);
+  constexpr int NT = threads_of(MODE, WQ), EW = epi_warps(MODE, WQ);
   constexpr int kStageBytes = stage_bytes(MODE), kABytes = HALVES * kABox;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -224,7 +302,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
   uint8_t *stages = smem;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * kStageBytes);
   uint64_t *full = bars;                 // [STAGES] CTA 0 only: both CTAs' copies landed
-  uint64_t *empty = bars + STAGES;       // [STAGES] pair MMA done with the stage (both CTAs)
+  uint64_t *empty = bars + STAGES;       // [STAGES] pair MMA (and weight quantisers) done with the stage
   uint64_t *tfull = bars + 2 * STAGES;   // [2] accumulator ready (both CTAs)
   uint64_t *tempty = tfull + 2;          // [2] CTA 0 only: both CTAs' epilogues done
   uint64_t *drain = tempty + 2;          // abort path: MMA completion
@@ -241,7 +319,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
   const int E = p.E;
   const int rank = static_cast<int>(cluster_ctarank());  // 0: issues the pair's MMAs
   uint8_t *epi_tiles = smem + epi_off(MODE);  // [epilogue warp] 32 x 32 bf16 staging tiles
-  uint8_t *gu_ring = smem + gu_off(MODE);     // dA: [kGuSlots] G chunk | U chunk
+  uint8_t *gu_ring = smem + gu_off(MODE, WQ); // dA: [kGuSlots] G chunk | U chunk
   const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
@@ -251,7 +329,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 2 * epi_warps(MODE));  // one arrival per epilogue warp of both CTAs
+      mbar_init(&tempty[b], 2 * EW);  // one arrival per epilogue warp of both CTAs
     }
     mbar_init(drain, 1);
     for (int s = 0; s < kGuSlots; ++s) {
@@ -269,7 +347,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
   }
   if (warp == 1) tmem_alloc_pair(tmem_slot, kTmemCols);
   // no offsets: one segment of all M_rows rows (the router projection's logits and dx)
-  for (int e = threadIdx.x; e <= E; e += threads_of(MODE))
+  for (int e = threadIdx.x; e <= E; e += NT)
     s_off[e] = p.offsets ? __ldg(p.offsets + e) : (e == 0 ? 0 : p.M_rows);
   __syncthreads();
   bool skewed = false;
@@ -282,7 +360,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
     int cmax = 0;
     for (int f = 0; f < E; ++f) cmax = max(cmax, s_off[f + 1] - s_off[f]);
     skewed = static_cast<int64_t>(cmax) * E > 2 * static_cast<int64_t>(s_off[E] - s_off[0]);
-    for (int e = threadIdx.x; e < E; e += threads_of(MODE)) {
+    for (int e = threadIdx.x; e < E; e += NT) {
       const int c = s_off[e + 1] - s_off[e];
       int r = 0;
       for (int f = 0; f < E; ++f) {
@@ -444,14 +522,46 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
       }
     }
     __syncwarp();
-  } else if (warp < 2 + epi_warps(MODE)) {
+  } else if (warp < 2 + EW) {
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     // column range: warps 2..5 the first, 6..9 the second (a constant 0 with 4 warps)
-    const int part = epi_warps(MODE) == 8 ? (warp - 2) >> 2 : 0;
+    const int part = EW == 8 ? (warp - 2) >> 2 : 0;
     const int rit = BM * rank + q * 32 + lane;  // row within the pair's 256-row tile
     const uint32_t tempty0 = peer_smem_addr(&tempty[0], 0);
     const uint32_t tempty1 = peer_smem_addr(&tempty[1], 0);
+    // weight quantisation (WQ): the bf16 weight and its codes, [E * wq_rows, wq_ld]
+    const int wq_rows = MODE == kFwdGateUp ? p.H : p.I;  // K of the forward GEMM
+    const int wq_ld = MODE == kFwdGateUp ? p.I : p.H;
+    const SfLayout wq_L{wq_rows, kMxBN};
+    const uint16_t *wq_src = p.wsrc[MODE == kFwdGateUp ? rank : 0];
+    uint8_t *wq_codes = p.wq[MODE == kFwdGateUp ? rank : 0];
+    uint8_t *wq_sf = p.wq_sf[MODE == kFwdGateUp ? rank : 0];
+    // The weights for an MXFP8 backward (WQ): of tile i's K blocks (64 weight rows
+    // each), the ones of stage ks (128 of K) with ks % (the expert's row tiles)
+    // equal to the tile's index among them, so every weight element is quantised
+    // once, spread over the expert's tiles.  The epilogue warps share them
+    // round-robin in 32-row units and do tile i's after the epilogue of tile
+    // i - 1, while tile i's TMA copies bring the same rows into L2, so the
+    // weight is read from memory about once.
+    auto quant_tile = [&](int i) {
+      const int tile = tile_at(i);
+      if (tile >= total) return;
+      const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off, s_pad);
+      const int col0 = MODE == kFwdGateUp ? t.n0 : t.n0 + (BN / 2) * rank;
+      if (col0 >= wq_ld) return;
+      const int nmt = s_tp[t.e + 1] - s_tp[t.e], mtl = (t.m0 - s_off[t.e]) / (2 * BM);
+      int u = 0;
+      for (int ks = mtl; ks * HALVES < t.nkb; ks += nmt)
+        for (int kb = ks * HALVES; kb < (ks + 1) * HALVES && kb < t.nkb; ++kb)
+          for (int q = 0; q < 2; ++q, ++u)
+            if ((u + i) % EW == warp - 2)
+              quant_weight_rows<MODE == kFwdGateUp ? 4 : 8>(wq_src, t.e * wq_rows + kb * BK + 32 * q, col0,
+                                                            wq_ld, wq_codes, wq_sf, wq_L, lane);
+    };
+    constexpr int kAhead = 1;
+    if constexpr (WQ)
+      for (int i = 0; i < kAhead; ++i) quant_tile(i);
     int it = 0, gbase = 0;
     for (int tile = tile_at(0); tile < total; tile = tile_at(++it)) {
       const Tile t = decode_tile<MODE>(tile, p, s_tp, s_off, s_pad);
@@ -467,11 +577,12 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
                                                gu_full, gu_empty, gbase, abort_flag))
           break;
       } else {
-        epilogue_tile<MODE>(t, tb, rit, p, part, epi_warps(MODE) / 4, stile);
+        epilogue_tile<MODE>(t, tb, rit, p, part, EW / 4, stile);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(buf ? tempty1 : tempty0);
+      if constexpr (WQ) quant_tile(it + kAhead);  // a coming tile's, while its operands stream in
     }
   } else {
     // ------------------------------------------------------------ dA: G/U loader (both CTAs)
@@ -579,6 +690,10 @@ bool make_map_gu(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t rows)
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <int MODE, bool WQ>
+cudaError_t launch_kernel(const CUtensorMap &mA0, const CUtensorMap &mA1, const CUtensorMap &mB0,
+                          const CUtensorMap &mB1, const Params &p, int num_sms, cudaStream_t s);
+
 template <int MODE>
 cudaError_t launch_mode(const GemmArgs &a, cudaStream_t s) {
   CUtensorMap mA0, mA1, mB0, mB1;
@@ -685,6 +800,26 @@ cudaError_t launch_mode(const GemmArgs &a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     p.expert_maps = maps;
   }
+  if constexpr (MODE == kFwdGateUp || MODE == kFwdDown) {
+    p.wsrc[0] = MODE == kFwdGateUp ? a.W_gate : a.W_down;
+    p.wsrc[1] = MODE == kFwdGateUp ? a.W_up : nullptr;
+    p.wq[0] = a.wq[0];
+    p.wq[1] = a.wq[1];
+    p.wq_sf[0] = a.wq_sf[0];
+    p.wq_sf[1] = a.wq_sf[1];
+    if (a.wq[0]) {  // the variant with weight quantisers
+      if (!a.wq_sf[0] || (MODE == kFwdGateUp && (!a.wq[1] || !a.wq_sf[1]))) return cudaErrorInvalidValue;
+      return launch_kernel<MODE, true>(mA0, mA1, mB0, mB1, p, a.num_sms, s);
+    }
+  }
+  return launch_kernel<MODE, false>(mA0, mA1, mB0, mB1, p, a.num_sms, s);
+}
+
+// One launch of a grouped GEMM kernel: clusters of two CTAs, as many pairs as
+// fit at once (at most one per two SMs).
+template <int MODE, bool WQ>
+cudaError_t launch_kernel(const CUtensorMap &mA0, const CUtensorMap &mA1, const CUtensorMap &mB0,
+                          const CUtensorMap &mB1, const Params &p, int num_sms, cudaStream_t s) {
   // once per device: the shared-memory opt-in, and how many CTA pairs fit at once
   static DeviceOnce once;
   cudaLaunchConfig_t cfg = {};
@@ -693,30 +828,30 @@ cudaError_t launch_mode(const GemmArgs &a, cudaStream_t s) {
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(threads_of(MODE));
-  cfg.dynamicSmemBytes = smem_bytes(MODE);
+  cfg.blockDim = dim3(threads_of(MODE, WQ));
+  cfg.dynamicSmemBytes = smem_bytes(MODE, WQ);
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int pair_grid = 0;
   cudaError_t e = once.get(
       [&](int *grid) {
-        cudaError_t r = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(MODE));
+        cudaError_t r = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, WQ>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(MODE, WQ));
         if (r != cudaSuccess) return r;
         cudaLaunchConfig_t q = cfg;
-        q.gridDim = dim3(a.num_sms & ~1);
+        q.gridDim = dim3(num_sms & ~1);
         int clusters = 0;
-        r = cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_kernel<MODE>, &q);
+        r = cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_kernel<MODE, WQ>, &q);
         if (r != cudaSuccess) return r;
         if (clusters < 1) return cudaErrorInvalidConfiguration;
-        *grid = 2 * (clusters < a.num_sms / 2 ? clusters : a.num_sms / 2);
+        *grid = 2 * (clusters < num_sms / 2 ? clusters : num_sms / 2);
         return cudaSuccess;
       },
       &pair_grid);
   if (e != cudaSuccess) return e;
   cfg.gridDim = dim3(pair_grid);
-  e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE>, mA0, mA1, mB0, mB1, p);
+  e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE, WQ>, mA0, mA1, mB0, mB1, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

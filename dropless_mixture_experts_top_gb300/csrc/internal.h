@@ -113,6 +113,10 @@ struct GemmArgs {
   // token axis (codes [I, Mpad], scales in 128-row atoms over K = Mpad), or null
   uint8_t *aw_t, *aw_t_sf;
   int Mpad;
+  // forward GEMMs for an MXFP8 backward: the weights quantised along their last
+  // axis as they pass through the GEMM (gate/up: W_gate [0] and W_up [1] as
+  // [E*H, I]; down: W_down [0] as [E*I, H]; codes and scale atoms), or null
+  uint8_t *wq[2], *wq_sf[2];
   // router projection: x [T,H], W_r [H,E], d_logits as bf16 [T,E]; fp32 output, its columns
   const uint16_t *r_x, *r_w, *r_dlog;
   float *r_out;
@@ -143,11 +147,6 @@ inline size_t sf_layout_bytes(size_t rows, size_t K, SfLayout L) {
 }
 // pad_off[e] = sum over e' < e of ceil(count/128)*128
 cudaError_t launch_pad_offsets(const int32_t *offsets, int E, int32_t *pad_off, cudaStream_t s);
-// rows along K (K % 128 == 0): dense (offsets == nullptr, rows_out input rows) or
-// into the padded per-expert row space (rows_out = padded row capacity)
-cudaError_t launch_quant_rows(const uint16_t *src, int rows_out, int K, const int32_t *offsets,
-                              const int32_t *pad_off, int E, uint8_t *codes, uint8_t *sf, SfLayout L,
-                              cudaStream_t s);
 // along tokens: [M, C] permuted rows -> codes [C, Mpad] (padded token axis);
 // with rows.codes set, also along C into the padded row space: codes [Mpad, C]
 struct RowCodes {

@@ -42,54 +42,6 @@ __device__ __forceinline__ int expert_of(int o, const int *s_pad, int E) {
   return lo;
 }
 
-// One thread per (output row, 32-element block).  Rows are either the input
-// rows themselves (dense: weights) or the padded per-expert row space.
-__global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t *__restrict__ src, int K,
-                                                         int rows_out,
-                                                         const int32_t *__restrict__ offsets,
-                                                         const int32_t *__restrict__ pad_off, int E,
-                                                         uint8_t *__restrict__ codes,
-                                                         uint8_t *__restrict__ sf, SfLayout L) {
-  __shared__ int s_off[kMaxExperts + 1], s_pad[kMaxExperts + 1];
-  if (offsets) {
-    for (int e = threadIdx.x; e <= E; e += blockDim.x) {
-      s_off[e] = __ldg(offsets + e);
-      s_pad[e] = __ldg(pad_off + e);
-    }
-    __syncthreads();
-  }
-  const int nb = K >> 5;
-  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (idx >= static_cast<int64_t>(rows_out) * nb) return;
-  const int o = static_cast<int>(idx / nb), b = static_cast<int>(idx % nb);
-  if (offsets && o >= s_pad[E]) return;  // past the padded total: never read
-  int in_row = o;
-  if (offsets) {
-    const int e = expert_of(o, s_pad, E);
-    const int local = o - s_pad[e];
-    in_row = local < s_off[e + 1] - s_off[e] ? s_off[e] + local : -1;
-  }
-  float v[32];
-  if (in_row >= 0) {
-    const uint4 *s4 = reinterpret_cast<const uint4 *>(src + static_cast<size_t>(in_row) * K + 32 * b);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint4 w = __ldg(s4 + q);
-      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        v[8 * q + 2 * h] = bf16_lo(ww[h]);
-        v[8 * q + 2 * h + 1] = bf16_hi(ww[h]);
-      }
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = 0.f;
-  }
-  sf[atom_byte(o, b, K, L)] =
-      quant32(v, reinterpret_cast<uint4 *>(codes + static_cast<size_t>(o) * K + 32 * b));
-}
-
 // Token-axis quantisation, output transposed: codes [C][Mpad] (tokens
 // contiguous).  A block takes 128 padded rows (one expert's, as segments are
 // 128-aligned) and walks their columns in 64-wide tiles.  The tiles are staged
@@ -416,15 +368,6 @@ __global__ void __launch_bounds__(32) pad_offsets_kernel(const int32_t *__restri
 
 cudaError_t launch_pad_offsets(const int32_t *offsets, int E, int32_t *pad_off, cudaStream_t s) {
   pad_offsets_kernel<<<1, 32, 0, s>>>(offsets, E, pad_off);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_quant_rows(const uint16_t *src, int rows_out, int K, const int32_t *offsets,
-                              const int32_t *pad_off, int E, uint8_t *codes, uint8_t *sf, SfLayout L,
-                              cudaStream_t s) {
-  const int64_t n = static_cast<int64_t>(rows_out) * (K / 32);
-  quant_rows_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(src, K, rows_out, offsets,
-                                                                            pad_off, E, codes, sf, L);
   return cudaGetLastError();
 }
 

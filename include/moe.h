@@ -124,8 +124,9 @@ typedef struct {
 } moe_saved_layout;
 moe_status moe_saved_offsets(const moe_config *cfg, moe_saved_layout *layout);
 
-/* MOE_PREC_FP8_BWD and MOE_PREC_MXFP8: byte offsets, inside moe_backward's scratch, of the
- * MXFP8 operands it writes, for inspection after the call.  m_pad is the padded
+/* MOE_PREC_FP8_BWD and MOE_PREC_MXFP8: byte offsets of the backward GEMMs' MXFP8
+ * operands, for inspection after the call: inside moe_backward's scratch, except
+ * the ones the forward writes (inside `saved`, listed below).  m_pad is the padded
  * token capacity (a multiple of 128): expert e's rows start at padded row
  * pad_offsets[e] = sum over e' < e of ceil(count/128)*128 (int32 [E+1]); rows
  * past an expert's count are zero codes with zero scale codes; padded rows at
@@ -133,9 +134,13 @@ moe_status moe_saved_offsets(const moe_config *cfg, moe_saved_layout *layout);
  *   *_q     E4M3 codes, K-major: dy_q [m_pad,H] (padded rows), wd_q [E*I,H],
  *           dg_q/du_q [m_pad,I], wg_q/wu_q [E*H,I];
  *   *_t     token-axis operands transposed, tokens contiguous: aw_t (w*A) and
- *           dg_t/du_t [I,m_pad], dy_t and x_t [H,m_pad]; aw_t and aw_t_sf are
- *           offsets inside `saved`, not the scratch: the forward's gate/up
- *           epilogue writes them (moe_forward and moe_forward_recompute);
+ *           dg_t/du_t [I,m_pad], dy_t and x_t [H,m_pad];
+ *   written by the forward (moe_forward and moe_forward_recompute), so their
+ *   offsets are inside `saved`, not the scratch: aw_t (the gate/up epilogue) and
+ *   the weights' wd_q, wg_q, wu_q with their scales (in MOE_PREC_FP8_BWD the two
+ *   bf16 GEMMs quantise each weight tile as it passes through them, so only the
+ *   experts that received rows are written -- no backward GEMM reads the others;
+ *   in MOE_PREC_MXFP8 the forward's weight passes write every expert);
  *   *_sf    their UE8M0 scale codes (2^(code-127)), one per 32 elements along
  *           K, in 512-byte atoms of 128 rows x 128 K, the order the tensor core
  *           reads them: row w of atom row-block rb, K-block b, sits at byte
@@ -167,8 +172,8 @@ moe_status moe_fp8_scratch_offsets(const moe_config *cfg, moe_fp8_layout *layout
  *   wdt_q [E*H,I]    W_down along I, transposed: row e*H + h holds W_down[e][:, h]
  *                    (N side, segments of H rows).
  * The same passes over the weights also write the backward GEMMs' weight
- * operands, which in this mode live in `saved` (moe_backward does not quantise
- * the weights again; moe_fp8_scratch_offsets reports 0 for them):
+ * operands, which live in `saved` (moe_backward does not quantise the weights
+ * again; moe_fp8_scratch_offsets reports the same offsets):
  *   bwd_wd_q [E*I,H], bwd_wg_q and bwd_wu_q [E*H,I] and their scales, laid
  *   out as moe_fp8_layout's wd_q, wg_q, wu_q (offsets inside `saved`).
  * Returns MOE_ERR_INVALID_ARG for other precisions or unsupported shapes. */

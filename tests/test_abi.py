@@ -132,9 +132,8 @@ def test_fp8_shapes_and_layout(L):
     moe_shape = MoEShape(T=300, H=H, I=I, E=E, k=2)
     Mp = q["m_pad"]
     assert Mp % 128 == 0 and Mp >= M + 127 * E
-    sizes = {"pad_offsets": 4 * (E + 1), "dy_q": Mp * H, "wd_q": E * I * H, "dg_q": Mp * I, "du_q": Mp * I,
-             "wg_q": E * H * I, "wu_q": E * H * I, "dy_t": H * Mp, "x_t": H * Mp,
-             "dg_t": I * Mp, "du_t": I * Mp}
+    sizes = {"pad_offsets": 4 * (E + 1), "dy_q": Mp * H, "dg_q": Mp * I, "du_q": Mp * I,
+             "dy_t": H * Mp, "x_t": H * Mp, "dg_t": I * Mp, "du_t": I * Mp}
     for n in list(sizes):
         if n != "pad_offsets":
             R, K = {"dy_q": (Mp, H), "wd_q": (E * I, H), "dg_q": (Mp, I), "du_q": (Mp, I), "wg_q": (E * H, I),
@@ -154,11 +153,19 @@ def test_fp8_shapes_and_layout(L):
     # quantised)
     assert spans[0][0] >= 256 + M * H * 2 + M * 4 * 4 and spans[-1][1] <= bs
     assert bs < bs16 + sum(sizes.values()) + 256 * len(sizes)
-    # w * A along tokens lives in `saved` (the forward writes it), after the bf16 activations
+    # w * A along tokens and the weights' codes live in `saved` (the forward writes them),
+    # after the bf16 activations
     _, sv, _, _ = moe.query_workspace(c)
     so = moe.saved_offsets(c)
-    assert q["aw_t"] >= so["A_w"] + M * I * 2 and q["aw_t_sf"] >= q["aw_t"] + I * Mp
-    assert q["aw_t_sf"] + moe.sf_layout_bytes(I, Mp, I, 128) <= sv
+    ssz = {"aw_t": I * Mp, "aw_t_sf": moe.sf_layout_bytes(I, Mp, I, 128),
+           "wd_q": E * I * H, "wg_q": E * H * I, "wu_q": E * H * I}
+    for n, (R, K, seg) in {"wd_q": (E * I, H, I), "wg_q": (E * H, I, H), "wu_q": (E * H, I, H)}.items():
+        ssz[n[:-2] + "_sf"] = moe.sf_layout_bytes(R, K, seg, moe.MX_BN)
+    sspans = sorted((q[n], q[n] + b, n) for n, b in ssz.items())
+    for (a0, a1, n0), (b0, b1, n1) in zip(sspans, sspans[1:]):
+        assert a1 <= b0, (n0, n1)
+    assert all(q[n] % 256 == 0 for n in ssz)
+    assert sspans[0][0] >= so["A_w"] + M * I * 2 and sspans[-1][1] <= sv
 
 
 def test_router_workspace_and_shapes(L):
@@ -214,8 +221,8 @@ def test_mxfp8_shapes_and_forward_layout(L):
     for (a0, a1, n0), (b0, b1, n1) in zip(wspans, wspans[1:]):
         assert a1 <= b0, (n0, n1)
     assert wspans[0][0] >= so["A_w"] + M * I * 2 and wspans[-1][1] <= sv
-    # the rest of the backward is fp8_bwd's; its scratch holds no weight codes in this mode
+    # the backward is fp8_bwd's, reading the same weight codes from `saved`
     q = moe.fp8_scratch_offsets(c)
-    assert all(q[n] == 0 for n in ("wd_q", "wd_sf", "wg_q", "wg_sf", "wu_q", "wu_sf"))
+    assert all(q[n] == f["bwd_" + n] for n in ("wd_q", "wd_sf", "wg_q", "wg_sf", "wu_q", "wu_sf"))
     c1 = cfg(T=T, H=H, I=I, E=E, k=k, prec=1)
-    assert bs < moe.query_workspace(c1)[3]
+    assert bs == moe.query_workspace(c1)[3]

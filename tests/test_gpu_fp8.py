@@ -1,8 +1,9 @@
 """The fp8_bwd backward (MXFP8 grouped GEMMs) through the C ABI against the
 oracle's quantised backward.
 
-Quantisers: the MXFP8 codes and scales the backward leaves in its scratch for
-operands that come straight from the seeded inputs (weights, dy, x) must equal
+Quantisers: the MXFP8 codes and scales of the operands that come straight
+from the seeded inputs (the weights, which the forward's bf16 GEMMs quantise as
+they pass through them, and dy and x, which the backward quantises) must equal
 the oracle quantiser's bit for bit, in the padded per-expert row space and the
 scale-atom order the tensor core reads.  Gradients: every element on small
 shapes (several tiles, ragged experts, half-filled 256-row operand boxes, empty
@@ -24,6 +25,26 @@ pytestmark = pytest.mark.gpu
 def _build():
     from dropless_mixture_experts_top_gb300 import _build as B
     B.build()
+
+
+def check_weight_codes(layer, inp, counts):
+    """The weights quantised along each backward GEMM's K by the forward GEMMs that
+    read them: every expert with rows (an empty expert's weights pass through no
+    GEMM, and no backward GEMM reads them)."""
+    s = layer.shape
+    E, H, I = s.E, s.H, s.I
+    Mp = moe.fp8_scratch_offsets(layer.cfg)["m_pad"]
+    for name, W, R, K in (("wd", inp["W_down"], E * I, H), ("wg", inp["W_gate"], E * H, I),
+                          ("wu", inp["W_up"], E * H, I)):
+        codes, sc, _ = O.mx_quantize_rows(W.reshape(R, K))
+        got = layer.fp8_tensor(name + "_q").cpu().numpy()
+        seg, group = moe.sf_grouping(name + "_q", s, Mp)
+        got_sc = atoms_to_scales(layer.fp8_tensor(name + "_sf").cpu().numpy(), R, K, seg, group)
+        rows = R // E
+        for e in np.nonzero(counts)[0]:
+            sl = slice(e * rows, (e + 1) * rows)
+            np.testing.assert_array_equal(got[sl], codes[sl], err_msg=f"{name} expert {e}")
+            np.testing.assert_array_equal(got_sc[sl], sc[sl], err_msg=f"{name}_sf expert {e}")
 
 
 def check_token_axis(layer, name, src_rows, offsets, pad, Mp):
@@ -59,15 +80,7 @@ def test_quantised_operands_bit_exact():
     Mp = lay["m_pad"]
     pad = np.concatenate([[0], np.cumsum((counts + 127) // 128 * 128)]).astype(np.int32)
     np.testing.assert_array_equal(layer.fp8_tensor("pad_offsets").cpu().numpy(), pad)
-    # weights, quantised along each backward GEMM's K
-    for name, W, R, K in (("wd", inp["W_down"], E * I, H), ("wg", inp["W_gate"], E * H, I),
-                          ("wu", inp["W_up"], E * H, I)):
-        codes, sc, _ = O.mx_quantize_rows(W.reshape(R, K))
-        np.testing.assert_array_equal(layer.fp8_tensor(name + "_q").cpu().numpy(), codes, err_msg=name)
-        seg, group = moe.sf_grouping(name + "_q", shape, Mp)
-        np.testing.assert_array_equal(
-            atoms_to_scales(layer.fp8_tensor(name + "_sf").cpu().numpy(), R, K, seg, group), sc,
-            err_msg=name + "_sf")
+    check_weight_codes(layer, inp, counts)
     # dy in the padded row space (dA's A operand), along H
     dy_perm = inp["dy"][sor // k]
     codes, sc, _ = O.mx_quantize_rows(dy_perm)
@@ -87,6 +100,9 @@ FP8_SHAPES = [
     ("wide", MoEShape(T=300, H=640, I=256, E=16, k=4)),
     ("single_expert", MoEShape(T=333, H=128, I=256, E=1, k=1)),
     ("E256_k16_max", MoEShape(T=300, H=256, I=128, E=256, k=16)),  # padded row space ~8x the rows
+    # one expert of four 256-row tiles, six stages per tile in both forward GEMMs: each
+    # tile's weight quantisers read one or two of its stages and pass over the rest
+    ("deep_k_row_tiles", MoEShape(T=1024, H=768, I=768, E=1, k=1)),
 ]
 
 
@@ -96,6 +112,7 @@ def test_fp8_layer_matches_quantised_oracle(name, shape):
     layer, out, grads = G.run_layer(shape, inp, precision="fp8_bwd")
     assert layer.status() == {"route": 0, "forward": 0, "backward": 0}
     idx, w = G.check_full(shape, inp, layer, out, grads, precision="fp8_bwd")
+    check_weight_codes(layer, inp, layer.routing["counts"].cpu().numpy())
     # the result follows the quantised semantics, not the exact ones
     dx_exact, _, _ = O.backward_tokens(shape, inp["x"], inp["logits"], idx, w, inp["W_gate"], inp["W_up"],
                                        inp["W_down"], inp["dy"])
@@ -143,6 +160,8 @@ def test_quantiser_sweeps_every_bf16_value():
     W_down = vals.reshape(E, I, H)
     inp = synth.make_inputs_shape(shape, 63)
     inp["W_down"] = W_down
+    inp["logits"][0::2, 0] += 50.0  # both experts receive tokens, so GEMM2 passes every weight row
+    inp["logits"][1::2, 1] += 50.0
     layer, out, grads = G.run_layer(shape, inp, precision="fp8_bwd")  # outputs may overflow: not compared
     codes, sc, _ = O.mx_quantize_rows(W_down.reshape(E * I, H))
     Mp = moe.fp8_scratch_offsets(layer.cfg)["m_pad"]
