@@ -82,6 +82,8 @@ def kernel_work(shape):
         # gradient, codes and scales written along H and along tokens, g in partials
         "mx_dy_quant_gdot": ("hbm", T * H * 2 + M * H * 2 + 2 * M * H * (1 + 1 / 32) + M * 4 * 4.0, "B"),
         "mx_quantT_x": q(M * H),
+        # fp8_bwd forward: x gathered into x_perm (bf16) and quantised along tokens, one pass
+        "permute_rows_quantT_x": ("hbm", T * H * 2 + M * H * 2.0 + M * H * (1 + 1 / 32) + M * 4, "B"),
         "mx_gemm_dA_dswiglu": ("tensor_fp8", 2 * MHI, "flop"),
         "mx_gemm_dX": ("tensor_fp8", 4 * MHI, "flop"),
         "mx_gemm_dW_down": ("tensor_fp8", 2 * MHI, "flop"),

@@ -38,8 +38,8 @@ struct Layout {
   size_t r_tickets, r_lrank, r_hist, r_gpref, r_zero, r_total;
   // saved
   size_t s_xperm, s_G, s_U, s_A, s_Y, s_Aw, s_total;
-  // forward scratch
-  size_t f_total;
+  // forward scratch (f_pad: fp8_bwd's padded expert offsets)
+  size_t f_pad, f_total;
   // backward scratch
   size_t b_dyp, b_dG, b_dU, b_dX, b_maps, b_gpart, b_total;
   // fp8_bwd and mxfp8: quantised operands inside the backward scratch (zero otherwise)
@@ -129,6 +129,9 @@ Layout layout_of(const moe_config *c) {
     q.wg_sf = take(sf_layout_bytes(E * H, I, sf_b(H)));
     q.wu_q = take(E * H * I);
     q.wu_sf = take(sf_layout_bytes(E * H, I, sf_b(H)));
+    // x along tokens (dW_gate/up's A operand), gathered from x by the forward
+    q.x_t = take(H * L.q.m_pad);
+    q.x_t_sf = take(H * L.q.m_pad / 32);
     if (c->precision == MOE_PREC_MXFP8) {
       moe_mxfp8_fwd_layout &f = L.fq;
       f.bwd_wd_q = q.wd_q;
@@ -141,6 +144,10 @@ Layout layout_of(const moe_config *c) {
   }
   L.s_total = o > 0 ? o : 256;
   o = kHeader;
+  if (c->precision == MOE_PREC_FP8_BWD) {
+    L.f_pad = o;
+    o += align256((E + 1) * 4);
+  }
   if (c->precision == MOE_PREC_MXFP8) {
     const size_t Mp = fp8_mpad(M, E);
     moe_mxfp8_fwd_layout &f = L.fq;
@@ -198,8 +205,6 @@ Layout layout_of(const moe_config *c) {
     q.du_sf = take(Mp * I / 32);
     q.dy_t = take(H * Mp);
     q.dy_t_sf = take(sf_layout_bytes(H, Mp, sf_b(H)));
-    q.x_t = take(H * Mp);
-    q.x_t_sf = take(H * Mp / 32);
     q.dg_t = take(I * Mp);
     q.dg_t_sf = take(sf_layout_bytes(I, Mp, sf_b(I)));
     q.du_t = take(I * Mp);
@@ -307,6 +312,7 @@ struct Fp8Bwd {
   int32_t *status;
   const uint16_t *x, *G, *U, *Y, *dy;
   const uint8_t *aw_t, *aw_t_sf;  // w * A along tokens, from the forward (in `saved`)
+  const uint8_t *x_t, *x_t_sf;    // x along tokens, from the forward (in `saved`)
   uint16_t *dX, *dx, *dW_gate, *dW_up, *dW_down;
   float *g_part, *d_logits, *d_topk_w;
   // the weights' codes for the three GEMMs that read them, written by the
@@ -390,13 +396,10 @@ moe_status backward_fp8(const Fp8Bwd &f, cudaStream_t s) {
   m.a1 = m.b1 = m.sfa1 = m.sfb1 = nullptr;
   m.o0 = f.dW_down;
   MOE_TRY(timed("mx_gemm_dW_down", s, [&] { return launch_mx_gemm(kMxGemmDWDown, m, s); }));
-  // dW_gate = Q(x)^T . Q(dG), dW_up = Q(x)^T . Q(dU), K = the expert's tokens
-  MOE_TRY(timed("mx_quantT_x", s, [&] {  // gathered from x by token, not re-read from x_perm
-    return launch_quant_cols(f.x, H, Mp, off, pad_off, E, sc + q.x_t, sc + q.x_t_sf, sf_a(H), RowCodes{}, s,
-                             f.r->slot_of_row, k);
-  }));
-  m.a0 = sc + q.x_t;
-  m.sfa0 = sc + q.x_t_sf;
+  // dW_gate = Q(x)^T . Q(dG), dW_up = Q(x)^T . Q(dU), K = the expert's tokens;
+  // Q(x) along tokens comes from the forward
+  m.a0 = f.x_t;
+  m.sfa0 = f.x_t_sf;
   m.b0 = sc + q.dg_t;
   m.sfb0 = sc + q.dg_t_sf;
   m.b1 = sc + q.du_t;
@@ -423,6 +426,7 @@ struct Mx8Fwd {
   uint16_t *x_perm, *A, *G, *U, *A_w, *Y;
   uint8_t *saved;  // the backward's weight codes go here
   uint8_t *aw_t, *aw_t_sf;  // and w * A along tokens
+  uint8_t *x_t, *x_t_sf;    // and x along tokens
   bool keep;       // write what the backward reads (the bf16 activations, the weight codes)
 };
 
@@ -441,6 +445,11 @@ moe_status forward_mx(const Mx8Fwd &f, cudaStream_t s) {
   MOE_TRY(timed("mx_zero_pad_rows", s, [&] {
     return launch_zero_pad_rows(off, pad_off, E, H, sc + q.x_q, sc + q.x_sf, sf_a(Mp), s);
   }));
+  if (f.keep)  // the backward's dW_gate/up operand: x along tokens, gathered from x by token
+    MOE_TRY(timed("mx_quantT_x", s, [&] {
+      return launch_quant_cols(f.x, H, Mp, off, pad_off, E, f.x_t, f.x_t_sf, sf_a(H), RowCodes{}, s,
+                               f.r->slot_of_row, k);
+    }));
   // each weight read once: along H for GEMM1 (transposed, interleaved) and
   // along I for the backward's dX (row by row, into `saved`)
   MOE_TRY(timed("mx_quant_W_gateup_fwd", s, [&] {
@@ -556,12 +565,28 @@ moe_status forward_impl(FwdKind kind, const moe_config *cfg, const void *x, cons
     f.saved = sv;
     f.aw_t = sv + L.q.aw_t;
     f.aw_t_sf = sv + L.q.aw_t_sf;
+    f.x_t = sv + L.q.x_t;
+    f.x_t_sf = sv + L.q.x_t_sf;
     f.keep = kind != kFwdNoSave;
     MOE_TRY(forward_mx(f, s));
   } else {
-    MOE_TRY(timed("permute_rows", s, [&] {
-      return launch_permute_rows(static_cast<const uint16_t *>(x), r->row_of_slot, x_perm, T, H, k, s);
-    }));
+    const bool keep = kind != kFwdNoSave;  // G, U and w * A are only the backward's
+    const bool fp8b = cfg->precision == MOE_PREC_FP8_BWD;  // its dW_down reads w * A quantised along tokens
+    if (keep && fp8b) {
+      // the permute in destination order, fused with x quantised along tokens
+      // (dW_gate/up's A operand in the MXFP8 backward) into the padded token axis
+      int32_t *pad_off = reinterpret_cast<int32_t *>(sc + L.f_pad);
+      MOE_TRY(timed("mx_pad_offsets_fwd", s, [&] { return launch_pad_offsets(r->offsets, cfg->E, pad_off, s); }));
+      MOE_TRY(timed("permute_rows_quantT_x", s, [&] {
+        return launch_quant_cols(static_cast<const uint16_t *>(x), H, static_cast<int>(L.q.m_pad), r->offsets,
+                                 pad_off, cfg->E, sv + L.q.x_t, sv + L.q.x_t_sf, sf_a(H), RowCodes{}, s,
+                                 r->slot_of_row, k, x_perm);
+      }));
+    } else {
+      MOE_TRY(timed("permute_rows", s, [&] {
+        return launch_permute_rows(static_cast<const uint16_t *>(x), r->row_of_slot, x_perm, T, H, k, s);
+      }));
+    }
     GemmArgs g = gemm_base(cfg, r, di.sms, status);
     g.x_perm = x_perm;
     g.W_gate = static_cast<const uint16_t *>(W_gate);
@@ -569,8 +594,6 @@ moe_status forward_impl(FwdKind kind, const moe_config *cfg, const void *x, cons
     g.W_down = static_cast<const uint16_t *>(W_down);
     g.w_row = r->w_row;
     g.o0 = A;
-    const bool keep = kind != kFwdNoSave;  // G, U and w * A are only the backward's
-    const bool fp8b = cfg->precision == MOE_PREC_FP8_BWD;  // its dW_down reads w * A quantised along tokens
     g.o1 = keep ? G : nullptr;
     g.o2 = keep ? U : nullptr;
     g.o3 = keep && !fp8b ? A_w : nullptr;
@@ -765,6 +788,8 @@ moe_status moe_backward(const moe_config *cfg, const void *dy, const void *x,
     f.U = U;
     f.aw_t = sv + L.q.aw_t;
     f.aw_t_sf = sv + L.q.aw_t_sf;
+    f.x_t = sv + L.q.x_t;
+    f.x_t_sf = sv + L.q.x_t_sf;
     f.Y = Y;
     f.dy = static_cast<const uint16_t *>(dy);
     f.g_part = g_part;

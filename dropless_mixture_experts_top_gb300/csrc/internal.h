@@ -147,17 +147,20 @@ inline size_t sf_layout_bytes(size_t rows, size_t K, SfLayout L) {
 }
 // pad_off[e] = sum over e' < e of ceil(count/128)*128
 cudaError_t launch_pad_offsets(const int32_t *offsets, int E, int32_t *pad_off, cudaStream_t s);
-// along tokens: [M, C] permuted rows -> codes [C, Mpad] (padded token axis);
-// with rows.codes set, also along C into the padded row space: codes [Mpad, C]
+// along tokens: [M, C] permuted rows -> codes [C, Mpad] (padded token axis; or
+// none, codes == nullptr); with rows.codes set, also along C into the padded
+// row space: codes [Mpad, C]
 struct RowCodes {
   uint8_t *codes, *sf;
   SfLayout L;
 };
 // With slot_of_row set, src is token-major ([T, C]) and permuted row r reads
-// token slot_of_row[r] / k.
+// token slot_of_row[r] / k; with xp set, the permuted rows are also written in
+// bf16 to xp [M, C] (a permute fused with the quantisation).
 cudaError_t launch_quant_cols(const uint16_t *src, int C, int Mpad, const int32_t *offsets,
                               const int32_t *pad_off, int E, uint8_t *codes, uint8_t *sf, SfLayout L,
-                              RowCodes rows, cudaStream_t s, const int32_t *slot_of_row = nullptr, int k = 1);
+                              RowCodes rows, cudaStream_t s, const int32_t *slot_of_row = nullptr, int k = 1,
+                              uint16_t *xp = nullptr);
 
 // The MXFP8 backward's one pass over dy: dy rows gathered by token for every
 // permuted row, quantised along H into the padded row space (rows) and along

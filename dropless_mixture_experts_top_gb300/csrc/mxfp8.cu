@@ -52,9 +52,10 @@ __device__ __forceinline__ int expert_of(int o, const int *s_pad, int E) {
 // bytes against bank conflicts), which leaves as full 128-byte rows.
 // Optionally the same tile is also quantised along its rows (one thread per
 // (row, 32-column block)) into the padded row space, so an operand needed on
-// both axes is read once; and the rows may be gathered from a token-major
-// source (permuted row r reads token slot_of_row[r] / k) instead of read from
-// a permuted copy.  Tiles past the padded total are skipped.
+// both axes is read once; the rows may be gathered from a token-major source
+// (permuted row r reads token slot_of_row[r] / k) instead of read from a
+// permuted copy, and the gathered rows may be written out in bf16 as well (the
+// permuted copy itself, xp).  Tiles past the padded total are skipped.
 constexpr int kQcRows = 128, kQcCols = 64, kQcThreads = 256;
 constexpr int kQcRing = 4;                         // staged tiles in flight per block
 constexpr int kQcTileElems = kQcRows * kQcCols;   // bf16 per staged tile (16 KB)
@@ -144,7 +145,8 @@ __global__ void __launch_bounds__(kQcThreads, 3) quant_cols_kernel(const uint16_
                                                                 uint8_t *__restrict__ codes,
                                                                 uint8_t *__restrict__ sf, SfLayout L,
                                                                 RowCodes rows,
-                                                                const int32_t *__restrict__ slot_of_row, int k) {
+                                                                const int32_t *__restrict__ slot_of_row, int k,
+                                                                uint16_t *__restrict__ xp) {
   extern __shared__ __align__(16) uint8_t qc_smem[];
   uint16_t *ring = reinterpret_cast<uint16_t *>(qc_smem);
   uint8_t *otile = qc_smem + kQcRing * kQcTileElems * 2;
@@ -176,6 +178,16 @@ __global__ void __launch_bounds__(kQcThreads, 3) quant_cols_kernel(const uint16_
     return r < nvalid ? src + static_cast<size_t>(s_src[r]) * C : nullptr;
   };
   qc_walk(ring, blockIdx.y * kQcCols, gridDim.y * kQcCols, C, row_ptr, [&](const uint16_t *tile, int c0) {
+    if (xp) {  // the staged rows in bf16: 16-byte pieces, 128 bytes per row
+#pragma unroll
+      for (int j = 0; j < kQcLoads; ++j) {
+        const int i = threadIdx.x + j * kQcThreads;
+        const int r = i >> 3, part = i & 7;
+        if (r < nvalid)
+          *reinterpret_cast<uint4 *>(xp + static_cast<size_t>(row0 + r) * C + c0 + part * 8) =
+              *reinterpret_cast<const uint4 *>(tile + r * kQcCols + ((part ^ (r & 7)) << 3));
+      }
+    }
     if (rows.codes) {  // along the rows: thread = (row, 32-column block); zero rows past the count
       const int r = threadIdx.x >> 1, bb = threadIdx.x & 1;
       float v[32];
@@ -184,18 +196,20 @@ __global__ void __launch_bounds__(kQcThreads, 3) quant_cols_kernel(const uint16_
       rows.sf[atom_byte(prow, kb, C, rows.L)] =
           quant32(v, reinterpret_cast<uint4 *>(rows.codes + static_cast<size_t>(prow) * C + c0 + 32 * bb));
     }
-    const int cc = threadIdx.x % kQcCols, b = threadIdx.x / kQcCols;  // 4 blocks of 32 tokens
-    float v[32];
-    qc_col32(tile, cc, b, v);
-    sf[atom_byte(c0 + cc, (prow0 >> 5) + b, Mpad, L)] =
-        quant32(v, reinterpret_cast<uint4 *>(otile + cc * kQcOutStride + 32 * b));
-    __syncthreads();
+    if (codes) {  // along the tokens, transposed
+      const int cc = threadIdx.x % kQcCols, b = threadIdx.x / kQcCols;  // 4 blocks of 32 tokens
+      float v[32];
+      qc_col32(tile, cc, b, v);
+      sf[atom_byte(c0 + cc, (prow0 >> 5) + b, Mpad, L)] =
+          quant32(v, reinterpret_cast<uint4 *>(otile + cc * kQcOutStride + 32 * b));
+      __syncthreads();
 #pragma unroll
-    for (int j = 0; j < (kQcCols * kQcRows / 16) / kQcThreads; ++j) {
-      const int i = threadIdx.x + j * kQcThreads;
-      const int r = i >> 3, part = i & 7;  // output row (column c0 + r), 16-byte piece
-      *reinterpret_cast<uint4 *>(codes + static_cast<size_t>(c0 + r) * Mpad + prow0 + part * 16) =
-          *reinterpret_cast<const uint4 *>(otile + r * kQcOutStride + part * 16);
+      for (int j = 0; j < (kQcCols * kQcRows / 16) / kQcThreads; ++j) {
+        const int i = threadIdx.x + j * kQcThreads;
+        const int r = i >> 3, part = i & 7;  // output row (column c0 + r), 16-byte piece
+        *reinterpret_cast<uint4 *>(codes + static_cast<size_t>(c0 + r) * Mpad + prow0 + part * 16) =
+            *reinterpret_cast<const uint4 *>(otile + r * kQcOutStride + part * 16);
+      }
     }
   });
 }
@@ -373,7 +387,7 @@ cudaError_t launch_pad_offsets(const int32_t *offsets, int E, int32_t *pad_off, 
 
 cudaError_t launch_quant_cols(const uint16_t *src, int C, int Mpad, const int32_t *offsets,
                               const int32_t *pad_off, int E, uint8_t *codes, uint8_t *sf, SfLayout L,
-                              RowCodes rows, cudaStream_t s, const int32_t *slot_of_row, int k) {
+                              RowCodes rows, cudaStream_t s, const int32_t *slot_of_row, int k, uint16_t *xp) {
   const int col_blocks = C / kQcCols < 4 ? C / kQcCols : 4;  // each loops over C / (64 * 4) column tiles
   const dim3 grid(static_cast<unsigned>(Mpad / kQcRows), static_cast<unsigned>(col_blocks));
   static DeviceOnce once;  // dynamic shared memory above 48 KB, opted in once per device
@@ -382,7 +396,7 @@ cudaError_t launch_quant_cols(const uint16_t *src, int C, int Mpad, const int32_
   });
   if (e != cudaSuccess) return e;
   quant_cols_kernel<<<grid, kQcThreads, kQcSmem, s>>>(src, C, Mpad, offsets, pad_off, E, codes, sf, L, rows,
-                                                       slot_of_row, k);
+                                                       slot_of_row, k, xp);
   return cudaGetLastError();
 }
 

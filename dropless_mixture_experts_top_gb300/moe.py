@@ -347,8 +347,8 @@ class MoELayer:
 
     def fp8_tensor(self, name):
         """A quantised operand left in the backward scratch (the fp8 modes), or for
-        aw_t (w * A along tokens) and the weights' wd_q, wg_q, wu_q (all written by
-        the forward) in `saved`: uint8 codes [rows, K] for *_q and *_t, the raw
+        aw_t (w * A along tokens), x_t (x along tokens) and the weights' wd_q, wg_q,
+        wu_q (all written by the forward) in `saved`: uint8 codes [rows, K] for *_q and *_t, the raw
         scale-atom bytes for *_sf, int32 [E+1] for pad_offsets."""
         lay = fp8_scratch_offsets(self.cfg)
         s = self.shape
@@ -357,7 +357,7 @@ class MoELayer:
                   "wg_q": (s.E * s.H, s.I), "wu_q": (s.E * s.H, s.I), "aw_t": (s.I, Mp),
                   "dy_t": (s.H, Mp), "x_t": (s.H, Mp), "dg_t": (s.I, Mp), "du_t": (s.I, Mp)}
         off = lay[name]
-        in_saved = name.startswith(("aw_t", "wd_", "wg_", "wu_"))  # written by the forward
+        in_saved = name.startswith(("aw_t", "x_t", "wd_", "wg_", "wu_"))  # written by the forward
         buf = self.saved if in_saved else self.bwd_scratch
         if name == "pad_offsets":
             return buf[off:off + 4 * (s.E + 1)].view(torch.int32)

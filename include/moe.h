@@ -136,11 +136,13 @@ moe_status moe_saved_offsets(const moe_config *cfg, moe_saved_layout *layout);
  *   *_t     token-axis operands transposed, tokens contiguous: aw_t (w*A) and
  *           dg_t/du_t [I,m_pad], dy_t and x_t [H,m_pad];
  *   written by the forward (moe_forward and moe_forward_recompute), so their
- *   offsets are inside `saved`, not the scratch: aw_t (the gate/up epilogue) and
- *   the weights' wd_q, wg_q, wu_q with their scales (in MOE_PREC_FP8_BWD the two
- *   bf16 GEMMs quantise each weight tile as it passes through them, so only the
- *   experts that received rows are written -- no backward GEMM reads the others;
- *   in MOE_PREC_MXFP8 the forward's weight passes write every expert);
+ *   offsets are inside `saved`, not the scratch: aw_t (the gate/up epilogue), x_t
+ *   (in MOE_PREC_FP8_BWD by the forward's permute, which gathers x into x_perm
+ *   and quantises it along tokens in one pass) and the weights' wd_q, wg_q, wu_q
+ *   with their scales (in MOE_PREC_FP8_BWD the two bf16 GEMMs quantise each
+ *   weight tile as it passes through them, so only the experts that received
+ *   rows are written -- no backward GEMM reads the others; in MOE_PREC_MXFP8 the
+ *   forward's weight passes write every expert);
  *   *_sf    their UE8M0 scale codes (2^(code-127)), one per 32 elements along
  *           K, in 512-byte atoms of 128 rows x 128 K, the order the tensor core
  *           reads them: row w of atom row-block rb, K-block b, sits at byte

@@ -133,7 +133,7 @@ def test_fp8_shapes_and_layout(L):
     Mp = q["m_pad"]
     assert Mp % 128 == 0 and Mp >= M + 127 * E
     sizes = {"pad_offsets": 4 * (E + 1), "dy_q": Mp * H, "dg_q": Mp * I, "du_q": Mp * I,
-             "dy_t": H * Mp, "x_t": H * Mp, "dg_t": I * Mp, "du_t": I * Mp}
+             "dy_t": H * Mp, "dg_t": I * Mp, "du_t": I * Mp}
     for n in list(sizes):
         if n != "pad_offsets":
             R, K = {"dy_q": (Mp, H), "wd_q": (E * I, H), "dg_q": (Mp, I), "du_q": (Mp, I), "wg_q": (E * H, I),
@@ -153,11 +153,12 @@ def test_fp8_shapes_and_layout(L):
     # quantised)
     assert spans[0][0] >= 256 + M * H * 2 + M * 4 * 4 and spans[-1][1] <= bs
     assert bs < bs16 + sum(sizes.values()) + 256 * len(sizes)
-    # w * A along tokens and the weights' codes live in `saved` (the forward writes them),
-    # after the bf16 activations
+    # w * A and x along tokens and the weights' codes live in `saved` (the forward writes
+    # them), after the bf16 activations
     _, sv, _, _ = moe.query_workspace(c)
     so = moe.saved_offsets(c)
     ssz = {"aw_t": I * Mp, "aw_t_sf": moe.sf_layout_bytes(I, Mp, I, 128),
+           "x_t": H * Mp, "x_t_sf": moe.sf_layout_bytes(H, Mp, H, 128),
            "wd_q": E * I * H, "wg_q": E * H * I, "wu_q": E * H * I}
     for n, (R, K, seg) in {"wd_q": (E * I, H, I), "wg_q": (E * H, I, H), "wu_q": (E * H, I, H)}.items():
         ssz[n[:-2] + "_sf"] = moe.sf_layout_bytes(R, K, seg, moe.MX_BN)
