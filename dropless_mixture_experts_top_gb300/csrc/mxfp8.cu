@@ -200,7 +200,8 @@ __global__ void __launch_bounds__(kQcThreads, 3) quant_cols_kernel(const uint16_
       const int cc = threadIdx.x % kQcCols, b = threadIdx.x / kQcCols;  // 4 blocks of 32 tokens
       float v[32];
       qc_col32(tile, cc, b, v);
-      sf[atom_byte(c0 + cc, (prow0 >> 5) + b, Mpad, L)] =
+      const size_t srow = L.group == 128 ? atom_row<128>(c0 + cc, Mpad, L) : atom_row(c0 + cc, Mpad, L);
+      sf[srow + atom_kblock((prow0 >> 5) + b)] =
           quant32(v, reinterpret_cast<uint4 *>(otile + cc * kQcOutStride + 32 * b));
       __syncthreads();
 #pragma unroll
@@ -223,7 +224,7 @@ __global__ void __launch_bounds__(kQcThreads, 3) quant_cols_kernel(const uint16_
 // block; transposed: dW_down's B operand), and every row accumulates its part
 // of g = <dy_t, Y_r> over the block's columns; the part of block column
 // y of row r goes to g_part[r * gridDim.y + y], added in order by the router
-// gradient kernel.
+// gradient kernel.  The transposed codes' scale rows are grouped by kMxBN.
 constexpr int kDyRing = 3;
 constexpr int kDySmem = kDyRing * 2 * kQcTileElems * 2 + kQcCols * kQcOutStride;
 
@@ -272,6 +273,7 @@ __global__ void __launch_bounds__(kQcThreads, 2) dy_quant_kernel(const uint16_t 
     qc_issue(slot + kQcTileElems, first + i * step, y_ptr, true);  // one group per tile: both sources
   };
   const int r = threadIdx.x >> 1, bb = threadIdx.x & 1;  // row pass: row, 32-column block
+  const size_t row_sf = atom_row(prow0 + r, H, rows.L);  // its scale bytes' row
   float gpart = 0.f;
   for (int i = 0; i < kDyRing - 1 && i < nt; ++i) issue(i);
   for (int it = 0; it < nt; ++it) {
@@ -288,13 +290,13 @@ __global__ void __launch_bounds__(kQcThreads, 2) dy_quant_kernel(const uint16_t 
 #pragma unroll
       for (int i = 0; i < 32; ++i) gpart = fmaf(v[i], yv[i], gpart);
       const int prow = prow0 + r, kb = (c0 >> 5) + bb;
-      rows.sf[atom_byte(prow, kb, H, rows.L)] =
+      rows.sf[row_sf + atom_kblock(kb)] =
           quant32(v, reinterpret_cast<uint4 *>(rows.codes + static_cast<size_t>(prow) * H + c0 + 32 * bb));
     }
     const int cc = threadIdx.x % kQcCols, b = threadIdx.x / kQcCols;  // 4 blocks of 32 tokens
     float v[32];
     qc_col32(tile, cc, b, v);
-    sf_t[atom_byte(c0 + cc, (prow0 >> 5) + b, Mpad, Lt)] =
+    sf_t[atom_row<kMxBN>(c0 + cc, Mpad, Lt) + atom_kblock((prow0 >> 5) + b)] =
         quant32(v, reinterpret_cast<uint4 *>(otile + cc * kQcOutStride + 32 * b));
     __syncthreads();
 #pragma unroll

@@ -61,6 +61,21 @@ __device__ __forceinline__ uint8_t quant32(const float (&v)[32], uint4 *dst) {
   return static_cast<uint8_t>(X + 127);
 }
 
+// Byte of (row, K block 0) in a scale-atom buffer of K columns grouped by L;
+// K block kb of the same row adds atom_kblock(kb).  With the group size known
+// at compile time (kGroup > 0) its divisions become multiplications.
+template <int kGroup = 0>
+__device__ __forceinline__ size_t atom_row(int row, int K, SfLayout L) {
+  const int group = kGroup > 0 ? kGroup : L.group;
+  const int sg = row / L.seg, r = row - sg * L.seg;
+  const int g = r / group, rr = r - g * group;
+  const int gps = (L.seg + group - 1) / group, apg = (group + 127) >> 7;
+  const size_t rb = (static_cast<size_t>(sg) * gps + g) * apg + (rr >> 7);
+  const int w = rr & 127;
+  return rb * (K >> 7) * 512 + (w & 31) * 16 + (w >> 5) * 4;
+}
+__device__ __forceinline__ size_t atom_kblock(int kblock) { return static_cast<size_t>(kblock >> 2) * 512 + (kblock & 3); }
+
 // Byte of (row, K block) in a scale-atom buffer of K columns grouped by L.
 __device__ __forceinline__ size_t atom_byte(int row, int kblock, int K, SfLayout L) {
   const int sg = row / L.seg, r = row - sg * L.seg;
