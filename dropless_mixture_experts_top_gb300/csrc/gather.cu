@@ -114,8 +114,8 @@ __global__ void __launch_bounds__(kWarps * 32) permute_quant_kernel(
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
       const int X = mx_scale_exp(amax);
       const float s = pow2_neg(X);
-      q[u] = make_uint2(pack_e4m3x4(f[0] * s, f[1] * s, f[2] * s, f[3] * s),
-                        pack_e4m3x4(f[4] * s, f[5] * s, f[6] * s, f[7] * s));
+      q[u] = make_uint2(pack_e4m3x4_scaled(f[0], f[1], f[2], f[3], s),
+                        pack_e4m3x4_scaled(f[4], f[5], f[6], f[7], s));
       scode[u] = static_cast<uint8_t>(X + 127);
     }
     for (int j = 0; j < k; ++j) {

@@ -266,10 +266,10 @@ __device__ __forceinline__ void quant_weight_rows(const uint16_t *__restrict__ w
       const int X = mx_scale_exp(amax);
       const float sc = pow2_neg(X);
       uint4 o;
-      o.x = pack_e4m3x4(v[0] * sc, v[1] * sc, v[2] * sc, v[3] * sc);
-      o.y = pack_e4m3x4(v[4] * sc, v[5] * sc, v[6] * sc, v[7] * sc);
-      o.z = pack_e4m3x4(v[8] * sc, v[9] * sc, v[10] * sc, v[11] * sc);
-      o.w = pack_e4m3x4(v[12] * sc, v[13] * sc, v[14] * sc, v[15] * sc);
+      o.x = pack_e4m3x4_scaled(v[0], v[1], v[2], v[3], sc);
+      o.y = pack_e4m3x4_scaled(v[4], v[5], v[6], v[7], sc);
+      o.z = pack_e4m3x4_scaled(v[8], v[9], v[10], v[11], sc);
+      o.w = pack_e4m3x4_scaled(v[12], v[13], v[14], v[15], sc);
       *reinterpret_cast<uint4 *>(dst + i * step) = o;
       // the row's four blocks: scale codes of lanes 0, 2, 4, 6 of its eight, one word
       const uint32_t x0 = static_cast<uint32_t>(X + 127);

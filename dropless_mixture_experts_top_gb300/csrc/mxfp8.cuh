@@ -39,6 +39,25 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
   return lo | (hi << 16);
 }
 
+// (a s, b s) with one paired multiply (each lane rounded as a plain fp32 product;
+// s is a power of two here, so the products are exact).
+__device__ __forceinline__ float2 mul2(float a, float b, float s) {
+  uint64_t x, y, r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a), "f"(b));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(y) : "f"(s));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(y));
+  float2 o;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+  return o;
+}
+
+// Four E4M3 codes of a s, b s, c s, d s, a's in the lowest byte.
+__device__ __forceinline__ uint32_t pack_e4m3x4_scaled(float a, float b, float c, float d, float s) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(mul2(a, b, s), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(mul2(c, d, s), __NV_SATFINITE, __NV_E4M3);
+  return lo | (hi << 16);
+}
+
 // Quantise 32 values held in registers; writes 32 code bytes; returns the E8M0 code.
 __device__ __forceinline__ uint8_t quant32(const float (&v)[32], uint4 *dst) {
   float m[8];  // eight independent max chains, then a tree
@@ -55,7 +74,7 @@ __device__ __forceinline__ uint8_t quant32(const float (&v)[32], uint4 *dst) {
   uint32_t w[8];
 #pragma unroll
   for (int q = 0; q < 8; ++q)
-    w[q] = pack_e4m3x4(v[4 * q] * s, v[4 * q + 1] * s, v[4 * q + 2] * s, v[4 * q + 3] * s);
+    w[q] = pack_e4m3x4_scaled(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3], s);
   dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
   dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
   return static_cast<uint8_t>(X + 127);
