@@ -51,6 +51,37 @@ __device__ __forceinline__ float2 mul2(float a, float b, float s) {
   return o;
 }
 
+// Paired fp32 arithmetic on (x, y) pairs, each lane rounded as the plain fp32
+// operation (PTX .f32x2).
+struct F2 {
+  uint64_t r;
+};
+__device__ __forceinline__ F2 f2(float a, float b) {
+  F2 o;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(o.r) : "f"(a), "f"(b));
+  return o;
+}
+__device__ __forceinline__ float2 f2_get(F2 x) {
+  float2 o;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(x.r));
+  return o;
+}
+__device__ __forceinline__ F2 f2_mul(F2 a, F2 b) {
+  F2 o;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(o.r) : "l"(a.r), "l"(b.r));
+  return o;
+}
+__device__ __forceinline__ F2 f2_sub(F2 a, F2 b) {
+  F2 o;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(o.r) : "l"(a.r), "l"(b.r));
+  return o;
+}
+__device__ __forceinline__ F2 f2_fma(F2 a, F2 b, F2 c) {
+  F2 o;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(o.r) : "l"(a.r), "l"(b.r), "l"(c.r));
+  return o;
+}
+
 // Four E4M3 codes of a s, b s, c s, d s, a's in the lowest byte.
 __device__ __forceinline__ uint32_t pack_e4m3x4_scaled(float a, float b, float c, float d, float s) {
   const uint32_t lo = __nv_cvt_float2_to_fp8x2(mul2(a, b, s), __NV_SATFINITE, __NV_E4M3);
@@ -93,7 +124,9 @@ __device__ __forceinline__ size_t atom_row(int row, int K, SfLayout L) {
   const int w = rr & 127;
   return rb * (K >> 7) * 512 + (w & 31) * 16 + (w >> 5) * 4;
 }
-__device__ __forceinline__ size_t atom_kblock(int kblock) { return static_cast<size_t>(kblock >> 2) * 512 + (kblock & 3); }
+__device__ __forceinline__ size_t atom_kblock(int kblock) {
+  return static_cast<size_t>(kblock >> 2) * 512 + (kblock & 3);
+}
 
 // Byte of (row, K block) in a scale-atom buffer of K columns grouped by L.
 __device__ __forceinline__ size_t atom_byte(int row, int kblock, int K, SfLayout L) {
