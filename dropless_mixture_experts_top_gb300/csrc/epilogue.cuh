@@ -167,11 +167,16 @@ __device__ __forceinline__ void epilogue_tile(const Tile &t, uint32_t tb, int ri
       tmem_ld32(tb + 128 + 32 * c, r1);
       tmem_ld_wait();
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float g = __uint_as_float(r0[i]), u = __uint_as_float(r1[i]);
-        v0[i] = g * sigmoidf_(g) * u;  // SwiGLU
-        v1[i] = g;
-        v2[i] = u;
+      for (int i = 0; i < 32; i += 2) {  // two columns at a time
+        const float g0 = __uint_as_float(r0[i]), g1 = __uint_as_float(r0[i + 1]);
+        const float u0 = __uint_as_float(r1[i]), u1 = __uint_as_float(r1[i + 1]);
+        const float2 a = f2_get(f2_mul(f2_mul(f2(g0, g1), f2(sigmoidf_(g0), sigmoidf_(g1))), f2(u0, u1)));
+        v0[i] = a.x;  // SwiGLU
+        v0[i + 1] = a.y;
+        v1[i] = g0;
+        v1[i + 1] = g1;
+        v2[i] = u0;
+        v2[i + 1] = u1;
       }
       const size_t off = static_cast<size_t>(row0) * p.I + col;
       store_rows32(tile, p.o0 + off, p.I, nvalid, v0);
@@ -351,15 +356,23 @@ __device__ __forceinline__ bool epilogue_da_ring(const Tile &t, uint32_t tb, int
     const int col = t.n0 + 32 * c;
     tmem_ld32(tb + 32 * c, r0);
     tmem_ld_wait();
+    const F2 w2 = f2(w, w), one = f2(1.f, 1.f);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {  // in place: v1 G -> dU, v2 U -> dG
-      const float acc = __uint_as_float(r0[i]), gg = v1[i], u = v2[i];
-      const float da = w * acc;
-      const float sg = sigmoidf_(gg);
-      const float silu = gg * sg;
-      gp = fmaf(acc, silu * u, gp);                   // <dy . W_down^T, A>
-      v2[i] = da * u * sg * (1.f + gg * (1.f - sg));  // dG
-      v1[i] = da * silu;                              // dU = dA * silu(G)
+    for (int i = 0; i < 32; i += 2) {  // in place: v1 G -> dU, v2 U -> dG; two columns at a time
+      const F2 acc = f2(__uint_as_float(r0[i]), __uint_as_float(r0[i + 1]));
+      const F2 gg = f2(v1[i], v1[i + 1]), u = f2(v2[i], v2[i + 1]);
+      const F2 da = f2_mul(w2, acc);
+      const F2 sg = f2(sigmoidf_(v1[i]), sigmoidf_(v1[i + 1]));
+      const F2 silu = f2_mul(gg, sg);
+      const float2 su = f2_get(f2_mul(silu, u));
+      gp = fmaf(__uint_as_float(r0[i]), su.x, gp);  // <dy . W_down^T, A>, in column order
+      gp = fmaf(__uint_as_float(r0[i + 1]), su.y, gp);
+      const float2 dg = f2_get(f2_mul(f2_mul(f2_mul(da, u), sg), f2_fma(gg, f2_sub(one, sg), one)));
+      const float2 du = f2_get(f2_mul(da, silu));  // dU = dA * silu(G)
+      v2[i] = dg.x;
+      v2[i + 1] = dg.y;
+      v1[i] = du.x;
+      v1[i + 1] = du.y;
     }
     store_rows32(tile, p.o0 + rowoff + col, p.I, nvalid, v2);
     store_rows32(tile, p.o1 + rowoff + col, p.I, nvalid, v1);
