@@ -206,6 +206,17 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   return r;
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched
+// allowed to start while the kernel before it in the stream finishes; it calls
+// griddep_wait() before it touches global memory that an earlier kernel may
+// write (a no-op when launched without that permission).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel in the stream be launched before this one finishes (it
+// still waits for this one's completion in its griddep_wait()).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Address of the same shared-memory location in CTA `rank` of this cluster.
 __device__ __forceinline__ uint32_t peer_smem_addr(const void *p, uint32_t rank) {
   uint32_t out;

@@ -50,6 +50,7 @@ __global__ void __launch_bounds__(kWarps * 32) permute_rows_kernel(const uint4 *
                                                                   const int32_t *__restrict__ ros,
                                                                   uint4 *__restrict__ xp, int T,
                                                                   int nv, int k) {
+  griddep_wait();  // the previous kernel in the stream has completed
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -82,6 +83,7 @@ __global__ void __launch_bounds__(kWarps * 32) permute_quant_kernel(
     const uint4 *__restrict__ x, const int32_t *__restrict__ ros, const int32_t *__restrict__ topk_idx,
     const int32_t *__restrict__ offsets, const int32_t *__restrict__ pad_off, uint4 *__restrict__ xp,
     uint8_t *__restrict__ codes, uint8_t *__restrict__ sf, SfLayout L, int T, int nv, int k) {
+  griddep_wait();  // the previous kernel in the stream has completed
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -142,6 +144,7 @@ __global__ void __launch_bounds__(256) zero_pad_rows_kernel(const int32_t *__res
                                                             const int32_t *__restrict__ pad_off, int K,
                                                             uint8_t *__restrict__ codes,
                                                             uint8_t *__restrict__ sf, SfLayout L) {
+  griddep_wait();  // the previous kernel in the stream has completed
   const int e = blockIdx.x;
   const int first = __ldg(pad_off + e) + (__ldg(offsets + e + 1) - __ldg(offsets + e));
   const int end = __ldg(pad_off + e + 1);
@@ -160,6 +163,7 @@ __global__ void __launch_bounds__(kWarps * 32) gather_sum_kernel(const uint4 *__
                                                                 const float *__restrict__ w,
                                                                 uint4 *__restrict__ out, int T,
                                                                 int nv, int k) {
+  griddep_wait();  // the previous kernel in the stream has completed
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -235,6 +239,7 @@ __global__ void __launch_bounds__(kWarps * 32) router_grad_kernel(
     const int32_t *__restrict__ ros, const int32_t *__restrict__ topk_idx, const float *__restrict__ topk_w,
     const float *__restrict__ g_part, int np, float *__restrict__ d_logits, float *__restrict__ d_topk_w,
     int T, int E, int k) {
+  griddep_wait();  // the previous kernel in the stream has completed
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -256,23 +261,16 @@ inline int blocks_for(int T) { return (T + kWarps - 1) / kWarps; }
 
 cudaError_t launch_permute_rows(const uint16_t *x, const int32_t *row_of_slot, uint16_t *x_perm,
                                 int T, int H, int k, cudaStream_t s) {
-  permute_rows_kernel<<<blocks_for(T), kWarps * 32, 0, s>>>(
-      reinterpret_cast<const uint4 *>(x), row_of_slot, reinterpret_cast<uint4 *>(x_perm), T, H / 8,
-      k);
-  return cudaGetLastError();
+  return launch_pdl(permute_rows_kernel, dim3(blocks_for(T)), dim3(kWarps * 32), 0, s, 1,
+                    reinterpret_cast<const uint4 *>(x), row_of_slot, reinterpret_cast<uint4 *>(x_perm), T, H / 8,
+                    k);
 }
 
 cudaError_t launch_gather_sum(const uint16_t *rows, const int32_t *row_of_slot, const float *w,
                               uint16_t *out, int T, int H, int k, cudaStream_t s) {
-  if (w)
-    gather_sum_kernel<true><<<blocks_for(T), kWarps * 32, 0, s>>>(
-        reinterpret_cast<const uint4 *>(rows), row_of_slot, w, reinterpret_cast<uint4 *>(out), T,
-        H / 8, k);
-  else
-    gather_sum_kernel<false><<<blocks_for(T), kWarps * 32, 0, s>>>(
-        reinterpret_cast<const uint4 *>(rows), row_of_slot, nullptr,
-        reinterpret_cast<uint4 *>(out), T, H / 8, k);
-  return cudaGetLastError();
+  return launch_pdl(w ? gather_sum_kernel<true> : gather_sum_kernel<false>, dim3(blocks_for(T)),
+                    dim3(kWarps * 32), 0, s, 1, reinterpret_cast<const uint4 *>(rows), row_of_slot, w,
+                    reinterpret_cast<uint4 *>(out), T, H / 8, k);
 }
 
 namespace {
@@ -283,6 +281,7 @@ namespace {
 // tokens [T i / S, T (i+1) / S)).
 __global__ void __launch_bounds__(256) router_dlogits_kernel(const float4 *__restrict__ in, uint2 *__restrict__ out,
                                                              int64_t n4, int32_t *split, int T, int S) {
+  griddep_wait();  // the previous kernel in the stream has completed
   if (blockIdx.x == 0 && static_cast<int>(threadIdx.x) <= S)
     split[threadIdx.x] = static_cast<int32_t>(static_cast<int64_t>(T) * threadIdx.x / S);
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -294,6 +293,7 @@ __global__ void __launch_bounds__(256) router_dlogits_kernel(const float4 *__res
 // out[i] = sum over s of parts[s][i], s ascending (a fixed order: deterministic).
 __global__ void __launch_bounds__(256) sum_segments_kernel(const float4 *__restrict__ parts, int S, int64_t n4,
                                                            float4 *__restrict__ out) {
+  griddep_wait();  // the previous kernel in the stream has completed
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n4) return;
   float4 a = __ldg(parts + i);
@@ -314,40 +314,35 @@ cudaError_t launch_router_dlogits(const float *d_logits, uint16_t *out, int64_t 
   if (S < 1 || S > 63) return cudaErrorInvalidValue;
   const int64_t n4 = n / 4;  // n = T * E, a multiple of 8 (E % 8 == 0)
   const int64_t blocks = (n4 + 255) / 256;
-  router_dlogits_kernel<<<static_cast<unsigned>(blocks > 0 ? blocks : 1), 256, 0, s>>>(
-      reinterpret_cast<const float4 *>(d_logits), reinterpret_cast<uint2 *>(out), n4, split, T, S);
-  return cudaGetLastError();
+  return launch_pdl(router_dlogits_kernel, dim3(static_cast<unsigned>(blocks > 0 ? blocks : 1)), dim3(256), 0, s,
+                    1, reinterpret_cast<const float4 *>(d_logits), reinterpret_cast<uint2 *>(out), n4, split, T, S);
 }
 
 cudaError_t launch_sum_segments(const float *parts, int S, int64_t n, float *out, cudaStream_t s) {
   const int64_t n4 = n / 4;  // n = H * E, a multiple of 8
   if (n4 == 0) return cudaSuccess;
-  sum_segments_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, s>>>(
-      reinterpret_cast<const float4 *>(parts), S, n4, reinterpret_cast<float4 *>(out));
-  return cudaGetLastError();
+  return launch_pdl(sum_segments_kernel, dim3(static_cast<unsigned>((n4 + 255) / 256)), dim3(256), 0, s, 1,
+                    reinterpret_cast<const float4 *>(parts), S, n4, reinterpret_cast<float4 *>(out));
 }
 
 cudaError_t launch_permute_quant(const uint16_t *x, const int32_t *row_of_slot, const int32_t *topk_idx,
                                  const int32_t *offsets, const int32_t *pad_off, uint16_t *x_perm,
                                  uint8_t *codes, uint8_t *sf, SfLayout L, int T, int H, int k, cudaStream_t s) {
-  permute_quant_kernel<<<blocks_for(T), kWarps * 32, 0, s>>>(
-      reinterpret_cast<const uint4 *>(x), row_of_slot, topk_idx, offsets, pad_off,
-      reinterpret_cast<uint4 *>(x_perm), codes, sf, L, T, H / 8, k);
-  return cudaGetLastError();
+  return launch_pdl(permute_quant_kernel, dim3(blocks_for(T)), dim3(kWarps * 32), 0, s, 1,
+                    reinterpret_cast<const uint4 *>(x), row_of_slot, topk_idx, offsets, pad_off,
+                    reinterpret_cast<uint4 *>(x_perm), codes, sf, L, T, H / 8, k);
 }
 
 cudaError_t launch_zero_pad_rows(const int32_t *offsets, const int32_t *pad_off, int E, int K, uint8_t *codes,
                                  uint8_t *sf, SfLayout L, cudaStream_t s) {
-  zero_pad_rows_kernel<<<E, 256, 0, s>>>(offsets, pad_off, K, codes, sf, L);
-  return cudaGetLastError();
+  return launch_pdl(zero_pad_rows_kernel, dim3(E), dim3(256), 0, s, 1, offsets, pad_off, K, codes, sf, L);
 }
 
 cudaError_t launch_router_grad(const int32_t *row_of_slot, const int32_t *topk_idx, const float *topk_w,
                                const float *g_part, int np, float *d_logits, float *d_topk_w, int T, int E, int k,
                                cudaStream_t s) {
-  router_grad_kernel<<<blocks_for(T), kWarps * 32, 0, s>>>(row_of_slot, topk_idx, topk_w, g_part, np, d_logits,
-                                                           d_topk_w, T, E, k);
-  return cudaGetLastError();
+  return launch_pdl(router_grad_kernel, dim3(blocks_for(T)), dim3(kWarps * 32), 0, s, 1, row_of_slot, topk_idx,
+                    topk_w, g_part, np, d_logits, d_topk_w, T, E, k);
 }
 
 }  // namespace moe

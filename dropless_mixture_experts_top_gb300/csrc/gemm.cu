@@ -346,6 +346,7 @@ __global__ void __launch_bounds__(threads_of(MODE, WQ), 1)
     tma_prefetch_desc(&tmB1);
   }
   if (warp == 1) tmem_alloc_pair(tmem_slot, kTmemCols);
+  griddep_wait();  // the set-up above overlaps the previous kernel's end; its outputs are read below
   // no offsets: one segment of all M_rows rows (the router projection's logits and dx)
   for (int e = threadIdx.x; e <= E; e += NT)
     s_off[e] = p.offsets ? __ldg(p.offsets + e) : (e == 0 ? 0 : p.M_rows);
@@ -453,6 +454,7 @@ __global__ void __launch_bounds__(threads_of(MODE, WQ), 1)
           }
         }
       }
+      griddep_launch_dependents();  // all loads issued: the next kernel may be launched
       if (*abort_flag && rank == 0) {  // let the pair's copies land before exit
         for (int s = 0; s < STAGES; ++s) {
           if (!((armed >> s) & 1u)) continue;
@@ -640,6 +642,7 @@ struct MapTemplates {
 __global__ void __launch_bounds__(256) expert_maps_kernel(const __grid_constant__ MapTemplates tm,
                                                           const int32_t *__restrict__ offsets, int E,
                                                           CUtensorMap *out) {
+  griddep_wait();  // the previous kernel in the stream has completed
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= E) return;
   const int end = __ldg(offsets + e + 1);
@@ -795,8 +798,8 @@ cudaError_t launch_mode(const GemmArgs &a, cudaStream_t s) {
     tm.m[1] = mB0;
     tm.m[2] = mB1;
     CUtensorMap *maps = static_cast<CUtensorMap *>(a.map_scratch);
-    expert_maps_kernel<<<(p.E + 255) / 256, 256, 0, s>>>(tm, a.offsets, p.E, maps);
-    cudaError_t e = cudaGetLastError();
+    const cudaError_t e = launch_pdl(expert_maps_kernel, dim3((p.E + 255) / 256), dim3(256), 0, s, 1, tm,
+                                     a.offsets, p.E, maps);
     if (e != cudaSuccess) return e;
     p.expert_maps = maps;
   }
@@ -823,11 +826,13 @@ cudaError_t launch_kernel(const CUtensorMap &mA0, const CUtensorMap &mA1, const 
   // once per device: the shared-memory opt-in, and how many CTA pairs fit at once
   static DeviceOnce once;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see launch_pdl
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(threads_of(MODE, WQ));
   cfg.dynamicSmemBytes = smem_bytes(MODE, WQ);
   cfg.stream = s;
@@ -851,6 +856,7 @@ cudaError_t launch_kernel(const CUtensorMap &mA0, const CUtensorMap &mA1, const 
       &pair_grid);
   if (e != cudaSuccess) return e;
   cfg.gridDim = dim3(pair_grid);
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE, WQ>, mA0, mA1, mB0, mB1, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

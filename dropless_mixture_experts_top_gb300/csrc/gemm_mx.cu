@@ -464,6 +464,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
     tma_prefetch_desc(&tmB1);
   }
   if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  griddep_wait();  // the set-up above overlaps the previous kernel's end; its outputs are read below
   for (int e = threadIdx.x; e <= E; e += threads_of(MODE)) {
     s_off[e] = __ldg(p.offsets + e);
     s_pad[e] = __ldg(p.pad_off + e);
@@ -521,6 +522,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 1)
           }
         }
       }
+      griddep_launch_dependents();  // all loads issued: the next kernel may be launched
       if (*abort_flag) {  // let the copies in flight land before the CTA exits
         for (int s = 0; s < STAGES; ++s) {
           if (!((armed >> s) & 1u)) continue;
@@ -782,9 +784,8 @@ cudaError_t launch_mx_mode(const MxGemmArgs &a, cudaStream_t s) {
                                 smem_bytes(MODE));
   });
   if (e != cudaSuccess) return e;
-  grouped_gemm_mx_kernel<MODE><<<a.num_sms, threads_of(MODE), smem_bytes(MODE), s>>>(mA0, mA1, mB0,
-                                                                                    mB1, p);
-  return cudaGetLastError();
+  return launch_pdl(grouped_gemm_mx_kernel<MODE>, dim3(a.num_sms), dim3(threads_of(MODE)), smem_bytes(MODE), s, 1,
+                    mA0, mA1, mB0, mB1, p);
 }
 
 }  // namespace

@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include <mutex>
+#include <utility>
 
 namespace moe {
 
@@ -31,6 +32,35 @@ struct DeviceOnce {
     return err[dev];
   }
 };
+
+// Launches `kernel` on stream s allowed to start before the kernel ahead of it
+// in the stream has finished (programmatic dependent launch); the kernel waits
+// for that one's completion (griddepcontrol.wait) before it reads its outputs.
+// Optionally as clusters of `cluster` CTAs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, int cluster,
+                       Args &&...args) {
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int n = 1;
+  if (cluster > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    n = 2;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
 
 // Status flags written by kernels into the scratch status word.
 constexpr int32_t kDevNonfiniteLogit = 0x1;

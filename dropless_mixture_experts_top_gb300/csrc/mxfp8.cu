@@ -147,6 +147,7 @@ __global__ void __launch_bounds__(kQcThreads, 3) quant_cols_kernel(const uint16_
                                                                 RowCodes rows,
                                                                 const int32_t *__restrict__ slot_of_row, int k,
                                                                 uint16_t *__restrict__ xp) {
+  griddep_wait();  // the previous kernel in the stream has completed
   extern __shared__ __align__(16) uint8_t qc_smem[];
   uint16_t *ring = reinterpret_cast<uint16_t *>(qc_smem);
   uint8_t *otile = qc_smem + kQcRing * kQcTileElems * 2;
@@ -235,6 +236,7 @@ __global__ void __launch_bounds__(kQcThreads, 2) dy_quant_kernel(const uint16_t 
                                                                  const int32_t *__restrict__ pad_off, int E,
                                                                  uint8_t *__restrict__ codes_t, uint8_t *__restrict__ sf_t,
                                                                  SfLayout Lt, RowCodes rows, float *__restrict__ g_part) {
+  griddep_wait();  // the previous kernel in the stream has completed
   extern __shared__ __align__(16) uint8_t qc_smem[];
   uint16_t *ring = reinterpret_cast<uint16_t *>(qc_smem);  // [kDyRing][dy tile | Y tile]
   uint8_t *otile = qc_smem + kDyRing * 2 * kQcTileElems * 2;
@@ -326,6 +328,7 @@ __global__ void __launch_bounds__(kQcThreads, 3) quant_wT_kernel(const uint16_t 
                                                                  uint8_t *__restrict__ codes,
                                                                  uint8_t *__restrict__ sf, SfLayout L,
                                                                  RowCodes rows) {
+  griddep_wait();  // the previous kernel in the stream has completed
   extern __shared__ __align__(16) uint8_t qc_smem[];
   uint16_t *ring = reinterpret_cast<uint16_t *>(qc_smem);
   uint8_t *otile = qc_smem + kQcRing * kQcTileElems * 2;
@@ -363,6 +366,7 @@ __global__ void __launch_bounds__(kQcThreads, 3) quant_wT_kernel(const uint16_t 
 // pad_off[e] = sum over e' < e of ceil(count/128)*128; pad_off[E] = padded total.
 __global__ void __launch_bounds__(32) pad_offsets_kernel(const int32_t *__restrict__ offsets, int E,
                                                          int32_t *__restrict__ pad_off) {
+  griddep_wait();  // the previous kernel in the stream has completed
   const int lane = threadIdx.x;
   int carry = 0;
   for (int base = 0; base < E; base += 32) {
@@ -383,8 +387,7 @@ __global__ void __launch_bounds__(32) pad_offsets_kernel(const int32_t *__restri
 }  // namespace
 
 cudaError_t launch_pad_offsets(const int32_t *offsets, int E, int32_t *pad_off, cudaStream_t s) {
-  pad_offsets_kernel<<<1, 32, 0, s>>>(offsets, E, pad_off);
-  return cudaGetLastError();
+  return launch_pdl(pad_offsets_kernel, dim3(1), dim3(32), 0, s, 1, offsets, E, pad_off);
 }
 
 cudaError_t launch_quant_cols(const uint16_t *src, int C, int Mpad, const int32_t *offsets,
@@ -397,9 +400,8 @@ cudaError_t launch_quant_cols(const uint16_t *src, int C, int Mpad, const int32_
     return cudaFuncSetAttribute(quant_cols_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQcSmem);
   });
   if (e != cudaSuccess) return e;
-  quant_cols_kernel<<<grid, kQcThreads, kQcSmem, s>>>(src, C, Mpad, offsets, pad_off, E, codes, sf, L, rows,
-                                                       slot_of_row, k, xp);
-  return cudaGetLastError();
+  return launch_pdl(quant_cols_kernel, grid, dim3(kQcThreads), kQcSmem, s, 1, src, C, Mpad, offsets, pad_off, E,
+                    codes, sf, L, rows, slot_of_row, k, xp);
 }
 
 cudaError_t launch_dy_quant(const uint16_t *dy, const uint16_t *Y, const int32_t *slot_of_row, int k, int H,
@@ -412,9 +414,8 @@ cudaError_t launch_dy_quant(const uint16_t *dy, const uint16_t *Y, const int32_t
     return cudaFuncSetAttribute(dy_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDySmem);
   });
   if (e != cudaSuccess) return e;
-  dy_quant_kernel<<<grid, kQcThreads, kDySmem, s>>>(dy, Y, slot_of_row, k, H, Mpad, offsets, pad_off, E, codes_t,
-                                                     sf_t, Lt, rows, g_part);
-  return cudaGetLastError();
+  return launch_pdl(dy_quant_kernel, grid, dim3(kQcThreads), kDySmem, s, 1, dy, Y, slot_of_row, k, H, Mpad, offsets,
+                    pad_off, E, codes_t, sf_t, Lt, rows, g_part);
 }
 
 int dy_quant_col_blocks(int H) { return H / kQcCols < 4 ? H / kQcCols : 4; }
@@ -428,8 +429,8 @@ cudaError_t launch_quant_wT(const uint16_t *W, int E, int R, int C, int interlea
     return cudaFuncSetAttribute(quant_wT_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQcSmem);
   });
   if (e != cudaSuccess) return e;
-  quant_wT_kernel<<<grid, kQcThreads, kQcSmem, s>>>(W, R, C, interleave, half, codes, sf, L, rows);
-  return cudaGetLastError();
+  return launch_pdl(quant_wT_kernel, grid, dim3(kQcThreads), kQcSmem, s, 1, W, R, C, interleave, half, codes, sf, L,
+                    rows);
 }
 
 }  // namespace moe

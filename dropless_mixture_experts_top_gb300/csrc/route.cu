@@ -175,6 +175,7 @@ __host__ __device__ constexpr int logit_stride(int E) { return E + 4; }
 
 template <int KMAX>
 __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(RouteArgs a) {
+  griddep_wait();  // the previous kernel in the stream has completed
   extern __shared__ __align__(16) float s_lg[];           // [TB][E + 4] this block's logits
   __shared__ uint32_t s_emask[kMaxExperts][kMaskWords];  // tokens of this block that chose expert e
   __shared__ uint8_t s_slot_e[TB * kMaxTopK];            // expert of each of the block's slots
@@ -368,6 +369,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(RouteArgs a) 
 }
 
 __global__ void __launch_bounds__(256) route_index_kernel(RouteArgs a) {
+  griddep_wait();  // the previous kernel in the stream has completed
   const int s = blockIdx.x * 256 + threadIdx.x;  // slot t * k + j
   if (s >= a.T * a.k) return;
   const int e = __ldg(a.topk_idx + s), r = __ldg(a.lrank + s);
@@ -395,8 +397,7 @@ cudaError_t launch_topk(const RouteArgs &a, cudaStream_t s) {
                                 TB * logit_stride(kMaxExperts) * static_cast<int>(sizeof(float)));
   });
   if (e != cudaSuccess) return e;
-  route_topk_kernel<KMAX><<<nblk, kRouteThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(route_topk_kernel<KMAX>, dim3(nblk), dim3(kRouteThreads), smem, s, 1, a);
 }
 
 cudaError_t launch_route_topk(const RouteArgs &a, cudaStream_t s) {
@@ -405,8 +406,7 @@ cudaError_t launch_route_topk(const RouteArgs &a, cudaStream_t s) {
 
 cudaError_t launch_route_index(const RouteArgs &a, cudaStream_t s) {
   const int slots = a.T * a.k;
-  route_index_kernel<<<(slots + 255) / 256, 256, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(route_index_kernel, dim3((slots + 255) / 256), dim3(256), 0, s, 1, a);
 }
 
 }  // namespace moe
