@@ -435,7 +435,8 @@ def run_ours(args):
     # pipeline runs it: each step copies its inputs (x, dy, logits) from pinned
     # host memory and its results (out, dx, d_logits) back, on two copy streams
     # beside the compute stream, double-buffered so that step i+1's inputs
-    # arrive and step i-1's results leave while step i computes.  Every step
+    # arrive and step i-1's results leave while step i computes; each phase of a
+    # step waits only for the inputs it reads, and out leaves after the forward.  Every step
     # moves all of its bytes; the time is the whole run's (first input copy to
     # last result copy) over K steps.  Inputs and weights exceed L2, so no flush.
     pin = {n: torch.from_numpy(inp[n].view(np.int16)).pin_memory() for n in ("x", "dy")}
@@ -450,28 +451,35 @@ def run_ours(args):
              "d_logits": torch.empty_like(grads["d_logits"]), "d_topk_w": torch.empty_like(grads["d_topk_w"])}
             for _ in range(2)]
     s_h2d, s_d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    h2d_done = [torch.cuda.Event() for _ in range(K)]
+    order = ("logits", "x", "dy")  # in the order the step reads them
+    h2d_done = [{n: torch.cuda.Event() for n in order} for _ in range(K)]
+    fwd_done = [torch.cuda.Event() for _ in range(K)]
     comp_done = [torch.cuda.Event() for _ in range(K)]
     d2h_done = [torch.cuda.Event() for _ in range(K)]
     e2e_start, e2e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
     def copy_in(i):
         with torch.cuda.stream(s_h2d):
-            for n in ("x", "dy", "logits"):
+            for n in order:
                 ins[i % 2][n].copy_(pin[n], non_blocking=True)
-            h2d_done[i].record(s_h2d)
+                h2d_done[i][n].record(s_h2d)
 
     torch.cuda.synchronize()
     e2e_start.record(s_h2d)
     copy_in(0)
     for i in range(K):
         b_in, b_out = ins[i % 2], outs[i % 2]
-        stream.wait_event(h2d_done[i])
         if i >= 2:
             stream.wait_event(d2h_done[i - 2])  # step i-2's results have left this buffer
         with torch.cuda.stream(stream):
+            # each phase waits only for the input it reads: the first step's dy (and x)
+            # still arriving while its route (and forward) run
+            stream.wait_event(h2d_done[i]["logits"])
             layer.route(b_in["logits"], stream)
+            stream.wait_event(h2d_done[i]["x"])
             layer.forward(b_in["x"], d["W_gate"], d["W_up"], d["W_down"], out=b_out["out"], stream=stream)
+            fwd_done[i].record(stream)
+            stream.wait_event(h2d_done[i]["dy"])
             g = dict(grads, dx=b_out["dx"], d_logits=b_out["d_logits"], d_topk_w=b_out["d_topk_w"])
             layer.backward(b_in["dy"], b_in["x"], d["W_gate"], d["W_up"], d["W_down"], grads=g, stream=stream)
             comp_done[i].record(stream)
@@ -480,8 +488,9 @@ def run_ours(args):
                 s_h2d.wait_event(comp_done[i - 1])  # step i-1 is done reading the other input buffer
             copy_in(i + 1)
         with torch.cuda.stream(s_d2h):
-            s_d2h.wait_event(comp_done[i])
+            s_d2h.wait_event(fwd_done[i])  # out leaves while the step's backward runs
             host_out.copy_(b_out["out"], non_blocking=True)
+            s_d2h.wait_event(comp_done[i])
             host_dx.copy_(b_out["dx"], non_blocking=True)
             host_dl.copy_(b_out["d_logits"], non_blocking=True)
             d2h_done[i].record(s_d2h)
@@ -618,7 +627,8 @@ def run_ours(args):
         "e2e": {"value": world_tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "pipeline": "K steps; inputs copied in on one stream, results out on another, "
-                            "double-buffered around the compute stream; no L2 flush (inputs exceed L2)"},
+                            "double-buffered around the compute stream (each phase waits for the inputs "
+                            "it reads; out leaves after the forward); no L2 flush (inputs exceed L2)"},
         "gpu_launches": launches_in_timed_region(labels, KH, K), "clocks": clk.summary(),
         "router_projection": router_ms,
     }
