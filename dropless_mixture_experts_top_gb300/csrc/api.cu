@@ -447,7 +447,7 @@ moe_status forward_mx(const Mx8Fwd &f, cudaStream_t s) {
   }));
   if (f.keep)  // the backward's dW_gate/up operand: x along tokens, gathered from x by token
     MOE_TRY(timed("mx_quantT_x", s, [&] {
-      return launch_quant_cols(f.x, H, Mp, off, pad_off, E, f.x_t, f.x_t_sf, sf_a(H), RowCodes{}, s,
+      return launch_quant_cols(f.x, H, Mp, off, pad_off, E, f.x_t, f.x_t_sf, sf_a(H), s,
                                f.r->slot_of_row, k);
     }));
   // each weight read once: along H for GEMM1 (transposed, interleaved) and
@@ -579,7 +579,7 @@ moe_status forward_impl(FwdKind kind, const moe_config *cfg, const void *x, cons
       MOE_TRY(timed("mx_pad_offsets_fwd", s, [&] { return launch_pad_offsets(r->offsets, cfg->E, pad_off, s); }));
       MOE_TRY(timed("permute_rows_quantT_x", s, [&] {
         return launch_quant_cols(static_cast<const uint16_t *>(x), H, static_cast<int>(L.q.m_pad), r->offsets,
-                                 pad_off, cfg->E, sv + L.q.x_t, sv + L.q.x_t_sf, sf_a(H), RowCodes{}, s,
+                                 pad_off, cfg->E, sv + L.q.x_t, sv + L.q.x_t_sf, sf_a(H), s,
                                  r->slot_of_row, k, x_perm);
       }));
     } else {

@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(kWarps * 32) permute_quant_kernel(
   for (int v0 = 0; v0 < nv; v0 += 32 * kVecPerLane) {
     uint4 buf[kVecPerLane];
     uint2 q[kVecPerLane];
-    uint8_t scode[kVecPerLane];
+    uint32_t sfw[kVecPerLane];
 #pragma unroll
     for (int u = 0; u < kVecPerLane; ++u) {
       const int v = v0 + u * 32 + lane;
@@ -118,20 +118,26 @@ __global__ void __launch_bounds__(kWarps * 32) permute_quant_kernel(
       const float s = pow2_neg(X);
       q[u] = make_uint2(pack_e4m3x4_scaled(f[0], f[1], f[2], f[3], s),
                         pack_e4m3x4_scaled(f[4], f[5], f[6], f[7], s));
-      scode[u] = static_cast<uint8_t>(X + 127);
+      // the four scale codes of K blocks (v >> 2) .. + 3, one atom word, gathered in
+      // lanes 0 and 16 (K blocks 8u + 4 (lane / 16) ..; H % 128 == 0, so a word is
+      // whole when its first block is inside the row)
+      const uint32_t c = static_cast<uint32_t>(X + 127);
+      sfw[u] = c | (__shfl_down_sync(0xffffffffu, c, 4) << 8) | (__shfl_down_sync(0xffffffffu, c, 8) << 16) |
+               (__shfl_down_sync(0xffffffffu, c, 12) << 24);
     }
     for (int j = 0; j < k; ++j) {
       const int row = __shfl_sync(0xffffffffu, myrow, j);
       const int prow = __shfl_sync(0xffffffffu, myprow, j);
       uint4 *dst = xp + static_cast<size_t>(row) * nv;
       uint2 *cdst = reinterpret_cast<uint2 *>(codes + static_cast<size_t>(prow) * H);
+      uint8_t *rsf = sf + atom_row_sg<128>(0, prow, H, L.seg);  // one segment, groups of 128
 #pragma unroll
       for (int u = 0; u < kVecPerLane; ++u) {
         const int v = v0 + u * 32 + lane;
         if (v < nv) {
           if (xp) dst[v] = buf[u];
           cdst[v] = q[u];
-          if ((lane & 3) == 0) sf[atom_byte(prow, v >> 2, H, L)] = scode[u];
+          if ((lane & 15) == 0) *reinterpret_cast<uint32_t *>(rsf + atom_kblock(v >> 2)) = sfw[u];
         }
       }
     }
@@ -328,6 +334,7 @@ cudaError_t launch_sum_segments(const float *parts, int S, int64_t n, float *out
 cudaError_t launch_permute_quant(const uint16_t *x, const int32_t *row_of_slot, const int32_t *topk_idx,
                                  const int32_t *offsets, const int32_t *pad_off, uint16_t *x_perm,
                                  uint8_t *codes, uint8_t *sf, SfLayout L, int T, int H, int k, cudaStream_t s) {
+  if (L.group != 128 || H % 128 != 0) return cudaErrorInvalidValue;  // padded rows in one segment (L.seg)
   return launch_pdl(permute_quant_kernel, dim3(blocks_for(T)), dim3(kWarps * 32), 0, s, 1,
                     reinterpret_cast<const uint4 *>(x), row_of_slot, topk_idx, offsets, pad_off,
                     reinterpret_cast<uint4 *>(x_perm), codes, sf, L, T, H / 8, k);

@@ -177,25 +177,28 @@ inline size_t sf_layout_bytes(size_t rows, size_t K, SfLayout L) {
 }
 // pad_off[e] = sum over e' < e of ceil(count/128)*128
 cudaError_t launch_pad_offsets(const int32_t *offsets, int E, int32_t *pad_off, cudaStream_t s);
-// along tokens: [M, C] permuted rows -> codes [C, Mpad] (padded token axis; or
-// none, codes == nullptr); with rows.codes set, also along C into the padded
-// row space: codes [Mpad, C]
+// Codes and scales of an operand quantised row by row (along its columns).
 struct RowCodes {
   uint8_t *codes, *sf;
   SfLayout L;
 };
-// With slot_of_row set, src is token-major ([T, C]) and permuted row r reads
-// token slot_of_row[r] / k; with xp set, the permuted rows are also written in
-// bf16 to xp [M, C] (a permute fused with the quantisation).
+// along tokens: [M, C] permuted rows -> codes [C, Mpad] (padded token axis;
+// scales in one segment, groups of 128: L.seg >= C, L.group == 128; or none,
+// codes == nullptr).  With slot_of_row set, src is token-major ([T, C]) and
+// permuted row r reads token slot_of_row[r] / k; with xp set, the permuted
+// rows are also written in bf16 to xp [M, C] (a permute fused with the
+// quantisation).  Other layouts: cudaErrorInvalidValue.
 cudaError_t launch_quant_cols(const uint16_t *src, int C, int Mpad, const int32_t *offsets,
                               const int32_t *pad_off, int E, uint8_t *codes, uint8_t *sf, SfLayout L,
-                              RowCodes rows, cudaStream_t s, const int32_t *slot_of_row = nullptr, int k = 1,
+                              cudaStream_t s, const int32_t *slot_of_row = nullptr, int k = 1,
                               uint16_t *xp = nullptr);
 
 // The MXFP8 backward's one pass over dy: dy rows gathered by token for every
 // permuted row, quantised along H into the padded row space (rows) and along
 // tokens (codes_t [H, Mpad]), and g = <dy_t, Y_r> in col_blocks partial sums per
-// row (g_part [M][col_blocks], added in order by launch_router_grad).
+// row (g_part [M][col_blocks], added in order by launch_router_grad).  Both
+// scale layouts are one segment: Lt grouped by kMxBN, rows.L by 128; other
+// layouts: cudaErrorInvalidValue.
 cudaError_t launch_dy_quant(const uint16_t *dy, const uint16_t *Y, const int32_t *slot_of_row, int k, int H,
                             int Mpad, const int32_t *offsets, const int32_t *pad_off, int E, uint8_t *codes_t,
                             uint8_t *sf_t, SfLayout Lt, RowCodes rows, float *g_part, int col_blocks,
@@ -203,8 +206,9 @@ cudaError_t launch_dy_quant(const uint16_t *dy, const uint16_t *Y, const int32_t
 int dy_quant_col_blocks(int H);  // column blocks of that pass (its partials per row)
 
 // mxfp8 forward: the permute with x quantised along H fused (codes and scales
-// to the padded row of every permuted row; H % 128 == 0), and zero codes and
-// scales for the padded rows past each expert's count
+// to the padded row of every permuted row; H % 128 == 0; scales of the padded
+// rows in one segment of L.seg rows, groups of 128, else cudaErrorInvalidValue),
+// and zero codes and scales for the padded rows past each expert's count
 cudaError_t launch_permute_quant(const uint16_t *x, const int32_t *row_of_slot, const int32_t *topk_idx,
                                  const int32_t *offsets, const int32_t *pad_off, uint16_t *x_perm,
                                  uint8_t *codes, uint8_t *sf, SfLayout L, int T, int H, int k, cudaStream_t s);
@@ -214,7 +218,9 @@ cudaError_t launch_zero_pad_rows(const int32_t *offsets, const int32_t *pad_off,
 // Weights [E, R, C] quantised along R (R % 128 == 0, C % 64 == 0), transposed:
 // codes [E * C, R] (interleave 0) or the gate|up interleave of the mxfp8 GEMM1
 // (interleave 1, codes [E * 2C, R]: row e*2C + (c/32)*64 + half*32 + c%32);
-// with rows.codes set, also along C row by row: codes [E * R, C].
+// with rows.codes set, also along C row by row: codes [E * R, C].  Scales
+// grouped by kMxBN in per-expert segments (L.seg = 2C or C, rows.L.seg = R);
+// other layouts: cudaErrorInvalidValue.
 cudaError_t launch_quant_wT(const uint16_t *W, int E, int R, int C, int interleave, int half,
                             uint8_t *codes, uint8_t *sf, SfLayout L, RowCodes rows, cudaStream_t s);
 

@@ -42,32 +42,37 @@ __device__ __forceinline__ int expert_of(int o, const int *s_pad, int E) {
   return lo;
 }
 
-// Token-axis quantisation, output transposed: codes [C][Mpad] (tokens
-// contiguous).  A block takes 128 padded rows (one expert's, as segments are
-// 128-aligned) and walks their columns in 64-wide tiles.  The tiles are staged
-// in shared memory by cp.async, kQcRing of them in flight (16-byte chunks
-// XOR-swizzled by row, so that both a column walk and a row walk are free of
-// bank conflicts); one thread per (column, 32-token block) quantises down the
-// column into a shared output tile (64 rows of 128 codes, rows padded to 144
-// bytes against bank conflicts), which leaves as full 128-byte rows.
-// Optionally the same tile is also quantised along its rows (one thread per
-// (row, 32-column block)) into the padded row space, so an operand needed on
-// both axes is read once; the rows may be gathered from a token-major source
-// (permuted row r reads token slot_of_row[r] / k) instead of read from a
-// permuted copy, and the gathered rows may be written out in bf16 as well (the
-// permuted copy itself, xp).  Tiles past the padded total are skipped.
+// The transposing quantisers stage 128 x 64 bf16 tiles in shared memory by
+// cp.async (16-byte chunks XOR-swizzled by row, so that both a column walk and
+// a row walk are free of bank conflicts), several tiles in flight per block.
+// Along the tiles' columns one thread per (column, 32-row block) quantises
+// down the column into a shared output tile (64 rows of 128 codes, rows padded
+// to 144 bytes against bank conflicts), which leaves as full 128-byte rows:
+// the codes of an operand whose reduction axis is the tiles' row axis, written
+// transposed.  Along the rows one thread per (row, 32-column block) quantises
+// straight from the staged tile.  Every address a thread uses is fixed up to
+// the tile's column offset, so it is computed once per block: a thread stages
+// 16-byte piece (tid mod 8) of rows tid/8 + 32 j of each tile (absent rows
+// zero-filled by the copy itself), reads row tid/2 in the row pass and column
+// tid mod 64 in the column pass, and stores 16-byte piece (tid mod 8) of output
+// rows tid/8 + 32 j.
 constexpr int kQcRows = 128, kQcCols = 64, kQcThreads = 256;
-constexpr int kQcRing = 4;                         // staged tiles in flight per block
-constexpr int kQcTileElems = kQcRows * kQcCols;   // bf16 per staged tile (16 KB)
-constexpr int kQcOutStride = kQcRows + 16;         // bytes per output row in shared memory
-constexpr int kQcSmem = kQcRing * kQcTileElems * 2 + kQcCols * kQcOutStride;  // dynamic shared memory
-constexpr int kQcLoads = (kQcRows * kQcCols / 8) / kQcThreads;  // 16-byte pieces per thread per tile
+constexpr int kQcRing = 4;                                  // staged tiles in flight per block
+constexpr int kQcTileElems = kQcRows * kQcCols;             // bf16 per staged tile
+constexpr int kQcTileBytes = kQcTileElems * 2;              // 16 KB
+constexpr int kQcOutStride = kQcRows + 16;                  // bytes per output row in shared memory
+constexpr int kQcSmem = kQcRing * kQcTileBytes + kQcCols * kQcOutStride;  // dynamic shared memory
+constexpr int kQcLoads = (kQcRows * kQcCols / 8) / kQcThreads;   // 16-byte pieces staged per thread per tile
+constexpr int kQcStores = (kQcCols * kQcRows / 16) / kQcThreads;  // 16-byte code pieces stored per thread per tile
+static_assert(kQcLoads == 4 && kQcStores == 2, "thread shares assume 256 threads and 128 x 64 tiles");
 
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem)), "l"(gmem) : "memory");
+// 16-byte cp.async; with src_bytes 0 nothing is read and the 16 bytes are zeroed.
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void *gmem, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(saddr), "l"(gmem), "r"(src_bytes)
+               : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// Wait until at most n of this thread's cp.async groups are still pending (n < kQcRing).
+// Wait until at most n of this thread's cp.async groups are still pending (n < 4).
 __device__ __forceinline__ void cp_async_wait_pending(int n) {
   if (n <= 0)
     asm volatile("cp.async.wait_group 0;" ::: "memory");
@@ -79,26 +84,35 @@ __device__ __forceinline__ void cp_async_wait_pending(int n) {
     asm volatile("cp.async.wait_group 3;" ::: "memory");
 }
 
-// Element (r, c) of a staged tile.
-__device__ __forceinline__ int qc_idx(int r, int c) { return r * kQcCols + (((c >> 3) ^ (r & 7)) << 3) + (c & 7); }
-
-// Issue one 128 x 64 tile: source row r at row_ptr(r) (nullptr: a zero row),
-// columns c0 .. c0 + 63; one cp.async group per call.
+// A thread's share of staging a tile: row tid/8 + 32 j (j < 4) of the source
+// starts at src[j] (its piece's column offset included), or is absent
+// (bytes[j] = 0: zero-filled, src[j] any readable address).
+struct QcStage {
+  const uint16_t *src[kQcLoads];
+  uint32_t bytes[kQcLoads];
+  uint32_t soff;  // byte offset of the thread's piece of row tid/8 in a tile
+};
 template <class RowPtr>
-__device__ __forceinline__ void qc_issue(uint16_t *dst, int c0, const RowPtr &row_ptr, bool commit = true) {
+__device__ __forceinline__ QcStage qc_stage_plan(const RowPtr &row_ptr, const uint16_t *readable) {
+  QcStage p;
+  const int lr = threadIdx.x >> 3, part = threadIdx.x & 7;
+  p.soff = static_cast<uint32_t>(lr * kQcCols + ((part ^ (lr & 7)) << 3)) * 2;
 #pragma unroll
   for (int j = 0; j < kQcLoads; ++j) {
-    const int i = threadIdx.x + j * kQcThreads;
-    const int r = i >> 3, part = i & 7;
-    uint16_t *d = dst + r * kQcCols + ((part ^ (r & 7)) << 3);
-    const uint16_t *sp = row_ptr(r);
-    if (sp)
-      cp_async16(d, sp + c0 + part * 8);
-    else
-      *reinterpret_cast<uint4 *>(d) = make_uint4(0, 0, 0, 0);
+    const uint16_t *s = row_ptr(lr + 32 * j);  // nullptr: absent row
+    p.src[j] = (s ? s : readable) + part * 8;
+    p.bytes[j] = s ? 16u : 0u;
   }
-  if (commit) cp_async_commit();
+  return p;
 }
+// Issue the thread's copies of columns c0 .. c0 + 63 into the tile at shared address tile.
+__device__ __forceinline__ void qc_stage(const QcStage &p, uint32_t tile, int c0) {
+#pragma unroll
+  for (int j = 0; j < kQcLoads; ++j) cp_async16(tile + p.soff + j * (32 * kQcCols * 2), p.src[j] + c0, p.bytes[j]);
+}
+
+// Element (r, c) of a staged tile.
+__device__ __forceinline__ int qc_idx(int r, int c) { return r * kQcCols + (((c >> 3) ^ (r & 7)) << 3) + (c & 7); }
 
 // 32 bf16 values of a staged tile: row r, columns 32 bb .. 32 bb + 31.
 __device__ __forceinline__ void qc_row32(const uint16_t *tile, int r, int bb, float (&v)[32]) {
@@ -120,37 +134,56 @@ __device__ __forceinline__ void qc_col32(const uint16_t *tile, int c, int b, flo
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(static_cast<uint32_t>(tile[qc_idx(32 * b + i, c)]) << 16);
 }
 
-// The column-tile walk shared by both transposing quantisers: tiles c0 =
-// first, first + step, ... < C, kQcRing - 1 of them issued ahead; work(tile,
-// c0) runs on each once it has landed, between two block barriers.
-template <class RowPtr, class Work>
-__device__ __forceinline__ void qc_walk(uint16_t *ring, int first, int step, int C, const RowPtr &row_ptr,
-                                        const Work &work) {
+// The column-tile walk shared by the transposing quantisers: tiles c0 = first,
+// first + step, ... < C through a ring of kRing slots of slot_bytes, kRing - 1
+// issued ahead; stage(slot address, c0) issues one tile's copies (one group);
+// work(slot, c0) runs once the tile has landed, after a block barrier.  A slot
+// is staged again at the top of the iteration after the one that read it, so
+// work must finish its reads of the slot before a block barrier of its own,
+// or ask for a trailing barrier (trail).
+template <int kRing, class Stage, class Work>
+__device__ __forceinline__ void qc_walk(uint8_t *ring, int slot_bytes, int first, int step, int C, bool trail,
+                                        const Stage &stage, const Work &work) {
   const int nt = first < C ? (C - first + step - 1) / step : 0;
-  for (int i = 0; i < kQcRing - 1 && i < nt; ++i) qc_issue(ring + i * kQcTileElems, first + i * step, row_ptr);
+  const uint32_t ring_s = smem_addr(ring);
+  for (int i = 0; i < kRing - 1 && i < nt; ++i) {
+    stage(ring_s + i * slot_bytes, first + i * step);
+    cp_async_commit();
+  }
+  int slot = 0;
   for (int it = 0; it < nt; ++it) {
-    const int ahead = it + kQcRing - 1;
-    if (ahead < nt) qc_issue(ring + (ahead % kQcRing) * kQcTileElems, first + ahead * step, row_ptr);
+    const int ahead = it + kRing - 1;
+    if (ahead < nt) {  // into the slot read in the previous iteration
+      stage(ring_s + (slot == 0 ? kRing - 1 : slot - 1) * slot_bytes, first + ahead * step);
+      cp_async_commit();
+    }
     cp_async_wait_pending(min(nt - 1, ahead) - it);  // this tile's group has landed
     __syncthreads();
-    work(ring + (it % kQcRing) * kQcTileElems, first + it * step);
-    __syncthreads();  // the tile's slot and the output tile are reused
+    work(ring + slot * slot_bytes, first + it * step);
+    if (trail) __syncthreads();
+    slot = slot + 1 == kRing ? 0 : slot + 1;
   }
 }
 
+// Token-axis quantisation, output transposed: codes [C][Mpad] (tokens
+// contiguous), scales grouped by 128 (one segment: L.seg >= C).  A block takes
+// 128 padded rows (one expert's, as segments are 128-aligned) and walks their
+// columns; the rows may be gathered from a token-major source (permuted row r
+// reads token slot_of_row[r] / k) instead of read from a permuted copy, and
+// the gathered rows may be written out in bf16 as well (the permuted copy
+// itself, xp); codes may be null (xp only).  Tiles past the padded total are
+// skipped.
 __global__ void __launch_bounds__(kQcThreads, 3) quant_cols_kernel(const uint16_t *__restrict__ src, int C,
                                                                 int Mpad,
                                                                 const int32_t *__restrict__ offsets,
                                                                 const int32_t *__restrict__ pad_off, int E,
                                                                 uint8_t *__restrict__ codes,
-                                                                uint8_t *__restrict__ sf, SfLayout L,
-                                                                RowCodes rows,
+                                                                uint8_t *__restrict__ sf,
                                                                 const int32_t *__restrict__ slot_of_row, int k,
                                                                 uint16_t *__restrict__ xp) {
   griddep_wait();  // the previous kernel in the stream has completed
   extern __shared__ __align__(16) uint8_t qc_smem[];
-  uint16_t *ring = reinterpret_cast<uint16_t *>(qc_smem);
-  uint8_t *otile = qc_smem + kQcRing * kQcTileElems * 2;
+  uint8_t *otile = qc_smem + kQcRing * kQcTileBytes;
   __shared__ int s_pad[kMaxExperts + 1];
   __shared__ int s_seg[3];  // first source row, valid rows of this tile, skip flag
   const int prow0 = blockIdx.x * kQcRows;
@@ -175,45 +208,39 @@ __global__ void __launch_bounds__(kQcThreads, 3) quant_cols_kernel(const uint16_
   for (int r = threadIdx.x; r < nvalid; r += kQcThreads)
     s_src[r] = slot_of_row ? __ldg(slot_of_row + row0 + r) / k : row0 + r;
   __syncthreads();
-  auto row_ptr = [&](int r) -> const uint16_t * {
-    return r < nvalid ? src + static_cast<size_t>(s_src[r]) * C : nullptr;
-  };
-  qc_walk(ring, blockIdx.y * kQcCols, gridDim.y * kQcCols, C, row_ptr, [&](const uint16_t *tile, int c0) {
-    if (xp) {  // the staged rows in bf16: 16-byte pieces, 128 bytes per row
+  const QcStage ld = qc_stage_plan(
+      [&](int r) -> const uint16_t * { return r < nvalid ? src + static_cast<size_t>(s_src[r]) * C : nullptr; }, src);
+  const int lr = threadIdx.x >> 3, part = threadIdx.x & 7;  // staged pieces (and xp's)
+  uint16_t *xrow = xp ? xp + static_cast<size_t>(row0 + lr) * C + part * 8 : nullptr;
+  const int cc = threadIdx.x % kQcCols, b = threadIdx.x / kQcCols;  // column pass: column, 32-token block
+  uint8_t *csf = sf + atom_kblock((prow0 >> 5) + b);
+  uint8_t *obase = codes ? codes + static_cast<size_t>(lr) * Mpad + prow0 + part * 16 : nullptr;
+  const uint8_t *osrc = otile + lr * kQcOutStride + part * 16;
+  qc_walk<kQcRing>(
+      qc_smem, kQcTileBytes, blockIdx.y * kQcCols, gridDim.y * kQcCols, C, codes == nullptr,
+      [&](uint32_t tile, int c0) { qc_stage(ld, tile, c0); },
+      [&](const uint8_t *slot, int c0) {
+        const uint16_t *tile = reinterpret_cast<const uint16_t *>(slot);
+        if (xp) {  // the staged rows in bf16: 16-byte pieces, 128 bytes per row
 #pragma unroll
-      for (int j = 0; j < kQcLoads; ++j) {
-        const int i = threadIdx.x + j * kQcThreads;
-        const int r = i >> 3, part = i & 7;
-        if (r < nvalid)
-          *reinterpret_cast<uint4 *>(xp + static_cast<size_t>(row0 + r) * C + c0 + part * 8) =
-              *reinterpret_cast<const uint4 *>(tile + r * kQcCols + ((part ^ (r & 7)) << 3));
-      }
-    }
-    if (rows.codes) {  // along the rows: thread = (row, 32-column block); zero rows past the count
-      const int r = threadIdx.x >> 1, bb = threadIdx.x & 1;
-      float v[32];
-      qc_row32(tile, r, bb, v);
-      const int prow = prow0 + r, kb = (c0 >> 5) + bb;
-      rows.sf[atom_byte(prow, kb, C, rows.L)] =
-          quant32(v, reinterpret_cast<uint4 *>(rows.codes + static_cast<size_t>(prow) * C + c0 + 32 * bb));
-    }
-    if (codes) {  // along the tokens, transposed
-      const int cc = threadIdx.x % kQcCols, b = threadIdx.x / kQcCols;  // 4 blocks of 32 tokens
-      float v[32];
-      qc_col32(tile, cc, b, v);
-      const size_t srow = L.group == 128 ? atom_row<128>(c0 + cc, Mpad, L) : atom_row(c0 + cc, Mpad, L);
-      sf[srow + atom_kblock((prow0 >> 5) + b)] =
-          quant32(v, reinterpret_cast<uint4 *>(otile + cc * kQcOutStride + 32 * b));
-      __syncthreads();
+          for (int j = 0; j < kQcLoads; ++j)
+            if (lr + 32 * j < nvalid)
+              *reinterpret_cast<uint4 *>(xrow + static_cast<size_t>(32 * j) * C + c0) =
+                  *reinterpret_cast<const uint4 *>(slot + ld.soff + j * (32 * kQcCols * 2));
+        }
+        if (codes) {  // along the tokens, transposed
+          float v[32];
+          qc_col32(tile, cc, b, v);
+          csf[atom_row_sg<128>(0, c0 + cc, Mpad, C)] =
+              quant32(v, reinterpret_cast<uint4 *>(otile + cc * kQcOutStride + 32 * b));
+          __syncthreads();  // the output tile is complete; the staged tile is no longer read
+          uint8_t *o = obase + static_cast<size_t>(c0) * Mpad;
 #pragma unroll
-      for (int j = 0; j < (kQcCols * kQcRows / 16) / kQcThreads; ++j) {
-        const int i = threadIdx.x + j * kQcThreads;
-        const int r = i >> 3, part = i & 7;  // output row (column c0 + r), 16-byte piece
-        *reinterpret_cast<uint4 *>(codes + static_cast<size_t>(c0 + r) * Mpad + prow0 + part * 16) =
-            *reinterpret_cast<const uint4 *>(otile + r * kQcOutStride + part * 16);
-      }
-    }
-  });
+          for (int j = 0; j < kQcStores; ++j)
+            *reinterpret_cast<uint4 *>(o + static_cast<size_t>(32 * j) * Mpad) =
+                *reinterpret_cast<const uint4 *>(osrc + 32 * j * kQcOutStride);
+        }
+      });
 }
 
 // The MXFP8 backward's pass over dy (one read, no bf16 copy): for 128 padded
@@ -221,25 +248,28 @@ __global__ void __launch_bounds__(kQcThreads, 3) quant_cols_kernel(const uint16_
 // permuted rows come from (gathered by token: slot_of_row / k) and the same
 // rows of Y are staged by cp.async, kDyRing tiles of each in flight.  Each
 // tile is quantised along H (thread = row, 32-column block; into the padded
-// row space: dA's A operand) and along tokens (thread = column, 32-token
-// block; transposed: dW_down's B operand), and every row accumulates its part
-// of g = <dy_t, Y_r> over the block's columns; the part of block column
-// y of row r goes to g_part[r * gridDim.y + y], added in order by the router
-// gradient kernel.  The transposed codes' scale rows are grouped by kMxBN.
-constexpr int kDyRing = 3;
-constexpr int kDySmem = kDyRing * 2 * kQcTileElems * 2 + kQcCols * kQcOutStride;
+// row space, scales grouped by 128 in one segment: dA's A operand) and along
+// tokens (thread = column, 32-token block; transposed, scales grouped by kMxBN
+// in one segment: dW_down's B operand), and every row accumulates its part of
+// g = <dy_t, Y_r> over the block's columns; the part of block column y of row
+// r goes to g_part[r * gridDim.y + y], added in order by the router gradient
+// kernel.  Two tile pairs in a ring (one in flight while the other is
+// quantised) keep the block at 73 KB and 80 registers, three blocks per SM:
+// measured faster than three pairs at two blocks per SM.
+constexpr int kDyRing = 2;
+constexpr int kDySmem = kDyRing * 2 * kQcTileBytes + kQcCols * kQcOutStride;
 
-__global__ void __launch_bounds__(kQcThreads, 2) dy_quant_kernel(const uint16_t *__restrict__ dy,
+__global__ void __launch_bounds__(kQcThreads, 3) dy_quant_kernel(const uint16_t *__restrict__ dy,
                                                                  const uint16_t *__restrict__ Y,
                                                                  const int32_t *__restrict__ slot_of_row, int k,
                                                                  int H, int Mpad, const int32_t *__restrict__ offsets,
                                                                  const int32_t *__restrict__ pad_off, int E,
                                                                  uint8_t *__restrict__ codes_t, uint8_t *__restrict__ sf_t,
-                                                                 SfLayout Lt, RowCodes rows, float *__restrict__ g_part) {
+                                                                 uint8_t *__restrict__ codes, uint8_t *__restrict__ sf,
+                                                                 float *__restrict__ g_part) {
   griddep_wait();  // the previous kernel in the stream has completed
   extern __shared__ __align__(16) uint8_t qc_smem[];
-  uint16_t *ring = reinterpret_cast<uint16_t *>(qc_smem);  // [kDyRing][dy tile | Y tile]
-  uint8_t *otile = qc_smem + kDyRing * 2 * kQcTileElems * 2;
+  uint8_t *otile = qc_smem + kDyRing * 2 * kQcTileBytes;
   __shared__ int s_pad[kMaxExperts + 1];
   __shared__ int s_seg[3];  // first source row, valid rows of this tile, skip flag
   __shared__ int s_tok[kQcRows];
@@ -263,53 +293,46 @@ __global__ void __launch_bounds__(kQcThreads, 2) dy_quant_kernel(const uint16_t 
   const int row0 = s_seg[0], nvalid = s_seg[1];
   for (int r = threadIdx.x; r < nvalid; r += kQcThreads) s_tok[r] = __ldg(slot_of_row + row0 + r) / k;
   __syncthreads();
-  auto dy_ptr = [&](int r) -> const uint16_t * {
-    return r < nvalid ? dy + static_cast<size_t>(s_tok[r]) * H : nullptr;
-  };
-  auto y_ptr = [&](int r) -> const uint16_t * { return r < nvalid ? Y + static_cast<size_t>(row0 + r) * H : nullptr; };
-  const int first = blockIdx.y * kQcCols, step = gridDim.y * kQcCols;
-  const int nt = first < H ? (H - first + step - 1) / step : 0;
-  auto issue = [&](int i) {
-    uint16_t *slot = ring + (i % kDyRing) * 2 * kQcTileElems;
-    qc_issue(slot, first + i * step, dy_ptr, false);
-    qc_issue(slot + kQcTileElems, first + i * step, y_ptr, true);  // one group per tile: both sources
-  };
+  const QcStage ldy = qc_stage_plan(
+      [&](int r) -> const uint16_t * { return r < nvalid ? dy + static_cast<size_t>(s_tok[r]) * H : nullptr; }, dy);
+  const QcStage ly = qc_stage_plan(
+      [&](int r) -> const uint16_t * { return r < nvalid ? Y + static_cast<size_t>(row0 + r) * H : nullptr; }, Y);
   const int r = threadIdx.x >> 1, bb = threadIdx.x & 1;  // row pass: row, 32-column block
-  const size_t row_sf = atom_row(prow0 + r, H, rows.L);  // its scale bytes' row
+  uint8_t *rcodes = codes + static_cast<size_t>(prow0 + r) * H + 32 * bb;
+  uint8_t *rsf = sf + atom_row_sg<128>(0, prow0 + r, H, Mpad);
+  const int cc = threadIdx.x % kQcCols, b = threadIdx.x / kQcCols;  // column pass: column, 32-token block
+  uint8_t *csf = sf_t + atom_kblock((prow0 >> 5) + b);
+  const int orow = threadIdx.x >> 3, opart = threadIdx.x & 7;  // output pieces
+  uint8_t *obase = codes_t + static_cast<size_t>(orow) * Mpad + prow0 + opart * 16;
+  const uint8_t *osrc = otile + orow * kQcOutStride + opart * 16;
   float gpart = 0.f;
-  for (int i = 0; i < kDyRing - 1 && i < nt; ++i) issue(i);
-  for (int it = 0; it < nt; ++it) {
-    const int ahead = it + kDyRing - 1;
-    if (ahead < nt) issue(ahead);
-    cp_async_wait_pending(min(nt - 1, ahead) - it);  // this tile's group has landed
-    __syncthreads();
-    const uint16_t *tile = ring + (it % kDyRing) * 2 * kQcTileElems, *ytile = tile + kQcTileElems;
-    const int c0 = first + it * step;
-    {
-      float v[32], yv[32];
-      qc_row32(tile, r, bb, v);
-      qc_row32(ytile, r, bb, yv);
+  qc_walk<kDyRing>(
+      qc_smem, 2 * kQcTileBytes, blockIdx.y * kQcCols, gridDim.y * kQcCols, H, false,
+      [&](uint32_t tile, int c0) {  // one group per tile: both sources
+        qc_stage(ldy, tile, c0);
+        qc_stage(ly, tile + kQcTileBytes, c0);
+      },
+      [&](const uint8_t *slot, int c0) {
+        const uint16_t *tile = reinterpret_cast<const uint16_t *>(slot), *ytile = tile + kQcTileElems;
+        {
+          float v[32], yv[32];
+          qc_row32(tile, r, bb, v);
+          qc_row32(ytile, r, bb, yv);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) gpart = fmaf(v[i], yv[i], gpart);
-      const int prow = prow0 + r, kb = (c0 >> 5) + bb;
-      rows.sf[row_sf + atom_kblock(kb)] =
-          quant32(v, reinterpret_cast<uint4 *>(rows.codes + static_cast<size_t>(prow) * H + c0 + 32 * bb));
-    }
-    const int cc = threadIdx.x % kQcCols, b = threadIdx.x / kQcCols;  // 4 blocks of 32 tokens
-    float v[32];
-    qc_col32(tile, cc, b, v);
-    sf_t[atom_row<kMxBN>(c0 + cc, Mpad, Lt) + atom_kblock((prow0 >> 5) + b)] =
-        quant32(v, reinterpret_cast<uint4 *>(otile + cc * kQcOutStride + 32 * b));
-    __syncthreads();
+          for (int i = 0; i < 32; ++i) gpart = fmaf(v[i], yv[i], gpart);
+          rsf[atom_kblock((c0 >> 5) + bb)] = quant32(v, reinterpret_cast<uint4 *>(rcodes + c0));
+        }
+        float v[32];
+        qc_col32(tile, cc, b, v);
+        csf[atom_row_sg<kMxBN>(0, c0 + cc, Mpad, H)] =
+            quant32(v, reinterpret_cast<uint4 *>(otile + cc * kQcOutStride + 32 * b));
+        __syncthreads();  // the output tile is complete; the staged tiles are no longer read
+        uint8_t *o = obase + static_cast<size_t>(c0) * Mpad;
 #pragma unroll
-    for (int j = 0; j < (kQcCols * kQcRows / 16) / kQcThreads; ++j) {
-      const int i = threadIdx.x + j * kQcThreads;
-      const int orow = i >> 3, part = i & 7;  // output row (column c0 + orow), 16-byte piece
-      *reinterpret_cast<uint4 *>(codes_t + static_cast<size_t>(c0 + orow) * Mpad + prow0 + part * 16) =
-          *reinterpret_cast<const uint4 *>(otile + orow * kQcOutStride + part * 16);
-    }
-    __syncthreads();  // the tile's slot and the output tile are reused
-  }
+        for (int j = 0; j < kQcStores; ++j)
+          *reinterpret_cast<uint4 *>(o + static_cast<size_t>(32 * j) * Mpad) =
+              *reinterpret_cast<const uint4 *>(osrc + 32 * j * kQcOutStride);
+      });
   gpart += __shfl_xor_sync(0xffffffffu, gpart, 1);  // the row's two 32-column halves
   if (bb == 0 && r < nvalid) g_part[static_cast<size_t>(row0 + r) * gridDim.y + blockIdx.y] = gpart;
 }
@@ -319,48 +342,56 @@ __global__ void __launch_bounds__(kQcThreads, 2) dy_quant_kernel(const uint16_t 
 // -> codes [rows, R] with output row (e, c) = e * C + c (W_down: the down
 // GEMM's B rows), or, interleaved for gate|up tiles, e * 2C + (c / 32) * 64 +
 // half * 32 + c % 32 (W_gate half 0, W_up half 1: every 64 B rows hold 32
-// gate columns then the same 32 up columns).  Optionally the same staged tile
-// is also quantised along C, row by row (the backward GEMMs' weight operand,
-// codes [E * R, C]), so each weight is read once for both.  Same staging and
-// column walk as the token-axis quantiser.
+// gate columns then the same 32 up columns); scales grouped by kMxBN in
+// segments of one expert's output rows.  Optionally the same staged tile is
+// also quantised along C, row by row (the backward GEMMs' weight operand,
+// codes [E * R, C], scales grouped by kMxBN in segments of R rows), so each
+// weight is read once for both.  A block takes 128 rows of one expert.
 __global__ void __launch_bounds__(kQcThreads, 3) quant_wT_kernel(const uint16_t *__restrict__ src, int R,
                                                                  int C, int interleave, int half,
                                                                  uint8_t *__restrict__ codes,
-                                                                 uint8_t *__restrict__ sf, SfLayout L,
-                                                                 RowCodes rows) {
+                                                                 uint8_t *__restrict__ sf, int seg,
+                                                                 uint8_t *__restrict__ rcodes_all,
+                                                                 uint8_t *__restrict__ rsf_all) {
   griddep_wait();  // the previous kernel in the stream has completed
   extern __shared__ __align__(16) uint8_t qc_smem[];
-  uint16_t *ring = reinterpret_cast<uint16_t *>(qc_smem);
-  uint8_t *otile = qc_smem + kQcRing * kQcTileElems * 2;
+  uint8_t *otile = qc_smem + kQcRing * kQcTileBytes;
   const int grow0 = blockIdx.x * kQcRows;  // first source row (of E * R)
   const int e = grow0 / R, r0 = grow0 - e * R;
-  auto out_row = [&](int c) {
-    return interleave ? e * 2 * C + (c >> 5) * 64 + half * 32 + (c & 31) : e * C + c;
-  };
-  auto row_ptr = [&](int r) -> const uint16_t * { return src + static_cast<size_t>(grow0 + r) * C; };
-  qc_walk(ring, blockIdx.y * kQcCols, gridDim.y * kQcCols, C, row_ptr, [&](const uint16_t *tile, int c0) {
-    if (rows.codes) {  // along C: thread = (row, 32-column block)
-      const int r = threadIdx.x >> 1, bb = threadIdx.x & 1;
-      float v[32];
-      qc_row32(tile, r, bb, v);
-      const int grow = grow0 + r;
-      rows.sf[atom_byte(grow, (c0 >> 5) + bb, C, rows.L)] =
-          quant32(v, reinterpret_cast<uint4 *>(rows.codes + static_cast<size_t>(grow) * C + c0 + 32 * bb));
-    }
-    const int cc = threadIdx.x % kQcCols, b = threadIdx.x / kQcCols;  // 4 blocks of 32 rows
-    float v[32];
-    qc_col32(tile, cc, b, v);
-    sf[atom_byte(out_row(c0 + cc), (r0 >> 5) + b, R, L)] =
-        quant32(v, reinterpret_cast<uint4 *>(otile + cc * kQcOutStride + 32 * b));
-    __syncthreads();
+  const QcStage ld = qc_stage_plan(
+      [&](int r) -> const uint16_t * { return src + static_cast<size_t>(grow0 + r) * C; }, src);
+  const int r = threadIdx.x >> 1, bb = threadIdx.x & 1;  // row pass: row, 32-column block
+  uint8_t *rcodes = rcodes_all ? rcodes_all + static_cast<size_t>(grow0 + r) * C + 32 * bb : nullptr;
+  uint8_t *rsf = rsf_all ? rsf_all + atom_row_sg<kMxBN>(e, r0 + r, C, R) : nullptr;
+  const int cc = threadIdx.x % kQcCols, b = threadIdx.x / kQcCols;  // column pass: column, 32-row block
+  uint8_t *csf = sf + atom_kblock((r0 >> 5) + b);
+  const int orow = threadIdx.x >> 3, opart = threadIdx.x & 7;  // output pieces
+  const uint8_t *osrc = otile + orow * kQcOutStride + opart * 16;
+  // output row of column c within the expert's segment
+  auto seg_row = [&](int c) { return interleave ? (c >> 5) * 64 + half * 32 + (c & 31) : c; };
+  qc_walk<kQcRing>(
+      qc_smem, kQcTileBytes, blockIdx.y * kQcCols, gridDim.y * kQcCols, C, false,
+      [&](uint32_t tile, int c0) { qc_stage(ld, tile, c0); },
+      [&](const uint8_t *slot, int c0) {
+        const uint16_t *tile = reinterpret_cast<const uint16_t *>(slot);
+        if (rcodes) {  // along C: thread = (row, 32-column block)
+          float v[32];
+          qc_row32(tile, r, bb, v);
+          rsf[atom_kblock((c0 >> 5) + bb)] = quant32(v, reinterpret_cast<uint4 *>(rcodes + c0));
+        }
+        float v[32];
+        qc_col32(tile, cc, b, v);
+        csf[atom_row_sg<kMxBN>(e, seg_row(c0 + cc), R, seg)] =
+            quant32(v, reinterpret_cast<uint4 *>(otile + cc * kQcOutStride + 32 * b));
+        __syncthreads();  // the output tile is complete; the staged tile is no longer read
+        // output rows c0 + orow + 32 j: (c >> 5) = (c0 >> 5) + j and c % 32 = orow, c0 being a multiple of 64
+        const size_t orow0 = static_cast<size_t>(e) * seg + seg_row(c0 + orow);
+        uint8_t *o = codes + orow0 * R + r0 + opart * 16;
+        const size_t jstride = static_cast<size_t>(interleave ? 64 : 32) * R;
 #pragma unroll
-    for (int j = 0; j < (kQcCols * kQcRows / 16) / kQcThreads; ++j) {
-      const int i = threadIdx.x + j * kQcThreads;
-      const int r = i >> 3, part = i & 7;  // output row (column c0 + r), 16-byte piece
-      *reinterpret_cast<uint4 *>(codes + static_cast<size_t>(out_row(c0 + r)) * R + r0 + part * 16) =
-          *reinterpret_cast<const uint4 *>(otile + r * kQcOutStride + part * 16);
-    }
-  });
+        for (int j = 0; j < kQcStores; ++j)
+          *reinterpret_cast<uint4 *>(o + j * jstride) = *reinterpret_cast<const uint4 *>(osrc + 32 * j * kQcOutStride);
+      });
 }
 
 // pad_off[e] = sum over e' < e of ceil(count/128)*128; pad_off[E] = padded total.
@@ -392,7 +423,8 @@ cudaError_t launch_pad_offsets(const int32_t *offsets, int E, int32_t *pad_off, 
 
 cudaError_t launch_quant_cols(const uint16_t *src, int C, int Mpad, const int32_t *offsets,
                               const int32_t *pad_off, int E, uint8_t *codes, uint8_t *sf, SfLayout L,
-                              RowCodes rows, cudaStream_t s, const int32_t *slot_of_row, int k, uint16_t *xp) {
+                              cudaStream_t s, const int32_t *slot_of_row, int k, uint16_t *xp) {
+  if (codes && (L.group != 128 || L.seg < C)) return cudaErrorInvalidValue;  // one segment, groups of 128
   const int col_blocks = C / kQcCols < 4 ? C / kQcCols : 4;  // each loops over C / (64 * 4) column tiles
   const dim3 grid(static_cast<unsigned>(Mpad / kQcRows), static_cast<unsigned>(col_blocks));
   static DeviceOnce once;  // dynamic shared memory above 48 KB, opted in once per device
@@ -401,13 +433,16 @@ cudaError_t launch_quant_cols(const uint16_t *src, int C, int Mpad, const int32_
   });
   if (e != cudaSuccess) return e;
   return launch_pdl(quant_cols_kernel, grid, dim3(kQcThreads), kQcSmem, s, 1, src, C, Mpad, offsets, pad_off, E,
-                    codes, sf, L, rows, slot_of_row, k, xp);
+                    codes, sf, slot_of_row, k, xp);
 }
 
 cudaError_t launch_dy_quant(const uint16_t *dy, const uint16_t *Y, const int32_t *slot_of_row, int k, int H,
                             int Mpad, const int32_t *offsets, const int32_t *pad_off, int E, uint8_t *codes_t,
                             uint8_t *sf_t, SfLayout Lt, RowCodes rows, float *g_part, int col_blocks,
                             cudaStream_t s) {
+  // both scale buffers in one segment: transposed grouped by kMxBN, rows by 128
+  if (Lt.group != kMxBN || Lt.seg < H || rows.L.group != 128 || rows.L.seg < Mpad || !rows.codes)
+    return cudaErrorInvalidValue;
   const dim3 grid(static_cast<unsigned>(Mpad / kQcRows), static_cast<unsigned>(col_blocks));
   static DeviceOnce once;  // dynamic shared memory above 48 KB, opted in once per device
   const cudaError_t e = once.get([](int *) {
@@ -415,13 +450,18 @@ cudaError_t launch_dy_quant(const uint16_t *dy, const uint16_t *Y, const int32_t
   });
   if (e != cudaSuccess) return e;
   return launch_pdl(dy_quant_kernel, grid, dim3(kQcThreads), kDySmem, s, 1, dy, Y, slot_of_row, k, H, Mpad, offsets,
-                    pad_off, E, codes_t, sf_t, Lt, rows, g_part);
+                    pad_off, E, codes_t, sf_t, rows.codes, rows.sf, g_part);
 }
 
 int dy_quant_col_blocks(int H) { return H / kQcCols < 4 ? H / kQcCols : 4; }
 
 cudaError_t launch_quant_wT(const uint16_t *W, int E, int R, int C, int interleave, int half,
                             uint8_t *codes, uint8_t *sf, SfLayout L, RowCodes rows, cudaStream_t s) {
+  // scales grouped by kMxBN in per-expert segments: the transposed codes' of the
+  // expert's output rows, the row codes' of its R rows
+  if (L.group != kMxBN || L.seg != (interleave ? 2 * C : C) ||
+      (rows.codes && (rows.L.group != kMxBN || rows.L.seg != R)))
+    return cudaErrorInvalidValue;
   const int col_blocks = C / kQcCols < 4 ? C / kQcCols : 4;
   const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(E) * R / kQcRows), static_cast<unsigned>(col_blocks));
   static DeviceOnce once;
@@ -429,8 +469,8 @@ cudaError_t launch_quant_wT(const uint16_t *W, int E, int R, int C, int interlea
     return cudaFuncSetAttribute(quant_wT_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQcSmem);
   });
   if (e != cudaSuccess) return e;
-  return launch_pdl(quant_wT_kernel, grid, dim3(kQcThreads), kQcSmem, s, 1, W, R, C, interleave, half, codes, sf, L,
-                    rows);
+  return launch_pdl(quant_wT_kernel, grid, dim3(kQcThreads), kQcSmem, s, 1, W, R, C, interleave, half, codes, sf,
+                    L.seg, rows.codes, rows.sf);
 }
 
 }  // namespace moe

@@ -127,6 +127,17 @@ __device__ __forceinline__ size_t atom_row(int row, int K, SfLayout L) {
 __device__ __forceinline__ size_t atom_kblock(int kblock) {
   return static_cast<size_t>(kblock >> 2) * 512 + (kblock & 3);
 }
+// atom_row<kGroup> of row r of segment sg (segments of `seg` rows), for a caller
+// that knows the segment: no division by the segment length.
+template <int kGroup>
+__device__ __forceinline__ size_t atom_row_sg(int sg, int r, int K, int seg) {
+  const int g = r / kGroup, rr = r - g * kGroup;
+  constexpr int apg = (kGroup + 127) >> 7;
+  const int gps = (seg + kGroup - 1) / kGroup;
+  const size_t rb = (static_cast<size_t>(sg) * gps + g) * apg + (rr >> 7);
+  const int w = rr & 127;
+  return rb * (K >> 7) * 512 + (w & 31) * 16 + (w >> 5) * 4;
+}
 
 // Byte of (row, K block) in a scale-atom buffer of K columns grouped by L.
 __device__ __forceinline__ size_t atom_byte(int row, int kblock, int K, SfLayout L) {
