@@ -145,22 +145,23 @@ __global__ void __launch_bounds__(kWarps * 32) permute_quant_kernel(
 }
 
 // Padded rows past each expert's count (up to the next 128-row boundary): zero
-// codes and zero scale codes.  One block per expert.
+// codes and zero scale codes.  One block per expert, a warp per row: 16-byte
+// pieces of codes, and the row's scale words (four K blocks each) at the row's
+// atom position (scales in one segment, groups of 128 rows).
 __global__ void __launch_bounds__(256) zero_pad_rows_kernel(const int32_t *__restrict__ offsets,
                                                             const int32_t *__restrict__ pad_off, int K,
                                                             uint8_t *__restrict__ codes,
-                                                            uint8_t *__restrict__ sf, SfLayout L) {
+                                                            uint8_t *__restrict__ sf, int seg) {
   griddep_wait();  // the previous kernel in the stream has completed
-  const int e = blockIdx.x;
+  const int e = blockIdx.x, lane = threadIdx.x & 31;
   const int first = __ldg(pad_off + e) + (__ldg(offsets + e + 1) - __ldg(offsets + e));
   const int end = __ldg(pad_off + e + 1);
-  const int per_row = K / 16;
-  for (int i = threadIdx.x; i < (end - first) * per_row; i += blockDim.x) {
-    const int r = first + i / per_row, c = i % per_row;
-    reinterpret_cast<uint4 *>(codes + static_cast<size_t>(r) * K)[c] = make_uint4(0, 0, 0, 0);
+  for (int r = first + (threadIdx.x >> 5); r < end; r += blockDim.x >> 5) {
+    uint4 *row = reinterpret_cast<uint4 *>(codes + static_cast<size_t>(r) * K);
+    for (int c = lane; c < K / 16; c += 32) row[c] = make_uint4(0, 0, 0, 0);
+    uint8_t *rsf = sf + atom_row_sg<128>(0, r, K, seg);
+    for (int j = lane; j < K / 128; j += 32) *reinterpret_cast<uint32_t *>(rsf + static_cast<size_t>(j) * 512) = 0u;
   }
-  for (int i = threadIdx.x; i < (end - first) * (K / 32); i += blockDim.x)
-    sf[atom_byte(first + i / (K / 32), i % (K / 32), K, L)] = 0;
 }
 
 template <bool kWeighted>
@@ -342,7 +343,8 @@ cudaError_t launch_permute_quant(const uint16_t *x, const int32_t *row_of_slot, 
 
 cudaError_t launch_zero_pad_rows(const int32_t *offsets, const int32_t *pad_off, int E, int K, uint8_t *codes,
                                  uint8_t *sf, SfLayout L, cudaStream_t s) {
-  return launch_pdl(zero_pad_rows_kernel, dim3(E), dim3(256), 0, s, 1, offsets, pad_off, K, codes, sf, L);
+  if (L.group != 128 || K % 128 != 0) return cudaErrorInvalidValue;  // padded rows in one segment (L.seg)
+  return launch_pdl(zero_pad_rows_kernel, dim3(E), dim3(256), 0, s, 1, offsets, pad_off, K, codes, sf, L.seg);
 }
 
 cudaError_t launch_router_grad(const int32_t *row_of_slot, const int32_t *topk_idx, const float *topk_w,
