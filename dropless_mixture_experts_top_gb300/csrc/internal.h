@@ -208,7 +208,7 @@ int dy_quant_col_blocks(int H);  // column blocks of that pass (its partials per
 // mxfp8 forward: the permute with x quantised along H fused (codes and scales
 // to the padded row of every permuted row; H % 128 == 0; scales of the padded
 // rows in one segment of L.seg rows, groups of 128, else cudaErrorInvalidValue),
-// and zero codes and scales for the padded rows past each expert's count (K % 128 == 0)
+// and zero codes and scales for the padded rows past each expert's count
 cudaError_t launch_permute_quant(const uint16_t *x, const int32_t *row_of_slot, const int32_t *topk_idx,
                                  const int32_t *offsets, const int32_t *pad_off, uint16_t *x_perm,
                                  uint8_t *codes, uint8_t *sf, SfLayout L, int T, int H, int k, cudaStream_t s);
