@@ -169,34 +169,53 @@ struct StageLoad {
 };
 
 // This CTA's share of one stage: 128 rows of A, 128 columns of B.
+// This CTA's rows of A in a ragged M tile: all 128 (one box), or, where the
+// expert's rows end inside them, the 32-row boxes that hold its rows (nbox of
+// them; the MMA reads the rest of the slot, whose rows are never stored).
+template <class Load>
+__device__ __forceinline__ void load_a_rows(const Load &ld, uint8_t *sa, const CUtensorMap *full,
+                                            const CUtensorMap *part, int k0, int arow, int nbox) {
+  if (nbox >= 4) {
+    ld(sa, full, k0, arow);
+  } else {
+    for (int b = 0; b < nbox; ++b) ld(sa + b * 32 * BK * 2, part, k0, arow + 32 * b);
+  }
+}
+__device__ __forceinline__ int a_boxes(const Tile &t, int rank) {
+  const int valid = t.row_end - (t.m0 + BM * rank);
+  return valid >= BM ? 4 : (valid > 0 ? (valid + 31) / 32 : 0);
+}
+
 template <int MODE, class Load>
 __device__ __forceinline__ void produce_stage(const Tile &t, int kb, int rank, uint8_t *sa,
                                               uint8_t *sb, const Load &ld, const Params &p,
                                               const CUtensorMap *a0, const CUtensorMap *a1,
-                                              const CUtensorMap *b0, const CUtensorMap *b1) {
+                                              const CUtensorMap *b0, const CUtensorMap *b1,
+                                              const CUtensorMap *a0s, const CUtensorMap *a1s) {
   const int arow = t.m0 + BM * rank;        // ragged M: this CTA's rows of A
+  const int nbox = a_boxes(t, rank);
   const int bcol = t.n0 + (BN / 2) * rank;  // this CTA's columns of B (unpaired modes)
   if constexpr (MODE == kFwdGateUp) {
-    ld(sa, a0, kb * BK, arow);
+    load_a_rows(ld, sa, a0, a0s, kb * BK, arow, nbox);
     const CUtensorMap *w = rank == 0 ? b0 : b1;  // gate columns | up columns
     const int wrow = t.e * p.H + kb * BK;
     ld(sb, w, t.n0, wrow);
     ld(sb + kBox, w, t.n0 + 64, wrow);
   } else if constexpr (MODE == kFwdDown || MODE == kRouterFwd) {
-    ld(sa, a0, kb * BK, arow);
+    load_a_rows(ld, sa, a0, a0s, kb * BK, arow, nbox);
     const int wrow = t.e * p.I + kb * BK;
     ld(sb, b0, bcol, wrow);
     ld(sb + kBox, b0, bcol + 64, wrow);
   } else if constexpr (MODE == kBwdDA || MODE == kRouterDX) {
-    ld(sa, a0, kb * BK, arow);
+    load_a_rows(ld, sa, a0, a0s, kb * BK, arow, nbox);
     ld(sb, b0, kb * BK, t.e * p.I + bcol);
   } else if constexpr (MODE == kBwdDX) {
     const int kbi = p.I / BK;
     if (kb < kbi) {
-      ld(sa, a0, kb * BK, arow);
+      load_a_rows(ld, sa, a0, a0s, kb * BK, arow, nbox);
       ld(sb, b0, kb * BK, t.e * p.H + bcol);
     } else {
-      ld(sa, a1, (kb - kbi) * BK, arow);
+      load_a_rows(ld, sa, a1, a1s, (kb - kbi) * BK, arow, nbox);
       ld(sb, b1, (kb - kbi) * BK, t.e * p.H + bcol);
     }
   } else if constexpr (MODE == kBwdDWDown || MODE == kRouterDW) {
@@ -290,7 +309,9 @@ __global__ void __launch_bounds__(threads_of(MODE, WQ), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                         const __grid_constant__ CUtensorMap tmA1,
                         const __grid_constant__ CUtensorMap tmB0,
-                        const __grid_constant__ CUtensorMap tmB1, const Params p) {
+                        const __grid_constant__ CUtensorMap tmB1,
+                        const __grid_constant__ CUtensorMap tmA0s,
+                        const __grid_constant__ CUtensorMap tmA1s, const Params p) {
   using Tr = Traits<MODE>;
   static_assert(!WQ || MODE == kFwdGateUp || MODE == kFwdDown, "weight codes come from the forward GEMMs");
   constexpr int STAGES = stages_of(MODE), HALVES = halves_of(MODE);
@@ -438,14 +459,19 @@ __global__ void __launch_bounds__(threads_of(MODE, WQ), 1)
             break;
           }
           uint8_t *sa = stages + stage * kStageBytes;
-          if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);  // both CTAs' bytes
+          if (rank == 0) {  // both CTAs' bytes
+            uint32_t bytes = 2 * kStageBytes;
+            if constexpr (!Tr::kRaggedK)
+              bytes -= HALVES * (8 - a_boxes(t, 0) - a_boxes(t, 1)) * (32 * BK * 2);
+            mbar_arrive_expect_tx(&full[stage], bytes);
+          }
           const StageLoad ld{full_cl0 + 8u * stage};
           // a K block past the end (odd count of 64-blocks) loads zero fill or rows
           // that no MMA reads, so every stage carries the same bytes
 #pragma unroll
           for (int h = 0; h < HALVES; ++h)
             produce_stage<MODE>(t, ks * HALVES + h, rank, sa + h * kABox, sa + kABytes + h * kBBox, ld,
-                                p, &tmA0, &tmA1, &tmB0, &tmB1);
+                                p, &tmA0, &tmA1, &tmB0, &tmB1, &tmA0s, &tmA1s);
           armed |= 1u << stage;
           arm_par = (arm_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -695,11 +721,12 @@ bool make_map_gu(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t rows)
 
 template <int MODE, bool WQ>
 cudaError_t launch_kernel(const CUtensorMap &mA0, const CUtensorMap &mA1, const CUtensorMap &mB0,
-                          const CUtensorMap &mB1, const Params &p, int num_sms, cudaStream_t s);
+                          const CUtensorMap &mB1, const CUtensorMap &mA0s, const CUtensorMap &mA1s,
+                          const Params &p, int num_sms, cudaStream_t s);
 
 template <int MODE>
 cudaError_t launch_mode(const GemmArgs &a, cudaStream_t s) {
-  CUtensorMap mA0, mA1, mB0, mB1;
+  CUtensorMap mA0, mA1, mB0, mB1, mA0s, mA1s;
   Params p{};
   p.M_rows = a.M_rows;
   p.H = a.H;
@@ -728,21 +755,25 @@ cudaError_t launch_mode(const GemmArgs &a, cudaStream_t s) {
   switch (MODE) {
     case kFwdGateUp:
       ok = make_map(&mA0, a.x_perm, H, M, 128) && make_map(&mB0, a.W_gate, I, E * H, 64) &&
-           make_map(&mB1, a.W_up, I, E * H, 64);
+           make_map(&mB1, a.W_up, I, E * H, 64) && make_map(&mA0s, a.x_perm, H, M, 32);
       mA1 = mA0;
+      mA1s = mA0s;
       p.kdim = a.H;
       p.n_tiles = (a.I + 127) / 128;
       break;
     case kFwdDown:
-      ok = make_map(&mA0, a.act, I, M, 128) && make_map(&mB0, a.W_down, H, E * I, 64);
+      ok = make_map(&mA0, a.act, I, M, 128) && make_map(&mB0, a.W_down, H, E * I, 64) &&
+           make_map(&mA0s, a.act, I, M, 32);
       mA1 = mA0;
+      mA1s = mA0s;
       mB1 = mB0;
       p.kdim = a.I;
       p.n_tiles = (a.H + 255) / 256;
       break;
     case kBwdDA:  // A1, B1: G and U for the epilogue's ring (32 columns x 128 rows)
       ok = make_map(&mA0, a.dy_perm, H, M, 128) && make_map(&mB0, a.W_down, H, E * I, 128) &&
-           make_map_gu(&mA1, a.G, I, M) && make_map_gu(&mB1, a.U, I, M);
+           make_map_gu(&mA1, a.G, I, M) && make_map_gu(&mB1, a.U, I, M) && make_map(&mA0s, a.dy_perm, H, M, 32);
+      mA1s = mA0s;
       p.G = a.G;
       p.U = a.U;
       p.kdim = a.H;
@@ -750,7 +781,8 @@ cudaError_t launch_mode(const GemmArgs &a, cudaStream_t s) {
       break;
     case kBwdDX:
       ok = make_map(&mA0, a.dG, I, M, 128) && make_map(&mA1, a.dU, I, M, 128) &&
-           make_map(&mB0, a.W_gate, I, E * H, 128) && make_map(&mB1, a.W_up, I, E * H, 128);
+           make_map(&mB0, a.W_gate, I, E * H, 128) && make_map(&mB1, a.W_up, I, E * H, 128) &&
+           make_map(&mA0s, a.dG, I, M, 32) && make_map(&mA1s, a.dU, I, M, 32);
       p.kdim = 2 * a.I;
       p.n_tiles = (a.H + 255) / 256;
       break;
@@ -762,15 +794,19 @@ cudaError_t launch_mode(const GemmArgs &a, cudaStream_t s) {
       p.n_tiles = (a.H + 255) / 256;
       break;
     case kRouterFwd:  // x [T,H] . W_r [H,E]: one expert, K = H, N = E
-      ok = make_map(&mA0, a.r_x, H, M, 128) && make_map(&mB0, a.r_w, E_out, H, 64);
+      ok = make_map(&mA0, a.r_x, H, M, 128) && make_map(&mB0, a.r_w, E_out, H, 64) &&
+           make_map(&mA0s, a.r_x, H, M, 32);
       mA1 = mA0;
+      mA1s = mA0s;
       mB1 = mB0;
       p.kdim = a.H;
       p.n_tiles = (a.E + 255) / 256;
       break;
     case kRouterDX:  // bf16(d_logits) [T,E] . W_r^T: K = E (zero-filled to 64s), N = H
-      ok = make_map(&mA0, a.r_dlog, E_out, M, 128) && make_map(&mB0, a.r_w, E_out, H, 128);
+      ok = make_map(&mA0, a.r_dlog, E_out, M, 128) && make_map(&mB0, a.r_w, E_out, H, 128) &&
+           make_map(&mA0s, a.r_dlog, E_out, M, 32);
       mA1 = mA0;
+      mA1s = mA0s;
       mB1 = mB0;
       p.kdim = (a.E + BK - 1) / BK * BK;
       p.n_tiles = (a.H + 255) / 256;
@@ -791,6 +827,10 @@ cudaError_t launch_mode(const GemmArgs &a, cudaStream_t s) {
       break;
   }
   if (!ok) return cudaErrorInvalidValue;
+  if constexpr (Traits<MODE>::kRaggedK) {  // whole K blocks: no partial A boxes
+    mA0s = mA0;
+    mA1s = mA1;
+  }
   if constexpr (Traits<MODE>::kRaggedK) {
     if (!a.map_scratch) return cudaErrorInvalidValue;
     MapTemplates tm;
@@ -812,17 +852,18 @@ cudaError_t launch_mode(const GemmArgs &a, cudaStream_t s) {
     p.wq_sf[1] = a.wq_sf[1];
     if (a.wq[0]) {  // the variant with weight quantisers
       if (!a.wq_sf[0] || (MODE == kFwdGateUp && (!a.wq[1] || !a.wq_sf[1]))) return cudaErrorInvalidValue;
-      return launch_kernel<MODE, true>(mA0, mA1, mB0, mB1, p, a.num_sms, s);
+      return launch_kernel<MODE, true>(mA0, mA1, mB0, mB1, mA0s, mA1s, p, a.num_sms, s);
     }
   }
-  return launch_kernel<MODE, false>(mA0, mA1, mB0, mB1, p, a.num_sms, s);
+  return launch_kernel<MODE, false>(mA0, mA1, mB0, mB1, mA0s, mA1s, p, a.num_sms, s);
 }
 
 // One launch of a grouped GEMM kernel: clusters of two CTAs, as many pairs as
 // fit at once (at most one per two SMs).
 template <int MODE, bool WQ>
 cudaError_t launch_kernel(const CUtensorMap &mA0, const CUtensorMap &mA1, const CUtensorMap &mB0,
-                          const CUtensorMap &mB1, const Params &p, int num_sms, cudaStream_t s) {
+                          const CUtensorMap &mB1, const CUtensorMap &mA0s, const CUtensorMap &mA1s,
+                          const Params &p, int num_sms, cudaStream_t s) {
   // once per device: the shared-memory opt-in, and how many CTA pairs fit at once
   static DeviceOnce once;
   cudaLaunchConfig_t cfg = {};
@@ -857,7 +898,7 @@ cudaError_t launch_kernel(const CUtensorMap &mA0, const CUtensorMap &mA1, const 
   if (e != cudaSuccess) return e;
   cfg.gridDim = dim3(pair_grid);
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE, WQ>, mA0, mA1, mB0, mB1, p);
+  e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE, WQ>, mA0, mA1, mB0, mB1, mA0s, mA1s, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
