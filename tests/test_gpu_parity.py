@@ -95,6 +95,23 @@ def test_many_hot_experts():
 PRECISIONS = ["bf16", "fp8_bwd", "mxfp8"]
 
 
+# expert segments ending at and around every 32-row boundary of a 256-row tile:
+# a CTA of a ragged tile loads 1-4 of its 32-row A boxes, or none
+BOX_COUNTS = [1, 31, 32, 33, 63, 64, 65, 96, 97, 127, 128, 129, 160, 255, 256, 257]
+
+
+@pytest.mark.parametrize("precision", PRECISIONS)
+def test_segments_ending_at_every_box_boundary(precision):
+    shape = MoEShape(T=sum(BOX_COUNTS), H=128, I=128, E=len(BOX_COUNTS), k=1)
+    inp = synth.make_inputs_shape(shape, 71)
+    owner = np.repeat(np.arange(shape.E), BOX_COUNTS)
+    np.random.default_rng(71).shuffle(owner)  # tokens of an expert spread over the batch
+    inp["logits"][np.arange(shape.T), owner] += 100.0
+    layer, out, grads = G.run_layer(shape, inp, precision=precision)
+    G.check_full(shape, inp, layer, out, grads, precision=precision)
+    assert list(layer.routing["counts"].cpu().numpy()) == BOX_COUNTS
+
+
 @pytest.mark.parametrize("precision", PRECISIONS)
 def test_zero_tokens(precision):
     shape = MoEShape(T=0, H=128, I=128, E=4, k=2)
