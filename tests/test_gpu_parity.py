@@ -170,6 +170,34 @@ def test_deterministic_bitwise(precision):
 
 
 @pytest.mark.parametrize("precision", PRECISIONS)
+def test_two_layers_on_two_streams_concurrently(precision):
+    """The library keeps no per-call state: two layers with different shapes and
+    inputs, their calls interleaved on two streams, give the bits each gives alone."""
+    shapes = [MoEShape(T=700, H=256, I=256, E=6, k=2), MoEShape(T=512, H=384, I=128, E=16, k=4)]
+    inps = [synth.make_inputs_shape(sh, 73 + i) for i, sh in enumerate(shapes)]
+    alone = [G.run_layer(sh, inp, precision=precision) for sh, inp in zip(shapes, inps)]
+    layers = [moe.MoELayer(sh, precision=precision) for sh in shapes]
+    ts = [G.to_dev(inp) for inp in inps]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    outs, grads = [None, None], [None, None]
+    for i in (0, 1):
+        layers[i].route(ts[i]["logits"], streams[i])
+    for i in (0, 1):
+        outs[i] = layers[i].forward(ts[i]["x"], ts[i]["W_gate"], ts[i]["W_up"], ts[i]["W_down"], stream=streams[i])
+    for i in (1, 0):
+        grads[i] = layers[i].backward(ts[i]["dy"], ts[i]["x"], ts[i]["W_gate"], ts[i]["W_up"], ts[i]["W_down"],
+                                      stream=streams[i])
+    torch.cuda.synchronize()
+    for i in (0, 1):
+        assert layers[i].status(streams[i]) == {"route": 0, "forward": 0, "backward": 0}
+        _, out_a, g_a = alone[i]
+        assert torch.equal(outs[i], out_a), i
+        for n in g_a:
+            assert torch.equal(grads[i][n], g_a[n]), (i, n)
+
+
+@pytest.mark.parametrize("precision", PRECISIONS)
 def test_cuda_graph_capture_and_replay_with_new_routing(precision):
     shape = MoEShape(T=512, H=128, I=128, E=8, k=2)
     inp = synth.make_inputs_shape(shape, 59)
