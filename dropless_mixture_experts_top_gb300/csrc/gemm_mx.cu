@@ -359,7 +359,7 @@ __device__ __forceinline__ void epilogue_gateup_mx(const MxTile &x, uint32_t tb,
 #pragma unroll
         for (int i = 0; i < 32; ++i) v1[i] = valid ? round_bf16(v0[i]) : 0.f;
         const int prow0 = prow - lane;
-        const size_t sfb = atom_byte(col + lane, prow0 >> 5, p.Mpad, SfLayout{p.I, 128});
+        const size_t sfb = atom_row_sg<128>(0, col + lane, p.Mpad, p.I) + atom_kblock(prow0 >> 5);  // one segment
         quant_down_rows32(tile, v1, p.aw_t, static_cast<size_t>(p.Mpad), col, prow0, p.aw_t_sf + sfb);
       }
     }

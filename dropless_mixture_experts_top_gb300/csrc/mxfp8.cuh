@@ -32,13 +32,6 @@ __device__ __forceinline__ float pow2_neg(int X) {  // 2^-X for X in [-127, 126]
   return __uint_as_float(static_cast<uint32_t>(127 - X) << 23);
 }
 
-// Four E4M3 codes, a in the lowest byte (two paired conversions).
-__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
-  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
-  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
-  return lo | (hi << 16);
-}
-
 // (a s, b s) with one paired multiply (each lane rounded as a plain fp32 product;
 // s is a power of two here, so the products are exact).
 __device__ __forceinline__ float2 mul2(float a, float b, float s) {
@@ -111,24 +104,11 @@ __device__ __forceinline__ uint8_t quant32(const float (&v)[32], uint4 *dst) {
   return static_cast<uint8_t>(X + 127);
 }
 
-// Byte of (row, K block 0) in a scale-atom buffer of K columns grouped by L;
-// K block kb of the same row adds atom_kblock(kb).  With the group size known
-// at compile time (kGroup > 0) its divisions become multiplications.
-template <int kGroup = 0>
-__device__ __forceinline__ size_t atom_row(int row, int K, SfLayout L) {
-  const int group = kGroup > 0 ? kGroup : L.group;
-  const int sg = row / L.seg, r = row - sg * L.seg;
-  const int g = r / group, rr = r - g * group;
-  const int gps = (L.seg + group - 1) / group, apg = (group + 127) >> 7;
-  const size_t rb = (static_cast<size_t>(sg) * gps + g) * apg + (rr >> 7);
-  const int w = rr & 127;
-  return rb * (K >> 7) * 512 + (w & 31) * 16 + (w >> 5) * 4;
-}
-__device__ __forceinline__ size_t atom_kblock(int kblock) {
-  return static_cast<size_t>(kblock >> 2) * 512 + (kblock & 3);
-}
-// atom_row<kGroup> of row r of segment sg (segments of `seg` rows), for a caller
-// that knows the segment: no division by the segment length.
+// Byte of (row r of segment sg, K block 0) in a scale-atom buffer of K columns
+// whose rows are cut into segments of `seg` rows and groups of kGroup rows (a
+// caller that knows the segment: no division by the segment length, and the
+// group size's divisions become multiplications); K block kb of the same row
+// adds atom_kblock(kb).
 template <int kGroup>
 __device__ __forceinline__ size_t atom_row_sg(int sg, int r, int K, int seg) {
   const int g = r / kGroup, rr = r - g * kGroup;
@@ -137,6 +117,9 @@ __device__ __forceinline__ size_t atom_row_sg(int sg, int r, int K, int seg) {
   const size_t rb = (static_cast<size_t>(sg) * gps + g) * apg + (rr >> 7);
   const int w = rr & 127;
   return rb * (K >> 7) * 512 + (w & 31) * 16 + (w >> 5) * 4;
+}
+__device__ __forceinline__ size_t atom_kblock(int kblock) {
+  return static_cast<size_t>(kblock >> 2) * 512 + (kblock & 3);
 }
 
 // Byte of (row, K block) in a scale-atom buffer of K columns grouped by L.
